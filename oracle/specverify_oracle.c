@@ -1,0 +1,319 @@
+/*
+ * specverify_oracle.c -- plain fp64 CPU oracle of the speculative-decoding
+ * verification step.
+ *
+ * TEST INFRASTRUCTURE ONLY (see specverify_oracle.h): the checker of the CUDA
+ * library, never a fallback for it. Single-threaded, one request at a time,
+ * one position at a time, in the order the pages describe the method. Every
+ * logit is widened exactly to double; every probability, sum and comparison
+ * is done in double. Nothing is blocked, fused or reordered: each row's
+ * softmax is recomputed from its logits where the algorithm needs it.
+ */
+#include "specverify_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+int oracle_version(void) { return 1; }
+
+/* Logit idx of a tensor: binary32 read as is; a bfloat16 holds the top 16
+ * bits of a binary32, so it widens exactly by a 16-bit shift. */
+static double logit_at(const void* base, int dtype, size_t idx) {
+    if (dtype == ORACLE_F32) return (double)((const float*)base)[idx];
+    uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+static void load_row(const void* base, int dtype, size_t row, int V, double* l) {
+    for (int x = 0; x < V; ++x) l[x] = logit_at(base, dtype, row * (size_t)V + (size_t)x);
+}
+
+/* A row can be used when it holds no NaN, no +inf, and at least one value
+ * above -inf (a row of only -inf has no distribution). */
+static int row_usable(const double* l, int V) {
+    int has_finite = 0;
+    for (int x = 0; x < V; ++x) {
+        if (isnan(l[x])) return 0;
+        if (isinf(l[x])) {
+            if (l[x] > 0) return 0;
+        } else {
+            has_finite = 1;
+        }
+    }
+    return has_finite;
+}
+
+static double row_max(const double* l, int V) {
+    double m = l[0];
+    for (int x = 1; x < V; ++x)
+        if (l[x] > m) m = l[x];
+    return m;
+}
+
+/* Greedy rule of "Speculative Decoding : accélérer l'inférence des LLM",
+ * §Pourquoi la qualité est préservée: the target's most likely token; on a
+ * tie the lowest index (reading: the pages do not say). */
+static int row_argmax(const double* l, int V) {
+    int a = 0;
+    for (int x = 1; x < V; ++x)
+        if (l[x] > l[a]) a = x;
+    return a;
+}
+
+/* Temperature softmax p(x) = exp(l(x)/T) / sum_y exp(l(y)/T), evaluated as
+ * exp((l(x) - m)/T) / Z with m the row max so that no term overflows; Z is
+ * summed in index order. Returns log sum_y exp(l(y)/T) = m/T + log Z. */
+static double softmax_T(const double* l, int V, double T, double* p) {
+    double m = row_max(l, V);
+    double Z = 0.0;
+    for (int x = 0; x < V; ++x) {
+        p[x] = exp((l[x] - m) / T);
+        Z += p[x];
+    }
+    for (int x = 0; x < V; ++x) p[x] /= Z;
+    return m / T + log(Z);
+}
+
+/* Inverse-CDF draw over non-negative weights w (need not sum to one):
+ * W = sum w, t = u * W, and the token is the smallest k whose inclusive
+ * prefix sum C_k exceeds t, so a zero-weight token is never drawn. If
+ * rounding leaves no such k, the last k with w_k > 0. Reports W and the
+ * distance of t to the nearer edge of the chosen interval, divided by W. */
+static int draw_inverse_cdf(const double* w, int V, double u, double* W_out,
+                            double* margin_out) {
+    double W = 0.0;
+    for (int x = 0; x < V; ++x) W += w[x];
+    *W_out = W;
+    double t = u * W;
+    double C = 0.0;
+    for (int k = 0; k < V; ++k) {
+        double before = C;
+        C += w[k];
+        if (C > t) {
+            double lo = t - before, hi = C - t;
+            *margin_out = (lo < hi ? lo : hi) / W;
+            return k;
+        }
+    }
+    *margin_out = 0.0;
+    for (int k = V - 1; k >= 0; --k)
+        if (w[k] > 0.0) return k;
+    return 0; /* unreachable: callers pass W > 0 */
+}
+
+static void set_d(double* a, size_t i, double v) {
+    if (a) a[i] = v;
+}
+static void set_i(int32_t* a, size_t i, int32_t v) {
+    if (a) a[i] = v;
+}
+
+typedef struct {
+    const void* target;
+    const void* draft;
+    int dtype, gamma, V;
+    double *lt, *ld, *p, *q, *w;
+} scratch_t;
+
+/* Report-only pass for the checker: the max, argmax and log-normaliser of
+ * every row the request reads. It does not feed the decisions. */
+static void report_rows(const scratch_t* s, int b, double T, const oracle_detail* d) {
+    const int G = s->gamma, V = s->V;
+    for (int i = 0; i <= G; ++i) {
+        size_t r = (size_t)b * (size_t)(G + 1) + (size_t)i;
+        load_row(s->target, s->dtype, r, V, s->lt);
+        set_d(d->max_target, r, row_max(s->lt, V));
+        set_i(d->argmax_target, r, row_argmax(s->lt, V));
+        if (T > 0.0) set_d(d->lse_target, r, softmax_T(s->lt, V, T, s->p));
+    }
+    if (T > 0.0) {
+        for (int i = 0; i < G; ++i) {
+            size_t r = (size_t)b * (size_t)G + (size_t)i;
+            load_row(s->draft, s->dtype, r, V, s->ld);
+            set_d(d->max_draft, r, row_max(s->ld, V));
+            set_d(d->lse_draft, r, softmax_T(s->ld, V, T, s->q));
+        }
+    }
+}
+
+static void clear_detail(const oracle_detail* d, int b, int G) {
+    for (int i = 0; i <= G; ++i) {
+        size_t r = (size_t)b * (size_t)(G + 1) + (size_t)i;
+        set_d(d->max_target, r, NAN);
+        set_d(d->lse_target, r, NAN);
+        set_i(d->argmax_target, r, -1);
+    }
+    for (int i = 0; i < G; ++i) {
+        size_t r = (size_t)b * (size_t)G + (size_t)i;
+        set_d(d->max_draft, r, NAN);
+        set_d(d->lse_draft, r, NAN);
+        set_d(d->p_x, r, NAN);
+        set_d(d->q_x, r, NAN);
+        set_d(d->alpha, r, NAN);
+        set_d(d->accept_margin, r, NAN);
+    }
+    set_d(d->w_total, (size_t)b, NAN);
+    set_d(d->sample_margin, (size_t)b, NAN);
+    set_i(d->kind, (size_t)b, ORACLE_KIND_ERROR);
+}
+
+/* Whether request b can be verified at all (see the header for the rule). */
+static int request_valid(const scratch_t* s, int b, double T, const int32_t* tok) {
+    const int G = s->gamma, V = s->V;
+    if (isnan(T) || isinf(T) || T < 0.0) return 0;
+    for (int i = 0; i < G; ++i)
+        if (tok[i] < 0 || tok[i] >= V) return 0;
+    for (int i = 0; i <= G; ++i) {
+        load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
+        if (!row_usable(s->lt, V)) return 0;
+    }
+    if (T > 0.0) {
+        for (int i = 0; i < G; ++i) {
+            load_row(s->draft, s->dtype, (size_t)b * (size_t)G + (size_t)i, V, s->ld);
+            if (!row_usable(s->ld, V)) return 0;
+        }
+    }
+    return 1;
+}
+
+/* Temperature zero ("Speculative Decoding : accélérer l'inférence des LLM",
+ * §Pourquoi la qualité est préservée): a draft token is accepted iff it is
+ * the target argmax at its position; the first mismatch is replaced by that
+ * argmax and ends the scan; if all gamma match, the argmax of the last target
+ * row is the extra token. Returns n. */
+static int verify_greedy(const scratch_t* s, int b, const int32_t* tok, int32_t* out) {
+    const int G = s->gamma, V = s->V;
+    for (int i = 0; i < G; ++i) {
+        load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
+        int a = row_argmax(s->lt, V);
+        if (tok[i] == a) {
+            out[i] = tok[i];
+        } else {
+            out[i] = a;
+            return i;
+        }
+    }
+    load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)G, V, s->lt);
+    out[G] = row_argmax(s->lt, V);
+    return G;
+}
+
+/* Temperature T > 0. Left to right, draft token x_i is accepted iff
+ * u_i < alpha_i = min(1, p_i(x_i) / q_i(x_i)) (eq. alpha(x) of the wiki page
+ * "Speculative Decoding"); the first rejection at position n ends the scan
+ * and the later draft tokens are dropped ("Il meccanismo: draft model, target
+ * model, rejection sampling"). The replacement is drawn from
+ * p_corr = max(p_n - q_n, 0) / sum max(p_n - q_n, 0) (eq. p_corr); if nothing
+ * was rejected, the extra token is drawn from p at the last target row
+ * ("Accélérer Sonar grâce à la spéculation", §Décodage spéculatif). */
+static int verify_sampled(const scratch_t* s, int b, double T, const int32_t* tok,
+                          const float* ua, float us, int32_t* out,
+                          const oracle_detail* d) {
+    const int G = s->gamma, V = s->V;
+    int n = G;
+    for (int i = 0; i < G; ++i) {
+        size_t r = (size_t)b * (size_t)G + (size_t)i;
+        int x = tok[i];
+        load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
+        softmax_T(s->lt, V, T, s->p);
+        load_row(s->draft, s->dtype, r, V, s->ld);
+        softmax_T(s->ld, V, T, s->q);
+        double px = s->p[x], qx = s->q[x];
+        double alpha;
+        if (qx > 0.0)
+            alpha = px / qx < 1.0 ? px / qx : 1.0;
+        else
+            alpha = px > 0.0 ? 1.0 : 0.0;
+        double u = (double)ua[i];
+        set_d(d->p_x, r, px);
+        set_d(d->q_x, r, qx);
+        set_d(d->alpha, r, alpha);
+        set_d(d->accept_margin, r, alpha > 0.0 ? fabs(u - alpha) / alpha : INFINITY);
+        if (u < alpha) {
+            out[i] = x;
+        } else {
+            n = i;
+            break;
+        }
+    }
+    double W = 0.0;
+    if (n < G) {
+        /* s->p and s->q still hold the distributions of position n. */
+        for (int x = 0; x < V; ++x) {
+            double diff = s->p[x] - s->q[x];
+            s->w[x] = diff > 0.0 ? diff : 0.0;
+            W += s->w[x];
+        }
+        if (W == 0.0) /* unreachable in exact arithmetic: fall back to p_n */
+            memcpy(s->w, s->p, sizeof(double) * (size_t)V);
+        set_i(d->kind, (size_t)b, ORACLE_KIND_RESIDUAL);
+    } else {
+        load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)G, V, s->lt);
+        softmax_T(s->lt, V, T, s->p);
+        memcpy(s->w, s->p, sizeof(double) * (size_t)V);
+        set_i(d->kind, (size_t)b, ORACLE_KIND_BONUS);
+    }
+    double margin = 0.0;
+    out[n] = draw_inverse_cdf(s->w, V, (double)us, &W, &margin);
+    set_d(d->w_total, (size_t)b, W);
+    set_d(d->sample_margin, (size_t)b, margin);
+    return n;
+}
+
+int oracle_spec_verify(const void* target, const void* draft, int dtype, int B, int gamma,
+                       int V, const int32_t* tokens, const float* u_accept,
+                       const float* u_sample, const float* temperature,
+                       int32_t* out_tokens, int32_t* out_num_accepted,
+                       const oracle_detail* detail) {
+    if (B < 0 || gamma < 1 || V < 1) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+    if (B == 0) return 0;
+    if (!target || !draft || !tokens || !u_accept || !u_sample || !temperature ||
+        !out_tokens || !out_num_accepted)
+        return -1;
+    oracle_detail none;
+    memset(&none, 0, sizeof none);
+    const oracle_detail* d = detail ? detail : &none;
+
+    scratch_t s;
+    s.target = target;
+    s.draft = draft;
+    s.dtype = dtype;
+    s.gamma = gamma;
+    s.V = V;
+    s.lt = (double*)malloc(sizeof(double) * (size_t)V);
+    s.ld = (double*)malloc(sizeof(double) * (size_t)V);
+    s.p = (double*)malloc(sizeof(double) * (size_t)V);
+    s.q = (double*)malloc(sizeof(double) * (size_t)V);
+    s.w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!s.lt || !s.ld || !s.p || !s.q || !s.w) {
+        free(s.lt), free(s.ld), free(s.p), free(s.q), free(s.w);
+        return -1;
+    }
+
+    for (int b = 0; b < B; ++b) {
+        const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
+        int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
+        double T = (double)temperature[b];
+        for (int j = 0; j <= gamma; ++j) out[j] = -1;
+        clear_detail(d, b, gamma);
+        if (!request_valid(&s, b, T, tok)) {
+            out_num_accepted[b] = -1;
+            continue;
+        }
+        if (detail) report_rows(&s, b, T, d);
+        if (T == 0.0) {
+            set_i(d->kind, (size_t)b, ORACLE_KIND_GREEDY);
+            out_num_accepted[b] = verify_greedy(&s, b, tok, out);
+        } else {
+            out_num_accepted[b] = verify_sampled(&s, b, T, tok,
+                                                 u_accept + (size_t)b * (size_t)gamma,
+                                                 u_sample[b], out, d);
+        }
+    }
+    free(s.lt), free(s.ld), free(s.p), free(s.q), free(s.w);
+    return 0;
+}

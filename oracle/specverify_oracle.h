@@ -1,0 +1,108 @@
+/*
+ * specverify_oracle.h -- the CPU oracle of the speculative-decoding
+ * verification step.
+ *
+ * TEST INFRASTRUCTURE ONLY. This header and specverify_oracle.c are the
+ * plain, slow, fp64 restatement of the method that the CUDA library is
+ * checked against. Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load it. It shares no code, header, table or helper
+ * with the CUDA library (speculative_decoding_verification_06_gb300/csrc),
+ * and the CUDA library never calls it.
+ *
+ * Sources (page title, section):
+ *  - "Speculative Decoding : accélérer l'inférence des LLM",
+ *    §Principe et garanties mathématiques (propose gamma tokens, verify in one
+ *    target pass, accept while compatible, correct the first rejection, at
+ *    least one and at most gamma+1 tokens per cycle) and
+ *    §Pourquoi la qualité est préservée (accept with probability
+ *    min(1, p(x)/q(x)); on rejection draw from p - q clipped at zero and
+ *    renormalised; at temperature zero accept iff the token is the target
+ *    argmax, else replace it by that argmax).
+ *  - "Speculative Decoding — Come Accelerare l'Inferenza LLM di 2-3x Senza
+ *    Perdere Qualità", §Il meccanismo: draft model, target model, rejection
+ *    sampling (the later draft tokens are discarded after a rejection).
+ *  - "Speculative Decoding" (wiki), §数式で見る speculative decoding の正しさ,
+ *    eq. alpha(x) and eq. p_corr.
+ *  - "Accélérer Sonar grâce à la spéculation", §Décodage spéculatif (up to
+ *    n + 1 tokens per step; the target logits at the mismatch position or at
+ *    the end of the sequence give the extra token).
+ *
+ * Readings where the pages are silent (all stated again in the design doc):
+ *  - temperature: p = softmax(l_target / T), q = softmax(l_draft / T), the
+ *    same T for both rows; T == 0 is the greedy rule;
+ *  - accept iff u_accept < alpha, u in [0, 1); alpha = min(1, p/q); q == 0
+ *    gives alpha = 1 when p > 0 and alpha = 0 when p == 0;
+ *  - one uniform u_sample per request draws the replacement or the bonus
+ *    token by inverse CDF in index order: the token is the smallest k with
+ *    C_k > u * W, C_k the inclusive prefix sum of the weights, W their total;
+ *    if rounding leaves no such k, the last k with a positive weight;
+ *  - if the residual weights sum to zero (impossible in exact arithmetic),
+ *    the replacement is drawn from p at that position instead;
+ *  - argmax ties go to the lowest index;
+ *  - a request is invalid (num_accepted = -1, every output token -1) when T
+ *    is NaN, negative or infinite, a draft token is outside [0, V), or a row
+ *    the request reads holds a NaN or +inf or only -inf values (the draft
+ *    rows of a T == 0 request are never read).
+ */
+#ifndef SPECVERIFY_ORACLE_H
+#define SPECVERIFY_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ORACLE_F32 0  /* logits stored as IEEE binary32 */
+#define ORACLE_BF16 1 /* logits stored as bfloat16 bit patterns (uint16) */
+
+#define ORACLE_KIND_ERROR (-1)
+#define ORACLE_KIND_GREEDY 0
+#define ORACLE_KIND_RESIDUAL 1
+#define ORACLE_KIND_BONUS 2
+
+/* Optional per-row and per-request facts the checker compares. Every pointer
+ * may be NULL. Entries the algorithm does not reach hold NaN (doubles) or -1
+ * (integers). Row arrays are indexed like the logits: target [B, gamma+1],
+ * draft [B, gamma]. */
+typedef struct {
+    double* max_target;    /* [B*(gamma+1)] max_x l(x) of every target row */
+    double* lse_target;    /* [B*(gamma+1)] log sum_x exp(l(x)/T), T > 0 rows */
+    int32_t* argmax_target;/* [B*(gamma+1)] lowest-index argmax of every row */
+    double* max_draft;     /* [B*gamma] rows of T > 0 requests */
+    double* lse_draft;     /* [B*gamma] rows of T > 0 requests */
+    double* p_x;           /* [B*gamma] p_i(x_i) at the evaluated positions */
+    double* q_x;           /* [B*gamma] q_i(x_i) at the evaluated positions */
+    double* alpha;         /* [B*gamma] min(1, p/q) at the evaluated positions */
+    double* accept_margin; /* [B*gamma] |u - alpha| / alpha (inf if alpha == 0) */
+    double* w_total;       /* [B] W of the residual or bonus draw */
+    double* sample_margin; /* [B] min(t - C_{k-1}, C_k - t) / W of that draw */
+    int32_t* kind;         /* [B] ORACLE_KIND_* */
+} oracle_detail;
+
+/* The verification step for B independent requests, all on host memory.
+ *   target      [B, gamma+1, V] logits (dtype), row i scores draft token i,
+ *               row gamma is the bonus row
+ *   draft       [B, gamma, V] logits (dtype)
+ *   tokens      [B, gamma] draft tokens
+ *   u_accept    [B, gamma] uniforms in [0, 1)
+ *   u_sample    [B] uniforms in [0, 1)
+ *   temperature [B]
+ *   out_tokens  [B, gamma+1]: accepted tokens, then the replacement or bonus
+ *               token, then -1
+ *   out_num_accepted [B]: n in [0, gamma], or -1 for an invalid request
+ * Returns 0, or -1 for a bad argument (nothing written). */
+int oracle_spec_verify(const void* target, const void* draft, int dtype,
+                       int B, int gamma, int V,
+                       const int32_t* tokens, const float* u_accept,
+                       const float* u_sample, const float* temperature,
+                       int32_t* out_tokens, int32_t* out_num_accepted,
+                       const oracle_detail* detail);
+
+int oracle_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_ORACLE_H */

@@ -1,0 +1,397 @@
+"""Pins of the CPU oracle: checks against facts fixed by the pages and by
+mathematics, never against the oracle itself.
+
+Each ``pin_*`` takes a loaded oracle library and raises AssertionError when
+the oracle disagrees with the fact it pins. ``test_oracle_pins.py`` runs them
+on the real oracle; ``test_oracle_mutants.py`` runs them on deliberately
+broken copies to show that a plausible mistake fails at least one.
+
+Independent sources used here: hand-worked values (``golden/hand_v4.json``),
+closed forms (P(accept) = sum_x min(p(x), q(x)); expected tokens per pass
+(1 - a^(g+1)) / (1 - a); sum_x max(p-q, 0) = 1 - sum_x min(p, q)), library
+routines (scipy.special.softmax / logsumexp, numpy argmax / cumsum /
+searchsorted) and chi-square goodness of fit against the target
+distribution, which the pages state the output follows exactly.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+from scipy import special, stats
+
+import oracle
+from workloads.synthetic import bf16_bits_to_f32, f32_to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_v4.json")
+CHI2_P = 1e-3  # goodness-of-fit level; inputs are seeded, so a pass is reproducible
+
+
+def _run(lib, target, draft, tokens, ua, us, T, detail=False):
+    return oracle.verify(target, draft, tokens, ua, us, T, detail=detail, lib=lib)
+
+
+def _chi2_ok(counts, probs, label):
+    counts = np.asarray(counts, dtype=np.float64)
+    probs = np.asarray(probs, dtype=np.float64)
+    n = counts.sum()
+    nz = probs > 0
+    assert np.all(counts[~nz] == 0), f"{label}: a zero-probability outcome was drawn: {counts}"
+    exp = n * probs[nz]
+    chi2 = float(((counts[nz] - exp) ** 2 / exp).sum())
+    dof = int(nz.sum()) - 1
+    limit = float(stats.chi2.isf(CHI2_P, dof))
+    assert chi2 < limit, f"{label}: chi2 = {chi2:.2f} >= {limit:.2f} (dof {dof})"
+
+
+def _within_5_sigma(mean, expect, sd, n, label):
+    tol = 5.0 * sd / np.sqrt(n)
+    assert abs(mean - expect) < tol, f"{label}: mean {mean:.6f} vs {expect:.6f} (5 sigma = {tol:.2e})"
+
+
+# ---------------------------------------------------------------- hand-worked
+
+def pin_hand_examples(lib, quick=False):
+    """The constructed V=4 examples, worked by hand (golden/hand_v4.json)."""
+    cases = json.load(open(GOLDEN))["cases"]
+    for c in cases:
+        g = c["gamma"]
+        if "target_p" in c:
+            tl = np.log(np.array(c["target_p"], dtype=np.float64)).astype(np.float32)
+            dl = np.log(np.array(c["draft_p"], dtype=np.float64)).astype(np.float32)
+        else:
+            tl = np.array(c["target_logits"], dtype=np.float32)
+            dl = np.array(c["draft_logits"], dtype=np.float32)
+        out, n, det = _run(lib, tl[None], dl[None], np.array([c["tokens"]], np.int32),
+                           np.array([c["u_accept"]], np.float32),
+                           np.array([c["u_sample"]], np.float32),
+                           np.array([c["T"]], np.float32), detail=True)
+        assert list(out[0]) == c["expect_tokens"], (c["name"], out[0])
+        assert int(n[0]) == c["expect_n"], (c["name"], n[0])
+        for key, dk in (("expect_p_x", "p_x"), ("expect_q_x", "q_x"), ("expect_alpha", "alpha")):
+            if key in c:
+                got = det[dk][0][: len(c[key])]
+                assert np.allclose(got, c[key], rtol=1e-6, atol=0), (c["name"], dk, got)
+        if "expect_W" in c:
+            assert abs(det["w_total"][0] - c["expect_W"]) < 1e-6, (c["name"], det["w_total"][0])
+        _ = g
+
+
+# ------------------------------------------------ Monte Carlo at V = 8, gamma 1
+
+def _v8_setup(seed, T, N):
+    T = float(np.float32(T))  # the oracle receives T as binary32
+    rng = np.random.Generator(np.random.Philox(seed))
+    lt = rng.normal(0, 1.5, (2, 8)).astype(np.float32)   # row 0 and the bonus row
+    ld = (lt[:1] + rng.normal(0, 1.2, (1, 8))).astype(np.float32)
+    p0 = special.softmax(lt[0].astype(np.float64) / T)
+    pb = special.softmax(lt[1].astype(np.float64) / T)
+    q0 = special.softmax(ld[0].astype(np.float64) / T)
+    x = rng.choice(8, size=N, p=q0).astype(np.int32)
+    ua = rng.random((N, 1), dtype=np.float32)
+    us = rng.random(N, dtype=np.float32)
+    target = np.ascontiguousarray(np.broadcast_to(lt, (N, 2, 8)))
+    draft = np.ascontiguousarray(np.broadcast_to(ld, (N, 1, 8)))
+    return target, draft, x[:, None], ua, us, np.full(N, T, np.float32), p0, q0, pb
+
+
+def _v8_trials(lib, quick, T, seed):
+    N = 200_000 if quick else 1_000_000
+    target, draft, x, ua, us, temp, p0, q0, pb = _v8_setup(seed, T, N)
+    out, n, _ = _run(lib, target, draft, x, ua, us, temp)
+    return out, n, p0, q0, pb, N
+
+
+def pin_accept_probability(lib, quick=False):
+    """P(accept) = sum_x q(x) min(1, p(x)/q(x)) = sum_x min(p(x), q(x))."""
+    for T, seed in ((1.0, 11), (0.6, 12)):
+        out, n, p0, q0, _, N = _v8_trials(lib, quick, T, seed)
+        beta = float(np.minimum(p0, q0).sum())
+        acc = (n == 1).astype(np.float64)
+        _within_5_sigma(acc.mean(), beta, np.sqrt(beta * (1 - beta)), N, f"P(accept) T={T}")
+
+
+def pin_output_distribution(lib, quick=False):
+    """The first emitted token is distributed exactly as p_0; conditioned on a
+    rejection it follows p_corr = max(p-q,0)/sum; conditioned on acceptance the
+    extra token follows the bonus row's p."""
+    for T, seed in ((1.0, 21), (0.6, 22)):
+        out, n, p0, q0, pb, N = _v8_trials(lib, quick, T, seed)
+        _chi2_ok(np.bincount(out[:, 0], minlength=8), p0, f"first token ~ p T={T}")
+        rej = n == 0
+        pc = np.maximum(p0 - q0, 0.0)
+        pc /= pc.sum()
+        _chi2_ok(np.bincount(out[rej, 0], minlength=8), pc, f"residual ~ p_corr T={T}")
+        acc = n == 1
+        _chi2_ok(np.bincount(out[acc, 1], minlength=8), pb, f"bonus ~ p_bonus T={T}")
+        assert np.all(out[rej, 1] == -1)
+
+
+def pin_tokens_per_pass(lib, quick=False):
+    """Every position has p = (0.7, 0.3), q = (0.9, 0.1): alpha = sum min = 0.8.
+    With gamma = 4 the expected tokens per target pass is
+    (1 - 0.8^5)/(1 - 0.8) = 3.3616 ("about 3.4"), and the expected number
+    accepted is sum_{k=1..4} 0.8^k = 2.3616; P(n = k) = 0.8^k 0.2 for k < 4
+    and 0.8^4 for k = 4."""
+    N = 200_000 if quick else 1_000_000
+    G = 4
+    rng = np.random.Generator(np.random.Philox(31))
+    lt = np.log(np.array([0.7, 0.3]))
+    ld = np.log(np.array([0.9, 0.1]))
+    target = np.ascontiguousarray(np.broadcast_to(lt.astype(np.float32), (N, G + 1, 2)))
+    draft = np.ascontiguousarray(np.broadcast_to(ld.astype(np.float32), (N, G, 2)))
+    x = (rng.random((N, G)) < 0.1).astype(np.int32)  # token 1 with prob q(1) = 0.1
+    ua = rng.random((N, G), dtype=np.float32)
+    us = rng.random(N, dtype=np.float32)
+    out, n, _ = _run(lib, target, draft, x, ua, us, np.ones(N, np.float32))
+    a = 0.8
+    emitted = n.astype(np.float64) + 1
+    pk = np.array([a ** k * (1 - a) for k in range(G)] + [a ** G])
+    mean_n = sum(k * pk[k] for k in range(G + 1))
+    sd_n = np.sqrt(sum((k - mean_n) ** 2 * pk[k] for k in range(G + 1)))
+    assert abs((1 - a ** (G + 1)) / (1 - a) - 3.3616) < 1e-12
+    _within_5_sigma(emitted.mean(), 3.3616, sd_n, N, "tokens per pass")
+    _within_5_sigma(n.mean(), sum(a ** k for k in range(1, G + 1)), sd_n, N, "mean accepted")
+    _chi2_ok(np.bincount(n, minlength=G + 1), pk, "P(n = k)")
+    assert np.all((out >= 0).sum(axis=1) == n + 1)
+
+
+def pin_position_acceptance(lib, quick=False):
+    """Logits that do not depend on earlier tokens make positions independent:
+    P(n = k) = prod_{i<k} beta_i (1 - beta_k), P(n = gamma) = prod beta_i, with
+    beta_i = sum min(p_i, q_i) from scipy's softmax."""
+    N = 100_000 if quick else 400_000
+    G, V, T = 3, 5, float(np.float32(0.8))
+    rng = np.random.Generator(np.random.Philox(41))
+    lt = rng.normal(0, 1.5, (G + 1, V)).astype(np.float32)
+    ld = (lt[:G] + rng.normal(0, 1.0, (G, V))).astype(np.float32)
+    p = special.softmax(lt.astype(np.float64) / T, axis=1)
+    q = special.softmax(ld.astype(np.float64) / T, axis=1)
+    beta = np.minimum(p[:G], q).sum(axis=1)
+    x = np.stack([rng.choice(V, size=N, p=q[i]) for i in range(G)], axis=1).astype(np.int32)
+    out, n, _ = _run(lib, np.ascontiguousarray(np.broadcast_to(lt, (N, G + 1, V))),
+                     np.ascontiguousarray(np.broadcast_to(ld, (N, G, V))), x,
+                     rng.random((N, G), dtype=np.float32), rng.random(N, dtype=np.float32),
+                     np.full(N, T, np.float32))
+    pk = [np.prod(beta[:k]) * (1 - beta[k]) for k in range(G)] + [np.prod(beta)]
+    _chi2_ok(np.bincount(n, minlength=G + 1), pk, "P(n = k) per position")
+    # accepted tokens are the draft tokens themselves
+    for k in range(G):
+        sel = n > k
+        assert np.array_equal(out[sel, k], x[sel, k])
+
+
+# --------------------------------------------------------------- greedy rule
+
+def pin_greedy_is_argmax_decoding(lib, quick=False):
+    """At T = 0 the output is plain argmax decoding of the target rows: the
+    leading draft tokens that equal numpy's argmax (first index on ties) are
+    kept, then that argmax replaces the first mismatch or follows the last."""
+    rng = np.random.Generator(np.random.Philox(51))
+    for dtype in ("f32", "bf16"):
+        B, G, V = 300, 5, 40
+        lt = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+        # plant ties: copy the row max to another, sometimes lower, index
+        for b in range(0, B, 3):
+            for i in range(G + 1):
+                j = rng.integers(V)
+                lt[b, i, j] = lt[b, i].max()
+        if dtype == "bf16":
+            tbits = f32_to_bf16_bits(lt)
+            tvals = bf16_bits_to_f32(tbits)
+            target, draft = tbits, f32_to_bf16_bits(rng.normal(0, 2, (B, G, V)))
+        else:
+            tvals = lt
+            target, draft = lt, rng.normal(0, 2, (B, G, V)).astype(np.float32)
+        am = np.argmax(tvals, axis=2)
+        keep = rng.integers(0, G + 1, B)
+        x = am[:, :G].copy()
+        for b in range(B):
+            if keep[b] < G:
+                x[b, keep[b]] = (am[b, keep[b]] + 1 + rng.integers(V - 1)) % V
+        out, n, _ = _run(lib, target, draft, x.astype(np.int32),
+                         np.full((B, G), 0.5, np.float32), np.full(B, 0.5, np.float32),
+                         np.zeros(B, np.float32))
+        for b in range(B):
+            k = keep[b]
+            assert n[b] == k, (dtype, b, n[b], k)
+            assert list(out[b, :k]) == list(x[b, :k])
+            assert out[b, k] == am[b, k]
+            assert np.all(out[b, k + 1:] == -1)
+
+
+def pin_small_temperature_matches_greedy(lib, quick=False):
+    """As T -> 0+, softmax(l/T) becomes one-hot at the argmax, so at T = 1e-4
+    with every runner-up at least 0.25 below the max the sampled rule gives the
+    greedy result exactly, whatever the uniforms."""
+    rng = np.random.Generator(np.random.Philox(61))
+    B, G, V = 200, 4, 30
+    lt = rng.normal(0, 1, (B, G + 1, V)).astype(np.float32)
+    ld = rng.normal(0, 1, (B, G, V)).astype(np.float32)
+    for arr in (lt, ld):
+        flat = arr.reshape(-1, V)
+        top = rng.integers(V, size=flat.shape[0])
+        flat[np.arange(flat.shape[0]), top] = flat.max(axis=1) + 0.25
+    ld[: B // 2] = lt[: B // 2, :G]          # half the requests: draft agrees
+    x = np.argmax(ld, axis=2).astype(np.int32)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    o1, n1, _ = _run(lib, lt, ld, x, ua, us, np.full(B, 1e-4, np.float32))
+    o0, n0, _ = _run(lib, lt, ld, x, ua, us, np.zeros(B, np.float32))
+    assert np.array_equal(n1, n0) and np.array_equal(o1, o0)
+
+
+# ------------------------------------------------------------ normalisers etc.
+
+def pin_logsumexp_and_row_facts(lib, quick=False):
+    """Per-row facts against library routines: max and argmax (numpy), and the
+    log-normaliser log sum exp(l/T) against scipy.special.logsumexp."""
+    rng = np.random.Generator(np.random.Philox(71))
+    B, G, V = 12, 3, 1000
+    lt = rng.normal(0, 3, (B, G + 1, V)).astype(np.float32)
+    ld = (lt[:, :G] + rng.normal(0, 1, (B, G, V))).astype(np.float32)
+    T = np.array([0.3, 1.0, 2.5, 0.7] * 3, np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    _, _, det = _run(lib, lt, ld, x, rng.random((B, G), dtype=np.float32),
+                     rng.random(B, dtype=np.float32), T, detail=True)
+    lt64, ld64 = lt.astype(np.float64), ld.astype(np.float64)
+    Tc = T.astype(np.float64)[:, None, None]
+    ref_t = special.logsumexp(lt64 / Tc, axis=2)
+    ref_d = special.logsumexp(ld64 / Tc, axis=2)
+    assert np.allclose(det["lse_target"], ref_t, rtol=1e-12, atol=1e-12)
+    assert np.allclose(det["lse_draft"], ref_d, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(det["max_target"], lt64.max(axis=2))
+    assert np.array_equal(det["argmax_target"], np.argmax(lt, axis=2))
+    # gathered probabilities where evaluated
+    p = special.softmax(lt64 / Tc, axis=2)
+    q = special.softmax(ld64 / Tc, axis=2)
+    for b in range(B):
+        for i in range(G):
+            if not np.isnan(det["p_x"][b, i]):
+                assert abs(det["p_x"][b, i] - p[b, i, x[b, i]]) <= 1e-12 * p[b, i, x[b, i]] + 1e-300
+                assert abs(det["q_x"][b, i] - q[b, i, x[b, i]]) <= 1e-12 * q[b, i, x[b, i]] + 1e-300
+
+
+def pin_residual_mass_identity(lib, quick=False):
+    """For a residual draw at position n: W = sum max(p_n - q_n, 0) equals
+    1 - sum min(p_n, q_n) (p and q from scipy's softmax)."""
+    rng = np.random.Generator(np.random.Philox(81))
+    B, G, V, T = 400, 3, 64, float(np.float32(0.9))
+    lt = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+    ld = (lt[:, :G] + rng.normal(0, 1.5, (B, G, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    out, n, det = _run(lib, lt, ld, x, rng.random((B, G), dtype=np.float32),
+                       rng.random(B, dtype=np.float32), np.full(B, T, np.float32), detail=True)
+    p = special.softmax(lt.astype(np.float64) / T, axis=2)
+    q = special.softmax(ld.astype(np.float64) / T, axis=2)
+    seen = 0
+    for b in range(B):
+        k = int(n[b])
+        if k < G:
+            seen += 1
+            assert det["kind"][b] == oracle.KIND_RESIDUAL
+            W = 1.0 - np.minimum(p[b, k], q[b, k]).sum()
+            assert abs(det["w_total"][b] - W) < 1e-12, (b, det["w_total"][b], W)
+            assert p[b, k, out[b, k]] > q[b, k, out[b, k]]  # drawn where p exceeds q
+        else:
+            assert det["kind"][b] == oracle.KIND_BONUS
+            assert abs(det["w_total"][b] - 1.0) < 1e-12
+    assert B // 4 < seen < B  # both kinds of draw occur
+
+
+def pin_equal_rows_reduce_to_categorical(lib, quick=False):
+    """With q = p every draft token is accepted (alpha = 1 > u) and the extra
+    token is a categorical draw from the last row: numpy's
+    searchsorted(cumsum(p), u * sum(p), side='right')."""
+    rng = np.random.Generator(np.random.Philox(91))
+    B, G, V, T = 500, 3, 50, float(np.float32(1.3))
+    lt = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+    ld = lt[:, :G].copy()
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    us = rng.random(B, dtype=np.float32)
+    out, n, _ = _run(lib, lt, ld, x, rng.random((B, G), dtype=np.float32), us,
+                     np.full(B, T, np.float32))
+    assert np.all(n == G)
+    assert np.array_equal(out[:, :G], x)
+    p = special.softmax(lt[:, G].astype(np.float64) / T, axis=1)
+    for b in range(B):
+        c = np.cumsum(p[b])
+        t = float(us[b]) * c[-1]
+        k = int(np.searchsorted(c, t, side="right"))
+        edges = np.concatenate([[0.0], c])
+        if np.min(np.abs(edges - t)) > 1e-9:
+            assert out[b, G] == k, (b, out[b, G], k)
+
+
+# --------------------------------------------------------------- data errors
+
+def pin_invalid_requests(lib, quick=False):
+    """A request that reads a NaN or +inf logit, a row of only -inf, a draft
+    token outside [0, V) or a temperature that is NaN, negative or infinite is
+    reported as n = -1 with every token -1; the other requests are unchanged.
+    -inf logits are allowed and are never drawn. The draft rows of a T = 0
+    request are not read, so a NaN there does not matter."""
+    rng = np.random.Generator(np.random.Philox(101))
+    B, G, V = 12, 3, 16
+    lt = rng.normal(0, 1, (B, G + 1, V)).astype(np.float32)
+    ld = (lt[:, :G] + rng.normal(0, 1, (B, G, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    T = np.full(B, 0.8, np.float32)
+    T[10:] = 0.0
+    base_out, base_n, _ = _run(lib, lt, ld, x, ua, us, T)
+    bad = {}
+    lt2, ld2, x2, T2 = lt.copy(), ld.copy(), x.copy(), T.copy()
+    lt2[0, 2, 5] = np.nan; bad[0] = True
+    lt2[1, 0, 1] = np.inf; bad[1] = True
+    lt2[2, G, :] = -np.inf; bad[2] = True
+    ld2[3, 1, 7] = np.nan; bad[3] = True
+    x2[4, 2] = V; bad[4] = True
+    x2[5, 0] = -1; bad[5] = True
+    T2[6] = -0.5; bad[6] = True
+    T2[7] = np.nan; bad[7] = True
+    T2[8] = np.inf; bad[8] = True
+    ld2[10, 0, 3] = np.nan          # T = 0: draft never read -> still valid
+    lt2[11, 1, :8] = -np.inf        # some -inf is fine
+    out, n, _ = _run(lib, lt2, ld2, x2, ua, us, T2)
+    for b in range(B):
+        if bad.get(b):
+            assert n[b] == -1 and np.all(out[b] == -1), b
+        elif b in (9, 10):
+            assert n[b] == base_n[b] and np.array_equal(out[b], base_out[b]), b
+    assert n[11] >= 0
+    # -inf tokens are never drawn, whatever u
+    lt3 = np.zeros((64, 1 + 1, 6), np.float32)
+    lt3[:, :, ::2] = -np.inf
+    ld3 = np.zeros((64, 1, 6), np.float32)
+    us3 = np.linspace(0, 0.999, 64).astype(np.float32)
+    x3 = (np.arange(64) % 2).astype(np.int32)[:, None]   # token 0 has p = 0: rejected
+    out3, n3, _ = _run(lib, lt3, ld3, x3, np.full((64, 1), 0.9, np.float32),
+                       us3, np.ones(64, np.float32))
+    assert np.array_equal(n3, x3[:, 0])
+    assert np.all(out3[np.arange(64), n3] % 2 == 1)
+    # q(x) = 0 < p(x): alpha is taken as 1, so the token is always accepted
+    ld4 = np.zeros((64, 1, 6), np.float32)
+    ld4[:, 0, 2] = -np.inf
+    lt4 = np.zeros((64, 2, 6), np.float32)
+    out4, n4, _ = _run(lib, lt4, ld4, np.full((64, 1), 2, np.int32),
+                       np.linspace(0, 0.999, 64).astype(np.float32)[:, None], us3,
+                       np.ones(64, np.float32))
+    assert np.all(n4 == 1) and np.all(out4[:, 0] == 2)
+
+
+ALL_PINS = [
+    pin_hand_examples,
+    pin_accept_probability,
+    pin_output_distribution,
+    pin_tokens_per_pass,
+    pin_position_acceptance,
+    pin_greedy_is_argmax_decoding,
+    pin_small_temperature_matches_greedy,
+    pin_logsumexp_and_row_facts,
+    pin_residual_mass_identity,
+    pin_equal_rows_reduce_to_categorical,
+    pin_invalid_requests,
+]

@@ -1,0 +1,76 @@
+"""Mutation check of the oracle's pins.
+
+Each mutant is a copy of the oracle source with one plausible mistake
+planted on the CPU (a swapped operand, a flipped comparison, a dropped term,
+a wrong row or index, a wrong scale). The test compiles the copy and runs the
+pins against it: at least one pin must fail. A mutant that passes every pin
+would mean the pins leave that part of the oracle unchecked.
+"""
+import os
+import shutil
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "specverify_oracle.c")
+
+SAMPLED_TARGET_ROW = ("load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);\n"
+                      "        softmax_T(s->lt, V, T, s->p);\n        load_row(s->draft")
+SAMPLED_BONUS_ROW = ("load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)G, V, s->lt);\n"
+                     "        softmax_T")
+
+MUTANTS = [
+    ("alpha_q_over_p", "alpha = px / qx < 1.0 ? px / qx : 1.0;", "alpha = qx / px < 1.0 ? qx / px : 1.0;"),
+    ("accept_flipped", "if (u < alpha) {", "if (u > alpha) {"),
+    ("residual_q_minus_p", "double diff = s->p[x] - s->q[x];", "double diff = s->q[x] - s->p[x];"),
+    ("temperature_multiplied", "p[x] = exp((l[x] - m) / T);", "p[x] = exp((l[x] - m) * T);"),
+    ("tie_to_highest_index", "if (l[x] > l[a]) a = x;", "if (l[x] >= l[a]) a = x;"),
+    ("bonus_from_row_gamma_minus_1", SAMPLED_BONUS_ROW,
+     SAMPLED_BONUS_ROW.replace("(size_t)G, V", "(size_t)(G - 1), V")),
+    ("draw_without_W", "double t = u * W;", "double t = u;"),
+    ("normaliser_drops_a_term", "        Z += p[x];", "        if (x > 0) Z += p[x];"),
+    ("q_read_from_target", "double px = s->p[x], qx = s->q[x];", "double px = s->p[x], qx = s->p[x];"),
+    ("gather_off_by_one", "        int x = tok[i];", "        int x = (tok[i] + 1) % V;"),
+    ("greedy_keeps_draft_token", "            out[i] = a;\n            return i;",
+     "            out[i] = tok[i];\n            return i;"),
+    ("greedy_count_off_by_one", "            out[i] = a;\n            return i;",
+     "            out[i] = a;\n            return i + 1;"),
+    ("target_row_stride_gamma", SAMPLED_TARGET_ROW,
+     SAMPLED_TARGET_ROW.replace("(size_t)b * (size_t)(G + 1) + (size_t)i", "(size_t)b * (size_t)G + (size_t)i")),
+    ("draft_rows_reversed", "load_row(s->draft, s->dtype, r, V, s->ld);\n        softmax_T(s->ld, V, T, s->q);",
+     "load_row(s->draft, s->dtype, (size_t)b * (size_t)G + (size_t)(G - 1 - i), V, s->ld);\n"
+     "        softmax_T(s->ld, V, T, s->q);"),
+    ("bf16_decoded_wrong", "[idx]) << 16;", "[idx]) << 15;"),
+    ("accepted_token_not_copied", "            out[i] = x;\n        } else {", "            out[i] = tok[0];\n        } else {"),
+    ("no_padding_after_n", "for (int j = 0; j <= gamma; ++j) out[j] = -1;",
+     "for (int j = 0; j < gamma; ++j) out[j] = -1;"),
+    ("residual_from_next_row", "            n = i;\n            break;",
+     "            n = i;\n            if (i + 1 < G) {\n"
+     "                load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)(i + 1), V, s->lt);\n"
+     "                softmax_T(s->lt, V, T, s->p);\n            }\n            break;"),
+    ("q_zero_rejects", "alpha = px > 0.0 ? 1.0 : 0.0;", "alpha = 0.0;"),
+    ("nan_not_detected", "if (isnan(l[x])) return 0;", "if (0) return 0;"),
+    ("draw_from_first_token", "        if (C > t) {", "        if (C >= 0.0) {"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_fails_a_pin(name, old, new, tmp_path):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mdir = tmp_path / "oracle_mutant"
+    mdir.mkdir()
+    shutil.copy(os.path.join(os.path.dirname(SRC), "specverify_oracle.h"), mdir)
+    msrc = mdir / "specverify_oracle.c"
+    msrc.write_text(src.replace(old, new))
+    lib = oracle.load_path(oracle.build(force=True, src=str(msrc), out=str(mdir / "lib.so")))
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib, quick=True)
+        except AssertionError:
+            failed.append(pin.__name__)
+            break
+    assert failed, f"mutant {name} passed every pin"
