@@ -1,0 +1,190 @@
+/*
+ * specverify.h -- C ABI of libspecverify, the GB300 (sm_103a) speculative-
+ * decoding verification step.
+ *
+ * The operation (page title, section):
+ *  - "Speculative Decoding : accélérer l'inférence des LLM",
+ *    §Principe et garanties mathématiques: a draft proposes gamma tokens, the
+ *    target scores all of them in one pass, candidates are accepted while they
+ *    are compatible and the first rejection is corrected by a token drawn from
+ *    the target, so one cycle emits between 1 and gamma + 1 tokens;
+ *    §Pourquoi la qualité est préservée: x is accepted with probability
+ *    min(1, p(x)/q(x)); on rejection the replacement is drawn from p - q
+ *    clipped at zero and renormalised; at temperature zero a token is
+ *    accepted iff it equals the target argmax, else replaced by that argmax.
+ *  - "Speculative Decoding — Come Accelerare l'Inferenza LLM di 2-3x Senza
+ *    Perdere Qualità", §Il meccanismo: the later draft tokens are discarded
+ *    after a rejection.
+ *  - wiki "Speculative Decoding", §数式で見る speculative decoding の正しさ:
+ *    eq. alpha(x) = min(1, p(x)/q(x)) and eq. p_corr(x) = max(p-q,0)/sum.
+ *  - "Accélérer Sonar grâce à la spéculation", §Décodage spéculatif: with n
+ *    draft tokens up to n + 1 tokens are emitted; the target logits at the
+ *    mismatch position, or after the last draft token, give the extra token.
+ *
+ * Readings where the pages are silent: p = softmax(target_logits / T) and
+ * q = softmax(draft_logits / T) with the request's temperature T; accept iff
+ * u_accept < alpha; alpha = 1 when q(x) == 0 < p(x) and 0 when both are 0;
+ * the replacement (or the extra token after gamma acceptances) is the
+ * smallest k with C_k > u_sample * W, C_k the inclusive prefix sum of the
+ * weights in index order and W their total (if rounding leaves none, the last
+ * k with a positive weight); residual weights that sum to zero fall back to
+ * p at that position; argmax ties go to the lowest index.
+ *
+ * Conventions for every entry point:
+ *  - Memory: the caller owns every buffer. Array arguments of spec_verify and
+ *    spec_verify_ex are DEVICE pointers on the current CUDA device. Nothing is
+ *    allocated by the library.
+ *  - Stream: work is enqueued on `stream` (NULL = the legacy default stream)
+ *    and the call returns without waiting for it.
+ *  - Layout: row-major and contiguous. Logit rows are V values; target row i
+ *    of request b is at element (b*(gamma+1) + i)*V, draft row i at
+ *    (b*gamma + i)*V. Row i scores draft token i; target row gamma is the
+ *    bonus row.
+ *  - Argument errors (NULL pointers, B < 0, gamma < 1, V < 1, an unknown
+ *    dtype, a workspace too small, sizes above the limits below) are
+ *    returned before anything is enqueued. B == 0 is a no-op.
+ *  - Data errors never trap: a request whose temperature is NaN, negative or
+ *    infinite, whose draft token lies outside [0, V), or whose rows hold a
+ *    NaN, a +inf or only -inf values gets out_num_accepted = -1 and all its
+ *    out_tokens -1; the draft rows of a T == 0 request are never read.
+ *  - Determinism: the same inputs on the same device give bit-identical
+ *    outputs.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as the CUDA runtime's cudaStream_t. */
+typedef struct CUstream_st* sv_stream_t;
+
+typedef int32_t sv_dtype;
+#define SV_F32 0  /* IEEE binary32 logits */
+#define SV_BF16 1 /* bfloat16 logits (16-bit patterns) */
+
+typedef int32_t sv_status;
+#define SV_OK 0
+#define SV_ERR_INVALID_ARG 1 /* a NULL pointer, a size out of range, an unknown dtype */
+#define SV_ERR_UNSUPPORTED 2 /* no CUDA device, or not compute capability 10.3 */
+#define SV_ERR_CUDA 3        /* a CUDA call failed while enqueueing */
+#define SV_ERR_WORKSPACE 4   /* workspace NULL or smaller than the size query says */
+#define SV_ERR_TIMEOUT 5     /* reserved for host-side waits; kernels report timeouts
+                                through the device status word */
+
+/* Bits of the optional device status word (int32), OR-ed in by the kernels. */
+#define SV_STATUS_BAD_REQUEST 0x1 /* at least one request was invalid (-1) */
+#define SV_STATUS_TIMEOUT 0x2     /* a bounded wait inside a kernel ran out; the
+                                     outputs of that call are not valid */
+
+/* Size limits checked before launch. */
+#define SV_MAX_GAMMA 64
+#define SV_MAX_V (1 << 24)
+
+/* Execution paths of spec_verify_ex (sv_options.path). */
+#define SV_PATH_AUTO 0      /* the library chooses (the streaming path where it applies) */
+#define SV_PATH_ROWWISE 1   /* one thread block per request; any V and alignment */
+#define SV_PATH_STREAMING 2 /* persistent grid streaming all rows with bulk copies into
+                               shared memory; needs V * element size to be a multiple of
+                               16 bytes and 16-byte aligned logit pointers */
+
+/* Bytes of device workspace spec_verify needs for this shape on the current
+ * device (the streaming path's per-row partial results, sampling partial sums
+ * and grid-barrier words). Writes the size to *bytes. Needs the current CUDA
+ * device to read its SM count; returns SV_ERR_UNSUPPORTED without one. */
+sv_status spec_verify_workspace_size(int B, int gamma, int V, sv_dtype dtype, size_t* bytes);
+
+/* The verification step.
+ *  target_logits    [B, gamma+1, V] dtype, device.
+ *  draft_logits     [B, gamma, V] dtype, device; rows of T == 0 requests are never read.
+ *  draft_tokens     [B, gamma] int32, device.
+ *  u_accept         [B, gamma] float, device, uniforms in [0, 1).
+ *  u_sample         [B] float, device, uniforms in [0, 1).
+ *  temperature      [B] float, device; 0 selects the greedy rule.
+ *  out_tokens       [B, gamma+1] int32, device: the n accepted draft tokens,
+ *                   then the replacement (n < gamma) or extra (n == gamma)
+ *                   token, then -1.
+ *  out_num_accepted [B] int32, device: n in [0, gamma], or -1 (invalid request).
+ *  workspace        device, at least spec_verify_workspace_size() bytes,
+ *                   16-byte aligned; its contents need no initialisation and
+ *                   are overwritten. Two calls in flight at once must not share
+ *                   a workspace.
+ * Enqueues work on `stream` and returns SV_OK, or an error before enqueueing. */
+sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      int B, int gamma, int V, const int32_t* draft_tokens,
+                      const float* u_accept, const float* u_sample, const float* temperature,
+                      int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
+                      size_t workspace_bytes, sv_stream_t stream);
+
+/* Optional per-row and per-request facts for checking, all DEVICE pointers,
+ * each may be NULL. Entries the kernels do not compute are written as NaN
+ * (floating point) or -1 (integers). lse is log sum_x exp(l(x)/T), the log
+ * of the softmax normaliser. */
+typedef struct {
+    float* max_target;      /* [B*(gamma+1)] row max */
+    double* lse_target;     /* [B*(gamma+1)] rows of T > 0 requests */
+    int32_t* argmax_target; /* [B*(gamma+1)] rows of T == 0 requests */
+    float* max_draft;       /* [B*gamma] rows of T > 0 requests */
+    double* lse_draft;      /* [B*gamma] rows of T > 0 requests */
+    double* p_x;            /* [B*gamma] p_i(x_i) at the positions evaluated (T > 0) */
+    double* q_x;            /* [B*gamma] q_i(x_i) at the positions evaluated (T > 0) */
+    double* w_total;        /* [B] total weight W of the replacement or extra draw (T > 0) */
+    int32_t* kind;          /* [B] -1 invalid, 0 greedy, 1 residual draw, 2 extra-token draw */
+} sv_debug_out;
+
+typedef struct {
+    int32_t path;      /* SV_PATH_* */
+    int32_t grid_ctas; /* streaming path: thread blocks in the persistent grid; 0 = the
+                          device's full co-resident grid. Smaller grids split rows over
+                          fewer blocks (used by tests to exercise every split). */
+    int32_t reserved[6];
+} sv_options;
+
+/* spec_verify with checking outputs and options. `dbg`, `d_status` and
+ * `opts` may be NULL. `d_status` is a device int32 into which the kernels OR
+ * SV_STATUS_* bits; the caller clears it. */
+sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                         int B, int gamma, int V, const int32_t* draft_tokens,
+                         const float* u_accept, const float* u_sample, const float* temperature,
+                         int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
+                         size_t workspace_bytes, sv_stream_t stream, const sv_debug_out* dbg,
+                         int32_t* d_status, const sv_options* opts);
+
+/* Bytes of device staging memory spec_verify_host needs (inputs, outputs and
+ * workspace) on the current device. */
+sv_status spec_verify_host_staging_size(int B, int gamma, int V, sv_dtype dtype, size_t* bytes);
+
+/* The verification step on HOST buffers: the same arguments as spec_verify
+ * with every array in host memory (page-locked memory keeps the copies
+ * asynchronous), plus one caller-owned DEVICE staging buffer of
+ * spec_verify_host_staging_size() bytes. Enqueues on `stream`: the host to
+ * device copies of the inputs (draft rows only for T > 0 requests, whose
+ * temperatures the host reads here), the verification, and the device to
+ * host copies of out_tokens and out_num_accepted. The outputs are valid once
+ * the stream has reached that point (e.g. after cudaStreamSynchronize). */
+sv_status spec_verify_host(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                           int B, int gamma, int V, const int32_t* draft_tokens,
+                           const float* u_accept, const float* u_sample,
+                           const float* temperature, int32_t* out_tokens,
+                           int32_t* out_num_accepted, void* staging, size_t staging_bytes,
+                           sv_stream_t stream);
+
+/* Number of kernel launches the last successful spec_verify* call on this
+ * host thread enqueued (memsets and copies not counted). */
+int spec_verify_last_launch_count(void);
+
+/* A static English description of a status code. */
+const char* spec_verify_status_string(sv_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int spec_verify_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

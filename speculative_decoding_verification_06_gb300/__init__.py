@@ -1,0 +1,221 @@
+"""Python binding of libspecverify, the sm_103a speculative-decoding
+verification step.
+
+Argument marshalling only: every step of the verification runs in the CUDA
+library (``_lib/libspecverify.so``, built by ``build.py``); this module turns
+torch tensors into device pointers and the current CUDA stream, and calls the
+C ABI of ``include/specverify.h`` by the same names. There is no fallback:
+if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+from . import build as _build
+
+LIB_PATH = _build.LIB_PATH
+
+SV_F32, SV_BF16 = 0, 1
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_WORKSPACE, SV_ERR_TIMEOUT = range(6)
+SV_STATUS_BAD_REQUEST, SV_STATUS_TIMEOUT = 0x1, 0x2
+SV_MAX_GAMMA, SV_MAX_V = 64, 1 << 24
+SV_PATH_AUTO, SV_PATH_ROWWISE, SV_PATH_STREAMING = 0, 1, 2
+KIND_INVALID, KIND_GREEDY, KIND_RESIDUAL, KIND_BONUS = -1, 0, 1, 2
+
+EXPORTED = (
+    "spec_verify_workspace_size", "spec_verify", "spec_verify_ex",
+    "spec_verify_host_staging_size", "spec_verify_host", "spec_verify_last_launch_count",
+    "spec_verify_status_string", "spec_verify_version",
+)
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+        self.status = status
+
+
+class _Debug(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "max_target", "lse_target", "argmax_target", "max_draft", "lse_draft", "p_x", "q_x",
+        "w_total", "kind")]
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 6)]
+
+
+_lib = None
+
+
+def _declare(lib):
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    int_ = ctypes.c_int
+    lib.spec_verify_workspace_size.argtypes = [int_, int_, int_, i32, ctypes.POINTER(sz)]
+    lib.spec_verify_host_staging_size.argtypes = [int_, int_, int_, i32, ctypes.POINTER(sz)]
+    common = [vp, vp, i32, int_, int_, int_, vp, vp, vp, vp, vp, vp]
+    lib.spec_verify.argtypes = common + [vp, sz, vp]
+    lib.spec_verify_ex.argtypes = common + [vp, sz, vp, ctypes.POINTER(_Debug), vp,
+                                            ctypes.POINTER(_Options)]
+    lib.spec_verify_host.argtypes = common + [vp, sz, vp]
+    for name in ("spec_verify_workspace_size", "spec_verify_host_staging_size", "spec_verify",
+                 "spec_verify_ex", "spec_verify_host"):
+        getattr(lib, name).restype = i32
+    lib.spec_verify_status_string.argtypes = [i32]
+    lib.spec_verify_status_string.restype = ctypes.c_char_p
+    lib.spec_verify_version.restype = int_
+    lib.spec_verify_last_launch_count.restype = int_
+    return lib
+
+
+def load():
+    """Load the built library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libspecverify is not built ({LIB_PATH} missing): "
+                               "run __graft_entry__.build() or python -m "
+                               "speculative_decoding_verification_06_gb300.build")
+        _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().spec_verify_status_string(status).decode()
+
+
+def version() -> int:
+    return load().spec_verify_version()
+
+
+def last_launch_count() -> int:
+    return load().spec_verify_last_launch_count()
+
+
+def _check(status: int, where: str):
+    if status != SV_OK:
+        raise SpecVerifyError(status, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype in (torch.bfloat16, torch.int16, torch.uint16):
+        return SV_BF16
+    raise TypeError(f"logits must be float32 or bfloat16 (or 16-bit raw bits), got {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def workspace_size(B: int, gamma: int, V: int, dtype: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().spec_verify_workspace_size(B, gamma, V, dtype, ctypes.byref(n)),
+           "spec_verify_workspace_size")
+    return n.value
+
+
+def host_staging_size(B: int, gamma: int, V: int, dtype: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().spec_verify_host_staging_size(B, gamma, V, dtype, ctypes.byref(n)),
+           "spec_verify_host_staging_size")
+    return n.value
+
+
+@dataclass
+class Outputs:
+    out_tokens: object        # [B, gamma+1] int32
+    out_num_accepted: object  # [B] int32
+    debug: dict | None = None
+    status: object = None     # [1] int32 device status word (spec_verify_ex)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature,
+                out_tokens=None, out_num_accepted=None, workspace=None, stream=None,
+                debug: bool = False, path: int = SV_PATH_AUTO, grid_ctas: int = 0,
+                status=None) -> Outputs:
+    """Verify one batch of CUDA tensors (see include/specverify.h).
+
+    ``target_logits`` [B, gamma+1, V] and ``draft_logits`` [B, gamma, V]
+    float32 or bfloat16, ``draft_tokens`` [B, gamma] int32, ``u_accept``
+    [B, gamma] float32, ``u_sample`` [B] float32, ``temperature`` [B] float32,
+    all contiguous on the current CUDA device. Outputs and workspace are
+    allocated with torch when not given. With ``debug``, ``path``,
+    ``grid_ctas`` or ``status`` the call goes through ``spec_verify_ex``.
+    """
+    import torch
+    lib = load()
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dt = _dtype_code(target_logits)
+    dev = target_logits.device
+    for t in (target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("every input must be a contiguous CUDA tensor")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(16, workspace_size(B, G, V, dt)), dtype=torch.uint8, device=dev)
+    s = _stream_handle(stream)
+    args = (_ptr(target_logits), _ptr(draft_logits), dt, B, G, V, _ptr(draft_tokens),
+            _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
+            _ptr(out_num_accepted), _ptr(workspace), workspace.numel() * workspace.element_size(), s)
+    dbg = None
+    if debug or path != SV_PATH_AUTO or grid_ctas or status is not None:
+        d = _Debug()
+        if debug:
+            f64, f32, i32 = torch.float64, torch.float32, torch.int32
+            dbg = {
+                "max_target": torch.empty((B, G1), dtype=f32, device=dev),
+                "lse_target": torch.empty((B, G1), dtype=f64, device=dev),
+                "argmax_target": torch.empty((B, G1), dtype=i32, device=dev),
+                "max_draft": torch.empty((B, G), dtype=f32, device=dev),
+                "lse_draft": torch.empty((B, G), dtype=f64, device=dev),
+                "p_x": torch.empty((B, G), dtype=f64, device=dev),
+                "q_x": torch.empty((B, G), dtype=f64, device=dev),
+                "w_total": torch.empty((B,), dtype=f64, device=dev),
+                "kind": torch.empty((B,), dtype=i32, device=dev),
+            }
+            for k, v in dbg.items():
+                setattr(d, k, v.data_ptr())
+        o = _Options(path, grid_ctas)
+        rc = lib.spec_verify_ex(*args, ctypes.byref(d), _ptr(status), ctypes.byref(o))
+        _check(rc, "spec_verify_ex")
+    else:
+        _check(lib.spec_verify(*args), "spec_verify")
+    return Outputs(out_tokens, out_num_accepted, dbg, status)
+
+
+def spec_verify_host(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature,
+                     out_tokens, out_num_accepted, staging, stream=None) -> None:
+    """``spec_verify_host``: every array a CPU tensor (pinned for asynchronous
+    copies), ``staging`` a CUDA uint8 tensor of ``host_staging_size`` bytes.
+    Enqueues copies and kernels on ``stream``; the outputs are written when the
+    stream reaches them."""
+    lib = load()
+    B, G1, V = target_logits.shape
+    dt = _dtype_code(target_logits)
+    for t in (target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature,
+              out_tokens, out_num_accepted):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("spec_verify_host takes contiguous host tensors")
+    rc = lib.spec_verify_host(
+        _ptr(target_logits), _ptr(draft_logits), dt, B, G1 - 1, V, _ptr(draft_tokens),
+        _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
+        _ptr(out_num_accepted), _ptr(staging), staging.numel() * staging.element_size(),
+        _stream_handle(stream))
+    _check(rc, "spec_verify_host")

@@ -1,0 +1,280 @@
+// extern "C" entry points of libspecverify (declared in include/specverify.h):
+// argument validation, device query, choice of execution path, and the
+// host-buffer variant that stages inputs and outputs through device memory.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+thread_local int g_last_launches = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+size_t elem_bytes(int dtype) { return dtype == SV_F32 ? 4 : 2; }
+
+bool shape_ok(int B, int gamma, int V, sv_dtype dtype) {
+    return B >= 0 && gamma >= 1 && gamma <= SV_MAX_GAMMA && V >= 1 && V <= SV_MAX_V &&
+           (dtype == SV_F32 || dtype == SV_BF16);
+}
+
+size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+// Bytes the call needs in its workspace for this shape and device.
+size_t workspace_need(int B, int gamma, int V, sv_dtype dtype, const DeviceInfo& dev) {
+    return streaming_workspace_bytes(B, gamma, V, dtype, streaming_default_grid(dev));
+}
+
+}  // namespace
+
+bool current_device(DeviceInfo* info) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (d.device != dev) {
+        DeviceInfo n;
+        n.device = dev;
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        n.num_sms = v;
+        cudaDeviceGetAttribute(&n.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&n.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        n.smem_optin = static_cast<size_t>(v);
+        d = n;
+    }
+    *info = d;
+    return true;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+int spec_verify_version(void) { return 10000; }
+
+int spec_verify_last_launch_count(void) { return g_last_launches; }
+
+const char* spec_verify_status_string(sv_status s) {
+    switch (s) {
+        case SV_OK: return "ok";
+        case SV_ERR_INVALID_ARG: return "invalid argument (null pointer, size out of range or unknown dtype)";
+        case SV_ERR_UNSUPPORTED: return "unsupported device (needs a CUDA device of compute capability 10.3)";
+        case SV_ERR_CUDA: return "a CUDA call failed while enqueueing";
+        case SV_ERR_WORKSPACE: return "workspace missing or smaller than spec_verify_workspace_size()";
+        case SV_ERR_TIMEOUT: return "a bounded wait ran out";
+        default: return "unknown status";
+    }
+}
+
+sv_status spec_verify_workspace_size(int B, int gamma, int V, sv_dtype dtype, size_t* bytes) {
+    if (!bytes || !shape_ok(B, gamma, V, dtype)) return SV_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return SV_ERR_UNSUPPORTED;
+    *bytes = workspace_need(B, gamma, V, dtype, dev);
+    return SV_OK;
+}
+
+sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype dtype, int B,
+                         int gamma, int V, const int32_t* draft_tokens, const float* u_accept,
+                         const float* u_sample, const float* temperature, int32_t* out_tokens,
+                         int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                         sv_stream_t stream, const sv_debug_out* dbg, int32_t* d_status,
+                         const sv_options* opts) {
+    g_last_launches = 0;
+    if (!shape_ok(B, gamma, V, dtype)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !temperature ||
+        !out_tokens || !out_num_accepted)
+        return SV_ERR_INVALID_ARG;
+    const int path = opts ? opts->path : SV_PATH_AUTO;
+    if (path != SV_PATH_AUTO && path != SV_PATH_ROWWISE && path != SV_PATH_STREAMING)
+        return SV_ERR_INVALID_ARG;
+    if (opts && opts->grid_ctas < 0) return SV_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return SV_ERR_UNSUPPORTED;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return SV_ERR_UNSUPPORTED;
+
+    Args a;
+    a.target = target_logits;
+    a.draft = draft_logits;
+    a.dtype = dtype;
+    a.B = B;
+    a.gamma = gamma;
+    a.V = V;
+    a.tokens = draft_tokens;
+    a.u_accept = u_accept;
+    a.u_sample = u_sample;
+    a.temperature = temperature;
+    a.out_tokens = out_tokens;
+    a.out_num_accepted = out_num_accepted;
+    std::memset(&a.dbg, 0, sizeof a.dbg);
+    if (dbg) a.dbg = *dbg;
+    a.d_status = d_status;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    bool use_stream = false;
+    if (path == SV_PATH_STREAMING) {
+        if (!streaming_applicable(a)) return SV_ERR_INVALID_ARG;
+        use_stream = true;
+    } else if (path == SV_PATH_AUTO) {
+        use_stream = streaming_applicable(a);
+    }
+    cudaError_t err;
+    if (use_stream) {
+        int grid = streaming_default_grid(dev);
+        if (opts && opts->grid_ctas > 0) grid = std::min(grid, opts->grid_ctas);
+        const size_t need = streaming_workspace_bytes(B, gamma, V, dtype, grid);
+        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
+            return SV_ERR_WORKSPACE;
+        err = launch_streaming(a, dev, grid, workspace, workspace_bytes, s);
+        if (err == cudaSuccess) g_last_launches = 1;
+    } else {
+        err = launch_rowwise(a, dev, s);
+        if (err == cudaSuccess) g_last_launches = 1;
+    }
+    if (err != cudaSuccess) {
+        g_last_launches = 0;
+        return SV_ERR_CUDA;
+    }
+    return SV_OK;
+}
+
+sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype, int B,
+                      int gamma, int V, const int32_t* draft_tokens, const float* u_accept,
+                      const float* u_sample, const float* temperature, int32_t* out_tokens,
+                      int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                      sv_stream_t stream) {
+    return spec_verify_ex(target_logits, draft_logits, dtype, B, gamma, V, draft_tokens, u_accept,
+                          u_sample, temperature, out_tokens, out_num_accepted, workspace,
+                          workspace_bytes, stream, nullptr, nullptr, nullptr);
+}
+
+// ---------------------------------------------------------------- host path
+
+namespace {
+
+struct Staging {
+    size_t target, draft, tokens, u_accept, u_sample, temperature, out_tokens, out_num, workspace,
+        end;
+};
+
+Staging staging_layout(int B, int gamma, int V, sv_dtype dtype, size_t ws) {
+    const size_t es = elem_bytes(dtype);
+    Staging l;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align16(off + bytes);
+        return at;
+    };
+    l.target = take(static_cast<size_t>(B) * (gamma + 1) * V * es);
+    l.draft = take(static_cast<size_t>(B) * gamma * V * es);
+    l.tokens = take(static_cast<size_t>(B) * gamma * 4);
+    l.u_accept = take(static_cast<size_t>(B) * gamma * 4);
+    l.u_sample = take(static_cast<size_t>(B) * 4);
+    l.temperature = take(static_cast<size_t>(B) * 4);
+    l.out_tokens = take(static_cast<size_t>(B) * (gamma + 1) * 4);
+    l.out_num = take(static_cast<size_t>(B) * 4);
+    l.workspace = take(ws);
+    l.end = off;
+    return l;
+}
+
+}  // namespace
+
+sv_status spec_verify_host_staging_size(int B, int gamma, int V, sv_dtype dtype, size_t* bytes) {
+    if (!bytes || !shape_ok(B, gamma, V, dtype)) return SV_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return SV_ERR_UNSUPPORTED;
+    *bytes = staging_layout(B, gamma, V, dtype, workspace_need(B, gamma, V, dtype, dev)).end;
+    return SV_OK;
+}
+
+sv_status spec_verify_host(const void* target_logits, const void* draft_logits, sv_dtype dtype, int B,
+                           int gamma, int V, const int32_t* draft_tokens, const float* u_accept,
+                           const float* u_sample, const float* temperature, int32_t* out_tokens,
+                           int32_t* out_num_accepted, void* staging, size_t staging_bytes,
+                           sv_stream_t stream) {
+    g_last_launches = 0;
+    if (!shape_ok(B, gamma, V, dtype)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !temperature ||
+        !out_tokens || !out_num_accepted)
+        return SV_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return SV_ERR_UNSUPPORTED;
+    const size_t ws = workspace_need(B, gamma, V, dtype, dev);
+    const Staging l = staging_layout(B, gamma, V, dtype, ws);
+    if (!staging || staging_bytes < l.end || (reinterpret_cast<uintptr_t>(staging) & 15))
+        return SV_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(staging);
+    const size_t es = elem_bytes(dtype);
+    const size_t drow_bytes = static_cast<size_t>(gamma) * V * es;
+    auto h2d = [&](size_t off, const void* src, size_t bytes) {
+        return cudaMemcpyAsync(base + off, src, bytes, cudaMemcpyHostToDevice, s);
+    };
+    cudaError_t err = h2d(l.target, target_logits, static_cast<size_t>(B) * (gamma + 1) * V * es);
+    // Draft rows: only requests with T > 0 are read, copied in runs of
+    // consecutive such requests.
+    for (int b = 0; b < B && err == cudaSuccess;) {
+        if (!(temperature[b] > 0.0f)) {
+            ++b;
+            continue;
+        }
+        int e = b + 1;
+        while (e < B && temperature[e] > 0.0f) ++e;
+        err = h2d(l.draft + static_cast<size_t>(b) * drow_bytes,
+                  static_cast<const char*>(draft_logits) + static_cast<size_t>(b) * drow_bytes,
+                  static_cast<size_t>(e - b) * drow_bytes);
+        b = e;
+    }
+    if (err == cudaSuccess) err = h2d(l.tokens, draft_tokens, static_cast<size_t>(B) * gamma * 4);
+    if (err == cudaSuccess) err = h2d(l.u_accept, u_accept, static_cast<size_t>(B) * gamma * 4);
+    if (err == cudaSuccess) err = h2d(l.u_sample, u_sample, static_cast<size_t>(B) * 4);
+    if (err == cudaSuccess) err = h2d(l.temperature, temperature, static_cast<size_t>(B) * 4);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    sv_status st = spec_verify(base + l.target, base + l.draft, dtype, B, gamma, V,
+                               reinterpret_cast<const int32_t*>(base + l.tokens),
+                               reinterpret_cast<const float*>(base + l.u_accept),
+                               reinterpret_cast<const float*>(base + l.u_sample),
+                               reinterpret_cast<const float*>(base + l.temperature),
+                               reinterpret_cast<int32_t*>(base + l.out_tokens),
+                               reinterpret_cast<int32_t*>(base + l.out_num), base + l.workspace, ws,
+                               stream);
+    if (st != SV_OK) return st;
+    const int launches = g_last_launches;
+    err = cudaMemcpyAsync(out_tokens, base + l.out_tokens, static_cast<size_t>(B) * (gamma + 1) * 4,
+                          cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess)
+        err = cudaMemcpyAsync(out_num_accepted, base + l.out_num, static_cast<size_t>(B) * 4,
+                              cudaMemcpyDeviceToHost, s);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        g_last_launches = 0;
+        return SV_ERR_CUDA;
+    }
+    g_last_launches = launches;
+    return SV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,208 @@
+// Device-side building blocks shared by the two execution paths of
+// libspecverify: logit loads, the per-row online (max, sum) state, the
+// argmax state, the acceptance test and the inverse-CDF weights.
+//
+// Arithmetic conventions (both paths):
+//  * c = log2(e) / T, rounded once to binary32. A row's normaliser is kept as
+//    (m, s) with m the row max and s = sum_x 2^((l(x) - m) * c); the
+//    difference l - m is exact for bfloat16 inputs, so the dominant terms
+//    carry almost no exponent error.
+//  * 2^x uses the special-function unit (PTX ex2.approx.ftz.f32).
+//  * The acceptance test of "Speculative Decoding : accélérer l'inférence des
+//    LLM", §Pourquoi la qualité est préservée, u < min(1, p(x)/q(x)), is
+//    evaluated in double from the row statistics.
+//  * Inverse-CDF draws: each thread sums the binary32 weights of a run of
+//    consecutive tokens; the run sums are converted to unsigned 64-bit fixed
+//    point (2^-60 units for residual weights, which sum to at most 1; 2^-39
+//    for unnormalised target weights, each at most 1 and at most 2^24 of
+//    them) so that every prefix sum is exact and independent of the order in
+//    which a reduction or scan adds them.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "specverify.h"
+
+namespace sv {
+
+constexpr double kLog2e = 1.4426950408889634073599246810019;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
+__device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000u); }
+
+// 2^x on the special-function unit; results below 2^-126 flush to zero.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float temp_scale(float T) {
+    return __double2float_rn(kLog2e / static_cast<double>(T));
+}
+
+__device__ __forceinline__ float bf16_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+__device__ __forceinline__ float bf16x2_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16x2_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// A logit that must not be read: NaN or +inf.
+__device__ __forceinline__ bool bad_logit(float x) { return !(x < pos_inf()); }
+
+template <int DT>
+__device__ __forceinline__ float load_logit(const void* base, size_t idx);
+
+template <>
+__device__ __forceinline__ float load_logit<SV_F32>(const void* base, size_t idx) {
+    return __ldg(static_cast<const float*>(base) + idx);
+}
+
+template <>
+__device__ __forceinline__ float load_logit<SV_BF16>(const void* base, size_t idx) {
+    return bf16_to_float(__ldg(static_cast<const unsigned short*>(base) + idx));
+}
+
+// ---------------------------------------------------------------- row state
+
+// Online normaliser state: s = sum 2^((l - m) c) over the logits seen so far.
+struct MaxSum {
+    float m;
+    float s;
+};
+
+__device__ __forceinline__ MaxSum maxsum_empty() { return {neg_inf(), 0.0f}; }
+
+// Adds one logit (the caller screens NaN and +inf).
+__device__ __forceinline__ void maxsum_add(MaxSum& st, float x, float c) {
+    if (x > st.m) {
+        st.s = (st.m == neg_inf()) ? 1.0f : __fadd_rn(__fmul_rn(st.s, ex2(__fmul_rn(__fsub_rn(st.m, x), c))), 1.0f);
+        st.m = x;
+    } else if (x != neg_inf()) {
+        st.s = __fadd_rn(st.s, ex2(__fmul_rn(__fsub_rn(x, st.m), c)));
+    }
+}
+
+// Merges b into a.
+__device__ __forceinline__ MaxSum maxsum_merge(MaxSum a, MaxSum b, float c) {
+    if (b.m > a.m) {
+        MaxSum t = a;
+        a = b;
+        b = t;
+    }
+    if (b.m == neg_inf()) return a;
+    a.s = __fadd_rn(a.s, __fmul_rn(b.s, ex2(__fmul_rn(__fsub_rn(b.m, a.m), c))));
+    return a;
+}
+
+// Argmax state with the lowest index winning ties.
+struct ArgMax {
+    float v;
+    int32_t i;
+};
+
+__device__ __forceinline__ ArgMax argmax_empty() { return {neg_inf(), 0x7fffffff}; }
+
+__device__ __forceinline__ ArgMax argmax_merge(ArgMax a, ArgMax b) {
+    return (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;
+}
+
+// ------------------------------------------------------------ decisions
+
+// p(x) = 2^((l - m) c) / s, in double.
+__device__ __forceinline__ double prob_from_stats(float l, float m, float s, float c) {
+    return exp2((static_cast<double>(l) - static_cast<double>(m)) * static_cast<double>(c)) /
+           static_cast<double>(s);
+}
+
+// u < alpha with alpha = min(1, p/q); alpha = 1 if q == 0 < p, 0 if p == q == 0.
+__device__ __forceinline__ bool accept_draft(double p, double q, float u) {
+    double alpha = q > 0.0 ? fmin(1.0, p / q) : (p > 0.0 ? 1.0 : 0.0);
+    return static_cast<double>(u) < alpha;
+}
+
+// log sum_x exp(l(x)/T) from (m, s): m/T + ln(s), with m/T in double.
+__device__ __forceinline__ double lse_from_stats(float m, float s, float T) {
+    return static_cast<double>(m) / static_cast<double>(T) + log(static_cast<double>(s));
+}
+
+// ------------------------------------------------------- inverse-CDF weights
+
+// Draw kinds, also reported in sv_debug_out.kind.
+constexpr int kKindInvalid = -1;
+constexpr int kKindGreedy = 0;
+constexpr int kKindResidual = 1;
+constexpr int kKindBonus = 2;
+
+constexpr float kFixResidual = 1152921504606846976.0f;  // 2^60
+constexpr float kFixTarget = 549755813888.0f;           // 2^39
+constexpr double kFixResidualInv = 1.0 / 1152921504606846976.0;
+constexpr double kFixTargetInv = 1.0 / 549755813888.0;
+
+// Weights of one draw. Residual: max(p - q, 0) from target row n and draft
+// row n ("Speculative Decoding" wiki, eq. p_corr). Target: 2^((l - m) c),
+// proportional to p at the target row (the extra token, or the fallback when
+// residual weights sum to zero).
+struct DrawParams {
+    int kind;      // kKindResidual or kKindBonus
+    float c;
+    float mp, isp; // target row: max and 1/s
+    float mq, isq; // draft row (residual only)
+    float fix;     // fixed-point scale
+};
+
+__device__ __forceinline__ float weight_target(float lt, const DrawParams& d) {
+    return ex2(__fmul_rn(__fsub_rn(lt, d.mp), d.c));
+}
+
+__device__ __forceinline__ float weight_residual(float lt, float ld, const DrawParams& d) {
+    float p = __fmul_rn(ex2(__fmul_rn(__fsub_rn(lt, d.mp), d.c)), d.isp);
+    float q = __fmul_rn(ex2(__fmul_rn(__fsub_rn(ld, d.mq), d.c)), d.isq);
+    return fmaxf(__fsub_rn(p, q), 0.0f);
+}
+
+__device__ __forceinline__ unsigned long long to_fixed(float run_sum, float fix) {
+    return __float2ull_rz(__fmul_rn(run_sum, fix));
+}
+
+// ------------------------------------------------------------ reductions
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Exclusive prefix sum of v over the threads of a block of NT threads (exact:
+// integers). `scratch` holds NT/32 + 1 values. Also returns the block total.
+template <int NT>
+__device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v,
+                                                                  unsigned long long* scratch,
+                                                                  unsigned long long* total) {
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long run = 0;
+        for (int w = 0; w < NW; ++w) {
+            unsigned long long t = scratch[w];
+            scratch[w] = run;
+            run += t;
+        }
+        scratch[NW] = run;
+    }
+    __syncthreads();
+    unsigned long long excl = scratch[warp] + (x - v);
+    *total = scratch[NW];
+    __syncthreads();
+    return excl;
+}
+
+}  // namespace sv

@@ -1,0 +1,49 @@
+// Internal declarations shared by the translation units of libspecverify.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "specverify.h"
+
+namespace sv {
+
+// All arguments of one verification call, after host-side validation.
+struct Args {
+    const void* target;  // [B, gamma+1, V]
+    const void* draft;   // [B, gamma, V]
+    int dtype;           // SV_F32 / SV_BF16
+    int B, gamma, V;
+    const int32_t* tokens;      // [B, gamma]
+    const float* u_accept;      // [B, gamma]
+    const float* u_sample;      // [B]
+    const float* temperature;   // [B]
+    int32_t* out_tokens;        // [B, gamma+1]
+    int32_t* out_num_accepted;  // [B]
+    sv_debug_out dbg;           // device pointers, each may be null
+    int32_t* d_status;          // may be null
+};
+
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    size_t smem_optin = 0;
+};
+
+// Cached properties of the current device; false when there is none.
+bool current_device(DeviceInfo* info);
+
+// Rowwise path: one thread block per request. Enqueues one kernel.
+cudaError_t launch_rowwise(const Args& a, const DeviceInfo& dev, cudaStream_t stream);
+
+// Streaming path: persistent grid. Workspace layout and launch.
+bool streaming_applicable(const Args& a);
+size_t streaming_workspace_bytes(int B, int gamma, int V, int dtype, int grid);
+int streaming_default_grid(const DeviceInfo& dev);
+cudaError_t launch_streaming(const Args& a, const DeviceInfo& dev, int grid, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+}  // namespace sv

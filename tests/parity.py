@@ -1,0 +1,186 @@
+"""Element-by-element comparison of the CUDA library against the CPU oracle.
+
+Tolerances (derivation in DESIGN.md, "Parity bar"):
+  * greedy requests: tokens and accepted counts bit-exact;
+  * invalid requests: both sides report -1;
+  * row maxima: exact; argmax of greedy rows: exact;
+  * log-normalisers log sum exp(l/T): within 1e-5 absolute (1e-5 relative
+    on the normaliser); gathered p(x_i), q(x_i) and the draw total W: within
+    1e-5 relative;
+  * sampled requests: every accept decision whose margin |u - alpha| / alpha
+    exceeds 1e-5, and every draw whose distance of t = u W to the nearer CDF
+    edge exceeds 1e-5 W, must match exactly. A decision inside the margin is
+    a near tie: it is counted, the outputs before it must match, and a draw
+    inside the margin must still pick a token whose CDF interval (oracle
+    arithmetic, fp64) lies within 1e-5 W of t.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+MARGIN = 1e-5
+REL_TOL = 1e-5
+
+
+@dataclass
+class Report:
+    requests: int = 0
+    greedy: int = 0
+    sampled: int = 0
+    invalid: int = 0
+    exact_rows: int = 0
+    accept_near_ties: int = 0
+    sample_near_ties: int = 0
+    max_lse_err: float = 0.0
+    max_px_rel: float = 0.0
+    max_w_rel: float = 0.0
+    notes: list = field(default_factory=list)
+
+    def summary(self) -> str:
+        return (f"{self.requests} requests ({self.greedy} greedy, {self.sampled} sampled, "
+                f"{self.invalid} invalid): {self.exact_rows} exact, near ties: "
+                f"{self.accept_near_ties} accept / {self.sample_near_ties} draw; max |dlse| "
+                f"{self.max_lse_err:.2e}, max rel p/q {self.max_px_rel:.2e}, max rel W "
+                f"{self.max_w_rel:.2e}")
+
+
+def _row_values(arr, dtype):
+    from workloads.synthetic import bf16_bits_to_f32
+    a = np.asarray(arr)
+    return (bf16_bits_to_f32(a) if a.dtype == np.uint16 else a).astype(np.float64)
+
+
+def _draw_weights(batch, b, n, kind):
+    """fp64 weights of the oracle's draw (used only to judge near-tie draws)."""
+    from scipy import special
+    T = float(batch.temperature[b])
+    lt = _row_values(batch.target[b, n], None)
+    p = special.softmax(lt / T)
+    if kind == 1:
+        ld = _row_values(batch.draft[b, n], None)
+        w = np.maximum(p - special.softmax(ld / T), 0.0)
+        if w.sum() == 0.0:
+            w = p
+        return w
+    return p
+
+
+def compare(batch, gpu, ora, det, margin=MARGIN, rel_tol=REL_TOL) -> Report:
+    """``gpu``: dict of numpy arrays out_tokens, out_num_accepted and the
+    debug arrays; ``ora`` = (out_tokens, num_accepted), ``det`` the oracle's
+    detail dict. Raises AssertionError on the first mismatch."""
+    go, gn = gpu["out_tokens"], gpu["out_num_accepted"]
+    oo, on = ora
+    B, G1 = oo.shape
+    G = G1 - 1
+    rep = Report(requests=B)
+    T = batch.temperature
+    for b in range(B):
+        ctx = f"request {b} (T={T[b]})"
+        if on[b] == -1:
+            rep.invalid += 1
+            assert gn[b] == -1 and np.all(go[b] == -1), f"{ctx}: oracle invalid, gpu {gn[b]} {go[b]}"
+            continue
+        assert gn[b] != -1, f"{ctx}: gpu reports invalid, oracle n={on[b]}"
+        if T[b] == 0.0:
+            rep.greedy += 1
+            assert gn[b] == on[b] and np.array_equal(go[b], oo[b]), \
+                f"{ctx}: greedy mismatch gpu n={gn[b]} {go[b]} oracle n={on[b]} {oo[b]}"
+            rep.exact_rows += 1
+            continue
+        rep.sampled += 1
+        n_o = int(on[b])
+        am = det["accept_margin"][b]
+        tie = next((i for i in range(min(n_o + 1, G)) if am[i] <= margin), None)
+        if tie is not None:
+            rep.accept_near_ties += 1
+            assert gn[b] >= tie and np.array_equal(go[b, :tie], oo[b, :tie]), \
+                f"{ctx}: mismatch before the near-tie decision at {tie}"
+            continue
+        assert gn[b] == n_o and np.array_equal(go[b, :n_o], oo[b, :n_o]), \
+            f"{ctx}: accept mismatch gpu n={gn[b]} {go[b]} oracle n={n_o} {oo[b]} margins {am}"
+        assert np.all(go[b, n_o + 1:] == -1)
+        if det["sample_margin"][b] > margin:
+            assert go[b, n_o] == oo[b, n_o], \
+                f"{ctx}: draw mismatch gpu {go[b, n_o]} oracle {oo[b, n_o]} margin {det['sample_margin'][b]}"
+            rep.exact_rows += 1
+        else:
+            rep.sample_near_ties += 1
+            w = _draw_weights(batch, b, n_o, int(det["kind"][b]))
+            C = np.cumsum(w)
+            W = C[-1]
+            t = float(batch.u_sample[b]) * W
+            k = int(go[b, n_o])
+            lo = C[k - 1] if k > 0 else 0.0
+            assert w[k] > 0 and lo - margin * W <= t <= C[k] + margin * W, \
+                f"{ctx}: near-tie draw picked token {k} outside the margin"
+    # normalisers and gathered probabilities
+    if "lse_target" in gpu:
+        samp = T > 0
+        valid = on >= 0
+        rows = samp & valid
+        if rows.any():
+            d = np.abs(gpu["lse_target"][rows] - det["lse_target"][rows])
+            rep.max_lse_err = max(rep.max_lse_err, float(d.max()))
+            dd = np.abs(gpu["lse_draft"][rows] - det["lse_draft"][rows])
+            rep.max_lse_err = max(rep.max_lse_err, float(dd.max()))
+            assert rep.max_lse_err <= 1e-5, f"log-normaliser error {rep.max_lse_err}"
+            assert np.array_equal(gpu["max_draft"][rows].astype(np.float64), det["max_draft"][rows])
+        if valid.any():
+            assert np.array_equal(gpu["max_target"][valid].astype(np.float64), det["max_target"][valid])
+        g = (T == 0) & valid
+        if g.any():
+            assert np.array_equal(gpu["argmax_target"][g], det["argmax_target"][g])
+        both = ~np.isnan(det["p_x"]) & ~np.isnan(gpu["p_x"])
+        if both.any():
+            for key in ("p_x", "q_x"):
+                ref = det[key][both]
+                err = np.abs(gpu[key][both] - ref) / np.maximum(ref, 1e-300)
+                rep.max_px_rel = max(rep.max_px_rel, float(err.max()))
+            assert rep.max_px_rel <= rel_tol, f"gathered probability error {rep.max_px_rel}"
+        same = samp & valid & (gn == on) & ~np.isnan(det["w_total"])
+        if same.any():
+            err = np.abs(gpu["w_total"][same] - det["w_total"][same]) / det["w_total"][same]
+            rep.max_w_rel = float(err.max())
+            assert rep.max_w_rel <= rel_tol, f"draw total error {rep.max_w_rel}"
+    return rep
+
+
+# ------------------------------------------------------------ running both
+
+def to_device(batch, device="cuda"):
+    import torch
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return [t(a) for a in batch.arrays()]
+
+
+def run_gpu(batch, debug=True, device="cuda", **kw):
+    """Runs the CUDA library on ``batch``; returns numpy outputs (and debug)."""
+    import torch
+    import speculative_decoding_verification_06_gb300 as sv
+    args = to_device(batch, device)
+    status = torch.zeros(1, dtype=torch.int32, device=device) if debug else None
+    res = sv.spec_verify(*args, debug=debug, status=status, **kw)
+    torch.cuda.synchronize()
+    out = {"out_tokens": res.out_tokens.cpu().numpy(),
+           "out_num_accepted": res.out_num_accepted.cpu().numpy()}
+    if res.debug:
+        out.update({k: v.cpu().numpy() for k, v in res.debug.items()})
+    if status is not None:
+        out["status"] = int(status.cpu()[0])
+    return out
+
+
+def run_oracle(batch, threads=None):
+    import oracle
+    o, n, det = oracle.verify_threaded(*batch.arrays(), detail=True, threads=threads)
+    return (o, n), det
+
+
+def check(batch, threads=None, **kw) -> Report:
+    gpu = run_gpu(batch, **kw)
+    ora, det = run_oracle(batch, threads)
+    return compare(batch, gpu, ora, det)

@@ -1,0 +1,202 @@
+"""Parity of the CUDA library with the CPU oracle, through the C ABI.
+
+Every test here needs a GPU (marker ``gpu``). Inputs are the seeded
+synthetic workloads; the oracle runs on the same bytes. Comparison rules are
+in parity.py.
+"""
+import numpy as np
+import pytest
+
+import parity
+from workloads import synthetic
+
+pytestmark = pytest.mark.gpu
+
+sv = pytest.importorskip("speculative_decoding_verification_06_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    sv.build.build()
+    sv.load()
+    torch.cuda.set_device(0)
+
+
+ROWWISE = dict(path=sv.SV_PATH_ROWWISE)
+AUTO = dict(path=sv.SV_PATH_AUTO)
+
+
+def _small(config, **changes):
+    return synthetic.WORKLOADS[config].variant(**changes)
+
+
+SMALL_CASES = [
+    ("tiny", _small(1)),
+    ("mixed_V4096_bf16", _small(4, B=6, V=4096)),
+    ("mixed_V4099_ragged_bf16", _small(4, B=5, gamma=3, V=4099)),
+    ("sampling_V3000_f32", _small(3, B=7, gamma=2, V=3000, hot_tokens=5)),
+    ("sampling_V1_f32", _small(3, B=3, gamma=2, V=1, hot_tokens=0)),
+    ("sampling_V2_bf16", _small(5, B=9, gamma=5, V=2, zipf_s=0.0)),
+    ("large_gamma16_V777", _small(4, B=4, gamma=16, V=777)),
+    ("greedy_V20000", _small(2, B=3, V=20000)),
+]
+
+
+@pytest.mark.parametrize("name,w", SMALL_CASES, ids=[c[0] for c in SMALL_CASES])
+@pytest.mark.parametrize("opts", [ROWWISE, AUTO], ids=["rowwise", "auto"])
+def test_small_cases(name, w, opts):
+    for k in range(3):
+        batch = synthetic.generate(w, k=k)
+        rep = parity.check(batch, **opts)
+        assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
+
+
+@pytest.mark.parametrize("config", [1, 2, 3, 4, 5])
+def test_full_configs(config):
+    batch = synthetic.generate(config)
+    gpu = parity.run_gpu(batch)
+    ora, det = parity.run_oracle(batch)
+    rep = parity.compare(batch, gpu, ora, det)
+    print(f"config {config}:", rep.summary())
+    assert rep.invalid == 0
+    # near ties are rare events; a large count would point at an accuracy loss
+    assert rep.accept_near_ties <= max(2, batch.B // 100)
+
+
+def test_full_config_rowwise_cross_check():
+    """The two execution paths agree on a full-size mixed batch (outside
+    near ties, where both must match the oracle)."""
+    batch = synthetic.generate(4)
+    ora, det = parity.run_oracle(batch)
+    for opts in (ROWWISE, AUTO):
+        parity.compare(batch, parity.run_gpu(batch, **opts), ora, det)
+
+
+def test_deterministic():
+    batch = synthetic.generate(_small(4, B=16, V=50000))
+    a = parity.run_gpu(batch)
+    b = parity.run_gpu(batch)
+    for key in ("out_tokens", "out_num_accepted", "lse_target", "p_x", "w_total"):
+        assert np.array_equal(a[key], b[key], equal_nan=True), key
+
+
+def test_invalid_requests():
+    rng = np.random.Generator(np.random.Philox(7))
+    B, G, V = 12, 3, 640
+    lt = rng.normal(0, 1, (B, G + 1, V)).astype(np.float32)
+    ld = (lt[:, :G] + rng.normal(0, 1, (B, G, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    T = np.full(B, 0.8, np.float32)
+    T[10:] = 0.0
+    lt[0, 2, 5] = np.nan
+    lt[1, 0, 1] = np.inf
+    lt[2, G, :] = -np.inf
+    ld[3, 1, 7] = np.nan
+    x[4, 2] = V
+    x[5, 0] = -1
+    T[6] = -0.5
+    T[7] = np.nan
+    T[8] = np.inf
+    ld[10, 0, 3] = np.nan
+    lt[11, 1, :300] = -np.inf
+    w = synthetic.WORKLOADS[3].variant(B=B, gamma=G, V=V)
+    batch = synthetic.Batch(w, 0, lt, ld, x, ua, us, T)
+    for opts in (ROWWISE, AUTO):
+        gpu = parity.run_gpu(batch, **opts)
+        ora, det = parity.run_oracle(batch)
+        rep = parity.compare(batch, gpu, ora, det)
+        assert rep.invalid == 9
+        assert gpu["status"] & sv.SV_STATUS_BAD_REQUEST
+
+
+def _v8_batch(N, T, seed):
+    from scipy import special
+    rng = np.random.Generator(np.random.Philox(seed))
+    lt = rng.normal(0, 1.5, (2, 8)).astype(np.float32)
+    ld = (lt[:1] + rng.normal(0, 1.2, (1, 8))).astype(np.float32)
+    Tf = float(np.float32(T))
+    p0 = special.softmax(lt[0].astype(np.float64) / Tf)
+    q0 = special.softmax(ld[0].astype(np.float64) / Tf)
+    pb = special.softmax(lt[1].astype(np.float64) / Tf)
+    x = rng.choice(8, size=N, p=q0).astype(np.int32)[:, None]
+    w = synthetic.WORKLOADS[1].variant(B=N, gamma=1, V=8)
+    batch = synthetic.Batch(w, seed, np.ascontiguousarray(np.broadcast_to(lt, (N, 2, 8))),
+                            np.ascontiguousarray(np.broadcast_to(ld, (N, 1, 8))), x,
+                            rng.random((N, 1), dtype=np.float32), rng.random(N, dtype=np.float32),
+                            np.full(N, T, np.float32))
+    return batch, p0, q0, pb
+
+
+def _chi2_ok(counts, probs, label):
+    from scipy import stats
+    counts = np.asarray(counts, np.float64)
+    nz = probs > 0
+    assert np.all(counts[~nz] == 0), label
+    exp = counts.sum() * probs[nz]
+    chi2 = float(((counts[nz] - exp) ** 2 / exp).sum())
+    limit = float(stats.chi2.isf(1e-3, int(nz.sum()) - 1))
+    assert chi2 < limit, f"{label}: chi2 {chi2:.2f} >= {limit:.2f}"
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_output_distribution_on_gpu(T):
+    """10^6 trials at V = 8 through the CUDA path: P(accept) = sum min(p, q),
+    first token ~ p, residual ~ p_corr, extra token ~ p of the last row."""
+    N = 1_000_000
+    batch, p0, q0, pb = _v8_batch(N, T, seed=5 if T == 1.0 else 6)
+    gpu = parity.run_gpu(batch, debug=False)
+    out, n = gpu["out_tokens"], gpu["out_num_accepted"]
+    beta = float(np.minimum(p0, q0).sum())
+    acc = (n == 1).mean()
+    assert abs(acc - beta) < 5 * np.sqrt(beta * (1 - beta) / N)
+    _chi2_ok(np.bincount(out[:, 0], minlength=8), p0, "first token ~ p")
+    pc = np.maximum(p0 - q0, 0)
+    _chi2_ok(np.bincount(out[n == 0, 0], minlength=8), pc / pc.sum(), "residual ~ p_corr")
+    _chi2_ok(np.bincount(out[n == 1, 1], minlength=8), pb, "bonus ~ p")
+
+
+def test_tokens_per_pass_on_gpu():
+    """alpha = 0.8, gamma = 4: (1 - 0.8^5)/(1 - 0.8) = 3.3616 tokens per pass."""
+    N, G = 1_000_000, 4
+    rng = np.random.Generator(np.random.Philox(9))
+    lt = np.log(np.array([0.7, 0.3])).astype(np.float32)
+    ld = np.log(np.array([0.9, 0.1])).astype(np.float32)
+    w = synthetic.WORKLOADS[1].variant(B=N, gamma=G, V=2)
+    batch = synthetic.Batch(w, 0, np.ascontiguousarray(np.broadcast_to(lt, (N, G + 1, 2))),
+                            np.ascontiguousarray(np.broadcast_to(ld, (N, G, 2))),
+                            (rng.random((N, G)) < 0.1).astype(np.int32),
+                            rng.random((N, G), dtype=np.float32), rng.random(N, dtype=np.float32),
+                            np.ones(N, np.float32))
+    n = parity.run_gpu(batch, debug=False)["out_num_accepted"]
+    pk = np.array([0.8 ** k * 0.2 for k in range(G)] + [0.8 ** G])
+    sd = np.sqrt(sum((k - 2.3616) ** 2 * pk[k] for k in range(G + 1)))
+    assert abs((n + 1).mean() - 3.3616) < 5 * sd / np.sqrt(N)
+    _chi2_ok(np.bincount(n, minlength=G + 1), pk, "P(n = k)")
+
+
+def test_host_entry_matches_device_entry():
+    import torch
+    batch = synthetic.generate(_small(4, B=12, V=8192))
+    dev = parity.run_gpu(batch, debug=False)
+    t = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in batch.arrays()]
+    out_tokens = torch.empty((batch.B, batch.workload.gamma + 1), dtype=torch.int32).pin_memory()
+    out_n = torch.empty((batch.B,), dtype=torch.int32).pin_memory()
+    wl = batch.workload
+    staging = torch.empty(sv.host_staging_size(wl.B, wl.gamma, wl.V, sv.SV_BF16),
+                          dtype=torch.uint8, device="cuda")
+    sv.spec_verify_host(*t, out_tokens, out_n, staging)
+    torch.cuda.synchronize()
+    assert sv.last_launch_count() >= 1
+    assert np.array_equal(out_tokens.numpy(), dev["out_tokens"])
+    assert np.array_equal(out_n.numpy(), dev["out_num_accepted"])
+
+
+def test_one_launch_per_call():
+    batch = synthetic.generate(_small(4, B=8, V=8192))
+    parity.run_gpu(batch, debug=False)
+    assert sv.last_launch_count() == 1

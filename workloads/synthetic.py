@@ -29,6 +29,7 @@ round-to-nearest-even.
 """
 from __future__ import annotations
 
+import dataclasses
 import os
 from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
@@ -58,9 +59,11 @@ class Workload:
 
     def scaled(self, B: int) -> "Workload":
         """The same recipe with another batch size (for bounded samples)."""
-        return Workload(self.config, self.name, B, self.gamma, self.V, self.dtype,
-                        self.temperatures, self.target_sigma, self.draft_sigma,
-                        self.hot_tokens, self.hot_boost, self.zipf_s, self.description)
+        return dataclasses.replace(self, B=B)
+
+    def variant(self, **changes) -> "Workload":
+        """The same recipe with other fields (e.g. a smaller V for quick checks)."""
+        return dataclasses.replace(self, **changes)
 
 
 WORKLOADS = {
