@@ -1,0 +1,367 @@
+"""Benchmark of the speculative-decoding verification step on GB300.
+
+python bench.py [--gpus N --steps K --warmup W] [--workload mixed] [--impl ours|reference]
+
+One step = one spec_verify call over one batch of the workload (all rows of
+the verification: row statistics, acceptance scan, residual or extra-token
+draw, outputs). The default workload is the mixed batch (B=256, gamma=8,
+V=128256, bf16, T in {0, 0.3, 0.7, 1}): every part of the path runs in it at
+full form. Inputs (1.57 GB of logits) are larger than the 129 MB L2, so
+consecutive steps re-read them from HBM.
+
+value: verified rows/s = steps * B * (gamma+1) / time, the whole job (all
+ranks; each rank verifies its own batch: weak scaling), timed on the device
+with CUDA events, max over ranks. e2e: the same metric through
+spec_verify_host (host buffers; copies inside the timed region).
+roofline: algorithmic bytes per call / average call duration, against the
+measured HBM copy bandwidth. cpu_baseline / --impl reference: the CPU oracle
+(test infrastructure) timed on this host's cores on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "spec-verify rows/s and achieved HBM GB/s vs ~8 TB/s peak, B×(γ+1)×V"
+UNIT = "rows/s"
+PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["speculative_decoding_verification_06_gb300/csrc"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixed",
+                    help="tiny | greedy | sampling | mixed | large (default: mixed)")
+    ap.add_argument("--path", choices=["auto", "rowwise", "streaming"], default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peak_hbm():
+    try:
+        with open(PEAKS) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for d in KERNEL_SOURCES:
+        base = os.path.join(ROOT, d)
+        for name in sorted(os.listdir(base)):
+            with open(os.path.join(base, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def algorithmic_bytes(batch, num_accepted) -> int:
+    """Logit bytes the method must read once, plus the re-read of the rows the
+    draw needs, plus the small inputs and outputs: s*V*[B(g+1) + g*B_samp +
+    sum over sampled requests (2 if n < g else 1)] + B*g*8 + B*12 + B*(g+1)*4."""
+    w = batch.workload
+    s, V, G, B = w.elem_bytes, w.V, w.gamma, batch.B
+    samp = (batch.temperature > 0) & (num_accepted >= 0)
+    reread = np.where(num_accepted[samp] < G, 2, 1).sum()
+    rows = B * (G + 1) + G * int(samp.sum()) + int(reread)
+    return int(s * V * rows + B * G * 8 + B * 12 + B * (G + 1) * 4)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(batch, seconds: float, rows_per_request: int):
+    """The oracle as it stands, one host thread, over whole passes of the
+    batch (or a prefix of it) until about ``seconds`` of CPU time."""
+    import oracle
+    lib = oracle.load()
+    t0 = time.perf_counter()
+    oracle.verify(*batch.slice(0, 1).arrays(), lib=lib)
+    one = max(time.perf_counter() - t0, 1e-6)
+    n_req = int(min(batch.B, max(1, seconds / one)))
+    sample = batch.slice(0, n_req)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify(*sample.arrays(), lib=lib)
+        done += n_req
+        el = time.perf_counter() - t0
+        if el >= seconds or done >= 3 * batch.B:
+            break
+    return {"value": done * rows_per_request / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"requests 0..{n_req - 1} of the same batch, {done // n_req} pass(es), "
+                      f"{el:.1f} s single-threaded fp64 C"}
+
+
+def run_reference(args, w, rank, world):
+    """--impl reference: the CPU oracle on the host cores, bounded sample per step."""
+    from workloads import synthetic
+    if rank != 0:
+        return
+    batch = synthetic.generate(w, k=0)
+    rows = w.gamma + 1
+    import oracle
+    lib = oracle.load()
+    t0 = time.perf_counter()
+    oracle.verify(*batch.slice(0, 1).arrays(), lib=lib)
+    one = max(time.perf_counter() - t0, 1e-6)
+    per_step_s = max(0.2, min(2.0, 60.0 / max(1, args.steps + args.warmup)))
+    n_req = int(min(batch.B, max(1, per_step_s / one)))
+    sample = batch.slice(0, n_req)
+    for _ in range(args.warmup):
+        oracle.verify(*sample.arrays(), lib=lib)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify(*sample.arrays(), lib=lib)
+    el = time.perf_counter() - t0
+    value = args.steps * n_req * rows / el
+    desc = f"requests 0..{n_req - 1} of the {w.name} batch per step, single-threaded fp64 C oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.description, "B": w.B, "gamma": w.gamma, "V": w.V,
+                   "logits": w.dtype, "sample_requests": n_req},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    from workloads import synthetic
+    w = synthetic.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import torch
+    import speculative_decoding_verification_06_gb300 as sv
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    sv.build.build()
+    sv.load()
+
+    batch = synthetic.generate(w, k=rank)
+    dev = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in batch.arrays()]
+    B, G, V = batch.B, w.gamma, w.V
+    dt = sv.SV_F32 if w.dtype == "f32" else sv.SV_BF16
+    path = {"auto": sv.SV_PATH_AUTO, "rowwise": sv.SV_PATH_ROWWISE,
+            "streaming": sv.SV_PATH_STREAMING}[args.path]
+    out_tokens = torch.empty((B, G + 1), dtype=torch.int32, device="cuda")
+    out_n = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(16, sv.workspace_size(B, G, V, dt)), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        sv.spec_verify(*dev, out_tokens=out_tokens, out_num_accepted=out_n, workspace=ws,
+                       stream=stream, path=path)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    launches_per_call = sv.last_launch_count()
+    num_acc = out_n.cpu().numpy()
+
+    # ---- timed region (device events on the launching stream)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for i in range(K):
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    per_call_ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
+    if dist:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    rows_per_step = B * (G + 1)
+    value = world * K * rows_per_step / (total_ms * 1e-3)
+
+    abytes = algorithmic_bytes(batch, num_acc)
+    peak, peak_src = peak_hbm()
+    avg_call_s = float(per_call_ms.mean()) * 1e-3
+    achieved = abytes / avg_call_s / 1e9
+    traffic = None
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            prof = json.load(f)
+        entry = prof.get(args.workload)
+        if entry and entry.get("kernel_hash") == kernel_hash():
+            traffic = entry.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in batch.arrays()]
+        h_out = torch.empty((B, G + 1), dtype=torch.int32).pin_memory()
+        h_n = torch.empty((B,), dtype=torch.int32).pin_memory()
+        staging = torch.empty(sv.host_staging_size(B, G, V, dt), dtype=torch.uint8, device="cuda")
+        for _ in range(2):
+            sv.spec_verify_host(*host, h_out, h_n, staging, stream=stream)
+        torch.cuda.synchronize()
+        KE = max(1, args.e2e_steps)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(KE):
+            sv.spec_verify_host(*host, h_out, h_n, staging, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if dist:
+            tt = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        es = w.elem_bytes
+        samp = int((batch.temperature > 0).sum())
+        h2d = B * (G + 1) * V * es + samp * G * V * es + B * G * 8 + B * 8
+        d2h = B * (G + 1) * 4 + B * 4
+        assert np.array_equal(h_n.numpy(), num_acc), "host entry disagrees with device entry"
+        e2e = {"value": world * KE * rows_per_step / (e2e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": KE}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(batch, args.cpu_seconds, G + 1)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    samp_mask = (batch.temperature > 0) & (num_acc >= 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.description, "B": B, "gamma": G, "V": V, "logits": w.dtype,
+                   "seeds": f"1000*{w.config}+rank", "path": args.path,
+                   "l2": f"inputs {(batch.target.nbytes + batch.draft.nbytes) / 1e9:.2f} GB > 129 MB L2; "
+                         "no flush between steps",
+                   "parallelism": f"replicas: {world} independent batches"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_call": abytes,
+                     "avg_call_us": avg_call_s * 1e6,
+                     "p10_p50_p90_call_us": [float(np.percentile(per_call_ms, q)) * 1e3 for q in (10, 50, 90)]},
+        "gpu_launches": int(K * launches_per_call),
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "requests_per_s": world * K * B / (total_ms * 1e-3),
+        "mean_accepted": float(num_acc[num_acc >= 0].mean()),
+        "acceptance_rate_sampled": float(num_acc[samp_mask].mean() / G) if samp_mask.any() else None,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

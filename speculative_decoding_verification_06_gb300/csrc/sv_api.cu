@@ -128,17 +128,20 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     a.d_status = d_status;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int grid = streaming_default_grid(dev);
+    if (opts && opts->grid_ctas > 0) grid = std::min(grid, opts->grid_ctas);
+    const bool stream_ok = streaming_applicable(a) && streaming_grid_ok(B, grid);
     bool use_stream = false;
     if (path == SV_PATH_STREAMING) {
-        if (!streaming_applicable(a)) return SV_ERR_INVALID_ARG;
+        if (!stream_ok) return SV_ERR_INVALID_ARG;
         use_stream = true;
     } else if (path == SV_PATH_AUTO) {
-        use_stream = streaming_applicable(a);
+        // below about 64 KB of target logits one block per request is quicker
+        const size_t target_bytes = static_cast<size_t>(B) * (gamma + 1) * V * elem_bytes(dtype);
+        use_stream = stream_ok && target_bytes >= (64u << 10);
     }
     cudaError_t err;
     if (use_stream) {
-        int grid = streaming_default_grid(dev);
-        if (opts && opts->grid_ctas > 0) grid = std::min(grid, opts->grid_ctas);
         const size_t need = streaming_workspace_bytes(B, gamma, V, dtype, grid);
         if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
             return SV_ERR_WORKSPACE;

@@ -41,6 +41,7 @@ cudaError_t launch_rowwise(const Args& a, const DeviceInfo& dev, cudaStream_t st
 
 // Streaming path: persistent grid. Workspace layout and launch.
 bool streaming_applicable(const Args& a);
+bool streaming_grid_ok(int B, int grid);
 size_t streaming_workspace_bytes(int B, int gamma, int V, int dtype, int grid);
 int streaming_default_grid(const DeviceInfo& dev);
 cudaError_t launch_streaming(const Args& a, const DeviceInfo& dev, int grid, void* workspace,

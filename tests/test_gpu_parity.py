@@ -27,6 +27,7 @@ def built():
 
 ROWWISE = dict(path=sv.SV_PATH_ROWWISE)
 AUTO = dict(path=sv.SV_PATH_AUTO)
+STREAM = dict(path=sv.SV_PATH_STREAMING)
 
 
 def _small(config, **changes):
@@ -54,6 +55,31 @@ def test_small_cases(name, w, opts):
         assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
 
 
+# Streaming path on aligned rows (V * element size a multiple of 16 bytes),
+# with grids of 1, 3 and 7 blocks as well as the full grid, so that rows split
+# over several blocks at every kind of boundary, stages end mid-row and slices
+# end mid-stage.
+STREAM_CASES = [
+    ("mixed_V4096_bf16", _small(4, B=6, V=4096)),
+    ("mixed_V8200_bf16", _small(4, B=5, gamma=3, V=8200)),
+    ("sampling_V3000_f32", _small(3, B=7, gamma=2, V=3000, hot_tokens=5)),
+    ("sampling_V20004_f32", _small(3, B=3, gamma=3, V=20004, hot_tokens=5)),
+    ("large_V8_bf16", _small(5, B=40, gamma=5, V=8, zipf_s=0.0)),
+    ("large_gamma16_V776", _small(4, B=4, gamma=16, V=776)),
+    ("greedy_V32000", _small(2, B=3)),
+    ("mixed_V40000_B64", _small(4, B=64, V=40000)),
+]
+
+
+@pytest.mark.parametrize("name,w", STREAM_CASES, ids=[c[0] for c in STREAM_CASES])
+@pytest.mark.parametrize("grid", [0, 1, 3, 7])
+def test_streaming_small_cases(name, w, grid):
+    for k in range(2):
+        batch = synthetic.generate(w, k=k)
+        rep = parity.check(batch, path=sv.SV_PATH_STREAMING, grid_ctas=grid)
+        assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
+
+
 @pytest.mark.parametrize("config", [1, 2, 3, 4, 5])
 def test_full_configs(config):
     batch = synthetic.generate(config)
@@ -71,7 +97,7 @@ def test_full_config_rowwise_cross_check():
     near ties, where both must match the oracle)."""
     batch = synthetic.generate(4)
     ora, det = parity.run_oracle(batch)
-    for opts in (ROWWISE, AUTO):
+    for opts in (ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=37)):
         parity.compare(batch, parity.run_gpu(batch, **opts), ora, det)
 
 
@@ -106,7 +132,7 @@ def test_invalid_requests():
     lt[11, 1, :300] = -np.inf
     w = synthetic.WORKLOADS[3].variant(B=B, gamma=G, V=V)
     batch = synthetic.Batch(w, 0, lt, ld, x, ua, us, T)
-    for opts in (ROWWISE, AUTO):
+    for opts in (ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=5)):
         gpu = parity.run_gpu(batch, **opts)
         ora, det = parity.run_oracle(batch)
         rep = parity.compare(batch, gpu, ora, det)
