@@ -75,6 +75,8 @@ typedef int32_t sv_status;
 #define SV_ERR_WORKSPACE 4   /* workspace NULL or smaller than the size query says */
 #define SV_ERR_TIMEOUT 5     /* reserved for host-side waits; kernels report timeouts
                                 through the device status word */
+#define SV_ERR_SCRATCH_LIMIT 6 /* spec_verify_noalloc: the shape needs more scratch than
+                                  SV_NOALLOC_SCRATCH_BYTES */
 
 /* Bits of the optional device status word (int32), OR-ed in by the kernels. */
 #define SV_STATUS_BAD_REQUEST 0x1 /* at least one request was invalid (-1) */
@@ -172,6 +174,32 @@ sv_status spec_verify_host(const void* target_logits, const void* draft_logits, 
                            const float* temperature, int32_t* out_tokens,
                            int32_t* out_num_accepted, void* staging, size_t staging_bytes,
                            sv_stream_t stream);
+
+/* Size of the static scratch of spec_verify_noalloc: 8 MiB of device memory,
+ * held on every GPU that loads this library until the process exits. */
+#define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* spec_verify without a workspace argument, for callers that cannot allocate
+ * device memory: a plugin that a host runtime gives only its input and output
+ * tensors, or a serving loop whose device memory is fixed at start-up and that
+ * must not call cudaMalloc on its hot path (cudaMalloc may synchronize the
+ * device). The pages describe no such entry point; it has no counterpart
+ * there. Arguments and results are those of spec_verify; it always runs the
+ * streaming path, so V * element size must be a multiple of 16 bytes, the
+ * logit pointers 16-byte aligned and B at most 4096 (else SV_ERR_INVALID_ARG).
+ * Its scratch is a static device array of SV_NOALLOC_SCRATCH_BYTES inside the
+ * library; a shape that needs more returns SV_ERR_SCRATCH_LIMIT before
+ * anything is enqueued. Nothing is allocated: no cudaMalloc, no cudaFree.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. All calls in the process share the one array,
+ * which keeps the previous call's contents (the call clears the part that
+ * must start at zero itself): two calls that overlap on the GPU, on any
+ * streams, race on it and give undefined results. */
+sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                              int B, int gamma, int V, const int32_t* draft_tokens,
+                              const float* u_accept, const float* u_sample, const float* temperature,
+                              int32_t* out_tokens, int32_t* out_num_accepted, sv_stream_t stream);
 
 /* Number of kernel launches the last successful spec_verify* call on this
  * host thread enqueued (memsets and copies not counted). */

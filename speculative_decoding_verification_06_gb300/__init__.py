@@ -19,6 +19,8 @@ LIB_PATH = _build.LIB_PATH
 
 SV_F32, SV_BF16 = 0, 1
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_WORKSPACE, SV_ERR_TIMEOUT = range(6)
+SV_ERR_SCRATCH_LIMIT = 6
+SV_NOALLOC_SCRATCH_BYTES = 8 << 20
 SV_STATUS_BAD_REQUEST, SV_STATUS_TIMEOUT = 0x1, 0x2
 SV_MAX_GAMMA, SV_MAX_V = 64, 1 << 24
 SV_PATH_AUTO, SV_PATH_ROWWISE, SV_PATH_STREAMING = 0, 1, 2
@@ -27,7 +29,7 @@ KIND_INVALID, KIND_GREEDY, KIND_RESIDUAL, KIND_BONUS = -1, 0, 1, 2
 EXPORTED = (
     "spec_verify_workspace_size", "spec_verify", "spec_verify_ex",
     "spec_verify_host_staging_size", "spec_verify_host", "spec_verify_last_launch_count",
-    "spec_verify_status_string", "spec_verify_version",
+    "spec_verify_status_string", "spec_verify_version", "spec_verify_noalloc",
 )
 
 
@@ -61,8 +63,9 @@ def _declare(lib):
     lib.spec_verify_ex.argtypes = common + [vp, sz, vp, ctypes.POINTER(_Debug), vp,
                                             ctypes.POINTER(_Options)]
     lib.spec_verify_host.argtypes = common + [vp, sz, vp]
+    lib.spec_verify_noalloc.argtypes = common + [vp]
     for name in ("spec_verify_workspace_size", "spec_verify_host_staging_size", "spec_verify",
-                 "spec_verify_ex", "spec_verify_host"):
+                 "spec_verify_ex", "spec_verify_host", "spec_verify_noalloc"):
         getattr(lib, name).restype = i32
     lib.spec_verify_status_string.argtypes = [i32]
     lib.spec_verify_status_string.restype = ctypes.c_char_p
@@ -219,3 +222,24 @@ def spec_verify_host(target_logits, draft_logits, draft_tokens, u_accept, u_samp
         _ptr(out_num_accepted), _ptr(staging), staging.numel() * staging.element_size(),
         _stream_handle(stream))
     _check(rc, "spec_verify_host")
+
+
+def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature,
+                        out_tokens, out_num_accepted, stream=None) -> None:
+    """``spec_verify_noalloc``: the verification with the library's own static
+    scratch, for callers that cannot allocate device memory. Every argument is
+    a contiguous CUDA tensor the caller already owns (outputs included); this
+    wrapper allocates nothing either. Calls that overlap on the GPU share the
+    scratch and must not overlap."""
+    lib = load()
+    B, G1, V = target_logits.shape
+    dt = _dtype_code(target_logits)
+    for t in (target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature,
+              out_tokens, out_num_accepted):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("every argument must be a contiguous CUDA tensor")
+    rc = lib.spec_verify_noalloc(
+        _ptr(target_logits), _ptr(draft_logits), dt, B, G1 - 1, V, _ptr(draft_tokens),
+        _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
+        _ptr(out_num_accepted), _stream_handle(stream))
+    _check(rc, "spec_verify_noalloc")

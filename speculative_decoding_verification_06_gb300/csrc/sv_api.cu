@@ -33,6 +33,8 @@ size_t workspace_need(int B, int gamma, int V, sv_dtype dtype, const DeviceInfo&
 
 }  // namespace
 
+void set_last_launch_count(int n) { g_last_launches = n; }
+
 bool current_device(DeviceInfo* info) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -78,6 +80,7 @@ const char* spec_verify_status_string(sv_status s) {
         case SV_ERR_CUDA: return "a CUDA call failed while enqueueing";
         case SV_ERR_WORKSPACE: return "workspace missing or smaller than spec_verify_workspace_size()";
         case SV_ERR_TIMEOUT: return "a bounded wait ran out";
+        case SV_ERR_SCRATCH_LIMIT: return "shape needs more scratch than spec_verify_noalloc holds (SV_NOALLOC_SCRATCH_BYTES)";
         default: return "unknown status";
     }
 }

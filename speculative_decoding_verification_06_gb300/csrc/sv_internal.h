@@ -33,6 +33,9 @@ struct DeviceInfo {
     size_t smem_optin = 0;
 };
 
+// Sets what spec_verify_last_launch_count() reports on this host thread.
+void set_last_launch_count(int n);
+
 // Cached properties of the current device; false when there is none.
 bool current_device(DeviceInfo* info);
 

@@ -1,0 +1,98 @@
+// spec_verify_noalloc: the streaming path with its scratch memory in a
+// static device array of this library instead of a caller-owned workspace.
+//
+// For callers that cannot allocate device memory themselves: a plugin that
+// another runtime hands only its input and output tensors, or a serving loop
+// whose device memory is fixed at start-up and that must not call cudaMalloc
+// on its hot path (cudaMalloc can synchronize the device and grows the
+// process's footprint). The entry point allocates nothing: the scratch is the
+// file-scope array below, which every GPU that loads this library holds, at
+// its full size, until the process exits.
+#include <mutex>
+
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+// The scratch (grid-barrier words, partial row statistics, draw jobs, draw
+// sums). Its size is SV_NOALLOC_SCRATCH_BYTES; shapes that need more are
+// rejected with SV_ERR_SCRATCH_LIMIT.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device. In host code the
+// array's name is only a host-side handle; the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+cudaError_t scratch_address(int device, void** ptr) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_ptr[device]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[device] = p;
+    }
+    *ptr = g_scratch_ptr[device];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                                         sv_dtype dtype, int B, int gamma, int V,
+                                         const int32_t* draft_tokens, const float* u_accept,
+                                         const float* u_sample, const float* temperature,
+                                         int32_t* out_tokens, int32_t* out_num_accepted,
+                                         sv_stream_t stream) {
+    set_last_launch_count(0);
+    if (B < 0 || gamma < 1 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_V ||
+        (dtype != SV_F32 && dtype != SV_BF16))
+        return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !temperature ||
+        !out_tokens || !out_num_accepted)
+        return SV_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return SV_ERR_UNSUPPORTED;
+    if (dev.cc_major != 10 || dev.cc_minor != 3 || dev.device >= kMaxDevices) return SV_ERR_UNSUPPORTED;
+
+    Args a = {};
+    a.target = target_logits;
+    a.draft = draft_logits;
+    a.dtype = dtype;
+    a.B = B;
+    a.gamma = gamma;
+    a.V = V;
+    a.tokens = draft_tokens;
+    a.u_accept = u_accept;
+    a.u_sample = u_sample;
+    a.temperature = temperature;
+    a.out_tokens = out_tokens;
+    a.out_num_accepted = out_num_accepted;
+
+    const int grid = streaming_default_grid(dev);
+    if (!streaming_applicable(a) || !streaming_grid_ok(B, grid)) return SV_ERR_INVALID_ARG;
+    if (streaming_workspace_bytes(B, gamma, V, dtype, grid) > SV_NOALLOC_SCRATCH_BYTES)
+        return SV_ERR_SCRATCH_LIMIT;
+    void* scratch = nullptr;
+    if (scratch_address(dev.device, &scratch) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    // launch_streaming clears the barrier words at the start of the scratch
+    // (the only part that must start at zero) before it launches.
+    const cudaError_t e = launch_streaming(a, dev, grid, scratch, SV_NOALLOC_SCRATCH_BYTES,
+                                           reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    set_last_launch_count(1);
+    return SV_OK;
+}
