@@ -136,7 +136,16 @@ typedef struct {
     double* q_x;            /* [B*gamma] q_i(x_i) at the positions evaluated (T > 0) */
     double* w_total;        /* [B] total weight W of the replacement or extra draw (T > 0) */
     int32_t* kind;          /* [B] -1 invalid, 0 greedy, 1 residual draw, 2 extra-token draw */
+    uint64_t* phase_ns;     /* [SV_PHASE_SLOTS] streaming path only: global-timer stamps
+                               (ns). Slot 0 is the earliest block start and slot 1 the
+                               latest; slots 2..9 are the latest time over all blocks at
+                               which each block finished: phase 1 stream, grid barrier 1,
+                               phase 2, barrier 2, phase 3 stream, barrier 3, phase 3
+                               search, kernel. The caller fills slot 0 with UINT64_MAX and
+                               the others with 0 before the call. */
 } sv_debug_out;
+
+#define SV_PHASE_SLOTS 10
 
 typedef struct {
     int32_t path;      /* SV_PATH_* */

@@ -21,6 +21,7 @@ SV_F32, SV_BF16 = 0, 1
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_WORKSPACE, SV_ERR_TIMEOUT = range(6)
 SV_ERR_SCRATCH_LIMIT = 6
 SV_NOALLOC_SCRATCH_BYTES = 8 << 20
+SV_PHASE_SLOTS = 10
 SV_STATUS_BAD_REQUEST, SV_STATUS_TIMEOUT = 0x1, 0x2
 SV_MAX_GAMMA, SV_MAX_V = 64, 1 << 24
 SV_PATH_AUTO, SV_PATH_ROWWISE, SV_PATH_STREAMING = 0, 1, 2
@@ -42,7 +43,7 @@ class SpecVerifyError(RuntimeError):
 class _Debug(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "max_target", "lse_target", "argmax_target", "max_draft", "lse_draft", "p_x", "q_x",
-        "w_total", "kind")]
+        "w_total", "kind", "phase_ns")]
 
 
 class _Options(ctypes.Structure):
@@ -192,7 +193,9 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
                 "q_x": torch.empty((B, G), dtype=f64, device=dev),
                 "w_total": torch.empty((B,), dtype=f64, device=dev),
                 "kind": torch.empty((B,), dtype=i32, device=dev),
+                "phase_ns": torch.zeros((SV_PHASE_SLOTS,), dtype=torch.int64, device=dev),
             }
+            dbg["phase_ns"][0] = -1  # UINT64_MAX
             for k, v in dbg.items():
                 setattr(d, k, v.data_ptr())
         o = _Options(path, grid_ctas)

@@ -4,9 +4,11 @@
 //
 // Arithmetic conventions (both paths):
 //  * c = log2(e) / T, rounded once to binary32. A row's normaliser is kept as
-//    (m, s) with m the row max and s = sum_x 2^((l(x) - m) * c); the
-//    difference l - m is exact for bfloat16 inputs, so the dominant terms
-//    carry almost no exponent error.
+//    (m, s): m the row max and s = sum_x 2^(l(x) * c - mc), mc = fl(m * c)
+//    (the binary32 product). Each term is one fused multiply-add and one
+//    2^x; the rounding of mc is a common factor 2^(m*c - mc) of every term of
+//    the row, and every consumer of (m, s) recomputes mc the same way, so it
+//    cancels exactly in p(x) = 2^(l(x) c - mc) / s.
 //  * 2^x uses the special-function unit (PTX ex2.approx.ftz.f32).
 //  * The acceptance test of "Speculative Decoding : accélérer l'inférence des
 //    LLM", §Pourquoi la qualité est préservée, u < min(1, p(x)/q(x)), is
@@ -65,7 +67,7 @@ __device__ __forceinline__ float load_logit<SV_BF16>(const void* base, size_t id
 
 // ---------------------------------------------------------------- row state
 
-// Online normaliser state: s = sum 2^((l - m) c) over the logits seen so far.
+// Online normaliser state: s = sum 2^(l c - fl(m c)) over the logits seen.
 struct MaxSum {
     float m;
     float s;
@@ -73,13 +75,20 @@ struct MaxSum {
 
 __device__ __forceinline__ MaxSum maxsum_empty() { return {neg_inf(), 0.0f}; }
 
+__device__ __forceinline__ float scaled_max(float m, float c) { return __fmul_rn(m, c); }
+
+// 2^(l c - mc), the term of logit l in a row whose scaled max is mc.
+__device__ __forceinline__ float row_term(float l, float c, float mc) { return ex2(__fmaf_rn(l, c, -mc)); }
+
 // Adds one logit (the caller screens NaN and +inf).
 __device__ __forceinline__ void maxsum_add(MaxSum& st, float x, float c) {
     if (x > st.m) {
-        st.s = (st.m == neg_inf()) ? 1.0f : __fadd_rn(__fmul_rn(st.s, ex2(__fmul_rn(__fsub_rn(st.m, x), c))), 1.0f);
+        const float mc = scaled_max(x, c);
+        st.s = (st.m == neg_inf()) ? 0.0f : __fmul_rn(st.s, ex2(__fsub_rn(scaled_max(st.m, c), mc)));
         st.m = x;
+        st.s = __fadd_rn(st.s, row_term(x, c, mc));
     } else if (x != neg_inf()) {
-        st.s = __fadd_rn(st.s, ex2(__fmul_rn(__fsub_rn(x, st.m), c)));
+        st.s = __fadd_rn(st.s, row_term(x, c, scaled_max(st.m, c)));
     }
 }
 
@@ -91,7 +100,7 @@ __device__ __forceinline__ MaxSum maxsum_merge(MaxSum a, MaxSum b, float c) {
         b = t;
     }
     if (b.m == neg_inf()) return a;
-    a.s = __fadd_rn(a.s, __fmul_rn(b.s, ex2(__fmul_rn(__fsub_rn(b.m, a.m), c))));
+    a.s = __fadd_rn(a.s, __fmul_rn(b.s, ex2(__fsub_rn(scaled_max(b.m, c), scaled_max(a.m, c)))));
     return a;
 }
 
@@ -109,10 +118,10 @@ __device__ __forceinline__ ArgMax argmax_merge(ArgMax a, ArgMax b) {
 
 // ------------------------------------------------------------ decisions
 
-// p(x) = 2^((l - m) c) / s, in double.
+// p(x) = 2^(l c - fl(m c)) / s, in double.
 __device__ __forceinline__ double prob_from_stats(float l, float m, float s, float c) {
-    return exp2((static_cast<double>(l) - static_cast<double>(m)) * static_cast<double>(c)) /
-           static_cast<double>(s);
+    const double mc = static_cast<double>(scaled_max(m, c));
+    return exp2(static_cast<double>(l) * static_cast<double>(c) - mc) / static_cast<double>(s);
 }
 
 // u < alpha with alpha = min(1, p/q); alpha = 1 if q == 0 < p, 0 if p == q == 0.
@@ -121,9 +130,13 @@ __device__ __forceinline__ bool accept_draft(double p, double q, float u) {
     return static_cast<double>(u) < alpha;
 }
 
-// log sum_x exp(l(x)/T) from (m, s): m/T + ln(s), with m/T in double.
-__device__ __forceinline__ double lse_from_stats(float m, float s, float T) {
-    return static_cast<double>(m) / static_cast<double>(T) + log(static_cast<double>(s));
+// log sum_x exp(l(x)/T) from (m, s, c): s = 2^(m c - fl(m c)) sum 2^((l - m) c),
+// so the log is m/T + ln s - (m c - fl(m c)) ln 2, with m/T and m c in double.
+__device__ __forceinline__ double lse_from_stats(float m, float s, float c, float T) {
+    const double mc_exact = static_cast<double>(m) * static_cast<double>(c);
+    const double mc = static_cast<double>(scaled_max(m, c));
+    return static_cast<double>(m) / static_cast<double>(T) + log(static_cast<double>(s)) -
+           (mc_exact - mc) * 0.69314718055994530942;
 }
 
 // ------------------------------------------------------- inverse-CDF weights
@@ -144,20 +157,20 @@ constexpr double kFixTargetInv = 1.0 / 549755813888.0;
 // proportional to p at the target row (the extra token, or the fallback when
 // residual weights sum to zero).
 struct DrawParams {
-    int kind;      // kKindResidual or kKindBonus
+    int kind;       // kKindResidual or kKindBonus
     float c;
-    float mp, isp; // target row: max and 1/s
-    float mq, isq; // draft row (residual only)
-    float fix;     // fixed-point scale
+    float mcp, isp; // target row: fl(max * c) and 1/s
+    float mcq, isq; // draft row (residual only)
+    float fix;      // fixed-point scale
 };
 
 __device__ __forceinline__ float weight_target(float lt, const DrawParams& d) {
-    return ex2(__fmul_rn(__fsub_rn(lt, d.mp), d.c));
+    return row_term(lt, d.c, d.mcp);
 }
 
 __device__ __forceinline__ float weight_residual(float lt, float ld, const DrawParams& d) {
-    float p = __fmul_rn(ex2(__fmul_rn(__fsub_rn(lt, d.mp), d.c)), d.isp);
-    float q = __fmul_rn(ex2(__fmul_rn(__fsub_rn(ld, d.mq), d.c)), d.isq);
+    const float p = __fmul_rn(row_term(lt, d.c, d.mcp), d.isp);
+    const float q = __fmul_rn(row_term(ld, d.c, d.mcq), d.isq);
     return fmaxf(__fsub_rn(p, q), 0.0f);
 }
 

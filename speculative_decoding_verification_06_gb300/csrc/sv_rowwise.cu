@@ -23,7 +23,7 @@ constexpr int kWarps = kThreads / 32;
 
 struct RowStat {
     float m;      // max (T > 0) or max value (T == 0)
-    float s;      // sum 2^((l - m) c) (T > 0)
+    float s;      // sum 2^(l c - fl(m c)) (T > 0)
     int32_t idx;  // lowest-index argmax (T == 0)
     int32_t bad;  // NaN, +inf, or only -inf
 };
@@ -199,14 +199,14 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             size_t r = static_cast<size_t>(b) * (G + 1) + j;
             const RowStat& st = sh.st[j];
             if (a.dbg.max_target) a.dbg.max_target[r] = st.m;
-            if (a.dbg.lse_target) a.dbg.lse_target[r] = greedy ? nan("") : lse_from_stats(st.m, st.s, T);
+            if (a.dbg.lse_target) a.dbg.lse_target[r] = greedy ? nan("") : lse_from_stats(st.m, st.s, c, T);
             if (a.dbg.argmax_target) a.dbg.argmax_target[r] = greedy ? st.idx : -1;
         }
         for (int j = threadIdx.x; j < G; j += kThreads) {
             size_t r = static_cast<size_t>(b) * G + j;
             const RowStat& st = sh.st[G + 1 + j];
             if (a.dbg.max_draft) a.dbg.max_draft[r] = greedy ? nanf("") : st.m;
-            if (a.dbg.lse_draft) a.dbg.lse_draft[r] = greedy ? nan("") : lse_from_stats(st.m, st.s, T);
+            if (a.dbg.lse_draft) a.dbg.lse_draft[r] = greedy ? nan("") : lse_from_stats(st.m, st.s, c, T);
             if (a.dbg.p_x) a.dbg.p_x[r] = nan("");
             if (a.dbg.q_x) a.dbg.q_x[r] = nan("");
         }
@@ -247,16 +247,16 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                 }
                 DrawParams d;
                 d.c = c;
-                d.mp = sh.st[n].m;
+                d.mcp = scaled_max(sh.st[n].m, c);
                 d.isp = __double2float_rn(1.0 / static_cast<double>(sh.st[n].s));
                 if (n < G) {
                     d.kind = kKindResidual;
-                    d.mq = sh.st[G + 1 + n].m;
+                    d.mcq = scaled_max(sh.st[G + 1 + n].m, c);
                     d.isq = __double2float_rn(1.0 / static_cast<double>(sh.st[G + 1 + n].s));
                     d.fix = kFixResidual;
                 } else {
                     d.kind = kKindBonus;
-                    d.mq = 0.0f;
+                    d.mcq = 0.0f;
                     d.isq = 0.0f;
                     d.fix = kFixTarget;
                 }

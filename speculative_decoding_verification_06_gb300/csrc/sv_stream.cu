@@ -13,19 +13,20 @@
 //     is cut into G equal 16-byte-aligned slices, one per thread block. A
 //     producer warp copies its slice through a ring of kStages shared-memory
 //     stages with cp.async.bulk (completion on mbarriers); eight consumer warps
-//     fold each stage into per-thread (max, sum of 2^((l-m)c)) or argmax
-//     states. When the stream moves to a new row each warp writes its partial
-//     result for the row piece; there is no block-wide barrier in the stream.
+//     fold each stage into per-thread (max, sum of 2^(l c - fl(m c))) or argmax
+//     states. At the end of each row piece every warp writes its partial
+//     result; there is no block-wide barrier inside the stream.
 //  2. Acceptance scan. One warp per request merges the pieces of its rows in
 //     a fixed order, evaluates p(x_i) and q(x_i) in double, finds the first
 //     rejection, writes the accepted tokens and a draw job.
 //  3. Draw. The rows the draws need (target row n and draft row n for a
 //     residual, target row gamma for the extra token) are streamed again in
 //     chunks of one stage; each thread sums the weights of a run of
-//     consecutive tokens, and the runs are added into per-chunk totals as
-//     64-bit fixed-point integers (exact and order-independent). After a grid
-//     barrier one warp per job picks the chunk holding u * W, re-reads that one
-//     chunk and finds the token.
+//     consecutive tokens and each warp stores the sum of its 32 runs as a
+//     64-bit fixed-point integer (exact, so any order of addition gives the
+//     same prefix sums). After a grid barrier one warp per job finds the
+//     chunk, then the warp, then the run holding u * W, re-reads those 32
+//     runs and finds the token.
 //
 // Every wait is bounded (about two seconds, by the global timer): a barrier or
 // a stage that never completes sets SV_STATUS_TIMEOUT and the kernel returns.
@@ -44,7 +45,9 @@ constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kStages = 8;
 constexpr int kStageBytes = 16384;
 constexpr int kVecPerThread = kStageBytes / 16 / kConsumers;  // 4
-constexpr int kMapMax = 256;
+constexpr int kMapMax = 256;   // compacted requests in one block's draft slice
+constexpr int kMaxGrid = 256;  // blocks (partition tables live in shared memory)
+constexpr int kJobCache = 64;  // draw jobs cached per block in phase 3
 constexpr int kMaxB = 4096;
 constexpr int kMaxRowsPerReq = 2 * SV_MAX_GAMMA + 1;
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
@@ -55,7 +58,7 @@ constexpr int kBarHandoff = 2;    // consumers arrive, producer waits (288)
 
 struct Rec {
     float m;      // max value (both modes)
-    float s;      // sum 2^((l - m) c) (max/sum mode)
+    float s;      // sum 2^(l c - fl(m c)) (max/sum mode)
     int32_t idx;  // argmax (argmax mode)
     int32_t bad;  // NaN or +inf seen
 };
@@ -68,8 +71,8 @@ struct Job {
 // Byte offsets into the caller's workspace and the partition constants.
 struct Layout {
     long long Et;  // target elements B*(gamma+1)*V
-    int G, MT, MD, NCH, vec, chunk_elems;
-    size_t hdr, prefix, req, rec_t, rec_d, jobs, chunks, total;
+    int G, MT, MD, NCH, vec;
+    size_t hdr, prefix, rec_t, rec_d, jobs, wsums, total;
 };
 
 __host__ __device__ inline long long part_begin(long long E, int G, int g, int vec) {
@@ -77,13 +80,6 @@ __host__ __device__ inline long long part_begin(long long E, int G, int g, int v
     if (g >= G) return E;
     long long x = (E * g) / G;
     return x - x % vec;
-}
-
-__device__ inline int part_owner(long long E, int G, int vec, long long e) {
-    int g = static_cast<int>(min(static_cast<long long>(G - 1), (e * G) / E));
-    while (g + 1 < G && part_begin(E, G, g + 1, vec) <= e) ++g;
-    while (g > 0 && part_begin(E, G, g, vec) > e) --g;
-    return g;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -96,8 +92,8 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     const long long Ed_max = static_cast<long long>(B) * gamma * V;
     L.MT = static_cast<int>(((L.Et + G - 1) / G + L.vec - 1) / V + 2);
     L.MD = static_cast<int>(((Ed_max + G - 1) / G + L.vec - 1) / V + 2);
-    L.chunk_elems = kStageBytes / es;
-    L.NCH = (V + L.chunk_elems - 1) / L.chunk_elems;
+    const int chunk_elems = kStageBytes / es;
+    L.NCH = (V + chunk_elems - 1) / chunk_elems;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t at = off;
@@ -106,11 +102,10 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     };
     L.hdr = take(256);
     L.prefix = take(static_cast<size_t>(B) * 4);
-    L.req = take(static_cast<size_t>(B) * 4);
     L.rec_t = take(static_cast<size_t>(G) * L.MT * kConsumerWarps * sizeof(Rec));
     L.rec_d = take(static_cast<size_t>(G) * L.MD * kConsumerWarps * sizeof(Rec));
     L.jobs = take(static_cast<size_t>(B) * sizeof(Job));
-    L.chunks = take(static_cast<size_t>(B) * L.NCH * 8);
+    L.wsums = take(static_cast<size_t>(B) * L.NCH * kConsumerWarps * 8);
     L.total = off;
     return L;
 }
@@ -190,31 +185,6 @@ __device__ __forceinline__ float f32_max_nan(float a, float b) {
     return r;
 }
 
-// Packed pairs of binary32 (sm_100 family f32x2 arithmetic).
-__device__ __forceinline__ unsigned long long f2(float lo, float hi) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(unsigned long long v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
-    unsigned long long r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
-    unsigned long long r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
-    unsigned long long r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-
 // ---------------------------------------------------------------- barriers
 
 struct Hdr {
@@ -246,7 +216,7 @@ __device__ bool grid_sync(Hdr* h, int32_t* d_status, int* s_flag) {
                     if (d_status) atomicOr(d_status, SV_STATUS_TIMEOUT);
                     break;
                 }
-                __nanosleep(100);
+                __nanosleep(64);
             }
         }
         __threadfence();
@@ -256,13 +226,30 @@ __device__ bool grid_sync(Hdr* h, int32_t* d_status, int* s_flag) {
     return *s_flag != 0;
 }
 
+// Checking output: global-timer stamps (see sv_debug_out.phase_ns).
+__device__ __forceinline__ void stamp(unsigned long long* slots, int i) {
+    if (slots && threadIdx.x == 0) {
+        const unsigned long long now = global_ns();
+        if (i == 0) {
+            atomicMin(slots, now);
+            atomicMax(slots + 1, now);
+        } else {
+            atomicMax(slots + i, now);
+        }
+    }
+}
+
 // ------------------------------------------------------------ kernel context
 
 struct Ctl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    long long tbeg[kMaxGrid + 1];  // target partition
+    long long dbeg[kMaxGrid + 1];  // draft partition (after the prologue)
+    Job jobs[kJobCache];           // phase 3: this block's draw jobs
     int n_samp;
-    int k_lo;   // first compacted request of this block's draft slice
+    int k_lo;  // first compacted request of this block's draft slice
+    int job_lo, job_n;
     int abort;
     int flag;
     int map[kMapMax];
@@ -270,26 +257,38 @@ struct Ctl {
 };
 
 struct RowLoc {
-    int kind;        // 0 target row, 1 draft row
-    long long row;   // target row index, or compacted draft row index
-    int req;         // request b
-    int slot;        // row slot of this block
+    int kind;       // 0 target row, 1 draft row
+    long long row;  // target row index, or compacted draft row index
+    int req;        // request b
+    int slot;       // row slot of this block
 };
 
-// One stage of the phase-1 stream.
-struct Stage1 {
+// A piece of one row inside this block's slice.
+struct Segment {
     const char* src;
-    unsigned bytes;
-    int elems;
+    long long elems;
     long long e0;  // first element, offset within the row
     RowLoc loc;
 };
+
+// Largest g with beg[g] <= e (beg non-decreasing, beg[0] = 0 <= e < beg[G]).
+__device__ __forceinline__ int owner(const long long* beg, int G, long long e) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (beg[mid] <= e)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
 
 template <int DT>
 struct Kern {
     static constexpr int ES = DT == SV_F32 ? 4 : 2;
     static constexpr int kChunkElems = kStageBytes / ES;
-    static constexpr int kTPT = kChunkElems / kConsumers;  // tokens per thread run
+    static constexpr int kTPT = kChunkElems / kConsumers;  // tokens per thread run (64 bytes)
 
     const Args& a;
     const Layout& L;
@@ -300,55 +299,41 @@ struct Kern {
 
     __device__ Hdr* hdr() const { return reinterpret_cast<Hdr*>(ws + L.hdr); }
     __device__ int* prefix() const { return reinterpret_cast<int*>(ws + L.prefix); }
-    __device__ int* req() const { return reinterpret_cast<int*>(ws + L.req); }
     __device__ Rec* rec_t() const { return reinterpret_cast<Rec*>(ws + L.rec_t); }
     __device__ Rec* rec_d() const { return reinterpret_cast<Rec*>(ws + L.rec_d); }
     __device__ Job* jobs() const { return reinterpret_cast<Job*>(ws + L.jobs); }
-    __device__ unsigned long long* chunks() const {
-        return reinterpret_cast<unsigned long long*>(ws + L.chunks);
+    __device__ unsigned long long* wsums() const {
+        return reinterpret_cast<unsigned long long*>(ws + L.wsums);
     }
 
     __device__ static bool sampled(float T) { return T > 0.0f && T < pos_inf(); }
 
-    __device__ long long Ed() const {
-        return static_cast<long long>(ctl.n_samp) * a.gamma * a.V;
-    }
-
-    // ---- phase-1 stage schedule, shared by the producer and the consumers:
-    // this block's slice of the target rows, then of the compacted draft rows
-    // (the latter needs the prologue's n_samp and map).
+    // ---- phase-1 schedule: row pieces of this block's slices, in order
     template <typename F>
-    __device__ void for_each_target_stage(F&& f) const {
+    __device__ void for_each_target_segment(long long ts, long long te, F&& f) const {
         const int V = a.V, GM = a.gamma;
-        const long long ts = part_begin(L.Et, G, g, L.vec), te = part_begin(L.Et, G, g + 1, L.vec);
-        const long long first_t = ts / V;
+        const long long first = ts / V;
         for (long long e = ts; e < te;) {
             const long long r = e / V;
-            const long long seg_end = min(te, (r + 1) * V);
-            while (e < seg_end) {
-                const int n = static_cast<int>(min(seg_end - e, static_cast<long long>(kChunkElems)));
-                Stage1 st;
-                st.src = static_cast<const char*>(a.target) + e * ES;
-                st.bytes = static_cast<unsigned>(n * ES);
-                st.elems = n;
-                st.e0 = e - r * V;
-                st.loc = {0, r, static_cast<int>(r / (GM + 1)), static_cast<int>(r - first_t)};
-                f(st);
-                e += n;
-            }
+            const long long end = min(te, (r + 1) * V);
+            Segment sg;
+            sg.src = static_cast<const char*>(a.target) + e * ES;
+            sg.elems = end - e;
+            sg.e0 = e - r * V;
+            sg.loc = {0, r, static_cast<int>(r / (GM + 1)), static_cast<int>(r - first)};
+            f(sg);
+            e = end;
         }
     }
 
     template <typename F>
-    __device__ void for_each_draft_stage(F&& f) const {
+    __device__ void for_each_draft_segment(F&& f) const {
         const int V = a.V, GM = a.gamma;
-        const long long E2 = Ed();
-        if (E2 == 0) return;
-        const long long ds = part_begin(E2, G, g, L.vec), de = part_begin(E2, G, g + 1, L.vec);
-        const long long first_d = ds / V;
+        const long long ds = ctl.dbeg[g], de = ctl.dbeg[g + 1];
+        const long long first = ds / V;
         for (long long e = ds; e < de;) {
             const long long kr = e / V;
-            const long long seg_end = min(de, (kr + 1) * V);
+            const long long end = min(de, (kr + 1) * V);
             const int k = static_cast<int>(kr / GM), i = static_cast<int>(kr % GM);
             const int rel = k - ctl.k_lo;
             const int b = (rel >= 0 && rel < kMapMax) ? ctl.map[rel] : -1;
@@ -357,29 +342,27 @@ struct Kern {
                 return;
             }
             const long long base = (static_cast<long long>(b) * GM + i) * V;
-            while (e < seg_end) {
-                const int n = static_cast<int>(min(seg_end - e, static_cast<long long>(kChunkElems)));
-                Stage1 st;
-                st.src = static_cast<const char*>(a.draft) + (base + (e - kr * V)) * ES;
-                st.bytes = static_cast<unsigned>(n * ES);
-                st.elems = n;
-                st.e0 = e - kr * V;
-                st.loc = {1, kr, b, static_cast<int>(kr - first_d)};
-                f(st);
-                e += n;
-            }
+            Segment sg;
+            sg.src = static_cast<const char*>(a.draft) + (base + (e - kr * V)) * ES;
+            sg.elems = end - e;
+            sg.e0 = e - kr * V;
+            sg.loc = {1, kr, b, static_cast<int>(kr - first)};
+            f(sg);
+            e = end;
         }
     }
 
-    // ---- producer: lane 0 issues the copies of a schedule into the ring
-    struct Producer {
+    // ---- the ring: producer and consumer cursors
+    struct Cursor {
         unsigned it = 0;
     };
 
-    __device__ bool produce(Producer& p, const char* src, unsigned bytes) const {
+    // Producer warp: issue one copy into the next stage (lane 0 issues).
+    __device__ bool produce(Cursor& p, const char* src, unsigned bytes) const {
         const int slot = p.it % kStages;
         const unsigned round = p.it / kStages;
-        if (round > 0 && !mbar_wait(&ctl.empty[slot], (round - 1) & 1)) return false;
+        // the verdict is made warp-uniform so that a timeout cannot split the warp
+        if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(&ctl.empty[slot], (round - 1) & 1))) return false;
         if ((threadIdx.x & 31) == 0) {
             mbar_expect_tx(&ctl.full[slot], bytes);
             bulk_copy(stages + static_cast<size_t>(slot) * kStageBytes, src, bytes, &ctl.full[slot]);
@@ -390,22 +373,18 @@ struct Kern {
     }
 
     // Waits (bounded) until every copy the producer issued has landed.
-    __device__ void drain(const Producer& p) const {
+    __device__ void drain(const Cursor& p) const {
         const unsigned n = p.it;
         for (unsigned j = (n > kStages ? n - kStages : 0); j < n; ++j)
             mbar_wait(&ctl.full[j % kStages], (j / kStages) & 1);
     }
 
-    struct Consumer {
-        unsigned it = 0;
-    };
-
-    __device__ const char* consume_begin(Consumer& c) const {
+    __device__ const char* consume_begin(Cursor& c) const {
         const int slot = c.it % kStages;
-        if (!mbar_wait(&ctl.full[slot], (c.it / kStages) & 1)) return nullptr;
+        if (!__all_sync(0xffffffffu, mbar_wait(&ctl.full[slot], (c.it / kStages) & 1))) return nullptr;
         return stages + static_cast<size_t>(slot) * kStageBytes;
     }
-    __device__ void consume_end(Consumer& c) const {
+    __device__ void consume_end(Cursor& c) const {
         __syncwarp();
         if ((threadIdx.x & 31) == 0) mbar_arrive(&ctl.empty[c.it % kStages]);
         ++c.it;
@@ -417,25 +396,29 @@ struct Kern {
         if (d_status) atomicOr(d_status, SV_STATUS_TIMEOUT);
     }
 
-    // ---- phase-1 prologue (consumers): count the T > 0 requests, map this
-    // block's draft slice to requests; block 0 publishes the compaction.
+    // ---- phase-1 prologue (consumers): partition tables, the count of T > 0
+    // requests, the map of this block's draft slice to requests; block 0
+    // publishes the compaction.
     __device__ void prologue() const {
         const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+        for (int gg = t; gg <= G; gg += kConsumers) ctl.tbeg[gg] = part_begin(L.Et, G, gg, L.vec);
         int cnt = 0;
         for (int b = t; b < a.B; b += kConsumers) cnt += sampled(a.temperature[b]) ? 1 : 0;
         cnt = __reduce_add_sync(0xffffffffu, cnt);
         if (lane == 0) ctl.wtmp[warp] = cnt;
         bar_sync(kBarConsumers, kConsumers);
+        int n = 0;
+        for (int w = 0; w < kConsumerWarps; ++w) n += ctl.wtmp[w];
+        const long long E2 = static_cast<long long>(n) * a.gamma * a.V;
+        for (int gg = t; gg <= G; gg += kConsumers) ctl.dbeg[gg] = part_begin(E2, G, gg, L.vec);
+        const int k_lo = n > 0 ? static_cast<int>(part_begin(E2, G, g, L.vec) /
+                                                  (static_cast<long long>(a.gamma) * a.V))
+                               : 0;
         if (t == 0) {
-            int n = 0;
-            for (int w = 0; w < kConsumerWarps; ++w) n += ctl.wtmp[w];
             ctl.n_samp = n;
-            const long long E2 = static_cast<long long>(n) * a.gamma * a.V;
-            const long long ds = part_begin(E2, G, g, L.vec);
-            ctl.k_lo = n > 0 ? static_cast<int>(ds / (static_cast<long long>(a.gamma) * a.V)) : 0;
+            ctl.k_lo = k_lo;
         }
         bar_sync(kBarConsumers, kConsumers);
-        const int k_lo = ctl.k_lo;
         int carry = 0;
         for (int base = 0; base < a.B; base += kConsumers) {
             const int b = base + t;
@@ -444,16 +427,16 @@ struct Kern {
             const int in_warp = __popc(ball & ((1u << lane) - 1u));
             if (lane == 0) ctl.wtmp[warp] = __popc(ball);
             bar_sync(kBarConsumers, kConsumers);
-            int before = carry;
-            for (int w = 0; w < warp; ++w) before += ctl.wtmp[w];
-            int total = 0;
-            for (int w = 0; w < kConsumerWarps; ++w) total += ctl.wtmp[w];
+            int before = carry, total = 0;
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                if (w < warp) before += ctl.wtmp[w];
+                total += ctl.wtmp[w];
+            }
             const int k = before + in_warp;
             if (b < a.B) {
                 if (f) {
                     const int rel = k - k_lo;
                     if (rel >= 0 && rel < kMapMax) ctl.map[rel] = b;
-                    if (g == 0) req()[k] = b;
                 }
                 if (g == 0) prefix()[b] = f ? k : -1;
             }
@@ -462,20 +445,28 @@ struct Kern {
         }
     }
 
-    // ---- phase-1 consumer: fold stages into per-thread row states
+    // ---- phase-1 consumer: per-thread state of the current row piece
     struct RowState {
-        float m, s;    // max/sum mode
-        int idx;       // argmax mode
+        float m, mc, s;  // max/sum mode (mc = fl(m c))
+        int idx;         // argmax mode
         int bad;
-        bool argmax;   // mode of the current row
+        bool argmax;
         float c;
-        long long key; // kind * 2^62 + row, -1 = none
-        RowLoc loc;
     };
 
-    __device__ void flush_row(RowState& rs) const {
-        if (rs.key < 0) return;
-        int bad = __any_sync(0xffffffffu, rs.bad);
+    __device__ void start_row(RowState& rs, const RowLoc& loc) const {
+        const float T = a.temperature[loc.req];
+        rs.argmax = loc.kind == 0 && !sampled(T);
+        rs.c = rs.argmax ? 0.0f : temp_scale(T);
+        rs.m = neg_inf();
+        rs.mc = neg_inf();
+        rs.s = 0.0f;
+        rs.idx = 0x7fffffff;
+        rs.bad = 0;
+    }
+
+    __device__ void flush_row(const RowState& rs, const RowLoc& loc) const {
+        const int bad = __any_sync(0xffffffffu, rs.bad);
         Rec rec;
         if (rs.argmax) {
             ArgMax st{rs.m, rs.idx};
@@ -496,40 +487,27 @@ struct Kern {
         }
         if ((threadIdx.x & 31) == 0) {
             const int warp = threadIdx.x >> 5;
-            Rec* dst = rs.loc.kind == 0 ? rec_t() + ((static_cast<size_t>(g) * L.MT + rs.loc.slot) * kConsumerWarps + warp)
-                                        : rec_d() + ((static_cast<size_t>(g) * L.MD + rs.loc.slot) * kConsumerWarps + warp);
+            Rec* dst = loc.kind == 0
+                           ? rec_t() + ((static_cast<size_t>(g) * L.MT + loc.slot) * kConsumerWarps + warp)
+                           : rec_d() + ((static_cast<size_t>(g) * L.MD + loc.slot) * kConsumerWarps + warp);
             *dst = rec;
         }
     }
 
-    __device__ void start_row(RowState& rs, const RowLoc& loc) const {
-        rs.loc = loc;
-        rs.key = (static_cast<long long>(loc.kind) << 62) + loc.row;
-        const float T = a.temperature[loc.req];
-        rs.argmax = loc.kind == 0 && !sampled(T);
-        rs.c = rs.argmax ? 0.0f : temp_scale(T);
-        rs.m = neg_inf();
-        rs.s = 0.0f;
-        rs.idx = 0x7fffffff;
-        rs.bad = 0;
-    }
-
-    __device__ void fold_stage(RowState& rs, const char* sm, const Stage1& st) const {
+    // Folds one stage (nvec 16-byte vectors, element offset e0 in the row).
+    __device__ void fold_stage(RowState& rs, const char* sm, int nvec, long long e0) const {
         const int t = threadIdx.x;
-        const int nvec = static_cast<int>(st.bytes / 16);
         uint4 v[kVecPerThread];
 #pragma unroll
         for (int k = 0; k < kVecPerThread; ++k) {
             const int vi = t + k * kConsumers;
-            if (vi < nvec) {
+            if (vi < nvec)
                 v[k] = *reinterpret_cast<const uint4*>(sm + static_cast<size_t>(vi) * 16);
-            } else if (DT == SV_BF16) {
+            else if (DT == SV_BF16)
                 v[k] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-            } else {
+            else
                 v[k] = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
-            }
         }
-        // tile max, NaN-propagating
         float tmax;
         if (DT == SV_BF16) {
             uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(v[0].x, v[0].y), bf16x2_max_nan(v[0].z, v[0].w));
@@ -555,79 +533,77 @@ struct Kern {
                 // first position of tmax among this thread's elements (increasing index)
                 int found = -1;
 #pragma unroll
-                for (int k = 0; k < kVecPerThread; ++k) {
+                for (int k = kVecPerThread - 1; k >= 0; --k) {
                     const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 3; q >= 0; --q) {
                         if (DT == SV_BF16) {
-                            if (found < 0 && bf16x2_lo(w4[q]) == tmax) found = (t + k * kConsumers) * 8 + 2 * q;
-                            if (found < 0 && bf16x2_hi(w4[q]) == tmax) found = (t + k * kConsumers) * 8 + 2 * q + 1;
+                            if (bf16x2_hi(w4[q]) == tmax) found = (t + k * kConsumers) * 8 + 2 * q + 1;
+                            if (bf16x2_lo(w4[q]) == tmax) found = (t + k * kConsumers) * 8 + 2 * q;
                         } else {
-                            if (found < 0 && __uint_as_float(w4[q]) == tmax) found = (t + k * kConsumers) * 4 + q;
+                            if (__uint_as_float(w4[q]) == tmax) found = (t + k * kConsumers) * 4 + q;
                         }
                     }
                 }
                 rs.m = tmax;
-                rs.idx = static_cast<int>(st.e0) + found;
+                rs.idx = static_cast<int>(e0) + found;
             }
             return;
         }
         const float c = rs.c;
         if (tmax > rs.m) {
-            rs.s = (rs.m == neg_inf()) ? 0.0f : __fmul_rn(rs.s, ex2(__fmul_rn(__fsub_rn(rs.m, tmax), c)));
+            const float mc = scaled_max(tmax, c);
+            rs.s = (rs.m == neg_inf()) ? 0.0f : __fmul_rn(rs.s, ex2(__fsub_rn(rs.mc, mc)));
             rs.m = tmax;
+            rs.mc = mc;
         }
-        const unsigned long long mm = f2(rs.m, rs.m), cc = f2(c, c);
-        unsigned long long acc = f2(0.0f, 0.0f);
+        const float nmc = -rs.mc;
+        float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
         for (int k = 0; k < kVecPerThread; ++k) {
             const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
             if (DT == SV_BF16) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const unsigned long long d = f2_mul(f2_sub(f2(bf16x2_lo(w4[q]), bf16x2_hi(w4[q])), mm), cc);
-                    float d0, d1;
-                    f2_unpack(d, d0, d1);
-                    acc = f2_add(acc, f2(ex2(d0), ex2(d1)));
+                    acc0 = __fadd_rn(acc0, ex2(__fmaf_rn(bf16x2_lo(w4[q]), c, nmc)));
+                    acc1 = __fadd_rn(acc1, ex2(__fmaf_rn(bf16x2_hi(w4[q]), c, nmc)));
                 }
             } else {
 #pragma unroll
                 for (int q = 0; q < 4; q += 2) {
-                    const unsigned long long d =
-                        f2_mul(f2_sub(f2(__uint_as_float(w4[q]), __uint_as_float(w4[q + 1])), mm), cc);
-                    float d0, d1;
-                    f2_unpack(d, d0, d1);
-                    acc = f2_add(acc, f2(ex2(d0), ex2(d1)));
+                    acc0 = __fadd_rn(acc0, ex2(__fmaf_rn(__uint_as_float(w4[q]), c, nmc)));
+                    acc1 = __fadd_rn(acc1, ex2(__fmaf_rn(__uint_as_float(w4[q + 1]), c, nmc)));
                 }
             }
         }
-        float a0, a1;
-        f2_unpack(acc, a0, a1);
-        rs.s = __fadd_rn(rs.s, __fadd_rn(a0, a1));
+        rs.s = __fadd_rn(rs.s, __fadd_rn(acc0, acc1));
     }
 
-    // ---- phase 2: merge of a row's pieces
+    // ---- phase 2: merge of a row's pieces, in block and warp order
     __device__ Rec merge_row(int kind, long long row, bool argmax, float c) const {
-        const long long E = kind == 0 ? L.Et : Ed();
+        const long long* beg = kind == 0 ? ctl.tbeg : ctl.dbeg;
         const int MM = kind == 0 ? L.MT : L.MD;
         const Rec* base = kind == 0 ? rec_t() : rec_d();
         const long long e0 = row * a.V, e1 = e0 + a.V - 1;
-        const int g0 = part_owner(E, G, L.vec, e0), g1 = part_owner(E, G, L.vec, e1);
+        const int g0 = owner(beg, G, e0), g1 = owner(beg, G, e1);
         MaxSum ms = maxsum_empty();
         ArgMax am = argmax_empty();
         int bad = 0;
         for (int gg = g0; gg <= g1; ++gg) {
-            const long long b0 = part_begin(E, G, gg, L.vec), b1 = part_begin(E, G, gg + 1, L.vec);
+            const long long b0 = beg[gg], b1 = beg[gg + 1];
             if (b1 <= b0) continue;
             const int slot = static_cast<int>(row - b0 / a.V);
-            const Rec* r = base + (static_cast<size_t>(gg) * MM + slot) * kConsumerWarps;
+            const uint4* r =
+                reinterpret_cast<const uint4*>(base + (static_cast<size_t>(gg) * MM + slot) * kConsumerWarps);
+#pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
-                const Rec x = r[w];
-                bad |= x.bad;
+                const uint4 x = __ldcg(r + w);
+                const float m = __uint_as_float(x.x), s = __uint_as_float(x.y);
+                bad |= static_cast<int>(x.w);
                 if (argmax)
-                    am = argmax_merge(am, ArgMax{x.m, x.idx});
+                    am = argmax_merge(am, ArgMax{m, static_cast<int32_t>(x.z)});
                 else
-                    ms = maxsum_merge(ms, MaxSum{x.m, x.s}, c);
+                    ms = maxsum_merge(ms, MaxSum{m, s}, c);
             }
         }
         Rec out;
@@ -646,9 +622,23 @@ struct Kern {
         const bool greedy = t_ok && T == 0.0f;
         const bool samp = sampled(T);
         const float c = samp ? temp_scale(T) : 0.0f;
-        const int k = prefix()[b];
+        const int k = __ldcg(prefix() + b);
         const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
         int bad = t_ok ? 0 : 1;
+        // this lane's first position (gamma <= 32 in one pass): its token, the two
+        // gathered logits and the uniform are loaded before the row merges
+        int x0 = 0;
+        float lt0 = 0.0f, ld0 = 0.0f, u0 = 0.0f;
+        if (lane < GM) {
+            x0 = tok[lane];
+            if (!greedy && x0 >= 0 && x0 < V) {
+                const size_t tr = static_cast<size_t>(b) * (GM + 1) + lane;
+                const size_t dr = static_cast<size_t>(b) * GM + lane;
+                lt0 = load_logit<DT>(a.target, tr * V + x0);
+                ld0 = load_logit<DT>(a.draft, dr * V + x0);
+                u0 = a.u_accept[dr];
+            }
+        }
         for (int i = lane; i < GM; i += 32) {
             const int x = tok[i];
             if (x < 0 || x >= V) bad = 1;
@@ -694,13 +684,14 @@ struct Kern {
         for (int j = lane; j <= GM; j += 32) {
             const size_t r = static_cast<size_t>(b) * (GM + 1) + j;
             if (dbg.max_target) dbg.max_target[r] = st[j].m;
-            if (dbg.lse_target) dbg.lse_target[r] = greedy ? nan("") : lse_from_stats(st[j].m, st[j].s, T);
+            if (dbg.lse_target) dbg.lse_target[r] = greedy ? nan("") : lse_from_stats(st[j].m, st[j].s, c, T);
             if (dbg.argmax_target) dbg.argmax_target[r] = greedy ? st[j].idx : -1;
         }
         for (int j = lane; j < GM; j += 32) {
             const size_t r = static_cast<size_t>(b) * GM + j;
             if (dbg.max_draft) dbg.max_draft[r] = greedy ? nanf("") : st[GM + 1 + j].m;
-            if (dbg.lse_draft) dbg.lse_draft[r] = greedy ? nan("") : lse_from_stats(st[GM + 1 + j].m, st[GM + 1 + j].s, T);
+            if (dbg.lse_draft)
+                dbg.lse_draft[r] = greedy ? nan("") : lse_from_stats(st[GM + 1 + j].m, st[GM + 1 + j].s, c, T);
         }
         // first failing position over all lanes (gamma may exceed 32)
         int n = GM;
@@ -714,12 +705,15 @@ struct Kern {
                 } else {
                     const size_t tr = static_cast<size_t>(b) * (GM + 1) + i;
                     const size_t dr = static_cast<size_t>(b) * GM + i;
-                    const double p = prob_from_stats(load_logit<DT>(a.target, tr * V + x), st[i].m, st[i].s, c);
-                    const double q = prob_from_stats(load_logit<DT>(a.draft, dr * V + x), st[GM + 1 + i].m,
-                                                     st[GM + 1 + i].s, c);
+                    const bool pre_loaded = base == 0;
+                    const float lt = pre_loaded ? lt0 : load_logit<DT>(a.target, tr * V + x);
+                    const float ld = pre_loaded ? ld0 : load_logit<DT>(a.draft, dr * V + x);
+                    const float u = pre_loaded ? u0 : a.u_accept[dr];
+                    const double p = prob_from_stats(lt, st[i].m, st[i].s, c);
+                    const double q = prob_from_stats(ld, st[GM + 1 + i].m, st[GM + 1 + i].s, c);
                     if (dbg.p_x) dbg.p_x[dr] = p;
                     if (dbg.q_x) dbg.q_x[dr] = q;
-                    fail = !accept_draft(p, q, a.u_accept[dr]);
+                    fail = !accept_draft(p, q, u);
                 }
             }
             const unsigned ball = __ballot_sync(0xffffffffu, fail);
@@ -752,16 +746,16 @@ struct Kern {
                 j.pad = 0;
                 DrawParams& d = j.d;
                 d.c = c;
-                d.mp = st[n].m;
+                d.mcp = scaled_max(st[n].m, c);
                 d.isp = __double2float_rn(1.0 / static_cast<double>(st[n].s));
                 if (n < GM) {
                     d.kind = kKindResidual;
-                    d.mq = st[GM + 1 + n].m;
+                    d.mcq = scaled_max(st[GM + 1 + n].m, c);
                     d.isq = __double2float_rn(1.0 / static_cast<double>(st[GM + 1 + n].s));
                     d.fix = kFixResidual;
                 } else {
                     d.kind = kKindBonus;
-                    d.mq = 0.0f;
+                    d.mcq = 0.0f;
                     d.isq = 0.0f;
                     d.fix = kFixTarget;
                 }
@@ -770,23 +764,17 @@ struct Kern {
                 if (dbg.kind) dbg.kind[b] = d.kind;
             }
         }
-        if (!greedy)
-            for (int j = lane; j < L.NCH; j += 32) chunks()[static_cast<size_t>(k) * L.NCH + j] = 0ull;
     }
 
     // ---- phase 3 schedule: draw items (job k, chunk j) of this block
     __device__ static int job_cost(int kind) { return kind == kKindResidual ? 2 : (kind == kKindBonus ? 1 : 0); }
 
-    // Calls f(k, j) for every item whose first cost unit falls in this
-    // block's share. `pre` holds the cost prefix over jobs (n_samp + 1).
-    template <typename F>
-    __device__ void for_each_item(const int* pre, F&& f) const {
+    // The block's unit range and the first job with units after u_lo.
+    __device__ void item_range(const int* pre, long long& u_lo, long long& u_hi, int& k_first) const {
         const int ns = ctl.n_samp;
         const long long U = static_cast<long long>(pre[ns]) * L.NCH;
-        if (U == 0) return;
-        const long long u_lo = part_begin(U, G, g, 1), u_hi = part_begin(U, G, g + 1, 1);
-        if (u_hi <= u_lo) return;
-        // first job whose units end after u_lo
+        u_lo = part_begin(U, G, g, 1);
+        u_hi = part_begin(U, G, g + 1, 1);
         int lo = 0, hi = ns - 1;
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
@@ -795,7 +783,19 @@ struct Kern {
             else
                 lo = mid + 1;
         }
-        for (int k = lo; k < ns; ++k) {
+        k_first = lo;
+    }
+
+    // Calls f(k, j) for every item whose first cost unit falls in this
+    // block's share. `pre` holds the cost prefix over jobs (n_samp + 1).
+    template <typename F>
+    __device__ void for_each_item(const int* pre, F&& f) const {
+        const int ns = ctl.n_samp;
+        long long u_lo, u_hi;
+        int k0;
+        item_range(pre, u_lo, u_hi, k0);
+        if (u_hi <= u_lo) return;
+        for (int k = k0; k < ns; ++k) {
             const int cost = pre[k + 1] - pre[k];
             if (cost == 0) continue;
             const long long base = static_cast<long long>(pre[k]) * L.NCH;
@@ -810,48 +810,84 @@ struct Kern {
         }
     }
 
-    // Weight sum of one thread run: tokens [j*CH + t*TPT, ... + TPT) of the
-    // chunk, in index order. `tv`/`dv` hold the run's logits.
-    __device__ static float run_sum(const float* lt, const float* ld, int valid, const DrawParams& d,
+    __device__ bool job_cached(int k) const { return k >= ctl.job_lo && k < ctl.job_lo + ctl.job_n; }
+
+    // A run is kTPT consecutive tokens, 64 bytes, held packed as 4 vectors.
+    using Run = uint4[4];
+
+    // Token e of a packed run as binary32.
+    __device__ static __forceinline__ float token_at(const Run& v, int e) {
+        const int q = DT == SV_BF16 ? e >> 3 : e >> 2;
+        const int i = DT == SV_BF16 ? (e >> 1) & 3 : e & 3;
+        const uint32_t w = i == 0 ? v[q].x : i == 1 ? v[q].y : i == 2 ? v[q].z : v[q].w;
+        if (DT == SV_BF16) return (e & 1) ? bf16x2_hi(w) : bf16x2_lo(w);
+        return __uint_as_float(w);
+    }
+
+    // Weight of token e of a run (target run vt, draft run vd).
+    __device__ static __forceinline__ float run_weight(const Run& vt, const Run& vd, int e,
+                                                       const DrawParams& d, int kind) {
+        return kind == kKindResidual ? weight_residual(token_at(vt, e), token_at(vd, e), d)
+                                     : weight_target(token_at(vt, e), d);
+    }
+
+    // Weight sum of the first `valid` tokens of a run, in index order.
+    __device__ static __forceinline__ float run_sum(const Run& vt, const Run& vd, int valid, const DrawParams& d,
                                     int kind) {
         float run = 0.0f;
+        if (kind == kKindResidual) {
 #pragma unroll
-        for (int e = 0; e < kTPT; ++e) {
-            if (e < valid) {
-                const float w = kind == kKindResidual ? weight_residual(lt[e], ld[e], d) : weight_target(lt[e], d);
-                run = __fadd_rn(run, w);
-            }
+            for (int e = 0; e < kTPT; ++e)
+                if (e < valid) run = __fadd_rn(run, weight_residual(token_at(vt, e), token_at(vd, e), d));
+        } else {
+#pragma unroll
+            for (int e = 0; e < kTPT; ++e)
+                if (e < valid) run = __fadd_rn(run, weight_target(token_at(vt, e), d));
         }
         return run;
     }
 
-    // Loads a thread run from shared memory (64 bytes, swizzled order to
-    // avoid bank conflicts) into binary32 values.
-    __device__ static void load_run_smem(const char* sm, int t, float* out) {
-        uint4 v[4];
+    // Run t of a stage in shared memory (swizzled order: conflict-free).
+    // Thread t reads its vectors in the order r, r+1, r+2, r+3 (mod 4) with
+    // r = (t >> 1) & 3, so the 8 lanes of each shared-memory wavefront hit
+    // distinct banks; compile-time selects put them back in index order.
+    __device__ static __forceinline__ void load_run_smem(const char* sm, int t, Run& v) {
+        const int r = (t >> 1) & 3;
+        const uint4* base = reinterpret_cast<const uint4*>(sm + static_cast<size_t>(t) * 64);
+        uint4 raw[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int q = (k + (t >> 1)) & 3;
-            v[q] = *reinterpret_cast<const uint4*>(sm + static_cast<size_t>(t) * 64 + q * 16);
-        }
+        for (int k = 0; k < 4; ++k) raw[k] = base[(k + r) & 3];  // raw[k] is vector (k + r) & 3
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (DT == SV_BF16) {
-                    out[q * 8 + 2 * i] = bf16x2_lo(w4[i]);
-                    out[q * 8 + 2 * i + 1] = bf16x2_hi(w4[i]);
-                } else {
-                    out[q * 4 + i] = __uint_as_float(w4[i]);
-                }
-            }
+            const uint4 a0 = raw[q], a1 = raw[(q + 3) & 3], a2 = raw[(q + 2) & 3], a3 = raw[(q + 1) & 3];
+            v[q].x = r == 0 ? a0.x : r == 1 ? a1.x : r == 2 ? a2.x : a3.x;
+            v[q].y = r == 0 ? a0.y : r == 1 ? a1.y : r == 2 ? a2.y : a3.y;
+            v[q].z = r == 0 ? a0.z : r == 1 ? a1.z : r == 2 ? a2.z : a3.z;
+            v[q].w = r == 0 ? a0.w : r == 1 ? a1.w : r == 2 ? a2.w : a3.w;
         }
     }
 
-    __device__ static void load_run_global(const void* base, long long row_elem0, int count, float* out) {
+    // A run from global memory starting at element `e` (64-byte aligned in the
+    // row); its first `valid` tokens are whole 16-byte vectors because rows
+    // end on 16-byte boundaries. The rest is zero.
+    __device__ static __forceinline__ void load_run_global(const void* base, long long e, int valid, Run& v) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const char*>(base) + e * ES);
+        const int nv = valid * ES / 16;
 #pragma unroll
-        for (int e = 0; e < kTPT; ++e) out[e] = e < count ? load_logit<DT>(base, row_elem0 + e) : 0.0f;
+        for (int q = 0; q < 4; ++q) v[q] = q < nv ? __ldg(p + q) : make_uint4(0u, 0u, 0u, 0u);
+    }
+
+    // Fixed-point weight sum of run r of chunk j of a job, from global memory.
+    __device__ __forceinline__ unsigned long long run_fixed_global(long long trow, long long drow, int j, int r,
+                                                   const DrawParams& d, int kind) const {
+        const long long e0 = static_cast<long long>(j) * kChunkElems;
+        const int cnt = static_cast<int>(min(static_cast<long long>(kChunkElems), a.V - e0));
+        const int valid = max(0, min(kTPT, cnt - r * kTPT));
+        if (valid <= 0) return 0ull;
+        Run vt, vd;
+        load_run_global(a.target, trow + e0 + r * kTPT, valid, vt);
+        if (kind == kKindResidual) load_run_global(a.draft, drow + e0 + r * kTPT, valid, vd);
+        return to_fixed(run_sum(vt, vd, valid, d, kind), d.fix);
     }
 };
 
@@ -863,9 +899,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     Rec* warp_rows = reinterpret_cast<Rec*>(smem + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl));
     int* pre = reinterpret_cast<int*>(warp_rows + kConsumerWarps * kMaxRowsPerReq);
 
-    Kern<DT> K{a, L, ws, ctl, stages, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x)};
+    using KT = Kern<DT>;
+    KT K{a, L, ws, ctl, stages, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x)};
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const bool producer = warp == kConsumerWarps;
+    unsigned long long* ph = reinterpret_cast<unsigned long long*>(a.dbg.phase_ns);
+    stamp(ph, 0);
 
     if (t == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -878,72 +917,84 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     for (int i = t; i < kMapMax; i += kThreads) ctl.map[i] = -1;
     __syncthreads();
 
+    const long long ts = part_begin(L.Et, K.G, K.g, L.vec), te = part_begin(L.Et, K.G, K.g + 1, L.vec);
+
     // -------------------------------------------------------------- phase 1
-    typename Kern<DT>::Producer prod;
-    typename Kern<DT>::Consumer cons;
+    typename KT::Cursor prod, cons;
     if (producer) {
         bool ok = true;
-        auto issue = [&](const Stage1& st) {
-            if (!ok || ctl.abort) return;
-            ok = K.produce(prod, st.src, st.bytes);
+        auto issue = [&](const Segment& sg) {
+            for (long long off = 0; off < sg.elems && ok && !ctl.abort; off += KT::kChunkElems) {
+                const long long n = min(static_cast<long long>(KT::kChunkElems), sg.elems - off);
+                ok = K.produce(prod, sg.src + off * KT::ES, static_cast<unsigned>(n * KT::ES));
+            }
         };
-        K.for_each_target_stage(issue);
+        K.for_each_target_segment(ts, te, issue);
         bar_sync(kBarHandoff, kThreads);  // the consumers' prologue is done
-        K.for_each_draft_stage(issue);
+        K.for_each_draft_segment(issue);
         if (!ok) K.set_abort(a.d_status);
         if (ctl.abort) K.drain(prod);
     } else {
-        // target stages do not depend on the prologue, but the consumers
-        // compute it first: the ring holds kStages stages meanwhile.
+        // the ring fills with target stages while the consumers run the prologue
         K.prologue();
         bar_arrive(kBarHandoff, kThreads);
-        typename Kern<DT>::RowState rs;
-        rs.key = -1;
         bool ok = true;
-        auto fold = [&](const Stage1& st) {
+        auto fold = [&](const Segment& sg) {
             if (!ok) return;
-            const long long key = (static_cast<long long>(st.loc.kind) << 62) + st.loc.row;
-            if (key != rs.key) {
-                K.flush_row(rs);
-                K.start_row(rs, st.loc);
+            typename KT::RowState rs;
+            K.start_row(rs, sg.loc);
+            for (long long off = 0; off < sg.elems; off += KT::kChunkElems) {
+                const long long n = min(static_cast<long long>(KT::kChunkElems), sg.elems - off);
+                const char* sm = K.consume_begin(cons);
+                if (!sm) {
+                    ok = false;
+                    K.set_abort(a.d_status);
+                    return;
+                }
+                K.fold_stage(rs, sm, static_cast<int>(n * KT::ES / 16), sg.e0 + off);
+                K.consume_end(cons);
             }
-            const char* sm = K.consume_begin(cons);
-            if (!sm) {
-                ok = false;
-                K.set_abort(a.d_status);
-                return;
-            }
-            K.fold_stage(rs, sm, st);
-            K.consume_end(cons);
+            K.flush_row(rs, sg.loc);
         };
-        K.for_each_target_stage(fold);
-        K.for_each_draft_stage(fold);
-        if (ok) K.flush_row(rs);
+        K.for_each_target_segment(ts, te, fold);
+        K.for_each_draft_segment(fold);
     }
+    __syncthreads();
+    stamp(ph, 2);
     Hdr* hdr = K.hdr();
     if (!grid_sync(hdr, a.d_status, &ctl.flag)) return;
+    stamp(ph, 3);
     if (ctl.abort) return;
 
     // -------------------------------------------------------------- phase 2
     if (!producer) {
         Rec* st = warp_rows + warp * kMaxRowsPerReq;
-        for (int b = blockIdx.x * kConsumerWarps + warp; b < a.B; b += gridDim.x * kConsumerWarps) {
+        // requests spread over the blocks first, then over the warps
+        for (int b = warp * gridDim.x + blockIdx.x; b < a.B; b += gridDim.x * kConsumerWarps) {
             K.verify_request(b, st);
             __syncwarp();
         }
     }
-    if (ctl.n_samp == 0) return;
+    __syncthreads();
+    stamp(ph, 4);
+    const int ns = ctl.n_samp;
+    if (ns == 0) {
+        stamp(ph, 9);
+        return;
+    }
     if (!grid_sync(hdr, a.d_status, &ctl.flag)) return;
+    stamp(ph, 5);
 
     // -------------------------------------------------------------- phase 3a
-    const int ns = ctl.n_samp;
+    constexpr int TPT = KT::kTPT;
+    constexpr int CH = KT::kChunkElems;
     if (!producer) {
-        // cost prefix over jobs, on the consumers
-        Job* jobs = K.jobs();
+        // cost prefix over jobs, then this block's jobs into shared memory
+        const Job* gjobs = K.jobs();
         int carry = 0;
         for (int base = 0; base < ns; base += kConsumers) {
             const int k = base + t;
-            const int cost = k < ns ? Kern<DT>::job_cost(jobs[k].kind) : 0;
+            const int cost = k < ns ? KT::job_cost(gjobs[k].kind) : 0;
             int x = cost;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -952,194 +1003,262 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             }
             if (lane == 31) ctl.wtmp[warp] = x;
             bar_sync(kBarConsumers, kConsumers);
-            int before = carry;
-            for (int w = 0; w < warp; ++w) before += ctl.wtmp[w];
-            int total = 0;
-            for (int w = 0; w < kConsumerWarps; ++w) total += ctl.wtmp[w];
+            int before = carry, total = 0;
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                if (w < warp) before += ctl.wtmp[w];
+                total += ctl.wtmp[w];
+            }
             if (k < ns) pre[k] = before + x - cost;
             carry += total;
             bar_sync(kBarConsumers, kConsumers);
         }
         if (t == 0) pre[ns] = carry;
         bar_sync(kBarConsumers, kConsumers);
+        long long u_lo, u_hi;
+        int k0;
+        K.item_range(pre, u_lo, u_hi, k0);
+        int k1 = k0;  // one past the last job with an item here
+        if (u_hi > u_lo) {
+            int lo = k0, hi = ns;
+            while (lo < hi) {  // first job whose units start at or after u_hi
+                const int mid = (lo + hi) >> 1;
+                if (static_cast<long long>(pre[mid]) * L.NCH >= u_hi)
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            k1 = lo;
+        }
+        const int njobs = min(kJobCache, max(0, k1 - k0));
+        for (int i = t; i < njobs; i += kConsumers) ctl.jobs[i] = gjobs[k0 + i];
+        if (t == 0) {
+            ctl.job_lo = k0;
+            ctl.job_n = njobs;
+        }
+        bar_sync(kBarConsumers, kConsumers);
         bar_arrive(kBarHandoff, kThreads);
     }
     if (producer) {
         bar_sync(kBarHandoff, kThreads);
         bool ok = true;
-        Job* jobs = K.jobs();
+        const Job* gjobs = K.jobs();
         K.for_each_item(pre, [&](int k, int j) {
             if (!ok || ctl.abort) return;
-            const Job& jb = jobs[k];
-            const long long e0 = static_cast<long long>(j) * Kern<DT>::kChunkElems;
-            const int cnt = static_cast<int>(min(static_cast<long long>(Kern<DT>::kChunkElems), a.V - e0));
-            const unsigned bytes = static_cast<unsigned>(cnt * Kern<DT>::ES);
+            const Job& jb = K.job_cached(k) ? ctl.jobs[k - ctl.job_lo] : gjobs[k];
+            const long long e0 = static_cast<long long>(j) * CH;
+            const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+            const unsigned bytes = static_cast<unsigned>(cnt * KT::ES);
             const long long trow = static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n;
-            ok = K.produce(prod, static_cast<const char*>(a.target) + (trow * a.V + e0) * Kern<DT>::ES, bytes);
+            ok = K.produce(prod, static_cast<const char*>(a.target) + (trow * a.V + e0) * KT::ES, bytes);
             if (ok && jb.kind == kKindResidual) {
                 const long long drow = static_cast<long long>(jb.b) * a.gamma + jb.n;
-                ok = K.produce(prod, static_cast<const char*>(a.draft) + (drow * a.V + e0) * Kern<DT>::ES, bytes);
+                ok = K.produce(prod, static_cast<const char*>(a.draft) + (drow * a.V + e0) * KT::ES, bytes);
             }
         });
         if (!ok) K.set_abort(a.d_status);
         if (ctl.abort) K.drain(prod);
     } else {
         bool ok = true;
-        Job* jobs = K.jobs();
-        unsigned long long* csum = K.chunks();
+        const Job* gjobs = K.jobs();
+        unsigned long long* wsums = K.wsums();
         K.for_each_item(pre, [&](int k, int j) {
             if (!ok) return;
-            const Job jb = jobs[k];
-            const long long e0 = static_cast<long long>(j) * Kern<DT>::kChunkElems;
-            const int cnt = static_cast<int>(min(static_cast<long long>(Kern<DT>::kChunkElems), a.V - e0));
-            const int valid = max(0, min(Kern<DT>::kTPT, cnt - t * Kern<DT>::kTPT));
-            float lt[Kern<DT>::kTPT], ld[Kern<DT>::kTPT];
+            const Job jb = K.job_cached(k) ? ctl.jobs[k - ctl.job_lo] : gjobs[k];
+            const long long e0 = static_cast<long long>(j) * CH;
+            const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+            const int valid = max(0, min(TPT, cnt - t * TPT));
+            typename KT::Run lt, ld;
             const char* smt = K.consume_begin(cons);
             if (!smt) {
                 ok = false;
                 K.set_abort(a.d_status);
                 return;
             }
-            if (valid > 0) Kern<DT>::load_run_smem(smt, t, lt);
-            const bool resid = jb.kind == kKindResidual;
-            if (resid) {
-                K.consume_end(cons);  // release the target stage after loading
+            if (valid > 0) KT::load_run_smem(smt, t, lt);
+            if (jb.kind == kKindResidual) {
+                K.consume_end(cons);  // release the target stage once loaded
                 const char* smd = K.consume_begin(cons);
                 if (!smd) {
                     ok = false;
                     K.set_abort(a.d_status);
                     return;
                 }
-                if (valid > 0) Kern<DT>::load_run_smem(smd, t, ld);
+                if (valid > 0) KT::load_run_smem(smd, t, ld);
             }
             K.consume_end(cons);
-            const float run = valid > 0 ? Kern<DT>::run_sum(lt, ld, valid, jb.d, jb.kind) : 0.0f;
+            const float run = valid > 0 ? KT::run_sum(lt, ld, valid, jb.d, jb.kind) : 0.0f;
             const unsigned long long wsum = warp_sum_u64(to_fixed(run, jb.d.fix));
-            if (lane == 0 && wsum) atomicAdd(csum + static_cast<size_t>(k) * L.NCH + j, wsum);
+            if (lane == 0) wsums[(static_cast<size_t>(k) * L.NCH + j) * kConsumerWarps + warp] = wsum;
         });
     }
+    __syncthreads();
+    stamp(ph, 6);
     if (!grid_sync(hdr, a.d_status, &ctl.flag)) return;
+    stamp(ph, 7);
     if (ctl.abort || producer) return;
 
     // -------------------------------------------------------------- phase 3b
-    Job* jobs = K.jobs();
-    const unsigned long long* csum = K.chunks();
-    constexpr int TPT = Kern<DT>::kTPT;
-    constexpr int CH = Kern<DT>::kChunkElems;
-    for (int k = blockIdx.x * kConsumerWarps + warp; k < ns; k += gridDim.x * kConsumerWarps) {
-        const Job jb = jobs[k];
+    const Job* gjobs = K.jobs();
+    const unsigned long long* wsums = K.wsums();
+    for (int k = warp * gridDim.x + blockIdx.x; k < ns; k += gridDim.x * kConsumerWarps) {
+        const Job jb = gjobs[k];
         if (jb.kind != kKindResidual && jb.kind != kKindBonus) continue;
         DrawParams d = jb.d;
         int kind = jb.kind;
         const long long trow = (static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n) * a.V;
         const long long drow = (static_cast<long long>(jb.b) * a.gamma + jb.n) * a.V;
-        // chunk totals of this job (recomputed on the warp for the fallback)
-        unsigned long long total = 0;
-        for (int j = lane; j < L.NCH; j += 32) total += csum[static_cast<size_t>(k) * L.NCH + j];
-        total = warp_sum_u64(total);
+        const unsigned long long* js = wsums + static_cast<size_t>(k) * L.NCH * kConsumerWarps;
+        // per-warp sums of chunk j (from phase 3a, or recomputed on the fallback)
         bool fallback = false;
+        auto warp_part = [&](int j, int w) -> unsigned long long {
+            if (!fallback) return js[static_cast<size_t>(j) * kConsumerWarps + w];
+            return warp_sum_u64(K.run_fixed_global(trow, drow, j, w * 32 + lane, d, kind));
+        };
+        // total of chunk j, computed by the calling lane alone (phase-3a sums)
+        auto chunk_total_lane = [&](int j) -> unsigned long long {
+            const ulonglong2* p = reinterpret_cast<const ulonglong2*>(js + static_cast<size_t>(j) * kConsumerWarps);
+            unsigned long long s = 0;
+#pragma unroll
+            for (int h = 0; h < kConsumerWarps / 2; ++h) {
+                const ulonglong2 x = p[h];
+                s += x.x + x.y;
+            }
+            return s;
+        };
+        // total of chunk j on the fallback, computed by the whole warp
+        auto chunk_total_warp = [&](int j) -> unsigned long long {
+            unsigned long long s = 0;
+            for (int w = 0; w < kConsumerWarps; ++w) s += warp_part(j, w);
+            return s;
+        };
+        const int nch_lane = (L.NCH + 31) / 32;  // chunks per lane
+        unsigned long long ctot[4];               // this lane's chunk totals (NCH <= 128 here)
+        unsigned long long total = 0;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int j = h * 32 + lane;
+            ctot[h] = (h < nch_lane && j < L.NCH) ? chunk_total_lane(j) : 0ull;
+            total += ctot[h];
+        }
+        total = warp_sum_u64(total);
         if (total == 0ull) {
             // residual weights rounded to zero everywhere: draw from p_n
             fallback = true;
             kind = kKindBonus;
             d.fix = kFixTarget;
-        }
-        auto chunk_total = [&](int j) -> unsigned long long {
-            // sum over the chunk's 256 runs, on this warp
-            unsigned long long acc = 0;
-            const long long e0 = static_cast<long long>(j) * CH;
-            const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
-            for (int vt = lane; vt < kConsumers; vt += 32) {
-                const int valid = max(0, min(TPT, cnt - vt * TPT));
-                if (valid <= 0) continue;
-                float lt[TPT], ld[TPT];
-                Kern<DT>::load_run_global(a.target, trow + e0 + vt * TPT, valid, lt);
-                if (kind == kKindResidual) Kern<DT>::load_run_global(a.draft, drow + e0 + vt * TPT, valid, ld);
-                acc += to_fixed(Kern<DT>::run_sum(lt, ld, valid, d, kind), d.fix);
-            }
-            return warp_sum_u64(acc);
-        };
-        if (fallback) {
             total = 0;
-            for (int j = 0; j < L.NCH; ++j) total += chunk_total(j);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                unsigned long long mine = 0;
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = h * 32 + jj;
+                    if (h < nch_lane && j < L.NCH) {
+                        const unsigned long long c = chunk_total_warp(j);
+                        if (jj == lane) mine = c;
+                    }
+                }
+                ctot[h] = mine;
+                total += warp_sum_u64(mine);
+            }
         }
         const unsigned long long tt =
             __double2ull_rz(static_cast<double>(a.u_sample[jb.b]) * static_cast<double>(total));
-        // the chunk holding tt (prefix over chunks, exact integers)
         unsigned long long before = 0;
-        int jsel = L.NCH - 1;
-        for (int j = 0; j < L.NCH; ++j) {
-            const unsigned long long cs = fallback ? chunk_total(j) : csum[static_cast<size_t>(k) * L.NCH + j];
-            if (tt < before + cs) {
-                jsel = j;
-                break;
-            }
-            before += cs;
-        }
-        // runs of chunk jsel: values, exclusive prefix in run order
-        const long long e0 = static_cast<long long>(jsel) * CH;
-        const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
-        const unsigned long long tin = tt - before;
-        unsigned long long carry = 0;
-        int found_vt = -1;
-        unsigned long long found_start = 0;
-        for (int r0 = 0; r0 < kConsumers && found_vt < 0; r0 += 32) {
-            const int vt = r0 + lane;
-            const int valid = max(0, min(TPT, cnt - vt * TPT));
-            unsigned long long q = 0;
-            if (valid > 0) {
-                float lt[TPT], ld[TPT];
-                Kern<DT>::load_run_global(a.target, trow + e0 + vt * TPT, valid, lt);
-                if (kind == kKindResidual) Kern<DT>::load_run_global(a.draft, drow + e0 + vt * TPT, valid, ld);
-                q = to_fixed(Kern<DT>::run_sum(lt, ld, valid, d, kind), d.fix);
-            }
-            unsigned long long x = q;
+        int jsel = -1;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            if (jsel >= 0 || h >= nch_lane) break;
+            const int j0 = h * 32;
+            const unsigned long long cs = ctot[h];
+            unsigned long long incl = cs;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
             }
-            const unsigned long long start = carry + x - q;
-            const bool mine = q > 0 && start <= tin && tin < start + q;
-            const unsigned ball = __ballot_sync(0xffffffffu, mine);
-            if (ball) {
-                const int src = __ffs(ball) - 1;
-                found_vt = r0 + src;
-                found_start = __shfl_sync(0xffffffffu, start, src);
+            const unsigned long long st0 = before + incl - cs;
+            const unsigned hit = __ballot_sync(0xffffffffu, cs > 0 && st0 <= tt && tt < st0 + cs);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                jsel = j0 + src;
+                before = __shfl_sync(0xffffffffu, st0, src);
+            } else {
+                before += __shfl_sync(0xffffffffu, incl, 31);
             }
-            carry += __shfl_sync(0xffffffffu, x, 31);
         }
-        if (lane == 0) {
-            int token = a.V - 1;
-            if (found_vt >= 0) {
-                const int valid = max(0, min(TPT, cnt - found_vt * TPT));
-                float lt[TPT], ld[TPT];
-                Kern<DT>::load_run_global(a.target, trow + e0 + found_vt * TPT, valid, lt);
-                if (kind == kKindResidual) Kern<DT>::load_run_global(a.draft, drow + e0 + found_vt * TPT, valid, ld);
-                float run = 0.0f;
-                int last_pos = -1;
-                token = -1;
-                for (int e = 0; e < valid; ++e) {
-                    const float w = kind == kKindResidual ? weight_residual(lt[e], ld[e], d) : weight_target(lt[e], d);
-                    run = __fadd_rn(run, w);
+        if (jsel < 0) jsel = L.NCH - 1;  // cannot happen: tt < total
+        // the warp of that chunk: lanes 0..7 hold its per-warp sums (on the
+        // fallback warp_part is warp-collective, so every lane calls it)
+        unsigned long long part = 0ull;
+        if (!fallback) {
+            if (lane < kConsumerWarps) part = js[static_cast<size_t>(jsel) * kConsumerWarps + lane];
+        } else {
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const unsigned long long v = warp_part(jsel, w);
+                if (lane == w) part = v;
+            }
+        }
+        unsigned long long pincl = part;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, pincl, o);
+            if (lane >= o) pincl += y;
+        }
+        const unsigned long long pst = before + pincl - part;
+        const unsigned whit = __ballot_sync(0xffffffffu, part > 0 && pst <= tt && tt < pst + part);
+        const int wsel = whit ? __ffs(whit) - 1 : kConsumerWarps - 1;
+        before = __shfl_sync(0xffffffffu, pst, wsel);
+        // its 32 runs, one per lane, re-read with the weights of phase 3a
+        const long long e0 = static_cast<long long>(jsel) * CH;
+        const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+        const int vt = wsel * 32 + lane;
+        const int valid = max(0, min(TPT, cnt - vt * TPT));
+        typename KT::Run lt, ld;
+        if (valid > 0) {
+            KT::load_run_global(a.target, trow + e0 + vt * TPT, valid, lt);
+            if (kind == kKindResidual) KT::load_run_global(a.draft, drow + e0 + vt * TPT, valid, ld);
+        }
+        const float run = valid > 0 ? KT::run_sum(lt, ld, valid, d, kind) : 0.0f;
+        const unsigned long long q = to_fixed(run, d.fix);
+        unsigned long long x = q;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        const unsigned long long start = before + x - q;
+        const bool mine = q > 0 && start <= tt && tt < start + q;
+        const unsigned ball = __ballot_sync(0xffffffffu, mine);
+        if (mine && lane == __ffs(ball) - 1) {
+            // the first token of the run whose prefix passes tt
+            float r2 = 0.0f;
+            int token = -1, last_pos = -1;
+#pragma unroll
+            for (int e = 0; e < TPT; ++e) {
+                if (e < valid) {
+                    const float w = KT::run_weight(lt, ld, e, d, kind);
+                    r2 = __fadd_rn(r2, w);
                     if (w > 0.0f) last_pos = e;
-                    if (found_start + to_fixed(run, d.fix) > tin) {
-                        token = e;
-                        break;
-                    }
+                    if (token < 0 && start + to_fixed(r2, d.fix) > tt) token = e;
                 }
-                if (token < 0) token = last_pos;
-                token += static_cast<int>(e0) + found_vt * TPT;
             }
-            a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.n] = token;
-            if (a.dbg.w_total) {
-                const double W = static_cast<double>(total);
-                a.dbg.w_total[jb.b] = kind == kKindResidual ? W * kFixResidualInv
-                                                            : W * kFixTargetInv * static_cast<double>(d.isp);
-            }
+            if (token < 0) token = last_pos;
+            a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.n] = static_cast<int>(e0) + vt * TPT + token;
+        }
+        if (!ball && lane == 0) {
+            // cannot happen: the runs partition [0, total) exactly
+            a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.n] = a.V - 1;
+        }
+        if (lane == 0 && a.dbg.w_total) {
+            const double W = static_cast<double>(total);
+            a.dbg.w_total[jb.b] =
+                kind == kKindResidual ? W * kFixResidualInv : W * kFixTargetInv * static_cast<double>(d.isp);
         }
         __syncwarp();
     }
+    bar_sync(kBarConsumers, kConsumers);
+    stamp(ph, 8);
+    stamp(ph, 9);
 }
 
 size_t smem_bytes() {
@@ -1154,12 +1273,13 @@ bool streaming_applicable(const Args& a) {
     if ((static_cast<size_t>(a.V) * es) % 16 != 0) return false;
     if ((reinterpret_cast<uintptr_t>(a.target) & 15) || (reinterpret_cast<uintptr_t>(a.draft) & 15)) return false;
     if (a.B > kMaxB) return false;
+    if (static_cast<size_t>(a.V) * es > static_cast<size_t>(128) * kStageBytes) return false;  // <= 128 chunks per row
     return true;
 }
 
-int streaming_default_grid(const DeviceInfo& dev) { return dev.num_sms; }
+int streaming_default_grid(const DeviceInfo& dev) { return std::min(dev.num_sms, kMaxGrid); }
 
-bool streaming_grid_ok(int B, int grid) { return (B + grid - 1) / grid + 3 <= kMapMax; }
+bool streaming_grid_ok(int B, int grid) { return grid <= kMaxGrid && (B + grid - 1) / grid + 3 <= kMapMax; }
 
 size_t streaming_workspace_bytes(int B, int gamma, int V, int dtype, int grid) {
     return make_layout(B, gamma, V, dtype == SV_F32 ? 4 : 2, grid).total;

@@ -140,6 +140,38 @@ def test_invalid_requests():
         assert gpu["status"] & sv.SV_STATUS_BAD_REQUEST
 
 
+def test_residual_rounding_to_zero_falls_back_to_p():
+    """A rejection whose residual weights all round to zero in binary32 draws
+    from p at that position (the fallback reading). Target and draft rows are
+    equal (logit 10 at token 0, 0 elsewhere) except token x, whose draft logit
+    is 1e-4 higher: alpha = exp(-1e-4) < u = 0.99999, and p - q differs from
+    zero by about 4e-9 p, below binary32 resolution, so the two rows get the
+    same normaliser and every residual weight is exactly 0 on the GPU (the
+    oracle, in fp64, still sees a residual mass of about 4e-9). The drawn
+    token must lie in the CDF interval of p that holds u."""
+    from scipy import special
+    B, G, V = 64, 1, 1024
+    lt = np.zeros((B, G + 1, V), np.float32)
+    lt[:, :, 0] = 10.0
+    ld = lt[:, :G].copy()
+    x = (1 + np.arange(B) * 37 % (V - 1)).astype(np.int32)
+    ld[np.arange(B), 0, x] = np.float32(1e-4)
+    us = ((np.arange(B) + 0.5) / B).astype(np.float32)
+    w = synthetic.WORKLOADS[3].variant(B=B, gamma=G, V=V)
+    batch = synthetic.Batch(w, 0, lt, ld, x[:, None], np.full((B, 1), 0.99999, np.float32), us,
+                            np.ones(B, np.float32))
+    C = np.cumsum(special.softmax(lt[0, 0].astype(np.float64)))
+    for opts in (ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=3)):
+        gpu = parity.run_gpu(batch, **opts)
+        assert gpu["status"] == 0
+        assert np.all(gpu["out_num_accepted"] == 0)
+        tok = gpu["out_tokens"][:, 0]
+        lo = np.where(tok > 0, C[np.maximum(tok - 1, 0)], 0.0)
+        assert np.all((lo - 1e-4 <= us) & (us <= C[tok] + 1e-4)), tok
+        fell_back = np.abs(gpu["w_total"] - 1.0) < 1e-3  # reported as the mass of p
+        assert fell_back.sum() >= B // 2, gpu["w_total"]
+
+
 def _v8_batch(N, T, seed):
     from scipy import special
     rng = np.random.Generator(np.random.Philox(seed))
