@@ -130,6 +130,21 @@ __device__ __forceinline__ bool accept_draft(double p, double q, float u) {
     return static_cast<double>(u) < alpha;
 }
 
+// The accept test u < min(1, p(x)/q(x)) from the gathered logits and the two
+// rows' (m, s): p/q = 2^e * s_q / s_p with e = (lt - ld) c - (fl(mp c) - fl(mq c)),
+// e formed exactly in double, then rounded once and raised on the SFU (relative
+// error about 3e-7). q(x) = 0 (ld = -inf) gives alpha = 1 if p(x) > 0, else 0;
+// u = 0 accepts whenever p(x) > 0, even where 2^e underflows.
+__device__ __forceinline__ bool accept_from_logits(float lt, float ld, float mp, float sp, float mq, float sq,
+                                                   float c, float u) {
+    if (lt == neg_inf()) return false;  // p(x) = 0 < alpha requires p(x) > 0
+    if (ld == neg_inf() || u == 0.0f) return true;
+    const double e = (static_cast<double>(lt) - static_cast<double>(ld)) * static_cast<double>(c) -
+                     (static_cast<double>(scaled_max(mp, c)) - static_cast<double>(scaled_max(mq, c)));
+    const float alpha = __fmul_rn(ex2(__double2float_rn(e)), __fdiv_rn(sq, sp));
+    return u < alpha;
+}
+
 // log sum_x exp(l(x)/T) from (m, s, c): s = 2^(m c - fl(m c)) sum 2^((l - m) c),
 // so the log is m/T + ln s - (m c - fl(m c)) ln 2, with m/T and m c in double.
 __device__ __forceinline__ double lse_from_stats(float m, float s, float c, float T) {

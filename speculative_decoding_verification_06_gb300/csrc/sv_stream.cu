@@ -42,9 +42,10 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr int kStages = 8;
-constexpr int kStageBytes = 16384;
-constexpr int kVecPerThread = kStageBytes / 16 / kConsumers;  // 4
+constexpr int kStages = 4;
+constexpr int kStageBytes = 32768;
+constexpr int kVecPerThread = kStageBytes / 16 / kConsumers;  // 8
+constexpr int kChunkBytes = 16384;  // phase-3 chunk of one row (a residual item fills a stage)
 constexpr int kMapMax = 256;   // compacted requests in one block's draft slice
 constexpr int kMaxGrid = 256;  // blocks (partition tables live in shared memory)
 constexpr int kJobCache = 64;  // draw jobs cached per block in phase 3
@@ -92,7 +93,7 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     const long long Ed_max = static_cast<long long>(B) * gamma * V;
     L.MT = static_cast<int>(((L.Et + G - 1) / G + L.vec - 1) / V + 2);
     L.MD = static_cast<int>(((Ed_max + G - 1) / G + L.vec - 1) / V + 2);
-    const int chunk_elems = kStageBytes / es;
+    const int chunk_elems = kChunkBytes / es;
     L.NCH = (V + chunk_elems - 1) / chunk_elems;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -182,6 +183,40 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float f32_max_nan(float a, float b) {
     float r;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// Byte permute: the bytes of x selected by `sel` (zero bytes come from the
+// second operand, 0).
+__device__ __forceinline__ uint32_t prmt(uint32_t x, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(x), "r"(sel));
+    return r;
+}
+
+// Packed pairs of binary32 (the sm_100-family f32x2 arithmetic).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_pack_bits(uint32_t lo, uint32_t hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
 
@@ -287,7 +322,8 @@ __device__ __forceinline__ int owner(const long long* beg, int G, long long e) {
 template <int DT>
 struct Kern {
     static constexpr int ES = DT == SV_F32 ? 4 : 2;
-    static constexpr int kChunkElems = kStageBytes / ES;
+    static constexpr int kStageElems = kStageBytes / ES;  // phase-1 stage
+    static constexpr int kChunkElems = kChunkBytes / ES;  // phase-3 chunk
     static constexpr int kTPT = kChunkElems / kConsumers;  // tokens per thread run (64 bytes)
 
     const Args& a;
@@ -357,15 +393,19 @@ struct Kern {
         unsigned it = 0;
     };
 
-    // Producer warp: issue one copy into the next stage (lane 0 issues).
-    __device__ bool produce(Cursor& p, const char* src, unsigned bytes) const {
+    // Producer warp: fill the next stage with one copy, or two (the second at
+    // byte offset kChunkBytes); lane 0 issues.
+    __device__ bool produce(Cursor& p, const char* src, unsigned bytes, const char* src2 = nullptr,
+                            unsigned bytes2 = 0) const {
         const int slot = p.it % kStages;
         const unsigned round = p.it / kStages;
         // the verdict is made warp-uniform so that a timeout cannot split the warp
         if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(&ctl.empty[slot], (round - 1) & 1))) return false;
         if ((threadIdx.x & 31) == 0) {
-            mbar_expect_tx(&ctl.full[slot], bytes);
-            bulk_copy(stages + static_cast<size_t>(slot) * kStageBytes, src, bytes, &ctl.full[slot]);
+            char* dst = stages + static_cast<size_t>(slot) * kStageBytes;
+            mbar_expect_tx(&ctl.full[slot], bytes + bytes2);
+            bulk_copy(dst, src, bytes, &ctl.full[slot]);
+            if (src2) bulk_copy(dst + kChunkBytes, src2, bytes2, &ctl.full[slot]);
         }
         __syncwarp();
         ++p.it;
@@ -495,19 +535,31 @@ struct Kern {
     }
 
     // Folds one stage (nvec 16-byte vectors, element offset e0 in the row).
-    __device__ void fold_stage(RowState& rs, const char* sm, int nvec, long long e0) const {
-        const int t = threadIdx.x;
+    // Full stages (the common case) take a path without per-vector bounds.
+    __device__ __forceinline__ void fold_stage(RowState& rs, const char* sm, int nvec, long long e0) const {
         uint4 v[kVecPerThread];
+        const int t = threadIdx.x;
+        if (nvec == kVecPerThread * kConsumers) {
 #pragma unroll
-        for (int k = 0; k < kVecPerThread; ++k) {
-            const int vi = t + k * kConsumers;
-            if (vi < nvec)
-                v[k] = *reinterpret_cast<const uint4*>(sm + static_cast<size_t>(vi) * 16);
-            else if (DT == SV_BF16)
-                v[k] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-            else
-                v[k] = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+            for (int k = 0; k < kVecPerThread; ++k)
+                v[k] = *reinterpret_cast<const uint4*>(sm + static_cast<size_t>(t + k * kConsumers) * 16);
+        } else {
+#pragma unroll
+            for (int k = 0; k < kVecPerThread; ++k) {
+                const int vi = t + k * kConsumers;
+                if (vi < nvec)
+                    v[k] = *reinterpret_cast<const uint4*>(sm + static_cast<size_t>(vi) * 16);
+                else if (DT == SV_BF16)
+                    v[k] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+                else
+                    v[k] = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+            }
         }
+        fold_vectors(rs, v, e0);
+    }
+
+    __device__ __forceinline__ void fold_vectors(RowState& rs, const uint4 (&v)[kVecPerThread], long long e0) const {
+        const int t = threadIdx.x;
         float tmax;
         if (DT == SV_BF16) {
             uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(v[0].x, v[0].y), bf16x2_max_nan(v[0].z, v[0].w));
@@ -557,26 +609,28 @@ struct Kern {
             rs.m = tmax;
             rs.mc = mc;
         }
-        const float nmc = -rs.mc;
-        float acc0 = 0.0f, acc1 = 0.0f;
+        // Pairs of logits in packed binary32 arithmetic: fma.rn.f32x2 and
+        // add.rn.f32x2 round each lane exactly as two scalar instructions would.
+        const unsigned long long cc = f2_pack(c, c), nmc = f2_pack(-rs.mc, -rs.mc);
+        unsigned long long acc = f2_pack(0.0f, 0.0f);
 #pragma unroll
         for (int k = 0; k < kVecPerThread; ++k) {
             const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-            if (DT == SV_BF16) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc0 = __fadd_rn(acc0, ex2(__fmaf_rn(bf16x2_lo(w4[q]), c, nmc)));
-                    acc1 = __fadd_rn(acc1, ex2(__fmaf_rn(bf16x2_hi(w4[q]), c, nmc)));
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; q += 2) {
-                    acc0 = __fadd_rn(acc0, ex2(__fmaf_rn(__uint_as_float(w4[q]), c, nmc)));
-                    acc1 = __fadd_rn(acc1, ex2(__fmaf_rn(__uint_as_float(w4[q + 1]), c, nmc)));
-                }
+            for (int q = 0; q < 4; q += (DT == SV_BF16 ? 1 : 2)) {
+                unsigned long long x2;
+                if (DT == SV_BF16)
+                    x2 = f2_pack_bits(prmt(w4[q], 0x1044u), prmt(w4[q], 0x3244u));
+                else
+                    x2 = f2_pack_bits(w4[q], w4[q + 1]);
+                float d0, d1;
+                f2_unpack(f2_fma(x2, cc, nmc), d0, d1);
+                acc = f2_add(acc, f2_pack(ex2(d0), ex2(d1)));
             }
         }
-        rs.s = __fadd_rn(rs.s, __fadd_rn(acc0, acc1));
+        float a0, a1;
+        f2_unpack(acc, a0, a1);
+        rs.s = __fadd_rn(rs.s, __fadd_rn(a0, a1));
     }
 
     // ---- phase 2: merge of a row's pieces, in block and warp order
@@ -595,13 +649,15 @@ struct Kern {
             const int slot = static_cast<int>(row - b0 / a.V);
             const uint4* r =
                 reinterpret_cast<const uint4*>(base + (static_cast<size_t>(gg) * MM + slot) * kConsumerWarps);
+            uint4 x[kConsumerWarps];  // all loads issued before the merges
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) x[w] = __ldcg(r + w);
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
-                const uint4 x = __ldcg(r + w);
-                const float m = __uint_as_float(x.x), s = __uint_as_float(x.y);
-                bad |= static_cast<int>(x.w);
+                const float m = __uint_as_float(x[w].x), s = __uint_as_float(x[w].y);
+                bad |= static_cast<int>(x[w].w);
                 if (argmax)
-                    am = argmax_merge(am, ArgMax{m, static_cast<int32_t>(x.z)});
+                    am = argmax_merge(am, ArgMax{m, static_cast<int32_t>(x[w].z)});
                 else
                     ms = maxsum_merge(ms, MaxSum{m, s}, c);
             }
@@ -709,11 +765,9 @@ struct Kern {
                     const float lt = pre_loaded ? lt0 : load_logit<DT>(a.target, tr * V + x);
                     const float ld = pre_loaded ? ld0 : load_logit<DT>(a.draft, dr * V + x);
                     const float u = pre_loaded ? u0 : a.u_accept[dr];
-                    const double p = prob_from_stats(lt, st[i].m, st[i].s, c);
-                    const double q = prob_from_stats(ld, st[GM + 1 + i].m, st[GM + 1 + i].s, c);
-                    if (dbg.p_x) dbg.p_x[dr] = p;
-                    if (dbg.q_x) dbg.q_x[dr] = q;
-                    fail = !accept_draft(p, q, u);
+                    if (dbg.p_x) dbg.p_x[dr] = prob_from_stats(lt, st[i].m, st[i].s, c);
+                    if (dbg.q_x) dbg.q_x[dr] = prob_from_stats(ld, st[GM + 1 + i].m, st[GM + 1 + i].s, c);
+                    fail = !accept_from_logits(lt, ld, st[i].m, st[i].s, st[GM + 1 + i].m, st[GM + 1 + i].s, c, u);
                 }
             }
             const unsigned ball = __ballot_sync(0xffffffffu, fail);
@@ -831,19 +885,34 @@ struct Kern {
                                      : weight_target(token_at(vt, e), d);
     }
 
-    // Weight sum of the first `valid` tokens of a run, in index order.
-    __device__ static __forceinline__ float run_sum(const Run& vt, const Run& vd, int valid, const DrawParams& d,
-                                    int kind) {
-        float run = 0.0f;
+    // The weights of a run's tokens (0 past `valid`): independent of each
+    // other, so they are computed before the serial sum.
+    __device__ static __forceinline__ void run_weights(const Run& vt, const Run& vd, int valid, const DrawParams& d,
+                                                       int kind, float (&w)[kTPT]) {
         if (kind == kKindResidual) {
 #pragma unroll
-            for (int e = 0; e < kTPT; ++e)
-                if (e < valid) run = __fadd_rn(run, weight_residual(token_at(vt, e), token_at(vd, e), d));
+            for (int e = 0; e < kTPT; ++e) {
+                const float x = weight_residual(token_at(vt, e), token_at(vd, e), d);
+                w[e] = e < valid ? x : 0.0f;
+            }
         } else {
 #pragma unroll
-            for (int e = 0; e < kTPT; ++e)
-                if (e < valid) run = __fadd_rn(run, weight_target(token_at(vt, e), d));
+            for (int e = 0; e < kTPT; ++e) {
+                const float x = weight_target(token_at(vt, e), d);
+                w[e] = e < valid ? x : 0.0f;
+            }
         }
+    }
+
+    // Weight sum of the first `valid` tokens of a run, added in index order
+    // (adding the +0 weights past `valid` leaves the non-negative sum as is).
+    __device__ static __forceinline__ float run_sum(const Run& vt, const Run& vd, int valid, const DrawParams& d,
+                                    int kind) {
+        float w[kTPT];
+        run_weights(vt, vd, valid, d, kind, w);
+        float run = 0.0f;
+#pragma unroll
+        for (int e = 0; e < kTPT; ++e) run = __fadd_rn(run, w[e]);
         return run;
     }
 
@@ -857,14 +926,17 @@ struct Kern {
         uint4 raw[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) raw[k] = base[(k + r) & 3];  // raw[k] is vector (k + r) & 3
+        // rotate back by r: by 2 if r & 2, then by 1 if r & 1 (selects on constants)
+        const bool r2 = (r & 2) != 0, r1 = (r & 1) != 0;
+        uint4 m[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 a0 = raw[q], a1 = raw[(q + 3) & 3], a2 = raw[(q + 2) & 3], a3 = raw[(q + 1) & 3];
-            v[q].x = r == 0 ? a0.x : r == 1 ? a1.x : r == 2 ? a2.x : a3.x;
-            v[q].y = r == 0 ? a0.y : r == 1 ? a1.y : r == 2 ? a2.y : a3.y;
-            v[q].z = r == 0 ? a0.z : r == 1 ? a1.z : r == 2 ? a2.z : a3.z;
-            v[q].w = r == 0 ? a0.w : r == 1 ? a1.w : r == 2 ? a2.w : a3.w;
-        }
+        for (int q = 0; q < 4; ++q) m[q] = sel4(r2, raw[(q + 2) & 3], raw[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = sel4(r1, m[(q + 3) & 3], m[q]);
+    }
+
+    __device__ static __forceinline__ uint4 sel4(bool c, const uint4& a, const uint4& b) {
+        return make_uint4(c ? a.x : b.x, c ? a.y : b.y, c ? a.z : b.z, c ? a.w : b.w);
     }
 
     // A run from global memory starting at element `e` (64-byte aligned in the
@@ -924,8 +996,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     if (producer) {
         bool ok = true;
         auto issue = [&](const Segment& sg) {
-            for (long long off = 0; off < sg.elems && ok && !ctl.abort; off += KT::kChunkElems) {
-                const long long n = min(static_cast<long long>(KT::kChunkElems), sg.elems - off);
+            for (long long off = 0; off < sg.elems && ok && !ctl.abort; off += KT::kStageElems) {
+                const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
                 ok = K.produce(prod, sg.src + off * KT::ES, static_cast<unsigned>(n * KT::ES));
             }
         };
@@ -943,8 +1015,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             if (!ok) return;
             typename KT::RowState rs;
             K.start_row(rs, sg.loc);
-            for (long long off = 0; off < sg.elems; off += KT::kChunkElems) {
-                const long long n = min(static_cast<long long>(KT::kChunkElems), sg.elems - off);
+            for (long long off = 0; off < sg.elems; off += KT::kStageElems) {
+                const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
                 const char* sm = K.consume_begin(cons);
                 if (!sm) {
                     ok = false;
@@ -1049,10 +1121,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
             const unsigned bytes = static_cast<unsigned>(cnt * KT::ES);
             const long long trow = static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n;
-            ok = K.produce(prod, static_cast<const char*>(a.target) + (trow * a.V + e0) * KT::ES, bytes);
-            if (ok && jb.kind == kKindResidual) {
+            const char* src_t = static_cast<const char*>(a.target) + (trow * a.V + e0) * KT::ES;
+            if (jb.kind == kKindResidual) {
                 const long long drow = static_cast<long long>(jb.b) * a.gamma + jb.n;
-                ok = K.produce(prod, static_cast<const char*>(a.draft) + (drow * a.V + e0) * KT::ES, bytes);
+                ok = K.produce(prod, src_t, bytes, static_cast<const char*>(a.draft) + (drow * a.V + e0) * KT::ES,
+                               bytes);
+            } else {
+                ok = K.produce(prod, src_t, bytes);
             }
         });
         if (!ok) K.set_abort(a.d_status);
@@ -1074,16 +1149,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                 K.set_abort(a.d_status);
                 return;
             }
-            if (valid > 0) KT::load_run_smem(smt, t, lt);
-            if (jb.kind == kKindResidual) {
-                K.consume_end(cons);  // release the target stage once loaded
-                const char* smd = K.consume_begin(cons);
-                if (!smd) {
-                    ok = false;
-                    K.set_abort(a.d_status);
-                    return;
-                }
-                if (valid > 0) KT::load_run_smem(smd, t, ld);
+            if (valid > 0) {
+                KT::load_run_smem(smt, t, lt);
+                if (jb.kind == kKindResidual) KT::load_run_smem(smt + kChunkBytes, t, ld);
             }
             K.consume_end(cons);
             const float run = valid > 0 ? KT::run_sum(lt, ld, valid, jb.d, jb.kind) : 0.0f;
@@ -1231,16 +1299,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         const unsigned ball = __ballot_sync(0xffffffffu, mine);
         if (mine && lane == __ffs(ball) - 1) {
             // the first token of the run whose prefix passes tt
+            float w[TPT];
+            KT::run_weights(lt, ld, valid, d, kind, w);
             float r2 = 0.0f;
             int token = -1, last_pos = -1;
 #pragma unroll
             for (int e = 0; e < TPT; ++e) {
-                if (e < valid) {
-                    const float w = KT::run_weight(lt, ld, e, d, kind);
-                    r2 = __fadd_rn(r2, w);
-                    if (w > 0.0f) last_pos = e;
-                    if (token < 0 && start + to_fixed(r2, d.fix) > tt) token = e;
-                }
+                r2 = __fadd_rn(r2, w[e]);
+                if (w[e] > 0.0f) last_pos = e;
+                if (token < 0 && start + to_fixed(r2, d.fix) > tt) token = e;
             }
             if (token < 0) token = last_pos;
             a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.n] = static_cast<int>(e0) + vt * TPT + token;
@@ -1273,7 +1340,7 @@ bool streaming_applicable(const Args& a) {
     if ((static_cast<size_t>(a.V) * es) % 16 != 0) return false;
     if ((reinterpret_cast<uintptr_t>(a.target) & 15) || (reinterpret_cast<uintptr_t>(a.draft) & 15)) return false;
     if (a.B > kMaxB) return false;
-    if (static_cast<size_t>(a.V) * es > static_cast<size_t>(128) * kStageBytes) return false;  // <= 128 chunks per row
+    if (static_cast<size_t>(a.V) * es > static_cast<size_t>(128) * kChunkBytes) return false;  // <= 128 chunks per row
     return true;
 }
 
