@@ -41,9 +41,9 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ float temp_scale(float T) {
-    return __double2float_rn(kLog2e / static_cast<double>(T));
-}
+// c = log2(e) / T, one correctly rounded binary32 division of the binary32
+// log2(e) (no FP64 on the hot path: FP64 is a small fraction of FP32 here).
+__device__ __forceinline__ float temp_scale(float T) { return __fdiv_rn(1.44269504088896340736f, T); }
 
 __device__ __forceinline__ float bf16_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 __device__ __forceinline__ float bf16x2_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -139,9 +139,16 @@ __device__ __forceinline__ bool accept_from_logits(float lt, float ld, float mp,
                                                    float c, float u) {
     if (lt == neg_inf()) return false;  // p(x) = 0 < alpha requires p(x) > 0
     if (ld == neg_inf() || u == 0.0f) return true;
-    const double e = (static_cast<double>(lt) - static_cast<double>(ld)) * static_cast<double>(c) -
-                     (static_cast<double>(scaled_max(mp, c)) - static_cast<double>(scaled_max(mq, c)));
-    const float alpha = __fmul_rn(ex2(__double2float_rn(e)), __fdiv_rn(sq, sp));
+    // e with error-free transformations in binary32: d = lt - ld and
+    // m = fl(mp c) - fl(mq c) as two-sums, d * c as a two-product
+    const float d = __fsub_rn(lt, ld);
+    const float dz = __fsub_rn(d, lt), d_lo = __fadd_rn(__fsub_rn(lt, __fsub_rn(d, dz)), __fsub_rn(-ld, dz));
+    const float mcp = scaled_max(mp, c), mcq = scaled_max(mq, c);
+    const float m = __fsub_rn(mcp, mcq);
+    const float mz = __fsub_rn(m, mcp), m_lo = __fadd_rn(__fsub_rn(mcp, __fsub_rn(m, mz)), __fsub_rn(-mcq, mz));
+    const float p_hi = __fmul_rn(d, c), p_lo = __fmaf_rn(d, c, -p_hi);
+    const float e = __fadd_rn(__fsub_rn(p_hi, m), __fsub_rn(__fmaf_rn(d_lo, c, p_lo), m_lo));
+    const float alpha = __fmul_rn(ex2(e), __fdiv_rn(sq, sp));
     return u < alpha;
 }
 
@@ -187,6 +194,20 @@ __device__ __forceinline__ float weight_residual(float lt, float ld, const DrawP
     const float p = __fmul_rn(row_term(lt, d.c, d.mcp), d.isp);
     const float q = __fmul_rn(row_term(ld, d.c, d.mcq), d.isq);
     return fmaxf(__fsub_rn(p, q), 0.0f);
+}
+
+// floor(u * total) exactly, for u in [0, 1): u = M 2^e with an integer M < 2^24,
+// so the product is a 128-bit integer shifted right by -e.
+__device__ __forceinline__ unsigned long long scale_uniform(float u, unsigned long long total) {
+    const uint32_t bits = __float_as_uint(u);
+    const uint32_t ex = (bits >> 23) & 0xffu;
+    if (u <= 0.0f || total == 0ull) return 0ull;
+    const unsigned long long M = ex ? ((bits & 0x7fffffu) | 0x800000u) : (bits & 0x7fffffu);
+    const int shift = 150 - static_cast<int>(ex ? ex : 1);  // u = M 2^-shift
+    const unsigned long long lo = total * M, hi = __umul64hi(total, M);
+    if (shift >= 128) return 0ull;
+    if (shift >= 64) return hi >> (shift - 64);
+    return (hi << (64 - shift)) | (lo >> shift);
 }
 
 __device__ __forceinline__ unsigned long long to_fixed(float run_sum, float fix) {

@@ -248,11 +248,11 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                 DrawParams d;
                 d.c = c;
                 d.mcp = scaled_max(sh.st[n].m, c);
-                d.isp = __double2float_rn(1.0 / static_cast<double>(sh.st[n].s));
+                d.isp = __frcp_rn(sh.st[n].s);
                 if (n < G) {
                     d.kind = kKindResidual;
                     d.mcq = scaled_max(sh.st[G + 1 + n].m, c);
-                    d.isq = __double2float_rn(1.0 / static_cast<double>(sh.st[G + 1 + n].s));
+                    d.isq = __frcp_rn(sh.st[G + 1 + n].s);
                     d.fix = kFixResidual;
                 } else {
                     d.kind = kKindBonus;
@@ -289,8 +289,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                 qv = to_fixed(run, d.fix);
                 excl = block_excl_scan_u64<kThreads>(qv, sh.scan, &total);
             }
-            const unsigned long long t =
-                __double2ull_rz(static_cast<double>(a.u_sample[b]) * static_cast<double>(total));
+            const unsigned long long t = scale_uniform(a.u_sample[b], total);
             if (excl <= t && t < excl + qv) {
                 float run2 = 0.0f;
                 int token = hi - 1;

@@ -51,6 +51,7 @@ constexpr int kMaxGrid = 256;  // blocks (partition tables live in shared memory
 constexpr int kJobCache = 64;  // draw jobs cached per block in phase 3
 constexpr int kMaxB = 4096;
 constexpr int kMaxRowsPerReq = 2 * SV_MAX_GAMMA + 1;
+constexpr int kFlushSlots = 16;  // row pieces in flight between the fastest and slowest warp
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
 // Named barriers (0 is __syncthreads).
@@ -103,8 +104,8 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     };
     L.hdr = take(256);
     L.prefix = take(static_cast<size_t>(B) * 4);
-    L.rec_t = take(static_cast<size_t>(G) * L.MT * kConsumerWarps * sizeof(Rec));
-    L.rec_d = take(static_cast<size_t>(G) * L.MD * kConsumerWarps * sizeof(Rec));
+    L.rec_t = take(static_cast<size_t>(G) * L.MT * sizeof(Rec));
+    L.rec_d = take(static_cast<size_t>(G) * L.MD * sizeof(Rec));
     L.jobs = take(static_cast<size_t>(B) * sizeof(Job));
     L.wsums = take(static_cast<size_t>(B) * L.NCH * kConsumerWarps * 8);
     L.total = off;
@@ -289,6 +290,8 @@ struct Ctl {
     int flag;
     int map[kMapMax];
     int wtmp[kConsumerWarps + 1];
+    Rec wrec[kFlushSlots][kConsumerWarps];  // per-warp partials of a row piece
+    int wcnt[kFlushSlots];                  // warps that have flushed the piece
 };
 
 struct RowLoc {
@@ -505,7 +508,11 @@ struct Kern {
         rs.bad = 0;
     }
 
-    __device__ void flush_row(const RowState& rs, const RowLoc& loc) const {
+    // The warps of a block fold disjoint parts of each row piece. Each warp
+    // reduces its lanes, parks the result in shared slot `seq % kFlushSlots`,
+    // and the last warp to arrive merges the 8 partials in warp order and
+    // writes the block's record for the piece (no block-wide barrier).
+    __device__ void flush_row(const RowState& rs, const RowLoc& loc, unsigned seq) const {
         const int bad = __any_sync(0xffffffffu, rs.bad);
         Rec rec;
         if (rs.argmax) {
@@ -527,10 +534,30 @@ struct Kern {
         }
         if ((threadIdx.x & 31) == 0) {
             const int warp = threadIdx.x >> 5;
-            Rec* dst = loc.kind == 0
-                           ? rec_t() + ((static_cast<size_t>(g) * L.MT + loc.slot) * kConsumerWarps + warp)
-                           : rec_d() + ((static_cast<size_t>(g) * L.MD + loc.slot) * kConsumerWarps + warp);
-            *dst = rec;
+            const int fs = static_cast<int>(seq % kFlushSlots);
+            ctl.wrec[fs][warp] = rec;
+            __threadfence_block();
+            if (atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1) {
+                __threadfence_block();
+                Rec out = ctl.wrec[fs][0];
+                for (int w = 1; w < kConsumerWarps; ++w) {
+                    const Rec x = ctl.wrec[fs][w];
+                    out.bad |= x.bad;
+                    if (rs.argmax) {
+                        const ArgMax m = argmax_merge(ArgMax{out.m, out.idx}, ArgMax{x.m, x.idx});
+                        out.m = m.v;
+                        out.idx = m.i;
+                    } else {
+                        const MaxSum m = maxsum_merge(MaxSum{out.m, out.s}, MaxSum{x.m, x.s}, rs.c);
+                        out.m = m.m;
+                        out.s = m.s;
+                    }
+                }
+                ctl.wcnt[fs] = 0;
+                Rec* dst = loc.kind == 0 ? rec_t() + (static_cast<size_t>(g) * L.MT + loc.slot)
+                                         : rec_d() + (static_cast<size_t>(g) * L.MD + loc.slot);
+                *dst = out;
+            }
         }
     }
 
@@ -643,21 +670,30 @@ struct Kern {
         MaxSum ms = maxsum_empty();
         ArgMax am = argmax_empty();
         int bad = 0;
-        for (int gg = g0; gg <= g1; ++gg) {
-            const long long b0 = beg[gg], b1 = beg[gg + 1];
-            if (b1 <= b0) continue;
-            const int slot = static_cast<int>(row - b0 / a.V);
-            const uint4* r =
-                reinterpret_cast<const uint4*>(base + (static_cast<size_t>(gg) * MM + slot) * kConsumerWarps);
-            uint4 x[kConsumerWarps];  // all loads issued before the merges
+        constexpr int kBatch = 4;  // piece records loaded before they are merged
+        for (int gb = g0; gb <= g1; gb += kBatch) {
+            uint4 x[kBatch];
+            bool use[kBatch];
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) x[w] = __ldcg(r + w);
+            for (int q = 0; q < kBatch; ++q) {
+                const int gg = gb + q;
+                use[q] = false;
+                if (gg <= g1) {
+                    const long long b0 = beg[gg], b1 = beg[gg + 1];
+                    if (b1 > b0) {
+                        const int slot = static_cast<int>(row - b0 / a.V);
+                        x[q] = __ldcg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(gg) * MM + slot));
+                        use[q] = true;
+                    }
+                }
+            }
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float m = __uint_as_float(x[w].x), s = __uint_as_float(x[w].y);
-                bad |= static_cast<int>(x[w].w);
+            for (int q = 0; q < kBatch; ++q) {
+                if (!use[q]) continue;
+                const float m = __uint_as_float(x[q].x), s = __uint_as_float(x[q].y);
+                bad |= static_cast<int>(x[q].w);
                 if (argmax)
-                    am = argmax_merge(am, ArgMax{m, static_cast<int32_t>(x[w].z)});
+                    am = argmax_merge(am, ArgMax{m, static_cast<int32_t>(x[q].z)});
                 else
                     ms = maxsum_merge(ms, MaxSum{m, s}, c);
             }
@@ -797,15 +833,15 @@ struct Kern {
                 Job j;
                 j.b = b;
                 j.n = n;
-                j.pad = 0;
+                j.pad = __float_as_int(a.u_sample[b]);  // the draw's uniform
                 DrawParams& d = j.d;
                 d.c = c;
                 d.mcp = scaled_max(st[n].m, c);
-                d.isp = __double2float_rn(1.0 / static_cast<double>(st[n].s));
+                d.isp = __frcp_rn(st[n].s);
                 if (n < GM) {
                     d.kind = kKindResidual;
                     d.mcq = scaled_max(st[GM + 1 + n].m, c);
-                    d.isq = __double2float_rn(1.0 / static_cast<double>(st[GM + 1 + n].s));
+                    d.isq = __frcp_rn(st[GM + 1 + n].s);
                     d.fix = kFixResidual;
                 } else {
                     d.kind = kKindBonus;
@@ -987,6 +1023,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     for (int i = t; i < kMapMax; i += kThreads) ctl.map[i] = -1;
+    for (int i = t; i < kFlushSlots; i += kThreads) ctl.wcnt[i] = 0;
     __syncthreads();
 
     const long long ts = part_begin(L.Et, K.G, K.g, L.vec), te = part_begin(L.Et, K.G, K.g + 1, L.vec);
@@ -1011,6 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         K.prologue();
         bar_arrive(kBarHandoff, kThreads);
         bool ok = true;
+        unsigned seq = 0;  // row pieces folded so far (the same on every consumer warp)
         auto fold = [&](const Segment& sg) {
             if (!ok) return;
             typename KT::RowState rs;
@@ -1026,7 +1064,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                 K.fold_stage(rs, sm, static_cast<int>(n * KT::ES / 16), sg.e0 + off);
                 K.consume_end(cons);
             }
-            K.flush_row(rs, sg.loc);
+            K.flush_row(rs, sg.loc, seq++);
         };
         K.for_each_target_segment(ts, te, fold);
         K.for_each_draft_segment(fold);
@@ -1169,29 +1207,36 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     const Job* gjobs = K.jobs();
     const unsigned long long* wsums = K.wsums();
     for (int k = warp * gridDim.x + blockIdx.x; k < ns; k += gridDim.x * kConsumerWarps) {
+        const unsigned long long* js = wsums + static_cast<size_t>(k) * L.NCH * kConsumerWarps;
+        // this lane's chunk totals (lane j holds chunks j, j+32, ...; NCH <= 128),
+        // loaded together with the job: they depend on k only
+        const int nch_lane = (L.NCH + 31) / 32;
+        unsigned long long ctot[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int j = h * 32 + lane;
+            unsigned long long sum = 0;
+            if (h < nch_lane && j < L.NCH) {
+                const ulonglong2* p = reinterpret_cast<const ulonglong2*>(js + static_cast<size_t>(j) * kConsumerWarps);
+#pragma unroll
+                for (int hh = 0; hh < kConsumerWarps / 2; ++hh) {
+                    const ulonglong2 x = __ldcg(p + hh);
+                    sum += x.x + x.y;
+                }
+            }
+            ctot[h] = sum;
+        }
         const Job jb = gjobs[k];
         if (jb.kind != kKindResidual && jb.kind != kKindBonus) continue;
         DrawParams d = jb.d;
         int kind = jb.kind;
         const long long trow = (static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n) * a.V;
         const long long drow = (static_cast<long long>(jb.b) * a.gamma + jb.n) * a.V;
-        const unsigned long long* js = wsums + static_cast<size_t>(k) * L.NCH * kConsumerWarps;
         // per-warp sums of chunk j (from phase 3a, or recomputed on the fallback)
         bool fallback = false;
         auto warp_part = [&](int j, int w) -> unsigned long long {
             if (!fallback) return js[static_cast<size_t>(j) * kConsumerWarps + w];
             return warp_sum_u64(K.run_fixed_global(trow, drow, j, w * 32 + lane, d, kind));
-        };
-        // total of chunk j, computed by the calling lane alone (phase-3a sums)
-        auto chunk_total_lane = [&](int j) -> unsigned long long {
-            const ulonglong2* p = reinterpret_cast<const ulonglong2*>(js + static_cast<size_t>(j) * kConsumerWarps);
-            unsigned long long s = 0;
-#pragma unroll
-            for (int h = 0; h < kConsumerWarps / 2; ++h) {
-                const ulonglong2 x = p[h];
-                s += x.x + x.y;
-            }
-            return s;
         };
         // total of chunk j on the fallback, computed by the whole warp
         auto chunk_total_warp = [&](int j) -> unsigned long long {
@@ -1199,15 +1244,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             for (int w = 0; w < kConsumerWarps; ++w) s += warp_part(j, w);
             return s;
         };
-        const int nch_lane = (L.NCH + 31) / 32;  // chunks per lane
-        unsigned long long ctot[4];               // this lane's chunk totals (NCH <= 128 here)
         unsigned long long total = 0;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int j = h * 32 + lane;
-            ctot[h] = (h < nch_lane && j < L.NCH) ? chunk_total_lane(j) : 0ull;
-            total += ctot[h];
-        }
+        for (int h = 0; h < 4; ++h) total += ctot[h];
         total = warp_sum_u64(total);
         if (total == 0ull) {
             // residual weights rounded to zero everywhere: draw from p_n
@@ -1230,7 +1269,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             }
         }
         const unsigned long long tt =
-            __double2ull_rz(static_cast<double>(a.u_sample[jb.b]) * static_cast<double>(total));
+            scale_uniform(__int_as_float(jb.pad), total);
         unsigned long long before = 0;
         int jsel = -1;
 #pragma unroll
