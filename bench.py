@@ -64,6 +64,21 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed_k(rank: int) -> int:
+    """Weak scaling: rank r verifies its own batch, seeded 1000 * config + r."""
+    return rank
+
+
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's time (all ranks get it); x itself without a group."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peak_hbm():
     try:
         with open(PEAKS) as f:
@@ -226,7 +241,7 @@ def main():
     sv.build.build()
     sv.load()
 
-    batch = synthetic.generate(w, k=rank)
+    batch = synthetic.generate(w, k=rank_seed_k(rank))
     dev = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in batch.arrays()]
     B, G, V = batch.B, w.gamma, w.V
     dt = sv.SV_F32 if w.dtype == "f32" else sv.SV_BF16
@@ -272,9 +287,7 @@ def main():
     total_ms = t_begin.elapsed_time(t_end)
     per_call_ms = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
     if dist:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = max_over_ranks(total_ms, dist, "cuda")
     rows_per_step = B * (G + 1)
     value = world * K * rows_per_step / (total_ms * 1e-3)
 
@@ -314,9 +327,7 @@ def main():
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1)
         if dist:
-            tt = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+            e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
         es = w.elem_bytes
         samp = int((batch.temperature > 0).sum())
         h2d = B * (G + 1) * V * es + samp * G * V * es + B * G * 8 + B * 8

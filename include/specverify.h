@@ -152,7 +152,12 @@ typedef struct {
     int32_t grid_ctas; /* streaming path: thread blocks in the persistent grid; 0 = the
                           device's full co-resident grid. Smaller grids split rows over
                           fewer blocks (used by tests to exercise every split). */
-    int32_t reserved[6];
+    int32_t barrier_wait_us; /* streaming path: limit of each grid-barrier wait, in
+                                microseconds; 0 = the default (about 2 s). A block whose
+                                wait runs out sets SV_STATUS_TIMEOUT and returns (no copy
+                                is in flight at a barrier); the call's outputs are then
+                                not valid. A tiny value exercises that report. */
+    int32_t reserved[5];
 } sv_options;
 
 /* spec_verify with checking outputs and options. `dbg`, `d_status` and

@@ -48,7 +48,7 @@ class _Debug(ctypes.Structure):
 
 class _Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 6)]
+                ("barrier_wait_us", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
 
 
 _lib = None
@@ -149,7 +149,7 @@ def _ptr(t) -> int:
 def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature,
                 out_tokens=None, out_num_accepted=None, workspace=None, stream=None,
                 debug: bool = False, path: int = SV_PATH_AUTO, grid_ctas: int = 0,
-                status=None) -> Outputs:
+                status=None, barrier_wait_us: int = 0) -> Outputs:
     """Verify one batch of CUDA tensors (see include/specverify.h).
 
     ``target_logits`` [B, gamma+1, V] and ``draft_logits`` [B, gamma, V]
@@ -179,7 +179,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
             _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
             _ptr(out_num_accepted), _ptr(workspace), workspace.numel() * workspace.element_size(), s)
     dbg = None
-    if debug or path != SV_PATH_AUTO or grid_ctas or status is not None:
+    if debug or path != SV_PATH_AUTO or grid_ctas or status is not None or barrier_wait_us:
         d = _Debug()
         if debug:
             f64, f32, i32 = torch.float64, torch.float32, torch.int32
@@ -198,7 +198,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
             dbg["phase_ns"][0] = -1  # UINT64_MAX
             for k, v in dbg.items():
                 setattr(d, k, v.data_ptr())
-        o = _Options(path, grid_ctas)
+        o = _Options(path, grid_ctas, barrier_wait_us)
         rc = lib.spec_verify_ex(*args, ctypes.byref(d), _ptr(status), ctypes.byref(o))
         _check(rc, "spec_verify_ex")
     else:

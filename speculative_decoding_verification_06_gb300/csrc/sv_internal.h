@@ -24,6 +24,7 @@ struct Args {
     int32_t* out_num_accepted;  // [B]
     sv_debug_out dbg;           // device pointers, each may be null
     int32_t* d_status;          // may be null
+    unsigned long long barrier_wait_ns;  // streaming path: limit of each grid-barrier wait
 };
 
 struct DeviceInfo {

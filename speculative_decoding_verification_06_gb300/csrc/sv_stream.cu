@@ -231,7 +231,7 @@ struct Hdr {
 
 // Grid-wide barrier of the co-resident grid; false (and SV_STATUS_TIMEOUT)
 // when the other blocks do not arrive within the time limit.
-__device__ bool grid_sync(Hdr* h, int32_t* d_status, int* s_flag) {
+__device__ bool grid_sync(Hdr* h, int32_t* d_status, int* s_flag, unsigned long long wait_ns) {
     __syncthreads();
     if (threadIdx.x == 0) {
         volatile unsigned* vgen = &h->gen;
@@ -246,7 +246,7 @@ __device__ bool grid_sync(Hdr* h, int32_t* d_status, int* s_flag) {
         } else {
             const unsigned long long t0 = global_ns();
             while (*vgen == my_gen) {
-                if (global_ns() - t0 > kWaitTimeoutNs) {
+                if (global_ns() - t0 > wait_ns) {
                     ok = 0;
                     atomicOr(&h->status, SV_STATUS_TIMEOUT);
                     if (d_status) atomicOr(d_status, SV_STATUS_TIMEOUT);
@@ -1072,7 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     __syncthreads();
     stamp(ph, 2);
     Hdr* hdr = K.hdr();
-    if (!grid_sync(hdr, a.d_status, &ctl.flag)) return;
+    if (!grid_sync(hdr, a.d_status, &ctl.flag, a.barrier_wait_ns)) return;
     stamp(ph, 3);
     if (ctl.abort) return;
 
@@ -1092,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         stamp(ph, 9);
         return;
     }
-    if (!grid_sync(hdr, a.d_status, &ctl.flag)) return;
+    if (!grid_sync(hdr, a.d_status, &ctl.flag, a.barrier_wait_ns)) return;
     stamp(ph, 5);
 
     // -------------------------------------------------------------- phase 3a
@@ -1199,7 +1199,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     }
     __syncthreads();
     stamp(ph, 6);
-    if (!grid_sync(hdr, a.d_status, &ctl.flag)) return;
+    if (!grid_sync(hdr, a.d_status, &ctl.flag, a.barrier_wait_ns)) return;
     stamp(ph, 7);
     if (ctl.abort || producer) return;
 
