@@ -138,11 +138,14 @@ typedef struct {
     int32_t* kind;          /* [B] -1 invalid, 0 greedy, 1 residual draw, 2 extra-token draw */
     uint64_t* phase_ns;     /* [SV_PHASE_SLOTS] streaming path only: global-timer stamps
                                (ns). Slot 0 is the earliest block start and slot 1 the
-                               latest; slots 2..9 are the latest time over all blocks at
-                               which each block finished: phase 1 stream, grid barrier 1,
-                               phase 2, barrier 2, phase 3 stream, barrier 3, phase 3
-                               search, kernel. The caller fills slot 0 with UINT64_MAX and
-                               the others with 0 before the call. */
+                               latest; slots 2..7 and 9 are the latest time over all
+                               blocks at which: 2 the row-statistics stream ended, 3 the
+                               last acceptance scan ended, 4 the grid barrier was passed,
+                               5 the draw schedule was built, 6 the draw stream ended,
+                               7 the last token search ended, 9 the block ended. Slot 8 is
+                               not written. Slots 4..7 stay untouched when no request has
+                               T > 0. The caller fills slot 0 with UINT64_MAX and the
+                               others with 0 before the call. */
 } sv_debug_out;
 
 #define SV_PHASE_SLOTS 10

@@ -5,31 +5,37 @@
 // and eq. p_corr; "Accélérer Sonar grâce à la spéculation", §Décodage
 // spéculatif) needs, per request, the normaliser (or argmax) of gamma+1
 // target rows and gamma draft rows, a left-to-right scan, and one draw over a
-// row that is known only after the scan. The kernel runs that as three phases
-// separated by grid barriers:
+// row that is known only after the scan. Each block has eight consumer warps,
+// one producer warp and one finisher warp, and the kernel runs two streaming
+// phases with one grid barrier between them (none when no request samples):
 //
 //  1. Row statistics. The target rows of all requests, then the draft rows of
 //     the T > 0 requests (compacted), form one virtual stream of logits that
-//     is cut into G equal 16-byte-aligned slices, one per thread block. A
-//     producer warp copies its slice through a ring of kStages shared-memory
-//     stages with cp.async.bulk (completion on mbarriers); eight consumer warps
-//     fold each stage into per-thread (max, sum of 2^(l c - fl(m c))) or argmax
-//     states. At the end of each row piece every warp writes its partial
-//     result; there is no block-wide barrier inside the stream.
-//  2. Acceptance scan. One warp per request merges the pieces of its rows in
-//     a fixed order, evaluates p(x_i) and q(x_i) in double, finds the first
-//     rejection, writes the accepted tokens and a draw job.
-//  3. Draw. The rows the draws need (target row n and draft row n for a
+//     is cut into G equal 16-byte-aligned slices, one per thread block. The
+//     producer copies its slice through a ring of kStages shared-memory
+//     stages with cp.async.bulk (completion on mbarriers); the consumers fold
+//     each stage into per-thread (max, sum of 2^(l c - fl(m c))) or argmax
+//     states, and the last warp to finish a row piece writes the block's
+//     record for it. When a block's share of a request's rows is written, a
+//     consumer posts it to the finisher; the finisher adds it to the
+//     request's global count of folded logits, and the block that completes
+//     the count runs the request's acceptance scan at once, while the other
+//     blocks are still streaming: it merges the pieces of each row in a fixed
+//     order, finds the first rejection, writes the accepted tokens and a draw
+//     job.
+//  2. Draw. The rows the draws need (target row n and draft row n for a
 //     residual, target row gamma for the extra token) are streamed again in
-//     chunks of one stage; each thread sums the weights of a run of
+//     chunks of kChunkBytes; each thread sums the weights of a run of
 //     consecutive tokens and each warp stores the sum of its 32 runs as a
 //     64-bit fixed-point integer (exact, so any order of addition gives the
-//     same prefix sums). After a grid barrier one warp per job finds the
-//     chunk, then the warp, then the run holding u * W, re-reads those 32
-//     runs and finds the token.
+//     same prefix sums). A block's share of a job is counted the same way,
+//     and the finisher of the block that completes a job finds the chunk,
+//     then the warp, then the run holding u * W, re-reads those 32 runs and
+//     finds the token.
 //
-// Every wait is bounded (about two seconds, by the global timer): a barrier or
-// a stage that never completes sets SV_STATUS_TIMEOUT and the kernel returns.
+// Every wait is bounded (about two seconds, by the global timer): a barrier,
+// a stage or a message that never comes sets SV_STATUS_TIMEOUT and the kernel
+// returns.
 #include <algorithm>
 #include <cmath>
 
@@ -41,14 +47,18 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
+constexpr int kProducerWarp = kConsumerWarps;      // issues the bulk copies
+constexpr int kFinisherWarp = kConsumerWarps + 1;  // acceptance scans and token searches
+constexpr int kThreads = kConsumers + 64;
+constexpr int kHandoffThreads = kConsumers + 32;   // consumers + producer
+constexpr int kQueue = 256;                        // finisher message ring (slots)
 constexpr int kStages = 4;
 constexpr int kStageBytes = 32768;
 constexpr int kVecPerThread = kStageBytes / 16 / kConsumers;  // 8
-constexpr int kChunkBytes = 16384;  // phase-3 chunk of one row (a residual item fills a stage)
+constexpr int kChunkBytes = 16384;  // draw-phase chunk of one row (a residual item fills a stage)
 constexpr int kMapMax = 256;   // compacted requests in one block's draft slice
 constexpr int kMaxGrid = 256;  // blocks (partition tables live in shared memory)
-constexpr int kJobCache = 64;  // draw jobs cached per block in phase 3
+constexpr int kJobCache = 64;  // draw jobs cached per block in the draw phase
 constexpr int kMaxB = 4096;
 constexpr int kMaxRowsPerReq = 2 * SV_MAX_GAMMA + 1;
 constexpr int kFlushSlots = 16;  // row pieces in flight between the fastest and slowest warp
@@ -56,7 +66,7 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 
 // Named barriers (0 is __syncthreads).
 constexpr int kBarConsumers = 1;  // the 256 consumer threads
-constexpr int kBarHandoff = 2;    // consumers arrive, producer waits (288)
+constexpr int kBarHandoff = 2;    // consumers arrive, producer waits (kHandoffThreads)
 
 struct Rec {
     float m;      // max value (both modes)
@@ -74,7 +84,7 @@ struct Job {
 struct Layout {
     long long Et;  // target elements B*(gamma+1)*V
     int G, MT, MD, NCH, vec;
-    size_t hdr, prefix, rec_t, rec_d, jobs, wsums, total;
+    size_t hdr, req_done, job_done, clear_bytes, rec_t, rec_d, jobs, wsums, total;
 };
 
 __host__ __device__ inline long long part_begin(long long E, int G, int g, int vec) {
@@ -103,7 +113,9 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
         return at;
     };
     L.hdr = take(256);
-    L.prefix = take(static_cast<size_t>(B) * 4);
+    L.req_done = take(static_cast<size_t>(B) * 4);  // logits folded, per request
+    L.job_done = take(static_cast<size_t>(B) * 4);  // chunks summed, per draw job
+    L.clear_bytes = off;                            // cleared before every launch
     L.rec_t = take(static_cast<size_t>(G) * L.MT * sizeof(Rec));
     L.rec_d = take(static_cast<size_t>(G) * L.MD * sizeof(Rec));
     L.jobs = take(static_cast<size_t>(B) * sizeof(Job));
@@ -263,8 +275,8 @@ __device__ bool grid_sync(Hdr* h, int32_t* d_status, int* s_flag, unsigned long 
 }
 
 // Checking output: global-timer stamps (see sv_debug_out.phase_ns).
-__device__ __forceinline__ void stamp(unsigned long long* slots, int i) {
-    if (slots && threadIdx.x == 0) {
+__device__ __forceinline__ void stamp(unsigned long long* slots, int i, bool who) {
+    if (slots && who) {
         const unsigned long long now = global_ns();
         if (i == 0) {
             atomicMin(slots, now);
@@ -282,7 +294,7 @@ struct Ctl {
     uint64_t empty[kStages];
     long long tbeg[kMaxGrid + 1];  // target partition
     long long dbeg[kMaxGrid + 1];  // draft partition (after the prologue)
-    Job jobs[kJobCache];           // phase 3: this block's draw jobs
+    Job jobs[kJobCache];           // draw phase: this block's draw jobs
     int n_samp;
     int k_lo;  // first compacted request of this block's draft slice
     int job_lo, job_n;
@@ -292,6 +304,13 @@ struct Ctl {
     int wtmp[kConsumerWarps + 1];
     Rec wrec[kFlushSlots][kConsumerWarps];  // per-warp partials of a row piece
     int wcnt[kFlushSlots];                  // warps that have flushed the piece
+    int fq_item[kQueue];                    // finisher ring: request (phase 1) or job (phase 2)
+    unsigned fq_val[kQueue];                // logits (phase 1) or chunks (phase 2) it covers
+    unsigned fq_seq[kQueue];                // reservation number + 1 of the entry in the slot
+    unsigned fq_tail;                       // reservations so far
+    unsigned fq_head;                       // entries the finisher has taken
+    int cons_done[2];                       // consumer warps done with phase 1, phase 2
+    short kmap[kMaxB];                      // compacted index of each T > 0 request, else -1
 };
 
 struct RowLoc {
@@ -307,6 +326,7 @@ struct Segment {
     long long elems;
     long long e0;  // first element, offset within the row
     RowLoc loc;
+    bool last;     // the last piece of this request's rows in the slice
 };
 
 // Largest g with beg[g] <= e (beg non-decreasing, beg[0] = 0 <= e < beg[G]).
@@ -326,7 +346,7 @@ template <int DT>
 struct Kern {
     static constexpr int ES = DT == SV_F32 ? 4 : 2;
     static constexpr int kStageElems = kStageBytes / ES;  // phase-1 stage
-    static constexpr int kChunkElems = kChunkBytes / ES;  // phase-3 chunk
+    static constexpr int kChunkElems = kChunkBytes / ES;  // draw-phase chunk
     static constexpr int kTPT = kChunkElems / kConsumers;  // tokens per thread run (64 bytes)
 
     const Args& a;
@@ -337,10 +357,11 @@ struct Kern {
     int G, g;
 
     __device__ Hdr* hdr() const { return reinterpret_cast<Hdr*>(ws + L.hdr); }
-    __device__ int* prefix() const { return reinterpret_cast<int*>(ws + L.prefix); }
     __device__ Rec* rec_t() const { return reinterpret_cast<Rec*>(ws + L.rec_t); }
     __device__ Rec* rec_d() const { return reinterpret_cast<Rec*>(ws + L.rec_d); }
     __device__ Job* jobs() const { return reinterpret_cast<Job*>(ws + L.jobs); }
+    __device__ unsigned* req_done() const { return reinterpret_cast<unsigned*>(ws + L.req_done); }
+    __device__ unsigned* job_done() const { return reinterpret_cast<unsigned*>(ws + L.job_done); }
     __device__ unsigned long long* wsums() const {
         return reinterpret_cast<unsigned long long*>(ws + L.wsums);
     }
@@ -360,6 +381,7 @@ struct Kern {
             sg.elems = end - e;
             sg.e0 = e - r * V;
             sg.loc = {0, r, static_cast<int>(r / (GM + 1)), static_cast<int>(r - first)};
+            sg.last = end == te || (r + 1) % (GM + 1) == 0;
             f(sg);
             e = end;
         }
@@ -386,6 +408,7 @@ struct Kern {
             sg.elems = end - e;
             sg.e0 = e - kr * V;
             sg.loc = {1, kr, b, static_cast<int>(kr - first)};
+            sg.last = end == de || (kr + 1) % GM == 0;
             f(sg);
             e = end;
         }
@@ -439,6 +462,100 @@ struct Kern {
         if (d_status) atomicOr(d_status, SV_STATUS_TIMEOUT);
     }
 
+    // ---- the finisher's message ring. One consumer lane posts a message once
+    // this block's share of a request (phase 1) or of a draw job (phase 2) is
+    // in global memory; the finisher warp adds the share to the item's global
+    // counter, and the block whose share completes the item finishes it. The
+    // consumers never wait on a global atomic or fence.
+    //
+    // Posts (one lane): false if the ring stayed full for the time limit.
+    __device__ bool post(int item, unsigned val) const {
+        const unsigned s = atomicAdd(&ctl.fq_tail, 1u);
+        volatile unsigned* vhead = &ctl.fq_head;
+        volatile int* vabort = &ctl.abort;
+        if (s - *vhead >= static_cast<unsigned>(kQueue)) {
+            const unsigned long long t0 = global_ns();
+            while (s - *vhead >= static_cast<unsigned>(kQueue)) {
+                if (*vabort || global_ns() - t0 > kWaitTimeoutNs) return false;
+                __nanosleep(128);
+            }
+        }
+        const int i = static_cast<int>(s % kQueue);
+        ctl.fq_item[i] = item;
+        ctl.fq_val[i] = val;
+        __threadfence_block();  // the entry, then its sequence number
+        reinterpret_cast<volatile unsigned*>(ctl.fq_seq)[i] = s + 1;
+        return true;
+    }
+
+    // A consumer warp is done with phase `ph` (after its last post).
+    __device__ void consumer_done(int ph) const {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) {
+            __threadfence_block();
+            atomicAdd(&ctl.cons_done[ph], 1);
+        }
+    }
+
+    // Finisher warp: takes the ring's messages in batches of up to 32 until
+    // every consumer warp is done with phase `ph` and the ring is empty.
+    // count(item, val), one lane per message, adds the share to the item's
+    // global counter and returns whether that completed the item;
+    // work(item), on the whole warp, then finishes each completed item.
+    template <typename C, typename W>
+    __device__ void finish(unsigned& head, int ph, C&& count, W&& work) const {
+        const int lane = threadIdx.x & 31;
+        volatile unsigned* vseq = ctl.fq_seq;
+        volatile int* vdone = ctl.cons_done;
+        volatile int* vabort = &ctl.abort;
+        unsigned long long t0 = global_ns();
+        for (;;) {
+            const unsigned s = head + lane;
+            const unsigned ready = __ballot_sync(0xffffffffu, vseq[s % kQueue] == s + 1);
+            const int n = ready == 0xffffffffu ? 32 : __ffs(~ready) - 1;  // ready entries from head on
+            if (n > 0) {
+                __threadfence_block();
+                int item = -1;
+                unsigned val = 0;
+                if (lane < n) {
+                    item = ctl.fq_item[s % kQueue];
+                    val = ctl.fq_val[s % kQueue];
+                }
+                __syncwarp();
+                head += n;
+                if (lane == 0) *reinterpret_cast<volatile unsigned*>(&ctl.fq_head) = head;
+                bool completed = false;
+                if (lane < n) {
+                    __threadfence();  // this block's share is visible before it is counted
+                    completed = count(item, val);
+                    __threadfence();  // and the other blocks' shares before they are read
+                }
+                unsigned done = __ballot_sync(0xffffffffu, completed);
+                while (done) {
+                    const int src = __ffs(done) - 1;
+                    done &= done - 1;
+                    work(__shfl_sync(0xffffffffu, item, src));
+                    __syncwarp();
+                }
+                t0 = global_ns();
+                continue;
+            }
+            int stop = 0;
+            if (lane == 0) {
+                if (vdone[ph] == kConsumerWarps) {
+                    __threadfence_block();
+                    if (*reinterpret_cast<volatile unsigned*>(&ctl.fq_tail) == head || *vabort) stop = 1;
+                }
+                if (!stop && global_ns() - t0 > kWaitTimeoutNs) {
+                    set_abort(a.d_status);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) return;
+            __nanosleep(200);
+        }
+    }
+
     // ---- phase-1 prologue (consumers): partition tables, the count of T > 0
     // requests, the map of this block's draft slice to requests; block 0
     // publishes the compaction.
@@ -481,7 +598,7 @@ struct Kern {
                     const int rel = k - k_lo;
                     if (rel >= 0 && rel < kMapMax) ctl.map[rel] = b;
                 }
-                if (g == 0) prefix()[b] = f ? k : -1;
+                ctl.kmap[b] = static_cast<short>(f ? k : -1);
             }
             carry += total;
             bar_sync(kBarConsumers, kConsumers);
@@ -512,7 +629,9 @@ struct Kern {
     // reduces its lanes, parks the result in shared slot `seq % kFlushSlots`,
     // and the last warp to arrive merges the 8 partials in warp order and
     // writes the block's record for the piece (no block-wide barrier).
-    __device__ void flush_row(const RowState& rs, const RowLoc& loc, unsigned seq) const {
+    // When `share` is non-zero this piece ends the request's rows in the slice:
+    // the merging warp then posts the request with the share's element count.
+    __device__ void flush_row(const RowState& rs, const RowLoc& loc, unsigned seq, unsigned share) const {
         const int bad = __any_sync(0xffffffffu, rs.bad);
         Rec rec;
         if (rs.argmax) {
@@ -557,6 +676,7 @@ struct Kern {
                 Rec* dst = loc.kind == 0 ? rec_t() + (static_cast<size_t>(g) * L.MT + loc.slot)
                                          : rec_d() + (static_cast<size_t>(g) * L.MD + loc.slot);
                 *dst = out;
+                if (share && !post(loc.req, share)) set_abort(a.d_status);
             }
         }
     }
@@ -660,7 +780,7 @@ struct Kern {
         rs.s = __fadd_rn(rs.s, __fadd_rn(a0, a1));
     }
 
-    // ---- phase 2: merge of a row's pieces, in block and warp order
+    // ---- acceptance scan: merge of a row's pieces, in block and warp order
     __device__ Rec merge_row(int kind, long long row, bool argmax, float c) const {
         const long long* beg = kind == 0 ? ctl.tbeg : ctl.dbeg;
         const int MM = kind == 0 ? L.MT : L.MD;
@@ -706,7 +826,8 @@ struct Kern {
         return out;
     }
 
-    // Phase 2 for request b on one warp; `st` is this warp's shared scratch.
+    // Acceptance scan of request b on one warp (the finisher); `st` is its
+    // shared scratch of 2 gamma + 1 row records.
     __device__ void verify_request(int b, Rec* st) const {
         const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V;
         const float T = a.temperature[b];
@@ -714,7 +835,7 @@ struct Kern {
         const bool greedy = t_ok && T == 0.0f;
         const bool samp = sampled(T);
         const float c = samp ? temp_scale(T) : 0.0f;
-        const int k = __ldcg(prefix() + b);
+        const int k = ctl.kmap[b];
         const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
         int bad = t_ok ? 0 : 1;
         // this lane's first position (gamma <= 32 in one pass): its token, the two
@@ -820,7 +941,7 @@ struct Kern {
             if (j < n)
                 out[j] = tok[j];
             else if (j == n)
-                out[j] = greedy ? st[n].idx : -1;  // the draw fills it in phase 3
+                out[j] = greedy ? st[n].idx : -1;  // the draw fills it in phase 2
             else
                 out[j] = -1;
         }
@@ -856,7 +977,7 @@ struct Kern {
         }
     }
 
-    // ---- phase 3 schedule: draw items (job k, chunk j) of this block
+    // ---- phase-2 schedule: draw items (job k, chunk j) of this block
     __device__ static int job_cost(int kind) { return kind == kKindResidual ? 2 : (kind == kKindBonus ? 1 : 0); }
 
     // The block's unit range and the first job with units after u_lo.
@@ -876,8 +997,10 @@ struct Kern {
         k_first = lo;
     }
 
-    // Calls f(k, j) for every item whose first cost unit falls in this
-    // block's share. `pre` holds the cost prefix over jobs (n_samp + 1).
+    // Calls f(k, j, last, cnt) for every item whose first cost unit falls in
+    // this block's share: item j of job k, whether it is the block's last item
+    // of job k, and how many items of job k the block has. `pre` holds the
+    // cost prefix over jobs (n_samp + 1).
     template <typename F>
     __device__ void for_each_item(const int* pre, F&& f) const {
         const int ns = ctl.n_samp;
@@ -892,11 +1015,10 @@ struct Kern {
             if (base >= u_hi) break;
             int j0 = 0;
             if (base < u_lo) j0 = static_cast<int>((u_lo - base + cost - 1) / cost);
-            for (int j = j0; j < L.NCH; ++j) {
-                const long long u0 = base + static_cast<long long>(j) * cost;
-                if (u0 >= u_hi) return;
-                f(k, j);
-            }
+            // last item whose first unit is below u_hi
+            const int j1 = static_cast<int>(min(static_cast<long long>(L.NCH - 1), (u_hi - 1 - base) / cost));
+            for (int j = j0; j <= j1; ++j) f(k, j, j == j1, j1 - j0 + 1);
+            if (j1 < L.NCH - 1) return;
         }
     }
 
@@ -997,217 +1119,17 @@ struct Kern {
         if (kind == kKindResidual) load_run_global(a.draft, drow + e0 + r * kTPT, valid, vd);
         return to_fixed(run_sum(vt, vd, valid, d, kind), d.fix);
     }
-};
 
-template <int DT>
-__global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, char* ws) {
-    extern __shared__ __align__(128) char smem[];
-    char* stages = smem;
-    Ctl& ctl = *reinterpret_cast<Ctl*>(smem + static_cast<size_t>(kStages) * kStageBytes);
-    Rec* warp_rows = reinterpret_cast<Rec*>(smem + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl));
-    int* pre = reinterpret_cast<int*>(warp_rows + kConsumerWarps * kMaxRowsPerReq);
-
-    using KT = Kern<DT>;
-    KT K{a, L, ws, ctl, stages, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x)};
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const bool producer = warp == kConsumerWarps;
-    unsigned long long* ph = reinterpret_cast<unsigned long long*>(a.dbg.phase_ns);
-    stamp(ph, 0);
-
-    if (t == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl.full[s], 1);
-            mbar_init(&ctl.empty[s], kConsumerWarps);
-        }
-        ctl.abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    for (int i = t; i < kMapMax; i += kThreads) ctl.map[i] = -1;
-    for (int i = t; i < kFlushSlots; i += kThreads) ctl.wcnt[i] = 0;
-    __syncthreads();
-
-    const long long ts = part_begin(L.Et, K.G, K.g, L.vec), te = part_begin(L.Et, K.G, K.g + 1, L.vec);
-
-    // -------------------------------------------------------------- phase 1
-    typename KT::Cursor prod, cons;
-    if (producer) {
-        bool ok = true;
-        auto issue = [&](const Segment& sg) {
-            for (long long off = 0; off < sg.elems && ok && !ctl.abort; off += KT::kStageElems) {
-                const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
-                ok = K.produce(prod, sg.src + off * KT::ES, static_cast<unsigned>(n * KT::ES));
-            }
-        };
-        K.for_each_target_segment(ts, te, issue);
-        bar_sync(kBarHandoff, kThreads);  // the consumers' prologue is done
-        K.for_each_draft_segment(issue);
-        if (!ok) K.set_abort(a.d_status);
-        if (ctl.abort) K.drain(prod);
-    } else {
-        // the ring fills with target stages while the consumers run the prologue
-        K.prologue();
-        bar_arrive(kBarHandoff, kThreads);
-        bool ok = true;
-        unsigned seq = 0;  // row pieces folded so far (the same on every consumer warp)
-        auto fold = [&](const Segment& sg) {
-            if (!ok) return;
-            typename KT::RowState rs;
-            K.start_row(rs, sg.loc);
-            for (long long off = 0; off < sg.elems; off += KT::kStageElems) {
-                const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
-                const char* sm = K.consume_begin(cons);
-                if (!sm) {
-                    ok = false;
-                    K.set_abort(a.d_status);
-                    return;
-                }
-                K.fold_stage(rs, sm, static_cast<int>(n * KT::ES / 16), sg.e0 + off);
-                K.consume_end(cons);
-            }
-            K.flush_row(rs, sg.loc, seq++);
-        };
-        K.for_each_target_segment(ts, te, fold);
-        K.for_each_draft_segment(fold);
-    }
-    __syncthreads();
-    stamp(ph, 2);
-    Hdr* hdr = K.hdr();
-    if (!grid_sync(hdr, a.d_status, &ctl.flag, a.barrier_wait_ns)) return;
-    stamp(ph, 3);
-    if (ctl.abort) return;
-
-    // -------------------------------------------------------------- phase 2
-    if (!producer) {
-        Rec* st = warp_rows + warp * kMaxRowsPerReq;
-        // requests spread over the blocks first, then over the warps
-        for (int b = warp * gridDim.x + blockIdx.x; b < a.B; b += gridDim.x * kConsumerWarps) {
-            K.verify_request(b, st);
-            __syncwarp();
-        }
-    }
-    __syncthreads();
-    stamp(ph, 4);
-    const int ns = ctl.n_samp;
-    if (ns == 0) {
-        stamp(ph, 9);
-        return;
-    }
-    if (!grid_sync(hdr, a.d_status, &ctl.flag, a.barrier_wait_ns)) return;
-    stamp(ph, 5);
-
-    // -------------------------------------------------------------- phase 3a
-    constexpr int TPT = KT::kTPT;
-    constexpr int CH = KT::kChunkElems;
-    if (!producer) {
-        // cost prefix over jobs, then this block's jobs into shared memory
-        const Job* gjobs = K.jobs();
-        int carry = 0;
-        for (int base = 0; base < ns; base += kConsumers) {
-            const int k = base + t;
-            const int cost = k < ns ? KT::job_cost(gjobs[k].kind) : 0;
-            int x = cost;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            if (lane == 31) ctl.wtmp[warp] = x;
-            bar_sync(kBarConsumers, kConsumers);
-            int before = carry, total = 0;
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                if (w < warp) before += ctl.wtmp[w];
-                total += ctl.wtmp[w];
-            }
-            if (k < ns) pre[k] = before + x - cost;
-            carry += total;
-            bar_sync(kBarConsumers, kConsumers);
-        }
-        if (t == 0) pre[ns] = carry;
-        bar_sync(kBarConsumers, kConsumers);
-        long long u_lo, u_hi;
-        int k0;
-        K.item_range(pre, u_lo, u_hi, k0);
-        int k1 = k0;  // one past the last job with an item here
-        if (u_hi > u_lo) {
-            int lo = k0, hi = ns;
-            while (lo < hi) {  // first job whose units start at or after u_hi
-                const int mid = (lo + hi) >> 1;
-                if (static_cast<long long>(pre[mid]) * L.NCH >= u_hi)
-                    hi = mid;
-                else
-                    lo = mid + 1;
-            }
-            k1 = lo;
-        }
-        const int njobs = min(kJobCache, max(0, k1 - k0));
-        for (int i = t; i < njobs; i += kConsumers) ctl.jobs[i] = gjobs[k0 + i];
-        if (t == 0) {
-            ctl.job_lo = k0;
-            ctl.job_n = njobs;
-        }
-        bar_sync(kBarConsumers, kConsumers);
-        bar_arrive(kBarHandoff, kThreads);
-    }
-    if (producer) {
-        bar_sync(kBarHandoff, kThreads);
-        bool ok = true;
-        const Job* gjobs = K.jobs();
-        K.for_each_item(pre, [&](int k, int j) {
-            if (!ok || ctl.abort) return;
-            const Job& jb = K.job_cached(k) ? ctl.jobs[k - ctl.job_lo] : gjobs[k];
-            const long long e0 = static_cast<long long>(j) * CH;
-            const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
-            const unsigned bytes = static_cast<unsigned>(cnt * KT::ES);
-            const long long trow = static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n;
-            const char* src_t = static_cast<const char*>(a.target) + (trow * a.V + e0) * KT::ES;
-            if (jb.kind == kKindResidual) {
-                const long long drow = static_cast<long long>(jb.b) * a.gamma + jb.n;
-                ok = K.produce(prod, src_t, bytes, static_cast<const char*>(a.draft) + (drow * a.V + e0) * KT::ES,
-                               bytes);
-            } else {
-                ok = K.produce(prod, src_t, bytes);
-            }
-        });
-        if (!ok) K.set_abort(a.d_status);
-        if (ctl.abort) K.drain(prod);
-    } else {
-        bool ok = true;
-        const Job* gjobs = K.jobs();
-        unsigned long long* wsums = K.wsums();
-        K.for_each_item(pre, [&](int k, int j) {
-            if (!ok) return;
-            const Job jb = K.job_cached(k) ? ctl.jobs[k - ctl.job_lo] : gjobs[k];
-            const long long e0 = static_cast<long long>(j) * CH;
-            const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
-            const int valid = max(0, min(TPT, cnt - t * TPT));
-            typename KT::Run lt, ld;
-            const char* smt = K.consume_begin(cons);
-            if (!smt) {
-                ok = false;
-                K.set_abort(a.d_status);
-                return;
-            }
-            if (valid > 0) {
-                KT::load_run_smem(smt, t, lt);
-                if (jb.kind == kKindResidual) KT::load_run_smem(smt + kChunkBytes, t, ld);
-            }
-            K.consume_end(cons);
-            const float run = valid > 0 ? KT::run_sum(lt, ld, valid, jb.d, jb.kind) : 0.0f;
-            const unsigned long long wsum = warp_sum_u64(to_fixed(run, jb.d.fix));
-            if (lane == 0) wsums[(static_cast<size_t>(k) * L.NCH + j) * kConsumerWarps + warp] = wsum;
-        });
-    }
-    __syncthreads();
-    stamp(ph, 6);
-    if (!grid_sync(hdr, a.d_status, &ctl.flag, a.barrier_wait_ns)) return;
-    stamp(ph, 7);
-    if (ctl.abort || producer) return;
-
-    // -------------------------------------------------------------- phase 3b
-    const Job* gjobs = K.jobs();
-    const unsigned long long* wsums = K.wsums();
-    for (int k = warp * gridDim.x + blockIdx.x; k < ns; k += gridDim.x * kConsumerWarps) {
-        const unsigned long long* js = wsums + static_cast<size_t>(k) * L.NCH * kConsumerWarps;
+    // ---- phase 2, finisher: the token of draw job k. The chunk holding
+    // floor(u W), then the warp within it, from the stored fixed-point sums;
+    // then that warp's 32 runs are re-read and summed exactly as in the
+    // streaming pass, and one lane walks its run token by token.
+    __device__ void search_job(int k) const {
+        constexpr int TPT = kTPT;
+        constexpr int CH = kChunkElems;
+        const int lane = threadIdx.x & 31;
+        const Job* gjobs = jobs();
+        const unsigned long long* js = wsums() + static_cast<size_t>(k) * L.NCH * kConsumerWarps;
         // this lane's chunk totals (lane j holds chunks j, j+32, ...; NCH <= 128),
         // loaded together with the job: they depend on k only
         const int nch_lane = (L.NCH + 31) / 32;
@@ -1227,16 +1149,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             ctot[h] = sum;
         }
         const Job jb = gjobs[k];
-        if (jb.kind != kKindResidual && jb.kind != kKindBonus) continue;
+        if (jb.kind != kKindResidual && jb.kind != kKindBonus) return;
         DrawParams d = jb.d;
         int kind = jb.kind;
         const long long trow = (static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n) * a.V;
         const long long drow = (static_cast<long long>(jb.b) * a.gamma + jb.n) * a.V;
-        // per-warp sums of chunk j (from phase 3a, or recomputed on the fallback)
+        // per-warp sums of chunk j (from the draw stream, or recomputed on the fallback)
         bool fallback = false;
         auto warp_part = [&](int j, int w) -> unsigned long long {
-            if (!fallback) return js[static_cast<size_t>(j) * kConsumerWarps + w];
-            return warp_sum_u64(K.run_fixed_global(trow, drow, j, w * 32 + lane, d, kind));
+            if (!fallback) return __ldcg(js + static_cast<size_t>(j) * kConsumerWarps + w);
+            return warp_sum_u64(run_fixed_global(trow, drow, j, w * 32 + lane, d, kind));
         };
         // total of chunk j on the fallback, computed by the whole warp
         auto chunk_total_warp = [&](int j) -> unsigned long long {
@@ -1298,7 +1220,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         // fallback warp_part is warp-collective, so every lane calls it)
         unsigned long long part = 0ull;
         if (!fallback) {
-            if (lane < kConsumerWarps) part = js[static_cast<size_t>(jsel) * kConsumerWarps + lane];
+            if (lane < kConsumerWarps) part = __ldcg(js + static_cast<size_t>(jsel) * kConsumerWarps + lane);
         } else {
             for (int w = 0; w < kConsumerWarps; ++w) {
                 const unsigned long long v = warp_part(jsel, w);
@@ -1315,17 +1237,17 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         const unsigned whit = __ballot_sync(0xffffffffu, part > 0 && pst <= tt && tt < pst + part);
         const int wsel = whit ? __ffs(whit) - 1 : kConsumerWarps - 1;
         before = __shfl_sync(0xffffffffu, pst, wsel);
-        // its 32 runs, one per lane, re-read with the weights of phase 3a
+        // its 32 runs, one per lane, re-read with the weights of the draw stream
         const long long e0 = static_cast<long long>(jsel) * CH;
         const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
         const int vt = wsel * 32 + lane;
         const int valid = max(0, min(TPT, cnt - vt * TPT));
-        typename KT::Run lt, ld;
+        Run lt, ld;
         if (valid > 0) {
-            KT::load_run_global(a.target, trow + e0 + vt * TPT, valid, lt);
-            if (kind == kKindResidual) KT::load_run_global(a.draft, drow + e0 + vt * TPT, valid, ld);
+            load_run_global(a.target, trow + e0 + vt * TPT, valid, lt);
+            if (kind == kKindResidual) load_run_global(a.draft, drow + e0 + vt * TPT, valid, ld);
         }
-        const float run = valid > 0 ? KT::run_sum(lt, ld, valid, d, kind) : 0.0f;
+        const float run = valid > 0 ? run_sum(lt, ld, valid, d, kind) : 0.0f;
         const unsigned long long q = to_fixed(run, d.fix);
         unsigned long long x = q;
 #pragma unroll
@@ -1339,7 +1261,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         if (mine && lane == __ffs(ball) - 1) {
             // the first token of the run whose prefix passes tt
             float w[TPT];
-            KT::run_weights(lt, ld, valid, d, kind, w);
+            run_weights(lt, ld, valid, d, kind, w);
             float r2 = 0.0f;
             int token = -1, last_pos = -1;
 #pragma unroll
@@ -1360,16 +1282,247 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             a.dbg.w_total[jb.b] =
                 kind == kKindResidual ? W * kFixResidualInv : W * kFixTargetInv * static_cast<double>(d.isp);
         }
-        __syncwarp();
     }
-    bar_sync(kBarConsumers, kConsumers);
-    stamp(ph, 8);
-    stamp(ph, 9);
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, char* ws) {
+    extern __shared__ __align__(128) char smem[];
+    char* stages = smem;
+    Ctl& ctl = *reinterpret_cast<Ctl*>(smem + static_cast<size_t>(kStages) * kStageBytes);
+    Rec* fin_rows = reinterpret_cast<Rec*>(smem + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl));
+    int* pre = reinterpret_cast<int*>(fin_rows + kMaxRowsPerReq);
+
+    using KT = Kern<DT>;
+    KT K{a, L, ws, ctl, stages, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x)};
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const bool producer = warp == kProducerWarp, finisher = warp == kFinisherWarp;
+    unsigned long long* ph = reinterpret_cast<unsigned long long*>(a.dbg.phase_ns);
+    stamp(ph, 0, t == 0);
+
+    if (t == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl.full[s], 1);
+            mbar_init(&ctl.empty[s], kConsumerWarps);
+        }
+        ctl.abort = 0;
+        ctl.fq_tail = 0;
+        ctl.fq_head = 0;
+        ctl.cons_done[0] = 0;
+        ctl.cons_done[1] = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int i = t; i < kMapMax; i += kThreads) ctl.map[i] = -1;
+    for (int i = t; i < kFlushSlots; i += kThreads) ctl.wcnt[i] = 0;
+    for (int i = t; i < kQueue; i += kThreads) ctl.fq_seq[i] = 0;
+    __syncthreads();
+
+    const long long ts = part_begin(L.Et, K.G, K.g, L.vec), te = part_begin(L.Et, K.G, K.g + 1, L.vec);
+    unsigned head = 0;  // finisher: ring entries taken
+
+    // ------------------------------------- phase 1 (+ acceptance scans on the finisher)
+    typename KT::Cursor prod, cons;
+    if (producer) {
+        bool ok = true;
+        auto issue = [&](const Segment& sg) {
+            for (long long off = 0; off < sg.elems && ok && !ctl.abort; off += KT::kStageElems) {
+                const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
+                ok = K.produce(prod, sg.src + off * KT::ES, static_cast<unsigned>(n * KT::ES));
+            }
+        };
+        K.for_each_target_segment(ts, te, issue);
+        bar_sync(kBarHandoff, kHandoffThreads);  // the consumers' prologue is done
+        K.for_each_draft_segment(issue);
+        if (!ok) K.set_abort(a.d_status);
+        if (ctl.abort) K.drain(prod);
+    } else if (finisher) {
+        // a request is scanned by the block whose share completes its 2 gamma + 1
+        // rows (gamma + 1 at T = 0), as soon as that share is folded
+        const unsigned V = static_cast<unsigned>(a.V), GM = static_cast<unsigned>(a.gamma);
+        unsigned* req_done = K.req_done();
+        K.finish(
+            head, 0,
+            [&](int b, unsigned share) {
+                const unsigned need = (KT::sampled(a.temperature[b]) ? 2 * GM + 1 : GM + 1) * V;
+                return atomicAdd(req_done + b, share) + share == need;
+            },
+            [&](int b) { K.verify_request(b, fin_rows); });
+        stamp(ph, 3, lane == 0);
+    } else {
+        // the ring fills with target stages while the consumers run the prologue
+        K.prologue();
+        bar_arrive(kBarHandoff, kHandoffThreads);
+        bool ok = true;
+        unsigned seq = 0;    // row pieces folded so far (the same on every consumer warp)
+        unsigned share = 0;  // elements of the current request folded in this slice
+        auto fold = [&](const Segment& sg) {
+            if (!ok) return;
+            typename KT::RowState rs;
+            K.start_row(rs, sg.loc);
+            for (long long off = 0; off < sg.elems; off += KT::kStageElems) {
+                const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
+                const char* sm = K.consume_begin(cons);
+                if (!sm) {
+                    ok = false;
+                    K.set_abort(a.d_status);
+                    return;
+                }
+                K.fold_stage(rs, sm, static_cast<int>(n * KT::ES / 16), sg.e0 + off);
+                K.consume_end(cons);
+            }
+            share += static_cast<unsigned>(sg.elems);
+            K.flush_row(rs, sg.loc, seq++, sg.last ? share : 0u);
+            if (sg.last) share = 0;
+        };
+        K.for_each_target_segment(ts, te, fold);
+        K.for_each_draft_segment(fold);
+        K.consumer_done(0);
+        stamp(ph, 2, lane == 0);
+    }
+    __syncthreads();
+    const int ns = ctl.n_samp;
+    if (ns == 0) {  // every request greedy or invalid: nothing to draw
+        stamp(ph, 9, t == 0);
+        return;
+    }
+    Hdr* hdr = K.hdr();
+    if (!grid_sync(hdr, a.d_status, &ctl.flag, a.barrier_wait_ns)) return;
+    stamp(ph, 4, t == 0);
+    if (ctl.abort) return;
+
+    // ------------------------------------------- phase 2 (+ token searches on the finisher)
+    constexpr int TPT = KT::kTPT;
+    constexpr int CH = KT::kChunkElems;
+    if (producer) {
+        bar_sync(kBarHandoff, kHandoffThreads);  // the schedule is in shared memory
+        bool ok = true;
+        const Job* gjobs = K.jobs();
+        K.for_each_item(pre, [&](int k, int j, bool, int) {
+            if (!ok || ctl.abort) return;
+            const Job& jb = K.job_cached(k) ? ctl.jobs[k - ctl.job_lo] : gjobs[k];
+            const long long e0 = static_cast<long long>(j) * CH;
+            const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+            const unsigned bytes = static_cast<unsigned>(cnt * KT::ES);
+            const long long trow = static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n;
+            const char* src_t = static_cast<const char*>(a.target) + (trow * a.V + e0) * KT::ES;
+            if (jb.kind == kKindResidual) {
+                const long long drow = static_cast<long long>(jb.b) * a.gamma + jb.n;
+                ok = K.produce(prod, src_t, bytes, static_cast<const char*>(a.draft) + (drow * a.V + e0) * KT::ES,
+                               bytes);
+            } else {
+                ok = K.produce(prod, src_t, bytes);
+            }
+        });
+        if (!ok) K.set_abort(a.d_status);
+        if (ctl.abort) K.drain(prod);
+        return;
+    }
+    if (finisher) {
+        // a job is searched by the block whose chunk sums complete it
+        const unsigned NCH = static_cast<unsigned>(L.NCH);
+        unsigned* job_done = K.job_done();
+        K.finish(
+            head, 1, [&](int k, unsigned cnt) { return atomicAdd(job_done + k, cnt) + cnt == NCH; },
+            [&](int k) { K.search_job(k); });
+        stamp(ph, 7, lane == 0);
+        stamp(ph, 9, lane == 0);
+        return;
+    }
+    // consumers: cost prefix over jobs, then this block's jobs into shared memory
+    {
+        const Job* gjobs = K.jobs();
+        int carry = 0;
+        for (int base = 0; base < ns; base += kConsumers) {
+            const int k = base + t;
+            const int cost = k < ns ? KT::job_cost(gjobs[k].kind) : 0;
+            int x = cost;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == 31) ctl.wtmp[warp] = x;
+            bar_sync(kBarConsumers, kConsumers);
+            int before = carry, total = 0;
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                if (w < warp) before += ctl.wtmp[w];
+                total += ctl.wtmp[w];
+            }
+            if (k < ns) pre[k] = before + x - cost;
+            carry += total;
+            bar_sync(kBarConsumers, kConsumers);
+        }
+        if (t == 0) pre[ns] = carry;
+        bar_sync(kBarConsumers, kConsumers);
+        long long u_lo, u_hi;
+        int k0;
+        K.item_range(pre, u_lo, u_hi, k0);
+        int k1 = k0;  // one past the last job with an item here
+        if (u_hi > u_lo) {
+            int lo = k0, hi = ns;
+            while (lo < hi) {  // first job whose units start at or after u_hi
+                const int mid = (lo + hi) >> 1;
+                if (static_cast<long long>(pre[mid]) * L.NCH >= u_hi)
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            k1 = lo;
+        }
+        const int njobs = min(kJobCache, max(0, k1 - k0));
+        for (int i = t; i < njobs; i += kConsumers) ctl.jobs[i] = gjobs[k0 + i];
+        if (t == 0) {
+            ctl.job_lo = k0;
+            ctl.job_n = njobs;
+        }
+        bar_sync(kBarConsumers, kConsumers);
+        bar_arrive(kBarHandoff, kHandoffThreads);
+        stamp(ph, 5, t == 0);
+    }
+    bool ok = true;
+    const Job* gjobs = K.jobs();
+    unsigned long long* wsums = K.wsums();
+    K.for_each_item(pre, [&](int k, int j, bool last, int cnt) {
+        if (!ok) return;
+        const Job jb = K.job_cached(k) ? ctl.jobs[k - ctl.job_lo] : gjobs[k];
+        const long long e0 = static_cast<long long>(j) * CH;
+        const int n = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+        const int valid = max(0, min(TPT, n - t * TPT));
+        typename KT::Run lt, ld;
+        const char* smt = K.consume_begin(cons);
+        if (!smt) {
+            ok = false;
+            K.set_abort(a.d_status);
+            return;
+        }
+        if (valid > 0) {
+            KT::load_run_smem(smt, t, lt);
+            if (jb.kind == kKindResidual) KT::load_run_smem(smt + kChunkBytes, t, ld);
+        }
+        K.consume_end(cons);
+        const float run = valid > 0 ? KT::run_sum(lt, ld, valid, jb.d, jb.kind) : 0.0f;
+        const unsigned long long wsum = warp_sum_u64(to_fixed(run, jb.d.fix));
+        if (lane == 0) {
+            wsums[(static_cast<size_t>(k) * L.NCH + j) * kConsumerWarps + warp] = wsum;
+            if (last) {
+                // the block's share of job k is stored once all 8 warps are here
+                const int fs = (k - ctl.job_lo) % kFlushSlots;
+                __threadfence_block();
+                if (atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1) {
+                    __threadfence_block();
+                    ctl.wcnt[fs] = 0;
+                    if (!K.post(k, static_cast<unsigned>(cnt))) K.set_abort(a.d_status);
+                }
+            }
+        }
+    });
+    K.consumer_done(1);
+    stamp(ph, 6, lane == 0);
 }
 
 size_t smem_bytes() {
-    return static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl) +
-           sizeof(Rec) * kConsumerWarps * kMaxRowsPerReq + sizeof(int) * (kMaxB + 1);
+    return static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl) + sizeof(Rec) * kMaxRowsPerReq +
+           sizeof(int) * (kMaxB + 1);
 }
 
 }  // namespace
@@ -1415,7 +1568,8 @@ cudaError_t launch_streaming(const Args& a, const DeviceInfo& dev, int grid, voi
         attr_device = dev.device;
     }
     if (grid > dev.num_sms) return cudaErrorInvalidValue;
-    cudaError_t e = cudaMemsetAsync(workspace, 0, 256, stream);
+    // the barrier words and the completion counters start at zero
+    cudaError_t e = cudaMemsetAsync(workspace, 0, L.clear_bytes, stream);
     if (e != cudaSuccess) return e;
     Args args = a;
     Layout lay = L;
