@@ -45,17 +45,17 @@
 namespace sv {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 12;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;      // issues the bulk copies
 constexpr int kFinisherWarp = kConsumerWarps + 1;  // acceptance scans and token searches
 constexpr int kThreads = kConsumers + 64;
 constexpr int kHandoffThreads = kConsumers + 32;   // consumers + producer
 constexpr int kQueue = 256;                        // finisher message ring (slots)
-constexpr int kStages = 4;
-constexpr int kStageBytes = 32768;
+constexpr int kStages = 3;
+constexpr int kStageBytes = 49152;
 constexpr int kVecPerThread = kStageBytes / 16 / kConsumers;  // 8
-constexpr int kChunkBytes = 16384;  // draw-phase chunk of one row (a residual item fills a stage)
+constexpr int kChunkBytes = 24576;  // draw-phase chunk of one row (a residual item fills a stage)
 constexpr int kMapMax = 256;   // compacted requests in one block's draft slice
 constexpr int kMaxGrid = 256;  // blocks (partition tables live in shared memory)
 constexpr int kJobCache = 64;  // draw jobs cached per block in the draw phase
@@ -1024,77 +1024,104 @@ struct Kern {
 
     __device__ bool job_cached(int k) const { return k >= ctl.job_lo && k < ctl.job_lo + ctl.job_n; }
 
-    // A run is kTPT consecutive tokens, 64 bytes, held packed as 4 vectors.
+    // A run is kTPT consecutive tokens, 64 bytes, held packed as 4 vectors of
+    // kTPV tokens. Its weight sum is defined vector by vector: S_q adds the
+    // weights of vector q in index order, and the run total is
+    // ((S_0 + S_1) + S_2) + S_3. The token search walks the same order, so
+    // the prefix at a run's last token is the total the stream pass stored.
     using Run = uint4[4];
+    static constexpr int kTPV = 16 / ES;  // tokens per 16-byte vector
 
-    // Token e of a packed run as binary32.
-    __device__ static __forceinline__ float token_at(const Run& v, int e) {
-        const int q = DT == SV_BF16 ? e >> 3 : e >> 2;
-        const int i = DT == SV_BF16 ? (e >> 1) & 3 : e & 3;
-        const uint32_t w = i == 0 ? v[q].x : i == 1 ? v[q].y : i == 2 ? v[q].z : v[q].w;
-        if (DT == SV_BF16) return (e & 1) ? bf16x2_hi(w) : bf16x2_lo(w);
-        return __uint_as_float(w);
-    }
-
-    // Weight of token e of a run (target run vt, draft run vd).
-    __device__ static __forceinline__ float run_weight(const Run& vt, const Run& vd, int e,
-                                                       const DrawParams& d, int kind) {
-        return kind == kKindResidual ? weight_residual(token_at(vt, e), token_at(vd, e), d)
-                                     : weight_target(token_at(vt, e), d);
-    }
-
-    // The weights of a run's tokens (0 past `valid`): independent of each
-    // other, so they are computed before the serial sum.
-    __device__ static __forceinline__ void run_weights(const Run& vt, const Run& vd, int valid, const DrawParams& d,
-                                                       int kind, float (&w)[kTPT]) {
-        if (kind == kKindResidual) {
+    // The weights of one vector's tokens (target vt, draft vd). The exponent
+    // arguments l c - mc are formed pair by pair with fma.rn.f32x2 (each lane
+    // rounded as a scalar fma), so every weight equals weight_residual or
+    // weight_target of that token.
+    __device__ static __forceinline__ void vec_weights(const uint4& vt, const uint4& vd, const DrawParams& d,
+                                                       int kind, float (&w)[kTPV]) {
+        const uint32_t t4[4] = {vt.x, vt.y, vt.z, vt.w};
+        const uint32_t d4[4] = {vd.x, vd.y, vd.z, vd.w};
+        const unsigned long long cc = f2_pack(d.c, d.c), nmp = f2_pack(-d.mcp, -d.mcp);
 #pragma unroll
-            for (int e = 0; e < kTPT; ++e) {
-                const float x = weight_residual(token_at(vt, e), token_at(vd, e), d);
-                w[e] = e < valid ? x : 0.0f;
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < kTPT; ++e) {
-                const float x = weight_target(token_at(vt, e), d);
-                w[e] = e < valid ? x : 0.0f;
+        for (int i = 0; i < kTPV / 2; ++i) {
+            const unsigned long long xt = DT == SV_BF16 ? f2_pack_bits(prmt(t4[i], 0x1044u), prmt(t4[i], 0x3244u))
+                                                        : f2_pack_bits(t4[2 * i], t4[2 * i + 1]);
+            float e0, e1;
+            f2_unpack(f2_fma(xt, cc, nmp), e0, e1);
+            if (kind == kKindResidual) {
+                const unsigned long long xd = DT == SV_BF16
+                                                  ? f2_pack_bits(prmt(d4[i], 0x1044u), prmt(d4[i], 0x3244u))
+                                                  : f2_pack_bits(d4[2 * i], d4[2 * i + 1]);
+                float g0, g1;
+                f2_unpack(f2_fma(xd, cc, f2_pack(-d.mcq, -d.mcq)), g0, g1);
+                // p and q are each rounded to binary32 before the difference:
+                // scalar __fmul_rn/__fsub_rn are never merged into a fused
+                // multiply-add, so weights that cancel in binary32 are exactly 0
+                w[2 * i] = fmaxf(__fsub_rn(__fmul_rn(ex2(e0), d.isp), __fmul_rn(ex2(g0), d.isq)), 0.0f);
+                w[2 * i + 1] = fmaxf(__fsub_rn(__fmul_rn(ex2(e1), d.isp), __fmul_rn(ex2(g1), d.isq)), 0.0f);
+            } else {
+                w[2 * i] = ex2(e0);
+                w[2 * i + 1] = ex2(e1);
             }
         }
     }
 
-    // Weight sum of the first `valid` tokens of a run, added in index order
-    // (adding the +0 weights past `valid` leaves the non-negative sum as is).
-    __device__ static __forceinline__ float run_sum(const Run& vt, const Run& vd, int valid, const DrawParams& d,
-                                    int kind) {
-        float w[kTPT];
-        run_weights(vt, vd, valid, d, kind, w);
-        float run = 0.0f;
+    // S_q of one vector: its weights added in index order.
+    __device__ static __forceinline__ float vec_sum(const uint4& vt, const uint4& vd, const DrawParams& d, int kind) {
+        float w[kTPV];
+        vec_weights(vt, vd, d, kind, w);
+        float s = w[0];
 #pragma unroll
-        for (int e = 0; e < kTPT; ++e) run = __fadd_rn(run, w[e]);
-        return run;
+        for (int e = 1; e < kTPV; ++e) s = __fadd_rn(s, w[e]);
+        return s;
     }
 
-    // Run t of a stage in shared memory (swizzled order: conflict-free).
-    // Thread t reads its vectors in the order r, r+1, r+2, r+3 (mod 4) with
-    // r = (t >> 1) & 3, so the 8 lanes of each shared-memory wavefront hit
-    // distinct banks; compile-time selects put them back in index order.
-    __device__ static __forceinline__ void load_run_smem(const char* sm, int t, Run& v) {
+    __device__ static __forceinline__ float run_total(const float (&S)[4]) {
+        return __fadd_rn(__fadd_rn(__fadd_rn(S[0], S[1]), S[2]), S[3]);
+    }
+
+    // S_0..S_3 of a run held in index order; vectors at or past `valid`
+    // tokens weigh 0 (rows end on 16-byte boundaries, so a vector is either
+    // wholly in the row or wholly past it).
+    __device__ static __forceinline__ void run_vec_sums(const Run& vt, const Run& vd, int valid, const DrawParams& d,
+                                                        int kind, float (&S)[4]) {
+        // all four are computed (straight-line code), then the ones past the
+        // row are dropped
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float x = vec_sum(vt[q], vd[q], d, kind);
+            S[q] = q * kTPV < valid ? x : 0.0f;
+        }
+    }
+
+    // Run t of a stage in shared memory, read in rotated order so that the 8
+    // lanes of each shared-memory wavefront hit distinct banks: raw[k] is
+    // vector (k + r) & 3 with r = (t >> 1) & 3.
+    __device__ static __forceinline__ void load_run_smem(const char* sm, int t, Run& raw) {
         const int r = (t >> 1) & 3;
         const uint4* base = reinterpret_cast<const uint4*>(sm + static_cast<size_t>(t) * 64);
-        uint4 raw[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) raw[k] = base[(k + r) & 3];  // raw[k] is vector (k + r) & 3
-        // rotate back by r: by 2 if r & 2, then by 1 if r & 1 (selects on constants)
-        const bool r2 = (r & 2) != 0, r1 = (r & 1) != 0;
-        uint4 m[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) m[q] = sel4(r2, raw[(q + 2) & 3], raw[q]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = sel4(r1, m[(q + 3) & 3], m[q]);
+        for (int k = 0; k < 4; ++k) raw[k] = base[(k + r) & 3];
     }
 
-    __device__ static __forceinline__ uint4 sel4(bool c, const uint4& a, const uint4& b) {
-        return make_uint4(c ? a.x : b.x, c ? a.y : b.y, c ? a.z : b.z, c ? a.w : b.w);
+    // Run total of a run read by load_run_smem: the vector sums are computed
+    // in the rotated order and put back in index order (rotate by 2 if r & 2,
+    // then by 1 if r & 1; selects on constant indices) before they are added.
+    __device__ static __forceinline__ float run_total_rotated(const Run& rt, const Run& rd, int t, int valid,
+                                                              const DrawParams& d, int kind) {
+        const int r = (t >> 1) & 3;
+        float Sr[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float x = vec_sum(rt[k], rd[k], d, kind);  // stale shared memory past the row is dropped
+            Sr[k] = ((k + r) & 3) * kTPV < valid ? x : 0.0f;
+        }
+        const bool r2 = (r & 2) != 0, r1 = (r & 1) != 0;
+        float m[4], S[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m[q] = r2 ? Sr[(q + 2) & 3] : Sr[q];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) S[q] = r1 ? m[(q + 3) & 3] : m[q];
+        return run_total(S);
     }
 
     // A run from global memory starting at element `e` (64-byte aligned in the
@@ -1117,7 +1144,9 @@ struct Kern {
         Run vt, vd;
         load_run_global(a.target, trow + e0 + r * kTPT, valid, vt);
         if (kind == kKindResidual) load_run_global(a.draft, drow + e0 + r * kTPT, valid, vd);
-        return to_fixed(run_sum(vt, vd, valid, d, kind), d.fix);
+        float S[4];
+        run_vec_sums(vt, vd, valid, d, kind, S);
+        return to_fixed(run_total(S), d.fix);
     }
 
     // ---- phase 2, finisher: the token of draw job k. The chunk holding
@@ -1247,8 +1276,9 @@ struct Kern {
             load_run_global(a.target, trow + e0 + vt * TPT, valid, lt);
             if (kind == kKindResidual) load_run_global(a.draft, drow + e0 + vt * TPT, valid, ld);
         }
-        const float run = valid > 0 ? run_sum(lt, ld, valid, d, kind) : 0.0f;
-        const unsigned long long q = to_fixed(run, d.fix);
+        float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (valid > 0) run_vec_sums(lt, ld, valid, d, kind, S);
+        const unsigned long long q = to_fixed(run_total(S), d.fix);
         unsigned long long x = q;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -1259,18 +1289,40 @@ struct Kern {
         const bool mine = q > 0 && start <= tt && tt < start + q;
         const unsigned ball = __ballot_sync(0xffffffffu, mine);
         if (mine && lane == __ffs(ball) - 1) {
-            // the first token of the run whose prefix passes tt
-            float w[TPT];
-            run_weights(lt, ld, valid, d, kind, w);
-            float r2 = 0.0f;
-            int token = -1, last_pos = -1;
+            // the vector, then the token, whose prefix passes tt: the prefix
+            // after vector v is P_{v+1} = P_v + S_v (P_0 = 0), and within vector
+            // v it is P_v plus the vector's partial sum
+            float P = 0.0f, Pv = 0.0f;
+            int vsel = -1;
 #pragma unroll
-            for (int e = 0; e < TPT; ++e) {
-                r2 = __fadd_rn(r2, w[e]);
-                if (w[e] > 0.0f) last_pos = e;
-                if (token < 0 && start + to_fixed(r2, d.fix) > tt) token = e;
+            for (int v = 0; v < 4; ++v) {
+                const float next = __fadd_rn(P, S[v]);
+                if (vsel < 0 && S[v] > 0.0f && start + to_fixed(next, d.fix) > tt) {
+                    vsel = v;
+                    Pv = P;
+                }
+                P = next;
             }
-            if (token < 0) token = last_pos;
+            int token = -1;
+            if (vsel >= 0) {
+                const uint4 wt = vsel == 0 ? lt[0] : vsel == 1 ? lt[1] : vsel == 2 ? lt[2] : lt[3];
+                const uint4 wd = vsel == 0 ? ld[0] : vsel == 1 ? ld[1] : vsel == 2 ? ld[2] : ld[3];
+                float w[kTPV];
+                vec_weights(wt, wd, d, kind, w);
+                float part = w[0];
+                int last_pos = w[0] > 0.0f ? 0 : -1;
+                if (start + to_fixed(__fadd_rn(Pv, part), d.fix) > tt) token = 0;
+#pragma unroll
+                for (int e = 1; e < kTPV; ++e) {
+                    part = __fadd_rn(part, w[e]);
+                    if (w[e] > 0.0f) last_pos = e;
+                    if (token < 0 && start + to_fixed(__fadd_rn(Pv, part), d.fix) > tt) token = e;
+                }
+                if (token < 0) token = last_pos;  // cannot happen: the vector's last prefix passes tt
+                token += vsel * kTPV;
+            } else {
+                token = valid - 1;  // cannot happen: the run's total passes tt
+            }
             a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.n] = static_cast<int>(e0) + vt * TPT + token;
         }
         if (!ball && lane == 0) {
@@ -1500,7 +1552,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             if (jb.kind == kKindResidual) KT::load_run_smem(smt + kChunkBytes, t, ld);
         }
         K.consume_end(cons);
-        const float run = valid > 0 ? KT::run_sum(lt, ld, valid, jb.d, jb.kind) : 0.0f;
+        const float run = valid > 0 ? KT::run_total_rotated(lt, ld, t, valid, jb.d, jb.kind) : 0.0f;
         const unsigned long long wsum = warp_sum_u64(to_fixed(run, jb.d.fix));
         if (lane == 0) {
             wsums[(static_cast<size_t>(k) * L.NCH + j) * kConsumerWarps + warp] = wsum;
