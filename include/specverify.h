@@ -138,13 +138,13 @@ typedef struct {
     int32_t* kind;          /* [B] -1 invalid, 0 greedy, 1 residual draw, 2 extra-token draw */
     uint64_t* phase_ns;     /* [SV_PHASE_SLOTS] streaming path only: global-timer stamps
                                (ns). Slot 0 is the earliest block start and slot 1 the
-                               latest; slots 2..7 and 9 are the latest time over all
-                               blocks at which: 2 the row-statistics stream ended, 3 the
-                               last acceptance scan ended, 4 the grid barrier was passed,
-                               5 the draw schedule was built, 6 the draw stream ended,
-                               7 the last token search ended, 9 the block ended. Slot 8 is
-                               not written. Slots 4..7 stay untouched when no request has
-                               T > 0. The caller fills slot 0 with UINT64_MAX and the
+                               latest; slots 2, 3, 4, 6, 7 and 9 are the latest time over
+                               all blocks at which: 2 a block's row-statistics stream
+                               ended, 3 an acceptance scan ended, 4 a block's producer
+                               took its first draw job, 6 a block's draw stream ended,
+                               7 a token search ended, 9 a block ended. Slots 5 and 8
+                               are not written; 4, 6 and 7 stay untouched when no request
+                               has T > 0. The caller fills slot 0 with UINT64_MAX and the
                                others with 0 before the call. */
 } sv_debug_out;
 
@@ -155,12 +155,18 @@ typedef struct {
     int32_t grid_ctas; /* streaming path: thread blocks in the persistent grid; 0 = the
                           device's full co-resident grid. Smaller grids split rows over
                           fewer blocks (used by tests to exercise every split). */
-    int32_t barrier_wait_us; /* streaming path: limit of each grid-barrier wait, in
-                                microseconds; 0 = the default (about 2 s). A block whose
-                                wait runs out sets SV_STATUS_TIMEOUT and returns (no copy
-                                is in flight at a barrier); the call's outputs are then
-                                not valid. A tiny value exercises that report. */
-    int32_t reserved[5];
+    int32_t peer_wait_us; /* streaming path: limit of each wait on work of other thread
+                             blocks (a draw job to be published, the hold flag), in
+                             microseconds; 0 = the default (about 2 s). A block whose wait
+                             runs out sets SV_STATUS_TIMEOUT, ends its draw phase and
+                             returns; the call's outputs are then not valid. */
+    int32_t reserved0;
+    const int32_t* hold_flag; /* streaming path, checking only; NULL normally. A device
+                                 int32: every block waits, for at most peer_wait_us, until
+                                 it is non-zero before its draw phase. A flag nothing sets
+                                 makes every such wait run out, which exercises the
+                                 SV_STATUS_TIMEOUT report deterministically. */
+    int32_t reserved[2];
 } sv_options;
 
 /* spec_verify with checking outputs and options. `dbg`, `d_status` and

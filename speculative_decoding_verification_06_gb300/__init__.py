@@ -48,7 +48,8 @@ class _Debug(ctypes.Structure):
 
 class _Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
-                ("barrier_wait_us", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
+                ("peer_wait_us", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("hold_flag", ctypes.c_void_p), ("reserved", ctypes.c_int32 * 2)]
 
 
 _lib = None
@@ -149,7 +150,7 @@ def _ptr(t) -> int:
 def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature,
                 out_tokens=None, out_num_accepted=None, workspace=None, stream=None,
                 debug: bool = False, path: int = SV_PATH_AUTO, grid_ctas: int = 0,
-                status=None, barrier_wait_us: int = 0) -> Outputs:
+                status=None, peer_wait_us: int = 0, hold_flag=None) -> Outputs:
     """Verify one batch of CUDA tensors (see include/specverify.h).
 
     ``target_logits`` [B, gamma+1, V] and ``draft_logits`` [B, gamma, V]
@@ -157,7 +158,8 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
     [B, gamma] float32, ``u_sample`` [B] float32, ``temperature`` [B] float32,
     all contiguous on the current CUDA device. Outputs and workspace are
     allocated with torch when not given. With ``debug``, ``path``,
-    ``grid_ctas`` or ``status`` the call goes through ``spec_verify_ex``.
+    ``grid_ctas``, ``status``, ``peer_wait_us`` or ``hold_flag`` (a CUDA int32
+    tensor, checking only) the call goes through ``spec_verify_ex``.
     """
     import torch
     lib = load()
@@ -179,7 +181,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
             _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
             _ptr(out_num_accepted), _ptr(workspace), workspace.numel() * workspace.element_size(), s)
     dbg = None
-    if debug or path != SV_PATH_AUTO or grid_ctas or status is not None or barrier_wait_us:
+    if debug or path != SV_PATH_AUTO or grid_ctas or status is not None or peer_wait_us or hold_flag is not None:
         d = _Debug()
         if debug:
             f64, f32, i32 = torch.float64, torch.float32, torch.int32
@@ -198,7 +200,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
             dbg["phase_ns"][0] = -1  # UINT64_MAX
             for k, v in dbg.items():
                 setattr(d, k, v.data_ptr())
-        o = _Options(path, grid_ctas, barrier_wait_us)
+        o = _Options(path, grid_ctas, peer_wait_us, 0, _ptr(hold_flag) or None)
         rc = lib.spec_verify_ex(*args, ctypes.byref(d), _ptr(status), ctypes.byref(o))
         _check(rc, "spec_verify_ex")
     else:

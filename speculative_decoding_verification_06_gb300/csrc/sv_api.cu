@@ -108,7 +108,7 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     const int path = opts ? opts->path : SV_PATH_AUTO;
     if (path != SV_PATH_AUTO && path != SV_PATH_ROWWISE && path != SV_PATH_STREAMING)
         return SV_ERR_INVALID_ARG;
-    if (opts && (opts->grid_ctas < 0 || opts->barrier_wait_us < 0)) return SV_ERR_INVALID_ARG;
+    if (opts && (opts->grid_ctas < 0 || opts->peer_wait_us < 0)) return SV_ERR_INVALID_ARG;
     DeviceInfo dev;
     if (!current_device(&dev)) return SV_ERR_UNSUPPORTED;
     if (dev.cc_major != 10 || dev.cc_minor != 3) return SV_ERR_UNSUPPORTED;
@@ -129,8 +129,9 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     std::memset(&a.dbg, 0, sizeof a.dbg);
     if (dbg) a.dbg = *dbg;
     a.d_status = d_status;
-    a.barrier_wait_ns = (opts && opts->barrier_wait_us > 0) ? 1000ull * static_cast<unsigned>(opts->barrier_wait_us)
-                                                           : 2000000000ull;
+    a.peer_wait_ns = (opts && opts->peer_wait_us > 0) ? 1000ull * static_cast<unsigned>(opts->peer_wait_us)
+                                                     : 2000000000ull;
+    a.hold_flag = opts ? opts->hold_flag : nullptr;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int grid = streaming_default_grid(dev);

@@ -24,7 +24,8 @@ struct Args {
     int32_t* out_num_accepted;  // [B]
     sv_debug_out dbg;           // device pointers, each may be null
     int32_t* d_status;          // may be null
-    unsigned long long barrier_wait_ns;  // streaming path: limit of each grid-barrier wait
+    unsigned long long peer_wait_ns;  // streaming path: limit of each wait on other blocks' work
+    const int32_t* hold_flag;         // streaming path, checking only (sv_options.hold_flag)
 };
 
 struct DeviceInfo {

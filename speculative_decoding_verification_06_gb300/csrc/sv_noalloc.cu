@@ -75,7 +75,7 @@ extern "C" sv_status spec_verify_noalloc(const void* target_logits, const void* 
     a.temperature = temperature;
     a.out_tokens = out_tokens;
     a.out_num_accepted = out_num_accepted;
-    a.barrier_wait_ns = 2000000000ull;
+    a.peer_wait_ns = 2000000000ull;
 
     const int grid = streaming_default_grid(dev);
     if (!streaming_applicable(a) || !streaming_grid_ok(B, grid)) return SV_ERR_INVALID_ARG;

@@ -52,13 +52,15 @@ constexpr int kFinisherWarp = kConsumerWarps + 1;  // acceptance scans and token
 constexpr int kThreads = kConsumers + 64;
 constexpr int kHandoffThreads = kConsumers + 32;   // consumers + producer
 constexpr int kQueue = 256;                        // finisher message ring (slots)
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kStageBytes = 49152;
 constexpr int kVecPerThread = kStageBytes / 16 / kConsumers;  // 8
 constexpr int kChunkBytes = 24576;  // draw-phase chunk of one row (a residual item fills a stage)
 constexpr int kMapMax = 256;   // compacted requests in one block's draft slice
 constexpr int kMaxGrid = 256;  // blocks (partition tables live in shared memory)
-constexpr int kJobCache = 64;  // draw jobs cached per block in the draw phase
+constexpr int kGrab = 4;       // draw items a producer takes per atomic
+constexpr int kJobMsg = 0x40000000;  // finisher message flag: a draw item of job (item & ~flag)
+constexpr int kEndKind = -2;   // stage descriptor kind: no more draw items
 constexpr int kMaxB = 4096;
 constexpr int kMaxRowsPerReq = 2 * SV_MAX_GAMMA + 1;
 constexpr int kFlushSlots = 16;  // row pieces in flight between the fastest and slowest warp
@@ -80,11 +82,17 @@ struct Job {
     DrawParams d;
 };
 
+// What a draw-phase stage holds: chunk j of job k (kind kEndKind: none).
+struct StageDesc {
+    Job job;
+    int32_t k, j;
+};
+
 // Byte offsets into the caller's workspace and the partition constants.
 struct Layout {
     long long Et;  // target elements B*(gamma+1)*V
     int G, MT, MD, NCH, vec;
-    size_t hdr, req_done, job_done, clear_bytes, rec_t, rec_d, jobs, wsums, total;
+    size_t hdr, req_done, job_done, ready, clear_bytes, rec_t, rec_d, jobs, wsums, total;
 };
 
 __host__ __device__ inline long long part_begin(long long E, int G, int g, int vec) {
@@ -115,6 +123,7 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.hdr = take(256);
     L.req_done = take(static_cast<size_t>(B) * 4);  // logits folded, per request
     L.job_done = take(static_cast<size_t>(B) * 4);  // chunks summed, per draw job
+    L.ready = take(static_cast<size_t>(B) * 4);     // published draw jobs (k + 1), in order
     L.clear_bytes = off;                            // cleared before every launch
     L.rec_t = take(static_cast<size_t>(G) * L.MT * sizeof(Rec));
     L.rec_d = take(static_cast<size_t>(G) * L.MD * sizeof(Rec));
@@ -181,6 +190,12 @@ __device__ __forceinline__ void bulk_copy(void* dst_smem, const void* src, unsig
         : "memory");
 }
 
+// Adds v to a global counter with release semantics at GPU scope, without
+// waiting for the result.
+__device__ __forceinline__ void red_release_add(unsigned* addr, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -236,43 +251,10 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
 // ---------------------------------------------------------------- barriers
 
 struct Hdr {
-    unsigned count;
-    unsigned gen;
-    int status;
+    int status;          // SV_STATUS_* bits of this call
+    unsigned n_pub;      // draw jobs published so far
+    unsigned next_item;  // draw items handed out so far
 };
-
-// Grid-wide barrier of the co-resident grid; false (and SV_STATUS_TIMEOUT)
-// when the other blocks do not arrive within the time limit.
-__device__ bool grid_sync(Hdr* h, int32_t* d_status, int* s_flag, unsigned long long wait_ns) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        volatile unsigned* vgen = &h->gen;
-        const unsigned my_gen = *vgen;
-        __threadfence();
-        const unsigned prev = atomicAdd(&h->count, 1u);
-        int ok = 1;
-        if (prev == gridDim.x - 1) {
-            atomicExch(&h->count, 0u);
-            __threadfence();
-            atomicAdd(&h->gen, 1u);
-        } else {
-            const unsigned long long t0 = global_ns();
-            while (*vgen == my_gen) {
-                if (global_ns() - t0 > wait_ns) {
-                    ok = 0;
-                    atomicOr(&h->status, SV_STATUS_TIMEOUT);
-                    if (d_status) atomicOr(d_status, SV_STATUS_TIMEOUT);
-                    break;
-                }
-                __nanosleep(64);
-            }
-        }
-        __threadfence();
-        *s_flag = ok;
-    }
-    __syncthreads();
-    return *s_flag != 0;
-}
 
 // Checking output: global-timer stamps (see sv_debug_out.phase_ns).
 __device__ __forceinline__ void stamp(unsigned long long* slots, int i, bool who) {
@@ -294,12 +276,10 @@ struct Ctl {
     uint64_t empty[kStages];
     long long tbeg[kMaxGrid + 1];  // target partition
     long long dbeg[kMaxGrid + 1];  // draft partition (after the prologue)
-    Job jobs[kJobCache];           // draw phase: this block's draw jobs
+    StageDesc desc[kStages];       // draw phase: the item in each stage
     int n_samp;
     int k_lo;  // first compacted request of this block's draft slice
-    int job_lo, job_n;
     int abort;
-    int flag;
     int map[kMapMax];
     int wtmp[kConsumerWarps + 1];
     Rec wrec[kFlushSlots][kConsumerWarps];  // per-warp partials of a row piece
@@ -309,7 +289,7 @@ struct Ctl {
     unsigned fq_seq[kQueue];                // reservation number + 1 of the entry in the slot
     unsigned fq_tail;                       // reservations so far
     unsigned fq_head;                       // entries the finisher has taken
-    int cons_done[2];                       // consumer warps done with phase 1, phase 2
+    int cons_done;                          // consumer warps done with both phases
     short kmap[kMaxB];                      // compacted index of each T > 0 request, else -1
 };
 
@@ -362,6 +342,7 @@ struct Kern {
     __device__ Job* jobs() const { return reinterpret_cast<Job*>(ws + L.jobs); }
     __device__ unsigned* req_done() const { return reinterpret_cast<unsigned*>(ws + L.req_done); }
     __device__ unsigned* job_done() const { return reinterpret_cast<unsigned*>(ws + L.job_done); }
+    __device__ int* ready() const { return reinterpret_cast<int*>(ws + L.ready); }
     __device__ unsigned long long* wsums() const {
         return reinterpret_cast<unsigned long long*>(ws + L.wsums);
     }
@@ -420,18 +401,25 @@ struct Kern {
     };
 
     // Producer warp: fill the next stage with one copy, or two (the second at
-    // byte offset kChunkBytes); lane 0 issues.
+    // byte offset kChunkBytes); lane 0 issues. In the draw phase lane 0 first
+    // writes the stage's descriptor; `src` null with `desc` sends the end
+    // marker (the stage completes with no bytes).
     __device__ bool produce(Cursor& p, const char* src, unsigned bytes, const char* src2 = nullptr,
-                            unsigned bytes2 = 0) const {
+                            unsigned bytes2 = 0, const StageDesc* desc = nullptr) const {
         const int slot = p.it % kStages;
         const unsigned round = p.it / kStages;
         // the verdict is made warp-uniform so that a timeout cannot split the warp
         if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(&ctl.empty[slot], (round - 1) & 1))) return false;
         if ((threadIdx.x & 31) == 0) {
-            char* dst = stages + static_cast<size_t>(slot) * kStageBytes;
-            mbar_expect_tx(&ctl.full[slot], bytes + bytes2);
-            bulk_copy(dst, src, bytes, &ctl.full[slot]);
-            if (src2) bulk_copy(dst + kChunkBytes, src2, bytes2, &ctl.full[slot]);
+            if (desc) ctl.desc[slot] = *desc;
+            if (src) {
+                char* dst = stages + static_cast<size_t>(slot) * kStageBytes;
+                mbar_expect_tx(&ctl.full[slot], bytes + bytes2);
+                bulk_copy(dst, src, bytes, &ctl.full[slot]);
+                if (src2) bulk_copy(dst + kChunkBytes, src2, bytes2, &ctl.full[slot]);
+            } else {
+                mbar_arrive(&ctl.full[slot]);  // release: the descriptor is visible to the waiters
+            }
         }
         __syncwarp();
         ++p.it;
@@ -462,6 +450,56 @@ struct Kern {
         if (d_status) atomicOr(d_status, SV_STATUS_TIMEOUT);
     }
 
+    // Publishes draw job k (its record written by this thread): the producers
+    // of every block take draw items from the jobs in publication order.
+    __device__ void publish(int k) const {
+        __threadfence();
+        const unsigned p = atomicAdd(&hdr()->n_pub, 1u);
+        reinterpret_cast<volatile int*>(ready())[p] = k + 1;
+    }
+
+    // Finisher warp: the token searches of the jobs published at positions
+    // g, g + G, g + 2G, ... belong to block g, so that consecutive jobs, which
+    // complete at about the same time, are searched by different blocks. Lane
+    // 0 keeps the next owned position (own_p) and its job once published
+    // (own_k); a poll reads one global word and runs the search when the job's
+    // last chunk is counted. Returns whether it made progress.
+    __device__ bool poll_owned(int& own_p, int& own_k) const {
+        int k = -1, moved = 0;
+        if ((threadIdx.x & 31) == 0) {
+            const int ns = *reinterpret_cast<const volatile int*>(&ctl.n_samp);
+            if (own_p < ns) {
+                if (own_k < 0) {
+                    const int v = reinterpret_cast<const volatile int*>(ready())[own_p];
+                    if (v) {
+                        __threadfence();
+                        own_k = v - 1;
+                        const int kind = __ldcg(&jobs()[own_k].kind);
+                        if (kind != kKindResidual && kind != kKindBonus) {  // no items, no search
+                            own_p += G;
+                            own_k = -1;
+                            moved = 1;
+                        }
+                    }
+                }
+                if (own_k >= 0 &&
+                    reinterpret_cast<const volatile unsigned*>(job_done())[own_k] == static_cast<unsigned>(L.NCH)) {
+                    __threadfence();  // the other blocks' chunk sums before they are read
+                    k = own_k;
+                    own_p += G;
+                    own_k = -1;
+                }
+            }
+        }
+        k = __shfl_sync(0xffffffffu, k, 0);
+        moved = __shfl_sync(0xffffffffu, moved, 0);
+        if (k < 0) return moved != 0;
+        search_job(k);
+        __syncwarp();
+        stamp(reinterpret_cast<unsigned long long*>(a.dbg.phase_ns), 7, (threadIdx.x & 31) == 0);
+        return true;
+    }
+
     // ---- the finisher's message ring. One consumer lane posts a message once
     // this block's share of a request (phase 1) or of a draw job (phase 2) is
     // in global memory; the finisher warp adds the share to the item's global
@@ -488,27 +526,32 @@ struct Kern {
         return true;
     }
 
-    // A consumer warp is done with phase `ph` (after its last post).
-    __device__ void consumer_done(int ph) const {
+    // A consumer warp is done with both phases (after its last post).
+    __device__ void consumer_done() const {
         __syncwarp();
         if ((threadIdx.x & 31) == 0) {
             __threadfence_block();
-            atomicAdd(&ctl.cons_done[ph], 1);
+            atomicAdd(&ctl.cons_done, 1);
         }
     }
 
-    // Finisher warp: takes the ring's messages in batches of up to 32 until
-    // every consumer warp is done with phase `ph` and the ring is empty.
+    // Finisher warp: takes the ring's messages in batches of up to 32; with
+    // the ring empty it polls its owned token searches (at most every half
+    // microsecond). It returns once every consumer warp is done, the ring is
+    // empty and every owned search has run.
     // count(item, val), one lane per message, adds the share to the item's
-    // global counter and returns whether that completed the item;
-    // work(item), on the whole warp, then finishes each completed item.
+    // global counter (with the fences its reader needs) and returns whether
+    // that completed the item; work(item), on the whole warp, then finishes
+    // each completed item.
     template <typename C, typename W>
-    __device__ void finish(unsigned& head, int ph, C&& count, W&& work) const {
+    __device__ void finish(C&& count, W&& work) const {
         const int lane = threadIdx.x & 31;
         volatile unsigned* vseq = ctl.fq_seq;
-        volatile int* vdone = ctl.cons_done;
+        volatile int* vdone = &ctl.cons_done;
+        unsigned head = 0;
         volatile int* vabort = &ctl.abort;
-        unsigned long long t0 = global_ns();
+        unsigned long long t0 = global_ns(), last_poll = 0;
+        int own_p = blockIdx.x, own_k = -1;  // lane 0: next owned job position, its job
         for (;;) {
             const unsigned s = head + lane;
             const unsigned ready = __ballot_sync(0xffffffffu, vseq[s % kQueue] == s + 1);
@@ -525,11 +568,7 @@ struct Kern {
                 head += n;
                 if (lane == 0) *reinterpret_cast<volatile unsigned*>(&ctl.fq_head) = head;
                 bool completed = false;
-                if (lane < n) {
-                    __threadfence();  // this block's share is visible before it is counted
-                    completed = count(item, val);
-                    __threadfence();  // and the other blocks' shares before they are read
-                }
+                if (lane < n) completed = count(item, val);
                 unsigned done = __ballot_sync(0xffffffffu, completed);
                 while (done) {
                     const int src = __ffs(done) - 1;
@@ -540,11 +579,20 @@ struct Kern {
                 t0 = global_ns();
                 continue;
             }
+            if (global_ns() - last_poll > 500ull) {
+                if (poll_owned(own_p, own_k)) {
+                    t0 = global_ns();
+                    continue;
+                }
+                last_poll = global_ns();
+            }
             int stop = 0;
             if (lane == 0) {
-                if (vdone[ph] == kConsumerWarps) {
+                if (*vabort) {
+                    stop = 1;
+                } else if (*vdone == kConsumerWarps) {
                     __threadfence_block();
-                    if (*reinterpret_cast<volatile unsigned*>(&ctl.fq_tail) == head || *vabort) stop = 1;
+                    if (*reinterpret_cast<volatile unsigned*>(&ctl.fq_tail) == head && own_p >= ctl.n_samp) stop = 1;
                 }
                 if (!stop && global_ns() - t0 > kWaitTimeoutNs) {
                     set_abort(a.d_status);
@@ -890,7 +938,10 @@ struct Kern {
                 if (a.d_status) atomicOr(a.d_status, SV_STATUS_BAD_REQUEST);
                 if (dbg.kind) dbg.kind[b] = kKindInvalid;
                 if (dbg.w_total) dbg.w_total[b] = nan("");
-                if (k >= 0) jobs()[k].kind = kKindInvalid;
+                if (k >= 0) {  // its draw job is published as invalid (no items, no search)
+                    jobs()[k].kind = kKindInvalid;
+                    publish(k);
+                }
             }
             return;
         }
@@ -972,57 +1023,11 @@ struct Kern {
                 }
                 j.kind = d.kind;
                 jobs()[k] = j;
+                publish(k);
                 if (dbg.kind) dbg.kind[b] = d.kind;
             }
         }
     }
-
-    // ---- phase-2 schedule: draw items (job k, chunk j) of this block
-    __device__ static int job_cost(int kind) { return kind == kKindResidual ? 2 : (kind == kKindBonus ? 1 : 0); }
-
-    // The block's unit range and the first job with units after u_lo.
-    __device__ void item_range(const int* pre, long long& u_lo, long long& u_hi, int& k_first) const {
-        const int ns = ctl.n_samp;
-        const long long U = static_cast<long long>(pre[ns]) * L.NCH;
-        u_lo = part_begin(U, G, g, 1);
-        u_hi = part_begin(U, G, g + 1, 1);
-        int lo = 0, hi = ns - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (static_cast<long long>(pre[mid + 1]) * L.NCH > u_lo)
-                hi = mid;
-            else
-                lo = mid + 1;
-        }
-        k_first = lo;
-    }
-
-    // Calls f(k, j, last, cnt) for every item whose first cost unit falls in
-    // this block's share: item j of job k, whether it is the block's last item
-    // of job k, and how many items of job k the block has. `pre` holds the
-    // cost prefix over jobs (n_samp + 1).
-    template <typename F>
-    __device__ void for_each_item(const int* pre, F&& f) const {
-        const int ns = ctl.n_samp;
-        long long u_lo, u_hi;
-        int k0;
-        item_range(pre, u_lo, u_hi, k0);
-        if (u_hi <= u_lo) return;
-        for (int k = k0; k < ns; ++k) {
-            const int cost = pre[k + 1] - pre[k];
-            if (cost == 0) continue;
-            const long long base = static_cast<long long>(pre[k]) * L.NCH;
-            if (base >= u_hi) break;
-            int j0 = 0;
-            if (base < u_lo) j0 = static_cast<int>((u_lo - base + cost - 1) / cost);
-            // last item whose first unit is below u_hi
-            const int j1 = static_cast<int>(min(static_cast<long long>(L.NCH - 1), (u_hi - 1 - base) / cost));
-            for (int j = j0; j <= j1; ++j) f(k, j, j == j1, j1 - j0 + 1);
-            if (j1 < L.NCH - 1) return;
-        }
-    }
-
-    __device__ bool job_cached(int k) const { return k >= ctl.job_lo && k < ctl.job_lo + ctl.job_n; }
 
     // A run is kTPT consecutive tokens, 64 bytes, held packed as 4 vectors of
     // kTPV tokens. Its weight sum is defined vector by vector: S_q adds the
@@ -1343,7 +1348,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     char* stages = smem;
     Ctl& ctl = *reinterpret_cast<Ctl*>(smem + static_cast<size_t>(kStages) * kStageBytes);
     Rec* fin_rows = reinterpret_cast<Rec*>(smem + static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl));
-    int* pre = reinterpret_cast<int*>(fin_rows + kMaxRowsPerReq);
 
     using KT = Kern<DT>;
     KT K{a, L, ws, ctl, stages, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x)};
@@ -1358,10 +1362,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             mbar_init(&ctl.empty[s], kConsumerWarps);
         }
         ctl.abort = 0;
+        ctl.n_samp = -1;  // set by the consumers' prologue
         ctl.fq_tail = 0;
         ctl.fq_head = 0;
-        ctl.cons_done[0] = 0;
-        ctl.cons_done[1] = 0;
+        ctl.cons_done = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     for (int i = t; i < kMapMax; i += kThreads) ctl.map[i] = -1;
@@ -1369,15 +1373,50 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     for (int i = t; i < kQueue; i += kThreads) ctl.fq_seq[i] = 0;
     __syncthreads();
 
-    const long long ts = part_begin(L.Et, K.G, K.g, L.vec), te = part_begin(L.Et, K.G, K.g + 1, L.vec);
-    unsigned head = 0;  // finisher: ring entries taken
+    // ------------------------------------------------------------ finisher
+    if (finisher) {
+        // a request is scanned by the block whose share completes its 2 gamma + 1
+        // rows (gamma + 1 at T = 0); a draw job is searched by the block that
+        // sums its last chunk
+        const unsigned V = static_cast<unsigned>(a.V), GM = static_cast<unsigned>(a.gamma);
+        const unsigned NCH = static_cast<unsigned>(L.NCH);
+        unsigned* req_done = K.req_done();
+        unsigned* job_done = K.job_done();
+        K.finish(
+            [&](int item, unsigned share) {
+                if (item & kJobMsg) {
+                    // fire and forget: the job's owner polls the count; the
+                    // release orders this block's chunk sums before it
+                    red_release_add(job_done + (item & ~kJobMsg), share);
+                    return false;
+                }
+                const unsigned need = (KT::sampled(a.temperature[item]) ? 2 * GM + 1 : GM + 1) * V;
+                __threadfence();  // this block's row records are visible before they are counted
+                const bool done = atomicAdd(req_done + item, share) + share == need;
+                __threadfence();  // and the other blocks' records before they are read
+                return done;
+            },
+            [&](int item) {
+                if (!(item & kJobMsg)) {
+                    K.verify_request(item, fin_rows);
+                    stamp(ph, 3, lane == 0);
+                }
+            });
+        stamp(ph, 9, lane == 0);
+        return;
+    }
 
-    // ------------------------------------- phase 1 (+ acceptance scans on the finisher)
+    const long long ts = part_begin(L.Et, K.G, K.g, L.vec), te = part_begin(L.Et, K.G, K.g + 1, L.vec);
     typename KT::Cursor prod, cons;
+    constexpr int TPT = KT::kTPT;
+    constexpr int CH = KT::kChunkElems;
+    volatile int* vabort = &ctl.abort;
+
+    // ------------------------------------------------------------ producer
     if (producer) {
         bool ok = true;
         auto issue = [&](const Segment& sg) {
-            for (long long off = 0; off < sg.elems && ok && !ctl.abort; off += KT::kStageElems) {
+            for (long long off = 0; off < sg.elems && ok && !*vabort; off += KT::kStageElems) {
                 const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
                 ok = K.produce(prod, sg.src + off * KT::ES, static_cast<unsigned>(n * KT::ES));
             }
@@ -1385,196 +1424,186 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         K.for_each_target_segment(ts, te, issue);
         bar_sync(kBarHandoff, kHandoffThreads);  // the consumers' prologue is done
         K.for_each_draft_segment(issue);
-        if (!ok) K.set_abort(a.d_status);
-        if (ctl.abort) K.drain(prod);
-    } else if (finisher) {
-        // a request is scanned by the block whose share completes its 2 gamma + 1
-        // rows (gamma + 1 at T = 0), as soon as that share is folded
-        const unsigned V = static_cast<unsigned>(a.V), GM = static_cast<unsigned>(a.gamma);
-        unsigned* req_done = K.req_done();
-        K.finish(
-            head, 0,
-            [&](int b, unsigned share) {
-                const unsigned need = (KT::sampled(a.temperature[b]) ? 2 * GM + 1 : GM + 1) * V;
-                return atomicAdd(req_done + b, share) + share == need;
-            },
-            [&](int b) { K.verify_request(b, fin_rows); });
-        stamp(ph, 3, lane == 0);
-    } else {
-        // the ring fills with target stages while the consumers run the prologue
-        K.prologue();
-        bar_arrive(kBarHandoff, kHandoffThreads);
-        bool ok = true;
-        unsigned seq = 0;    // row pieces folded so far (the same on every consumer warp)
-        unsigned share = 0;  // elements of the current request folded in this slice
-        auto fold = [&](const Segment& sg) {
-            if (!ok) return;
-            typename KT::RowState rs;
-            K.start_row(rs, sg.loc);
-            for (long long off = 0; off < sg.elems; off += KT::kStageElems) {
-                const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
-                const char* sm = K.consume_begin(cons);
-                if (!sm) {
-                    ok = false;
-                    K.set_abort(a.d_status);
-                    return;
+        const int ns = ctl.n_samp;
+        if (ns > 0) {
+            // draw items i = 0 .. ns * NCH - 1: chunk i % NCH of the job published
+            // i / NCH-th, taken kGrab at a time from the global counter (the next
+            // batch is requested while the current one is issued)
+            if (a.hold_flag && ok && lane == 0) {  // checking only: a flag that holds the draw phase
+                const unsigned long long t0 = global_ns();
+                while (*reinterpret_cast<const volatile int32_t*>(a.hold_flag) == 0) {
+                    if (global_ns() - t0 > a.peer_wait_ns) {
+                        K.set_abort(a.d_status);
+                        break;
+                    }
+                    __nanosleep(256);
                 }
-                K.fold_stage(rs, sm, static_cast<int>(n * KT::ES / 16), sg.e0 + off);
-                K.consume_end(cons);
             }
-            share += static_cast<unsigned>(sg.elems);
-            K.flush_row(rs, sg.loc, seq++, sg.last ? share : 0u);
-            if (sg.last) share = 0;
-        };
-        K.for_each_target_segment(ts, te, fold);
-        K.for_each_draft_segment(fold);
-        K.consumer_done(0);
-        stamp(ph, 2, lane == 0);
-    }
-    __syncthreads();
-    const int ns = ctl.n_samp;
-    if (ns == 0) {  // every request greedy or invalid: nothing to draw
-        stamp(ph, 9, t == 0);
-        return;
-    }
-    Hdr* hdr = K.hdr();
-    if (!grid_sync(hdr, a.d_status, &ctl.flag, a.barrier_wait_ns)) return;
-    stamp(ph, 4, t == 0);
-    if (ctl.abort) return;
-
-    // ------------------------------------------- phase 2 (+ token searches on the finisher)
-    constexpr int TPT = KT::kTPT;
-    constexpr int CH = KT::kChunkElems;
-    if (producer) {
-        bar_sync(kBarHandoff, kHandoffThreads);  // the schedule is in shared memory
-        bool ok = true;
-        const Job* gjobs = K.jobs();
-        K.for_each_item(pre, [&](int k, int j, bool, int) {
-            if (!ok || ctl.abort) return;
-            const Job& jb = K.job_cached(k) ? ctl.jobs[k - ctl.job_lo] : gjobs[k];
-            const long long e0 = static_cast<long long>(j) * CH;
-            const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
-            const unsigned bytes = static_cast<unsigned>(cnt * KT::ES);
-            const long long trow = static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n;
-            const char* src_t = static_cast<const char*>(a.target) + (trow * a.V + e0) * KT::ES;
-            if (jb.kind == kKindResidual) {
-                const long long drow = static_cast<long long>(jb.b) * a.gamma + jb.n;
-                ok = K.produce(prod, src_t, bytes, static_cast<const char*>(a.draft) + (drow * a.V + e0) * KT::ES,
-                               bytes);
-            } else {
-                ok = K.produce(prod, src_t, bytes);
-            }
-        });
-        if (!ok) K.set_abort(a.d_status);
-        if (ctl.abort) K.drain(prod);
-        return;
-    }
-    if (finisher) {
-        // a job is searched by the block whose chunk sums complete it
-        const unsigned NCH = static_cast<unsigned>(L.NCH);
-        unsigned* job_done = K.job_done();
-        K.finish(
-            head, 1, [&](int k, unsigned cnt) { return atomicAdd(job_done + k, cnt) + cnt == NCH; },
-            [&](int k) { K.search_job(k); });
-        stamp(ph, 7, lane == 0);
-        stamp(ph, 9, lane == 0);
-        return;
-    }
-    // consumers: cost prefix over jobs, then this block's jobs into shared memory
-    {
-        const Job* gjobs = K.jobs();
-        int carry = 0;
-        for (int base = 0; base < ns; base += kConsumers) {
-            const int k = base + t;
-            const int cost = k < ns ? KT::job_cost(gjobs[k].kind) : 0;
-            int x = cost;
+            __syncwarp();
+            Hdr* h = K.hdr();
+            const long long n_items = static_cast<long long>(ns) * L.NCH;
+            unsigned next = 0;
+            if (lane == 0) next = atomicAdd(&h->next_item, static_cast<unsigned>(kGrab));
+            long long i = 0, i_end = 0;
+            int cur_p = -1;
+            StageDesc desc;  // lane 0's copy of the current job
+            desc.k = -1;
+            while (ok && !*vabort) {
+                if (i == i_end) {
+                    i = __shfl_sync(0xffffffffu, next, 0);
+                    i_end = i + kGrab;
+                    if (i >= n_items) break;
+                    if (lane == 0) next = atomicAdd(&h->next_item, static_cast<unsigned>(kGrab));
+                }
+                if (i >= n_items) break;
+                const int p = static_cast<int>(i / L.NCH), j = static_cast<int>(i - static_cast<long long>(p) * L.NCH);
+                if (p != cur_p) {
+                    // the p-th published job (bounded wait: it is published by the
+                    // finisher of the block that completes its request)
+                    int got = 1;
+                    if (lane == 0) {
+                        const volatile int* rd = K.ready();
+                        int v = rd[p];
+                        if (v == 0) {
+                            const unsigned long long t0 = global_ns();
+                            while ((v = rd[p]) == 0) {
+                                if (*vabort || global_ns() - t0 > a.peer_wait_ns) {
+                                    got = 0;
+                                    break;
+                                }
+                                __nanosleep(64);
+                            }
+                        }
+                        if (got) {
+                            __threadfence();
+                            desc.k = v - 1;
+                            const int* src = reinterpret_cast<const int*>(K.jobs() + desc.k);
+                            int* dst = reinterpret_cast<int*>(&desc.job);
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
+                            for (int q = 0; q < static_cast<int>(sizeof(Job) / 4); ++q) dst[q] = __ldcg(src + q);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+                        if (lane == 0) K.set_abort(a.d_status);
+                        ok = false;
+                        break;
+                    }
+                    if (cur_p < 0) stamp(ph, 4, lane == 0);
+                    cur_p = p;
+                }
+                const int kind = __shfl_sync(0xffffffffu, desc.job.kind, 0);
+                if (kind == kKindResidual || kind == kKindBonus) {
+                    const int b = __shfl_sync(0xffffffffu, desc.job.b, 0), n = __shfl_sync(0xffffffffu, desc.job.n, 0);
+                    desc.j = j;
+                    const long long e0 = static_cast<long long>(j) * CH;
+                    const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+                    const unsigned bytes = static_cast<unsigned>(cnt * KT::ES);
+                    const long long trow = static_cast<long long>(b) * (a.gamma + 1) + n;
+                    const char* src_t = static_cast<const char*>(a.target) + (trow * a.V + e0) * KT::ES;
+                    if (kind == kKindResidual) {
+                        const long long drow = static_cast<long long>(b) * a.gamma + n;
+                        ok = K.produce(prod, src_t, bytes,
+                                       static_cast<const char*>(a.draft) + (drow * a.V + e0) * KT::ES, bytes, &desc);
+                    } else {
+                        ok = K.produce(prod, src_t, bytes, nullptr, 0u, &desc);
+                    }
+                }
+                ++i;
             }
-            if (lane == 31) ctl.wtmp[warp] = x;
-            bar_sync(kBarConsumers, kConsumers);
-            int before = carry, total = 0;
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                if (w < warp) before += ctl.wtmp[w];
-                total += ctl.wtmp[w];
-            }
-            if (k < ns) pre[k] = before + x - cost;
-            carry += total;
-            bar_sync(kBarConsumers, kConsumers);
+            if (!ok && lane == 0) K.set_abort(a.d_status);
+            __syncwarp();
+            // the end marker, also after a failure (bounded: the consumers'
+            // own waits are bounded too)
+            StageDesc end;
+            end.job.kind = kEndKind;
+            end.k = -1;
+            end.j = -1;
+            K.produce(prod, nullptr, 0u, nullptr, 0u, &end);
         }
-        if (t == 0) pre[ns] = carry;
-        bar_sync(kBarConsumers, kConsumers);
-        long long u_lo, u_hi;
-        int k0;
-        K.item_range(pre, u_lo, u_hi, k0);
-        int k1 = k0;  // one past the last job with an item here
-        if (u_hi > u_lo) {
-            int lo = k0, hi = ns;
-            while (lo < hi) {  // first job whose units start at or after u_hi
-                const int mid = (lo + hi) >> 1;
-                if (static_cast<long long>(pre[mid]) * L.NCH >= u_hi)
-                    hi = mid;
-                else
-                    lo = mid + 1;
-            }
-            k1 = lo;
-        }
-        const int njobs = min(kJobCache, max(0, k1 - k0));
-        for (int i = t; i < njobs; i += kConsumers) ctl.jobs[i] = gjobs[k0 + i];
-        if (t == 0) {
-            ctl.job_lo = k0;
-            ctl.job_n = njobs;
-        }
-        bar_sync(kBarConsumers, kConsumers);
-        bar_arrive(kBarHandoff, kHandoffThreads);
-        stamp(ph, 5, t == 0);
+        if (!ok && lane == 0) K.set_abort(a.d_status);
+        if (*vabort) K.drain(prod);
+        return;
     }
+
+    // ------------------------------------------------------------ consumers
+    // the ring fills with target stages while the consumers run the prologue
+    K.prologue();
+    bar_arrive(kBarHandoff, kHandoffThreads);
     bool ok = true;
-    const Job* gjobs = K.jobs();
-    unsigned long long* wsums = K.wsums();
-    K.for_each_item(pre, [&](int k, int j, bool last, int cnt) {
+    unsigned seq = 0;    // row pieces folded so far (the same on every consumer warp)
+    unsigned share = 0;  // elements of the current request folded in this slice
+    auto fold = [&](const Segment& sg) {
         if (!ok) return;
-        const Job jb = K.job_cached(k) ? ctl.jobs[k - ctl.job_lo] : gjobs[k];
-        const long long e0 = static_cast<long long>(j) * CH;
-        const int n = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
-        const int valid = max(0, min(TPT, n - t * TPT));
-        typename KT::Run lt, ld;
-        const char* smt = K.consume_begin(cons);
-        if (!smt) {
-            ok = false;
-            K.set_abort(a.d_status);
-            return;
+        typename KT::RowState rs;
+        K.start_row(rs, sg.loc);
+        for (long long off = 0; off < sg.elems; off += KT::kStageElems) {
+            const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
+            const char* sm = K.consume_begin(cons);
+            if (!sm) {
+                ok = false;
+                K.set_abort(a.d_status);
+                return;
+            }
+            K.fold_stage(rs, sm, static_cast<int>(n * KT::ES / 16), sg.e0 + off);
+            K.consume_end(cons);
         }
-        if (valid > 0) {
-            KT::load_run_smem(smt, t, lt);
-            if (jb.kind == kKindResidual) KT::load_run_smem(smt + kChunkBytes, t, ld);
-        }
-        K.consume_end(cons);
-        const float run = valid > 0 ? KT::run_total_rotated(lt, ld, t, valid, jb.d, jb.kind) : 0.0f;
-        const unsigned long long wsum = warp_sum_u64(to_fixed(run, jb.d.fix));
-        if (lane == 0) {
-            wsums[(static_cast<size_t>(k) * L.NCH + j) * kConsumerWarps + warp] = wsum;
-            if (last) {
-                // the block's share of job k is stored once all 8 warps are here
-                const int fs = (k - ctl.job_lo) % kFlushSlots;
+        share += static_cast<unsigned>(sg.elems);
+        K.flush_row(rs, sg.loc, seq++, sg.last ? share : 0u);
+        if (sg.last) share = 0;
+    };
+    K.for_each_target_segment(ts, te, fold);
+    K.for_each_draft_segment(fold);
+    stamp(ph, 2, lane == 0);
+
+    if (ctl.n_samp > 0 && ok) {
+        // draw items until the producer's end marker; each warp stores the
+        // fixed-point sum of its 32 runs, and the last warp done with an item
+        // posts it to the finisher
+        unsigned long long* wsums = K.wsums();
+        for (unsigned iseq = 0;; ++iseq) {
+            const int slot = static_cast<int>(cons.it % kStages);
+            const char* smt = K.consume_begin(cons);
+            if (!smt) {
+                K.set_abort(a.d_status);
+                break;
+            }
+            const StageDesc ds = ctl.desc[slot];
+            if (ds.job.kind == kEndKind) {
+                K.consume_end(cons);
+                break;
+            }
+            const long long e0 = static_cast<long long>(ds.j) * CH;
+            const int n = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+            const int valid = max(0, min(TPT, n - t * TPT));
+            typename KT::Run lt, ld;
+            if (valid > 0) {
+                KT::load_run_smem(smt, t, lt);
+                if (ds.job.kind == kKindResidual) KT::load_run_smem(smt + kChunkBytes, t, ld);
+            }
+            K.consume_end(cons);
+            const float run = valid > 0 ? KT::run_total_rotated(lt, ld, t, valid, ds.job.d, ds.job.kind) : 0.0f;
+            const unsigned long long wsum = warp_sum_u64(to_fixed(run, ds.job.d.fix));
+            if (lane == 0) {
+                wsums[(static_cast<size_t>(ds.k) * L.NCH + ds.j) * kConsumerWarps + warp] = wsum;
+                // items continue the row pieces' numbering: a warp that starts
+                // the draw phase early never shares a slot with a piece that
+                // slower warps are still flushing
+                const int fs = static_cast<int>((seq + iseq) % kFlushSlots);
                 __threadfence_block();
                 if (atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1) {
                     __threadfence_block();
                     ctl.wcnt[fs] = 0;
-                    if (!K.post(k, static_cast<unsigned>(cnt))) K.set_abort(a.d_status);
+                    if (!K.post(ds.k | kJobMsg, 1u)) K.set_abort(a.d_status);
                 }
             }
         }
-    });
-    K.consumer_done(1);
+    }
+    K.consumer_done();
     stamp(ph, 6, lane == 0);
 }
 
 size_t smem_bytes() {
-    return static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl) + sizeof(Rec) * kMaxRowsPerReq +
-           sizeof(int) * (kMaxB + 1);
+    return static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl) + sizeof(Rec) * kMaxRowsPerReq;
 }
 
 }  // namespace
