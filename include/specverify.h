@@ -82,6 +82,8 @@ typedef int32_t sv_status;
 #define SV_STATUS_BAD_REQUEST 0x1 /* at least one request was invalid (-1) */
 #define SV_STATUS_TIMEOUT 0x2     /* a bounded wait inside a kernel ran out; the
                                      outputs of that call are not valid */
+#define SV_STATUS_TRUNCATED 0x4   /* spec_commit: not every emitted token of a request
+                                     fitted in its token buffer */
 
 /* Size limits checked before launch. */
 #define SV_MAX_GAMMA 64
@@ -233,6 +235,37 @@ const char* spec_verify_status_string(sv_status status);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int spec_verify_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Post-verify bookkeeping ("Accélérer Sonar grâce à la spéculation",
+ * §Planification MTP pour un jeton unique: a kernel inserts the next target
+ * tokens into their slots, so the accepted length needs no CPU
+ * synchronisation before the next step; "Speculative Decoding : accélérer
+ * l'inférence des LLM", §Principe et garanties mathématiques: a pass emits
+ * the n accepted draft tokens and one token of the target).
+ *
+ * Appends the tokens request b emitted, out_tokens[b, 0..n] with
+ * n = out_num_accepted[b], to token_buf[b] at seq_lens[b] and advances
+ * seq_lens[b]. All pointers are DEVICE pointers owned by the caller; the call
+ * enqueues one kernel on `stream` and returns without synchronising.
+ *   out_tokens        [B, gamma+1] int32 (spec_verify's output)
+ *   out_num_accepted  [B] int32
+ *   token_buf         [B, max_len] int32, row-major; updated in place
+ *   seq_lens          [B] int32; updated in place
+ *   next_input        [B] int32 or NULL: the last token of each history after
+ *                     the commit (the next draft step's input), -1 if empty
+ *   d_status          int32 or NULL; the kernel ORs in
+ *                     SV_STATUS_BAD_REQUEST: n outside [0, gamma], a negative
+ *                       emitted token, or seq_lens[b] outside [0, max_len];
+ *                       that request is left unchanged, next_input[b] = -1;
+ *                     SV_STATUS_TRUNCATED: not every emitted token fitted in
+ *                       max_len; the ones that fit are appended.
+ * Returns SV_ERR_INVALID_ARG for B < 0, gamma outside [1, SV_MAX_GAMMA],
+ * max_len < 1 or a NULL required pointer (nothing enqueued); B == 0 enqueues
+ * nothing. */
+sv_status spec_commit(const int32_t* out_tokens, const int32_t* out_num_accepted, int B, int gamma,
+                      int32_t* token_buf, int max_len, int32_t* seq_lens, int32_t* next_input,
+                      int32_t* d_status, sv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -23,6 +23,7 @@ SV_ERR_SCRATCH_LIMIT = 6
 SV_NOALLOC_SCRATCH_BYTES = 8 << 20
 SV_PHASE_SLOTS = 10
 SV_STATUS_BAD_REQUEST, SV_STATUS_TIMEOUT = 0x1, 0x2
+SV_STATUS_TRUNCATED = 0x4
 SV_MAX_GAMMA, SV_MAX_V = 64, 1 << 24
 SV_PATH_AUTO, SV_PATH_ROWWISE, SV_PATH_STREAMING = 0, 1, 2
 KIND_INVALID, KIND_GREEDY, KIND_RESIDUAL, KIND_BONUS = -1, 0, 1, 2
@@ -31,6 +32,7 @@ EXPORTED = (
     "spec_verify_workspace_size", "spec_verify", "spec_verify_ex",
     "spec_verify_host_staging_size", "spec_verify_host", "spec_verify_last_launch_count",
     "spec_verify_status_string", "spec_verify_version", "spec_verify_noalloc",
+    "spec_commit",
 )
 
 
@@ -66,8 +68,9 @@ def _declare(lib):
                                             ctypes.POINTER(_Options)]
     lib.spec_verify_host.argtypes = common + [vp, sz, vp]
     lib.spec_verify_noalloc.argtypes = common + [vp]
+    lib.spec_commit.argtypes = [vp, vp, int_, int_, vp, int_, vp, vp, vp, vp]
     for name in ("spec_verify_workspace_size", "spec_verify_host_staging_size", "spec_verify",
-                 "spec_verify_ex", "spec_verify_host", "spec_verify_noalloc"):
+                 "spec_verify_ex", "spec_verify_host", "spec_verify_noalloc", "spec_commit"):
         getattr(lib, name).restype = i32
     lib.spec_verify_status_string.argtypes = [i32]
     lib.spec_verify_status_string.restype = ctypes.c_char_p
@@ -248,3 +251,20 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, u_accept, u_s
         _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
         _ptr(out_num_accepted), _stream_handle(stream))
     _check(rc, "spec_verify_noalloc")
+
+
+def spec_commit(out_tokens, out_num_accepted, token_buf, seq_lens, next_input=None, status=None,
+                stream=None) -> None:
+    """``spec_commit``: append each request's emitted tokens to ``token_buf``
+    [B, max_len] int32 at ``seq_lens`` [B] int32 (both updated in place on the
+    GPU); ``next_input`` [B] int32 and ``status`` [1] int32 are optional CUDA
+    tensors. Enqueued on ``stream``; nothing is copied to the host."""
+    lib = load()
+    B, G1 = out_tokens.shape
+    for t in (out_tokens, out_num_accepted, token_buf, seq_lens):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("every array must be a contiguous CUDA tensor")
+    rc = lib.spec_commit(_ptr(out_tokens), _ptr(out_num_accepted), B, G1 - 1, _ptr(token_buf),
+                         token_buf.shape[1], _ptr(seq_lens), _ptr(next_input), _ptr(status),
+                         _stream_handle(stream))
+    _check(rc, "spec_commit")

@@ -23,7 +23,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(spec_verify\w*)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(spec_\w+)\s*\(", text)))
 
 
 def exported_symbols():
@@ -86,3 +86,14 @@ def test_no_device_is_reported_not_faked(lib):
     n = ctypes.c_size_t(0)
     assert lib.spec_verify_workspace_size(1, 1, 10, 0, ctypes.byref(n)) == sv.SV_ERR_UNSUPPORTED
     assert _call(lib) == sv.SV_ERR_UNSUPPORTED
+
+
+def test_commit_rejects_bad_arguments_before_launch(lib):
+    p = 0x1000
+    assert lib.spec_commit(p, p, -1, 4, p, 16, p, p, p, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_commit(p, p, 2, 0, p, 16, p, p, p, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_commit(p, p, 2, 65, p, 16, p, p, p, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_commit(p, p, 2, 4, p, 0, p, p, p, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_commit(0, p, 2, 4, p, 16, p, p, p, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_commit(p, p, 2, 4, p, 16, 0, p, p, None) == sv.SV_ERR_INVALID_ARG
+    assert lib.spec_commit(p, p, 0, 4, p, 16, p, p, p, None) == sv.SV_OK
