@@ -267,6 +267,34 @@ sv_status spec_commit(const int32_t* out_tokens, const int32_t* out_num_accepted
                       int32_t* token_buf, int max_len, int32_t* seq_lens, int32_t* next_input,
                       int32_t* d_status, sv_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Model-free draft tokens by n-gram (prompt) lookup ("Speculative Decoding :
+ * accélérer l'inférence des LLM", §N-gram lookup et variantes sans modèle:
+ * find the context's last n tokens earlier in the context and propose the
+ * tokens that followed them; §Mise en œuvre dans vLLM: prompt_lookup_min = 2,
+ * prompt_lookup_max = 5). The page leaves open which occurrence and what to
+ * do at the end of the history; this library takes: n from n_max down to
+ * n_min, the first (longest) n with an earlier occurrence wins; of its
+ * occurrences ending at or before L - 1 the latest is used; the proposal is
+ * the up to gamma tokens that follow it, cut at the end of the history.
+ *
+ * All pointers are DEVICE pointers owned by the caller; one kernel on
+ * `stream`, no synchronisation.
+ *   token_buf     [B, max_len] int32: request b's history is
+ *                 token_buf[b, :seq_lens[b]] (prompt and generated tokens)
+ *   seq_lens      [B] int32
+ *   draft_tokens  [B, gamma] int32 out: the proposal, then -1
+ *   num_draft     [B] int32 out: proposal length k in [0, gamma] (0: none)
+ *   d_status      int32 or NULL: ORs SV_STATUS_BAD_REQUEST for a length
+ *                 outside [0, max_len] (that request proposes nothing)
+ * Returns SV_ERR_INVALID_ARG for B < 0, max_len < 1, gamma outside
+ * [1, SV_MAX_GAMMA], n_min < 1, n_max < n_min, n_max > SV_NGRAM_MAX_N or a
+ * NULL required pointer; B == 0 enqueues nothing. */
+#define SV_NGRAM_MAX_N 16
+sv_status spec_ngram_propose(const int32_t* token_buf, int B, int max_len, const int32_t* seq_lens,
+                             int gamma, int n_min, int n_max, int32_t* draft_tokens, int32_t* num_draft,
+                             int32_t* d_status, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

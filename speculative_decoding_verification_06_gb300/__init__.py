@@ -32,7 +32,7 @@ EXPORTED = (
     "spec_verify_workspace_size", "spec_verify", "spec_verify_ex",
     "spec_verify_host_staging_size", "spec_verify_host", "spec_verify_last_launch_count",
     "spec_verify_status_string", "spec_verify_version", "spec_verify_noalloc",
-    "spec_commit",
+    "spec_commit", "spec_ngram_propose",
 )
 
 
@@ -69,8 +69,10 @@ def _declare(lib):
     lib.spec_verify_host.argtypes = common + [vp, sz, vp]
     lib.spec_verify_noalloc.argtypes = common + [vp]
     lib.spec_commit.argtypes = [vp, vp, int_, int_, vp, int_, vp, vp, vp, vp]
+    lib.spec_ngram_propose.argtypes = [vp, int_, int_, vp, int_, int_, int_, vp, vp, vp, vp]
     for name in ("spec_verify_workspace_size", "spec_verify_host_staging_size", "spec_verify",
-                 "spec_verify_ex", "spec_verify_host", "spec_verify_noalloc", "spec_commit"):
+                 "spec_verify_ex", "spec_verify_host", "spec_verify_noalloc", "spec_commit",
+                 "spec_ngram_propose"):
         getattr(lib, name).restype = i32
     lib.spec_verify_status_string.argtypes = [i32]
     lib.spec_verify_status_string.restype = ctypes.c_char_p
@@ -268,3 +270,24 @@ def spec_commit(out_tokens, out_num_accepted, token_buf, seq_lens, next_input=No
                          token_buf.shape[1], _ptr(seq_lens), _ptr(next_input), _ptr(status),
                          _stream_handle(stream))
     _check(rc, "spec_commit")
+
+
+def spec_ngram_propose(token_buf, seq_lens, gamma, n_min=2, n_max=5, draft_tokens=None, num_draft=None,
+                       status=None, stream=None):
+    """``spec_ngram_propose``: n-gram lookup drafts from each history
+    ``token_buf[b, :seq_lens[b]]`` (CUDA int32 tensors). Returns
+    ``(draft_tokens [B, gamma], num_draft [B])`` CUDA int32 tensors."""
+    import torch
+    lib = load()
+    B, max_len = token_buf.shape
+    for t in (token_buf, seq_lens):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("token_buf and seq_lens must be contiguous CUDA tensors")
+    if draft_tokens is None:
+        draft_tokens = torch.empty((B, gamma), dtype=torch.int32, device=token_buf.device)
+    if num_draft is None:
+        num_draft = torch.empty((B,), dtype=torch.int32, device=token_buf.device)
+    rc = lib.spec_ngram_propose(_ptr(token_buf), B, max_len, _ptr(seq_lens), gamma, n_min, n_max,
+                                _ptr(draft_tokens), _ptr(num_draft), _ptr(status), _stream_handle(stream))
+    _check(rc, "spec_ngram_propose")
+    return draft_tokens, num_draft

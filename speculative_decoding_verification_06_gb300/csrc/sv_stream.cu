@@ -1379,7 +1379,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         // rows (gamma + 1 at T = 0); a draw job is searched by the block that
         // sums its last chunk
         const unsigned V = static_cast<unsigned>(a.V), GM = static_cast<unsigned>(a.gamma);
-        const unsigned NCH = static_cast<unsigned>(L.NCH);
         unsigned* req_done = K.req_done();
         unsigned* job_done = K.job_done();
         K.finish(

@@ -97,3 +97,21 @@ def test_commit_rejects_bad_arguments_before_launch(lib):
     assert lib.spec_commit(0, p, 2, 4, p, 16, p, p, p, None) == sv.SV_ERR_INVALID_ARG
     assert lib.spec_commit(p, p, 2, 4, p, 16, 0, p, p, None) == sv.SV_ERR_INVALID_ARG
     assert lib.spec_commit(p, p, 0, 4, p, 16, p, p, p, None) == sv.SV_OK
+
+
+def test_ngram_rejects_bad_arguments_before_launch(lib):
+    p = 0x1000
+    ok = dict(B=2, max_len=16, gamma=4, n_min=2, n_max=5)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return lib.spec_ngram_propose(kw.get("buf", p), a["B"], a["max_len"], kw.get("lens", p), a["gamma"],
+                                      a["n_min"], a["n_max"], p, p, p, None)
+    assert call(B=-1) == sv.SV_ERR_INVALID_ARG
+    assert call(max_len=0) == sv.SV_ERR_INVALID_ARG
+    assert call(gamma=0) == sv.SV_ERR_INVALID_ARG
+    assert call(n_min=0) == sv.SV_ERR_INVALID_ARG
+    assert call(n_min=4, n_max=3) == sv.SV_ERR_INVALID_ARG
+    assert call(n_max=17) == sv.SV_ERR_INVALID_ARG
+    assert call(buf=0) == sv.SV_ERR_INVALID_ARG
+    assert call(B=0) == sv.SV_OK

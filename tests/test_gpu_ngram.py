@@ -1,0 +1,89 @@
+"""spec_ngram_propose against its oracle through the C ABI: the hand-worked
+cases, random histories over small vocabularies (many repeats and ties),
+copy-heavy synthetic histories up to 8192 tokens, and every n range.
+Integer work: exact equality."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import ngram
+from workloads import synthetic
+
+pytestmark = pytest.mark.gpu
+
+sv = pytest.importorskip("speculative_decoding_verification_06_gb300")
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    sv.build.build()
+    sv.load()
+    torch.cuda.set_device(0)
+
+
+def _gpu(buf, lens, gamma, n_min=2, n_max=5):
+    import torch
+    tb = torch.from_numpy(np.ascontiguousarray(buf, dtype=np.int32)).cuda()
+    sl = torch.from_numpy(np.ascontiguousarray(lens, dtype=np.int32)).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, num = sv.spec_ngram_propose(tb, sl, gamma, n_min, n_max, status=st)
+    torch.cuda.synchronize()
+    assert sv.last_launch_count() == 1
+    return out.cpu().numpy(), num.cpu().numpy(), int(st.item())
+
+
+def _check(buf, lens, gamma, n_min=2, n_max=5):
+    got = _gpu(buf, lens, gamma, n_min, n_max)
+    want = ngram.propose(buf, lens, gamma, n_min, n_max)
+    assert np.array_equal(got[0], want[0])
+    assert np.array_equal(got[1], want[1])
+    assert got[2] == want[2]
+
+
+def test_hand_cases():
+    with open(os.path.join(HERE, "golden", "ngram_cases.json")) as f:
+        g = json.load(f)
+    n = len(g["cases"])
+    buf = np.full((n + 1, g["max_len"]), 777, dtype=np.int32)
+    lens = np.zeros(n + 1, dtype=np.int32)
+    for i, c in enumerate(g["cases"]):
+        buf[i, :len(c["hist"])] = c["hist"]
+        lens[i] = len(c["hist"])
+    lens[-1] = g["bad_length_case"]["seq_len"]
+    out, num, st = _gpu(buf, lens, g["gamma"], g["n_min"], g["n_max"])
+    for i, c in enumerate(g["cases"]):
+        assert out[i].tolist() == c["expect"], c["name"]
+        assert num[i] == c["k"], c["name"]
+    assert num[-1] == 0 and st == g["bad_length_case"]["expect_status"]
+
+
+@pytest.mark.parametrize("vocab", [2, 3, 7, 1000])
+def test_random_small_vocab(vocab):
+    rng = np.random.default_rng(vocab)
+    B, M = 300, 200
+    buf = rng.integers(0, vocab, (B, M)).astype(np.int32)
+    lens = rng.integers(0, M + 1, B).astype(np.int32)
+    lens[:3] = [0, 1, M]
+    for gamma in (1, 4, 9):
+        _check(buf, lens, gamma)
+
+
+@pytest.mark.parametrize("n_min,n_max", [(1, 1), (2, 5), (3, 3), (1, 16)])
+def test_n_ranges(n_min, n_max):
+    rng = np.random.default_rng(n_min * 100 + n_max)
+    B, M = 128, 300
+    buf = rng.integers(0, 4, (B, M)).astype(np.int32)
+    lens = rng.integers(0, M + 1, B).astype(np.int32)
+    _check(buf, lens, 6, n_min, n_max)
+
+
+def test_copy_heavy_histories():
+    h = synthetic.histories(64, 8192, (1, 8192), vocab=32000, copy_prob=0.5, seed=5)
+    _check(h.token_buf, h.seq_lens, 4)
+    _check(h.token_buf, h.seq_lens, 8)

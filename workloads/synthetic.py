@@ -205,3 +205,38 @@ def generate(w: Workload | int | str, k: int = 0, B: int | None = None,
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(lambda b: _gen_request(w, seed, b, bias, out), range(w.B)))
     return out
+
+
+# ---------------------------------------------------------------- token histories
+
+@dataclass
+class Histories:
+    """Token histories for the n-gram proposer and the commit step."""
+    token_buf: np.ndarray  # [B, max_len] int32, padding 0
+    seq_lens: np.ndarray   # [B] int32
+
+
+def histories(B: int, max_len: int, lengths=(256, 4096), vocab: int = 32000, copy_prob: float = 0.5,
+              span=(4, 32), seed: int = 0) -> Histories:
+    """Synthetic histories shaped like the workloads n-gram lookup targets
+    (summaries, extraction, code rewriting, RAG): each request draws a length
+    L ~ U[lengths], a random prefix of L // 4 tokens (the prompt), then extends
+    it in spans: with probability ``copy_prob`` a span copies tokens from a
+    random earlier position, otherwise it is fresh random tokens. Span lengths
+    ~ U[span]. Request b uses the Philox stream SeedSequence([seed, b])."""
+    buf = np.zeros((B, max_len), dtype=np.int32)
+    lens = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        rng = request_rng(seed, b)
+        L = int(min(max_len, rng.integers(lengths[0], lengths[1] + 1)))
+        h = list(rng.integers(0, vocab, max(1, L // 4)))
+        while len(h) < L:
+            s = int(rng.integers(span[0], span[1] + 1))
+            if rng.random() < copy_prob and len(h) > 1:
+                j = int(rng.integers(0, len(h) - 1))
+                h.extend(h[j:j + s])
+            else:
+                h.extend(rng.integers(0, vocab, s))
+        buf[b, :L] = np.asarray(h[:L], dtype=np.int32)
+        lens[b] = L
+    return Histories(buf, lens)
