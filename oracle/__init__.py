@@ -65,6 +65,11 @@ def _bind(lib):
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_Detail)]
+    lib.oracle_spec_verify_onehot.restype = ctypes.c_int
+    lib.oracle_spec_verify_onehot.argtypes = [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_Detail)]
     lib.oracle_version.restype = ctypes.c_int
     return lib
 
@@ -117,14 +122,7 @@ def verify(target, draft, tokens, u_accept, u_sample, temperature, detail=False,
     det = None
     dptr = None
     if detail:
-        det = {
-            "max_target": np.empty((B, G1)), "lse_target": np.empty((B, G1)),
-            "argmax_target": np.empty((B, G1), dtype=np.int32),
-            "max_draft": np.empty((B, G)), "lse_draft": np.empty((B, G)),
-            "p_x": np.empty((B, G)), "q_x": np.empty((B, G)), "alpha": np.empty((B, G)),
-            "accept_margin": np.empty((B, G)), "w_total": np.empty((B,)),
-            "sample_margin": np.empty((B,)), "kind": np.empty((B,), dtype=np.int32),
-        }
+        det = _detail_arrays(B, G)
         d = _Detail(**{k: _ptr(v) for k, v in det.items()})
         dptr = ctypes.byref(d)
     rc = lib.oracle_spec_verify(
@@ -133,6 +131,47 @@ def verify(target, draft, tokens, u_accept, u_sample, temperature, detail=False,
         _ptr(out_tokens), _ptr(num_acc), dptr)
     if rc != 0:
         raise ValueError("oracle_spec_verify rejected its arguments")
+    return out_tokens, num_acc, det
+
+
+def _detail_arrays(B, G):
+    G1 = G + 1
+    return {
+            "max_target": np.empty((B, G1)), "lse_target": np.empty((B, G1)),
+            "argmax_target": np.empty((B, G1), dtype=np.int32),
+            "max_draft": np.empty((B, G)), "lse_draft": np.empty((B, G)),
+            "p_x": np.empty((B, G)), "q_x": np.empty((B, G)), "alpha": np.empty((B, G)),
+            "accept_margin": np.empty((B, G)), "w_total": np.empty((B,)),
+            "sample_margin": np.empty((B,)), "kind": np.empty((B,), dtype=np.int32),
+    }
+
+
+def verify_onehot(target, tokens, num_draft, u_accept, u_sample, temperature, detail=False, lib=None):
+    """The oracle for deterministic (one-hot) proposals: ``num_draft`` [B]
+    int32 proposals per request, no draft logits. Returns
+    ``(out_tokens, num_accepted, det)`` like ``verify``."""
+    lib = lib or load()
+    target = np.ascontiguousarray(target)
+    B, G1, V = target.shape
+    G = G1 - 1
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, G)
+    num_draft = np.ascontiguousarray(num_draft, dtype=np.int32).reshape(B)
+    u_accept = np.ascontiguousarray(u_accept, dtype=np.float32).reshape(B, G)
+    u_sample = np.ascontiguousarray(u_sample, dtype=np.float32).reshape(B)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+    out_tokens = np.full((B, G1), -7, dtype=np.int32)
+    num_acc = np.full((B,), -7, dtype=np.int32)
+    det = None
+    dptr = None
+    if detail:
+        det = _detail_arrays(B, G)
+        d = _Detail(**{k: _ptr(v) for k, v in det.items()})
+        dptr = ctypes.byref(d)
+    rc = lib.oracle_spec_verify_onehot(
+        _ptr(target), dtype_code(target), B, G, V, _ptr(tokens), _ptr(num_draft),
+        _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens), _ptr(num_acc), dptr)
+    if rc != 0:
+        raise ValueError("oracle_spec_verify_onehot rejected its arguments")
     return out_tokens, num_acc, det
 
 

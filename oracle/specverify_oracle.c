@@ -317,3 +317,159 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype, int B, 
     free(s.lt), free(s.ld), free(s.p), free(s.q), free(s.w);
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Deterministic proposals ("Speculative Decoding : accélérer l'inférence des
+ * LLM", §N-gram lookup et variantes sans modèle: the draft tokens come from a
+ * lookup, not from a model). Such a proposer puts all its probability on the
+ * token it proposes: q_i is one-hot at x_i. The rule of §Pourquoi la qualité
+ * est préservée then reads: alpha_i = min(1, p_i(x_i) / 1) = min(1, p_i(x_i));
+ * the residual max(p_n - q_n, 0) is p_n with the weight of x_n set to zero.
+ * Request b proposes k = num_draft[b] tokens (0 <= k <= gamma); the extra token
+ * after k acceptances comes from target row k. Target rows past k are not part
+ * of the request and are never read. */
+
+static int request_valid_onehot(const scratch_t* s, int b, double T, const int32_t* tok, int k) {
+    const int G = s->gamma, V = s->V;
+    if (isnan(T) || isinf(T) || T < 0.0) return 0;
+    if (k < 0 || k > G) return 0;
+    for (int i = 0; i < k; ++i)
+        if (tok[i] < 0 || tok[i] >= V) return 0;
+    for (int i = 0; i <= k; ++i) {
+        load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
+        if (!row_usable(s->lt, V)) return 0;
+    }
+    return 1;
+}
+
+static void report_rows_onehot(const scratch_t* s, int b, double T, int k, const oracle_detail* d) {
+    const int G = s->gamma, V = s->V;
+    for (int i = 0; i <= k; ++i) {
+        size_t r = (size_t)b * (size_t)(G + 1) + (size_t)i;
+        load_row(s->target, s->dtype, r, V, s->lt);
+        set_d(d->max_target, r, row_max(s->lt, V));
+        set_i(d->argmax_target, r, row_argmax(s->lt, V));
+        if (T > 0.0) set_d(d->lse_target, r, softmax_T(s->lt, V, T, s->p));
+    }
+}
+
+/* T == 0: as verify_greedy, over the k proposals; the extra token is the
+ * argmax of target row k. */
+static int verify_greedy_onehot(const scratch_t* s, int b, const int32_t* tok, int k, int32_t* out) {
+    const int G = s->gamma, V = s->V;
+    for (int i = 0; i < k; ++i) {
+        load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
+        int a = row_argmax(s->lt, V);
+        if (tok[i] == a) {
+            out[i] = tok[i];
+        } else {
+            out[i] = a; /* the target's argmax replaces the proposal */
+            return i;
+        }
+    }
+    load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)k, V, s->lt);
+    out[k] = row_argmax(s->lt, V);
+    return k;
+}
+
+/* T > 0 with q_i one-hot at x_i. */
+static int verify_sampled_onehot(const scratch_t* s, int b, double T, const int32_t* tok, int k,
+                                 const float* ua, float us, int32_t* out, const oracle_detail* d) {
+    const int G = s->gamma, V = s->V;
+    int n = k;
+    for (int i = 0; i < k; ++i) {
+        size_t r = (size_t)b * (size_t)G + (size_t)i;
+        const int x = tok[i];
+        load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
+        softmax_T(s->lt, V, T, s->p);
+        double px = s->p[x], qx = 1.0; /* q_i(x_i) of a one-hot proposal */
+        double alpha = fmin(1.0, px / qx);
+        double u = (double)ua[i];
+        set_d(d->p_x, r, px);
+        set_d(d->q_x, r, qx);
+        set_d(d->alpha, r, alpha);
+        set_d(d->accept_margin, r, alpha > 0.0 ? fabs(u - alpha) / alpha : INFINITY);
+        if (alpha > u) {
+            out[i] = x; /* accepted */
+        } else {
+            n = i; /* the first rejection */
+            break;
+        }
+    }
+    double W = 0.0;
+    if (n < k) {
+        /* s->p holds p_n; q_n is one-hot at x_n */
+        for (int x = 0; x < V; ++x) {
+            double diff = s->p[x] - (x == tok[n] ? 1.0 : 0.0);
+            s->w[x] = diff > 0.0 ? diff : 0.0;
+            W += s->w[x];
+        }
+        if (W == 0.0) /* unreachable in exact arithmetic: fall back to p_n */
+            memcpy(s->w, s->p, sizeof(double) * (size_t)V);
+        set_i(d->kind, (size_t)b, ORACLE_KIND_RESIDUAL);
+    } else {
+        load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)k, V, s->lt);
+        softmax_T(s->lt, V, T, s->p);
+        memcpy(s->w, s->p, sizeof(double) * (size_t)V);
+        set_i(d->kind, (size_t)b, ORACLE_KIND_BONUS);
+    }
+    double margin = 0.0;
+    out[n] = draw_inverse_cdf(s->w, V, (double)us, &W, &margin);
+    set_d(d->w_total, (size_t)b, W);
+    set_d(d->sample_margin, (size_t)b, margin);
+    return n;
+}
+
+int oracle_spec_verify_onehot(const void* target, int dtype, int B, int gamma, int V,
+                              const int32_t* tokens, const int32_t* num_draft,
+                              const float* u_accept, const float* u_sample,
+                              const float* temperature, int32_t* out_tokens,
+                              int32_t* out_num_accepted, const oracle_detail* detail) {
+    if (B < 0 || gamma < 1 || V < 1) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+    if (B == 0) return 0;
+    if (!target || !tokens || !num_draft || !u_accept || !u_sample || !temperature || !out_tokens ||
+        !out_num_accepted)
+        return -1;
+    oracle_detail none;
+    memset(&none, 0, sizeof none);
+    const oracle_detail* d = detail ? detail : &none;
+
+    scratch_t s;
+    memset(&s, 0, sizeof s);
+    s.target = target;
+    s.dtype = dtype;
+    s.gamma = gamma;
+    s.V = V;
+    s.lt = (double*)malloc(sizeof(double) * (size_t)V);
+    s.p = (double*)malloc(sizeof(double) * (size_t)V);
+    s.w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!s.lt || !s.p || !s.w) {
+        free(s.lt), free(s.p), free(s.w);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
+        int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
+        double T = (double)temperature[b];
+        int k = num_draft[b];
+        for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
+        clear_detail(d, b, gamma);
+        if (!request_valid_onehot(&s, b, T, tok, k)) {
+            out_num_accepted[b] = -1;
+            continue;
+        }
+        if (detail) report_rows_onehot(&s, b, T, k, d);
+        if (T == 0.0) {
+            set_i(d->kind, (size_t)b, ORACLE_KIND_GREEDY);
+            out_num_accepted[b] = verify_greedy_onehot(&s, b, tok, k, out);
+        } else {
+            out_num_accepted[b] = verify_sampled_onehot(&s, b, T, tok, k,
+                                                        u_accept + (size_t)b * (size_t)gamma,
+                                                        u_sample[b], out, d);
+        }
+    }
+    free(s.lt), free(s.p), free(s.w);
+    return 0;
+}
+

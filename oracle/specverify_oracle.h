@@ -101,6 +101,17 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype,
 
 int oracle_version(void);
 
+/* The same step for deterministic proposals (n-gram lookup): q_i is one-hot
+ * at x_i, so alpha_i = min(1, p_i(x_i)) and the residual is p_n without x_n.
+ * Request b proposes num_draft[b] in [0, gamma] tokens (outside: invalid);
+ * target rows past num_draft[b] are never read; tokens past it are ignored.
+ * No draft logits. Detail: q_x = 1 at the evaluated positions, draft rows NaN. */
+int oracle_spec_verify_onehot(const void* target, int dtype, int B, int gamma, int V,
+                              const int32_t* tokens, const int32_t* num_draft,
+                              const float* u_accept, const float* u_sample,
+                              const float* temperature, int32_t* out_tokens,
+                              int32_t* out_num_accepted, const oracle_detail* detail);
+
 #ifdef __cplusplus
 }
 #endif

@@ -382,6 +382,88 @@ def pin_invalid_requests(lib, quick=False):
     assert np.all(n4 == 1) and np.all(out4[:, 0] == 2)
 
 
+# ------------------------------------------------- one-hot (n-gram) proposals
+
+GOLDEN_ONEHOT = os.path.join(os.path.dirname(__file__), "golden", "onehot_v4.json")
+
+
+def pin_onehot_hand_examples(lib, quick=False):
+    """The constructed V=4 one-hot cases, worked by hand (golden/onehot_v4.json)."""
+    g = json.load(open(GOLDEN_ONEHOT))
+    P = np.array(g["target_p"], dtype=np.float64)
+    for c in g["cases"]:
+        G = c["gamma"]
+        lt = np.log(P[:G + 1]).astype(np.float32)[None]
+        if "nan_row" in c:
+            lt[0, c["nan_row"], :] = np.nan
+        out, n, _ = oracle.verify_onehot(lt, np.array([c["tokens"]]), np.array([c["k"]]),
+                                         np.array([c["u_accept"]], np.float32), np.array([c["u_sample"]], np.float32),
+                                         np.array([c["T"]], np.float32), lib=lib)
+        assert out[0].tolist() == c["out"] and n[0] == c["n"], (c["name"], out, n)
+
+
+def pin_onehot_is_the_general_rule(lib, quick=False):
+    """With q written out as one-hot draft logits (0 at x, -inf elsewhere) the
+    general rule, pinned above, gives the same outputs and the same p(x),
+    alpha and W as the one-hot entry point."""
+    rng = np.random.Generator(np.random.Philox(77))
+    B, G, V = (64 if quick else 512), 4, 24
+    lt = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    ld = np.full((B, G, V), -np.inf, np.float32)
+    np.put_along_axis(ld, x[:, :, None], 0.0, axis=2)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    T = rng.choice(np.array([0.0, 0.5, 1.0, 2.0], np.float32), B)
+    o1, n1, d1 = oracle.verify_onehot(lt, x, np.full(B, G, np.int32), ua, us, T, detail=True, lib=lib)
+    o2, n2, d2 = _run(lib, lt, ld, x, ua, us, T, detail=True)
+    assert np.array_equal(o1, o2) and np.array_equal(n1, n2)
+    for key in ("p_x", "alpha", "w_total"):
+        assert np.allclose(d1[key], d2[key], rtol=1e-12, atol=0, equal_nan=True), key
+
+
+def pin_onehot_accept_probability_and_distribution(lib, quick=False):
+    """A deterministic proposal x is accepted with probability p(x) (q(x) = 1),
+    and the first emitted token follows p exactly (chi-square at V = 8)."""
+    N = 20000 if quick else 400000
+    rng = np.random.Generator(np.random.Philox(91))
+    lt1 = rng.normal(0, 1.5, (2, 8)).astype(np.float32)
+    p0 = special.softmax(lt1[0].astype(np.float64))
+    x0 = int(np.argsort(p0)[4])  # a mid-probability proposal
+    lt = np.ascontiguousarray(np.broadcast_to(lt1, (N, 2, 8)))
+    ua = rng.random((N, 1), dtype=np.float32)
+    us = rng.random(N, dtype=np.float32)
+    out, n, _ = oracle.verify_onehot(lt, np.full((N, 1), x0, np.int32), np.ones(N, np.int32), ua, us,
+                                     np.ones(N, np.float32), lib=lib)
+    acc = (n == 1).mean()
+    _within_5_sigma(acc, p0[x0], np.sqrt(p0[x0] * (1 - p0[x0])), N, "one-hot P(accept)")
+    _chi2_ok(np.bincount(out[:, 0], minlength=8), p0, "one-hot first token")
+
+
+def pin_onehot_rows_past_k_unread(lib, quick=False):
+    """Request b proposes k_b tokens: rows past k_b take no part (NaN there is
+    not an error) and the result equals the same request cut to gamma = k_b."""
+    rng = np.random.Generator(np.random.Philox(55))
+    B, G, V = 40, 5, 16
+    lt = rng.normal(0, 1, (B, G + 1, V)).astype(np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    T = np.where(np.arange(B) % 4 == 0, 0.0, 0.9).astype(np.float32)
+    k = (np.arange(B) % (G + 1)).astype(np.int32)
+    lt_nan = lt.copy()
+    for b in range(B):
+        lt_nan[b, k[b] + 1:, :] = np.nan
+    out, n, _ = oracle.verify_onehot(lt_nan, x, k, ua, us, T, lib=lib)
+    for b in range(B):
+        kb = int(k[b])
+        g = max(kb, 1)
+        o1, n1, _ = oracle.verify_onehot(lt[b:b + 1, :g + 1], x[b:b + 1, :g], k[b:b + 1], ua[b:b + 1, :g],
+                                         us[b:b + 1], T[b:b + 1], lib=lib)
+        assert n[b] == n1[0] and out[b, :g + 1].tolist() == o1[0].tolist(), b
+        assert np.all(out[b, g + 1:] == -1)
+
+
 ALL_PINS = [
     pin_hand_examples,
     pin_accept_probability,
@@ -394,4 +476,8 @@ ALL_PINS = [
     pin_residual_mass_identity,
     pin_equal_rows_reduce_to_categorical,
     pin_invalid_requests,
+    pin_onehot_hand_examples,
+    pin_onehot_is_the_general_rule,
+    pin_onehot_accept_probability_and_distribution,
+    pin_onehot_rows_past_k_unread,
 ]

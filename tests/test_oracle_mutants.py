@@ -53,6 +53,12 @@ MUTANTS = [
     ("q_zero_rejects", "alpha = px > 0.0 ? 1.0 : 0.0;", "alpha = 0.0;"),
     ("nan_not_detected", "if (isnan(l[x])) return 0;", "if (0) return 0;"),
     ("draw_from_first_token", "        if (C > t) {", "        if (C >= 0.0) {"),
+    # deterministic (one-hot) proposals
+    ("onehot_residual_keeps_x", "double diff = s->p[x] - (x == tok[n] ? 1.0 : 0.0);", "double diff = s->p[x];"),
+    ("onehot_alpha_always_one", "double alpha = fmin(1.0, px / qx);", "double alpha = 1.0;"),
+    ("onehot_bonus_from_row_gamma", "(size_t)b * (size_t)(G + 1) + (size_t)k, V, s->lt);\n        softmax_T",
+     "(size_t)b * (size_t)(G + 1) + (size_t)G, V, s->lt);\n        softmax_T"),
+    ("onehot_count_ignored", "        int k = num_draft[b];", "        int k = gamma;"),
 ]
 
 
