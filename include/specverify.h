@@ -168,12 +168,16 @@ typedef struct {
                                  it is non-zero before its draw phase. A flag nothing sets
                                  makes every such wait run out, which exercises the
                                  SV_STATUS_TIMEOUT report deterministically. */
-    int32_t reserved[2];
+    const int32_t* num_draft; /* one-hot proposals only (draft_logits NULL): device [B]
+                                 int32 proposals per request, see spec_verify_onehot;
+                                 NULL = gamma each */
 } sv_options;
 
 /* spec_verify with checking outputs and options. `dbg`, `d_status` and
  * `opts` may be NULL. `d_status` is a device int32 into which the kernels OR
- * SV_STATUS_* bits; the caller clears it. */
+ * SV_STATUS_* bits; the caller clears it. `draft_logits` NULL selects
+ * deterministic (one-hot) proposals with opts->num_draft, as
+ * spec_verify_onehot. */
 sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype dtype,
                          int B, int gamma, int V, const int32_t* draft_tokens,
                          const float* u_accept, const float* u_sample, const float* temperature,
@@ -235,6 +239,29 @@ const char* spec_verify_status_string(sv_status status);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int spec_verify_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Verification of deterministic proposals ("Speculative Decoding : accélérer
+ * l'inférence des LLM", §N-gram lookup et variantes sans modèle: the draft
+ * tokens come from a lookup, not from a model). Such a proposer puts all its
+ * probability on the token it proposes, so q_i is one-hot at x_i and the rule
+ * of §Pourquoi la qualité est préservée becomes: accept x_i iff
+ * u_accept < min(1, p_i(x_i)); at the first rejection n, draw from p_n
+ * without x_n (max(p_n - q_n, 0) renormalised); after k acceptances draw the
+ * extra token from target row k. T == 0 is the greedy rule. No draft logits
+ * are read (half the bytes of spec_verify at equal gamma).
+ *   num_draft  [B] int32, device: request b proposes num_draft[b] in
+ *              [0, gamma] tokens, draft_tokens[b, :num_draft[b]]; the rest of
+ *              its row is ignored, and so are its target rows past
+ *              num_draft[b] (a NaN there is not an error). A count outside
+ *              [0, gamma] makes the request invalid (-1, SV_STATUS_BAD_REQUEST).
+ * Every other argument, the outputs, the workspace (spec_verify_workspace_size)
+ * and the error behaviour are those of spec_verify. */
+sv_status spec_verify_onehot(const void* target_logits, sv_dtype dtype, int B, int gamma, int V,
+                             const int32_t* draft_tokens, const int32_t* num_draft, const float* u_accept,
+                             const float* u_sample, const float* temperature, int32_t* out_tokens,
+                             int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                             sv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Post-verify bookkeeping ("Accélérer Sonar grâce à la spéculation",

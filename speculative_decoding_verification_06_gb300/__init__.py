@@ -32,7 +32,7 @@ EXPORTED = (
     "spec_verify_workspace_size", "spec_verify", "spec_verify_ex",
     "spec_verify_host_staging_size", "spec_verify_host", "spec_verify_last_launch_count",
     "spec_verify_status_string", "spec_verify_version", "spec_verify_noalloc",
-    "spec_commit", "spec_ngram_propose",
+    "spec_commit", "spec_ngram_propose", "spec_verify_onehot",
 )
 
 
@@ -51,7 +51,7 @@ class _Debug(ctypes.Structure):
 class _Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
                 ("peer_wait_us", ctypes.c_int32), ("reserved0", ctypes.c_int32),
-                ("hold_flag", ctypes.c_void_p), ("reserved", ctypes.c_int32 * 2)]
+                ("hold_flag", ctypes.c_void_p), ("num_draft", ctypes.c_void_p)]
 
 
 _lib = None
@@ -70,9 +70,10 @@ def _declare(lib):
     lib.spec_verify_noalloc.argtypes = common + [vp]
     lib.spec_commit.argtypes = [vp, vp, int_, int_, vp, int_, vp, vp, vp, vp]
     lib.spec_ngram_propose.argtypes = [vp, int_, int_, vp, int_, int_, int_, vp, vp, vp, vp]
+    lib.spec_verify_onehot.argtypes = [vp, i32, int_, int_, int_, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     for name in ("spec_verify_workspace_size", "spec_verify_host_staging_size", "spec_verify",
                  "spec_verify_ex", "spec_verify_host", "spec_verify_noalloc", "spec_commit",
-                 "spec_ngram_propose"):
+                 "spec_ngram_propose", "spec_verify_onehot"):
         getattr(lib, name).restype = i32
     lib.spec_verify_status_string.argtypes = [i32]
     lib.spec_verify_status_string.restype = ctypes.c_char_p
@@ -155,7 +156,7 @@ def _ptr(t) -> int:
 def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature,
                 out_tokens=None, out_num_accepted=None, workspace=None, stream=None,
                 debug: bool = False, path: int = SV_PATH_AUTO, grid_ctas: int = 0,
-                status=None, peer_wait_us: int = 0, hold_flag=None) -> Outputs:
+                status=None, peer_wait_us: int = 0, hold_flag=None, num_draft=None) -> Outputs:
     """Verify one batch of CUDA tensors (see include/specverify.h).
 
     ``target_logits`` [B, gamma+1, V] and ``draft_logits`` [B, gamma, V]
@@ -165,6 +166,8 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
     allocated with torch when not given. With ``debug``, ``path``,
     ``grid_ctas``, ``status``, ``peer_wait_us`` or ``hold_flag`` (a CUDA int32
     tensor, checking only) the call goes through ``spec_verify_ex``.
+    ``draft_logits`` None selects one-hot proposals (``spec_verify_onehot``)
+    with ``num_draft`` [B] int32 proposals per request (None: gamma each).
     """
     import torch
     lib = load()
@@ -172,8 +175,8 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
     G = G1 - 1
     dt = _dtype_code(target_logits)
     dev = target_logits.device
-    for t in (target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature):
-        if not t.is_cuda or not t.is_contiguous():
+    for t in (target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature, num_draft):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("every input must be a contiguous CUDA tensor")
     if out_tokens is None:
         out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
@@ -186,7 +189,8 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
             _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
             _ptr(out_num_accepted), _ptr(workspace), workspace.numel() * workspace.element_size(), s)
     dbg = None
-    if debug or path != SV_PATH_AUTO or grid_ctas or status is not None or peer_wait_us or hold_flag is not None:
+    if (debug or path != SV_PATH_AUTO or grid_ctas or status is not None or peer_wait_us or hold_flag is not None
+            or draft_logits is None):
         d = _Debug()
         if debug:
             f64, f32, i32 = torch.float64, torch.float32, torch.int32
@@ -205,7 +209,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
             dbg["phase_ns"][0] = -1  # UINT64_MAX
             for k, v in dbg.items():
                 setattr(d, k, v.data_ptr())
-        o = _Options(path, grid_ctas, peer_wait_us, 0, _ptr(hold_flag) or None)
+        o = _Options(path, grid_ctas, peer_wait_us, 0, _ptr(hold_flag) or None, _ptr(num_draft) or None)
         rc = lib.spec_verify_ex(*args, ctypes.byref(d), _ptr(status), ctypes.byref(o))
         _check(rc, "spec_verify_ex")
     else:
@@ -291,3 +295,31 @@ def spec_ngram_propose(token_buf, seq_lens, gamma, n_min=2, n_max=5, draft_token
                                 _ptr(draft_tokens), _ptr(num_draft), _ptr(status), _stream_handle(stream))
     _check(rc, "spec_ngram_propose")
     return draft_tokens, num_draft
+
+
+def spec_verify_onehot(target_logits, draft_tokens, num_draft, u_accept, u_sample, temperature,
+                       out_tokens=None, out_num_accepted=None, workspace=None, stream=None) -> Outputs:
+    """``spec_verify_onehot``: verification of deterministic proposals (q one-hot
+    at each proposed token, no draft logits); ``num_draft`` [B] int32 CUDA
+    tensor. Other arguments as ``spec_verify``."""
+    import torch
+    lib = load()
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dt = _dtype_code(target_logits)
+    dev = target_logits.device
+    for t in (target_logits, draft_tokens, num_draft, u_accept, u_sample, temperature):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("every input must be a contiguous CUDA tensor")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(16, workspace_size(B, G, V, dt)), dtype=torch.uint8, device=dev)
+    rc = lib.spec_verify_onehot(_ptr(target_logits), dt, B, G, V, _ptr(draft_tokens), _ptr(num_draft),
+                                _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
+                                _ptr(out_num_accepted), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(rc, "spec_verify_onehot")
+    return Outputs(out_tokens, out_num_accepted, None, None)

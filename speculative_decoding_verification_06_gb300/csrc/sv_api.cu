@@ -102,8 +102,9 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     g_last_launches = 0;
     if (!shape_ok(B, gamma, V, dtype)) return SV_ERR_INVALID_ARG;
     if (B == 0) return SV_OK;
-    if (!target_logits || !draft_logits || !draft_tokens || !u_accept || !u_sample || !temperature ||
-        !out_tokens || !out_num_accepted)
+    // draft_logits == NULL: deterministic (one-hot) proposals, see spec_verify_onehot
+    if (!target_logits || !draft_tokens || !u_accept || !u_sample || !temperature || !out_tokens ||
+        !out_num_accepted)
         return SV_ERR_INVALID_ARG;
     const int path = opts ? opts->path : SV_PATH_AUTO;
     if (path != SV_PATH_AUTO && path != SV_PATH_ROWWISE && path != SV_PATH_STREAMING)
@@ -116,6 +117,8 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     Args a;
     a.target = target_logits;
     a.draft = draft_logits;
+    a.onehot = draft_logits == nullptr;
+    a.num_draft = (a.onehot && opts) ? opts->num_draft : nullptr;
     a.dtype = dtype;
     a.B = B;
     a.gamma = gamma;
@@ -164,11 +167,26 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     return SV_OK;
 }
 
+sv_status spec_verify_onehot(const void* target_logits, sv_dtype dtype, int B, int gamma, int V,
+                             const int32_t* draft_tokens, const int32_t* num_draft, const float* u_accept,
+                             const float* u_sample, const float* temperature, int32_t* out_tokens,
+                             int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                             sv_stream_t stream) {
+    sv_options o;
+    std::memset(&o, 0, sizeof o);
+    o.num_draft = num_draft;
+    return spec_verify_ex(target_logits, nullptr, dtype, B, gamma, V, draft_tokens, u_accept, u_sample,
+                          temperature, out_tokens, out_num_accepted, workspace, workspace_bytes, stream,
+                          nullptr, nullptr, &o);
+}
+
 sv_status spec_verify(const void* target_logits, const void* draft_logits, sv_dtype dtype, int B,
                       int gamma, int V, const int32_t* draft_tokens, const float* u_accept,
                       const float* u_sample, const float* temperature, int32_t* out_tokens,
                       int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
                       sv_stream_t stream) {
+    g_last_launches = 0;
+    if (!draft_logits && B > 0) return SV_ERR_INVALID_ARG;  // one-hot proposals: spec_verify_onehot
     return spec_verify_ex(target_logits, draft_logits, dtype, B, gamma, V, draft_tokens, u_accept,
                           u_sample, temperature, out_tokens, out_num_accepted, workspace,
                           workspace_bytes, stream, nullptr, nullptr, nullptr);

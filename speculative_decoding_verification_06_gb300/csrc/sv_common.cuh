@@ -168,6 +168,9 @@ constexpr int kKindInvalid = -1;
 constexpr int kKindGreedy = 0;
 constexpr int kKindResidual = 1;
 constexpr int kKindBonus = 2;
+// Internal draw kind, reported as kKindResidual: the residual of a one-hot
+// (deterministic) proposal, p_n without the proposed token x_n.
+constexpr int kKindResidualOnehot = 3;
 
 constexpr float kFixResidual = 1152921504606846976.0f;  // 2^60
 constexpr float kFixTarget = 549755813888.0f;           // 2^39
@@ -179,11 +182,12 @@ constexpr double kFixTargetInv = 1.0 / 549755813888.0;
 // proportional to p at the target row (the extra token, or the fallback when
 // residual weights sum to zero).
 struct DrawParams {
-    int kind;       // kKindResidual or kKindBonus
+    int kind;       // kKindResidual, kKindBonus or kKindResidualOnehot
     float c;
     float mcp, isp; // target row: fl(max * c) and 1/s
     float mcq, isq; // draft row (residual only)
     float fix;      // fixed-point scale
+    int excl;       // kKindResidualOnehot: the token whose weight is zero
 };
 
 __device__ __forceinline__ float weight_target(float lt, const DrawParams& d) {
@@ -194,6 +198,13 @@ __device__ __forceinline__ float weight_residual(float lt, float ld, const DrawP
     const float p = __fmul_rn(row_term(lt, d.c, d.mcp), d.isp);
     const float q = __fmul_rn(row_term(ld, d.c, d.mcq), d.isq);
     return fmaxf(__fsub_rn(p, q), 0.0f);
+}
+
+// Weight of token `e` of the target row for a draw of kind kBonus or
+// kResidualOnehot: 2^((l - m) c), zero for the excluded token of a one-hot
+// residual (max(p - q, 0) with q one-hot at x_n is p without x_n).
+__device__ __forceinline__ float weight_target_excl(float lt, int e, const DrawParams& d, int kind) {
+    return (kind == kKindResidualOnehot && e == d.excl) ? 0.0f : weight_target(lt, d);
 }
 
 // floor(u * total) exactly, for u in [0, 1): u = M 2^e with an integer M < 2^24,

@@ -124,7 +124,7 @@ __device__ __forceinline__ float run_weights(const void* tgt, const void* dft, s
     for (int e = lo; e < hi; ++e) {
         float lt = load_logit<DT>(tgt, trow + e);
         float w = kind == kKindResidual ? weight_residual(lt, load_logit<DT>(dft, drow + e), d)
-                                        : weight_target(lt, d);
+                                        : weight_target_excl(lt, e, d, kind);
         run = __fadd_rn(run, w);
     }
     return run;
@@ -139,14 +139,19 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
         const bool t_ok = (T >= 0.0f) && (T < pos_inf());
         const bool greedy = t_ok && T == 0.0f;
         const float c = (t_ok && !greedy) ? temp_scale(T) : 0.0f;
-        int bad = t_ok ? 0 : 1;
-        for (int i = threadIdx.x; i < G; i += kThreads) {
+        // proposals: gamma, or num_draft[b] for one-hot proposals (no draft
+        // rows; target rows past num_draft[b] take no part)
+        const int kb = a.onehot && a.num_draft ? a.num_draft[b] : G;
+        const bool range_ok = t_ok && kb >= 0 && kb <= G;
+        const int np = range_ok ? kb : 0;
+        int bad = range_ok ? 0 : 1;
+        for (int i = threadIdx.x; i < np; i += kThreads) {
             int x = a.tokens[static_cast<size_t>(b) * G + i];
             if (x < 0 || x >= V) bad = 1;
         }
         bad = __syncthreads_or(bad);
         if (!bad) {
-            const int nrows = greedy ? G + 1 : 2 * G + 1;
+            const int nrows = (greedy || a.onehot) ? np + 1 : 2 * G + 1;
             for (int r = 0; r < nrows; ++r) {
                 RowStat st;
                 if (r <= G) {
@@ -197,16 +202,19 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
         // Per-row checking outputs.
         for (int j = threadIdx.x; j <= G; j += kThreads) {
             size_t r = static_cast<size_t>(b) * (G + 1) + j;
+            const bool read = j <= np || !a.onehot;
             const RowStat& st = sh.st[j];
-            if (a.dbg.max_target) a.dbg.max_target[r] = st.m;
-            if (a.dbg.lse_target) a.dbg.lse_target[r] = greedy ? nan("") : lse_from_stats(st.m, st.s, c, T);
-            if (a.dbg.argmax_target) a.dbg.argmax_target[r] = greedy ? st.idx : -1;
+            if (a.dbg.max_target) a.dbg.max_target[r] = read ? st.m : nanf("");
+            if (a.dbg.lse_target)
+                a.dbg.lse_target[r] = (greedy || !read) ? nan("") : lse_from_stats(st.m, st.s, c, T);
+            if (a.dbg.argmax_target) a.dbg.argmax_target[r] = (greedy && read) ? st.idx : -1;
         }
         for (int j = threadIdx.x; j < G; j += kThreads) {
             size_t r = static_cast<size_t>(b) * G + j;
+            const bool draft = !greedy && !a.onehot;
             const RowStat& st = sh.st[G + 1 + j];
-            if (a.dbg.max_draft) a.dbg.max_draft[r] = greedy ? nanf("") : st.m;
-            if (a.dbg.lse_draft) a.dbg.lse_draft[r] = greedy ? nan("") : lse_from_stats(st.m, st.s, c, T);
+            if (a.dbg.max_draft) a.dbg.max_draft[r] = draft ? st.m : nanf("");
+            if (a.dbg.lse_draft) a.dbg.lse_draft[r] = draft ? lse_from_stats(st.m, st.s, c, T) : nan("");
             if (a.dbg.p_x) a.dbg.p_x[r] = nan("");
             if (a.dbg.q_x) a.dbg.q_x[r] = nan("");
         }
@@ -215,9 +223,9 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
         // Left-to-right acceptance scan on one thread.
         if (threadIdx.x == 0) {
             const int32_t* tok = a.tokens + static_cast<size_t>(b) * G;
-            int n = G;
+            int n = np;
             if (greedy) {
-                for (int i = 0; i < G; ++i) {
+                for (int i = 0; i < np; ++i) {
                     if (tok[i] != sh.st[i].idx) {
                         n = i;
                         break;
@@ -229,14 +237,15 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                 if (a.dbg.w_total) a.dbg.w_total[b] = nan("");
             } else {
                 const float* ua = a.u_accept + static_cast<size_t>(b) * G;
-                for (int i = 0; i < G; ++i) {
+                for (int i = 0; i < np; ++i) {
                     const int x = tok[i];
                     const size_t tr = static_cast<size_t>(b) * (G + 1) + i;
                     const size_t dr = static_cast<size_t>(b) * G + i;
                     const RowStat& sp = sh.st[i];
                     const RowStat& sq = sh.st[G + 1 + i];
                     double p = prob_from_stats(load_logit<DT>(a.target, tr * V + x), sp.m, sp.s, c);
-                    double q = prob_from_stats(load_logit<DT>(a.draft, dr * V + x), sq.m, sq.s, c);
+                    // a one-hot proposal has q(x) = 1
+                    double q = a.onehot ? 1.0 : prob_from_stats(load_logit<DT>(a.draft, dr * V + x), sq.m, sq.s, c);
                     if (a.dbg.p_x) a.dbg.p_x[dr] = p;
                     if (a.dbg.q_x) a.dbg.q_x[dr] = q;
                     if (!accept_draft(p, q, ua[i])) {
@@ -249,19 +258,23 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                 d.c = c;
                 d.mcp = scaled_max(sh.st[n].m, c);
                 d.isp = __frcp_rn(sh.st[n].s);
-                if (n < G) {
+                d.excl = -1;
+                if (n < np && !a.onehot) {
                     d.kind = kKindResidual;
                     d.mcq = scaled_max(sh.st[G + 1 + n].m, c);
                     d.isq = __frcp_rn(sh.st[G + 1 + n].s);
                     d.fix = kFixResidual;
                 } else {
-                    d.kind = kKindBonus;
+                    // the extra token, or the residual of a one-hot proposal
+                    // (p_n without x_n, unnormalised weights)
+                    d.kind = n < np ? kKindResidualOnehot : kKindBonus;
+                    d.excl = n < np ? tok[n] : -1;
                     d.mcq = 0.0f;
                     d.isq = 0.0f;
                     d.fix = kFixTarget;
                 }
                 sh.draw = d;
-                if (a.dbg.kind) a.dbg.kind[b] = d.kind;
+                if (a.dbg.kind) a.dbg.kind[b] = d.kind == kKindResidualOnehot ? kKindResidual : d.kind;
             }
             for (int j = n + 1; j <= G; ++j) out[j] = -1;
             a.out_num_accepted[b] = n;
@@ -297,7 +310,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                     float lt = load_logit<DT>(a.target, trow + e);
                     float w = kind == kKindResidual
                                   ? weight_residual(lt, load_logit<DT>(a.draft, drow + e), d)
-                                  : weight_target(lt, d);
+                                  : weight_target_excl(lt, e, d, kind);
                     run2 = __fadd_rn(run2, w);
                     if (excl + to_fixed(run2, d.fix) > t) {
                         token = e;

@@ -475,7 +475,7 @@ struct Kern {
                         __threadfence();
                         own_k = v - 1;
                         const int kind = __ldcg(&jobs()[own_k].kind);
-                        if (kind != kKindResidual && kind != kKindBonus) {  // no items, no search
+                        if (kind != kKindResidual && kind != kKindBonus && kind != kKindResidualOnehot) {  // no items, no search
                             own_p += G;
                             own_k = -1;
                             moved = 1;
@@ -617,7 +617,8 @@ struct Kern {
         bar_sync(kBarConsumers, kConsumers);
         int n = 0;
         for (int w = 0; w < kConsumerWarps; ++w) n += ctl.wtmp[w];
-        const long long E2 = static_cast<long long>(n) * a.gamma * a.V;
+        // draft rows of the T > 0 requests (none for one-hot proposals)
+        const long long E2 = a.onehot ? 0ll : static_cast<long long>(n) * a.gamma * a.V;
         for (int gg = t; gg <= G; gg += kConsumers) ctl.dbeg[gg] = part_begin(E2, G, gg, L.vec);
         const int k_lo = n > 0 ? static_cast<int>(part_begin(E2, G, g, L.vec) /
                                                   (static_cast<long long>(a.gamma) * a.V))
@@ -885,26 +886,32 @@ struct Kern {
         const float c = samp ? temp_scale(T) : 0.0f;
         const int k = ctl.kmap[b];
         const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
-        int bad = t_ok ? 0 : 1;
-        // this lane's first position (gamma <= 32 in one pass): its token, the two
+        // proposals of this request: gamma, or num_draft[b] for one-hot proposals
+        // (whose rows past it take no part)
+        const int kb = a.onehot && a.num_draft ? a.num_draft[b] : GM;
+        const bool onehot = a.onehot;
+        const bool range_ok = t_ok && kb >= 0 && kb <= GM;
+        int bad = range_ok ? 0 : 1;
+        const int np = range_ok ? kb : 0;
+        // this lane's first position (gamma <= 32 in one pass): its token, the
         // gathered logits and the uniform are loaded before the row merges
         int x0 = 0;
         float lt0 = 0.0f, ld0 = 0.0f, u0 = 0.0f;
-        if (lane < GM) {
+        if (lane < np) {
             x0 = tok[lane];
             if (!greedy && x0 >= 0 && x0 < V) {
                 const size_t tr = static_cast<size_t>(b) * (GM + 1) + lane;
                 const size_t dr = static_cast<size_t>(b) * GM + lane;
                 lt0 = load_logit<DT>(a.target, tr * V + x0);
-                ld0 = load_logit<DT>(a.draft, dr * V + x0);
+                if (!onehot) ld0 = load_logit<DT>(a.draft, dr * V + x0);
                 u0 = a.u_accept[dr];
             }
         }
-        for (int i = lane; i < GM; i += 32) {
+        for (int i = lane; i < np; i += 32) {
             const int x = tok[i];
             if (x < 0 || x >= V) bad = 1;
         }
-        const int nrows = samp ? 2 * GM + 1 : GM + 1;
+        const int nrows = !range_ok ? 0 : (samp && !onehot ? 2 * GM + 1 : np + 1);
         for (int r = lane; r < nrows; r += 32) {
             Rec x;
             if (r <= GM)
@@ -947,22 +954,25 @@ struct Kern {
         }
         for (int j = lane; j <= GM; j += 32) {
             const size_t r = static_cast<size_t>(b) * (GM + 1) + j;
-            if (dbg.max_target) dbg.max_target[r] = st[j].m;
-            if (dbg.lse_target) dbg.lse_target[r] = greedy ? nan("") : lse_from_stats(st[j].m, st[j].s, c, T);
-            if (dbg.argmax_target) dbg.argmax_target[r] = greedy ? st[j].idx : -1;
+            const bool read = j <= np;  // one-hot: rows past the proposals are not part of the request
+            if (dbg.max_target) dbg.max_target[r] = read ? st[j].m : nanf("");
+            if (dbg.lse_target)
+                dbg.lse_target[r] = (greedy || !read) ? nan("") : lse_from_stats(st[j].m, st[j].s, c, T);
+            if (dbg.argmax_target) dbg.argmax_target[r] = (greedy && read) ? st[j].idx : -1;
         }
         for (int j = lane; j < GM; j += 32) {
             const size_t r = static_cast<size_t>(b) * GM + j;
-            if (dbg.max_draft) dbg.max_draft[r] = greedy ? nanf("") : st[GM + 1 + j].m;
+            const bool draft = !greedy && !onehot;
+            if (dbg.max_draft) dbg.max_draft[r] = draft ? st[GM + 1 + j].m : nanf("");
             if (dbg.lse_draft)
-                dbg.lse_draft[r] = greedy ? nan("") : lse_from_stats(st[GM + 1 + j].m, st[GM + 1 + j].s, c, T);
+                dbg.lse_draft[r] = draft ? lse_from_stats(st[GM + 1 + j].m, st[GM + 1 + j].s, c, T) : nan("");
         }
         // first failing position over all lanes (gamma may exceed 32)
-        int n = GM;
-        for (int base = 0; base < GM; base += 32) {
+        int n = np;
+        for (int base = 0; base < np; base += 32) {
             const int i = base + lane;
             bool fail = false;
-            if (i < GM) {
+            if (i < np) {
                 const int x = tok[i];
                 if (greedy) {
                     fail = x != st[i].idx;
@@ -971,19 +981,28 @@ struct Kern {
                     const size_t dr = static_cast<size_t>(b) * GM + i;
                     const bool pre_loaded = base == 0;
                     const float lt = pre_loaded ? lt0 : load_logit<DT>(a.target, tr * V + x);
-                    const float ld = pre_loaded ? ld0 : load_logit<DT>(a.draft, dr * V + x);
                     const float u = pre_loaded ? u0 : a.u_accept[dr];
                     if (dbg.p_x) dbg.p_x[dr] = prob_from_stats(lt, st[i].m, st[i].s, c);
-                    if (dbg.q_x) dbg.q_x[dr] = prob_from_stats(ld, st[GM + 1 + i].m, st[GM + 1 + i].s, c);
-                    fail = !accept_from_logits(lt, ld, st[i].m, st[i].s, st[GM + 1 + i].m, st[GM + 1 + i].s, c, u);
+                    if (onehot) {
+                        // q(x) = 1: the draft side of the test is a row whose only
+                        // logit is 0 (max 0, sum 1)
+                        if (dbg.q_x) dbg.q_x[dr] = 1.0;
+                        fail = !accept_from_logits(lt, 0.0f, st[i].m, st[i].s, 0.0f, 1.0f, c, u);
+                    } else {
+                        const float ld = pre_loaded ? ld0 : load_logit<DT>(a.draft, dr * V + x);
+                        if (dbg.q_x) dbg.q_x[dr] = prob_from_stats(ld, st[GM + 1 + i].m, st[GM + 1 + i].s, c);
+                        fail = !accept_from_logits(lt, ld, st[i].m, st[i].s, st[GM + 1 + i].m, st[GM + 1 + i].s,
+                                                   c, u);
+                    }
                 }
             }
             const unsigned ball = __ballot_sync(0xffffffffu, fail);
-            if (n == GM && ball) n = base + __ffs(ball) - 1;
+            if (n == np && ball) n = base + __ffs(ball) - 1;
         }
-        // positions after the first rejection (all of them at T = 0) are not evaluated
+        // positions after the first rejection, or not proposed (all of them at
+        // T = 0), are not evaluated
         for (int i = lane; i < GM; i += 32)
-            if (greedy || i > n) {
+            if (greedy || i > n || i >= np) {
                 const size_t dr = static_cast<size_t>(b) * GM + i;
                 if (dbg.p_x) dbg.p_x[dr] = nan("");
                 if (dbg.q_x) dbg.q_x[dr] = nan("");
@@ -1010,13 +1029,17 @@ struct Kern {
                 d.c = c;
                 d.mcp = scaled_max(st[n].m, c);
                 d.isp = __frcp_rn(st[n].s);
-                if (n < GM) {
+                d.excl = -1;
+                if (n < np && !onehot) {
                     d.kind = kKindResidual;
                     d.mcq = scaled_max(st[GM + 1 + n].m, c);
                     d.isq = __frcp_rn(st[GM + 1 + n].s);
                     d.fix = kFixResidual;
                 } else {
-                    d.kind = kKindBonus;
+                    // the extra token (n = np), or the residual of a one-hot
+                    // proposal: p_n without x_n, unnormalised weights
+                    d.kind = n < np ? kKindResidualOnehot : kKindBonus;
+                    d.excl = n < np ? tok[n] : -1;
                     d.mcq = 0.0f;
                     d.isq = 0.0f;
                     d.fix = kFixTarget;
@@ -1024,7 +1047,7 @@ struct Kern {
                 j.kind = d.kind;
                 jobs()[k] = j;
                 publish(k);
-                if (dbg.kind) dbg.kind[b] = d.kind;
+                if (dbg.kind) dbg.kind[b] = d.kind == kKindResidualOnehot ? kKindResidual : d.kind;
             }
         }
     }
@@ -1042,7 +1065,7 @@ struct Kern {
     // rounded as a scalar fma), so every weight equals weight_residual or
     // weight_target of that token.
     __device__ static __forceinline__ void vec_weights(const uint4& vt, const uint4& vd, const DrawParams& d,
-                                                       int kind, float (&w)[kTPV]) {
+                                                       int kind, int first, float (&w)[kTPV]) {
         const uint32_t t4[4] = {vt.x, vt.y, vt.z, vt.w};
         const uint32_t d4[4] = {vd.x, vd.y, vd.z, vd.w};
         const unsigned long long cc = f2_pack(d.c, d.c), nmp = f2_pack(-d.mcp, -d.mcp);
@@ -1068,12 +1091,18 @@ struct Kern {
                 w[2 * i + 1] = ex2(e1);
             }
         }
+        if (kind == kKindResidualOnehot) {  // p without the proposed token (first = this vector's first token)
+            const int rel = d.excl - first;
+#pragma unroll
+            for (int e = 0; e < kTPV; ++e) w[e] = e == rel ? 0.0f : w[e];
+        }
     }
 
     // S_q of one vector: its weights added in index order.
-    __device__ static __forceinline__ float vec_sum(const uint4& vt, const uint4& vd, const DrawParams& d, int kind) {
+    __device__ static __forceinline__ float vec_sum(const uint4& vt, const uint4& vd, const DrawParams& d, int kind,
+                                                    int first) {
         float w[kTPV];
-        vec_weights(vt, vd, d, kind, w);
+        vec_weights(vt, vd, d, kind, first, w);
         float s = w[0];
 #pragma unroll
         for (int e = 1; e < kTPV; ++e) s = __fadd_rn(s, w[e]);
@@ -1088,12 +1117,12 @@ struct Kern {
     // tokens weigh 0 (rows end on 16-byte boundaries, so a vector is either
     // wholly in the row or wholly past it).
     __device__ static __forceinline__ void run_vec_sums(const Run& vt, const Run& vd, int valid, const DrawParams& d,
-                                                        int kind, float (&S)[4]) {
+                                                        int kind, int first, float (&S)[4]) {
         // all four are computed (straight-line code), then the ones past the
-        // row are dropped
+        // row are dropped; `first` is the run's first token
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float x = vec_sum(vt[q], vd[q], d, kind);
+            const float x = vec_sum(vt[q], vd[q], d, kind, first + q * kTPV);
             S[q] = q * kTPV < valid ? x : 0.0f;
         }
     }
@@ -1112,12 +1141,13 @@ struct Kern {
     // in the rotated order and put back in index order (rotate by 2 if r & 2,
     // then by 1 if r & 1; selects on constant indices) before they are added.
     __device__ static __forceinline__ float run_total_rotated(const Run& rt, const Run& rd, int t, int valid,
-                                                              const DrawParams& d, int kind) {
+                                                              const DrawParams& d, int kind, int first) {
         const int r = (t >> 1) & 3;
         float Sr[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float x = vec_sum(rt[k], rd[k], d, kind);  // stale shared memory past the row is dropped
+            // stale shared memory past the row is dropped
+            const float x = vec_sum(rt[k], rd[k], d, kind, first + ((k + r) & 3) * kTPV);
             Sr[k] = ((k + r) & 3) * kTPV < valid ? x : 0.0f;
         }
         const bool r2 = (r & 2) != 0, r1 = (r & 1) != 0;
@@ -1150,7 +1180,7 @@ struct Kern {
         load_run_global(a.target, trow + e0 + r * kTPT, valid, vt);
         if (kind == kKindResidual) load_run_global(a.draft, drow + e0 + r * kTPT, valid, vd);
         float S[4];
-        run_vec_sums(vt, vd, valid, d, kind, S);
+        run_vec_sums(vt, vd, valid, d, kind, static_cast<int>(e0) + r * kTPT, S);
         return to_fixed(run_total(S), d.fix);
     }
 
@@ -1183,7 +1213,7 @@ struct Kern {
             ctot[h] = sum;
         }
         const Job jb = gjobs[k];
-        if (jb.kind != kKindResidual && jb.kind != kKindBonus) return;
+        if (jb.kind != kKindResidual && jb.kind != kKindBonus && jb.kind != kKindResidualOnehot) return;
         DrawParams d = jb.d;
         int kind = jb.kind;
         const long long trow = (static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n) * a.V;
@@ -1282,7 +1312,7 @@ struct Kern {
             if (kind == kKindResidual) load_run_global(a.draft, drow + e0 + vt * TPT, valid, ld);
         }
         float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (valid > 0) run_vec_sums(lt, ld, valid, d, kind, S);
+        if (valid > 0) run_vec_sums(lt, ld, valid, d, kind, static_cast<int>(e0) + vt * TPT, S);
         const unsigned long long q = to_fixed(run_total(S), d.fix);
         unsigned long long x = q;
 #pragma unroll
@@ -1313,7 +1343,7 @@ struct Kern {
                 const uint4 wt = vsel == 0 ? lt[0] : vsel == 1 ? lt[1] : vsel == 2 ? lt[2] : lt[3];
                 const uint4 wd = vsel == 0 ? ld[0] : vsel == 1 ? ld[1] : vsel == 2 ? ld[2] : ld[3];
                 float w[kTPV];
-                vec_weights(wt, wd, d, kind, w);
+                vec_weights(wt, wd, d, kind, static_cast<int>(e0) + vt * TPT + vsel * kTPV, w);
                 float part = w[0];
                 int last_pos = w[0] > 0.0f ? 0 : -1;
                 if (start + to_fixed(__fadd_rn(Pv, part), d.fix) > tt) token = 0;
@@ -1389,7 +1419,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                     red_release_add(job_done + (item & ~kJobMsg), share);
                     return false;
                 }
-                const unsigned need = (KT::sampled(a.temperature[item]) ? 2 * GM + 1 : GM + 1) * V;
+                const unsigned need = (!a.onehot && KT::sampled(a.temperature[item]) ? 2 * GM + 1 : GM + 1) * V;
                 __threadfence();  // this block's row records are visible before they are counted
                 const bool done = atomicAdd(req_done + item, share) + share == need;
                 __threadfence();  // and the other blocks' records before they are read
@@ -1491,7 +1521,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                     cur_p = p;
                 }
                 const int kind = __shfl_sync(0xffffffffu, desc.job.kind, 0);
-                if (kind == kKindResidual || kind == kKindBonus) {
+                if (kind == kKindResidual || kind == kKindBonus || kind == kKindResidualOnehot) {
                     const int b = __shfl_sync(0xffffffffu, desc.job.b, 0), n = __shfl_sync(0xffffffffu, desc.job.n, 0);
                     desc.j = j;
                     const long long e0 = static_cast<long long>(j) * CH;
@@ -1580,7 +1610,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                 if (ds.job.kind == kKindResidual) KT::load_run_smem(smt + kChunkBytes, t, ld);
             }
             K.consume_end(cons);
-            const float run = valid > 0 ? KT::run_total_rotated(lt, ld, t, valid, ds.job.d, ds.job.kind) : 0.0f;
+            const float run = valid > 0 ? KT::run_total_rotated(lt, ld, t, valid, ds.job.d, ds.job.kind,
+                                                                static_cast<int>(e0) + t * TPT)
+                                        : 0.0f;
             const unsigned long long wsum = warp_sum_u64(to_fixed(run, ds.job.d.fix));
             if (lane == 0) {
                 wsums[(static_cast<size_t>(ds.k) * L.NCH + ds.j) * kConsumerWarps + warp] = wsum;

@@ -52,25 +52,31 @@ def _row_values(arr, dtype):
     return (bf16_bits_to_f32(a) if a.dtype == np.uint16 else a).astype(np.float64)
 
 
-def _draw_weights(batch, b, n, kind):
+def _draw_weights(batch, b, n, kind, onehot=False):
     """fp64 weights of the oracle's draw (used only to judge near-tie draws)."""
     from scipy import special
     T = float(batch.temperature[b])
     lt = _row_values(batch.target[b, n], None)
     p = special.softmax(lt / T)
     if kind == 1:
-        ld = _row_values(batch.draft[b, n], None)
-        w = np.maximum(p - special.softmax(ld / T), 0.0)
+        if onehot:  # q one-hot at the proposed token
+            q = np.zeros_like(p)
+            q[int(batch.tokens[b, n])] = 1.0
+        else:
+            q = special.softmax(_row_values(batch.draft[b, n], None) / T)
+        w = np.maximum(p - q, 0.0)
         if w.sum() == 0.0:
             w = p
         return w
     return p
 
 
-def compare(batch, gpu, ora, det, margin=MARGIN, rel_tol=REL_TOL) -> Report:
+def compare(batch, gpu, ora, det, margin=MARGIN, rel_tol=REL_TOL, onehot=False) -> Report:
     """``gpu``: dict of numpy arrays out_tokens, out_num_accepted and the
     debug arrays; ``ora`` = (out_tokens, num_accepted), ``det`` the oracle's
-    detail dict. Raises AssertionError on the first mismatch."""
+    detail dict. ``onehot``: the batch holds deterministic proposals (no draft
+    rows; rows a request does not read are NaN on both sides). Raises
+    AssertionError on the first mismatch."""
     go, gn = gpu["out_tokens"], gpu["out_num_accepted"]
     oo, on = ora
     B, G1 = oo.shape
@@ -108,7 +114,7 @@ def compare(batch, gpu, ora, det, margin=MARGIN, rel_tol=REL_TOL) -> Report:
             rep.exact_rows += 1
         else:
             rep.sample_near_ties += 1
-            w = _draw_weights(batch, b, n_o, int(det["kind"][b]))
+            w = _draw_weights(batch, b, n_o, int(det["kind"][b]), onehot)
             C = np.cumsum(w)
             W = C[-1]
             t = float(batch.u_sample[b]) * W
@@ -122,14 +128,21 @@ def compare(batch, gpu, ora, det, margin=MARGIN, rel_tol=REL_TOL) -> Report:
         valid = on >= 0
         rows = samp & valid
         if rows.any():
-            d = np.abs(gpu["lse_target"][rows] - det["lse_target"][rows])
-            rep.max_lse_err = max(rep.max_lse_err, float(d.max()))
-            dd = np.abs(gpu["lse_draft"][rows] - det["lse_draft"][rows])
-            rep.max_lse_err = max(rep.max_lse_err, float(dd.max()))
+            lt_g, lt_o = gpu["lse_target"][rows], det["lse_target"][rows]
+            assert np.array_equal(np.isnan(lt_g), np.isnan(lt_o)), "rows read differ"
+            fin = ~np.isnan(lt_o)
+            if fin.any():
+                rep.max_lse_err = max(rep.max_lse_err, float(np.abs(lt_g[fin] - lt_o[fin]).max()))
+            if not onehot:
+                dd = np.abs(gpu["lse_draft"][rows] - det["lse_draft"][rows])
+                rep.max_lse_err = max(rep.max_lse_err, float(dd.max()))
+                assert np.array_equal(gpu["max_draft"][rows].astype(np.float64), det["max_draft"][rows])
+            else:
+                assert np.all(np.isnan(gpu["lse_draft"][rows])) and np.all(np.isnan(gpu["max_draft"][rows]))
             assert rep.max_lse_err <= 1e-5, f"log-normaliser error {rep.max_lse_err}"
-            assert np.array_equal(gpu["max_draft"][rows].astype(np.float64), det["max_draft"][rows])
         if valid.any():
-            assert np.array_equal(gpu["max_target"][valid].astype(np.float64), det["max_target"][valid])
+            assert np.array_equal(gpu["max_target"][valid].astype(np.float64), det["max_target"][valid],
+                                  equal_nan=True)
         g = (T == 0) & valid
         if g.any():
             assert np.array_equal(gpu["argmax_target"][g], det["argmax_target"][g])
