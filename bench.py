@@ -54,6 +54,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["verify", "onehot", "ngram", "commit", "loop"], default="verify",
+                    help="verify (default, the headline); onehot: spec_verify_onehot on the workload's "
+                         "target rows; ngram: spec_ngram_propose; commit: spec_commit; loop: ngram -> "
+                         "onehot verify -> commit, the model-free decoding step with no host sync")
     return ap.parse_args()
 
 
@@ -222,6 +226,125 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def time_calls(call, K, W, stream):
+    """W warm-up calls, then K calls each bracketed by CUDA events on `stream`.
+    Returns (total ms, per-call ms array)."""
+    import torch
+    for _ in range(max(3, W)):
+        call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), np.array([a.elapsed_time(b) for a, b in zip(starts, ends)])
+
+
+def run_aux(args, w, local):
+    """--op onehot | ngram | commit | loop on one GPU: one JSON line each, with
+    the same timing rules as the headline (warm-up, CUDA events on the
+    launching stream, per-call roofline)."""
+    import torch
+    import speculative_decoding_verification_06_gb300 as sv
+    from workloads import synthetic
+    torch.cuda.set_device(local)
+    sv.build.build()
+    sv.load()
+    stream = torch.cuda.current_stream()
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    batch = synthetic.generate(w, k=0)
+    B, G, V, es = batch.B, w.gamma, w.V, w.elem_bytes
+    dt = sv.SV_F32 if w.dtype == "f32" else sv.SV_BF16
+    peak, peak_src = peak_hbm()
+    M = 4096
+    hist = synthetic.histories(B, M, (256, M), vocab=V, copy_prob=0.5, seed=1)
+    out_t = torch.empty((B, G + 1), dtype=torch.int32, device="cuda")
+    out_n = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(16, sv.workspace_size(B, G, V, dt)), dtype=torch.uint8, device="cuda")
+    tgt, ua, us, T = d(batch.target), d(batch.u_accept), d(batch.u_sample), d(batch.temperature)
+    tok = d(batch.tokens)
+    full = torch.full((B,), G, dtype=torch.int32, device="cuda")
+    buf0, lens0 = d(hist.token_buf), d(hist.seq_lens)
+    buf, lens = buf0.clone(), lens0.clone()
+    props = torch.empty((B, G), dtype=torch.int32, device="cuda")
+    nprop = torch.empty((B,), dtype=torch.int32, device="cuda")
+    extra = {}
+    if args.op == "onehot":
+        def call():
+            sv.spec_verify_onehot(tgt, tok, full, ua, us, T, out_t, out_n, ws, stream)
+        unit, per_step = "rows/s", B * (G + 1)
+        metric = "spec-verify-onehot rows/s (deterministic proposals, target rows only), B×(γ+1)×V"
+    elif args.op == "ngram":
+        def call():
+            sv.spec_ngram_propose(buf0, lens0, G, 2, 5, props, nprop, stream=stream)
+        unit, per_step = "requests/s", B
+        metric = "n-gram proposals requests/s (prompt_lookup_min 2, max 5)"
+    elif args.op == "commit":
+        def call():
+            sv.spec_commit(out_t, out_n, buf, lens, stream=stream)
+        unit, per_step = "requests/s", B
+        metric = "post-verify commit requests/s"
+    else:
+        def call():
+            sv.spec_ngram_propose(buf, lens, G, 2, 5, props, nprop, stream=stream)
+            sv.spec_verify_onehot(tgt, props, nprop, ua, us, T, out_t, out_n, ws, stream)
+            sv.spec_commit(out_t, out_n, buf, lens, stream=stream)
+        unit, per_step = "rows/s", B * (G + 1)
+        metric = "model-free decoding step (ngram -> onehot verify -> commit) rows/s, B×(γ+1)×V"
+    if args.op == "commit":  # a verification result to commit, and room for every step
+        sv.spec_verify_onehot(tgt, tok, full, ua, us, T, out_t, out_n, ws, stream)
+        buf = torch.zeros((B, M + 70 * (args.steps + args.warmup + 8)), dtype=torch.int32, device="cuda")
+        lens = torch.zeros((B,), dtype=torch.int32, device="cuda")
+    if args.op == "loop":  # histories with room for every step
+        buf = torch.zeros((B, M + (G + 1) * (args.steps + args.warmup + 8)), dtype=torch.int32, device="cuda")
+        buf[:, :M] = buf0
+        lens = lens0.clone()
+    K = args.steps
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    total_ms, per_call = time_calls(call, K, args.warmup, stream)
+    clk = clocks.stop()
+    n_acc = out_n.cpu().numpy()
+    if args.op in ("onehot", "loop"):
+        samp = int(((batch.temperature > 0) & (n_acc >= 0)).sum())
+        abytes = es * V * (B * (G + 1) + samp) + B * G * 8 + B * 12 + B * (G + 1) * 4
+        extra["mean_accepted"] = float(n_acc[n_acc >= 0].mean())
+        if args.op == "loop":
+            abytes += 4 * int(hist.seq_lens.sum()) + B * (G + 1) * 4
+            extra["mean_proposed"] = float(nprop.float().mean().item())
+    elif args.op == "ngram":
+        abytes = 4 * int(hist.seq_lens.sum()) + B * G * 4 + B * 8
+        extra["mean_proposed"] = float(nprop.float().mean().item())
+    else:
+        abytes = B * (G + 1) * 4 + B * 4 * 3 + int((np.maximum(n_acc, -1) + 1).sum()) * 4
+    avg = float(per_call.mean()) * 1e-3
+    achieved = abytes / avg / 1e9
+    line = {
+        "metric": metric, "value": K * per_step / (total_ms * 1e-3), "unit": unit, "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype if args.op in ("onehot", "loop") else "int32", "data": "synthetic",
+        "op": args.op,
+        "config": {"workload": w.description, "B": B, "gamma": G, "V": V,
+                   "histories": f"lengths U(256, {M}), copy probability 0.5, vocab {V}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_call": int(abytes), "avg_call_us": avg * 1e6},
+        "clocks": clk,
+    }
+    line.update(extra)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -229,6 +352,10 @@ def main():
     w = synthetic.BY_NAME[args.workload]
     if args.impl == "reference":
         run_reference(args, w, rank, world)
+        return
+    if args.op != "verify":
+        if rank == 0:
+            run_aux(args, w, local)
         return
 
     import torch
