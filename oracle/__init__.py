@@ -70,6 +70,11 @@ def _bind(lib):
         ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_Detail)]
+    lib.oracle_spec_verify_early.restype = ctypes.c_int
+    lib.oracle_spec_verify_early.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_Detail)]
     lib.oracle_version.restype = ctypes.c_int
     return lib
 
@@ -194,3 +199,37 @@ def verify_threaded(target, draft, tokens, u_accept, u_sample, temperature,
     if detail:
         det = {k: np.concatenate([r[2][k] for r in res]) for k in res[0][2]}
     return out, acc, det
+
+
+def verify_early(target, draft, tokens, u_accept, u_sample, temperature, num_draft=None, detail=False,
+                 lib=None):
+    """The early-exit oracle: positions in order, nothing read after the first
+    rejection. ``draft`` None means one-hot proposals (``num_draft`` [B]
+    required). Returns ``(out_tokens, num_accepted, det)`` like ``verify``."""
+    lib = lib or load()
+    target = np.ascontiguousarray(target)
+    B, G1, V = target.shape
+    G = G1 - 1
+    if draft is not None:
+        draft = np.ascontiguousarray(draft)
+        assert draft.shape == (B, G, V) and draft.dtype == target.dtype
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, G)
+    nd = None if num_draft is None else np.ascontiguousarray(num_draft, dtype=np.int32).reshape(B)
+    u_accept = np.ascontiguousarray(u_accept, dtype=np.float32).reshape(B, G)
+    u_sample = np.ascontiguousarray(u_sample, dtype=np.float32).reshape(B)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+    out_tokens = np.full((B, G1), -7, dtype=np.int32)
+    num_acc = np.full((B,), -7, dtype=np.int32)
+    det = None
+    dptr = None
+    if detail:
+        det = _detail_arrays(B, G)
+        d = _Detail(**{k: _ptr(v) for k, v in det.items()})
+        dptr = ctypes.byref(d)
+    rc = lib.oracle_spec_verify_early(
+        _ptr(target), None if draft is None else _ptr(draft), dtype_code(target), B, G, V, _ptr(tokens),
+        None if nd is None else _ptr(nd), _ptr(u_accept), _ptr(u_sample), _ptr(temperature),
+        _ptr(out_tokens), _ptr(num_acc), dptr)
+    if rc != 0:
+        raise ValueError("oracle_spec_verify_early rejected its arguments")
+    return out_tokens, num_acc, det

@@ -473,3 +473,150 @@ int oracle_spec_verify_onehot(const void* target, int dtype, int B, int gamma, i
     return 0;
 }
 
+/* ------------------------------------------------------------------------
+ * Early exit ("Speculative Decoding — Come Accelerare l'Inferenza LLM di 2-3x
+ * Senza Perdere Qualità", §Il meccanismo: after the first rejection the later
+ * draft tokens are discarded; "Speculative Decoding : accélérer l'inférence
+ * des LLM", §Principe et garanties mathématiques: accept left to right while
+ * compatible). The decisions are those of oracle_spec_verify (or of the
+ * one-hot rule when draft is NULL); the difference is which rows are read:
+ * positions are taken in order and nothing after the first rejection is read,
+ * so a request is invalid only when a row it reads is bad (NaN, +inf, only
+ * -inf): target rows 0..n, the draft rows 0..n of the positions evaluated (T >
+ * 0, model proposals), and row n again for the draw. T, the proposal count and
+ * every proposed token are checked first, as before. */
+
+static int row_ok_at(const scratch_t* s, const void* base, size_t row, double* l) {
+    load_row(base, s->dtype, row, s->V, l);
+    return row_usable(l, s->V);
+}
+
+/* Returns n, or -1 for an invalid request. */
+static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok, int k,
+                        const float* ua, float us, int32_t* out, const oracle_detail* d) {
+    const int G = s->gamma, V = s->V;
+    const int onehot = s->draft == NULL;
+    for (int i = 0; i <= k; ++i) {
+        size_t tr = (size_t)b * (size_t)(G + 1) + (size_t)i;
+        if (!row_ok_at(s, s->target, tr, s->lt)) return -1;
+        set_d(d->max_target, tr, row_max(s->lt, V));
+        set_i(d->argmax_target, tr, row_argmax(s->lt, V));
+        if (T > 0.0) set_d(d->lse_target, tr, softmax_T(s->lt, V, T, s->p));
+        if (i == k) break; /* the extra-token row */
+        const int x = tok[i];
+        size_t r = (size_t)b * (size_t)G + (size_t)i;
+        if (T == 0.0) {
+            const int a = row_argmax(s->lt, V);
+            if (x != a) {
+                out[i] = a;
+                return i;
+            }
+            out[i] = x;
+            continue;
+        }
+        double qx = 1.0;
+        if (!onehot) {
+            if (!row_ok_at(s, s->draft, r, s->ld)) return -1;
+            set_d(d->max_draft, r, row_max(s->ld, V));
+            set_d(d->lse_draft, r, softmax_T(s->ld, V, T, s->q));
+            qx = s->q[x];
+        }
+        const double px = s->p[x];
+        double alpha;
+        if (qx > 0.0)
+            alpha = fmin(px / qx, 1.0);
+        else
+            alpha = (px > 0.0) ? 1.0 : 0.0;
+        const double u = (double)ua[i];
+        set_d(d->p_x, r, px);
+        set_d(d->q_x, r, qx);
+        set_d(d->alpha, r, alpha);
+        set_d(d->accept_margin, r, alpha > 0.0 ? fabs(u - alpha) / alpha : INFINITY);
+        if (!(u < alpha)) {
+            /* the residual of position i: p and q of that position are still in s->p, s->q */
+            double W = 0.0;
+            for (int y = 0; y < V; ++y) {
+                const double qy = onehot ? (y == x ? 1.0 : 0.0) : s->q[y];
+                const double diff = s->p[y] - qy;
+                s->w[y] = diff > 0.0 ? diff : 0.0;
+                W += s->w[y];
+            }
+            if (W == 0.0) /* unreachable in exact arithmetic: fall back to p_i */
+                memcpy(s->w, s->p, sizeof(double) * (size_t)V);
+            double margin = 0.0;
+            out[i] = draw_inverse_cdf(s->w, V, (double)us, &W, &margin);
+            set_i(d->kind, (size_t)b, ORACLE_KIND_RESIDUAL);
+            set_d(d->w_total, (size_t)b, W);
+            set_d(d->sample_margin, (size_t)b, margin);
+            return i;
+        }
+        out[i] = x;
+    }
+    /* all k accepted: the extra token from target row k (in s->lt / s->p) */
+    if (T == 0.0) {
+        out[k] = row_argmax(s->lt, V);
+        return k;
+    }
+    memcpy(s->w, s->p, sizeof(double) * (size_t)V);
+    double W = 0.0, margin = 0.0;
+    out[k] = draw_inverse_cdf(s->w, V, (double)us, &W, &margin);
+    set_i(d->kind, (size_t)b, ORACLE_KIND_BONUS);
+    set_d(d->w_total, (size_t)b, W);
+    set_d(d->sample_margin, (size_t)b, margin);
+    return k;
+}
+
+int oracle_spec_verify_early(const void* target, const void* draft, int dtype, int B, int gamma, int V,
+                             const int32_t* tokens, const int32_t* num_draft, const float* u_accept,
+                             const float* u_sample, const float* temperature, int32_t* out_tokens,
+                             int32_t* out_num_accepted, const oracle_detail* detail) {
+    if (B < 0 || gamma < 1 || V < 1) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+    if (B == 0) return 0;
+    if (!target || !tokens || !u_accept || !u_sample || !temperature || !out_tokens || !out_num_accepted)
+        return -1;
+    if (!draft && !num_draft) return -1;
+    oracle_detail none;
+    memset(&none, 0, sizeof none);
+    const oracle_detail* d = detail ? detail : &none;
+    scratch_t s;
+    memset(&s, 0, sizeof s);
+    s.target = target;
+    s.draft = draft;
+    s.dtype = dtype;
+    s.gamma = gamma;
+    s.V = V;
+    s.lt = (double*)malloc(sizeof(double) * (size_t)V);
+    s.ld = (double*)malloc(sizeof(double) * (size_t)V);
+    s.p = (double*)malloc(sizeof(double) * (size_t)V);
+    s.q = (double*)malloc(sizeof(double) * (size_t)V);
+    s.w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!s.lt || !s.ld || !s.p || !s.q || !s.w) {
+        free(s.lt), free(s.ld), free(s.p), free(s.q), free(s.w);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
+        int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
+        const double T = (double)temperature[b];
+        const int k = draft ? gamma : num_draft[b];
+        for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
+        clear_detail(d, b, gamma);
+        int ok = !(isnan(T) || isinf(T) || T < 0.0) && k >= 0 && k <= gamma;
+        for (int i = 0; ok && i < k; ++i)
+            if (tok[i] < 0 || tok[i] >= V) ok = 0;
+        int n = -1;
+        if (ok) {
+            set_i(d->kind, (size_t)b, T == 0.0 ? ORACLE_KIND_GREEDY : ORACLE_KIND_ERROR);
+            n = verify_early(&s, b, T, tok, k, u_accept + (size_t)b * (size_t)gamma, u_sample[b], out, d);
+        }
+        if (n < 0) {
+            for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
+            clear_detail(d, b, gamma);
+        }
+        out_num_accepted[b] = n;
+    }
+    free(s.lt), free(s.ld), free(s.p), free(s.q), free(s.w);
+    return 0;
+}
+

@@ -112,6 +112,16 @@ int oracle_spec_verify_onehot(const void* target, int dtype, int B, int gamma, i
                               const float* temperature, int32_t* out_tokens,
                               int32_t* out_num_accepted, const oracle_detail* detail);
 
+/* Early exit: the same decisions as oracle_spec_verify (draft != NULL) or
+ * oracle_spec_verify_onehot (draft == NULL, num_draft given), taking positions
+ * in order and reading nothing after the first rejection. A request is
+ * invalid only when a row it reads is bad, or T, the proposal count or a
+ * proposed token is. Detail holds NaN / -1 for the rows not read. */
+int oracle_spec_verify_early(const void* target, const void* draft, int dtype, int B, int gamma, int V,
+                             const int32_t* tokens, const int32_t* num_draft, const float* u_accept,
+                             const float* u_sample, const float* temperature, int32_t* out_tokens,
+                             int32_t* out_num_accepted, const oracle_detail* detail);
+
 #ifdef __cplusplus
 }
 #endif

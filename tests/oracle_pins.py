@@ -464,6 +464,70 @@ def pin_onehot_rows_past_k_unread(lib, quick=False):
         assert np.all(out[b, g + 1:] == -1)
 
 
+# ---------------------------------------------------------------- early exit
+
+def _early(lib, target, draft, tokens, ua, us, T, num_draft=None, detail=False):
+    return oracle.verify_early(target, draft, tokens, ua, us, T, num_draft=num_draft, detail=detail, lib=lib)
+
+
+def pin_early_equals_the_full_read(lib, quick=False):
+    """Reading nothing after the first rejection changes no decision: on valid
+    batches the early-exit oracle equals the pinned full-read rule (model
+    proposals) and the pinned one-hot rule, outputs and facts of the rows it
+    reads; the rows it does not read hold NaN."""
+    rng = np.random.Generator(np.random.Philox(313))
+    B, G, V = (48 if quick else 256), 5, 32
+    lt = rng.normal(0, 1.5, (B, G + 1, V)).astype(np.float32)
+    ld = (lt[:, :G] + rng.normal(0, 0.8, (B, G, V))).astype(np.float32)
+    x = np.argmax(ld + rng.gumbel(size=(B, G, V)).astype(np.float32), axis=2).astype(np.int32)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    T = rng.choice(np.array([0.0, 0.6, 1.0], np.float32), B)
+    o1, n1, d1 = _run(lib, lt, ld, x, ua, us, T, detail=True)
+    o2, n2, d2 = _early(lib, lt, ld, x, ua, us, T, detail=True)
+    assert np.array_equal(o1, o2) and np.array_equal(n1, n2)
+    for b in range(B):
+        n = n1[b]
+        for key in ("max_target", "argmax_target"):
+            assert np.array_equal(d1[key][b, :n + 1], d2[key][b, :n + 1]), (b, key)
+        if T[b] > 0:
+            assert np.allclose(d1["lse_target"][b, :n + 1], d2["lse_target"][b, :n + 1], rtol=0, atol=0)
+            assert np.array_equal(d1["p_x"][b, :n + 1][:G], d2["p_x"][b, :n + 1][:G], equal_nan=True)
+            assert d1["w_total"][b] == d2["w_total"][b]
+        assert np.all(np.isnan(d2["max_target"][b, n + 1:]))
+    k = rng.integers(0, G + 1, B).astype(np.int32)
+    o3, n3, _ = oracle.verify_onehot(lt, x, k, ua, us, T, lib=lib)
+    o4, n4, _ = _early(lib, lt, None, x, ua, us, T, num_draft=k)
+    assert np.array_equal(o3, o4) and np.array_equal(n3, n4)
+
+
+def pin_early_reads_nothing_after_the_rejection(lib, quick=False):
+    """A bad row after the first rejection (or, at T = 0, after the first
+    mismatch) is never read: the request keeps its result. A bad row at or
+    before it makes the request invalid."""
+    rng = np.random.Generator(np.random.Philox(314))
+    B, G, V = 40, 6, 24
+    lt = rng.normal(0, 1.5, (B, G + 1, V)).astype(np.float32)
+    ld = (lt[:, :G] + rng.normal(0, 1.5, (B, G, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    T = np.where(np.arange(B) % 5 == 0, 0.0, 0.8).astype(np.float32)
+    o, n, _ = _early(lib, lt, ld, x, ua, us, T)
+    assert np.all(n >= 0) and np.any(n < G)
+    lt2, ld2 = lt.copy(), ld.copy()
+    for b in range(B):
+        lt2[b, n[b] + 1:, 3] = np.nan
+        ld2[b, n[b] + 1:, 5] = np.nan
+    o2, n2, _ = _early(lib, lt2, ld2, x, ua, us, T)
+    assert np.array_equal(o, o2) and np.array_equal(n, n2)
+    lt3 = lt.copy()
+    for b in range(B):
+        lt3[b, n[b], 7] = np.inf
+    _, n3, _ = _early(lib, lt3, ld, x, ua, us, T)
+    assert np.all(n3 == -1)
+
+
 ALL_PINS = [
     pin_hand_examples,
     pin_accept_probability,
@@ -480,4 +544,6 @@ ALL_PINS = [
     pin_onehot_is_the_general_rule,
     pin_onehot_accept_probability_and_distribution,
     pin_onehot_rows_past_k_unread,
+    pin_early_equals_the_full_read,
+    pin_early_reads_nothing_after_the_rejection,
 ]

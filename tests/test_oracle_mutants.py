@@ -59,6 +59,14 @@ MUTANTS = [
     ("onehot_bonus_from_row_gamma", "(size_t)b * (size_t)(G + 1) + (size_t)k, V, s->lt);\n        softmax_T",
      "(size_t)b * (size_t)(G + 1) + (size_t)G, V, s->lt);\n        softmax_T"),
     ("onehot_count_ignored", "        int k = num_draft[b];", "        int k = gamma;"),
+    # early exit
+    ("early_alpha_ignores_q", "            alpha = fmin(px / qx, 1.0);", "            alpha = fmin(px, 1.0);"),
+    ("early_greedy_keeps_draft_token", "                out[i] = a;\n                return i;",
+     "                out[i] = x;\n                return i;"),
+    ("early_extra_token_from_row_k_minus_1", "    for (int i = 0; i <= k; ++i) {\n        size_t tr",
+     "    for (int i = 0; i < k + (k == 0); ++i) {\n        size_t tr"),
+    ("early_onehot_residual_keeps_x", "const double qy = onehot ? (y == x ? 1.0 : 0.0) : s->q[y];",
+     "const double qy = onehot ? 0.0 : s->q[y];"),
 ]
 
 
