@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--early-exit", action="store_true",
+                    help="early-exit verification: nothing after a request's first rejection is read")
     ap.add_argument("--op", choices=["verify", "onehot", "ngram", "commit", "loop"], default="verify",
                     help="verify (default, the headline); onehot: spec_verify_onehot on the workload's "
                          "target rows; ngram: spec_ngram_propose; commit: spec_commit; loop: ngram -> "
@@ -99,6 +101,25 @@ def kernel_hash() -> str:
             with open(os.path.join(base, name), "rb") as f:
                 h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
+
+
+def algorithmic_bytes_early(batch, num_accepted) -> int:
+    """Early exit: the rows the method needs. Per request with n accepted:
+    target rows 0..n (n + 1 rows), the draft rows of the positions evaluated
+    (T > 0: min(n + 1, g)), and the draw's re-read (2 rows for a residual, 1
+    for the extra token); plus the small inputs and outputs."""
+    w = batch.workload
+    s, V, G, B = w.elem_bytes, w.V, w.gamma, batch.B
+    rows = 0
+    for b in range(B):
+        n = int(num_accepted[b])
+        if n < 0:
+            rows += 1
+            continue
+        rows += n + 1
+        if batch.temperature[b] > 0:
+            rows += min(n + 1, G) + (2 if n < G else 1)
+    return int(s * V * rows + B * G * 8 + B * 12 + B * (G + 1) * 4)
 
 
 def algorithmic_bytes(batch, num_accepted) -> int:
@@ -381,7 +402,7 @@ def main():
 
     def call():
         sv.spec_verify(*dev, out_tokens=out_tokens, out_num_accepted=out_n, workspace=ws,
-                       stream=stream, path=path)
+                       stream=stream, path=path, early_exit=args.early_exit)
 
     for _ in range(max(3, args.warmup)):
         call()
@@ -418,7 +439,7 @@ def main():
     rows_per_step = B * (G + 1)
     value = world * K * rows_per_step / (total_ms * 1e-3)
 
-    abytes = algorithmic_bytes(batch, num_acc)
+    abytes = (algorithmic_bytes_early if args.early_exit else algorithmic_bytes)(batch, num_acc)
     peak, peak_src = peak_hbm()
     avg_call_s = float(per_call_ms.mean()) * 1e-3
     achieved = abytes / avg_call_s / 1e9
@@ -478,6 +499,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.description, "B": B, "gamma": G, "V": V, "logits": w.dtype,
                    "seeds": f"1000*{w.config}+rank", "path": args.path,
+                   "early_exit": bool(args.early_exit),
                    "l2": f"inputs {(batch.target.nbytes + batch.draft.nbytes) / 1e9:.2f} GB > 129 MB L2; "
                          "no flush between steps",
                    "parallelism": f"replicas: {world} independent batches"},

@@ -162,7 +162,11 @@ typedef struct {
                              microseconds; 0 = the default (about 2 s). A block whose wait
                              runs out sets SV_STATUS_TIMEOUT, ends its draw phase and
                              returns; the call's outputs are then not valid. */
-    int32_t reserved0;
+    int32_t early_exit; /* non-zero: early-exit verification. Positions are taken in
+                           order and nothing after a request's first rejection (first
+                           mismatch at T = 0) is read: same outputs, fewer bytes; a
+                           request is then invalid only when a row it reads is bad.
+                           Checking outputs hold NaN / -1 for the rows not read. */
     const int32_t* hold_flag; /* streaming path, checking only; NULL normally. A device
                                  int32: every block waits, for at most peer_wait_us, until
                                  it is non-zero before its draw phase. A flag nothing sets

@@ -50,7 +50,7 @@ class _Debug(ctypes.Structure):
 
 class _Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
-                ("peer_wait_us", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("peer_wait_us", ctypes.c_int32), ("early_exit", ctypes.c_int32),
                 ("hold_flag", ctypes.c_void_p), ("num_draft", ctypes.c_void_p)]
 
 
@@ -156,7 +156,8 @@ def _ptr(t) -> int:
 def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, temperature,
                 out_tokens=None, out_num_accepted=None, workspace=None, stream=None,
                 debug: bool = False, path: int = SV_PATH_AUTO, grid_ctas: int = 0,
-                status=None, peer_wait_us: int = 0, hold_flag=None, num_draft=None) -> Outputs:
+                status=None, peer_wait_us: int = 0, hold_flag=None, num_draft=None,
+                early_exit: bool = False) -> Outputs:
     """Verify one batch of CUDA tensors (see include/specverify.h).
 
     ``target_logits`` [B, gamma+1, V] and ``draft_logits`` [B, gamma, V]
@@ -190,7 +191,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
             _ptr(out_num_accepted), _ptr(workspace), workspace.numel() * workspace.element_size(), s)
     dbg = None
     if (debug or path != SV_PATH_AUTO or grid_ctas or status is not None or peer_wait_us or hold_flag is not None
-            or draft_logits is None):
+            or draft_logits is None or early_exit):
         d = _Debug()
         if debug:
             f64, f32, i32 = torch.float64, torch.float32, torch.int32
@@ -209,7 +210,8 @@ def spec_verify(target_logits, draft_logits, draft_tokens, u_accept, u_sample, t
             dbg["phase_ns"][0] = -1  # UINT64_MAX
             for k, v in dbg.items():
                 setattr(d, k, v.data_ptr())
-        o = _Options(path, grid_ctas, peer_wait_us, 0, _ptr(hold_flag) or None, _ptr(num_draft) or None)
+        o = _Options(path, grid_ctas, peer_wait_us, 1 if early_exit else 0, _ptr(hold_flag) or None,
+                     _ptr(num_draft) or None)
         rc = lib.spec_verify_ex(*args, ctypes.byref(d), _ptr(status), ctypes.byref(o))
         _check(rc, "spec_verify_ex")
     else:

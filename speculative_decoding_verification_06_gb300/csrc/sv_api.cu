@@ -118,6 +118,7 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     a.target = target_logits;
     a.draft = draft_logits;
     a.onehot = draft_logits == nullptr;
+    a.early = opts && opts->early_exit != 0;
     a.num_draft = (a.onehot && opts) ? opts->num_draft : nullptr;
     a.dtype = dtype;
     a.B = B;

@@ -15,6 +15,7 @@ struct Args {
     const void* target;  // [B, gamma+1, V]
     const void* draft;   // [B, gamma, V]; null in one-hot mode
     bool onehot;               // deterministic proposals: q_i one-hot at x_i, no draft logits
+    bool early;                // early exit: nothing after a request's first rejection is read
     const int32_t* num_draft;  // one-hot mode: proposals per request [B] (null: gamma each)
     int dtype;           // SV_F32 / SV_BF16
     int B, gamma, V;

@@ -37,6 +37,8 @@ struct Shared {
     DrawParams draw;
     int n;
     int request_bad;
+    int last_row;  // early exit: the last position whose rows were read
+    int stop;
 };
 
 template <int DT>
@@ -150,7 +152,46 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             if (x < 0 || x >= V) bad = 1;
         }
         bad = __syncthreads_or(bad);
-        if (!bad) {
+        if (!bad && a.early) {
+            // Early exit: position i's rows, then its decision on thread 0; nothing
+            // after the first rejection (or mismatch at T = 0) is read. The scan
+            // below then meets the same decisions from these rows.
+            const int32_t* tok = a.tokens + static_cast<size_t>(b) * G;
+            for (int i = 0; i <= np; ++i) {
+                const size_t trow = static_cast<size_t>(b) * (G + 1) + i;
+                const RowStat st = greedy ? row_argmax<DT>(a.target, trow, V, sh)
+                                          : row_maxsum<DT>(a.target, trow, V, c, sh);
+                const bool has_draft = !greedy && !a.onehot && i < np;
+                RowStat sd;
+                if (has_draft) sd = row_maxsum<DT>(a.draft, static_cast<size_t>(b) * G + i, V, c, sh);
+                if (threadIdx.x == 0) {
+                    sh.st[i] = st;
+                    if (has_draft) sh.st[G + 1 + i] = sd;
+                    int stop = (st.bad || (has_draft && sd.bad)) ? 2 : 0;
+                    if (!stop) {
+                        if (i == np) {
+                            stop = 1;
+                        } else if (greedy) {
+                            stop = tok[i] != st.idx ? 1 : 0;
+                        } else {
+                            const int x = tok[i];
+                            const double p = prob_from_stats(
+                                load_logit<DT>(a.target, trow * V + x), st.m, st.s, c);
+                            const double q = a.onehot ? 1.0
+                                                      : prob_from_stats(load_logit<DT>(
+                                                                            a.draft, (static_cast<size_t>(b) * G + i) * V + x),
+                                                                        sd.m, sd.s, c);
+                            stop = accept_draft(p, q, a.u_accept[static_cast<size_t>(b) * G + i]) ? 0 : 1;
+                        }
+                    }
+                    sh.stop = stop;
+                    sh.last_row = i;
+                }
+                __syncthreads();
+                if (sh.stop) break;
+            }
+            bad = sh.stop == 2;
+        } else if (!bad) {
             const int nrows = (greedy || a.onehot) ? np + 1 : 2 * G + 1;
             for (int r = 0; r < nrows; ++r) {
                 RowStat st;
@@ -200,9 +241,10 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
         }
 
         // Per-row checking outputs.
+        const int last = a.early ? sh.last_row : (a.onehot ? np : G);  // last target row read
         for (int j = threadIdx.x; j <= G; j += kThreads) {
             size_t r = static_cast<size_t>(b) * (G + 1) + j;
-            const bool read = j <= np || !a.onehot;
+            const bool read = j <= last;
             const RowStat& st = sh.st[j];
             if (a.dbg.max_target) a.dbg.max_target[r] = read ? st.m : nanf("");
             if (a.dbg.lse_target)
@@ -211,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
         }
         for (int j = threadIdx.x; j < G; j += kThreads) {
             size_t r = static_cast<size_t>(b) * G + j;
-            const bool draft = !greedy && !a.onehot;
+            const bool draft = !greedy && !a.onehot && (!a.early || (j <= last && j < np));
             const RowStat& st = sh.st[G + 1 + j];
             if (a.dbg.max_draft) a.dbg.max_draft[r] = draft ? st.m : nanf("");
             if (a.dbg.lse_draft) a.dbg.lse_draft[r] = draft ? lse_from_stats(st.m, st.s, c, T) : nan("");

@@ -82,17 +82,29 @@ struct Job {
     DrawParams d;
 };
 
-// What a draw-phase stage holds: chunk j of job k (kind kEndKind: none).
+// What a draw-phase stage holds: chunk j of job k (kind kEndKind: none). In
+// the early-exit kernel: chunk j of task k, a row-statistics task (type
+// kTaskStats: request job.b, position job.n, scale job.d.c, flags) or a draw
+// task (type kTaskDraw, the job itself).
 struct StageDesc {
     Job job;
     int32_t k, j;
+    int32_t type, flags;
 };
+
+// Early-exit tasks: the row statistics of one position of one request (the
+// target row, and the draft row for model proposals at T > 0), or one draw.
+constexpr int kTaskStats = 0;
+constexpr int kTaskDraw = 1;
+constexpr int kStatsArgmax = 1;  // StageDesc.flags: argmax (T == 0) instead of (max, sum)
+constexpr int kStatsDraft = 2;   // StageDesc.flags: the stage also holds the draft row's chunk
 
 // Byte offsets into the caller's workspace and the partition constants.
 struct Layout {
     long long Et;  // target elements B*(gamma+1)*V
     int G, MT, MD, NCH, vec;
-    size_t hdr, req_done, job_done, ready, clear_bytes, rec_t, rec_d, jobs, wsums, total;
+    size_t hdr, req_done, job_done, ready, ee_tasks, ee_done, clear_bytes, rec_t, rec_d, ee_rec, jobs, wsums, total;
+    int ee_cap;  // early exit: task slots, B (gamma + 2)
 };
 
 __host__ __device__ inline long long part_begin(long long E, int G, int g, int vec) {
@@ -124,9 +136,15 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.req_done = take(static_cast<size_t>(B) * 4);  // logits folded, per request
     L.job_done = take(static_cast<size_t>(B) * 4);  // chunks summed, per draw job
     L.ready = take(static_cast<size_t>(B) * 4);     // published draw jobs (k + 1), in order
-    L.clear_bytes = off;                            // cleared before every launch
+    // early exit: B position-0 tasks, then at most gamma more positions and one
+    // draw per request
+    L.ee_cap = B * (gamma + 2);
+    L.ee_tasks = take(static_cast<size_t>(L.ee_cap) * 4);  // published tasks (encoded + 1)
+    L.ee_done = take(static_cast<size_t>(L.ee_cap) * 4);   // chunks done, per task
+    L.clear_bytes = off;                                   // cleared before every launch
     L.rec_t = take(static_cast<size_t>(G) * L.MT * sizeof(Rec));
     L.rec_d = take(static_cast<size_t>(G) * L.MD * sizeof(Rec));
+    L.ee_rec = take(static_cast<size_t>(L.ee_cap) * L.NCH * 2 * sizeof(Rec));  // per (task, chunk): target, draft
     L.jobs = take(static_cast<size_t>(B) * sizeof(Job));
     L.wsums = take(static_cast<size_t>(B) * L.NCH * kConsumerWarps * 8);
     L.total = off;
@@ -252,8 +270,9 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
 
 struct Hdr {
     int status;          // SV_STATUS_* bits of this call
-    unsigned n_pub;      // draw jobs published so far
+    unsigned n_pub;      // draw jobs (early exit: tasks past the first B) published so far
     unsigned next_item;  // draw items handed out so far
+    unsigned n_fin;      // early exit: requests finished
 };
 
 // Checking output: global-timer stamps (see sv_debug_out.phase_ns).
@@ -283,6 +302,7 @@ struct Ctl {
     int map[kMapMax];
     int wtmp[kConsumerWarps + 1];
     Rec wrec[kFlushSlots][kConsumerWarps];  // per-warp partials of a row piece
+    Rec wrec2[kFlushSlots][kConsumerWarps]; // early exit: per-warp partials of the draft row
     int wcnt[kFlushSlots];                  // warps that have flushed the piece
     int fq_item[kQueue];                    // finisher ring: request (phase 1) or job (phase 2)
     unsigned fq_val[kQueue];                // logits (phase 1) or chunks (phase 2) it covers
@@ -343,6 +363,9 @@ struct Kern {
     __device__ unsigned* req_done() const { return reinterpret_cast<unsigned*>(ws + L.req_done); }
     __device__ unsigned* job_done() const { return reinterpret_cast<unsigned*>(ws + L.job_done); }
     __device__ int* ready() const { return reinterpret_cast<int*>(ws + L.ready); }
+    __device__ int* ee_tasks() const { return reinterpret_cast<int*>(ws + L.ee_tasks); }
+    __device__ unsigned* ee_done() const { return reinterpret_cast<unsigned*>(ws + L.ee_done); }
+    __device__ Rec* ee_rec() const { return reinterpret_cast<Rec*>(ws + L.ee_rec); }
     __device__ unsigned long long* wsums() const {
         return reinterpret_cast<unsigned long long*>(ws + L.wsums);
     }
@@ -543,15 +566,16 @@ struct Kern {
     // global counter (with the fences its reader needs) and returns whether
     // that completed the item; work(item), on the whole warp, then finishes
     // each completed item.
-    template <typename C, typename W>
-    __device__ void finish(C&& count, W&& work) const {
+    // poll(), on the whole warp, runs owned work that became ready and says
+    // whether it did; owned_done(), on lane 0, says that no owned work remains.
+    template <typename C, typename W, typename P, typename D>
+    __device__ void finish(C&& count, W&& work, P&& poll, D&& owned_done) const {
         const int lane = threadIdx.x & 31;
         volatile unsigned* vseq = ctl.fq_seq;
         volatile int* vdone = &ctl.cons_done;
         unsigned head = 0;
         volatile int* vabort = &ctl.abort;
         unsigned long long t0 = global_ns(), last_poll = 0;
-        int own_p = blockIdx.x, own_k = -1;  // lane 0: next owned job position, its job
         for (;;) {
             const unsigned s = head + lane;
             const unsigned ready = __ballot_sync(0xffffffffu, vseq[s % kQueue] == s + 1);
@@ -580,7 +604,7 @@ struct Kern {
                 continue;
             }
             if (global_ns() - last_poll > 500ull) {
-                if (poll_owned(own_p, own_k)) {
+                if (poll()) {
                     t0 = global_ns();
                     continue;
                 }
@@ -592,7 +616,7 @@ struct Kern {
                     stop = 1;
                 } else if (*vdone == kConsumerWarps) {
                     __threadfence_block();
-                    if (*reinterpret_cast<volatile unsigned*>(&ctl.fq_tail) == head && own_p >= ctl.n_samp) stop = 1;
+                    if (*reinterpret_cast<volatile unsigned*>(&ctl.fq_tail) == head && owned_done()) stop = 1;
                 }
                 if (!stop && global_ns() - t0 > kWaitTimeoutNs) {
                     set_abort(a.d_status);
@@ -732,16 +756,19 @@ struct Kern {
 
     // Folds one stage (nvec 16-byte vectors, element offset e0 in the row).
     // Full stages (the common case) take a path without per-vector bounds.
+    // NV vectors of 16 bytes per consumer thread: a phase-1 stage (kVecPerThread)
+    // or one draw-sized chunk of a row (kVecPerThread / 2, early exit).
+    template <int NV = kVecPerThread>
     __device__ __forceinline__ void fold_stage(RowState& rs, const char* sm, int nvec, long long e0) const {
-        uint4 v[kVecPerThread];
+        uint4 v[NV];
         const int t = threadIdx.x;
-        if (nvec == kVecPerThread * kConsumers) {
+        if (nvec == NV * kConsumers) {
 #pragma unroll
-            for (int k = 0; k < kVecPerThread; ++k)
+            for (int k = 0; k < NV; ++k)
                 v[k] = *reinterpret_cast<const uint4*>(sm + static_cast<size_t>(t + k * kConsumers) * 16);
         } else {
 #pragma unroll
-            for (int k = 0; k < kVecPerThread; ++k) {
+            for (int k = 0; k < NV; ++k) {
                 const int vi = t + k * kConsumers;
                 if (vi < nvec)
                     v[k] = *reinterpret_cast<const uint4*>(sm + static_cast<size_t>(vi) * 16);
@@ -751,23 +778,24 @@ struct Kern {
                     v[k] = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
             }
         }
-        fold_vectors(rs, v, e0);
+        fold_vectors<NV>(rs, v, e0);
     }
 
-    __device__ __forceinline__ void fold_vectors(RowState& rs, const uint4 (&v)[kVecPerThread], long long e0) const {
+    template <int NV>
+    __device__ __forceinline__ void fold_vectors(RowState& rs, const uint4 (&v)[NV], long long e0) const {
         const int t = threadIdx.x;
         float tmax;
         if (DT == SV_BF16) {
             uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(v[0].x, v[0].y), bf16x2_max_nan(v[0].z, v[0].w));
 #pragma unroll
-            for (int k = 1; k < kVecPerThread; ++k)
+            for (int k = 1; k < NV; ++k)
                 m2 = bf16x2_max_nan(m2, bf16x2_max_nan(bf16x2_max_nan(v[k].x, v[k].y),
                                                        bf16x2_max_nan(v[k].z, v[k].w)));
             tmax = f32_max_nan(bf16x2_lo(m2), bf16x2_hi(m2));
         } else {
             tmax = neg_inf();
 #pragma unroll
-            for (int k = 0; k < kVecPerThread; ++k)
+            for (int k = 0; k < NV; ++k)
                 tmax = f32_max_nan(tmax, f32_max_nan(f32_max_nan(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
                                                      f32_max_nan(__uint_as_float(v[k].z), __uint_as_float(v[k].w))));
         }
@@ -781,7 +809,7 @@ struct Kern {
                 // first position of tmax among this thread's elements (increasing index)
                 int found = -1;
 #pragma unroll
-                for (int k = kVecPerThread - 1; k >= 0; --k) {
+                for (int k = NV - 1; k >= 0; --k) {
                     const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
                     for (int q = 3; q >= 0; --q) {
@@ -810,7 +838,7 @@ struct Kern {
         const unsigned long long cc = f2_pack(c, c), nmc = f2_pack(-rs.mc, -rs.mc);
         unsigned long long acc = f2_pack(0.0f, 0.0f);
 #pragma unroll
-        for (int k = 0; k < kVecPerThread; ++k) {
+        for (int k = 0; k < NV; ++k) {
             const uint32_t w4[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
             for (int q = 0; q < 4; q += (DT == SV_BF16 ? 1 : 2)) {
@@ -1212,7 +1240,15 @@ struct Kern {
             }
             ctot[h] = sum;
         }
-        const Job jb = gjobs[k];
+        // the job comes from L2: it was written by another block, and a job
+        // sharing its cache line may have been read here earlier
+        Job jb;
+        {
+            const int* src = reinterpret_cast<const int*>(gjobs + k);
+            int* dst = reinterpret_cast<int*>(&jb);
+#pragma unroll
+            for (int q = 0; q < static_cast<int>(sizeof(Job) / 4); ++q) dst[q] = __ldcg(src + q);
+        }
         if (jb.kind != kKindResidual && jb.kind != kKindBonus && jb.kind != kKindResidualOnehot) return;
         DrawParams d = jb.d;
         int kind = jb.kind;
@@ -1370,6 +1406,500 @@ struct Kern {
                 kind == kKindResidual ? W * kFixResidualInv : W * kFixTargetInv * static_cast<double>(d.isp);
         }
     }
+
+    // ================================================================ early exit
+    // "Speculative Decoding — Come Accelerare l'Inferenza LLM di 2-3x Senza
+    // Perdere Qualità", §Il meccanismo: after the first rejection the later draft
+    // tokens are discarded, so their rows need not be read. The work is a list of
+    // tasks, each cut into L.NCH chunks of kChunkBytes of a row: the row
+    // statistics of one position of one request (its target row, and its draft
+    // row for model proposals at T > 0), or one draw. Tasks 0..B-1 are position 0
+    // of every request; the owner of a statistics task (block p mod G) decides
+    // that position and publishes the request's next task: its next position,
+    // or its draw. Producers take chunks of tasks in publication order.
+
+    __device__ static int ee_encode(int type, int b, int pos) { return ((type << 28) | (b << 8) | pos) + 1; }
+
+    // Proposals of request b (range-checked by the owner of its position 0).
+    __device__ int ee_kb(int b) const { return a.onehot && a.num_draft ? a.num_draft[b] : a.gamma; }
+
+    // One lane: appends a task (after whatever it reads is written).
+    __device__ void ee_publish(int type, int b, int pos) const {
+        __threadfence();
+        const unsigned q = atomicAdd(&hdr()->n_pub, 1u);
+        if (static_cast<long long>(a.B) + q < static_cast<long long>(L.ee_cap))  // always: at most gamma + 1 per request
+            reinterpret_cast<volatile int*>(ee_tasks())[a.B + q] = ee_encode(type, b, pos);
+    }
+
+    // One lane: request b is done (its outputs are written).
+    __device__ void ee_finish_request() const {
+        __threadfence();
+        atomicAdd(&hdr()->n_fin, 1u);
+    }
+
+    // One lane: task slot p will stay empty (every request is finished and the
+    // published tasks end before p).
+    __device__ bool ee_no_task(int p) const {
+        if (p >= L.ee_cap) return true;
+        if (*reinterpret_cast<volatile unsigned*>(&hdr()->n_fin) < static_cast<unsigned>(a.B)) return false;
+        __threadfence();
+        return static_cast<long long>(p) >=
+               static_cast<long long>(a.B) + *reinterpret_cast<volatile unsigned*>(&hdr()->n_pub);
+    }
+
+    __device__ void start_row_mode(RowState& rs, bool argmax, float c) const {
+        rs.argmax = argmax;
+        rs.c = c;
+        rs.m = neg_inf();
+        rs.mc = neg_inf();
+        rs.s = 0.0f;
+        rs.idx = 0x7fffffff;
+        rs.bad = 0;
+    }
+
+    // The lanes of a warp reduced to one record (every lane holds it).
+    __device__ static Rec warp_rec(const RowState& rs) {
+        const int bad = __any_sync(0xffffffffu, rs.bad);
+        if (rs.argmax) {
+            ArgMax st{rs.m, rs.idx};
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                ArgMax ot{__shfl_xor_sync(0xffffffffu, st.v, o), __shfl_xor_sync(0xffffffffu, st.i, o)};
+                st = argmax_merge(st, ot);
+            }
+            return Rec{st.v, 0.0f, st.i, bad};
+        }
+        MaxSum st{rs.m, rs.s};
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            MaxSum ot{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
+            st = maxsum_merge(st, ot, rs.c);
+        }
+        return Rec{st.m, st.s, -1, bad};
+    }
+
+    __device__ static Rec rec_merge(Rec x, const Rec& y, bool argmax, float c) {
+        x.bad |= y.bad;
+        if (argmax) {
+            const ArgMax m = argmax_merge(ArgMax{x.m, x.idx}, ArgMax{y.m, y.idx});
+            x.m = m.v;
+            x.idx = m.i;
+        } else {
+            const MaxSum m = maxsum_merge(MaxSum{x.m, x.s}, MaxSum{y.m, y.s}, c);
+            x.m = m.m;
+            x.s = m.s;
+        }
+        return x;
+    }
+
+    // End of a statistics chunk: each warp parks its records; the last warp
+    // merges the twelve in warp order, writes the chunk's records and posts the
+    // task to the finisher.
+    __device__ void ee_flush_item(const RowState& rt, const RowState& rd, bool has_draft, unsigned seq, int p,
+                                  int j) const {
+        const Rec t = warp_rec(rt);
+        Rec d = t;
+        if (has_draft) d = warp_rec(rd);
+        if ((threadIdx.x & 31) == 0) {
+            const int warp = threadIdx.x >> 5;
+            const int fs = static_cast<int>(seq % kFlushSlots);
+            ctl.wrec[fs][warp] = t;
+            ctl.wrec2[fs][warp] = d;
+            __threadfence_block();
+            if (atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1) {
+                __threadfence_block();
+                Rec ot = ctl.wrec[fs][0], od = ctl.wrec2[fs][0];
+                for (int w = 1; w < kConsumerWarps; ++w) {
+                    ot = rec_merge(ot, ctl.wrec[fs][w], rt.argmax, rt.c);
+                    if (has_draft) od = rec_merge(od, ctl.wrec2[fs][w], false, rd.c);
+                }
+                ctl.wcnt[fs] = 0;
+                Rec* dst = ee_rec() + (static_cast<size_t>(p) * L.NCH + j) * 2;
+                dst[0] = ot;
+                dst[1] = od;
+                if (!post(p | kJobMsg, 1u)) set_abort(a.d_status);
+            }
+        }
+    }
+
+    // Producer warp: chunks of tasks in publication order, one at a time from the
+    // global counter (a task's chunks then run on as many blocks), until every
+    // request is finished; then the end marker.
+    __device__ void ee_produce(Cursor& prod) const {
+        const int lane = threadIdx.x & 31;
+        volatile int* vabort = &ctl.abort;
+        Hdr* h = hdr();
+        const int NCH = L.NCH, GM = a.gamma;
+        constexpr int CH = kChunkElems;
+        unsigned next = 0;
+        if (lane == 0) next = atomicAdd(&h->next_item, 1u);
+        long long i = 0, i_end = 0;
+        int cur_p = -1;
+        StageDesc desc;  // lane 0's copy of the current task
+        desc.k = -1;
+        desc.type = -1;
+        desc.flags = 0;
+        desc.job.b = 0;
+        desc.job.n = 0;
+        desc.job.kind = 0;
+        bool ok = true;
+        while (ok && !*vabort) {
+            if (i == i_end) {
+                i = __shfl_sync(0xffffffffu, next, 0);
+                i_end = i + 1;
+                if (lane == 0) next = atomicAdd(&h->next_item, 1u);  // the next chunk, in flight meanwhile
+            }
+            const int p = static_cast<int>(i / NCH), j = static_cast<int>(i - static_cast<long long>(p) * NCH);
+            if (p != cur_p) {
+                int state = 1;  // 1 task known, 0 no more tasks, -1 the wait ran out
+                if (lane == 0) {
+                    int v = 0;
+                    if (p < a.B) {
+                        v = ee_encode(kTaskStats, p, 0);
+                    } else if (p >= L.ee_cap) {
+                        state = 0;
+                    } else {
+                        const volatile int* tp = ee_tasks() + p;
+                        const unsigned long long t0 = global_ns();
+                        while ((v = *tp) == 0) {
+                            if (ee_no_task(p)) {
+                                state = 0;
+                                break;
+                            }
+                            if (*vabort || global_ns() - t0 > a.peer_wait_ns) {
+                                state = -1;
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                    }
+                    if (state == 1) {
+                        __threadfence();
+                        v -= 1;
+                        const int type = v >> 28, b = (v >> 8) & 0xfffff, pos = v & 0xff;
+                        desc.k = p;
+                        desc.type = type;
+                        if (type == kTaskStats) {
+                            const float T = a.temperature[b];
+                            const bool samp = sampled(T);
+                            const int kb = ee_kb(b);
+                            desc.job.b = b;
+                            desc.job.n = pos;
+                            desc.job.kind = 0;
+                            desc.job.d.c = samp ? temp_scale(T) : 0.0f;
+                            desc.flags = (samp ? 0 : kStatsArgmax) |
+                                         ((samp && !a.onehot && pos < kb && pos < GM) ? kStatsDraft : 0);
+                        } else {
+                            const int* src = reinterpret_cast<const int*>(jobs() + b);
+                            int* dst = reinterpret_cast<int*>(&desc.job);
+#pragma unroll
+                            for (int q = 0; q < static_cast<int>(sizeof(Job) / 4); ++q) dst[q] = __ldcg(src + q);
+                            desc.flags = 0;
+                        }
+                    }
+                }
+                state = __shfl_sync(0xffffffffu, state, 0);
+                if (state <= 0) {
+                    if (state < 0 && lane == 0) set_abort(a.d_status);
+                    break;
+                }
+                cur_p = p;
+            }
+            const int type = __shfl_sync(0xffffffffu, desc.type, 0);
+            const int flags = __shfl_sync(0xffffffffu, desc.flags, 0);
+            const int b = __shfl_sync(0xffffffffu, desc.job.b, 0);
+            const int pos = __shfl_sync(0xffffffffu, desc.job.n, 0);
+            const int kind = __shfl_sync(0xffffffffu, desc.job.kind, 0);
+            desc.j = j;
+            const long long e0 = static_cast<long long>(j) * CH;
+            const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+            const unsigned bytes = static_cast<unsigned>(cnt * ES);
+            const long long trow = static_cast<long long>(b) * (GM + 1) + pos;  // pos: the draw's row n for draws
+            const char* src_t = static_cast<const char*>(a.target) + (trow * a.V + e0) * ES;
+            const bool two = type == kTaskStats ? (flags & kStatsDraft) != 0 : kind == kKindResidual;
+            if (two) {
+                const long long drow = static_cast<long long>(b) * GM + pos;
+                ok = produce(prod, src_t, bytes, static_cast<const char*>(a.draft) + (drow * a.V + e0) * ES, bytes,
+                             &desc);
+            } else {
+                ok = produce(prod, src_t, bytes, nullptr, 0u, &desc);
+            }
+            ++i;
+        }
+        if (!ok && lane == 0) set_abort(a.d_status);
+        __syncwarp();
+        StageDesc end;
+        end.job.kind = kEndKind;
+        end.k = -1;
+        end.j = -1;
+        end.type = -1;
+        end.flags = 0;
+        produce(prod, nullptr, 0u, nullptr, 0u, &end);  // bounded; the consumers' own waits are too
+    }
+
+    // Consumer warps: statistics chunks and draw chunks until the end marker.
+    __device__ void ee_consume(Cursor& cons) const {
+        const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+        constexpr int CH = kChunkElems, TPT = kTPT, NVC = kChunkBytes / 16 / kConsumers;
+        unsigned long long* ws_sum = wsums();
+        for (unsigned iseq = 0;; ++iseq) {
+            const int slot = static_cast<int>(cons.it % kStages);
+            const char* smt = consume_begin(cons);
+            if (!smt) {
+                set_abort(a.d_status);
+                break;
+            }
+            const StageDesc ds = ctl.desc[slot];
+            if (ds.job.kind == kEndKind) {
+                consume_end(cons);
+                break;
+            }
+            const long long e0 = static_cast<long long>(ds.j) * CH;
+            const int n = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+            if (ds.type == kTaskStats) {
+                const bool argmax = (ds.flags & kStatsArgmax) != 0, has_draft = (ds.flags & kStatsDraft) != 0;
+                RowState rt, rd;
+                start_row_mode(rt, argmax, ds.job.d.c);
+                start_row_mode(rd, false, ds.job.d.c);
+                fold_stage<NVC>(rt, smt, n * ES / 16, e0);
+                if (has_draft) fold_stage<NVC>(rd, smt + kChunkBytes, n * ES / 16, e0);
+                consume_end(cons);
+                ee_flush_item(rt, rd, has_draft, iseq, ds.k, ds.j);
+            } else {
+                const int valid = max(0, min(TPT, n - t * TPT));
+                Run lt, ld;
+                if (valid > 0) {
+                    load_run_smem(smt, t, lt);
+                    if (ds.job.kind == kKindResidual) load_run_smem(smt + kChunkBytes, t, ld);
+                }
+                consume_end(cons);
+                const float run = valid > 0 ? run_total_rotated(lt, ld, t, valid, ds.job.d, ds.job.kind,
+                                                                static_cast<int>(e0) + t * TPT)
+                                            : 0.0f;
+                const unsigned long long wsum = warp_sum_u64(to_fixed(run, ds.job.d.fix));
+                if (lane == 0) {
+                    ws_sum[(static_cast<size_t>(ds.job.b) * L.NCH + ds.j) * kConsumerWarps + warp] = wsum;
+                    const int fs = static_cast<int>(iseq % kFlushSlots);
+                    __threadfence_block();
+                    if (atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1) {
+                        __threadfence_block();
+                        ctl.wcnt[fs] = 0;
+                        if (!post(ds.k | kJobMsg, 1u)) set_abort(a.d_status);
+                    }
+                }
+            }
+        }
+    }
+
+    // Finisher, one lane: the request ends at n (-1: invalid); positions after
+    // n are -1, and the checking outputs of the rows not read are NaN / -1.
+    __device__ void ee_close(int b, int n, int from_row) const {
+        const int GM = a.gamma;
+        int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
+        const sv_debug_out& dbg = a.dbg;
+        for (int j = n < 0 ? 0 : n + 1; j <= GM; ++j) out[j] = -1;
+        a.out_num_accepted[b] = n;
+        for (int j = from_row; j <= GM; ++j) {
+            const size_t r = static_cast<size_t>(b) * (GM + 1) + j;
+            if (dbg.max_target) dbg.max_target[r] = nanf("");
+            if (dbg.lse_target) dbg.lse_target[r] = nan("");
+            if (dbg.argmax_target) dbg.argmax_target[r] = -1;
+        }
+        for (int j = from_row; j < GM; ++j) {
+            const size_t r = static_cast<size_t>(b) * GM + j;
+            if (dbg.max_draft) dbg.max_draft[r] = nanf("");
+            if (dbg.lse_draft) dbg.lse_draft[r] = nan("");
+            if (dbg.p_x) dbg.p_x[r] = nan("");
+            if (dbg.q_x) dbg.q_x[r] = nan("");
+        }
+    }
+
+    // Finisher warp: the decision at position pos of request b, from the chunk
+    // records of statistics task p.
+    __device__ void ee_decide(int p, int b, int pos) const {
+        const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V, NCH = L.NCH;
+        const float T = a.temperature[b];
+        const bool t_ok = (T >= 0.0f) && (T < pos_inf());
+        const bool greedy = t_ok && T == 0.0f;
+        const bool samp = sampled(T);
+        const float c = samp ? temp_scale(T) : 0.0f;
+        const int kb = ee_kb(b);
+        const bool range_ok = t_ok && kb >= 0 && kb <= GM;
+        const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
+        const bool proposal = range_ok && pos < kb;
+        const bool has_draft = samp && !a.onehot && proposal;
+        // this position's gathered logits and uniform, loaded before the merge
+        int x = -1;
+        float lt = 0.0f, ld = 0.0f, u = 0.0f;
+        if (lane == 0 && proposal) {
+            x = tok[pos];
+            if (samp && x >= 0 && x < V) {
+                const size_t tr = static_cast<size_t>(b) * (GM + 1) + pos, dr = static_cast<size_t>(b) * GM + pos;
+                lt = load_logit<DT>(a.target, tr * V + x);
+                if (!a.onehot) ld = load_logit<DT>(a.draft, dr * V + x);
+                u = a.u_accept[dr];
+            }
+        }
+        // request-wide checks at position 0: T, the proposal count, every proposed token
+        int bad = range_ok ? 0 : 1;
+        if (pos == 0 && range_ok)
+            for (int q = lane; q < kb; q += 32) {
+                const int y = tok[q];
+                if (y < 0 || y >= V) bad = 1;
+            }
+        // the chunk records of the position's rows, merged in chunk order per lane
+        // and then across lanes; lane 0's result is used
+        const bool argmax = !samp;
+        Rec rt{neg_inf(), 0.0f, 0x7fffffff, 0}, rd{neg_inf(), 0.0f, -1, 0};
+        bool first = true;
+        for (int jj = lane; jj < NCH; jj += 32) {
+            const uint4* src = reinterpret_cast<const uint4*>(ee_rec() + (static_cast<size_t>(p) * NCH + jj) * 2);
+            const uint4 vt = __ldcg(src), vd = __ldcg(src + 1);
+            const Rec xt{__uint_as_float(vt.x), __uint_as_float(vt.y), static_cast<int32_t>(vt.z), static_cast<int32_t>(vt.w)};
+            const Rec xd{__uint_as_float(vd.x), __uint_as_float(vd.y), static_cast<int32_t>(vd.z), static_cast<int32_t>(vd.w)};
+            if (first) {
+                rt = xt;
+                rd = xd;
+                first = false;
+            } else {
+                rt = rec_merge(rt, xt, argmax, c);
+                if (has_draft) rd = rec_merge(rd, xd, false, c);
+            }
+        }
+        const bool have = !first;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            Rec ot{__shfl_down_sync(0xffffffffu, rt.m, o), __shfl_down_sync(0xffffffffu, rt.s, o),
+                   __shfl_down_sync(0xffffffffu, rt.idx, o), __shfl_down_sync(0xffffffffu, rt.bad, o)};
+            Rec od{__shfl_down_sync(0xffffffffu, rd.m, o), __shfl_down_sync(0xffffffffu, rd.s, o),
+                   __shfl_down_sync(0xffffffffu, rd.idx, o), __shfl_down_sync(0xffffffffu, rd.bad, o)};
+            const bool oh = __shfl_down_sync(0xffffffffu, have ? 1 : 0, o) != 0;
+            if ((lane & (2 * o - 1)) == 0 && lane + o < 32 && oh) {
+                rt = rec_merge(rt, ot, argmax, c);
+                if (has_draft) rd = rec_merge(rd, od, false, c);
+            }
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (lane != 0) return;
+        const bool row_bad = rt.bad || rt.m == neg_inf() || (has_draft && (rd.bad || rd.m == neg_inf()));
+        int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
+        const sv_debug_out& dbg = a.dbg;
+        if (bad || row_bad) {
+            ee_close(b, -1, 0);
+            for (int j = 0; j <= GM; ++j) out[j] = -1;
+            if (a.d_status) atomicOr(a.d_status, SV_STATUS_BAD_REQUEST);
+            if (dbg.kind) dbg.kind[b] = kKindInvalid;
+            if (dbg.w_total) dbg.w_total[b] = nan("");
+            ee_finish_request();
+            return;
+        }
+        {  // this position's checking outputs
+            const size_t r = static_cast<size_t>(b) * (GM + 1) + pos;
+            if (dbg.max_target) dbg.max_target[r] = rt.m;
+            if (dbg.lse_target) dbg.lse_target[r] = greedy ? nan("") : lse_from_stats(rt.m, rt.s, c, T);
+            if (dbg.argmax_target) dbg.argmax_target[r] = greedy ? (rt.idx == 0x7fffffff ? 0 : rt.idx) : -1;
+            if (pos < GM) {
+                const size_t q = static_cast<size_t>(b) * GM + pos;
+                if (dbg.max_draft) dbg.max_draft[q] = has_draft ? rd.m : nanf("");
+                if (dbg.lse_draft) dbg.lse_draft[q] = has_draft ? lse_from_stats(rd.m, rd.s, c, T) : nan("");
+                if (dbg.p_x) dbg.p_x[q] = (samp && proposal) ? prob_from_stats(lt, rt.m, rt.s, c) : nan("");
+                if (dbg.q_x)
+                    dbg.q_x[q] = (samp && proposal) ? (a.onehot ? 1.0 : prob_from_stats(ld, rd.m, rd.s, c)) : nan("");
+            }
+        }
+        if (greedy) {
+            const int am = rt.idx == 0x7fffffff ? 0 : rt.idx;
+            if (proposal && tok[pos] == am) {
+                out[pos] = am;
+                ee_publish(kTaskStats, b, pos + 1);
+                return;
+            }
+            out[pos] = am;
+            ee_close(b, pos, pos + 1);
+            if (dbg.kind) dbg.kind[b] = kKindGreedy;
+            if (dbg.w_total) dbg.w_total[b] = nan("");
+            ee_finish_request();
+            return;
+        }
+        if (proposal) {
+            const bool acc = a.onehot ? accept_from_logits(lt, 0.0f, rt.m, rt.s, 0.0f, 1.0f, c, u)
+                                      : accept_from_logits(lt, ld, rt.m, rt.s, rd.m, rd.s, c, u);
+            if (acc) {
+                out[pos] = x;
+                ee_publish(kTaskStats, b, pos + 1);
+                return;
+            }
+        }
+        // the draw: the residual at a rejection, or the extra token from row kb
+        Job j;
+        j.b = b;
+        j.n = pos;
+        j.pad = __float_as_int(a.u_sample[b]);
+        DrawParams& d = j.d;
+        d.c = c;
+        d.mcp = scaled_max(rt.m, c);
+        d.isp = __frcp_rn(rt.s);
+        d.excl = -1;
+        if (proposal && !a.onehot) {
+            d.kind = kKindResidual;
+            d.mcq = scaled_max(rd.m, c);
+            d.isq = __frcp_rn(rd.s);
+            d.fix = kFixResidual;
+        } else {
+            d.kind = proposal ? kKindResidualOnehot : kKindBonus;
+            d.excl = proposal ? x : -1;
+            d.mcq = 0.0f;
+            d.isq = 0.0f;
+            d.fix = kFixTarget;
+        }
+        j.kind = d.kind;
+        jobs()[b] = j;
+        out[pos] = -1;  // the search fills it in
+        ee_close(b, pos, pos + 1);
+        if (dbg.kind) dbg.kind[b] = d.kind == kKindResidualOnehot ? kKindResidual : d.kind;
+        ee_publish(kTaskDraw, b, pos);
+    }
+
+    // Finisher warp: the next owned task (positions B + g, B + g + G, ... and
+    // g itself), decided or searched once all its chunks are counted. Lane 0
+    // keeps own_p and the task's code (own_v, 0 until it is published).
+    __device__ bool ee_poll_owned(int& own_p, int& own_v) const {
+        int act_p = -1, act_v = 0;
+        if ((threadIdx.x & 31) == 0 && own_p < L.ee_cap) {
+            if (own_v == 0) {
+                if (own_p < a.B) {
+                    own_v = ee_encode(kTaskStats, own_p, 0);
+                } else {
+                    const int v = reinterpret_cast<const volatile int*>(ee_tasks())[own_p];
+                    if (v) {
+                        __threadfence();
+                        own_v = v;
+                    }
+                }
+            }
+            if (own_v != 0 &&
+                reinterpret_cast<const volatile unsigned*>(ee_done())[own_p] >= static_cast<unsigned>(L.NCH)) {
+                __threadfence();  // the other blocks' chunk records and sums
+                act_p = own_p;
+                act_v = own_v;
+                own_v = 0;
+                own_p += G;
+            }
+        }
+        act_p = __shfl_sync(0xffffffffu, act_p, 0);
+        act_v = __shfl_sync(0xffffffffu, act_v, 0);
+        if (act_p < 0) return false;
+        const int v = act_v - 1, type = v >> 28, b = (v >> 8) & 0xfffff, pos = v & 0xff;
+        if (type == kTaskStats) {
+            ee_decide(act_p, b, pos);
+        } else {
+            search_job(b);
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ee_finish_request();
+        }
+        __syncwarp();
+        return true;
+    }
 };
 
 template <int DT>
@@ -1411,6 +1941,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         const unsigned V = static_cast<unsigned>(a.V), GM = static_cast<unsigned>(a.gamma);
         unsigned* req_done = K.req_done();
         unsigned* job_done = K.job_done();
+        int own_p = blockIdx.x, own_k = -1;  // lane 0: next owned job position, its job
         K.finish(
             [&](int item, unsigned share) {
                 if (item & kJobMsg) {
@@ -1430,7 +1961,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                     K.verify_request(item, fin_rows);
                     stamp(ph, 3, lane == 0);
                 }
-            });
+            },
+            [&]() { return K.poll_owned(own_p, own_k); }, [&]() { return own_p >= ctl.n_samp; });
         stamp(ph, 9, lane == 0);
         return;
     }
@@ -1633,6 +2165,58 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     stamp(ph, 6, lane == 0);
 }
 
+// Early-exit verification: the same producer / consumer / finisher warps,
+// with tasks (one position's row statistics, or one draw) taken in
+// publication order instead of a static row schedule and a draw phase.
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) early_kernel(Args a, Layout L, char* ws) {
+    extern __shared__ __align__(128) char smem[];
+    char* stages = smem;
+    Ctl& ctl = *reinterpret_cast<Ctl*>(smem + static_cast<size_t>(kStages) * kStageBytes);
+    using KT = Kern<DT>;
+    KT K{a, L, ws, ctl, stages, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x)};
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    unsigned long long* ph = reinterpret_cast<unsigned long long*>(a.dbg.phase_ns);
+    stamp(ph, 0, t == 0);
+    if (t == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl.full[s], 1);
+            mbar_init(&ctl.empty[s], kConsumerWarps);
+        }
+        ctl.abort = 0;
+        ctl.n_samp = 0;
+        ctl.fq_tail = 0;
+        ctl.fq_head = 0;
+        ctl.cons_done = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    for (int i = t; i < kFlushSlots; i += kThreads) ctl.wcnt[i] = 0;
+    for (int i = t; i < kQueue; i += kThreads) ctl.fq_seq[i] = 0;
+    __syncthreads();
+
+    typename KT::Cursor prod, cons;
+    if (warp == kFinisherWarp) {
+        int own_p = blockIdx.x, own_v = 0;  // lane 0: next owned task, its code once published
+        unsigned* done = K.ee_done();
+        K.finish([&](int item, unsigned v) {
+                     red_release_add(done + (item & ~kJobMsg), v);  // the task's owner polls the count
+                     return false;
+                 },
+                 [&](int) {}, [&]() { return K.ee_poll_owned(own_p, own_v); },
+                 [&]() { return own_p >= L.ee_cap || (own_v == 0 && K.ee_no_task(own_p)); });
+        stamp(ph, 9, lane == 0);
+        return;
+    }
+    if (warp == kProducerWarp) {
+        K.ee_produce(prod);
+        if (ctl.abort) K.drain(prod);
+        return;
+    }
+    K.ee_consume(cons);
+    K.consumer_done();
+    stamp(ph, 6, lane == 0);
+}
+
 size_t smem_bytes() {
     return static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl) + sizeof(Rec) * kMaxRowsPerReq;
 }
@@ -1663,14 +2247,22 @@ cudaError_t launch_streaming(const Args& a, const DeviceInfo& dev, int grid, voi
     const Layout L = make_layout(a.B, a.gamma, a.V, es, grid);
     if (workspace_bytes < L.total) return cudaErrorInvalidValue;
     const size_t smem = smem_bytes();
-    const void* fn = a.dtype == SV_F32 ? reinterpret_cast<const void*>(&stream_kernel<SV_F32>)
-                                       : reinterpret_cast<const void*>(&stream_kernel<SV_BF16>);
+    const void* fn = a.early ? (a.dtype == SV_F32 ? reinterpret_cast<const void*>(&early_kernel<SV_F32>)
+                                                   : reinterpret_cast<const void*>(&early_kernel<SV_BF16>))
+                             : (a.dtype == SV_F32 ? reinterpret_cast<const void*>(&stream_kernel<SV_F32>)
+                                                  : reinterpret_cast<const void*>(&stream_kernel<SV_BF16>));
     static thread_local int attr_device = -1;
     if (attr_device != dev.device) {
         cudaError_t e = cudaFuncSetAttribute(&stream_kernel<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(&stream_kernel<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(&early_kernel<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(&early_kernel<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         int per_sm = 0;

@@ -134,9 +134,13 @@ def compare(batch, gpu, ora, det, margin=MARGIN, rel_tol=REL_TOL, onehot=False) 
             if fin.any():
                 rep.max_lse_err = max(rep.max_lse_err, float(np.abs(lt_g[fin] - lt_o[fin]).max()))
             if not onehot:
-                dd = np.abs(gpu["lse_draft"][rows] - det["lse_draft"][rows])
-                rep.max_lse_err = max(rep.max_lse_err, float(dd.max()))
-                assert np.array_equal(gpu["max_draft"][rows].astype(np.float64), det["max_draft"][rows])
+                ld_g, ld_o = gpu["lse_draft"][rows], det["lse_draft"][rows]
+                assert np.array_equal(np.isnan(ld_g), np.isnan(ld_o)), "draft rows read differ"
+                fin_d = ~np.isnan(ld_o)
+                if fin_d.any():
+                    rep.max_lse_err = max(rep.max_lse_err, float(np.abs(ld_g[fin_d] - ld_o[fin_d]).max()))
+                assert np.array_equal(gpu["max_draft"][rows].astype(np.float64), det["max_draft"][rows],
+                                      equal_nan=True)
             else:
                 assert np.all(np.isnan(gpu["lse_draft"][rows])) and np.all(np.isnan(gpu["max_draft"][rows]))
             assert rep.max_lse_err <= 1e-5, f"log-normaliser error {rep.max_lse_err}"
@@ -155,9 +159,13 @@ def compare(batch, gpu, ora, det, margin=MARGIN, rel_tol=REL_TOL, onehot=False) 
             assert rep.max_px_rel <= rel_tol, f"gathered probability error {rep.max_px_rel}"
         same = samp & valid & (gn == on) & ~np.isnan(det["w_total"])
         if same.any():
-            err = np.abs(gpu["w_total"][same] - det["w_total"][same]) / det["w_total"][same]
-            rep.max_w_rel = float(err.max())
-            assert rep.max_w_rel <= rel_tol, f"draw total error {rep.max_w_rel}"
+            # W = sum max(p - q, 0): each binary32 p(x), q(x) carries up to 2^-22
+            # relative error, so |dW| <= 2^-21 absolute on top of the relative
+            # tolerance (W is a small difference of near-equal terms when p ~ q)
+            W = det["w_total"][same]
+            dW = np.abs(gpu["w_total"][same] - W)
+            rep.max_w_rel = float((dW / W).max())
+            assert np.all(dW <= rel_tol * W + 2.0 ** -21), f"draw total error {rep.max_w_rel} (W min {W.min():.3g})"
     return rep
 
 
