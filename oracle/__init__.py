@@ -75,6 +75,11 @@ def _bind(lib):
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_Detail)]
+    lib.oracle_spec_verify_tree.restype = ctypes.c_int
+    lib.oracle_spec_verify_tree.argtypes = [
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_Detail)]
     lib.oracle_version.restype = ctypes.c_int
     return lib
 
@@ -233,3 +238,34 @@ def verify_early(target, draft, tokens, u_accept, u_sample, temperature, num_dra
     if rc != 0:
         raise ValueError("oracle_spec_verify_early rejected its arguments")
     return out_tokens, num_acc, det
+
+
+def verify_tree(target, tokens, parents, num_nodes, u_accept, u_sample, temperature, detail=False, lib=None):
+    """The tree-verification oracle. ``target`` [B, G+1, V] (row j for node j),
+    ``tokens``/``parents``/``u_accept`` [B, G] indexed by node - 1,
+    ``num_nodes`` [B]. Returns ``(out_tokens, num_accepted, out_nodes, det)``."""
+    lib = lib or load()
+    target = np.ascontiguousarray(target)
+    B, G1, V = target.shape
+    G = G1 - 1
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32).reshape(B, G)
+    parents = np.ascontiguousarray(parents, dtype=np.int32).reshape(B, G)
+    num_nodes = np.ascontiguousarray(num_nodes, dtype=np.int32).reshape(B)
+    u_accept = np.ascontiguousarray(u_accept, dtype=np.float32).reshape(B, G)
+    u_sample = np.ascontiguousarray(u_sample, dtype=np.float32).reshape(B)
+    temperature = np.ascontiguousarray(temperature, dtype=np.float32).reshape(B)
+    out_tokens = np.full((B, G1), -7, dtype=np.int32)
+    num_acc = np.full((B,), -7, dtype=np.int32)
+    out_nodes = np.full((B, G), -7, dtype=np.int32)
+    det = None
+    dptr = None
+    if detail:
+        det = _detail_arrays(B, G)
+        d = _Detail(**{k: _ptr(v) for k, v in det.items()})
+        dptr = ctypes.byref(d)
+    rc = lib.oracle_spec_verify_tree(
+        _ptr(target), dtype_code(target), B, G, V, _ptr(tokens), _ptr(parents), _ptr(num_nodes),
+        _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens), _ptr(num_acc), _ptr(out_nodes), dptr)
+    if rc != 0:
+        raise ValueError("oracle_spec_verify_tree rejected its arguments")
+    return out_tokens, num_acc, out_nodes, det

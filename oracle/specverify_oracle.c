@@ -620,3 +620,154 @@ int oracle_spec_verify_early(const void* target, const void* draft, int dtype, i
     return 0;
 }
 
+/* ------------------------------------------------------------------------
+ * Tree verification ("Speculative Decoding : accélérer l'inférence des LLM",
+ * §Medusa : plusieurs têtes de prédiction and §EAGLE: candidate continuations
+ * arranged in a tree and verified in one target pass). The pages do not state
+ * the rule for several candidates; this is the plainest lossless reading, the
+ * rule of §Pourquoi la qualité est préservée applied candidate after candidate
+ * with deterministic (one-hot) proposals:
+ *  - node 0 is the root; node j in 1..m has token x_j and parent parents[j-1]
+ *    in [0, j-1]; target row j holds the logits for the token after node j;
+ *  - at node u, p = softmax(row u / T); u's children are tried in index
+ *    order; child c is accepted with probability min(1, p'(x_c)), p' being p
+ *    without the tokens of u's children rejected so far, renormalised; an
+ *    accepted child becomes u and its token is emitted;
+ *  - when every child is rejected (or u is a leaf) the last token is drawn
+ *    from p' by inverse CDF with u_sample;
+ *  - T == 0: the first child whose token is the argmax of row u is accepted;
+ *    with none, the argmax is emitted and the walk ends.
+ * A chain (parents[j-1] = j-1) is oracle_spec_verify_onehot. Every row 0..m is
+ * read (a bad one invalidates the request), as are the parents and tokens. */
+
+static int verify_tree_walk(const scratch_t* s, int b, double T, const int32_t* tok, const int32_t* par, int m,
+                            const float* ua, float us, int32_t* out, int32_t* nodes, const oracle_detail* d) {
+    const int G = s->gamma, V = s->V;
+    int u = 0, n = 0;
+    int excl[64];
+    for (;;) {
+        load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)u, V, s->lt);
+        int ne = 0;
+        if (T == 0.0) {
+            const int a = row_argmax(s->lt, V);
+            int next = -1;
+            for (int c = 1; c <= m && next < 0; ++c)
+                if (par[c - 1] == u && tok[c - 1] == a) next = c;
+            if (next < 0) {
+                out[n] = a;
+                return n;
+            }
+            out[n] = a;
+            nodes[n] = next;
+            ++n;
+            u = next;
+            continue;
+        }
+        softmax_T(s->lt, V, T, s->p);
+        double R = 0.0; /* probability of the children rejected so far */
+        int next = -1;
+        for (int c = 1; c <= m && next < 0; ++c) {
+            if (par[c - 1] != u) continue;
+            const int x = tok[c - 1];
+            int seen = 0;
+            for (int e = 0; e < ne; ++e)
+                if (excl[e] == x) seen = 1;
+            const double px = seen ? 0.0 : s->p[x];
+            const double rest = 1.0 - R;
+            const double alpha = rest > 0.0 ? fmin(1.0, px / rest) : 0.0;
+            const double uc = (double)ua[c - 1];
+            set_d(d->p_x, (size_t)b * (size_t)G + (size_t)(c - 1), px);
+            set_d(d->q_x, (size_t)b * (size_t)G + (size_t)(c - 1), 1.0);
+            set_d(d->alpha, (size_t)b * (size_t)G + (size_t)(c - 1), alpha);
+            set_d(d->accept_margin, (size_t)b * (size_t)G + (size_t)(c - 1),
+                  alpha > 0.0 ? fabs(uc - alpha) / alpha : INFINITY);
+            if (uc < alpha) {
+                next = c;
+            } else if (!seen) {
+                excl[ne++] = x;
+                R += px;
+            }
+        }
+        if (next >= 0) {
+            out[n] = tok[next - 1];
+            nodes[n] = next;
+            ++n;
+            u = next;
+            continue;
+        }
+        /* the last token: p without the rejected children's tokens */
+        double W = 0.0;
+        for (int y = 0; y < V; ++y) {
+            int ex = 0;
+            for (int e = 0; e < ne; ++e)
+                if (excl[e] == y) ex = 1;
+            s->w[y] = ex ? 0.0 : s->p[y];
+            W += s->w[y];
+        }
+        if (W == 0.0) /* unreachable in exact arithmetic: fall back to p */
+            memcpy(s->w, s->p, sizeof(double) * (size_t)V);
+        double margin = 0.0;
+        out[n] = draw_inverse_cdf(s->w, V, (double)us, &W, &margin);
+        set_i(d->kind, (size_t)b, ne > 0 ? ORACLE_KIND_RESIDUAL : ORACLE_KIND_BONUS);
+        set_d(d->w_total, (size_t)b, W);
+        set_d(d->sample_margin, (size_t)b, margin);
+        return n;
+    }
+}
+
+int oracle_spec_verify_tree(const void* target, int dtype, int B, int gamma, int V, const int32_t* tokens,
+                            const int32_t* parents, const int32_t* num_nodes, const float* u_accept,
+                            const float* u_sample, const float* temperature, int32_t* out_tokens,
+                            int32_t* out_num_accepted, int32_t* out_nodes, const oracle_detail* detail) {
+    if (B < 0 || gamma < 1 || gamma > 64 || V < 1) return -1;
+    if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+    if (B == 0) return 0;
+    if (!target || !tokens || !parents || !num_nodes || !u_accept || !u_sample || !temperature || !out_tokens ||
+        !out_num_accepted || !out_nodes)
+        return -1;
+    oracle_detail none;
+    memset(&none, 0, sizeof none);
+    const oracle_detail* d = detail ? detail : &none;
+    scratch_t s;
+    memset(&s, 0, sizeof s);
+    s.target = target;
+    s.dtype = dtype;
+    s.gamma = gamma;
+    s.V = V;
+    s.lt = (double*)malloc(sizeof(double) * (size_t)V);
+    s.p = (double*)malloc(sizeof(double) * (size_t)V);
+    s.w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!s.lt || !s.p || !s.w) {
+        free(s.lt), free(s.p), free(s.w);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
+        const int32_t* par = parents + (size_t)b * (size_t)gamma;
+        int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
+        int32_t* nodes = out_nodes + (size_t)b * (size_t)gamma;
+        const double T = (double)temperature[b];
+        const int m = num_nodes[b];
+        for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
+        for (int j = 0; j < gamma; ++j) nodes[j] = -1;
+        clear_detail(d, b, gamma);
+        int ok = !(isnan(T) || isinf(T) || T < 0.0) && m >= 0 && m <= gamma;
+        for (int j = 1; ok && j <= m; ++j)
+            if (par[j - 1] < 0 || par[j - 1] >= j || tok[j - 1] < 0 || tok[j - 1] >= V) ok = 0;
+        for (int j = 0; ok && j <= m; ++j) {
+            load_row(s.target, s.dtype, (size_t)b * (size_t)(gamma + 1) + (size_t)j, V, s.lt);
+            if (!row_usable(s.lt, V)) ok = 0;
+        }
+        if (!ok) {
+            out_num_accepted[b] = -1;
+            continue;
+        }
+        if (detail) report_rows_onehot(&s, b, T, m, d);
+        if (T == 0.0) set_i(d->kind, (size_t)b, ORACLE_KIND_GREEDY);
+        out_num_accepted[b] = verify_tree_walk(&s, b, T, tok, par, m, u_accept + (size_t)b * (size_t)gamma,
+                                               u_sample[b], out, nodes, d);
+    }
+    free(s.lt), free(s.p), free(s.w);
+    return 0;
+}
+

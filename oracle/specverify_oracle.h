@@ -122,6 +122,19 @@ int oracle_spec_verify_early(const void* target, const void* draft, int dtype, i
                              const float* u_sample, const float* temperature, int32_t* out_tokens,
                              int32_t* out_num_accepted, const oracle_detail* detail);
 
+/* Tree verification with deterministic candidates (see the comment above
+ * oracle_spec_verify_tree in the .c file for the rule). gamma = the most
+ * non-root nodes (at most 64); tokens, parents, u_accept [B, gamma] are
+ * indexed by node - 1; num_nodes [B] non-root nodes in use; target
+ * [B, gamma+1, V], row j for node j. Outputs: out_tokens [B, gamma+1] (the
+ * accepted path's tokens, then the last token, then -1), out_num_accepted [B]
+ * (path length, -1 invalid), out_nodes [B, gamma] (the accepted node indices,
+ * then -1). Detail p_x / alpha / accept_margin are indexed by node - 1. */
+int oracle_spec_verify_tree(const void* target, int dtype, int B, int gamma, int V, const int32_t* tokens,
+                            const int32_t* parents, const int32_t* num_nodes, const float* u_accept,
+                            const float* u_sample, const float* temperature, int32_t* out_tokens,
+                            int32_t* out_num_accepted, int32_t* out_nodes, const oracle_detail* detail);
+
 #ifdef __cplusplus
 }
 #endif

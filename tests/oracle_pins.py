@@ -528,6 +528,110 @@ def pin_early_reads_nothing_after_the_rejection(lib, quick=False):
     assert np.all(n3 == -1)
 
 
+# ------------------------------------------------------- tree verification
+
+GOLDEN_TREE = os.path.join(os.path.dirname(__file__), "golden", "tree_v4.json")
+
+
+def _tree(lib, target, tokens, parents, m, ua, us, T, detail=False):
+    return oracle.verify_tree(target, tokens, parents, m, ua, us, T, detail=detail, lib=lib)
+
+
+def pin_tree_hand_examples(lib, quick=False):
+    """The constructed V=4 tree cases, worked by hand (golden/tree_v4.json)."""
+    g = json.load(open(GOLDEN_TREE))
+    lt = np.log(np.array(g["target_p"])).astype(np.float32)[None]
+    for c in g["cases"]:
+        out, n, nodes, _ = _tree(lib, lt, np.array([g["tokens"]]), np.array([g["parents"]]), np.array([g["m"]]),
+                                 np.array([c["u_accept"]], np.float32), np.array([c["u_sample"]], np.float32),
+                                 np.array([c["T"]], np.float32))
+        assert out[0].tolist() == c["out"] and n[0] == c["n"] and nodes[0].tolist() == c["nodes"], c["name"]
+
+
+def pin_tree_chain_is_the_onehot_rule(lib, quick=False):
+    """A chain (every node's parent is the node before it) is the pinned
+    one-hot verifier; the accepted nodes are 1..n."""
+    rng = np.random.Generator(np.random.Philox(401))
+    B, G, V = (64 if quick else 256), 6, 20
+    lt = rng.normal(0, 1.5, (B, G + 1, V)).astype(np.float32)
+    x = np.argmax(lt[:, :G] + rng.gumbel(size=(B, G, V)).astype(np.float32), axis=2).astype(np.int32)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    T = rng.choice(np.array([0.0, 0.7, 1.0], np.float32), B)
+    m = rng.integers(0, G + 1, B).astype(np.int32)
+    par = np.tile(np.arange(G, dtype=np.int32), (B, 1))
+    o1, n1, nodes, _ = _tree(lib, lt, x, par, m, ua, us, T)
+    o2, n2, _ = oracle.verify_onehot(lt, x, m, ua, us, T, lib=lib)
+    assert np.array_equal(o1, o2) and np.array_equal(n1, n2)
+    for b in range(B):
+        assert nodes[b, :n1[b]].tolist() == list(range(1, n1[b] + 1))
+
+
+def pin_tree_output_follows_p(lib, quick=False):
+    """Three candidate children of the root: child k is accepted with
+    probability p(x_k) (closed form of trying them in order with the
+    renormalised residual), and the first token follows p (chi-square, V=8)."""
+    N = 20000 if quick else 400000
+    rng = np.random.Generator(np.random.Philox(402))
+    rows = rng.normal(0, 1.2, (4, 8)).astype(np.float32)
+    p0 = special.softmax(rows[0].astype(np.float64))
+    kids = np.argsort(p0)[[6, 3, 5]].astype(np.int32)  # distinct tokens, mixed probabilities
+    lt = np.ascontiguousarray(np.broadcast_to(rows, (N, 4, 8)))
+    tok = np.tile(kids, (N, 1))
+    par = np.zeros((N, 3), np.int32)
+    ua = rng.random((N, 3), dtype=np.float32)
+    us = rng.random(N, dtype=np.float32)
+    out, n, nodes, _ = _tree(lib, lt, tok, par, np.full(N, 3, np.int32), ua, us, np.ones(N, np.float32))
+    for k in range(3):
+        rate = (nodes[:, 0] == k + 1).mean()
+        pk = p0[kids[k]]
+        _within_5_sigma(rate, pk, np.sqrt(pk * (1 - pk)), N, f"tree P(accept child {k + 1})")
+    _chi2_ok(np.bincount(out[:, 0], minlength=8), p0, "tree first token")
+
+
+def pin_tree_greedy_follows_argmax(lib, quick=False):
+    """At T = 0 the accepted path follows, from the root, the first child
+    whose token is the row's argmax (numpy argmax over the stored values), and
+    ends with the argmax of the last node."""
+    rng = np.random.Generator(np.random.Philox(403))
+    B, G, V = 64, 12, 6
+    lt = rng.normal(0, 1.0, (B, G + 1, V)).astype(np.float32)
+    par = np.array([[rng.integers(0, j) for j in range(1, G + 1)] for _ in range(B)], np.int32)
+    tok = rng.integers(0, 3, (B, G)).astype(np.int32)  # small alphabet: argmax often matches
+    lt[:, :, :3] += 2.0
+    m = rng.integers(0, G + 1, B).astype(np.int32)
+    z = np.zeros((B, G), np.float32)
+    out, n, nodes, _ = _tree(lib, lt, tok, par, m, z, np.zeros(B, np.float32), np.zeros(B, np.float32))
+    for b in range(B):
+        u, path = 0, []
+        while True:
+            a = int(np.argmax(lt[b, u]))
+            kid = next((c for c in range(1, m[b] + 1) if par[b, c - 1] == u and tok[b, c - 1] == a), None)
+            path.append(a)
+            if kid is None:
+                break
+            u = kid
+        assert out[b, :len(path)].tolist() == path and n[b] == len(path) - 1, b
+
+
+def pin_tree_invalid(lib, quick=False):
+    """A parent that is not an earlier node, a token outside [0, V), a node
+    count outside [0, gamma] or a bad row invalidates the request alone."""
+    rng = np.random.Generator(np.random.Philox(404))
+    B, G, V = 8, 4, 10
+    lt = rng.normal(0, 1, (B, G + 1, V)).astype(np.float32)
+    par = np.tile(np.array([0, 0, 1, 2], np.int32), (B, 1))
+    tok = rng.integers(0, V, (B, G)).astype(np.int32)
+    m = np.full(B, G, np.int32)
+    par[1, 2] = 3       # not an earlier node
+    tok[2, 1] = V       # out of range
+    m[3] = G + 1        # too many nodes
+    lt[4, 3, 2] = np.nan
+    _, n, _, _ = _tree(lib, lt, tok, par, m, rng.random((B, G), dtype=np.float32), rng.random(B, dtype=np.float32),
+                       np.ones(B, np.float32))
+    assert np.all(n[1:5] == -1) and np.all(n[[0, 5, 6, 7]] >= 0)
+
+
 ALL_PINS = [
     pin_hand_examples,
     pin_accept_probability,
@@ -546,4 +650,9 @@ ALL_PINS = [
     pin_onehot_rows_past_k_unread,
     pin_early_equals_the_full_read,
     pin_early_reads_nothing_after_the_rejection,
+    pin_tree_hand_examples,
+    pin_tree_chain_is_the_onehot_rule,
+    pin_tree_output_follows_p,
+    pin_tree_greedy_follows_argmax,
+    pin_tree_invalid,
 ]

@@ -67,6 +67,14 @@ MUTANTS = [
      "    for (int i = 0; i < k + (k == 0); ++i) {\n        size_t tr"),
     ("early_onehot_residual_keeps_x", "const double qy = onehot ? (y == x ? 1.0 : 0.0) : s->q[y];",
      "const double qy = onehot ? 0.0 : s->q[y];"),
+    # tree verification
+    ("tree_alpha_not_renormalised", "const double alpha = rest > 0.0 ? fmin(1.0, px / rest) : 0.0;",
+     "const double alpha = rest > 0.0 ? fmin(1.0, px) : 0.0;"),
+    ("tree_children_of_the_root_only", "            if (par[c - 1] != u) continue;",
+     "            if (par[c - 1] != 0) continue;"),
+    ("tree_residual_keeps_rejected", "            s->w[y] = ex ? 0.0 : s->p[y];", "            s->w[y] = s->p[y];"),
+    ("tree_greedy_takes_first_child", "if (par[c - 1] == u && tok[c - 1] == a) next = c;",
+     "if (par[c - 1] == u) next = c;"),
 ]
 
 
