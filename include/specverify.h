@@ -268,6 +268,39 @@ sv_status spec_verify_onehot(const void* target_logits, sv_dtype dtype, int B, i
                              sv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Tree verification ("Speculative Decoding : accélérer l'inférence des LLM",
+ * §Medusa : plusieurs têtes de prédiction and §EAGLE: candidate continuations
+ * arranged in a tree, verified in one target pass). The pages do not state the
+ * rule for several candidates; this library applies the acceptance rule of
+ * §Pourquoi la qualité est préservée candidate after candidate, with
+ * deterministic candidates (q one-hot), which keeps the target distribution:
+ *  - node 0 is the root; node j in 1..num_nodes[b] has token
+ *    node_tokens[b, j-1] and parent parents[b, j-1] in [0, j-1]; target row j
+ *    ([B, gamma+1, V], row-major) holds the logits for the token after node j
+ *    (row 0: after the context);
+ *  - at node u the children are tried in index order; child c is accepted iff
+ *    u_accept[b, c-1] < min(1, p'(x_c)), p' = softmax(row u / T) without the
+ *    tokens of the children rejected so far, renormalised; it becomes u;
+ *  - when every child is rejected, or u is a leaf, the last token is drawn from
+ *    p' with u_sample[b] by inverse CDF;
+ *  - T == 0: the first child whose token is the argmax of row u is taken;
+ *    with none, the argmax ends the walk.
+ * A chain (parents[b, j-1] = j-1) gives spec_verify_onehot.
+ *   out_tokens [B, gamma+1]: the accepted path's tokens, the last token, -1
+ *   out_num_accepted [B]: path length (-1: invalid request)
+ *   out_nodes [B, gamma] or NULL: the accepted node indices, then -1
+ *   dbg, d_status: as spec_verify_ex (p_x, q_x indexed by node - 1), may be NULL
+ * Invalid requests (-1, SV_STATUS_BAD_REQUEST): T NaN, negative or infinite;
+ * num_nodes[b] outside [0, gamma]; a parent not an earlier node; a token
+ * outside [0, V); a bad row among 0..num_nodes[b]. Rows past num_nodes[b] are
+ * not read. This version runs one thread block per request (no workspace). */
+sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype, int B, int gamma, int V,
+                           const int32_t* node_tokens, const int32_t* parents, const int32_t* num_nodes,
+                           const float* u_accept, const float* u_sample, const float* temperature,
+                           int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_nodes, sv_stream_t stream,
+                           const sv_debug_out* dbg, int32_t* d_status);
+
+/* ---------------------------------------------------------------------------
  * Post-verify bookkeeping ("Accélérer Sonar grâce à la spéculation",
  * §Planification MTP pour un jeton unique: a kernel inserts the next target
  * tokens into their slots, so the accepted length needs no CPU

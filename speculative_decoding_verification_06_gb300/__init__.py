@@ -32,7 +32,7 @@ EXPORTED = (
     "spec_verify_workspace_size", "spec_verify", "spec_verify_ex",
     "spec_verify_host_staging_size", "spec_verify_host", "spec_verify_last_launch_count",
     "spec_verify_status_string", "spec_verify_version", "spec_verify_noalloc",
-    "spec_commit", "spec_ngram_propose", "spec_verify_onehot",
+    "spec_commit", "spec_ngram_propose", "spec_verify_onehot", "spec_verify_tree",
 )
 
 
@@ -71,9 +71,11 @@ def _declare(lib):
     lib.spec_commit.argtypes = [vp, vp, int_, int_, vp, int_, vp, vp, vp, vp]
     lib.spec_ngram_propose.argtypes = [vp, int_, int_, vp, int_, int_, int_, vp, vp, vp, vp]
     lib.spec_verify_onehot.argtypes = [vp, i32, int_, int_, int_, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.spec_verify_tree.argtypes = [vp, i32, int_, int_, int_, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                     ctypes.POINTER(_Debug), vp]
     for name in ("spec_verify_workspace_size", "spec_verify_host_staging_size", "spec_verify",
                  "spec_verify_ex", "spec_verify_host", "spec_verify_noalloc", "spec_commit",
-                 "spec_ngram_propose", "spec_verify_onehot"):
+                 "spec_ngram_propose", "spec_verify_onehot", "spec_verify_tree"):
         getattr(lib, name).restype = i32
     lib.spec_verify_status_string.argtypes = [i32]
     lib.spec_verify_status_string.restype = ctypes.c_char_p
@@ -325,3 +327,50 @@ def spec_verify_onehot(target_logits, draft_tokens, num_draft, u_accept, u_sampl
                                 workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(rc, "spec_verify_onehot")
     return Outputs(out_tokens, out_num_accepted, None, None)
+
+
+def spec_verify_tree(target_logits, node_tokens, parents, num_nodes, u_accept, u_sample, temperature,
+                     out_tokens=None, out_num_accepted=None, out_nodes=None, debug=False, status=None,
+                     stream=None):
+    """``spec_verify_tree``: verification of a candidate tree per request (see
+    include/specverify.h). ``target_logits`` [B, G+1, V], ``node_tokens`` /
+    ``parents`` / ``u_accept`` [B, G] indexed by node - 1, ``num_nodes`` [B];
+    CUDA tensors. Returns ``(Outputs, out_nodes)``."""
+    import torch
+    lib = load()
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dt = _dtype_code(target_logits)
+    dev = target_logits.device
+    for t in (target_logits, node_tokens, parents, num_nodes, u_accept, u_sample, temperature):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("every input must be a contiguous CUDA tensor")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_nodes is None:
+        out_nodes = torch.empty((B, G), dtype=torch.int32, device=dev)
+    d = _Debug()
+    dbg = None
+    if debug:
+        f64, f32, i32 = torch.float64, torch.float32, torch.int32
+        dbg = {
+            "max_target": torch.empty((B, G1), dtype=f32, device=dev),
+            "lse_target": torch.empty((B, G1), dtype=f64, device=dev),
+            "argmax_target": torch.empty((B, G1), dtype=i32, device=dev),
+            "max_draft": torch.empty((B, G), dtype=f32, device=dev),
+            "lse_draft": torch.empty((B, G), dtype=f64, device=dev),
+            "p_x": torch.empty((B, G), dtype=f64, device=dev),
+            "q_x": torch.empty((B, G), dtype=f64, device=dev),
+            "w_total": torch.empty((B,), dtype=f64, device=dev),
+            "kind": torch.empty((B,), dtype=i32, device=dev),
+        }
+        for k, v in dbg.items():
+            setattr(d, k, v.data_ptr())
+    rc = lib.spec_verify_tree(_ptr(target_logits), dt, B, G, V, _ptr(node_tokens), _ptr(parents), _ptr(num_nodes),
+                              _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
+                              _ptr(out_num_accepted), _ptr(out_nodes), _stream_handle(stream), ctypes.byref(d),
+                              _ptr(status))
+    _check(rc, "spec_verify_tree")
+    return Outputs(out_tokens, out_num_accepted, dbg, status), out_nodes

@@ -168,6 +168,46 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     return SV_OK;
 }
 
+sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype, int B, int gamma, int V,
+                           const int32_t* node_tokens, const int32_t* parents, const int32_t* num_nodes,
+                           const float* u_accept, const float* u_sample, const float* temperature,
+                           int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_nodes, sv_stream_t stream,
+                           const sv_debug_out* dbg, int32_t* d_status) {
+    g_last_launches = 0;
+    if (!shape_ok(B, gamma, V, dtype)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !node_tokens || !parents || !num_nodes || !u_accept || !u_sample || !temperature ||
+        !out_tokens || !out_num_accepted)
+        return SV_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if (!current_device(&dev)) return SV_ERR_UNSUPPORTED;
+    if (dev.cc_major != 10 || dev.cc_minor != 3) return SV_ERR_UNSUPPORTED;
+    Args a = {};
+    a.target = target_logits;
+    a.dtype = dtype;
+    a.B = B;
+    a.gamma = gamma;
+    a.V = V;
+    a.tokens = node_tokens;
+    a.u_accept = u_accept;
+    a.u_sample = u_sample;
+    a.temperature = temperature;
+    a.out_tokens = out_tokens;
+    a.out_num_accepted = out_num_accepted;
+    if (dbg) a.dbg = *dbg;
+    a.d_status = d_status;
+    a.peer_wait_ns = 2000000000ull;
+    a.onehot = true;  // candidates are tokens, not draws from a draft distribution
+    a.num_draft = num_nodes;
+    a.tree = true;
+    a.parents = parents;
+    a.out_nodes = out_nodes;
+    const cudaError_t err = launch_rowwise(a, dev, reinterpret_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return SV_ERR_CUDA;
+    g_last_launches = 1;
+    return SV_OK;
+}
+
 sv_status spec_verify_onehot(const void* target_logits, sv_dtype dtype, int B, int gamma, int V,
                              const int32_t* draft_tokens, const int32_t* num_draft, const float* u_accept,
                              const float* u_sample, const float* temperature, int32_t* out_tokens,

@@ -207,6 +207,16 @@ __device__ __forceinline__ float weight_target_excl(float lt, int e, const DrawP
     return (kind == kKindResidualOnehot && e == d.excl) ? 0.0f : weight_target(lt, d);
 }
 
+// Tree verification: the last token is drawn from p without the tokens of the
+// rejected children (at most SV_MAX_GAMMA of them).
+constexpr int kKindResidualTree = 4;  // internal, reported as kKindResidual
+
+__device__ __forceinline__ bool in_set(int e, const int* set, int n) {
+    for (int i = 0; i < n; ++i)
+        if (set[i] == e) return true;
+    return false;
+}
+
 // floor(u * total) exactly, for u in [0, 1): u = M 2^e with an integer M < 2^24,
 // so the product is a 128-bit integer shifted right by -e.
 __device__ __forceinline__ unsigned long long scale_uniform(float u, unsigned long long total) {

@@ -16,6 +16,9 @@ struct Args {
     const void* draft;   // [B, gamma, V]; null in one-hot mode
     bool onehot;               // deterministic proposals: q_i one-hot at x_i, no draft logits
     bool early;                // early exit: nothing after a request's first rejection is read
+    bool tree;                 // tree verification (one-hot candidates; num_draft = nodes in use)
+    const int32_t* parents;    // tree: [B, gamma] parent of node j at j - 1
+    int32_t* out_nodes;        // tree: [B, gamma] accepted node indices, may be null
     const int32_t* num_draft;  // one-hot mode: proposals per request [B] (null: gamma each)
     int dtype;           // SV_F32 / SV_BF16
     int B, gamma, V;

@@ -39,6 +39,9 @@ struct Shared {
     int request_bad;
     int last_row;  // early exit: the last position whose rows were read
     int stop;
+    int excl[SV_MAX_GAMMA];  // tree: tokens of the rejected children at the last node
+    int nexcl;
+    int draw_row;            // the row of the draw (tree: the last node)
 };
 
 template <int DT>
@@ -118,17 +121,22 @@ __device__ RowStat row_argmax(const void* base, size_t row, int V, Shared& sh) {
 }
 
 // Sum of the draw weights over [lo, hi) in index order (binary32).
+// Weight of token e of a draw (residual, extra token, one-hot or tree residual).
+template <int DT>
+__device__ __forceinline__ float draw_weight(const void* tgt, const void* dft, size_t trow, size_t drow, int e,
+                                             const DrawParams& d, int kind, const int* excl, int nexcl) {
+    const float lt = load_logit<DT>(tgt, trow + e);
+    if (kind == kKindResidual) return weight_residual(lt, load_logit<DT>(dft, drow + e), d);
+    if (kind == kKindResidualTree) return in_set(e, excl, nexcl) ? 0.0f : weight_target(lt, d);
+    return weight_target_excl(lt, e, d, kind);
+}
+
 template <int DT>
 __device__ __forceinline__ float run_weights(const void* tgt, const void* dft, size_t trow,
                                              size_t drow, int lo, int hi, const DrawParams& d,
-                                             int kind) {
+                                             int kind, const int* excl, int nexcl) {
     float run = 0.0f;
-    for (int e = lo; e < hi; ++e) {
-        float lt = load_logit<DT>(tgt, trow + e);
-        float w = kind == kKindResidual ? weight_residual(lt, load_logit<DT>(dft, drow + e), d)
-                                        : weight_target_excl(lt, e, d, kind);
-        run = __fadd_rn(run, w);
-    }
+    for (int e = lo; e < hi; ++e) run = __fadd_rn(run, draw_weight<DT>(tgt, dft, trow, drow, e, d, kind, excl, nexcl));
     return run;
 }
 
@@ -150,6 +158,11 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
         for (int i = threadIdx.x; i < np; i += kThreads) {
             int x = a.tokens[static_cast<size_t>(b) * G + i];
             if (x < 0 || x >= V) bad = 1;
+            // tree: node i + 1's parent is an earlier node
+            if (a.tree) {
+                const int par = a.parents[static_cast<size_t>(b) * G + i];
+                if (par < 0 || par > i) bad = 1;
+            }
         }
         bad = __syncthreads_or(bad);
         if (!bad && a.early) {
@@ -263,7 +276,82 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
         __syncthreads();
 
         // Left-to-right acceptance scan on one thread.
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 0 && a.tree) {
+            // Tree walk: at node u the children (nodes whose parent is u) are tried
+            // in index order; child c is accepted with min(1, p'(x_c)), p' being
+            // p without the tokens of the children rejected so far, renormalised;
+            // an accepted child becomes u. With every child rejected (or a leaf)
+            // the last token is drawn from p'; at T = 0 the first child whose
+            // token is the argmax is taken.
+            const int32_t* tok = a.tokens + static_cast<size_t>(b) * G;
+            const int32_t* par = a.parents + static_cast<size_t>(b) * G;
+            const float* ua = a.u_accept + static_cast<size_t>(b) * G;
+            int u = 0, n = 0, ne = 0;
+            for (;;) {
+                if (greedy) {
+                    const int am = sh.st[u].idx;
+                    int next = -1;
+                    for (int cn = 1; cn <= np && next < 0; ++cn)
+                        if (par[cn - 1] == u && tok[cn - 1] == am) next = cn;
+                    out[n] = am;
+                    if (next < 0) break;
+                    if (a.out_nodes) a.out_nodes[static_cast<size_t>(b) * G + n] = next;
+                    ++n;
+                    u = next;
+                    continue;
+                }
+                const size_t tr = static_cast<size_t>(b) * (G + 1) + u;
+                double R = 0.0;  // probability of the rejected children
+                int next = -1;
+                ne = 0;
+                for (int cn = 1; cn <= np && next < 0; ++cn) {
+                    if (par[cn - 1] != u) continue;
+                    const int x = tok[cn - 1];
+                    const bool seen = in_set(x, sh.excl, ne);
+                    const double px =
+                        seen ? 0.0 : prob_from_stats(load_logit<DT>(a.target, tr * V + x), sh.st[u].m, sh.st[u].s, c);
+                    const double rest = 1.0 - R;
+                    const double alpha = rest > 0.0 ? fmin(1.0, px / rest) : 0.0;
+                    const size_t dr = static_cast<size_t>(b) * G + (cn - 1);
+                    if (a.dbg.p_x) a.dbg.p_x[dr] = px;
+                    if (a.dbg.q_x) a.dbg.q_x[dr] = 1.0;
+                    if (ua[cn - 1] < alpha) {
+                        next = cn;
+                    } else if (!seen) {
+                        sh.excl[ne++] = x;
+                        R += px;
+                    }
+                }
+                if (next < 0) break;
+                out[n] = tok[next - 1];
+                if (a.out_nodes) a.out_nodes[static_cast<size_t>(b) * G + n] = next;
+                ++n;
+                u = next;
+            }
+            if (a.out_nodes)
+                for (int j = n; j < G; ++j) a.out_nodes[static_cast<size_t>(b) * G + j] = -1;
+            if (greedy) {
+                if (a.dbg.kind) a.dbg.kind[b] = kKindGreedy;
+                if (a.dbg.w_total) a.dbg.w_total[b] = nan("");
+            } else {
+                DrawParams d;
+                d.c = c;
+                d.mcp = scaled_max(sh.st[u].m, c);
+                d.isp = __frcp_rn(sh.st[u].s);
+                d.excl = -1;
+                d.kind = ne > 0 ? kKindResidualTree : kKindBonus;
+                d.mcq = 0.0f;
+                d.isq = 0.0f;
+                d.fix = kFixTarget;
+                sh.draw = d;
+                if (a.dbg.kind) a.dbg.kind[b] = ne > 0 ? kKindResidual : kKindBonus;
+            }
+            sh.nexcl = ne;
+            sh.draw_row = u;
+            for (int j = n + 1; j <= G; ++j) out[j] = -1;
+            a.out_num_accepted[b] = n;
+            sh.n = n;
+        } else if (threadIdx.x == 0) {
             const int32_t* tok = a.tokens + static_cast<size_t>(b) * G;
             int n = np;
             if (greedy) {
@@ -321,26 +409,28 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             for (int j = n + 1; j <= G; ++j) out[j] = -1;
             a.out_num_accepted[b] = n;
             sh.n = n;
+            sh.nexcl = 0;
+            sh.draw_row = n;
         }
         __syncthreads();
 
         if (!greedy) {
             // Inverse-CDF draw over row n: thread t owns tokens [t*E, t*E + E).
-            const int n = sh.n;
+            const int n = sh.n, row = sh.draw_row, nexcl = sh.nexcl;
             DrawParams d = sh.draw;
-            const size_t trow = (static_cast<size_t>(b) * (G + 1) + n) * V;
-            const size_t drow = (static_cast<size_t>(b) * G + (n < G ? n : 0)) * V;
+            const size_t trow = (static_cast<size_t>(b) * (G + 1) + row) * V;
+            const size_t drow = (static_cast<size_t>(b) * G + (row < G ? row : 0)) * V;
             const int E = (V + kThreads - 1) / kThreads;
             const int lo = min(V, static_cast<int>(threadIdx.x) * E), hi = min(V, lo + E);
             int kind = d.kind;
-            float run = run_weights<DT>(a.target, a.draft, trow, drow, lo, hi, d, kind);
+            float run = run_weights<DT>(a.target, a.draft, trow, drow, lo, hi, d, kind, sh.excl, nexcl);
             unsigned long long qv = to_fixed(run, d.fix), total;
             unsigned long long excl = block_excl_scan_u64<kThreads>(qv, sh.scan, &total);
             if (total == 0ull) {
                 // Residual weights that round to zero everywhere: draw from p_n.
                 kind = kKindBonus;
                 d.fix = kFixTarget;
-                run = run_weights<DT>(a.target, a.draft, trow, drow, lo, hi, d, kind);
+                run = run_weights<DT>(a.target, a.draft, trow, drow, lo, hi, d, kind, sh.excl, nexcl);
                 qv = to_fixed(run, d.fix);
                 excl = block_excl_scan_u64<kThreads>(qv, sh.scan, &total);
             }
@@ -349,11 +439,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                 float run2 = 0.0f;
                 int token = hi - 1;
                 for (int e = lo; e < hi; ++e) {
-                    float lt = load_logit<DT>(a.target, trow + e);
-                    float w = kind == kKindResidual
-                                  ? weight_residual(lt, load_logit<DT>(a.draft, drow + e), d)
-                                  : weight_target_excl(lt, e, d, kind);
-                    run2 = __fadd_rn(run2, w);
+                    run2 = __fadd_rn(run2, draw_weight<DT>(a.target, a.draft, trow, drow, e, d, kind, sh.excl, nexcl));
                     if (excl + to_fixed(run2, d.fix) > t) {
                         token = e;
                         break;
@@ -365,7 +451,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                 a.dbg.w_total[b] = kind == kKindResidual
                                        ? static_cast<double>(total) * kFixResidualInv
                                        : static_cast<double>(total) * kFixTargetInv /
-                                             static_cast<double>(sh.st[n].s);
+                                             static_cast<double>(sh.st[row].s);
         }
         __syncthreads();
     }
