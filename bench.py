@@ -56,10 +56,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--early-exit", action="store_true",
                     help="early-exit verification: nothing after a request's first rejection is read")
-    ap.add_argument("--op", choices=["verify", "onehot", "ngram", "commit", "loop"], default="verify",
+    ap.add_argument("--op", choices=["verify", "onehot", "ngram", "commit", "loop", "tree"], default="verify",
                     help="verify (default, the headline); onehot: spec_verify_onehot on the workload's "
                          "target rows; ngram: spec_ngram_propose; commit: spec_commit; loop: ngram -> "
-                         "onehot verify -> commit, the model-free decoding step with no host sync")
+                         "onehot verify -> commit, the model-free decoding step with no host sync; tree: "
+                         "spec_verify_tree over the workload's target rows")
     return ap.parse_args()
 
 
@@ -269,7 +270,7 @@ def time_calls(call, K, W, stream):
 
 
 def run_aux(args, w, local):
-    """--op onehot | ngram | commit | loop on one GPU: one JSON line each, with
+    """--op onehot | ngram | commit | loop | tree on one GPU: one JSON line each, with
     the same timing rules as the headline (warm-up, CUDA events on the
     launching stream, per-call roofline)."""
     import torch
@@ -312,6 +313,22 @@ def run_aux(args, w, local):
             sv.spec_commit(out_t, out_n, buf, lens, stream=stream)
         unit, per_step = "requests/s", B
         metric = "post-verify commit requests/s"
+    elif args.op == "tree":
+        # a candidate tree per request over the workload's target rows: gamma
+        # nodes; node j's parent is node j - 1 half the time (a chain, whose
+        # tokens, the workload's draft tokens, are plausible), else uniform
+        # over 0..j-1 (a branch)
+        rng = np.random.default_rng(5)
+        par = np.array([[j - 1 if rng.random() < 0.5 else rng.integers(0, j) for j in range(1, G + 1)]
+                        for _ in range(B)], np.int32)
+        tree_par, tree_m = d(par), torch.full((B,), G, dtype=torch.int32, device="cuda")
+        tree_nodes = torch.empty((B, G), dtype=torch.int32, device="cuda")
+
+        def call():
+            sv.spec_verify_tree(tgt, tok, tree_par, tree_m, ua, us, T, out_t, out_n, tree_nodes, workspace=ws,
+                                stream=stream)
+        unit, per_step = "rows/s", B * (G + 1)
+        metric = "tree verification rows/s (gamma nodes per request, one row each), B×(γ+1)×V"
     else:
         def call():
             sv.spec_ngram_propose(buf, lens, G, 2, 5, props, nprop, stream=stream)
@@ -334,7 +351,11 @@ def run_aux(args, w, local):
     total_ms, per_call = time_calls(call, K, args.warmup, stream)
     clk = clocks.stop()
     n_acc = out_n.cpu().numpy()
-    if args.op in ("onehot", "loop"):
+    if args.op == "tree":
+        samp = int(((batch.temperature > 0) & (n_acc >= 0)).sum())
+        abytes = es * V * (B * (G + 1) + samp) + B * G * 12 + B * 12 + B * (G + 1) * 4 + B * G * 4
+        extra["mean_accepted"] = float(n_acc[n_acc >= 0].mean())
+    elif args.op in ("onehot", "loop"):
         samp = int(((batch.temperature > 0) & (n_acc >= 0)).sum())
         abytes = es * V * (B * (G + 1) + samp) + B * G * 8 + B * 12 + B * (G + 1) * 4
         extra["mean_accepted"] = float(n_acc[n_acc >= 0].mean())
@@ -351,7 +372,8 @@ def run_aux(args, w, local):
     line = {
         "metric": metric, "value": K * per_step / (total_ms * 1e-3), "unit": unit, "n_gpus": 1, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.dtype if args.op in ("onehot", "loop") else "int32", "data": "synthetic",
+        "vs_baseline": None, "dtype": w.dtype if args.op in ("onehot", "loop", "tree") else "int32",
+        "data": "synthetic",
         "op": args.op,
         "config": {"workload": w.description, "B": B, "gamma": G, "V": V,
                    "histories": f"lengths U(256, {M}), copy probability 0.5, vocab {V}"},

@@ -293,12 +293,20 @@ sv_status spec_verify_onehot(const void* target_logits, sv_dtype dtype, int B, i
  * Invalid requests (-1, SV_STATUS_BAD_REQUEST): T NaN, negative or infinite;
  * num_nodes[b] outside [0, gamma]; a parent not an earlier node; a token
  * outside [0, V); a bad row among 0..num_nodes[b]. Rows past num_nodes[b] are
- * not read. This version runs one thread block per request (no workspace). */
+ * not read.
+ *   workspace, workspace_bytes: as spec_verify (spec_verify_workspace_size of
+ *              the same B, gamma, V, dtype); NULL keeps the call on one thread
+ *              block per request, which needs none (SV_PATH_STREAMING with a
+ *              NULL or short workspace returns SV_ERR_WORKSPACE)
+ *   opts       NULL, or path, grid_ctas, peer_wait_us and hold_flag as in
+ *              spec_verify_ex; early_exit must be 0 and num_draft is not read
+ *              (SV_ERR_INVALID_ARG otherwise). */
 sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype, int B, int gamma, int V,
                            const int32_t* node_tokens, const int32_t* parents, const int32_t* num_nodes,
                            const float* u_accept, const float* u_sample, const float* temperature,
-                           int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_nodes, sv_stream_t stream,
-                           const sv_debug_out* dbg, int32_t* d_status);
+                           int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_nodes, void* workspace,
+                           size_t workspace_bytes, sv_stream_t stream, const sv_debug_out* dbg, int32_t* d_status,
+                           const sv_options* opts);
 
 /* ---------------------------------------------------------------------------
  * Post-verify bookkeeping ("Accélérer Sonar grâce à la spéculation",

@@ -71,8 +71,8 @@ def _declare(lib):
     lib.spec_commit.argtypes = [vp, vp, int_, int_, vp, int_, vp, vp, vp, vp]
     lib.spec_ngram_propose.argtypes = [vp, int_, int_, vp, int_, int_, int_, vp, vp, vp, vp]
     lib.spec_verify_onehot.argtypes = [vp, i32, int_, int_, int_, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
-    lib.spec_verify_tree.argtypes = [vp, i32, int_, int_, int_, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                     ctypes.POINTER(_Debug), vp]
+    lib.spec_verify_tree.argtypes = [vp, i32, int_, int_, int_, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp,
+                                     ctypes.POINTER(_Debug), vp, ctypes.POINTER(_Options)]
     for name in ("spec_verify_workspace_size", "spec_verify_host_staging_size", "spec_verify",
                  "spec_verify_ex", "spec_verify_host", "spec_verify_noalloc", "spec_commit",
                  "spec_ngram_propose", "spec_verify_onehot", "spec_verify_tree"):
@@ -330,12 +330,14 @@ def spec_verify_onehot(target_logits, draft_tokens, num_draft, u_accept, u_sampl
 
 
 def spec_verify_tree(target_logits, node_tokens, parents, num_nodes, u_accept, u_sample, temperature,
-                     out_tokens=None, out_num_accepted=None, out_nodes=None, debug=False, status=None,
-                     stream=None):
+                     out_tokens=None, out_num_accepted=None, out_nodes=None, workspace=None, debug=False,
+                     status=None, stream=None, path: int = SV_PATH_AUTO, grid_ctas: int = 0, peer_wait_us: int = 0,
+                     hold_flag=None):
     """``spec_verify_tree``: verification of a candidate tree per request (see
     include/specverify.h). ``target_logits`` [B, G+1, V], ``node_tokens`` /
     ``parents`` / ``u_accept`` [B, G] indexed by node - 1, ``num_nodes`` [B];
-    CUDA tensors. Returns ``(Outputs, out_nodes)``."""
+    CUDA tensors. The workspace is allocated with torch when not given.
+    Returns ``(Outputs, out_nodes)``."""
     import torch
     lib = load()
     B, G1, V = target_logits.shape
@@ -351,6 +353,8 @@ def spec_verify_tree(target_logits, node_tokens, parents, num_nodes, u_accept, u
         out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
     if out_nodes is None:
         out_nodes = torch.empty((B, G), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(16, workspace_size(B, G, V, dt)), dtype=torch.uint8, device=dev)
     d = _Debug()
     dbg = None
     if debug:
@@ -368,9 +372,11 @@ def spec_verify_tree(target_logits, node_tokens, parents, num_nodes, u_accept, u
         }
         for k, v in dbg.items():
             setattr(d, k, v.data_ptr())
+    o = _Options(path, grid_ctas, peer_wait_us, 0, _ptr(hold_flag) or None, None)
     rc = lib.spec_verify_tree(_ptr(target_logits), dt, B, G, V, _ptr(node_tokens), _ptr(parents), _ptr(num_nodes),
                               _ptr(u_accept), _ptr(u_sample), _ptr(temperature), _ptr(out_tokens),
-                              _ptr(out_num_accepted), _ptr(out_nodes), _stream_handle(stream), ctypes.byref(d),
-                              _ptr(status))
+                              _ptr(out_num_accepted), _ptr(out_nodes), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream_handle(stream), ctypes.byref(d),
+                              _ptr(status), ctypes.byref(o))
     _check(rc, "spec_verify_tree")
     return Outputs(out_tokens, out_num_accepted, dbg, status), out_nodes

@@ -93,6 +93,37 @@ sv_status spec_verify_workspace_size(int B, int gamma, int V, sv_dtype dtype, si
     return SV_OK;
 }
 
+// Picks the kernel and launches it: the streaming kernel when asked for (or,
+// on SV_PATH_AUTO, when it applies and the target logits reach 64 KB: below
+// that one block per request is quicker), else one block per request.
+static sv_status dispatch(const Args& a, const DeviceInfo& dev, int path, int grid_ctas, void* workspace,
+                   size_t workspace_bytes, sv_stream_t stream) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int grid = streaming_default_grid(dev);
+    if (grid_ctas > 0) grid = std::min(grid, grid_ctas);
+    const bool stream_ok = streaming_applicable(a) && streaming_grid_ok(a.B, grid);
+    bool use_stream = false;
+    if (path == SV_PATH_STREAMING) {
+        if (!stream_ok) return SV_ERR_INVALID_ARG;
+        use_stream = true;
+    } else if (path == SV_PATH_AUTO) {
+        const size_t target_bytes = static_cast<size_t>(a.B) * (a.gamma + 1) * a.V * elem_bytes(a.dtype);
+        use_stream = stream_ok && target_bytes >= (64u << 10);
+    }
+    cudaError_t err;
+    if (use_stream) {
+        const size_t need = streaming_workspace_bytes(a.B, a.gamma, a.V, a.dtype, grid);
+        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
+            return SV_ERR_WORKSPACE;
+        err = launch_streaming(a, dev, grid, workspace, workspace_bytes, s);
+    } else {
+        err = launch_rowwise(a, dev, s);
+    }
+    if (err != cudaSuccess) return SV_ERR_CUDA;
+    g_last_launches = 1;
+    return SV_OK;
+}
+
 sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv_dtype dtype, int B,
                          int gamma, int V, const int32_t* draft_tokens, const float* u_accept,
                          const float* u_sample, const float* temperature, int32_t* out_tokens,
@@ -114,7 +145,7 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
     if (!current_device(&dev)) return SV_ERR_UNSUPPORTED;
     if (dev.cc_major != 10 || dev.cc_minor != 3) return SV_ERR_UNSUPPORTED;
 
-    Args a;
+    Args a = {};  // every field not set below is zero (no tree, no parents)
     a.target = target_logits;
     a.draft = draft_logits;
     a.onehot = draft_logits == nullptr;
@@ -137,48 +168,24 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
                                                      : 2000000000ull;
     a.hold_flag = opts ? opts->hold_flag : nullptr;
 
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int grid = streaming_default_grid(dev);
-    if (opts && opts->grid_ctas > 0) grid = std::min(grid, opts->grid_ctas);
-    const bool stream_ok = streaming_applicable(a) && streaming_grid_ok(B, grid);
-    bool use_stream = false;
-    if (path == SV_PATH_STREAMING) {
-        if (!stream_ok) return SV_ERR_INVALID_ARG;
-        use_stream = true;
-    } else if (path == SV_PATH_AUTO) {
-        // below about 64 KB of target logits one block per request is quicker
-        const size_t target_bytes = static_cast<size_t>(B) * (gamma + 1) * V * elem_bytes(dtype);
-        use_stream = stream_ok && target_bytes >= (64u << 10);
-    }
-    cudaError_t err;
-    if (use_stream) {
-        const size_t need = streaming_workspace_bytes(B, gamma, V, dtype, grid);
-        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
-            return SV_ERR_WORKSPACE;
-        err = launch_streaming(a, dev, grid, workspace, workspace_bytes, s);
-        if (err == cudaSuccess) g_last_launches = 1;
-    } else {
-        err = launch_rowwise(a, dev, s);
-        if (err == cudaSuccess) g_last_launches = 1;
-    }
-    if (err != cudaSuccess) {
-        g_last_launches = 0;
-        return SV_ERR_CUDA;
-    }
-    return SV_OK;
+    return dispatch(a, dev, path, opts ? opts->grid_ctas : 0, workspace, workspace_bytes, stream);
 }
 
 sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype, int B, int gamma, int V,
                            const int32_t* node_tokens, const int32_t* parents, const int32_t* num_nodes,
                            const float* u_accept, const float* u_sample, const float* temperature,
-                           int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_nodes, sv_stream_t stream,
-                           const sv_debug_out* dbg, int32_t* d_status) {
+                           int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_nodes, void* workspace,
+                           size_t workspace_bytes, sv_stream_t stream, const sv_debug_out* dbg, int32_t* d_status,
+                           const sv_options* opts) {
     g_last_launches = 0;
     if (!shape_ok(B, gamma, V, dtype)) return SV_ERR_INVALID_ARG;
     if (B == 0) return SV_OK;
     if (!target_logits || !node_tokens || !parents || !num_nodes || !u_accept || !u_sample || !temperature ||
         !out_tokens || !out_num_accepted)
         return SV_ERR_INVALID_ARG;
+    const int path = opts ? opts->path : SV_PATH_AUTO;
+    if (path != SV_PATH_AUTO && path != SV_PATH_ROWWISE && path != SV_PATH_STREAMING) return SV_ERR_INVALID_ARG;
+    if (opts && (opts->grid_ctas < 0 || opts->peer_wait_us < 0 || opts->early_exit)) return SV_ERR_INVALID_ARG;
     DeviceInfo dev;
     if (!current_device(&dev)) return SV_ERR_UNSUPPORTED;
     if (dev.cc_major != 10 || dev.cc_minor != 3) return SV_ERR_UNSUPPORTED;
@@ -196,16 +203,15 @@ sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype, int B, int
     a.out_num_accepted = out_num_accepted;
     if (dbg) a.dbg = *dbg;
     a.d_status = d_status;
-    a.peer_wait_ns = 2000000000ull;
+    a.peer_wait_ns = (opts && opts->peer_wait_us > 0) ? 1000ull * static_cast<unsigned>(opts->peer_wait_us)
+                                                     : 2000000000ull;
+    a.hold_flag = opts ? opts->hold_flag : nullptr;
     a.onehot = true;  // candidates are tokens, not draws from a draft distribution
     a.num_draft = num_nodes;
     a.tree = true;
     a.parents = parents;
     a.out_nodes = out_nodes;
-    const cudaError_t err = launch_rowwise(a, dev, reinterpret_cast<cudaStream_t>(stream));
-    if (err != cudaSuccess) return SV_ERR_CUDA;
-    g_last_launches = 1;
-    return SV_OK;
+    return dispatch(a, dev, path, opts ? opts->grid_ctas : 0, workspace, workspace_bytes, stream);
 }
 
 sv_status spec_verify_onehot(const void* target_logits, sv_dtype dtype, int B, int gamma, int V,

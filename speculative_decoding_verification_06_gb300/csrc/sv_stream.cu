@@ -78,7 +78,8 @@ struct Rec {
 };
 
 struct Job {
-    int32_t b, n, kind, pad;
+    int32_t b, n, kind, pad;  // request, the draw's row, kind, u_sample bits
+    int32_t slot;             // output position of the drawn token (the row n, except in trees)
     DrawParams d;
 };
 
@@ -103,7 +104,8 @@ constexpr int kStatsDraft = 2;   // StageDesc.flags: the stage also holds the dr
 struct Layout {
     long long Et;  // target elements B*(gamma+1)*V
     int G, MT, MD, NCH, vec;
-    size_t hdr, req_done, job_done, ready, ee_tasks, ee_done, clear_bytes, rec_t, rec_d, ee_rec, jobs, wsums, total;
+    size_t hdr, req_done, job_done, ready, ee_tasks, ee_done, clear_bytes, rec_t, rec_d, ee_rec, jobs, jobset, wsums,
+        total;
     int ee_cap;  // early exit: task slots, B (gamma + 2)
 };
 
@@ -146,6 +148,7 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.rec_d = take(static_cast<size_t>(G) * L.MD * sizeof(Rec));
     L.ee_rec = take(static_cast<size_t>(L.ee_cap) * L.NCH * 2 * sizeof(Rec));  // per (task, chunk): target, draft
     L.jobs = take(static_cast<size_t>(B) * sizeof(Job));
+    L.jobset = take(static_cast<size_t>(B) * gamma * 4);  // tree jobs: tokens excluded from the last draw
     L.wsums = take(static_cast<size_t>(B) * L.NCH * kConsumerWarps * 8);
     L.total = off;
     return L;
@@ -311,6 +314,8 @@ struct Ctl {
     unsigned fq_head;                       // entries the finisher has taken
     int cons_done;                          // consumer warps done with both phases
     short kmap[kMaxB];                      // compacted index of each T > 0 request, else -1
+    int dset[kStages][SV_MAX_GAMMA];        // tree draws: the excluded tokens of the item in each stage
+    int fset[SV_MAX_GAMMA];                 // tree draws: the excluded tokens of the job being searched
 };
 
 struct RowLoc {
@@ -360,6 +365,7 @@ struct Kern {
     __device__ Rec* rec_t() const { return reinterpret_cast<Rec*>(ws + L.rec_t); }
     __device__ Rec* rec_d() const { return reinterpret_cast<Rec*>(ws + L.rec_d); }
     __device__ Job* jobs() const { return reinterpret_cast<Job*>(ws + L.jobs); }
+    __device__ int* jobset() const { return reinterpret_cast<int*>(ws + L.jobset); }
     __device__ unsigned* req_done() const { return reinterpret_cast<unsigned*>(ws + L.req_done); }
     __device__ unsigned* job_done() const { return reinterpret_cast<unsigned*>(ws + L.job_done); }
     __device__ int* ready() const { return reinterpret_cast<int*>(ws + L.ready); }
@@ -428,11 +434,16 @@ struct Kern {
     // writes the stage's descriptor; `src` null with `desc` sends the end
     // marker (the stage completes with no bytes).
     __device__ bool produce(Cursor& p, const char* src, unsigned bytes, const char* src2 = nullptr,
-                            unsigned bytes2 = 0, const StageDesc* desc = nullptr) const {
+                            unsigned bytes2 = 0, const StageDesc* desc = nullptr, const int* set = nullptr,
+                            int nset = 0) const {
         const int slot = p.it % kStages;
         const unsigned round = p.it / kStages;
         // the verdict is made warp-uniform so that a timeout cannot split the warp
         if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(&ctl.empty[slot], (round - 1) & 1))) return false;
+        // a tree draw's excluded tokens travel with the stage (written by
+        // another block's finisher: read from L2)
+        for (int i = threadIdx.x & 31; i < nset; i += 32) ctl.dset[slot][i] = __ldcg(set + i);
+        __syncwarp();
         if ((threadIdx.x & 31) == 0) {
             if (desc) ctl.desc[slot] = *desc;
             if (src) {
@@ -498,7 +509,8 @@ struct Kern {
                         __threadfence();
                         own_k = v - 1;
                         const int kind = __ldcg(&jobs()[own_k].kind);
-                        if (kind != kKindResidual && kind != kKindBonus && kind != kKindResidualOnehot) {  // no items, no search
+                        if (kind != kKindResidual && kind != kKindBonus && kind != kKindResidualOnehot &&
+                            kind != kKindResidualTree) {  // no items, no search
                             own_p += G;
                             own_k = -1;
                             moved = 1;
@@ -925,7 +937,7 @@ struct Kern {
         // gathered logits and the uniform are loaded before the row merges
         int x0 = 0;
         float lt0 = 0.0f, ld0 = 0.0f, u0 = 0.0f;
-        if (lane < np) {
+        if (lane < np && !a.tree) {
             x0 = tok[lane];
             if (!greedy && x0 >= 0 && x0 < V) {
                 const size_t tr = static_cast<size_t>(b) * (GM + 1) + lane;
@@ -938,6 +950,10 @@ struct Kern {
         for (int i = lane; i < np; i += 32) {
             const int x = tok[i];
             if (x < 0 || x >= V) bad = 1;
+            if (a.tree) {  // node i + 1's parent is an earlier node
+                const int par = a.parents[static_cast<size_t>(b) * GM + i];
+                if (par < 0 || par > i) bad = 1;
+            }
         }
         const int nrows = !range_ok ? 0 : (samp && !onehot ? 2 * GM + 1 : np + 1);
         for (int r = lane; r < nrows; r += 32) {
@@ -994,6 +1010,10 @@ struct Kern {
             if (dbg.max_draft) dbg.max_draft[r] = draft ? st[GM + 1 + j].m : nanf("");
             if (dbg.lse_draft)
                 dbg.lse_draft[r] = draft ? lse_from_stats(st[GM + 1 + j].m, st[GM + 1 + j].s, c, T) : nan("");
+        }
+        if (a.tree) {
+            tree_walk(b, k, st, greedy, c, np);
+            return;
         }
         // first failing position over all lanes (gamma may exceed 32)
         int n = np;
@@ -1052,6 +1072,7 @@ struct Kern {
                 Job j;
                 j.b = b;
                 j.n = n;
+                j.slot = n;
                 j.pad = __float_as_int(a.u_sample[b]);  // the draw's uniform
                 DrawParams& d = j.d;
                 d.c = c;
@@ -1080,6 +1101,98 @@ struct Kern {
         }
     }
 
+    // Tree walk of request b (rows' statistics in st; np proposal nodes).
+    // At node u the children (the nodes whose parent is u) are tried in index
+    // order; child c is accepted with min(1, p'(x_c)), p' being p_u without
+    // the tokens of the children rejected so far, renormalised, and an
+    // accepted child becomes u. When every child is rejected (or u is a
+    // leaf) the last token is drawn from p' of u: its excluded tokens go to
+    // the job's set. At T = 0 the first child whose token is the argmax of
+    // p_u is followed. The test is made in binary64 on lane 0, as the
+    // one-block-per-request kernel makes it.
+    __device__ void tree_walk(int b, int k, const Rec* st, bool greedy, float c, int np) const {
+        const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V;
+        const sv_debug_out& dbg = a.dbg;
+        int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
+        for (int i = lane; i < GM; i += 32) {
+            const size_t dr = static_cast<size_t>(b) * GM + i;
+            if (dbg.p_x) dbg.p_x[dr] = nan("");  // children never tried
+            if (dbg.q_x) dbg.q_x[dr] = nan("");
+            if (a.out_nodes) a.out_nodes[dr] = -1;
+        }
+        for (int j = lane; j <= GM; j += 32) out[j] = -1;
+        __syncwarp();
+        if (lane != 0) return;
+        const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
+        const int32_t* par = a.parents + static_cast<size_t>(b) * GM;
+        const float* ua = a.u_accept + static_cast<size_t>(b) * GM;
+        int* set = greedy ? nullptr : jobset() + static_cast<size_t>(k) * GM;
+        int u = 0, n = 0, ne = 0;
+        for (;;) {
+            int next = -1;
+            if (greedy) {
+                const int am = st[u].idx;
+                for (int cn = 1; cn <= np && next < 0; ++cn)
+                    if (par[cn - 1] == u && tok[cn - 1] == am) next = cn;
+                if (next < 0) {
+                    out[n] = am;
+                    break;
+                }
+            } else {
+                const size_t tr = static_cast<size_t>(b) * (GM + 1) + u;
+                double R = 0.0;  // p_u of the rejected children
+                ne = 0;
+                for (int cn = 1; cn <= np && next < 0; ++cn) {
+                    if (par[cn - 1] != u) continue;
+                    const int x = tok[cn - 1];
+                    const bool seen = in_set(x, set, ne);
+                    const double px = seen ? 0.0 : prob_from_stats(load_logit<DT>(a.target, tr * V + x), st[u].m,
+                                                                   st[u].s, c);
+                    const double rest = 1.0 - R;
+                    const double alpha = rest > 0.0 ? fmin(1.0, px / rest) : 0.0;
+                    const size_t dr = static_cast<size_t>(b) * GM + (cn - 1);
+                    if (dbg.p_x) dbg.p_x[dr] = px;
+                    if (dbg.q_x) dbg.q_x[dr] = 1.0;
+                    if (ua[cn - 1] < alpha) {
+                        next = cn;
+                    } else if (!seen) {
+                        set[ne++] = x;
+                        R += px;
+                    }
+                }
+                if (next < 0) break;
+            }
+            out[n] = tok[next - 1];
+            if (a.out_nodes) a.out_nodes[static_cast<size_t>(b) * GM + n] = next;
+            ++n;
+            u = next;
+        }
+        a.out_num_accepted[b] = n;
+        if (greedy) {
+            if (dbg.kind) dbg.kind[b] = kKindGreedy;
+            if (dbg.w_total) dbg.w_total[b] = nan("");
+            return;
+        }
+        Job j;
+        j.b = b;
+        j.n = u;  // the draw's row: the last node
+        j.slot = n;
+        j.pad = __float_as_int(a.u_sample[b]);
+        DrawParams& d = j.d;
+        d.c = c;
+        d.mcp = scaled_max(st[u].m, c);
+        d.isp = __frcp_rn(st[u].s);
+        d.kind = ne > 0 ? kKindResidualTree : kKindBonus;
+        d.excl = ne > 0 ? ne : -1;
+        d.mcq = 0.0f;
+        d.isq = 0.0f;
+        d.fix = kFixTarget;
+        j.kind = d.kind;
+        jobs()[k] = j;
+        publish(k);  // its fence also orders the set before the job
+        if (dbg.kind) dbg.kind[b] = ne > 0 ? kKindResidual : kKindBonus;
+    }
+
     // A run is kTPT consecutive tokens, 64 bytes, held packed as 4 vectors of
     // kTPV tokens. Its weight sum is defined vector by vector: S_q adds the
     // weights of vector q in index order, and the run total is
@@ -1092,8 +1205,11 @@ struct Kern {
     // arguments l c - mc are formed pair by pair with fma.rn.f32x2 (each lane
     // rounded as a scalar fma), so every weight equals weight_residual or
     // weight_target of that token.
+    // `set` (shared memory): the tokens a tree residual excludes, d.excl of
+    // them; unused by the other kinds.
     __device__ static __forceinline__ void vec_weights(const uint4& vt, const uint4& vd, const DrawParams& d,
-                                                       int kind, int first, float (&w)[kTPV]) {
+                                                       int kind, int first, float (&w)[kTPV],
+                                                       const int* set = nullptr) {
         const uint32_t t4[4] = {vt.x, vt.y, vt.z, vt.w};
         const uint32_t d4[4] = {vd.x, vd.y, vd.z, vd.w};
         const unsigned long long cc = f2_pack(d.c, d.c), nmp = f2_pack(-d.mcp, -d.mcp);
@@ -1123,14 +1239,22 @@ struct Kern {
             const int rel = d.excl - first;
 #pragma unroll
             for (int e = 0; e < kTPV; ++e) w[e] = e == rel ? 0.0f : w[e];
+        } else if (kind == kKindResidualTree) {  // p without the rejected children's tokens
+            for (int i = 0; i < d.excl; ++i) {
+                const int rel = set[i] - first;
+                if (static_cast<unsigned>(rel) < static_cast<unsigned>(kTPV)) {
+#pragma unroll
+                    for (int e = 0; e < kTPV; ++e) w[e] = e == rel ? 0.0f : w[e];
+                }
+            }
         }
     }
 
     // S_q of one vector: its weights added in index order.
     __device__ static __forceinline__ float vec_sum(const uint4& vt, const uint4& vd, const DrawParams& d, int kind,
-                                                    int first) {
+                                                    int first, const int* set = nullptr) {
         float w[kTPV];
-        vec_weights(vt, vd, d, kind, first, w);
+        vec_weights(vt, vd, d, kind, first, w, set);
         float s = w[0];
 #pragma unroll
         for (int e = 1; e < kTPV; ++e) s = __fadd_rn(s, w[e]);
@@ -1145,12 +1269,12 @@ struct Kern {
     // tokens weigh 0 (rows end on 16-byte boundaries, so a vector is either
     // wholly in the row or wholly past it).
     __device__ static __forceinline__ void run_vec_sums(const Run& vt, const Run& vd, int valid, const DrawParams& d,
-                                                        int kind, int first, float (&S)[4]) {
+                                                        int kind, int first, float (&S)[4], const int* set = nullptr) {
         // all four are computed (straight-line code), then the ones past the
         // row are dropped; `first` is the run's first token
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float x = vec_sum(vt[q], vd[q], d, kind, first + q * kTPV);
+            const float x = vec_sum(vt[q], vd[q], d, kind, first + q * kTPV, set);
             S[q] = q * kTPV < valid ? x : 0.0f;
         }
     }
@@ -1169,13 +1293,14 @@ struct Kern {
     // in the rotated order and put back in index order (rotate by 2 if r & 2,
     // then by 1 if r & 1; selects on constant indices) before they are added.
     __device__ static __forceinline__ float run_total_rotated(const Run& rt, const Run& rd, int t, int valid,
-                                                              const DrawParams& d, int kind, int first) {
+                                                              const DrawParams& d, int kind, int first,
+                                                              const int* set = nullptr) {
         const int r = (t >> 1) & 3;
         float Sr[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             // stale shared memory past the row is dropped
-            const float x = vec_sum(rt[k], rd[k], d, kind, first + ((k + r) & 3) * kTPV);
+            const float x = vec_sum(rt[k], rd[k], d, kind, first + ((k + r) & 3) * kTPV, set);
             Sr[k] = ((k + r) & 3) * kTPV < valid ? x : 0.0f;
         }
         const bool r2 = (r & 2) != 0, r1 = (r & 1) != 0;
@@ -1199,7 +1324,7 @@ struct Kern {
 
     // Fixed-point weight sum of run r of chunk j of a job, from global memory.
     __device__ __forceinline__ unsigned long long run_fixed_global(long long trow, long long drow, int j, int r,
-                                                   const DrawParams& d, int kind) const {
+                                                   const DrawParams& d, int kind, const int* set = nullptr) const {
         const long long e0 = static_cast<long long>(j) * kChunkElems;
         const int cnt = static_cast<int>(min(static_cast<long long>(kChunkElems), a.V - e0));
         const int valid = max(0, min(kTPT, cnt - r * kTPT));
@@ -1208,7 +1333,7 @@ struct Kern {
         load_run_global(a.target, trow + e0 + r * kTPT, valid, vt);
         if (kind == kKindResidual) load_run_global(a.draft, drow + e0 + r * kTPT, valid, vd);
         float S[4];
-        run_vec_sums(vt, vd, valid, d, kind, static_cast<int>(e0) + r * kTPT, S);
+        run_vec_sums(vt, vd, valid, d, kind, static_cast<int>(e0) + r * kTPT, S, set);
         return to_fixed(run_total(S), d.fix);
     }
 
@@ -1249,7 +1374,14 @@ struct Kern {
 #pragma unroll
             for (int q = 0; q < static_cast<int>(sizeof(Job) / 4); ++q) dst[q] = __ldcg(src + q);
         }
-        if (jb.kind != kKindResidual && jb.kind != kKindBonus && jb.kind != kKindResidualOnehot) return;
+        if (jb.kind != kKindResidual && jb.kind != kKindBonus && jb.kind != kKindResidualOnehot &&
+            jb.kind != kKindResidualTree)
+            return;
+        if (jb.kind == kKindResidualTree) {
+            for (int i = lane; i < jb.d.excl; i += 32) ctl.fset[i] = __ldcg(jobset() + static_cast<size_t>(k) * a.gamma + i);
+            __syncwarp();
+        }
+        const int* set = ctl.fset;
         DrawParams d = jb.d;
         int kind = jb.kind;
         const long long trow = (static_cast<long long>(jb.b) * (a.gamma + 1) + jb.n) * a.V;
@@ -1258,7 +1390,7 @@ struct Kern {
         bool fallback = false;
         auto warp_part = [&](int j, int w) -> unsigned long long {
             if (!fallback) return __ldcg(js + static_cast<size_t>(j) * kConsumerWarps + w);
-            return warp_sum_u64(run_fixed_global(trow, drow, j, w * 32 + lane, d, kind));
+            return warp_sum_u64(run_fixed_global(trow, drow, j, w * 32 + lane, d, kind, set));
         };
         // total of chunk j on the fallback, computed by the whole warp
         auto chunk_total_warp = [&](int j) -> unsigned long long {
@@ -1348,7 +1480,7 @@ struct Kern {
             if (kind == kKindResidual) load_run_global(a.draft, drow + e0 + vt * TPT, valid, ld);
         }
         float S[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (valid > 0) run_vec_sums(lt, ld, valid, d, kind, static_cast<int>(e0) + vt * TPT, S);
+        if (valid > 0) run_vec_sums(lt, ld, valid, d, kind, static_cast<int>(e0) + vt * TPT, S, set);
         const unsigned long long q = to_fixed(run_total(S), d.fix);
         unsigned long long x = q;
 #pragma unroll
@@ -1379,7 +1511,7 @@ struct Kern {
                 const uint4 wt = vsel == 0 ? lt[0] : vsel == 1 ? lt[1] : vsel == 2 ? lt[2] : lt[3];
                 const uint4 wd = vsel == 0 ? ld[0] : vsel == 1 ? ld[1] : vsel == 2 ? ld[2] : ld[3];
                 float w[kTPV];
-                vec_weights(wt, wd, d, kind, static_cast<int>(e0) + vt * TPT + vsel * kTPV, w);
+                vec_weights(wt, wd, d, kind, static_cast<int>(e0) + vt * TPT + vsel * kTPV, w, set);
                 float part = w[0];
                 int last_pos = w[0] > 0.0f ? 0 : -1;
                 if (start + to_fixed(__fadd_rn(Pv, part), d.fix) > tt) token = 0;
@@ -1394,11 +1526,11 @@ struct Kern {
             } else {
                 token = valid - 1;  // cannot happen: the run's total passes tt
             }
-            a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.n] = static_cast<int>(e0) + vt * TPT + token;
+            a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.slot] = static_cast<int>(e0) + vt * TPT + token;
         }
         if (!ball && lane == 0) {
             // cannot happen: the runs partition [0, total) exactly
-            a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.n] = a.V - 1;
+            a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.slot] = a.V - 1;
         }
         if (lane == 0 && a.dbg.w_total) {
             const double W = static_cast<double>(total);
@@ -1834,6 +1966,7 @@ struct Kern {
         Job j;
         j.b = b;
         j.n = pos;
+        j.slot = pos;
         j.pad = __float_as_int(a.u_sample[b]);
         DrawParams& d = j.d;
         d.c = c;
@@ -2053,7 +2186,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                     cur_p = p;
                 }
                 const int kind = __shfl_sync(0xffffffffu, desc.job.kind, 0);
-                if (kind == kKindResidual || kind == kKindBonus || kind == kKindResidualOnehot) {
+                if (kind == kKindResidual || kind == kKindBonus || kind == kKindResidualOnehot ||
+                    kind == kKindResidualTree) {
                     const int b = __shfl_sync(0xffffffffu, desc.job.b, 0), n = __shfl_sync(0xffffffffu, desc.job.n, 0);
                     desc.j = j;
                     const long long e0 = static_cast<long long>(j) * CH;
@@ -2065,6 +2199,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                         const long long drow = static_cast<long long>(b) * a.gamma + n;
                         ok = K.produce(prod, src_t, bytes,
                                        static_cast<const char*>(a.draft) + (drow * a.V + e0) * KT::ES, bytes, &desc);
+                    } else if (kind == kKindResidualTree) {
+                        const int jk = __shfl_sync(0xffffffffu, desc.k, 0);
+                        const int ne = __shfl_sync(0xffffffffu, desc.job.d.excl, 0);
+                        ok = K.produce(prod, src_t, bytes, nullptr, 0u, &desc,
+                                       K.jobset() + static_cast<size_t>(jk) * a.gamma, ne);
                     } else {
                         ok = K.produce(prod, src_t, bytes, nullptr, 0u, &desc);
                     }
@@ -2141,10 +2280,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                 KT::load_run_smem(smt, t, lt);
                 if (ds.job.kind == kKindResidual) KT::load_run_smem(smt + kChunkBytes, t, ld);
             }
-            K.consume_end(cons);
+            // a tree draw reads its excluded tokens from the stage: the stage is
+            // released after the weights
+            const bool tree = ds.job.kind == kKindResidualTree;
+            if (!tree) K.consume_end(cons);
             const float run = valid > 0 ? KT::run_total_rotated(lt, ld, t, valid, ds.job.d, ds.job.kind,
-                                                                static_cast<int>(e0) + t * TPT)
+                                                                static_cast<int>(e0) + t * TPT, ctl.dset[slot])
                                         : 0.0f;
+            if (tree) K.consume_end(cons);
             const unsigned long long wsum = warp_sum_u64(to_fixed(run, ds.job.d.fix));
             if (lane == 0) {
                 wsums[(static_cast<size_t>(ds.k) * L.NCH + ds.j) * kConsumerWarps + warp] = wsum;

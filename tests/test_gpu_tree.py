@@ -1,9 +1,11 @@
 """Tree verification (spec_verify_tree) against the tree oracle through the C
 ABI: hand-worked cases, random trees at every temperature (bf16 and fp32,
 including EAGLE-sized trees of 60 nodes), chi-square checks of the output
-distribution, and invalid trees. Integer outputs are exact; sampled requests
-whose decisions fall within the 1e-5 margin are counted as near ties and
-checked for validity only (the rule of the parity tests)."""
+distribution, and invalid trees, on both kernels (one block per request, and
+the streaming kernel at its default grid and at small grids that put many
+requests on one block). Integer outputs are exact; sampled requests whose
+decisions fall within the 1e-5 margin are counted as near ties and checked
+for validity only (the rule of the parity tests)."""
 import json
 import os
 
@@ -18,6 +20,10 @@ pytestmark = pytest.mark.gpu
 sv = pytest.importorskip("speculative_decoding_verification_06_gb300")
 HERE = os.path.dirname(os.path.abspath(__file__))
 MARGIN = 1e-5
+ROWWISE = dict(path=1)
+STREAM = dict(path=2)
+PATHS = [ROWWISE, STREAM, dict(path=2, grid_ctas=3), dict(path=2, grid_ctas=7)]
+PATH_IDS = ["rowwise", "stream", "stream-g3", "stream-g7"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,11 +41,11 @@ def _dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
 
-def run_gpu(t):
+def run_gpu(t, **kw):
     import torch
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     res, nodes = sv.spec_verify_tree(_dev(t["target"]), _dev(t["tokens"]), _dev(t["parents"]), _dev(t["m"]),
-                                     _dev(t["ua"]), _dev(t["us"]), _dev(t["T"]), debug=True, status=status)
+                                     _dev(t["ua"]), _dev(t["us"]), _dev(t["T"]), debug=True, status=status, **kw)
     torch.cuda.synchronize()
     assert sv.last_launch_count() == 1
     out = {k: v.cpu().numpy() for k, v in res.debug.items()}
@@ -97,58 +103,97 @@ def random_trees(B, G, V, dtype, seed, temps=(0.0, 0.5, 1.0)):
                 T=rng.choice(np.array(temps, np.float32), B))
 
 
-def test_hand_cases():
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+def test_hand_cases(opts):
     g = json.load(open(os.path.join(HERE, "golden", "tree_v4.json")))
     lt = np.log(np.array(g["target_p"])).astype(np.float32)[None]
     for c in g["cases"]:
         t = dict(target=lt, tokens=np.array([g["tokens"]], np.int32), parents=np.array([g["parents"]], np.int32),
                  m=np.array([g["m"]], np.int32), ua=np.array([c["u_accept"]], np.float32),
                  us=np.array([c["u_sample"]], np.float32), T=np.array([c["T"]], np.float32))
-        gpu = run_gpu(t)
+        gpu = run_gpu(t, **opts)
         assert gpu["out_tokens"][0].tolist() == c["out"] and gpu["n"][0] == c["n"], c["name"]
         assert gpu["nodes"][0].tolist() == c["nodes"], c["name"]
 
 
+@pytest.mark.parametrize("opts", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("B,G,V,dtype", [(64, 8, 64, "f32"), (64, 16, 4096, "bf16"), (48, 12, 2000, "f32"),
                                          (32, 60, 32000, "bf16")])
-def test_random_trees(B, G, V, dtype):
+def test_random_trees(B, G, V, dtype, opts):
     t = random_trees(B, G, V, dtype, seed=B * 1000 + G)
-    gpu = run_gpu(t)
+    gpu = run_gpu(t, **opts)
     ties = compare(t, gpu)
     assert ties <= B // 4
     assert (gpu["n"] > 0).sum() > B // 8  # walks that go below the root
 
 
-def test_output_follows_p():
-    """Three children of the root: child k is accepted with probability p(x_k)
-    and the first token follows p (chi-square, V = 8, 2e5 trials)."""
-    from scipy import special, stats
-    N = 200000
+def test_eagle_sized_batch_streaming():
+    """The bench's tree workload shape (bf16, V = 32000, 60 nodes) at B = 256:
+    the streaming kernel against the oracle, request by request."""
+    t = random_trees(256, 60, 32000, "bf16", seed=606)
+    gpu = run_gpu(t, **STREAM)
+    ties = compare(t, gpu)
+    assert ties <= 256 // 4
+
+
+def _root_children(N, seed):
     rng = np.random.Generator(np.random.Philox(77))
     rows = rng.normal(0, 1.2, (4, 8)).astype(np.float32)
+    from scipy import special
     p0 = special.softmax(rows[0].astype(np.float64))
     kids = np.argsort(p0)[[6, 3, 5]].astype(np.int32)
+    rng = np.random.Generator(np.random.Philox(seed))
     t = dict(target=np.ascontiguousarray(np.broadcast_to(rows, (N, 4, 8))), tokens=np.tile(kids, (N, 1)),
              parents=np.zeros((N, 3), np.int32), m=np.full(N, 3, np.int32), ua=rng.random((N, 3), dtype=np.float32),
              us=rng.random(N, dtype=np.float32), T=np.ones(N, np.float32))
-    gpu = run_gpu(t)
+    return t, p0, kids
+
+
+@pytest.mark.parametrize("opts,calls,N", [(ROWWISE, 1, 200000), (STREAM, 49, 4096)], ids=["rowwise", "stream"])
+def test_output_follows_p(opts, calls, N):
+    """Three children of the root: child k is accepted with probability p(x_k)
+    and the first token follows p (chi-square, V = 8, ~2e5 trials)."""
+    from scipy import stats
+    node_counts = np.zeros(3)
+    counts = np.zeros(8)
+    total = 0
+    for i in range(calls):
+        t, p0, kids = _root_children(N, 900 + i)
+        gpu = run_gpu(t, **opts)
+        node_counts += [(gpu["nodes"][:, 0] == k + 1).sum() for k in range(3)]
+        counts += np.bincount(gpu["out_tokens"][:, 0], minlength=8)
+        total += N
     for k in range(3):
-        rate = (gpu["nodes"][:, 0] == k + 1).mean()
+        rate = node_counts[k] / total
         pk = p0[kids[k]]
-        assert abs(rate - pk) < 5 * np.sqrt(pk * (1 - pk) / N), (k, rate, pk)
-    counts = np.bincount(gpu["out_tokens"][:, 0], minlength=8)
-    chi2 = float(((counts - N * p0) ** 2 / (N * p0)).sum())
+        assert abs(rate - pk) < 5 * np.sqrt(pk * (1 - pk) / total), (k, rate, pk)
+    chi2 = float(((counts - total * p0) ** 2 / (total * p0)).sum())
     assert chi2 < stats.chi2.isf(1e-3, 7), chi2
 
 
-def test_invalid_trees():
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+def test_invalid_trees(opts):
     t = random_trees(8, 4, 64, "f32", seed=3, temps=(1.0,))
     t["m"][:] = 4
     t["parents"][1, 2] = 3  # not an earlier node
     t["tokens"][2, 1] = 64  # out of range
     t["m"][3] = 5           # more nodes than gamma
     t["target"][4, 3, 2] = np.nan
-    gpu = run_gpu(t)
+    gpu = run_gpu(t, **opts)
     assert np.all(gpu["n"][1:5] == -1) and np.all(gpu["n"][[0, 5, 6, 7]] >= 0)
     assert gpu["status"] & sv.SV_STATUS_BAD_REQUEST
     compare(t, gpu)
+
+
+def test_tree_options_checked():
+    """early_exit has no meaning for a tree: the call refuses it."""
+    import ctypes
+    t = random_trees(4, 4, 64, "f32", seed=5)
+    lib = sv.load()
+    o = sv._Options(0, 0, 0, 1, None, None)
+    z = _dev(np.zeros(64, np.int32))
+    rc = lib.spec_verify_tree(sv._ptr(_dev(t["target"])), sv.SV_F32, 4, 4, 64, sv._ptr(_dev(t["tokens"])),
+                              sv._ptr(_dev(t["parents"])), sv._ptr(_dev(t["m"])), sv._ptr(_dev(t["ua"])),
+                              sv._ptr(_dev(t["us"])), sv._ptr(_dev(t["T"])), sv._ptr(z), sv._ptr(z), None, None, 0,
+                              None, None, None, ctypes.byref(o))
+    assert rc == sv.SV_ERR_INVALID_ARG
