@@ -143,7 +143,7 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.ee_cap = B * (gamma + 2);
     L.ee_tasks = take(static_cast<size_t>(L.ee_cap) * 4);  // published tasks (encoded + 1)
     L.ee_done = take(static_cast<size_t>(L.ee_cap) * 4);   // chunks done, per task
-    L.clear_bytes = off;                                   // cleared before every launch
+    L.clear_bytes = off;  // cleared before every launch (up to ee_tasks without early exit)
     L.rec_t = take(static_cast<size_t>(G) * L.MT * sizeof(Rec));
     L.rec_d = take(static_cast<size_t>(G) * L.MD * sizeof(Rec));
     L.ee_rec = take(static_cast<size_t>(L.ee_cap) * L.NCH * 2 * sizeof(Rec));  // per (task, chunk): target, draft
@@ -442,8 +442,10 @@ struct Kern {
         if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(&ctl.empty[slot], (round - 1) & 1))) return false;
         // a tree draw's excluded tokens travel with the stage (written by
         // another block's finisher: read from L2)
-        for (int i = threadIdx.x & 31; i < nset; i += 32) ctl.dset[slot][i] = __ldcg(set + i);
-        __syncwarp();
+        if (nset > 0) {
+            for (int i = threadIdx.x & 31; i < nset; i += 32) ctl.dset[slot][i] = __ldcg(set + i);
+            __syncwarp();
+        }
         if ((threadIdx.x & 31) == 0) {
             if (desc) ctl.desc[slot] = *desc;
             if (src) {
@@ -1312,6 +1314,19 @@ struct Kern {
         return run_total(S);
     }
 
+    // run_total_rotated with the draw kind a compile-time constant: one
+    // straight-line body per kind, chosen once per stage.
+    __device__ static __forceinline__ float run_total_by_kind(const Run& rt, const Run& rd, int t, int valid,
+                                                              const DrawParams& d, int kind, int first,
+                                                              const int* set) {
+        switch (kind) {
+            case kKindResidual: return run_total_rotated(rt, rd, t, valid, d, kKindResidual, first, set);
+            case kKindResidualOnehot: return run_total_rotated(rt, rd, t, valid, d, kKindResidualOnehot, first, set);
+            case kKindResidualTree: return run_total_rotated(rt, rd, t, valid, d, kKindResidualTree, first, set);
+            default: return run_total_rotated(rt, rd, t, valid, d, kKindBonus, first, set);
+        }
+    }
+
     // A run from global memory starting at element `e` (64-byte aligned in the
     // row); its first `valid` tokens are whole 16-byte vectors because rows
     // end on 16-byte boundaries. The rest is zero.
@@ -1805,8 +1820,8 @@ struct Kern {
                     if (ds.job.kind == kKindResidual) load_run_smem(smt + kChunkBytes, t, ld);
                 }
                 consume_end(cons);
-                const float run = valid > 0 ? run_total_rotated(lt, ld, t, valid, ds.job.d, ds.job.kind,
-                                                                static_cast<int>(e0) + t * TPT)
+                const float run = valid > 0 ? run_total_by_kind(lt, ld, t, valid, ds.job.d, ds.job.kind,
+                                                                static_cast<int>(e0) + t * TPT, nullptr)
                                             : 0.0f;
                 const unsigned long long wsum = warp_sum_u64(to_fixed(run, ds.job.d.fix));
                 if (lane == 0) {
@@ -2284,7 +2299,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             // released after the weights
             const bool tree = ds.job.kind == kKindResidualTree;
             if (!tree) K.consume_end(cons);
-            const float run = valid > 0 ? KT::run_total_rotated(lt, ld, t, valid, ds.job.d, ds.job.kind,
+            const float run = valid > 0 ? KT::run_total_by_kind(lt, ld, t, valid, ds.job.d, ds.job.kind,
                                                                 static_cast<int>(e0) + t * TPT, ctl.dset[slot])
                                         : 0.0f;
             if (tree) K.consume_end(cons);
@@ -2416,7 +2431,7 @@ cudaError_t launch_streaming(const Args& a, const DeviceInfo& dev, int grid, voi
     }
     if (grid > dev.num_sms) return cudaErrorInvalidValue;
     // the barrier words and the completion counters start at zero
-    cudaError_t e = cudaMemsetAsync(workspace, 0, L.clear_bytes, stream);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, a.early ? L.clear_bytes : L.ee_tasks, stream);
     if (e != cudaSuccess) return e;
     Args args = a;
     Layout lay = L;
