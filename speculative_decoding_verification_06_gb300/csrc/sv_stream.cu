@@ -217,6 +217,23 @@ __device__ __forceinline__ void red_release_add(unsigned* addr, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }
 
+// Polled words in global memory are read and written with device-scope
+// relaxed accesses (a volatile access has system scope, more than these
+// words need); the orderings they need come from explicit fences.
+__device__ __forceinline__ int ld_relaxed(const int* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed(int* p, int v) {
+    asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
@@ -491,7 +508,7 @@ struct Kern {
     __device__ void publish(int k) const {
         __threadfence();
         const unsigned p = atomicAdd(&hdr()->n_pub, 1u);
-        reinterpret_cast<volatile int*>(ready())[p] = k + 1;
+        st_relaxed(ready() + p, k + 1);
     }
 
     // Finisher warp: the token searches of the jobs published at positions
@@ -506,7 +523,7 @@ struct Kern {
             const int ns = *reinterpret_cast<const volatile int*>(&ctl.n_samp);
             if (own_p < ns) {
                 if (own_k < 0) {
-                    const int v = reinterpret_cast<const volatile int*>(ready())[own_p];
+                    const int v = ld_relaxed(ready() + own_p);
                     if (v) {
                         __threadfence();
                         own_k = v - 1;
@@ -520,7 +537,7 @@ struct Kern {
                     }
                 }
                 if (own_k >= 0 &&
-                    reinterpret_cast<const volatile unsigned*>(job_done())[own_k] == static_cast<unsigned>(L.NCH)) {
+                    ld_relaxed(job_done() + own_k) == static_cast<unsigned>(L.NCH)) {
                     __threadfence();  // the other blocks' chunk sums before they are read
                     k = own_k;
                     own_p += G;
@@ -1575,7 +1592,7 @@ struct Kern {
         __threadfence();
         const unsigned q = atomicAdd(&hdr()->n_pub, 1u);
         if (static_cast<long long>(a.B) + q < static_cast<long long>(L.ee_cap))  // always: at most gamma + 1 per request
-            reinterpret_cast<volatile int*>(ee_tasks())[a.B + q] = ee_encode(type, b, pos);
+            st_relaxed(ee_tasks() + a.B + q, ee_encode(type, b, pos));
     }
 
     // One lane: request b is done (its outputs are written).
@@ -1588,10 +1605,10 @@ struct Kern {
     // published tasks end before p).
     __device__ bool ee_no_task(int p) const {
         if (p >= L.ee_cap) return true;
-        if (*reinterpret_cast<volatile unsigned*>(&hdr()->n_fin) < static_cast<unsigned>(a.B)) return false;
+        if (ld_relaxed(&hdr()->n_fin) < static_cast<unsigned>(a.B)) return false;
         __threadfence();
         return static_cast<long long>(p) >=
-               static_cast<long long>(a.B) + *reinterpret_cast<volatile unsigned*>(&hdr()->n_pub);
+               static_cast<long long>(a.B) + ld_relaxed(&hdr()->n_pub);
     }
 
     __device__ void start_row_mode(RowState& rs, bool argmax, float c) const {
@@ -1706,9 +1723,9 @@ struct Kern {
                     } else if (p >= L.ee_cap) {
                         state = 0;
                     } else {
-                        const volatile int* tp = ee_tasks() + p;
+                        const int* tp = ee_tasks() + p;
                         const unsigned long long t0 = global_ns();
-                        while ((v = *tp) == 0) {
+                        while ((v = ld_relaxed(tp)) == 0) {
                             if (ee_no_task(p)) {
                                 state = 0;
                                 break;
@@ -2018,7 +2035,7 @@ struct Kern {
                 if (own_p < a.B) {
                     own_v = ee_encode(kTaskStats, own_p, 0);
                 } else {
-                    const int v = reinterpret_cast<const volatile int*>(ee_tasks())[own_p];
+                    const int v = ld_relaxed(ee_tasks() + own_p);
                     if (v) {
                         __threadfence();
                         own_v = v;
@@ -2026,7 +2043,7 @@ struct Kern {
                 }
             }
             if (own_v != 0 &&
-                reinterpret_cast<const volatile unsigned*>(ee_done())[own_p] >= static_cast<unsigned>(L.NCH)) {
+                ld_relaxed(ee_done() + own_p) >= static_cast<unsigned>(L.NCH)) {
                 __threadfence();  // the other blocks' chunk records and sums
                 act_p = own_p;
                 act_v = own_v;
@@ -2140,7 +2157,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             // batch is requested while the current one is issued)
             if (a.hold_flag && ok && lane == 0) {  // checking only: a flag that holds the draw phase
                 const unsigned long long t0 = global_ns();
-                while (*reinterpret_cast<const volatile int32_t*>(a.hold_flag) == 0) {
+                while (ld_relaxed(a.hold_flag) == 0) {
                     if (global_ns() - t0 > a.peer_wait_ns) {
                         K.set_abort(a.d_status);
                         break;
@@ -2171,11 +2188,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                     // finisher of the block that completes its request)
                     int got = 1;
                     if (lane == 0) {
-                        const volatile int* rd = K.ready();
-                        int v = rd[p];
+                        int v = ld_relaxed(K.ready() + p);
                         if (v == 0) {
                             const unsigned long long t0 = global_ns();
-                            while ((v = rd[p]) == 0) {
+                            while ((v = ld_relaxed(K.ready() + p)) == 0) {
                                 if (*vabort || global_ns() - t0 > a.peer_wait_ns) {
                                     got = 0;
                                     break;
