@@ -76,6 +76,7 @@ struct Rec {
     int32_t idx;  // argmax (argmax mode)
     int32_t bad;  // NaN or +inf seen
 };
+constexpr uint32_t kNoPiece = 0xffffffffu;  // Rec.bad of a piece that does not exist
 
 struct Job {
     int32_t b, n, kind, pad;  // request, the draw's row, kind, u_sample bits
@@ -888,42 +889,57 @@ struct Kern {
         rs.s = __fadd_rn(rs.s, __fadd_rn(a0, a1));
     }
 
-    // ---- acceptance scan: merge of a row's pieces, in block and warp order
-    __device__ Rec merge_row(int kind, long long row, bool argmax, float c) const {
+    // ---- acceptance scan: merge of a row's pieces, in block and warp order.
+    // The records of a row's first two pieces are read first (row_load) and
+    // merged once the request's temperature is known (row_combine); a row
+    // over more slices reads the rest then.
+    struct RowRaw {
+        uint4 x[2];
+        int g0, g1;
+    };
+    __device__ void row_load(int kind, long long row, RowRaw& rr) const {
         const long long* beg = kind == 0 ? ctl.tbeg : ctl.dbeg;
         const int MM = kind == 0 ? L.MT : L.MD;
         const Rec* base = kind == 0 ? rec_t() : rec_d();
         const long long e0 = row * a.V, e1 = e0 + a.V - 1;
-        const int g0 = owner(beg, G, e0), g1 = owner(beg, G, e1);
+        rr.g0 = owner(beg, G, e0);
+        rr.g1 = owner(beg, G, e1);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int gg = rr.g0 + q;
+            rr.x[q] = make_uint4(0u, 0u, 0u, kNoPiece);
+            if (gg <= rr.g1) {
+                const long long b0 = beg[gg], b1 = beg[gg + 1];
+                if (b1 > b0)
+                    rr.x[q] = __ldcg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(gg) * MM +
+                                                                    static_cast<int>(row - b0 / a.V)));
+            }
+        }
+    }
+    __device__ Rec row_combine(int kind, long long row, const RowRaw& rr, bool argmax, float c) const {
         MaxSum ms = maxsum_empty();
         ArgMax am = argmax_empty();
         int bad = 0;
-        constexpr int kBatch = 4;  // piece records loaded before they are merged
-        for (int gb = g0; gb <= g1; gb += kBatch) {
-            uint4 x[kBatch];
-            bool use[kBatch];
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-                const int gg = gb + q;
-                use[q] = false;
-                if (gg <= g1) {
-                    const long long b0 = beg[gg], b1 = beg[gg + 1];
-                    if (b1 > b0) {
-                        const int slot = static_cast<int>(row - b0 / a.V);
-                        x[q] = __ldcg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(gg) * MM + slot));
-                        use[q] = true;
-                    }
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-                if (!use[q]) continue;
-                const float m = __uint_as_float(x[q].x), s = __uint_as_float(x[q].y);
-                bad |= static_cast<int>(x[q].w);
-                if (argmax)
-                    am = argmax_merge(am, ArgMax{m, static_cast<int32_t>(x[q].z)});
-                else
-                    ms = maxsum_merge(ms, MaxSum{m, s}, c);
+        auto take = [&](const uint4& x) {
+            if (x.w == kNoPiece) return;
+            const float m = __uint_as_float(x.x), s = __uint_as_float(x.y);
+            bad |= static_cast<int>(x.w);
+            if (argmax)
+                am = argmax_merge(am, ArgMax{m, static_cast<int32_t>(x.z)});
+            else
+                ms = maxsum_merge(ms, MaxSum{m, s}, c);
+        };
+        take(rr.x[0]);
+        take(rr.x[1]);
+        if (rr.g1 > rr.g0 + 1) {
+            const long long* beg = kind == 0 ? ctl.tbeg : ctl.dbeg;
+            const int MM = kind == 0 ? L.MT : L.MD;
+            const Rec* base = kind == 0 ? rec_t() : rec_d();
+            for (int gg = rr.g0 + 2; gg <= rr.g1; ++gg) {
+                const long long b0 = beg[gg], b1 = beg[gg + 1];
+                if (b1 > b0)
+                    take(__ldcg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(gg) * MM +
+                                                               static_cast<int>(row - b0 / a.V))));
             }
         }
         Rec out;
@@ -933,41 +949,52 @@ struct Kern {
             out = {ms.m, ms.s, -1, (bad || ms.m == neg_inf()) ? 1 : 0};
         return out;
     }
+    __device__ Rec merge_row(int kind, long long row, bool argmax, float c) const {
+        RowRaw rr;
+        row_load(kind, row, rr);
+        return row_combine(kind, row, rr, argmax, c);
+    }
 
     // Acceptance scan of request b on one warp (the finisher); `st` is its
     // shared scratch of 2 gamma + 1 row records.
     __device__ void verify_request(int b, Rec* st) const {
         const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V;
+        const int k = ctl.kmap[b];  // compacted index of a T > 0 request, else -1
+        const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
+        const bool onehot = a.onehot;
+        // The reads come in two rounds. First everything that depends on no
+        // other read: the temperature, the proposal count, this lane's token
+        // and uniform, and the first two piece records of rows `lane` and
+        // `lane + 32` (rows numbered target 0..gamma, then draft
+        // gamma+1..2 gamma). Then the logits at this lane's token, which need
+        // only the token (read even when the request turns out greedy).
         const float T = a.temperature[b];
+        // proposals of this request: gamma, or num_draft[b] for one-hot proposals
+        // (whose rows past it take no part)
+        const int kb = onehot && a.num_draft ? a.num_draft[b] : GM;
+        const int x_l = lane < GM ? tok[lane] : -1;
+        const float u_l = lane < GM ? a.u_accept[static_cast<size_t>(b) * GM + lane] : 0.0f;
+        const int nrows_max = (k >= 0 && !onehot) ? 2 * GM + 1 : GM + 1;
+        auto row_of = [&](int r) -> long long {
+            return r <= GM ? static_cast<long long>(b) * (GM + 1) + r : static_cast<long long>(k) * GM + (r - GM - 1);
+        };
+        RowRaw raw0, raw1;
+        if (lane < nrows_max) row_load(lane <= GM ? 0 : 1, row_of(lane), raw0);
+        if (lane + 32 < nrows_max) row_load(lane + 32 <= GM ? 0 : 1, row_of(lane + 32), raw1);
+        float lt_l = 0.0f, ld_l = 0.0f;
+        if (!a.tree && x_l >= 0 && x_l < V) {
+            lt_l = load_logit<DT>(a.target, (static_cast<size_t>(b) * (GM + 1) + lane) * V + x_l);
+            if (k >= 0 && !onehot) ld_l = load_logit<DT>(a.draft, (static_cast<size_t>(b) * GM + lane) * V + x_l);
+        }
         const bool t_ok = (T >= 0.0f) && (T < pos_inf());
         const bool greedy = t_ok && T == 0.0f;
         const bool samp = sampled(T);
         const float c = samp ? temp_scale(T) : 0.0f;
-        const int k = ctl.kmap[b];
-        const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
-        // proposals of this request: gamma, or num_draft[b] for one-hot proposals
-        // (whose rows past it take no part)
-        const int kb = a.onehot && a.num_draft ? a.num_draft[b] : GM;
-        const bool onehot = a.onehot;
         const bool range_ok = t_ok && kb >= 0 && kb <= GM;
         int bad = range_ok ? 0 : 1;
         const int np = range_ok ? kb : 0;
-        // this lane's first position (gamma <= 32 in one pass): its token, the
-        // gathered logits and the uniform are loaded before the row merges
-        int x0 = 0;
-        float lt0 = 0.0f, ld0 = 0.0f, u0 = 0.0f;
-        if (lane < np && !a.tree) {
-            x0 = tok[lane];
-            if (!greedy && x0 >= 0 && x0 < V) {
-                const size_t tr = static_cast<size_t>(b) * (GM + 1) + lane;
-                const size_t dr = static_cast<size_t>(b) * GM + lane;
-                lt0 = load_logit<DT>(a.target, tr * V + x0);
-                if (!onehot) ld0 = load_logit<DT>(a.draft, dr * V + x0);
-                u0 = a.u_accept[dr];
-            }
-        }
         for (int i = lane; i < np; i += 32) {
-            const int x = tok[i];
+            const int x = i < 32 ? x_l : tok[i];
             if (x < 0 || x >= V) bad = 1;
             if (a.tree) {  // node i + 1's parent is an earlier node
                 const int par = a.parents[static_cast<size_t>(b) * GM + i];
@@ -976,11 +1003,15 @@ struct Kern {
         }
         const int nrows = !range_ok ? 0 : (samp && !onehot ? 2 * GM + 1 : np + 1);
         for (int r = lane; r < nrows; r += 32) {
+            const int kind = r <= GM ? 0 : 1;
+            const bool am = kind == 0 && !samp;
             Rec x;
-            if (r <= GM)
-                x = merge_row(0, static_cast<long long>(b) * (GM + 1) + r, !samp, c);
+            if (r == lane)
+                x = row_combine(kind, row_of(r), raw0, am, c);
+            else if (r == lane + 32)
+                x = row_combine(kind, row_of(r), raw1, am, c);
             else
-                x = merge_row(1, static_cast<long long>(k) * GM + (r - GM - 1), false, c);
+                x = merge_row(kind, row_of(r), am, c);
             st[r] = x;
             bad |= x.bad;
         }
@@ -1040,15 +1071,15 @@ struct Kern {
             const int i = base + lane;
             bool fail = false;
             if (i < np) {
-                const int x = tok[i];
+                const int x = base == 0 ? x_l : tok[i];
                 if (greedy) {
                     fail = x != st[i].idx;
                 } else {
                     const size_t tr = static_cast<size_t>(b) * (GM + 1) + i;
                     const size_t dr = static_cast<size_t>(b) * GM + i;
                     const bool pre_loaded = base == 0;
-                    const float lt = pre_loaded ? lt0 : load_logit<DT>(a.target, tr * V + x);
-                    const float u = pre_loaded ? u0 : a.u_accept[dr];
+                    const float lt = pre_loaded ? lt_l : load_logit<DT>(a.target, tr * V + x);
+                    const float u = pre_loaded ? u_l : a.u_accept[dr];
                     if (dbg.p_x) dbg.p_x[dr] = prob_from_stats(lt, st[i].m, st[i].s, c);
                     if (onehot) {
                         // q(x) = 1: the draft side of the test is a row whose only
@@ -1056,7 +1087,7 @@ struct Kern {
                         if (dbg.q_x) dbg.q_x[dr] = 1.0;
                         fail = !accept_from_logits(lt, 0.0f, st[i].m, st[i].s, 0.0f, 1.0f, c, u);
                     } else {
-                        const float ld = pre_loaded ? ld0 : load_logit<DT>(a.draft, dr * V + x);
+                        const float ld = pre_loaded ? ld_l : load_logit<DT>(a.draft, dr * V + x);
                         if (dbg.q_x) dbg.q_x[dr] = prob_from_stats(ld, st[GM + 1 + i].m, st[GM + 1 + i].s, c);
                         fail = !accept_from_logits(lt, ld, st[i].m, st[i].s, st[GM + 1 + i].m, st[GM + 1 + i].s,
                                                    c, u);
