@@ -5,9 +5,9 @@
 // and eq. p_corr; "Accélérer Sonar grâce à la spéculation", §Décodage
 // spéculatif) needs, per request, the normaliser (or argmax) of gamma+1
 // target rows and gamma draft rows, a left-to-right scan, and one draw over a
-// row that is known only after the scan. Each block has eight consumer warps,
-// one producer warp and one finisher warp, and the kernel runs two streaming
-// phases with one grid barrier between them (none when no request samples):
+// row that is known only after the scan. Each block has twelve consumer
+// warps, one producer warp, one finisher warp and one search warp; there is
+// no grid barrier.
 //
 //  1. Row statistics. The target rows of all requests, then the draft rows of
 //     the T > 0 requests (compacted), form one virtual stream of logits that
@@ -21,21 +21,21 @@
 //     request's global count of folded logits, and the block that completes
 //     the count runs the request's acceptance scan at once, while the other
 //     blocks are still streaming: it merges the pieces of each row in a fixed
-//     order, finds the first rejection, writes the accepted tokens and a draw
-//     job.
-//  2. Draw. The rows the draws need (target row n and draft row n for a
-//     residual, target row gamma for the extra token) are streamed again in
-//     chunks of kChunkBytes; each thread sums the weights of a run of
-//     consecutive tokens and each warp stores the sum of its 32 runs as a
-//     64-bit fixed-point integer (exact, so any order of addition gives the
-//     same prefix sums). A block's share of a job is counted the same way,
-//     and the finisher of the block that completes a job finds the chunk,
-//     then the warp, then the run holding u * W, re-reads those 32 runs and
-//     finds the token.
+//     order, finds the first rejection, writes the accepted tokens and
+//     publishes a draw job.
+//  2. Draw. After its slice, a block's producer takes draw items (a job in
+//     publication order, a chunk of kChunkBytes of the row it needs: target
+//     row n and draft row n for a residual, target row n otherwise) from a
+//     global counter; each thread sums the weights of a run of consecutive
+//     tokens and each warp stores the sum of its 32 runs as a 64-bit
+//     fixed-point integer (exact, so any order of addition gives the same
+//     prefix sums). A job's chunks are counted in global memory, and the
+//     search warp of the block that owns the job finds the chunk, then the
+//     warp, then the run holding u * W, re-reads those 32 runs and finds the
+//     token.
 //
-// Every wait is bounded (about two seconds, by the global timer): a barrier,
-// a stage or a message that never comes sets SV_STATUS_TIMEOUT and the kernel
-// returns.
+// Every wait is bounded (about two seconds, by the global timer): a stage or
+// a message that never comes sets SV_STATUS_TIMEOUT and the kernel returns.
 #include <algorithm>
 #include <cmath>
 
@@ -48,8 +48,9 @@ namespace {
 constexpr int kConsumerWarps = 12;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;      // issues the bulk copies
-constexpr int kFinisherWarp = kConsumerWarps + 1;  // acceptance scans and token searches
-constexpr int kThreads = kConsumers + 64;
+constexpr int kFinisherWarp = kConsumerWarps + 1;  // counts, acceptance scans
+constexpr int kSearchWarp = kConsumerWarps + 2;    // token searches of the jobs this block owns
+constexpr int kThreads = kConsumers + 96;
 constexpr int kHandoffThreads = kConsumers + 32;   // consumers + producer
 constexpr int kQueue = 256;                        // finisher message ring (slots)
 constexpr int kStages = 4;
@@ -512,7 +513,7 @@ struct Kern {
         st_relaxed(ready() + p, k + 1);
     }
 
-    // Finisher warp: the token searches of the jobs published at positions
+    // Search warp: the token searches of the jobs published at positions
     // g, g + G, g + 2G, ... belong to block g, so that consecutive jobs, which
     // complete at about the same time, are searched by different blocks. Lane
     // 0 keeps the next owned position (own_p) and its job once published
@@ -2108,7 +2109,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     using KT = Kern<DT>;
     KT K{a, L, ws, ctl, stages, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x)};
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const bool producer = warp == kProducerWarp, finisher = warp == kFinisherWarp;
+    const bool producer = warp == kProducerWarp, finisher = warp == kFinisherWarp, searcher = warp == kSearchWarp;
     unsigned long long* ph = reinterpret_cast<unsigned long long*>(a.dbg.phase_ns);
     stamp(ph, 0, t == 0);
 
@@ -2132,12 +2133,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     // ------------------------------------------------------------ finisher
     if (finisher) {
         // a request is scanned by the block whose share completes its 2 gamma + 1
-        // rows (gamma + 1 at T = 0); a draw job is searched by the block that
-        // sums its last chunk
+        // rows (gamma + 1 at T = 0); a draw job's chunks are counted here and
+        // the job is searched by its owner's search warp
         const unsigned V = static_cast<unsigned>(a.V), GM = static_cast<unsigned>(a.gamma);
         unsigned* req_done = K.req_done();
         unsigned* job_done = K.job_done();
-        int own_p = blockIdx.x, own_k = -1;  // lane 0: next owned job position, its job
         K.finish(
             [&](int item, unsigned share) {
                 if (item & kJobMsg) {
@@ -2158,7 +2158,38 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                     stamp(ph, 3, lane == 0);
                 }
             },
-            [&]() { return K.poll_owned(own_p, own_k); }, [&]() { return own_p >= ctl.n_samp; });
+            [&]() { return false; }, [&]() { return true; });
+        stamp(ph, 9, lane == 0);
+        return;
+    }
+
+    // ------------------------------------------------------------ searcher
+    if (searcher) {
+        // the jobs published at positions g, g + G, ...: searched as soon as
+        // their last chunk is counted, beside the finisher's scans
+        int own_p = blockIdx.x, own_k = -1;  // lane 0: next owned job position, its job
+        volatile int* vab = &ctl.abort;
+        unsigned long long t0 = global_ns();
+        for (;;) {
+            if (K.poll_owned(own_p, own_k)) {
+                t0 = global_ns();
+                continue;
+            }
+            int stop = 0;
+            if (lane == 0) {
+                const int ns = *reinterpret_cast<volatile int*>(&ctl.n_samp);  // -1 until the consumers' prologue
+                if (*vab) {
+                    stop = 1;
+                } else if (ns >= 0 && own_p >= ns) {
+                    stop = 1;
+                } else if (global_ns() - t0 > kWaitTimeoutNs) {
+                    K.set_abort(a.d_status);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            __nanosleep(100);
+        }
         stamp(ph, 9, lane == 0);
         return;
     }
@@ -2400,6 +2431,7 @@ __global__ void __launch_bounds__(kThreads, 1) early_kernel(Args a, Layout L, ch
     __syncthreads();
 
     typename KT::Cursor prod, cons;
+    if (warp == kSearchWarp) return;  // the early-exit finisher searches its own draws
     if (warp == kFinisherWarp) {
         int own_p = blockIdx.x, own_v = 0;  // lane 0: next owned task, its code once published
         unsigned* done = K.ee_done();
