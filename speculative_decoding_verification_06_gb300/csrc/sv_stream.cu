@@ -1415,6 +1415,7 @@ struct Kern {
         // loaded together with the job: they depend on k only
         const int nch_lane = (L.NCH + 31) / 32;
         unsigned long long ctot[4];
+        unsigned long long wp0[kConsumerWarps];  // per-warp sums of chunk `lane` (kept: the search's next step)
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
             const int j = h * 32 + lane;
@@ -1425,10 +1426,21 @@ struct Kern {
                 for (int hh = 0; hh < kConsumerWarps / 2; ++hh) {
                     const ulonglong2 x = __ldcg(p + hh);
                     sum += x.x + x.y;
+                    if (h == 0) {
+                        wp0[2 * hh] = x.x;
+                        wp0[2 * hh + 1] = x.y;
+                    }
                 }
+            } else if (h == 0) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) wp0[w] = 0ull;
             }
             ctot[h] = sum;
         }
+        // a tree draw's excluded tokens, read in the same round (gamma <= 64)
+        const int* gset = jobset() + static_cast<size_t>(k) * a.gamma;
+        const int set0 = lane < a.gamma ? __ldcg(gset + lane) : 0;
+        const int set1 = lane + 32 < a.gamma ? __ldcg(gset + lane + 32) : 0;
         // the job comes from L2: it was written by another block, and a job
         // sharing its cache line may have been read here earlier
         Job jb;
@@ -1442,7 +1454,8 @@ struct Kern {
             jb.kind != kKindResidualTree)
             return;
         if (jb.kind == kKindResidualTree) {
-            for (int i = lane; i < jb.d.excl; i += 32) ctl.fset[i] = __ldcg(jobset() + static_cast<size_t>(k) * a.gamma + i);
+            if (lane < jb.d.excl) ctl.fset[lane] = set0;
+            if (lane + 32 < jb.d.excl) ctl.fset[lane + 32] = set1;
             __syncwarp();
         }
         const int* set = ctl.fset;
@@ -1515,7 +1528,14 @@ struct Kern {
         // the warp of that chunk: lanes 0..7 hold its per-warp sums (on the
         // fallback warp_part is warp-collective, so every lane calls it)
         unsigned long long part = 0ull;
-        if (!fallback) {
+        if (!fallback && jsel < 32) {
+            // held by lane jsel since the first round
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const unsigned long long v = __shfl_sync(0xffffffffu, wp0[w], jsel);
+                if (lane == w) part = v;
+            }
+        } else if (!fallback) {
             if (lane < kConsumerWarps) part = __ldcg(js + static_cast<size_t>(jsel) * kConsumerWarps + lane);
         } else {
             for (int w = 0; w < kConsumerWarps; ++w) {
