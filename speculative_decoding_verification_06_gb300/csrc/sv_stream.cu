@@ -787,13 +787,14 @@ struct Kern {
         }
     }
 
-    // Folds one stage (nvec 16-byte vectors, element offset e0 in the row).
-    // Full stages (the common case) take a path without per-vector bounds.
-    // NV vectors of 16 bytes per consumer thread: a phase-1 stage (kVecPerThread)
-    // or one draw-sized chunk of a row (kVecPerThread / 2, early exit).
+    // This thread's NV vectors of a stage (nvec 16-byte vectors; -inf past
+    // them): a phase-1 stage (kVecPerThread) or one draw-sized chunk of a row
+    // (kVecPerThread / 2, early exit). Full stages take a path without
+    // per-vector bounds. Callers release the stage as soon as these are in
+    // registers and fold them afterwards (fold_vectors), so that a ring slot
+    // is held only for the copy, not for the arithmetic.
     template <int NV = kVecPerThread>
-    __device__ __forceinline__ void fold_stage(RowState& rs, const char* sm, int nvec, long long e0) const {
-        uint4 v[NV];
+    __device__ __forceinline__ static void load_stage(const char* sm, int nvec, uint4 (&v)[NV]) {
         const int t = threadIdx.x;
         if (nvec == NV * kConsumers) {
 #pragma unroll
@@ -811,7 +812,6 @@ struct Kern {
                     v[k] = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
             }
         }
-        fold_vectors<NV>(rs, v, e0);
     }
 
     template <int NV>
@@ -1877,9 +1877,12 @@ struct Kern {
                 RowState rt, rd;
                 start_row_mode(rt, argmax, ds.job.d.c);
                 start_row_mode(rd, false, ds.job.d.c);
-                fold_stage<NVC>(rt, smt, n * ES / 16, e0);
-                if (has_draft) fold_stage<NVC>(rd, smt + kChunkBytes, n * ES / 16, e0);
+                uint4 vt[NVC], vd[NVC];
+                load_stage<NVC>(smt, n * ES / 16, vt);
+                if (has_draft) load_stage<NVC>(smt + kChunkBytes, n * ES / 16, vd);
                 consume_end(cons);
+                fold_vectors<NVC>(rt, vt, e0);
+                if (has_draft) fold_vectors<NVC>(rd, vd, e0);
                 ee_flush_item(rt, rd, has_draft, iseq, ds.k, ds.j);
             } else {
                 const int valid = max(0, min(TPT, n - t * TPT));
@@ -2357,8 +2360,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                 K.set_abort(a.d_status);
                 return;
             }
-            K.fold_stage(rs, sm, static_cast<int>(n * KT::ES / 16), sg.e0 + off);
+            uint4 v[kVecPerThread];
+            KT::load_stage(sm, static_cast<int>(n * KT::ES / 16), v);
             K.consume_end(cons);
+            K.fold_vectors(rs, v, sg.e0 + off);
         }
         share += static_cast<unsigned>(sg.elems);
         K.flush_row(rs, sg.loc, seq++, sg.last ? share : 0u);
