@@ -335,6 +335,7 @@ struct Ctl {
     short kmap[kMaxB];                      // compacted index of each T > 0 request, else -1
     int dset[kStages][SV_MAX_GAMMA];        // tree draws: the excluded tokens of the item in each stage
     int fset[SV_MAX_GAMMA];                 // tree draws: the excluded tokens of the job being searched
+    int wset[kConsumerWarps][SV_MAX_GAMMA]; // tree draws: each consumer warp's copy of its item's set
 };
 
 struct RowLoc {
@@ -452,17 +453,20 @@ struct Kern {
     // byte offset kChunkBytes); lane 0 issues. In the draw phase lane 0 first
     // writes the stage's descriptor; `src` null with `desc` sends the end
     // marker (the stage completes with no bytes).
+    // `set0`, `set1`: a tree draw's excluded tokens lane and lane + 32 (nset
+    // of them), copied into the stage's descriptor area.
     __device__ bool produce(Cursor& p, const char* src, unsigned bytes, const char* src2 = nullptr,
-                            unsigned bytes2 = 0, const StageDesc* desc = nullptr, const int* set = nullptr,
+                            unsigned bytes2 = 0, const StageDesc* desc = nullptr, int set0 = 0, int set1 = 0,
                             int nset = 0) const {
         const int slot = p.it % kStages;
         const unsigned round = p.it / kStages;
         // the verdict is made warp-uniform so that a timeout cannot split the warp
         if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(&ctl.empty[slot], (round - 1) & 1))) return false;
-        // a tree draw's excluded tokens travel with the stage (written by
-        // another block's finisher: read from L2)
+        // a tree draw's excluded tokens travel with the stage
         if (nset > 0) {
-            for (int i = threadIdx.x & 31; i < nset; i += 32) ctl.dset[slot][i] = __ldcg(set + i);
+            const int lane = threadIdx.x & 31;
+            if (lane < nset) ctl.dset[slot][lane] = set0;
+            if (lane + 32 < nset) ctl.dset[slot][lane + 32] = set1;
             __syncwarp();
         }
         if ((threadIdx.x & 31) == 0) {
@@ -2259,6 +2263,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             int cur_p = -1;
             StageDesc desc;  // lane 0's copy of the current job
             desc.k = -1;
+            int set0 = 0, set1 = 0;  // a tree job's excluded tokens (lane, lane + 32), read once per job
             while (ok && !*vabort) {
                 if (i == i_end) {
                     i = __shfl_sync(0xffffffffu, next, 0);
@@ -2298,6 +2303,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                         ok = false;
                         break;
                     }
+                    if (__shfl_sync(0xffffffffu, desc.job.kind, 0) == kKindResidualTree) {
+                        // written by the finisher that published the job: read from L2
+                        const int* gs = K.jobset() + static_cast<size_t>(__shfl_sync(0xffffffffu, desc.k, 0)) * a.gamma;
+                        set0 = lane < a.gamma ? __ldcg(gs + lane) : 0;
+                        set1 = lane + 32 < a.gamma ? __ldcg(gs + lane + 32) : 0;
+                    }
                     if (cur_p < 0) stamp(ph, 4, lane == 0);
                     cur_p = p;
                 }
@@ -2316,10 +2327,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                         ok = K.produce(prod, src_t, bytes,
                                        static_cast<const char*>(a.draft) + (drow * a.V + e0) * KT::ES, bytes, &desc);
                     } else if (kind == kKindResidualTree) {
-                        const int jk = __shfl_sync(0xffffffffu, desc.k, 0);
                         const int ne = __shfl_sync(0xffffffffu, desc.job.d.excl, 0);
-                        ok = K.produce(prod, src_t, bytes, nullptr, 0u, &desc,
-                                       K.jobset() + static_cast<size_t>(jk) * a.gamma, ne);
+                        ok = K.produce(prod, src_t, bytes, nullptr, 0u, &desc, set0, set1, ne);
                     } else {
                         ok = K.produce(prod, src_t, bytes, nullptr, 0u, &desc);
                     }
@@ -2398,14 +2407,18 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                 KT::load_run_smem(smt, t, lt);
                 if (ds.job.kind == kKindResidual) KT::load_run_smem(smt + kChunkBytes, t, ld);
             }
-            // a tree draw reads its excluded tokens from the stage: the stage is
-            // released after the weights
-            const bool tree = ds.job.kind == kKindResidualTree;
-            if (!tree) K.consume_end(cons);
+            // a tree draw's excluded tokens: this warp's own copy, so that the
+            // stage is released before the weights like the other kinds
+            int* wset = ctl.wset[warp];
+            if (ds.job.kind == kKindResidualTree) {
+                if (lane < ds.job.d.excl) wset[lane] = ctl.dset[slot][lane];
+                if (lane + 32 < ds.job.d.excl) wset[lane + 32] = ctl.dset[slot][lane + 32];
+                __syncwarp();
+            }
+            K.consume_end(cons);
             const float run = valid > 0 ? KT::run_total_by_kind(lt, ld, t, valid, ds.job.d, ds.job.kind,
-                                                                static_cast<int>(e0) + t * TPT, ctl.dset[slot])
+                                                                static_cast<int>(e0) + t * TPT, wset)
                                         : 0.0f;
-            if (tree) K.consume_end(cons);
             const unsigned long long wsum = warp_sum_u64(to_fixed(run, ds.job.d.fix));
             if (lane == 0) {
                 wsums[(static_cast<size_t>(ds.k) * L.NCH + ds.j) * kConsumerWarps + warp] = wsum;
