@@ -97,8 +97,8 @@ typedef int32_t sv_status;
                                16 bytes and 16-byte aligned logit pointers */
 
 /* Bytes of device workspace spec_verify needs for this shape on the current
- * device (the streaming path's per-row partial results, sampling partial sums
- * and grid-barrier words). Writes the size to *bytes. Needs the current CUDA
+ * device (the streaming path's per-row partial results, draw jobs, sampling
+ * partial sums, and the header and completion counters it clears itself). Writes the size to *bytes. Needs the current CUDA
  * device to read its SM count; returns SV_ERR_UNSUPPORTED without one. */
 sv_status spec_verify_workspace_size(int B, int gamma, int V, sv_dtype dtype, size_t* bytes);
 

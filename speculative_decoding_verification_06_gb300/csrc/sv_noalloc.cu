@@ -15,7 +15,7 @@
 namespace sv {
 namespace {
 
-// The scratch (grid-barrier words, completion counters, partial row
+// The scratch (the header and completion counters, partial row
 // statistics, draw jobs, draw sums). Its size is SV_NOALLOC_SCRATCH_BYTES; shapes that need more are
 // rejected with SV_ERR_SCRATCH_LIMIT.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
@@ -86,9 +86,9 @@ extern "C" sv_status spec_verify_noalloc(const void* target_logits, const void* 
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
-    // launch_streaming clears the barrier words and the completion counters at
-    // the start of the scratch (the only parts that must start at zero) before
-    // it launches.
+    // launch_streaming clears the header and the completion counters at the
+    // start of the scratch (the only parts that must start at zero) before it
+    // launches.
     const cudaError_t e = launch_streaming(a, dev, grid, scratch, SV_NOALLOC_SCRATCH_BYTES,
                                            reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {

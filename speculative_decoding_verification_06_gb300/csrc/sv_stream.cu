@@ -2547,7 +2547,7 @@ cudaError_t launch_streaming(const Args& a, const DeviceInfo& dev, int grid, voi
         attr_device = dev.device;
     }
     if (grid > dev.num_sms) return cudaErrorInvalidValue;
-    // the barrier words and the completion counters start at zero
+    // the header and the completion counters start at zero
     cudaError_t e = cudaMemsetAsync(workspace, 0, a.early ? L.clear_bytes : L.ee_tasks, stream);
     if (e != cudaSuccess) return e;
     Args args = a;
