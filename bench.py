@@ -315,13 +315,9 @@ def run_aux(args, w, local):
         metric = "post-verify commit requests/s"
     elif args.op == "tree":
         # a candidate tree per request over the workload's target rows: gamma
-        # nodes; node j's parent is node j - 1 half the time (a chain, whose
-        # tokens, the workload's draft tokens, are plausible), else uniform
-        # over 0..j-1 (a branch)
-        rng = np.random.default_rng(5)
-        par = np.array([[j - 1 if rng.random() < 0.5 else rng.integers(0, j) for j in range(1, G + 1)]
-                        for _ in range(B)], np.int32)
-        tree_par, tree_m = d(par), torch.full((B,), G, dtype=torch.int32, device="cuda")
+        # nodes, half chain, half branches (synthetic.tree_parents)
+        tree_par = d(synthetic.tree_parents(B, G, seed=5))
+        tree_m = torch.full((B,), G, dtype=torch.int32, device="cuda")
         tree_nodes = torch.empty((B, G), dtype=torch.int32, device="cuda")
 
         def call():

@@ -87,3 +87,10 @@ def test_copy_heavy_histories():
     h = synthetic.histories(64, 8192, (1, 8192), vocab=32000, copy_prob=0.5, seed=5)
     _check(h.token_buf, h.seq_lens, 4)
     _check(h.token_buf, h.seq_lens, 8)
+
+
+def test_bench_config():
+    """The proposals bench.py times (--op ngram): 256 histories of U(256, 4096)
+    tokens over a 128256-token vocabulary, copy probability 0.5, gamma 8."""
+    h = synthetic.histories(256, 4096, (256, 4096), vocab=128256, copy_prob=0.5, seed=1)
+    _check(h.token_buf, h.seq_lens, 8)

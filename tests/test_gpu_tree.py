@@ -127,6 +127,20 @@ def test_random_trees(B, G, V, dtype, opts):
     assert (gpu["n"] > 0).sum() > B // 8  # walks that go below the root
 
 
+def test_bench_tree_config():
+    """The tree workload bench.py times (--op tree): the mixed batch's target
+    rows and draft tokens (B=256, gamma=8, V=128256, bf16, T in {0, .3, .7,
+    1}) as gamma-node trees of synthetic.tree_parents, every node in use, on
+    the default path, against the oracle request by request."""
+    batch = synthetic.generate(synthetic.WORKLOADS[4], k=0)
+    B, G = batch.tokens.shape
+    t = dict(target=batch.target, tokens=batch.tokens, parents=synthetic.tree_parents(B, G, seed=5),
+             m=np.full(B, G, np.int32), ua=batch.u_accept, us=batch.u_sample, T=batch.temperature)
+    gpu = run_gpu(t)
+    ties = compare(t, gpu)
+    assert ties <= B // 4
+
+
 def test_eagle_sized_batch_streaming():
     """The bench's tree workload shape (bf16, V = 32000, 60 nodes) at B = 256:
     the streaming kernel against the oracle, request by request."""

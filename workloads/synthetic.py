@@ -240,3 +240,14 @@ def histories(B: int, max_len: int, lengths=(256, 4096), vocab: int = 32000, cop
         buf[b, :L] = np.asarray(h[:L], dtype=np.int32)
         lens[b] = L
     return Histories(buf, lens)
+
+
+def tree_parents(B: int, gamma: int, seed: int = 5) -> np.ndarray:
+    """Candidate-tree shapes [B, gamma] for a batch (parent of node j at
+    j - 1): node j's parent is node j - 1 half the time (a chain, whose
+    tokens, the workload's draft tokens, stay plausible), else uniform over
+    0..j-1 (a branch). One numpy Generator seeded with ``seed``, drawn in
+    request then node order."""
+    rng = np.random.default_rng(seed)
+    return np.array([[j - 1 if rng.random() < 0.5 else rng.integers(0, j) for j in range(1, gamma + 1)]
+                     for _ in range(B)], np.int32)
