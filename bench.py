@@ -38,7 +38,12 @@ UNIT = "rows/s"
 PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["speculative_decoding_verification_06_gb300/csrc"]
+# The files the streaming kernel is compiled from: the captured DRAM traffic
+# applies while they are unchanged.
+KERNEL_SOURCES = ["speculative_decoding_verification_06_gb300/csrc/sv_stream.cu",
+                  "speculative_decoding_verification_06_gb300/csrc/sv_common.cuh",
+                  "speculative_decoding_verification_06_gb300/csrc/sv_internal.h",
+                  "include/specverify.h"]
 
 
 def parse():
@@ -96,11 +101,9 @@ def peak_hbm():
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for d in KERNEL_SOURCES:
-        base = os.path.join(ROOT, d)
-        for name in sorted(os.listdir(base)):
-            with open(os.path.join(base, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(os.path.basename(rel).encode() + f.read())
     return h.hexdigest()[:16]
 
 

@@ -200,7 +200,19 @@ sv_status spec_verify_host_staging_size(int B, int gamma, int V, sv_dtype dtype,
  * device copies of the inputs (draft rows only for T > 0 requests, whose
  * temperatures the host reads here), the verification, and the device to
  * host copies of out_tokens and out_num_accepted. The outputs are valid once
- * the stream has reached that point (e.g. after cudaStreamSynchronize). */
+ * the stream has reached that point (e.g. after cudaStreamSynchronize).
+ * The host link is ~30x slower than HBM, so a batch of more than 64 MB of
+ * inputs is cut into up to 8 request slices (each >= 32 MB): the copies run on
+ * a library-owned copy stream of the current device, and `stream` verifies
+ * slice k (one spec_verify launch) as soon as it has landed, while slice k + 1
+ * is still being copied. The copies first wait for the work already on
+ * `stream`; `stream` waits for every copy, so the call stays ordered on it
+ * like one operation. Requests are independent: the outputs are those of one
+ * spec_verify over the whole batch (within the parity bar: row sums split at
+ * other places). The first call on a device creates that copy stream and its
+ * events, kept until the process exits (make it outside stream capture);
+ * calls take a lock while they enqueue. Calls that overlap on one staging
+ * buffer from different streams race on it. */
 sv_status spec_verify_host(const void* target_logits, const void* draft_logits, sv_dtype dtype,
                            int B, int gamma, int V, const int32_t* draft_tokens,
                            const float* u_accept, const float* u_sample,

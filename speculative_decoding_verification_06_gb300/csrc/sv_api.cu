@@ -248,6 +248,43 @@ struct Staging {
         end;
 };
 
+// Request slices of one spec_verify_host call: at most kHostSlices, each of
+// at least kHostSliceMinBytes of input (fewer for small batches).
+constexpr int kHostSlices = 8;
+constexpr size_t kHostSliceMinBytes = size_t(32) << 20;
+
+// Per device: the stream the host entry copies on, and its events. Made by the
+// first call on the device and kept until the process exits; calls hold
+// g_copy_mu while they enqueue, so they never share an event in flight.
+struct CopyLane {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t ready[kHostSlices] = {};
+};
+std::mutex g_copy_mu;
+CopyLane g_lane[kMaxDevices];
+
+CopyLane* copy_lane(int device) {
+    if (device < 0 || device >= kMaxDevices) return nullptr;
+    CopyLane& c = g_lane[device];
+    if (c.stream) return &c;
+    CopyLane n;
+    bool ok = cudaStreamCreateWithFlags(&n.stream, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int k = 0; ok && k < kHostSlices; ++k)
+        ok = cudaEventCreateWithFlags(&n.ready[k], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        if (n.fork) cudaEventDestroy(n.fork);
+        for (cudaEvent_t e : n.ready)
+            if (e) cudaEventDestroy(e);
+        if (n.stream) cudaStreamDestroy(n.stream);
+        return nullptr;
+    }
+    c = n;
+    return &c;
+}
+
 Staging staging_layout(int B, int gamma, int V, sv_dtype dtype, size_t ws) {
     const size_t es = elem_bytes(dtype);
     Staging l;
@@ -300,53 +337,84 @@ sv_status spec_verify_host(const void* target_logits, const void* draft_logits, 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(staging);
     const size_t es = elem_bytes(dtype);
-    const size_t drow_bytes = static_cast<size_t>(gamma) * V * es;
-    auto h2d = [&](size_t off, const void* src, size_t bytes) {
-        return cudaMemcpyAsync(base + off, src, bytes, cudaMemcpyHostToDevice, s);
+    const size_t trow_bytes = static_cast<size_t>(gamma + 1) * V * es;  // one request's target rows
+    const size_t drow_bytes = static_cast<size_t>(gamma) * V * es;      // one request's draft rows
+
+    // The inputs cross the host link far slower than the kernel reads them
+    // from HBM, so the batch is cut into request slices: the copy stream moves
+    // slice k while the caller's stream verifies slice k - 1 (requests are
+    // independent, so the outputs are those of one call over the batch).
+    size_t in_bytes = static_cast<size_t>(B) * trow_bytes;
+    for (int b = 0; b < B; ++b)
+        if (temperature[b] > 0.0f) in_bytes += drow_bytes;
+    const int slices = static_cast<int>(std::max<size_t>(
+        1, std::min<size_t>({static_cast<size_t>(kHostSlices), static_cast<size_t>(B),
+                             in_bytes / kHostSliceMinBytes})));
+
+    std::lock_guard<std::mutex> lock(g_copy_mu);
+    CopyLane* lane = copy_lane(dev.device);
+    if (!lane) return SV_ERR_CUDA;
+    cudaStream_t cs = lane->stream;
+    auto fail = [&]() {
+        cudaGetLastError();
+        g_last_launches = 0;
+        return SV_ERR_CUDA;
     };
-    cudaError_t err = h2d(l.target, target_logits, static_cast<size_t>(B) * (gamma + 1) * V * es);
-    // Draft rows: only requests with T > 0 are read, copied in runs of
-    // consecutive such requests.
-    for (int b = 0; b < B && err == cudaSuccess;) {
-        if (!(temperature[b] > 0.0f)) {
-            ++b;
-            continue;
-        }
-        int e = b + 1;
-        while (e < B && temperature[e] > 0.0f) ++e;
-        err = h2d(l.draft + static_cast<size_t>(b) * drow_bytes,
-                  static_cast<const char*>(draft_logits) + static_cast<size_t>(b) * drow_bytes,
-                  static_cast<size_t>(e - b) * drow_bytes);
-        b = e;
-    }
-    if (err == cudaSuccess) err = h2d(l.tokens, draft_tokens, static_cast<size_t>(B) * gamma * 4);
+    auto h2d = [&](size_t off, const void* src, size_t bytes) {
+        return cudaMemcpyAsync(base + off, src, bytes, cudaMemcpyHostToDevice, cs);
+    };
+    // The copies overwrite staging: they wait for the caller's earlier work.
+    if (cudaEventRecord(lane->fork, s) != cudaSuccess || cudaStreamWaitEvent(cs, lane->fork, 0) != cudaSuccess)
+        return fail();
+    cudaError_t err = h2d(l.tokens, draft_tokens, static_cast<size_t>(B) * gamma * 4);
     if (err == cudaSuccess) err = h2d(l.u_accept, u_accept, static_cast<size_t>(B) * gamma * 4);
     if (err == cudaSuccess) err = h2d(l.u_sample, u_sample, static_cast<size_t>(B) * 4);
     if (err == cudaSuccess) err = h2d(l.temperature, temperature, static_cast<size_t>(B) * 4);
-    if (err != cudaSuccess) {
-        cudaGetLastError();
-        return SV_ERR_CUDA;
+    if (err != cudaSuccess) return fail();
+
+    int launches = 0;
+    for (int k = 0; k < slices; ++k) {
+        const int b0 = static_cast<int>(static_cast<int64_t>(B) * k / slices);
+        const int b1 = static_cast<int>(static_cast<int64_t>(B) * (k + 1) / slices);
+        const int nb = b1 - b0;
+        err = h2d(l.target + b0 * trow_bytes, static_cast<const char*>(target_logits) + b0 * trow_bytes,
+                  static_cast<size_t>(nb) * trow_bytes);
+        // Draft rows: only requests with T > 0 are read, copied in runs of
+        // consecutive such requests.
+        for (int b = b0; b < b1 && err == cudaSuccess;) {
+            if (!(temperature[b] > 0.0f)) {
+                ++b;
+                continue;
+            }
+            int e = b + 1;
+            while (e < b1 && temperature[e] > 0.0f) ++e;
+            err = h2d(l.draft + b * drow_bytes, static_cast<const char*>(draft_logits) + b * drow_bytes,
+                      static_cast<size_t>(e - b) * drow_bytes);
+            b = e;
+        }
+        if (err != cudaSuccess || cudaEventRecord(lane->ready[k], cs) != cudaSuccess ||
+            cudaStreamWaitEvent(s, lane->ready[k], 0) != cudaSuccess)
+            return fail();
+        sv_status st = spec_verify(
+            base + l.target + b0 * trow_bytes, base + l.draft + b0 * drow_bytes, dtype, nb, gamma, V,
+            reinterpret_cast<const int32_t*>(base + l.tokens) + static_cast<size_t>(b0) * gamma,
+            reinterpret_cast<const float*>(base + l.u_accept) + static_cast<size_t>(b0) * gamma,
+            reinterpret_cast<const float*>(base + l.u_sample) + b0,
+            reinterpret_cast<const float*>(base + l.temperature) + b0,
+            reinterpret_cast<int32_t*>(base + l.out_tokens) + static_cast<size_t>(b0) * (gamma + 1),
+            reinterpret_cast<int32_t*>(base + l.out_num) + b0, base + l.workspace, ws, stream);
+        if (st != SV_OK) {
+            g_last_launches = 0;
+            return st;
+        }
+        launches += g_last_launches;
     }
-    sv_status st = spec_verify(base + l.target, base + l.draft, dtype, B, gamma, V,
-                               reinterpret_cast<const int32_t*>(base + l.tokens),
-                               reinterpret_cast<const float*>(base + l.u_accept),
-                               reinterpret_cast<const float*>(base + l.u_sample),
-                               reinterpret_cast<const float*>(base + l.temperature),
-                               reinterpret_cast<int32_t*>(base + l.out_tokens),
-                               reinterpret_cast<int32_t*>(base + l.out_num), base + l.workspace, ws,
-                               stream);
-    if (st != SV_OK) return st;
-    const int launches = g_last_launches;
     err = cudaMemcpyAsync(out_tokens, base + l.out_tokens, static_cast<size_t>(B) * (gamma + 1) * 4,
                           cudaMemcpyDeviceToHost, s);
     if (err == cudaSuccess)
         err = cudaMemcpyAsync(out_num_accepted, base + l.out_num, static_cast<size_t>(B) * 4,
                               cudaMemcpyDeviceToHost, s);
-    if (err != cudaSuccess) {
-        cudaGetLastError();
-        g_last_launches = 0;
-        return SV_ERR_CUDA;
-    }
+    if (err != cudaSuccess) return fail();
     g_last_launches = launches;
     return SV_OK;
 }
