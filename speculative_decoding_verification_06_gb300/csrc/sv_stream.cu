@@ -60,6 +60,7 @@ constexpr int kChunkBytes = 24576;  // draw-phase chunk of one row (a residual i
 constexpr int kMapMax = 256;   // compacted requests in one block's draft slice
 constexpr int kMaxGrid = 256;  // blocks (partition tables live in shared memory)
 constexpr int kGrab = 4;       // draw items a producer takes per atomic
+constexpr int kEeGroup = 4;    // early exit: chunks of one task taken as one item
 constexpr int kJobMsg = 0x40000000;  // finisher message flag: a draw item of job (item & ~flag)
 constexpr int kEndKind = -2;   // stage descriptor kind: no more draw items
 constexpr int kMaxB = 4096;
@@ -101,11 +102,14 @@ constexpr int kTaskStats = 0;
 constexpr int kTaskDraw = 1;
 constexpr int kStatsArgmax = 1;  // StageDesc.flags: argmax (T == 0) instead of (max, sum)
 constexpr int kStatsDraft = 2;   // StageDesc.flags: the stage also holds the draft row's chunk
+constexpr int kItemFirst = 4;    // StageDesc.flags: the first stage of an early-exit item
+constexpr int kItemLast = 8;     // StageDesc.flags: the last stage of an early-exit item
 
 // Byte offsets into the caller's workspace and the partition constants.
 struct Layout {
     long long Et;  // target elements B*(gamma+1)*V
     int G, MT, MD, NCH, vec;
+    int NI;  // early exit: items per task, groups of kEeGroup chunks
     size_t hdr, req_done, job_done, ready, ee_tasks, ee_done, clear_bytes, rec_t, rec_d, ee_rec, jobs, jobset, wsums,
         total;
     int ee_cap;  // early exit: task slots, B (gamma + 2)
@@ -130,6 +134,7 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.MD = static_cast<int>(((Ed_max + G - 1) / G + L.vec - 1) / V + 2);
     const int chunk_elems = kChunkBytes / es;
     L.NCH = (V + chunk_elems - 1) / chunk_elems;
+    L.NI = (L.NCH + kEeGroup - 1) / kEeGroup;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t at = off;
@@ -148,7 +153,7 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.clear_bytes = off;  // cleared before every launch (up to ee_tasks without early exit)
     L.rec_t = take(static_cast<size_t>(G) * L.MT * sizeof(Rec));
     L.rec_d = take(static_cast<size_t>(G) * L.MD * sizeof(Rec));
-    L.ee_rec = take(static_cast<size_t>(L.ee_cap) * L.NCH * 2 * sizeof(Rec));  // per (task, chunk): target, draft
+    L.ee_rec = take(static_cast<size_t>(L.ee_cap) * L.NI * 2 * sizeof(Rec));  // per (task, item): target, draft
     L.jobs = take(static_cast<size_t>(B) * sizeof(Job));
     L.jobset = take(static_cast<size_t>(B) * gamma * 4);  // tree jobs: tokens excluded from the last draw
     L.wsums = take(static_cast<size_t>(B) * L.NCH * kConsumerWarps * 8);
@@ -1636,7 +1641,11 @@ struct Kern {
     // row for model proposals at T > 0), or one draw. Tasks 0..B-1 are position 0
     // of every request; the owner of a statistics task (block p mod G) decides
     // that position and publishes the request's next task: its next position,
-    // or its draw. Producers take chunks of tasks in publication order.
+    // or its draw. Producers take items, fixed groups of kEeGroup consecutive
+    // chunks of one task (L.NI per task), in publication order; an item's
+    // statistics are folded into one record, so that the per-chunk costs (the
+    // grab, the task lookup, the cross-warp flush) are paid once per group,
+    // while a task's chunks still spread over several blocks.
 
     __device__ static int ee_encode(int type, int b, int pos) { return ((type << 28) | (b << 8) | pos) + 1; }
 
@@ -1712,11 +1721,11 @@ struct Kern {
         return x;
     }
 
-    // End of a statistics chunk: each warp parks its records; the last warp
-    // merges the twelve in warp order, writes the chunk's records and posts the
-    // task to the finisher.
+    // End of a statistics item (group grp of task p, nch chunks): each warp
+    // parks its records; the last warp merges the twelve in warp order, writes
+    // the item's records and posts its chunks to the finisher.
     __device__ void ee_flush_item(const RowState& rt, const RowState& rd, bool has_draft, unsigned seq, int p,
-                                  int j) const {
+                                  int grp, unsigned nch) const {
         const Rec t = warp_rec(rt);
         Rec d = t;
         if (has_draft) d = warp_rec(rd);
@@ -1734,27 +1743,27 @@ struct Kern {
                     if (has_draft) od = rec_merge(od, ctl.wrec2[fs][w], false, rd.c);
                 }
                 ctl.wcnt[fs] = 0;
-                Rec* dst = ee_rec() + (static_cast<size_t>(p) * L.NCH + j) * 2;
+                Rec* dst = ee_rec() + (static_cast<size_t>(p) * L.NI + grp) * 2;
                 dst[0] = ot;
                 dst[1] = od;
-                if (!post(p | kJobMsg, 1u)) set_abort(a.d_status);
+                if (!post(p | kJobMsg, nch)) set_abort(a.d_status);
             }
         }
     }
 
-    // Producer warp: chunks of tasks in publication order, one at a time from the
-    // global counter (a task's chunks then run on as many blocks), until every
-    // request is finished; then the end marker.
+    // Producer warp: items of tasks in publication order, one at a time from the
+    // global counter (a task's items then run on as many blocks), each as one
+    // stage per chunk, until every request is finished; then the end marker.
     __device__ void ee_produce(Cursor& prod) const {
         const int lane = threadIdx.x & 31;
         volatile int* vabort = &ctl.abort;
         Hdr* h = hdr();
-        const int NCH = L.NCH, GM = a.gamma;
+        const int NCH = L.NCH, NI = L.NI, GM = a.gamma;
         constexpr int CH = kChunkElems;
         unsigned next = 0;
         if (lane == 0) next = atomicAdd(&h->next_item, 1u);
-        long long i = 0, i_end = 0;
         int cur_p = -1;
+        int task_flags = 0;  // lane 0: the statistics flags of the current task
         StageDesc desc;  // lane 0's copy of the current task
         desc.k = -1;
         desc.type = -1;
@@ -1764,12 +1773,9 @@ struct Kern {
         desc.job.kind = 0;
         bool ok = true;
         while (ok && !*vabort) {
-            if (i == i_end) {
-                i = __shfl_sync(0xffffffffu, next, 0);
-                i_end = i + 1;
-                if (lane == 0) next = atomicAdd(&h->next_item, 1u);  // the next chunk, in flight meanwhile
-            }
-            const int p = static_cast<int>(i / NCH), j = static_cast<int>(i - static_cast<long long>(p) * NCH);
+            const long long i = __shfl_sync(0xffffffffu, next, 0);
+            if (lane == 0) next = atomicAdd(&h->next_item, 1u);  // the next item, in flight meanwhile
+            const int p = static_cast<int>(i / NI), grp = static_cast<int>(i - static_cast<long long>(p) * NI);
             if (p != cur_p) {
                 int state = 1;  // 1 task known, 0 no more tasks, -1 the wait ran out
                 if (lane == 0) {
@@ -1807,14 +1813,14 @@ struct Kern {
                             desc.job.n = pos;
                             desc.job.kind = 0;
                             desc.job.d.c = samp ? temp_scale(T) : 0.0f;
-                            desc.flags = (samp ? 0 : kStatsArgmax) |
+                            task_flags = (samp ? 0 : kStatsArgmax) |
                                          ((samp && !a.onehot && pos < kb && pos < GM) ? kStatsDraft : 0);
                         } else {
                             const int* src = reinterpret_cast<const int*>(jobs() + b);
                             int* dst = reinterpret_cast<int*>(&desc.job);
 #pragma unroll
                             for (int q = 0; q < static_cast<int>(sizeof(Job) / 4); ++q) dst[q] = __ldcg(src + q);
-                            desc.flags = 0;
+                            task_flags = 0;
                         }
                     }
                 }
@@ -1826,25 +1832,27 @@ struct Kern {
                 cur_p = p;
             }
             const int type = __shfl_sync(0xffffffffu, desc.type, 0);
-            const int flags = __shfl_sync(0xffffffffu, desc.flags, 0);
+            const int flags = __shfl_sync(0xffffffffu, task_flags, 0);
             const int b = __shfl_sync(0xffffffffu, desc.job.b, 0);
             const int pos = __shfl_sync(0xffffffffu, desc.job.n, 0);
             const int kind = __shfl_sync(0xffffffffu, desc.job.kind, 0);
-            desc.j = j;
-            const long long e0 = static_cast<long long>(j) * CH;
-            const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
-            const unsigned bytes = static_cast<unsigned>(cnt * ES);
             const long long trow = static_cast<long long>(b) * (GM + 1) + pos;  // pos: the draw's row n for draws
-            const char* src_t = static_cast<const char*>(a.target) + (trow * a.V + e0) * ES;
+            const long long drow = static_cast<long long>(b) * GM + pos;
             const bool two = type == kTaskStats ? (flags & kStatsDraft) != 0 : kind == kKindResidual;
-            if (two) {
-                const long long drow = static_cast<long long>(b) * GM + pos;
-                ok = produce(prod, src_t, bytes, static_cast<const char*>(a.draft) + (drow * a.V + e0) * ES, bytes,
-                             &desc);
-            } else {
-                ok = produce(prod, src_t, bytes, nullptr, 0u, &desc);
+            const int j0 = grp * kEeGroup, j1 = min(NCH, j0 + kEeGroup);
+            for (int j = j0; ok && j < j1; ++j) {
+                desc.j = j;
+                desc.flags = flags | (j == j0 ? kItemFirst : 0) | (j == j1 - 1 ? kItemLast : 0);
+                const long long e0 = static_cast<long long>(j) * CH;
+                const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+                const unsigned bytes = static_cast<unsigned>(cnt * ES);
+                const char* src_t = static_cast<const char*>(a.target) + (trow * a.V + e0) * ES;
+                if (two)
+                    ok = produce(prod, src_t, bytes, static_cast<const char*>(a.draft) + (drow * a.V + e0) * ES,
+                                 bytes, &desc);
+                else
+                    ok = produce(prod, src_t, bytes, nullptr, 0u, &desc);
             }
-            ++i;
         }
         if (!ok && lane == 0) set_abort(a.d_status);
         __syncwarp();
@@ -1857,12 +1865,17 @@ struct Kern {
         produce(prod, nullptr, 0u, nullptr, 0u, &end);  // bounded; the consumers' own waits are too
     }
 
-    // Consumer warps: statistics chunks and draw chunks until the end marker.
+    // Consumer warps: the stages of statistics items and draw items until the
+    // end marker. A statistics item's chunks fold into one state; a draw item's
+    // chunks each get their per-warp sums. Either posts once, at its last stage.
     __device__ void ee_consume(Cursor& cons) const {
         const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
         constexpr int CH = kChunkElems, TPT = kTPT, NVC = kChunkBytes / 16 / kConsumers;
         unsigned long long* ws_sum = wsums();
-        for (unsigned iseq = 0;; ++iseq) {
+        RowState rt, rd;  // the statistics item in progress
+        start_row_mode(rt, false, 0.0f);
+        start_row_mode(rd, false, 0.0f);
+        for (unsigned nitem = 0;;) {
             const int slot = static_cast<int>(cons.it % kStages);
             const char* smt = consume_begin(cons);
             if (!smt) {
@@ -1876,18 +1889,20 @@ struct Kern {
             }
             const long long e0 = static_cast<long long>(ds.j) * CH;
             const int n = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
+            const unsigned nch = static_cast<unsigned>(ds.j % kEeGroup) + 1;  // chunks of the item so far
             if (ds.type == kTaskStats) {
                 const bool argmax = (ds.flags & kStatsArgmax) != 0, has_draft = (ds.flags & kStatsDraft) != 0;
-                RowState rt, rd;
-                start_row_mode(rt, argmax, ds.job.d.c);
-                start_row_mode(rd, false, ds.job.d.c);
+                if (ds.flags & kItemFirst) {
+                    start_row_mode(rt, argmax, ds.job.d.c);
+                    start_row_mode(rd, false, ds.job.d.c);
+                }
                 uint4 vt[NVC], vd[NVC];
                 load_stage<NVC>(smt, n * ES / 16, vt);
                 if (has_draft) load_stage<NVC>(smt + kChunkBytes, n * ES / 16, vd);
                 consume_end(cons);
                 fold_vectors<NVC>(rt, vt, e0);
                 if (has_draft) fold_vectors<NVC>(rd, vd, e0);
-                ee_flush_item(rt, rd, has_draft, iseq, ds.k, ds.j);
+                if (ds.flags & kItemLast) ee_flush_item(rt, rd, has_draft, nitem++, ds.k, ds.j / kEeGroup, nch);
             } else {
                 const int valid = max(0, min(TPT, n - t * TPT));
                 Run lt, ld;
@@ -1902,14 +1917,17 @@ struct Kern {
                 const unsigned long long wsum = warp_sum_u64(to_fixed(run, ds.job.d.fix));
                 if (lane == 0) {
                     ws_sum[(static_cast<size_t>(ds.job.b) * L.NCH + ds.j) * kConsumerWarps + warp] = wsum;
-                    const int fs = static_cast<int>(iseq % kFlushSlots);
-                    __threadfence_block();
-                    if (atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1) {
+                    if (ds.flags & kItemLast) {
+                        const int fs = static_cast<int>(nitem % kFlushSlots);
                         __threadfence_block();
-                        ctl.wcnt[fs] = 0;
-                        if (!post(ds.k | kJobMsg, 1u)) set_abort(a.d_status);
+                        if (atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1) {
+                            __threadfence_block();
+                            ctl.wcnt[fs] = 0;
+                            if (!post(ds.k | kJobMsg, nch)) set_abort(a.d_status);
+                        }
                     }
                 }
+                if (ds.flags & kItemLast) ++nitem;
             }
         }
     }
@@ -1940,7 +1958,7 @@ struct Kern {
     // Finisher warp: the decision at position pos of request b, from the chunk
     // records of statistics task p.
     __device__ void ee_decide(int p, int b, int pos) const {
-        const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V, NCH = L.NCH;
+        const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V, NI = L.NI;
         const float T = a.temperature[b];
         const bool t_ok = (T >= 0.0f) && (T < pos_inf());
         const bool greedy = t_ok && T == 0.0f;
@@ -1970,13 +1988,13 @@ struct Kern {
                 const int y = tok[q];
                 if (y < 0 || y >= V) bad = 1;
             }
-        // the chunk records of the position's rows, merged in chunk order per lane
+        // the item records of the position's rows, merged in item order per lane
         // and then across lanes; lane 0's result is used
         const bool argmax = !samp;
         Rec rt{neg_inf(), 0.0f, 0x7fffffff, 0}, rd{neg_inf(), 0.0f, -1, 0};
         bool first = true;
-        for (int jj = lane; jj < NCH; jj += 32) {
-            const uint4* src = reinterpret_cast<const uint4*>(ee_rec() + (static_cast<size_t>(p) * NCH + jj) * 2);
+        for (int jj = lane; jj < NI; jj += 32) {
+            const uint4* src = reinterpret_cast<const uint4*>(ee_rec() + (static_cast<size_t>(p) * NI + jj) * 2);
             const uint4 vt = __ldcg(src), vd = __ldcg(src + 1);
             const Rec xt{__uint_as_float(vt.x), __uint_as_float(vt.y), static_cast<int32_t>(vt.z), static_cast<int32_t>(vt.w)};
             const Rec xd{__uint_as_float(vd.x), __uint_as_float(vd.y), static_cast<int32_t>(vd.z), static_cast<int32_t>(vd.w)};
