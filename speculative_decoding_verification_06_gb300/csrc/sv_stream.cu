@@ -1955,39 +1955,64 @@ struct Kern {
         }
     }
 
-    // Finisher warp: the decision at position pos of request b, from the chunk
-    // records of statistics task p.
-    __device__ void ee_decide(int p, int b, int pos) const {
-        const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V, NI = L.NI;
-        const float T = a.temperature[b];
+    // What a position's decision reads besides its rows' records: the request's
+    // temperature and proposal count, the proposed token, its two logits and
+    // its uniform (lane 0), and the request-wide token checks at position 0
+    // (each lane its share). The owner reads them as soon as it knows the task,
+    // while the task's chunks are still being read.
+    struct EePre {
+        float T, lt, ld, u;
+        int kb, x, bad;
+    };
+
+    __device__ EePre ee_prefetch(int b, int pos) const {
+        const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V;
+        EePre e;
+        e.T = a.temperature[b];
+        e.kb = ee_kb(b);
+        const bool t_ok = (e.T >= 0.0f) && (e.T < pos_inf());
+        const bool samp = sampled(e.T);
+        const bool range_ok = t_ok && e.kb >= 0 && e.kb <= GM;
+        const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
+        e.x = -1;
+        e.lt = 0.0f;
+        e.ld = 0.0f;
+        e.u = 0.0f;
+        if (lane == 0 && range_ok && pos < e.kb) {
+            e.x = tok[pos];
+            if (samp && e.x >= 0 && e.x < V) {
+                const size_t tr = static_cast<size_t>(b) * (GM + 1) + pos, dr = static_cast<size_t>(b) * GM + pos;
+                e.lt = load_logit<DT>(a.target, tr * V + e.x);
+                if (!a.onehot) e.ld = load_logit<DT>(a.draft, dr * V + e.x);
+                e.u = a.u_accept[dr];
+            }
+        }
+        // request-wide checks at position 0: T, the proposal count, every proposed token
+        e.bad = range_ok ? 0 : 1;
+        if (pos == 0 && range_ok)
+            for (int q = lane; q < e.kb; q += 32) {
+                const int y = tok[q];
+                if (y < 0 || y >= V) e.bad = 1;
+            }
+        return e;
+    }
+
+    // Search warp: the decision at position pos of request b, from the item
+    // records of statistics task p and its prefetched inputs.
+    __device__ void ee_decide(int p, int b, int pos, const EePre& e) const {
+        const int lane = threadIdx.x & 31, GM = a.gamma, NI = L.NI;
+        const float T = e.T;
         const bool t_ok = (T >= 0.0f) && (T < pos_inf());
         const bool greedy = t_ok && T == 0.0f;
         const bool samp = sampled(T);
         const float c = samp ? temp_scale(T) : 0.0f;
-        const int kb = ee_kb(b);
+        const int kb = e.kb;
         const bool range_ok = t_ok && kb >= 0 && kb <= GM;
-        const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
         const bool proposal = range_ok && pos < kb;
         const bool has_draft = samp && !a.onehot && proposal;
-        // this position's gathered logits and uniform, loaded before the merge
-        int x = -1;
-        float lt = 0.0f, ld = 0.0f, u = 0.0f;
-        if (lane == 0 && proposal) {
-            x = tok[pos];
-            if (samp && x >= 0 && x < V) {
-                const size_t tr = static_cast<size_t>(b) * (GM + 1) + pos, dr = static_cast<size_t>(b) * GM + pos;
-                lt = load_logit<DT>(a.target, tr * V + x);
-                if (!a.onehot) ld = load_logit<DT>(a.draft, dr * V + x);
-                u = a.u_accept[dr];
-            }
-        }
-        // request-wide checks at position 0: T, the proposal count, every proposed token
-        int bad = range_ok ? 0 : 1;
-        if (pos == 0 && range_ok)
-            for (int q = lane; q < kb; q += 32) {
-                const int y = tok[q];
-                if (y < 0 || y >= V) bad = 1;
-            }
+        const int x = e.x;
+        const float lt = e.lt, ld = e.ld, u = e.u;
+        int bad = e.bad;
         // the item records of the position's rows, merged in item order per lane
         // and then across lanes; lane 0's result is used
         const bool argmax = !samp;
@@ -2050,7 +2075,7 @@ struct Kern {
         }
         if (greedy) {
             const int am = rt.idx == 0x7fffffff ? 0 : rt.idx;
-            if (proposal && tok[pos] == am) {
+            if (proposal && x == am) {
                 out[pos] = am;
                 ee_publish(kTaskStats, b, pos + 1);
                 return;
@@ -2102,11 +2127,12 @@ struct Kern {
         ee_publish(kTaskDraw, b, pos);
     }
 
-    // Finisher warp: the next owned task (positions B + g, B + g + G, ... and
-    // g itself), decided or searched once all its chunks are counted. Lane 0
-    // keeps own_p and the task's code (own_v, 0 until it is published).
-    __device__ bool ee_poll_owned(int& own_p, int& own_v) const {
-        int act_p = -1, act_v = 0;
+    // Search warp: the next owned task (g, g + G, g + 2G, ...), decided or
+    // searched once all its chunks are counted. Lane 0 keeps own_p and the
+    // task's code (own_v, 0 until it is published); a statistics task's inputs
+    // are prefetched into `pre` (for task pre_p) as soon as its code is known.
+    __device__ bool ee_poll_owned(int& own_p, int& own_v, EePre& pre, int& pre_p) const {
+        int act_p = -1, act_v = 0, known_p = -1, known_v = 0;
         if ((threadIdx.x & 31) == 0 && own_p < L.ee_cap) {
             if (own_v == 0) {
                 if (own_p < a.B) {
@@ -2119,6 +2145,8 @@ struct Kern {
                     }
                 }
             }
+            known_p = own_p;
+            known_v = own_v;
             if (own_v != 0 &&
                 ld_relaxed(ee_done() + own_p) >= static_cast<unsigned>(L.NCH)) {
                 __threadfence();  // the other blocks' chunk records and sums
@@ -2128,12 +2156,20 @@ struct Kern {
                 own_p += G;
             }
         }
+        known_p = __shfl_sync(0xffffffffu, known_p, 0);
+        known_v = __shfl_sync(0xffffffffu, known_v, 0);
         act_p = __shfl_sync(0xffffffffu, act_p, 0);
         act_v = __shfl_sync(0xffffffffu, act_v, 0);
+        if (known_v != 0 && known_p != pre_p && ((known_v - 1) >> 28) == kTaskStats) {
+            const int v = known_v - 1;
+            pre = ee_prefetch((v >> 8) & 0xfffff, v & 0xff);
+            pre_p = known_p;
+        }
         if (act_p < 0) return false;
         const int v = act_v - 1, type = v >> 28, b = (v >> 8) & 0xfffff, pos = v & 0xff;
         if (type == kTaskStats) {
-            ee_decide(act_p, b, pos);
+            ee_decide(act_p, b, pos, pre);  // act_p == pre_p: its code was known above at the latest
+            pre_p = -1;
         } else {
             search_job(b);
             __syncwarp();
@@ -2487,16 +2523,42 @@ __global__ void __launch_bounds__(kThreads, 1) early_kernel(Args a, Layout L, ch
     __syncthreads();
 
     typename KT::Cursor prod, cons;
-    if (warp == kSearchWarp) return;  // the early-exit finisher searches its own draws
+    if (warp == kSearchWarp) {
+        // the owned tasks g, g + G, ...: decided or searched as soon as their
+        // last chunk is counted
+        int own_p = blockIdx.x, own_v = 0, pre_p = -1;  // lane 0: next owned task, its code once published
+        typename KT::EePre pre{};
+        volatile int* vab = &ctl.abort;
+        unsigned long long t0 = global_ns();
+        for (;;) {
+            if (K.ee_poll_owned(own_p, own_v, pre, pre_p)) {
+                t0 = global_ns();
+                continue;
+            }
+            int stop = 0;
+            if (lane == 0) {
+                if (*vab) {
+                    stop = 1;
+                } else if (own_p >= L.ee_cap || (own_v == 0 && K.ee_no_task(own_p))) {
+                    stop = 1;
+                } else if (global_ns() - t0 > kWaitTimeoutNs) {
+                    K.set_abort(a.d_status);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            __nanosleep(64);
+        }
+        stamp(ph, 9, lane == 0);
+        return;
+    }
     if (warp == kFinisherWarp) {
-        int own_p = blockIdx.x, own_v = 0;  // lane 0: next owned task, its code once published
         unsigned* done = K.ee_done();
         K.finish([&](int item, unsigned v) {
                      red_release_add(done + (item & ~kJobMsg), v);  // the task's owner polls the count
                      return false;
                  },
-                 [&](int) {}, [&]() { return K.ee_poll_owned(own_p, own_v); },
-                 [&]() { return own_p >= L.ee_cap || (own_v == 0 && K.ee_no_task(own_p)); });
+                 [&](int) {}, [&]() { return false; }, [&]() { return true; });
         stamp(ph, 9, lane == 0);
         return;
     }
