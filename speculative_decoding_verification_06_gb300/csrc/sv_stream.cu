@@ -1652,9 +1652,13 @@ struct Kern {
     // Proposals of request b (range-checked by the owner of its position 0).
     __device__ int ee_kb(int b) const { return a.onehot && a.num_draft ? a.num_draft[b] : a.gamma; }
 
-    // One lane: appends a task (after whatever it reads is written).
+    // One lane: appends a task. A draw task's job is written before it is
+    // published (the fence); a statistics task carries nothing its readers need
+    // from the publisher (they read the inputs, and the records of its own
+    // chunks), so it goes out without waiting for the publisher's earlier
+    // stores. The slot is stored after the count's increment has returned.
     __device__ void ee_publish(int type, int b, int pos) const {
-        __threadfence();
+        if (type != kTaskStats) __threadfence();
         const unsigned q = atomicAdd(&hdr()->n_pub, 1u);
         if (static_cast<long long>(a.B) + q < static_cast<long long>(L.ee_cap))  // always: at most gamma + 1 per request
             st_relaxed(ee_tasks() + a.B + q, ee_encode(type, b, pos));
