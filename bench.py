@@ -468,7 +468,7 @@ def main():
     try:
         with open(PROFILE_TRAFFIC) as f:
             prof = json.load(f)
-        entry = prof.get(args.workload)
+        entry = prof.get(args.workload + ("-early" if args.early_exit else ""))  # the captured kernel's workload
         if entry and entry.get("kernel_hash") == kernel_hash():
             traffic = entry.get("dram_bytes_per_launch")
     except Exception:
