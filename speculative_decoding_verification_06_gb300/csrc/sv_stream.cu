@@ -148,7 +148,7 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     // early exit: B position-0 tasks, then at most gamma more positions and one
     // draw per request
     L.ee_cap = B * (gamma + 2);
-    L.ee_tasks = take(static_cast<size_t>(L.ee_cap) * 4);  // published tasks (encoded + 1)
+    L.ee_tasks = take(static_cast<size_t>(L.ee_cap) * 8);  // published tasks: code (low word), scale c
     L.ee_done = take(static_cast<size_t>(L.ee_cap) * 4);   // chunks done, per task
     L.clear_bytes = off;  // cleared before every launch (up to ee_tasks without early exit)
     L.rec_t = take(static_cast<size_t>(G) * L.MT * sizeof(Rec));
@@ -239,6 +239,14 @@ __device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
 }
 __device__ __forceinline__ void st_relaxed(int* p, int v) {
     asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_relaxed(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void bar_sync(int id, int count) {
@@ -394,7 +402,11 @@ struct Kern {
     __device__ unsigned* req_done() const { return reinterpret_cast<unsigned*>(ws + L.req_done); }
     __device__ unsigned* job_done() const { return reinterpret_cast<unsigned*>(ws + L.job_done); }
     __device__ int* ready() const { return reinterpret_cast<int*>(ws + L.ready); }
-    __device__ int* ee_tasks() const { return reinterpret_cast<int*>(ws + L.ee_tasks); }
+    // Task slot p: the task's code in the low word (0 until published), and for
+    // a statistics task the bits of its scale c in the high word.
+    __device__ unsigned long long* ee_slot(int p) const {
+        return reinterpret_cast<unsigned long long*>(ws + L.ee_tasks) + p;
+    }
     __device__ unsigned* ee_done() const { return reinterpret_cast<unsigned*>(ws + L.ee_done); }
     __device__ Rec* ee_rec() const { return reinterpret_cast<Rec*>(ws + L.ee_rec); }
     __device__ unsigned long long* wsums() const {
@@ -1647,7 +1659,11 @@ struct Kern {
     // grab, the task lookup, the cross-warp flush) are paid once per group,
     // while a task's chunks still spread over several blocks.
 
-    __device__ static int ee_encode(int type, int b, int pos) { return ((type << 28) | (b << 8) | pos) + 1; }
+    // A task's code: type, the statistics flags (kStatsArgmax, kStatsDraft) of
+    // a published statistics task, request b < 4096, position; plus one.
+    __device__ static int ee_encode(int type, int b, int pos, int sflags = 0) {
+        return ((type << 28) | (sflags << 20) | (b << 8) | pos) + 1;
+    }
 
     // Proposals of request b (range-checked by the owner of its position 0).
     __device__ int ee_kb(int b) const { return a.onehot && a.num_draft ? a.num_draft[b] : a.gamma; }
@@ -1657,11 +1673,15 @@ struct Kern {
     // from the publisher (they read the inputs, and the records of its own
     // chunks), so it goes out without waiting for the publisher's earlier
     // stores. The slot is stored after the count's increment has returned.
-    __device__ void ee_publish(int type, int b, int pos) const {
+    // A statistics task travels with its flags and scale, so that the producers
+    // that take it need no read of their own before issuing its copies.
+    __device__ void ee_publish(int type, int b, int pos, float c = 0.0f, int sflags = 0) const {
         if (type != kTaskStats) __threadfence();
         const unsigned q = atomicAdd(&hdr()->n_pub, 1u);
         if (static_cast<long long>(a.B) + q < static_cast<long long>(L.ee_cap))  // always: at most gamma + 1 per request
-            st_relaxed(ee_tasks() + a.B + q, ee_encode(type, b, pos));
+            st_relaxed(ee_slot(a.B + static_cast<int>(q)),
+                       (static_cast<unsigned long long>(__float_as_uint(c)) << 32) |
+                           static_cast<unsigned>(ee_encode(type, b, pos, sflags)));
     }
 
     // One lane: request b is done (its outputs are written).
@@ -1784,14 +1804,16 @@ struct Kern {
                 int state = 1;  // 1 task known, 0 no more tasks, -1 the wait ran out
                 if (lane == 0) {
                     int v = 0;
+                    float cs = 0.0f;  // a published statistics task's scale
                     if (p < a.B) {
                         v = ee_encode(kTaskStats, p, 0);
                     } else if (p >= L.ee_cap) {
                         state = 0;
                     } else {
-                        const int* tp = ee_tasks() + p;
+                        const unsigned long long* tp = ee_slot(p);
                         const unsigned long long t0 = global_ns();
-                        while ((v = ld_relaxed(tp)) == 0) {
+                        unsigned long long e;
+                        while ((e = ld_relaxed(tp)) == 0ull) {
                             if (ee_no_task(p)) {
                                 state = 0;
                                 break;
@@ -1802,24 +1824,31 @@ struct Kern {
                             }
                             __nanosleep(64);
                         }
+                        v = static_cast<int>(static_cast<unsigned>(e));
+                        cs = __uint_as_float(static_cast<unsigned>(e >> 32));
                     }
                     if (state == 1) {
-                        __threadfence();
                         v -= 1;
-                        const int type = v >> 28, b = (v >> 8) & 0xfffff, pos = v & 0xff;
+                        const int type = v >> 28, b = (v >> 8) & 0xfff, pos = v & 0xff;
                         desc.k = p;
                         desc.type = type;
                         if (type == kTaskStats) {
-                            const float T = a.temperature[b];
-                            const bool samp = sampled(T);
-                            const int kb = ee_kb(b);
                             desc.job.b = b;
                             desc.job.n = pos;
                             desc.job.kind = 0;
-                            desc.job.d.c = samp ? temp_scale(T) : 0.0f;
-                            task_flags = (samp ? 0 : kStatsArgmax) |
-                                         ((samp && !a.onehot && pos < kb && pos < GM) ? kStatsDraft : 0);
+                            if (p < a.B) {  // position 0: from the request's inputs
+                                const float T = a.temperature[b];
+                                const bool samp = sampled(T);
+                                const int kb = ee_kb(b);
+                                desc.job.d.c = samp ? temp_scale(T) : 0.0f;
+                                task_flags = (samp ? 0 : kStatsArgmax) |
+                                             ((samp && !a.onehot && pos < kb && pos < GM) ? kStatsDraft : 0);
+                            } else {  // published with its scale and flags
+                                desc.job.d.c = cs;
+                                task_flags = (v >> 20) & (kStatsArgmax | kStatsDraft);
+                            }
                         } else {
+                            __threadfence();  // the job, written before its task was published
                             const int* src = reinterpret_cast<const int*>(jobs() + b);
                             int* dst = reinterpret_cast<int*>(&desc.job);
 #pragma unroll
@@ -2081,7 +2110,7 @@ struct Kern {
             const int am = rt.idx == 0x7fffffff ? 0 : rt.idx;
             if (proposal && x == am) {
                 out[pos] = am;
-                ee_publish(kTaskStats, b, pos + 1);
+                ee_publish(kTaskStats, b, pos + 1, 0.0f, kStatsArgmax);
                 return;
             }
             out[pos] = am;
@@ -2096,7 +2125,8 @@ struct Kern {
                                       : accept_from_logits(lt, ld, rt.m, rt.s, rd.m, rd.s, c, u);
             if (acc) {
                 out[pos] = x;
-                ee_publish(kTaskStats, b, pos + 1);
+                ee_publish(kTaskStats, b, pos + 1, c,
+                           (!a.onehot && pos + 1 < kb && pos + 1 < GM) ? kStatsDraft : 0);
                 return;
             }
         }
@@ -2142,7 +2172,7 @@ struct Kern {
                 if (own_p < a.B) {
                     own_v = ee_encode(kTaskStats, own_p, 0);
                 } else {
-                    const int v = ld_relaxed(ee_tasks() + own_p);
+                    const int v = ld_relaxed(reinterpret_cast<const int*>(ee_slot(own_p)));  // the code
                     if (v) {
                         __threadfence();
                         own_v = v;
@@ -2166,11 +2196,11 @@ struct Kern {
         act_v = __shfl_sync(0xffffffffu, act_v, 0);
         if (known_v != 0 && known_p != pre_p && ((known_v - 1) >> 28) == kTaskStats) {
             const int v = known_v - 1;
-            pre = ee_prefetch((v >> 8) & 0xfffff, v & 0xff);
+            pre = ee_prefetch((v >> 8) & 0xfff, v & 0xff);
             pre_p = known_p;
         }
         if (act_p < 0) return false;
-        const int v = act_v - 1, type = v >> 28, b = (v >> 8) & 0xfffff, pos = v & 0xff;
+        const int v = act_v - 1, type = v >> 28, b = (v >> 8) & 0xfff, pos = v & 0xff;
         if (type == kTaskStats) {
             ee_decide(act_p, b, pos, pre);  // act_p == pre_p: its code was known above at the latest
             pre_p = -1;
