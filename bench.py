@@ -121,7 +121,7 @@ def algorithmic_bytes_early(batch, num_accepted) -> int:
             rows += 1
             continue
         rows += n + 1
-        if batch.temperature[b] > 0:
+        if 0 < batch.temperature[b] < np.inf:
             rows += min(n + 1, G) + (2 if n < G else 1)
     return int(s * V * rows + B * G * 8 + B * 12 + B * (G + 1) * 4)
 
@@ -129,13 +129,32 @@ def algorithmic_bytes_early(batch, num_accepted) -> int:
 def algorithmic_bytes(batch, num_accepted) -> int:
     """Logit bytes the method must read once, plus the re-read of the rows the
     draw needs, plus the small inputs and outputs: s*V*[B(g+1) + g*B_samp +
-    sum over sampled requests (2 if n < g else 1)] + B*g*8 + B*12 + B*(g+1)*4."""
+    sum over valid sampled requests (2 if n < g else 1)] + B*g*8 + B*12 +
+    B*(g+1)*4, B_samp the requests with 0 < T < inf (their draft rows are read
+    whether or not the request turns out valid)."""
     w = batch.workload
     s, V, G, B = w.elem_bytes, w.V, w.gamma, batch.B
-    samp = (batch.temperature > 0) & (num_accepted >= 0)
-    reread = np.where(num_accepted[samp] < G, 2, 1).sum()
+    T = batch.temperature
+    samp = (T > 0) & np.isfinite(T)
+    drawn = samp & (num_accepted >= 0)
+    reread = np.where(num_accepted[drawn] < G, 2, 1).sum()
     rows = B * (G + 1) + G * int(samp.sum()) + int(reread)
     return int(s * V * rows + B * G * 8 + B * 12 + B * (G + 1) * 4)
+
+
+def captured_traffic(workload: str, early: bool, path: str | None = None):
+    """DRAM bytes per launch of this workload's kernel from the committed ncu
+    capture (`profiles/traffic.json`, keyed by workload, `-early` for early
+    exit), or None: no capture, or the kernel sources changed since."""
+    try:
+        with open(path or PROFILE_TRAFFIC) as f:
+            prof = json.load(f)
+        entry = prof.get(workload + ("-early" if early else ""))
+        if entry and entry.get("kernel_hash") == kernel_hash():
+            return entry.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
 
 
 class ClockSampler:
@@ -464,15 +483,7 @@ def main():
     peak, peak_src = peak_hbm()
     avg_call_s = float(per_call_ms.mean()) * 1e-3
     achieved = abytes / avg_call_s / 1e9
-    traffic = None
-    try:
-        with open(PROFILE_TRAFFIC) as f:
-            prof = json.load(f)
-        entry = prof.get(args.workload + ("-early" if args.early_exit else ""))  # the captured kernel's workload
-        if entry and entry.get("kernel_hash") == kernel_hash():
-            traffic = entry.get("dram_bytes_per_launch")
-    except Exception:
-        pass
+    traffic = captured_traffic(args.workload, args.early_exit)
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
     e2e = None
