@@ -1422,7 +1422,7 @@ struct Kern {
         return to_fixed(run_total(S), d.fix);
     }
 
-    // ---- phase 2, finisher: the token of draw job k. The chunk holding
+    // ---- phase 2, search warp of the job's owner: the token of draw job k. The chunk holding
     // floor(u W), then the warp within it, from the stored fixed-point sums;
     // then that warp's 32 runs are re-read and summed exactly as in the
     // streaming pass, and one lane walks its run token by token.
@@ -2183,7 +2183,7 @@ struct Kern {
             known_v = own_v;
             if (own_v != 0 &&
                 ld_relaxed(ee_done() + own_p) >= static_cast<unsigned>(L.NCH)) {
-                __threadfence();  // the other blocks' chunk records and sums
+                __threadfence();  // the other blocks' item records and chunk sums
                 act_p = own_p;
                 act_v = own_v;
                 own_v = 0;
@@ -2527,9 +2527,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     stamp(ph, 6, lane == 0);
 }
 
-// Early-exit verification: the same producer / consumer / finisher warps,
-// with tasks (one position's row statistics, or one draw) taken in
-// publication order instead of a static row schedule and a draw phase.
+// Early-exit verification: the same producer and consumer warps, with tasks
+// (one position's row statistics, or one draw) taken in publication order
+// instead of a static row schedule and a draw phase; the finisher only counts
+// the chunks done, and the search warp owns tasks g, g + G, ...: it decides
+// them (or searches their draws) and publishes what follows.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1) early_kernel(Args a, Layout L, char* ws) {
     extern __shared__ __align__(128) char smem[];
