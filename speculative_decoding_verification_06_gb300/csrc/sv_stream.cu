@@ -9,10 +9,13 @@
 // warps, one producer warp, one finisher warp and one search warp; there is
 // no grid barrier.
 //
-//  1. Row statistics. The target rows of all requests, then the draft rows of
-//     the T > 0 requests (compacted), form one virtual stream of logits that
-//     is cut into G equal 16-byte-aligned slices, one per thread block. The
-//     producer copies its slice through a ring of kStages shared-memory
+//  1. Row statistics. Three streams of logits are each cut into G equal
+//     16-byte-aligned slices, one per thread block: the target rows of the
+//     T > 0 requests, their draft rows, and the target rows of the others
+//     (greedy, or invalid). A block streams its three slices in that order,
+//     so that every request that needs a draw completes while the rows of
+//     those that need none are still streaming. The
+//     producer copies its slices through a ring of kStages shared-memory
 //     stages with cp.async.bulk (completion on mbarriers); the consumers fold
 //     each stage into per-thread (max, sum of 2^(l c - fl(m c))) or argmax
 //     states, and the last warp to finish a row piece writes the block's
@@ -130,7 +133,9 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.vec = 16 / es;
     L.Et = static_cast<long long>(B) * (gamma + 1) * V;
     const long long Ed_max = static_cast<long long>(B) * gamma * V;
-    L.MT = static_cast<int>(((L.Et + G - 1) / G + L.vec - 1) / V + 2);
+    // a block's two target slices (sampled requests', then the others') hold
+    // at most this many rows between them
+    L.MT = static_cast<int>(((L.Et + 2 * G - 1) / G + 2 * L.vec) / V + 6);
     L.MD = static_cast<int>(((Ed_max + G - 1) / G + L.vec - 1) / V + 2);
     const int chunk_elems = kChunkBytes / es;
     L.NCH = (V + chunk_elems - 1) / chunk_elems;
@@ -328,11 +333,14 @@ __device__ __forceinline__ void stamp(unsigned long long* slots, int i, bool who
 struct Ctl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    long long tbeg[kMaxGrid + 1];  // target partition
+    long long tbeg[kMaxGrid + 1];   // partition of the sampled requests' target rows (virtual elements 0..E1)
+    long long t3beg[kMaxGrid + 1];  // ... of the other requests' target rows (virtual elements E1..Et)
     long long dbeg[kMaxGrid + 1];  // draft partition (after the prologue)
     StageDesc desc[kStages];       // draw phase: the item in each stage
     int n_samp;
     int k_lo;  // first compacted request of this block's draft slice
+    int k1_lo;  // first compacted request of this block's sampled-target slice
+    int j3_lo;  // first other request (by its index among them) of this block's other-target slice
     int abort;
     int map[kMapMax];
     int wtmp[kConsumerWarps + 1];
@@ -345,7 +353,10 @@ struct Ctl {
     unsigned fq_tail;                       // reservations so far
     unsigned fq_head;                       // entries the finisher has taken
     int cons_done;                          // consumer warps done with both phases
-    short kmap[kMaxB];                      // compacted index of each T > 0 request, else -1
+    short kmap[kMaxB];                      // compacted index k of each T > 0 request, else -(j + 1),
+                                            // j its index among the others
+    short map1[kMapMax];                    // sampled-target slice: request of compacted index k1_lo + i
+    short map3[kMapMax];                    // other-target slice: request of other index j3_lo + i
     int dset[kStages][SV_MAX_GAMMA];        // tree draws: the excluded tokens of the item in each stage
     int fset[SV_MAX_GAMMA];                 // tree draws: the excluded tokens of the job being searched
     int wset[kConsumerWarps][SV_MAX_GAMMA]; // tree draws: each consumer warp's copy of its item's set
@@ -415,20 +426,53 @@ struct Kern {
 
     __device__ static bool sampled(float T) { return T > 0.0f && T < pos_inf(); }
 
-    // ---- phase-1 schedule: row pieces of this block's slices, in order
+    // ---- phase-1 schedule: row pieces of this block's slices, in order.
+    // Target rows are streamed in a virtual order: the T > 0 requests' rows
+    // (request of compacted index k at virtual rows k (gamma+1) ...), then the
+    // other requests' (index j among them, after all n_samp of the former).
+    // A block streams its slice of the first, its draft slice, and its slice
+    // of the second last, so that the requests that need a draw are complete
+    // (scanned, their jobs published) while the rows of those that need none
+    // still stream.
+
+    // Rows of block gg's slice of the T > 0 requests' target rows: its slice
+    // of the others' rows has its records after them.
+    __device__ int t1_rows(int gg) const {
+        const long long b0 = ctl.tbeg[gg], b1 = ctl.tbeg[gg + 1];
+        return b1 > b0 ? static_cast<int>((b1 - 1) / a.V - b0 / a.V + 1) : 0;
+    }
+
+    // Virtual target elements [vs, ve) of one slice; slot0 is the record slot
+    // of its first row.
     template <typename F>
-    __device__ void for_each_target_segment(long long ts, long long te, F&& f) const {
-        const int V = a.V, GM = a.gamma;
-        const long long first = ts / V;
-        for (long long e = ts; e < te;) {
-            const long long r = e / V;
-            const long long end = min(te, (r + 1) * V);
+    __device__ void for_each_target_segment(long long vs, long long ve, int slot0, F&& f) const {
+        const int V = a.V, GM = a.gamma, ns = ctl.n_samp;
+        const long long first = vs / V;
+        for (long long e = vs; e < ve;) {
+            const long long vr = e / V;
+            const long long end = min(ve, (vr + 1) * V);
+            const long long pos = vr / (GM + 1);
+            const int i = static_cast<int>(vr - pos * (GM + 1));
+            int b = -1;
+            if (pos < ns) {
+                const long long rel = pos - ctl.k1_lo;
+                if (rel >= 0 && rel < kMapMax) b = ctl.map1[rel];
+            } else {
+                const long long rel = pos - ns - ctl.j3_lo;
+                if (rel >= 0 && rel < kMapMax) b = ctl.map3[rel];
+            }
+            const int slot = slot0 + static_cast<int>(vr - first);
+            if (b < 0 || b >= a.B || slot >= L.MT) {  // cannot happen when the host checks hold
+                ctl.abort = 1;
+                return;
+            }
+            const long long row = static_cast<long long>(b) * (GM + 1) + i;  // its place in memory
             Segment sg;
-            sg.src = static_cast<const char*>(a.target) + e * ES;
+            sg.src = static_cast<const char*>(a.target) + (row * V + (e - vr * V)) * ES;
             sg.elems = end - e;
-            sg.e0 = e - r * V;
-            sg.loc = {0, r, static_cast<int>(r / (GM + 1)), static_cast<int>(r - first)};
-            sg.last = end == te || (r + 1) % (GM + 1) == 0;
+            sg.e0 = e - vr * V;
+            sg.loc = {0, vr, b, slot};
+            sg.last = end == ve || (vr + 1) % (GM + 1) == 0;
             f(sg);
             e = end;
         }
@@ -682,12 +726,12 @@ struct Kern {
         }
     }
 
-    // ---- phase-1 prologue (consumers): partition tables, the count of T > 0
-    // requests, the map of this block's draft slice to requests; block 0
-    // publishes the compaction.
+    // ---- phase-1 prologue (consumers): the count of T > 0 requests, the
+    // partition tables of the three streams (the T > 0 requests' target rows,
+    // their draft rows, the other requests' target rows), and the maps of this
+    // block's slices to requests.
     __device__ void prologue() const {
         const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-        for (int gg = t; gg <= G; gg += kConsumers) ctl.tbeg[gg] = part_begin(L.Et, G, gg, L.vec);
         int cnt = 0;
         for (int b = t; b < a.B; b += kConsumers) cnt += sampled(a.temperature[b]) ? 1 : 0;
         cnt = __reduce_add_sync(0xffffffffu, cnt);
@@ -701,9 +745,20 @@ struct Kern {
         const int k_lo = n > 0 ? static_cast<int>(part_begin(E2, G, g, L.vec) /
                                                   (static_cast<long long>(a.gamma) * a.V))
                                : 0;
+        // target rows in request order within each group: T > 0 requests first
+        const long long R = static_cast<long long>(a.gamma + 1) * a.V;
+        const long long E1 = static_cast<long long>(n) * R, E3 = static_cast<long long>(a.B - n) * R;
+        for (int gg = t; gg <= G; gg += kConsumers) {
+            ctl.tbeg[gg] = part_begin(E1, G, gg, L.vec);
+            ctl.t3beg[gg] = E1 + part_begin(E3, G, gg, L.vec);
+        }
+        const int k1_lo = static_cast<int>(part_begin(E1, G, g, L.vec) / R);
+        const int j3_lo = static_cast<int>(part_begin(E3, G, g, L.vec) / R);
         if (t == 0) {
             ctl.n_samp = n;
             ctl.k_lo = k_lo;
+            ctl.k1_lo = k1_lo;
+            ctl.j3_lo = j3_lo;
         }
         bar_sync(kBarConsumers, kConsumers);
         int carry = 0;
@@ -719,13 +774,20 @@ struct Kern {
                 if (w < warp) before += ctl.wtmp[w];
                 total += ctl.wtmp[w];
             }
-            const int k = before + in_warp;
+            const int k = before + in_warp;  // T > 0 requests before b
             if (b < a.B) {
                 if (f) {
                     const int rel = k - k_lo;
                     if (rel >= 0 && rel < kMapMax) ctl.map[rel] = b;
+                    const int rel1 = k - k1_lo;
+                    if (rel1 >= 0 && rel1 < kMapMax) ctl.map1[rel1] = static_cast<short>(b);
+                    ctl.kmap[b] = static_cast<short>(k);
+                } else {
+                    const int j = b - k;  // the others before b
+                    const int rel3 = j - j3_lo;
+                    if (rel3 >= 0 && rel3 < kMapMax) ctl.map3[rel3] = static_cast<short>(b);
+                    ctl.kmap[b] = static_cast<short>(-(j + 1));
                 }
-                ctl.kmap[b] = static_cast<short>(f ? k : -1);
             }
             carry += total;
             bar_sync(kBarConsumers, kConsumers);
@@ -915,14 +977,26 @@ struct Kern {
     // The records of a row's first two pieces are read first (row_load) and
     // merged once the request's temperature is known (row_combine); a row
     // over more slices reads the rest then.
+    // Row kinds: 0 a target row of a T > 0 request, 2 a target row of another
+    // request (`row` virtual in both), 1 a draft row (compacted).
     struct RowRaw {
         uint4 x[2];
         int g0, g1;
     };
+    __device__ const long long* row_part(int kind) const {
+        return kind == 1 ? ctl.dbeg : kind == 2 ? ctl.t3beg : ctl.tbeg;
+    }
+    // The record of `row`'s piece in block gg (whose slice starts at b0).
+    __device__ const uint4* piece_rec(int kind, int gg, long long b0, long long row) const {
+        if (kind == 1)
+            return reinterpret_cast<const uint4*>(rec_d() + static_cast<size_t>(gg) * L.MD +
+                                                  static_cast<int>(row - b0 / a.V));
+        const int slot0 = kind == 2 ? t1_rows(gg) : 0;
+        return reinterpret_cast<const uint4*>(rec_t() + static_cast<size_t>(gg) * L.MT + slot0 +
+                                              static_cast<int>(row - b0 / a.V));
+    }
     __device__ void row_load(int kind, long long row, RowRaw& rr) const {
-        const long long* beg = kind == 0 ? ctl.tbeg : ctl.dbeg;
-        const int MM = kind == 0 ? L.MT : L.MD;
-        const Rec* base = kind == 0 ? rec_t() : rec_d();
+        const long long* beg = row_part(kind);
         const long long e0 = row * a.V, e1 = e0 + a.V - 1;
         rr.g0 = owner(beg, G, e0);
         rr.g1 = owner(beg, G, e1);
@@ -932,9 +1006,7 @@ struct Kern {
             rr.x[q] = make_uint4(0u, 0u, 0u, kNoPiece);
             if (gg <= rr.g1) {
                 const long long b0 = beg[gg], b1 = beg[gg + 1];
-                if (b1 > b0)
-                    rr.x[q] = __ldcg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(gg) * MM +
-                                                                    static_cast<int>(row - b0 / a.V)));
+                if (b1 > b0) rr.x[q] = __ldcg(piece_rec(kind, gg, b0, row));
             }
         }
     }
@@ -954,14 +1026,10 @@ struct Kern {
         take(rr.x[0]);
         take(rr.x[1]);
         if (rr.g1 > rr.g0 + 1) {
-            const long long* beg = kind == 0 ? ctl.tbeg : ctl.dbeg;
-            const int MM = kind == 0 ? L.MT : L.MD;
-            const Rec* base = kind == 0 ? rec_t() : rec_d();
+            const long long* beg = row_part(kind);
             for (int gg = rr.g0 + 2; gg <= rr.g1; ++gg) {
                 const long long b0 = beg[gg], b1 = beg[gg + 1];
-                if (b1 > b0)
-                    take(__ldcg(reinterpret_cast<const uint4*>(base + static_cast<size_t>(gg) * MM +
-                                                               static_cast<int>(row - b0 / a.V))));
+                if (b1 > b0) take(__ldcg(piece_rec(kind, gg, b0, row)));
             }
         }
         Rec out;
@@ -981,7 +1049,10 @@ struct Kern {
     // shared scratch of 2 gamma + 1 row records.
     __device__ void verify_request(int b, Rec* st) const {
         const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V;
-        const int k = ctl.kmap[b];  // compacted index of a T > 0 request, else -1
+        const int k = ctl.kmap[b];  // compacted index of a T > 0 request, else negative
+        // the request's place in the virtual order of target rows, and their kind
+        const int vpos = k >= 0 ? k : ctl.n_samp - k - 1;
+        const int tkind = k >= 0 ? 0 : 2;
         const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
         const bool onehot = a.onehot;
         // The reads come in two rounds. First everything that depends on no
@@ -998,11 +1069,12 @@ struct Kern {
         const float u_l = lane < GM ? a.u_accept[static_cast<size_t>(b) * GM + lane] : 0.0f;
         const int nrows_max = (k >= 0 && !onehot) ? 2 * GM + 1 : GM + 1;
         auto row_of = [&](int r) -> long long {
-            return r <= GM ? static_cast<long long>(b) * (GM + 1) + r : static_cast<long long>(k) * GM + (r - GM - 1);
+            return r <= GM ? static_cast<long long>(vpos) * (GM + 1) + r : static_cast<long long>(k) * GM + (r - GM - 1);
         };
+        auto kind_of = [&](int r) { return r <= GM ? tkind : 1; };
         RowRaw raw0, raw1;
-        if (lane < nrows_max) row_load(lane <= GM ? 0 : 1, row_of(lane), raw0);
-        if (lane + 32 < nrows_max) row_load(lane + 32 <= GM ? 0 : 1, row_of(lane + 32), raw1);
+        if (lane < nrows_max) row_load(kind_of(lane), row_of(lane), raw0);
+        if (lane + 32 < nrows_max) row_load(kind_of(lane + 32), row_of(lane + 32), raw1);
         float lt_l = 0.0f, ld_l = 0.0f;
         if (!a.tree && x_l >= 0 && x_l < V) {
             lt_l = load_logit<DT>(a.target, (static_cast<size_t>(b) * (GM + 1) + lane) * V + x_l);
@@ -1025,8 +1097,8 @@ struct Kern {
         }
         const int nrows = !range_ok ? 0 : (samp && !onehot ? 2 * GM + 1 : np + 1);
         for (int r = lane; r < nrows; r += 32) {
-            const int kind = r <= GM ? 0 : 1;
-            const bool am = kind == 0 && !samp;
+            const int kind = kind_of(r);
+            const bool am = r <= GM && !samp;
             Rec x;
             if (r == lane)
                 x = row_combine(kind, row_of(r), raw0, am, c);
@@ -2309,7 +2381,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         return;
     }
 
-    const long long ts = part_begin(L.Et, K.G, K.g, L.vec), te = part_begin(L.Et, K.G, K.g + 1, L.vec);
     typename KT::Cursor prod, cons;
     constexpr int TPT = KT::kTPT;
     constexpr int CH = KT::kChunkElems;
@@ -2324,9 +2395,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                 ok = K.produce(prod, sg.src + off * KT::ES, static_cast<unsigned>(n * KT::ES));
             }
         };
-        K.for_each_target_segment(ts, te, issue);
-        bar_sync(kBarHandoff, kHandoffThreads);  // the consumers' prologue is done
+        bar_sync(kBarHandoff, kHandoffThreads);  // the consumers' prologue (partitions, maps) is done
+        K.for_each_target_segment(ctl.tbeg[K.g], ctl.tbeg[K.g + 1], 0, issue);
         K.for_each_draft_segment(issue);
+        K.for_each_target_segment(ctl.t3beg[K.g], ctl.t3beg[K.g + 1], K.t1_rows(K.g), issue);
         const int ns = ctl.n_samp;
         if (ns > 0) {
             // draw items i = 0 .. ns * NCH - 1: chunk i % NCH of the job published
@@ -2439,7 +2511,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     }
 
     // ------------------------------------------------------------ consumers
-    // the ring fills with target stages while the consumers run the prologue
+    // the producer starts once the prologue has laid out the three streams
     K.prologue();
     bar_arrive(kBarHandoff, kHandoffThreads);
     bool ok = true;
@@ -2466,8 +2538,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         K.flush_row(rs, sg.loc, seq++, sg.last ? share : 0u);
         if (sg.last) share = 0;
     };
-    K.for_each_target_segment(ts, te, fold);
+    K.for_each_target_segment(ctl.tbeg[K.g], ctl.tbeg[K.g + 1], 0, fold);
     K.for_each_draft_segment(fold);
+    K.for_each_target_segment(ctl.t3beg[K.g], ctl.t3beg[K.g + 1], K.t1_rows(K.g), fold);
     stamp(ph, 2, lane == 0);
 
     if (ctl.n_samp > 0 && ok) {
@@ -2608,9 +2681,10 @@ __global__ void __launch_bounds__(kThreads, 1) early_kernel(Args a, Layout L, ch
     stamp(ph, 6, lane == 0);
 }
 
-size_t smem_bytes() {
-    return static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl) + sizeof(Rec) * kMaxRowsPerReq;
-}
+constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + sizeof(Ctl) + sizeof(Rec) * kMaxRowsPerReq;
+static_assert(kSmemBytes <= 232448, "dynamic shared memory above the 227 KB a block may opt in to");
+
+size_t smem_bytes() { return kSmemBytes; }
 
 }  // namespace
 
