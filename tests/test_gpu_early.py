@@ -123,3 +123,12 @@ def test_bad_rows_read_make_the_request_invalid():
 def test_full_size(cfg):
     rep, n = check(model_batch(synthetic.WORKLOADS[cfg], seed=cfg, poison_after=False))
     assert rep.invalid == 0
+
+
+@pytest.mark.parametrize("grid", [0, 37])
+def test_largest_batch(grid):
+    """B = 4096 with early exit: task codes carry request numbers up to 4095."""
+    w = synthetic.WORKLOADS[4].variant(B=4096, gamma=2, V=64)
+    b = model_batch(w, seed=43, poison_after=False)
+    rep, n = check(b, path=2, grid_ctas=grid)
+    assert rep.requests == 4096 and (n >= 0).all()

@@ -306,3 +306,15 @@ def test_one_launch_per_call():
     batch = synthetic.generate(_small(4, B=8, V=8192))
     parity.run_gpu(batch, debug=False)
     assert sv.last_launch_count() == 1
+
+
+@pytest.mark.parametrize("grid", [0, 37])
+def test_largest_batch_streaming(grid):
+    """B = 4096, the most the streaming path takes: the compaction's indices
+    and its slice maps run to their ends (a mixed batch, so every block holds
+    slices of both groups of target rows)."""
+    w = synthetic.WORKLOADS[4].variant(B=4096, gamma=2, V=64)
+    batch = synthetic.generate(w, seed=41)
+    assert 0 < int((batch.temperature > 0).sum()) < batch.B
+    rep = parity.check(batch, path=sv.SV_PATH_STREAMING, grid_ctas=grid)
+    assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
