@@ -132,3 +132,11 @@ def test_largest_batch(grid):
     b = model_batch(w, seed=43, poison_after=False)
     rep, n = check(b, path=2, grid_ctas=grid)
     assert rep.requests == 4096 and (n >= 0).all()
+
+
+@pytest.mark.parametrize("opts", OPTS, ids=OPT_IDS)
+def test_largest_gamma(opts):
+    """gamma = 64 with early exit: positions up to 64 in the task codes."""
+    w = synthetic.WORKLOADS[4].variant(B=8, gamma=64, V=1024)
+    for seed in (3, 4):
+        check(model_batch(w, seed), **opts)

@@ -203,3 +203,11 @@ def test_propose_verify_commit_loop_on_the_gpu():
         assert np.array_equal(lens_g.cpu().numpy(), lens_o), step
         assert np.array_equal(buf_g.cpu().numpy(), buf_o), step
     assert int(lens_o.sum() - h.seq_lens.sum()) > 3 * B  # some proposals were accepted
+
+
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM, dict(path=2, grid_ctas=3)], ids=["rowwise", "stream", "stream-g3"])
+def test_largest_gamma(opts):
+    """Up to 64 deterministic proposals per request."""
+    w = synthetic.WORKLOADS[4].variant(B=10, gamma=64, V=1024)
+    for seed in (5, 6):
+        check(onehot_batch(w, seed), **opts)

@@ -318,3 +318,15 @@ def test_largest_batch_streaming(grid):
     assert 0 < int((batch.temperature > 0).sum()) < batch.B
     rep = parity.check(batch, path=sv.SV_PATH_STREAMING, grid_ctas=grid)
     assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
+
+
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=3)],
+                         ids=["rowwise", "stream", "stream-g3"])
+def test_largest_gamma(opts):
+    """gamma = 64, the most the library takes: 129 rows per sampled request,
+    two per lane in the scan's first round and the rest one by one."""
+    w = synthetic.WORKLOADS[4].variant(B=6, gamma=sv.SV_MAX_GAMMA, V=1024)
+    for k in range(2):
+        batch = synthetic.generate(w, k=k)
+        rep = parity.check(batch, **opts)
+        assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B

@@ -211,3 +211,11 @@ def test_tree_options_checked():
                               sv._ptr(_dev(t["us"])), sv._ptr(_dev(t["T"])), sv._ptr(z), sv._ptr(z), None, None, 0,
                               None, None, None, ctypes.byref(o))
     assert rc == sv.SV_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("opts", PATHS, ids=PATH_IDS)
+def test_largest_tree(opts):
+    """Trees of 64 nodes, the most the library takes."""
+    t = random_trees(16, 64, 1024, "bf16", seed=9)
+    gpu = run_gpu(t, **opts)
+    compare(t, gpu)
