@@ -44,18 +44,28 @@ struct Shared {
     int draw_row;            // the row of the draw (tree: the last node)
 };
 
+// Logits a thread folds into one partial before the partial joins its running
+// state: the binary32 sums then stay short at any V (a thread sees V / 128 of a
+// row, 131072 logits at V = 2^24).
+constexpr int kInner = 64;
+
 template <int DT>
 __device__ RowStat row_maxsum(const void* base, size_t row, int V, float c, Shared& sh) {
     MaxSum st = maxsum_empty();
     int bad = 0;
     const size_t off = row * static_cast<size_t>(V);
-    for (int x = threadIdx.x; x < V; x += kThreads) {
-        float l = load_logit<DT>(base, off + x);
-        if (bad_logit(l)) {
-            bad = 1;
-        } else {
-            maxsum_add(st, l, c);
+    for (int x0 = threadIdx.x; x0 < V; x0 += kThreads * kInner) {
+        MaxSum part = maxsum_empty();
+        const int x1 = static_cast<int>(min(static_cast<long long>(V), static_cast<long long>(x0) + kThreads * kInner));
+        for (int x = x0; x < x1; x += kThreads) {
+            const float l = load_logit<DT>(base, off + x);
+            if (bad_logit(l)) {
+                bad = 1;
+            } else {
+                maxsum_add(part, l, c);
+            }
         }
+        st = maxsum_merge(st, part, c);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -131,6 +141,11 @@ __device__ __forceinline__ float draw_weight(const void* tgt, const void* dft, s
     return weight_target_excl(lt, e, d, kind);
 }
 
+// A thread's tokens are summed in runs of kRun: each run in binary32 in index
+// order, converted to fixed point, and the runs added exactly, so that no
+// binary32 sum is longer than kRun at any V.
+constexpr int kRun = 32;
+
 template <int DT>
 __device__ __forceinline__ float run_weights(const void* tgt, const void* dft, size_t trow,
                                              size_t drow, int lo, int hi, const DrawParams& d,
@@ -138,6 +153,16 @@ __device__ __forceinline__ float run_weights(const void* tgt, const void* dft, s
     float run = 0.0f;
     for (int e = lo; e < hi; ++e) run = __fadd_rn(run, draw_weight<DT>(tgt, dft, trow, drow, e, d, kind, excl, nexcl));
     return run;
+}
+
+// The fixed-point sum of tokens [lo, hi), run by run.
+template <int DT>
+__device__ unsigned long long range_weights(const void* tgt, const void* dft, size_t trow, size_t drow, int lo,
+                                            int hi, const DrawParams& d, int kind, const int* excl, int nexcl) {
+    unsigned long long q = 0ull;
+    for (int r = lo; r < hi; r += kRun)
+        q += to_fixed(run_weights<DT>(tgt, dft, trow, drow, r, min(hi, r + kRun), d, kind, excl, nexcl), d.fix);
+    return q;
 }
 
 template <int DT>
@@ -423,27 +448,39 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             const int E = (V + kThreads - 1) / kThreads;
             const int lo = min(V, static_cast<int>(threadIdx.x) * E), hi = min(V, lo + E);
             int kind = d.kind;
-            float run = run_weights<DT>(a.target, a.draft, trow, drow, lo, hi, d, kind, sh.excl, nexcl);
-            unsigned long long qv = to_fixed(run, d.fix), total;
+            unsigned long long qv = range_weights<DT>(a.target, a.draft, trow, drow, lo, hi, d, kind, sh.excl, nexcl);
+            unsigned long long total;
             unsigned long long excl = block_excl_scan_u64<kThreads>(qv, sh.scan, &total);
             if (total == 0ull) {
                 // Residual weights that round to zero everywhere: draw from p_n.
                 kind = kKindBonus;
                 d.fix = kFixTarget;
-                run = run_weights<DT>(a.target, a.draft, trow, drow, lo, hi, d, kind, sh.excl, nexcl);
-                qv = to_fixed(run, d.fix);
+                qv = range_weights<DT>(a.target, a.draft, trow, drow, lo, hi, d, kind, sh.excl, nexcl);
                 excl = block_excl_scan_u64<kThreads>(qv, sh.scan, &total);
             }
             const unsigned long long t = scale_uniform(a.u_sample[b], total);
             if (excl <= t && t < excl + qv) {
-                float run2 = 0.0f;
+                // the run holding t, then the token, with the same run sums
                 int token = hi - 1;
-                for (int e = lo; e < hi; ++e) {
-                    run2 = __fadd_rn(run2, draw_weight<DT>(a.target, a.draft, trow, drow, e, d, kind, sh.excl, nexcl));
-                    if (excl + to_fixed(run2, d.fix) > t) {
-                        token = e;
+                unsigned long long before = excl;
+                for (int r = lo; r < hi; r += kRun) {
+                    const int r1 = min(hi, r + kRun);
+                    const unsigned long long qr = to_fixed(
+                        run_weights<DT>(a.target, a.draft, trow, drow, r, r1, d, kind, sh.excl, nexcl), d.fix);
+                    if (before + qr > t) {
+                        float run2 = 0.0f;
+                        token = r1 - 1;
+                        for (int e = r; e < r1; ++e) {
+                            run2 = __fadd_rn(run2,
+                                             draw_weight<DT>(a.target, a.draft, trow, drow, e, d, kind, sh.excl, nexcl));
+                            if (before + to_fixed(run2, d.fix) > t) {
+                                token = e;
+                                break;
+                            }
+                        }
                         break;
                     }
+                    before += qr;
                 }
                 out[n] = token;
             }

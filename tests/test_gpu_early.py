@@ -140,3 +140,9 @@ def test_largest_gamma(opts):
     w = synthetic.WORKLOADS[4].variant(B=8, gamma=64, V=1024)
     for seed in (3, 4):
         check(model_batch(w, seed), **opts)
+
+
+def test_longest_row_streaming():
+    """Early exit at V = 1572864 (bf16): 128 chunks a row, 32 items a task."""
+    w = synthetic.WORKLOADS[4].variant(B=3, gamma=2, V=128 * 24576 // 2)
+    check(model_batch(w, seed=54), path=2)

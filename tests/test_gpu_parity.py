@@ -330,3 +330,35 @@ def test_largest_gamma(opts):
         batch = synthetic.generate(w, k=k)
         rep = parity.check(batch, **opts)
         assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
+
+
+STREAM_V_MAX_BF16 = 128 * 24576 // 2  # 128 draw chunks of 24 KB: the longest bf16 row the streaming path takes
+
+
+@pytest.mark.parametrize("grid", [0, 7])
+def test_longest_row_streaming(grid):
+    """V = 1572864 (bf16): the token search scans 128 chunk totals, four per lane."""
+    w = synthetic.WORKLOADS[4].variant(B=3, gamma=2, V=STREAM_V_MAX_BF16)
+    batch = synthetic.generate(w, seed=51)
+    rep = parity.check(batch, path=sv.SV_PATH_STREAMING, grid_ctas=grid)
+    assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
+
+
+def test_row_past_the_streaming_limit_goes_one_block_per_request():
+    import torch
+    w = synthetic.WORKLOADS[4].variant(B=2, gamma=1, V=STREAM_V_MAX_BF16 + 8)
+    batch = synthetic.generate(w, seed=52)
+    with pytest.raises(sv.SpecVerifyError) as err:
+        parity.run_gpu(batch, path=sv.SV_PATH_STREAMING)
+    assert err.value.status == sv.SV_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    rep = parity.check(batch)  # the library's own choice
+    assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
+
+
+def test_largest_vocabulary():
+    """V = 2^24 (fp32), the most the library takes: one block per request."""
+    w = synthetic.WORKLOADS[3].variant(B=1, gamma=1, V=sv.SV_MAX_V, hot_tokens=5)
+    batch = synthetic.generate(w, seed=53)
+    rep = parity.check(batch)
+    assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
