@@ -28,7 +28,11 @@
  * smallest k with C_k > u_sample * W, C_k the inclusive prefix sum of the
  * weights in index order and W their total (if rounding leaves none, the last
  * k with a positive weight); residual weights that sum to zero fall back to
- * p at that position; argmax ties go to the lowest index.
+ * p at that position; argmax ties go to the lowest index; a temperature in
+ * (0, 2^-16) is read as 2^-16 (p is then one-hot to within e^-128 for logits
+ * more than 2^-9 apart, and the binary32 row statistics stay in range for
+ * logits up to ~2.2e4); alpha is evaluated from the logits, so it stays exact
+ * when p(x) and q(x) both lie below the floating-point range.
  *
  * Conventions for every entry point:
  *  - Memory: the caller owns every buffer. Array arguments of spec_verify and

@@ -63,6 +63,15 @@ static int row_argmax(const double* l, int V) {
     return a;
 }
 
+/* Reading (temperature floor): 0 < T < 2^-16 is read as T = 2^-16. The pages
+ * define p = softmax(l/T) for T > 0 and the greedy rule at T = 0; they do not
+ * say how close to 0 a positive T may come. At 2^-16 the softmax of logits
+ * more than 2^-9 apart is already one-hot to within e^-128. NaN, negative and
+ * infinite T are left as they are (such requests are invalid), and T = 0
+ * stays the greedy rule. */
+#define ORACLE_TEMP_MIN 0x1p-16
+static double temp_floor(double T) { return (T > 0.0 && T < ORACLE_TEMP_MIN) ? ORACLE_TEMP_MIN : T; }
+
 /* Temperature softmax p(x) = exp(l(x)/T) / sum_y exp(l(y)/T), evaluated as
  * exp((l(x) - m)/T) / Z with m the row max so that no term overflows; Z is
  * summed in index order. Returns log sum_y exp(l(y)/T) = m/T + log Z. */
@@ -75,6 +84,20 @@ static double softmax_T(const double* l, int V, double T, double* p) {
     }
     for (int x = 0; x < V; ++x) p[x] /= Z;
     return m / T + log(Z);
+}
+
+/* alpha = min(1, p(x) / q(x)) (eq. alpha(x) of the wiki page "Speculative
+ * Decoding") for the softmax rows whose log-normalisers are lse_p and lse_q,
+ * evaluated as exp(log p(x) - log q(x)) with log p(x) = l(x)/T - lse_p: the
+ * same value as the ratio of the probabilities, still defined when both lie
+ * below the fp64 range (at small T they underflow together while their ratio
+ * need not be small). A softmax probability is 0 only at a -inf logit: then
+ * alpha = 1 if q(x) = 0 < p(x), 0 if p(x) = 0 (reading R3). */
+static double accept_alpha(double lt_x, double lse_p, double ld_x, double lse_q, double T) {
+    if (lt_x == -INFINITY) return 0.0;
+    if (ld_x == -INFINITY) return 1.0;
+    const double lr = (lt_x / T - lse_p) - (ld_x / T - lse_q);
+    return lr >= 0.0 ? 1.0 : exp(lr);
 }
 
 /* Inverse-CDF draw over non-negative weights w (need not sum to one):
@@ -218,15 +241,11 @@ static int verify_sampled(const scratch_t* s, int b, double T, const int32_t* to
         size_t r = (size_t)b * (size_t)G + (size_t)i;
         int x = tok[i];
         load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
-        softmax_T(s->lt, V, T, s->p);
+        const double lse_p = softmax_T(s->lt, V, T, s->p);
         load_row(s->draft, s->dtype, r, V, s->ld);
-        softmax_T(s->ld, V, T, s->q);
+        const double lse_q = softmax_T(s->ld, V, T, s->q);
         double px = s->p[x], qx = s->q[x];
-        double alpha;
-        if (qx > 0.0)
-            alpha = px / qx < 1.0 ? px / qx : 1.0;
-        else
-            alpha = px > 0.0 ? 1.0 : 0.0;
+        double alpha = accept_alpha(s->lt[x], lse_p, s->ld[x], lse_q, T);
         double u = (double)ua[i];
         set_d(d->p_x, r, px);
         set_d(d->q_x, r, qx);
@@ -297,7 +316,7 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype, int B, 
     for (int b = 0; b < B; ++b) {
         const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
         int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
-        double T = (double)temperature[b];
+        double T = temp_floor((double)temperature[b]);
         for (int j = 0; j <= gamma; ++j) out[j] = -1;
         clear_detail(d, b, gamma);
         if (!request_valid(&s, b, T, tok)) {
@@ -451,7 +470,7 @@ int oracle_spec_verify_onehot(const void* target, int dtype, int B, int gamma, i
     for (int b = 0; b < B; ++b) {
         const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
         int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
-        double T = (double)temperature[b];
+        double T = temp_floor((double)temperature[b]);
         int k = num_draft[b];
         for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
         clear_detail(d, b, gamma);
@@ -501,7 +520,11 @@ static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok,
         if (!row_ok_at(s, s->target, tr, s->lt)) return -1;
         set_d(d->max_target, tr, row_max(s->lt, V));
         set_i(d->argmax_target, tr, row_argmax(s->lt, V));
-        if (T > 0.0) set_d(d->lse_target, tr, softmax_T(s->lt, V, T, s->p));
+        double lse_p = 0.0;
+        if (T > 0.0) {
+            lse_p = softmax_T(s->lt, V, T, s->p);
+            set_d(d->lse_target, tr, lse_p);
+        }
         if (i == k) break; /* the extra-token row */
         const int x = tok[i];
         size_t r = (size_t)b * (size_t)G + (size_t)i;
@@ -515,18 +538,18 @@ static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok,
             continue;
         }
         double qx = 1.0;
+        double alpha;
+        const double px = s->p[x];
         if (!onehot) {
             if (!row_ok_at(s, s->draft, r, s->ld)) return -1;
             set_d(d->max_draft, r, row_max(s->ld, V));
-            set_d(d->lse_draft, r, softmax_T(s->ld, V, T, s->q));
+            const double lse_q = softmax_T(s->ld, V, T, s->q);
+            set_d(d->lse_draft, r, lse_q);
             qx = s->q[x];
+            alpha = accept_alpha(s->lt[x], lse_p, s->ld[x], lse_q, T);
+        } else {
+            alpha = fmin(px, 1.0);  /* q one-hot at the proposal */
         }
-        const double px = s->p[x];
-        double alpha;
-        if (qx > 0.0)
-            alpha = fmin(px / qx, 1.0);
-        else
-            alpha = (px > 0.0) ? 1.0 : 0.0;
         const double u = (double)ua[i];
         set_d(d->p_x, r, px);
         set_d(d->q_x, r, qx);
@@ -598,7 +621,7 @@ int oracle_spec_verify_early(const void* target, const void* draft, int dtype, i
     for (int b = 0; b < B; ++b) {
         const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
         int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
-        const double T = (double)temperature[b];
+        const double T = temp_floor((double)temperature[b]);
         const int k = draft ? gamma : num_draft[b];
         for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
         clear_detail(d, b, gamma);
@@ -746,7 +769,7 @@ int oracle_spec_verify_tree(const void* target, int dtype, int B, int gamma, int
         const int32_t* par = parents + (size_t)b * (size_t)gamma;
         int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
         int32_t* nodes = out_nodes + (size_t)b * (size_t)gamma;
-        const double T = (double)temperature[b];
+        const double T = temp_floor((double)temperature[b]);
         const int m = num_nodes[b];
         for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
         for (int j = 0; j < gamma; ++j) nodes[j] = -1;

@@ -43,7 +43,14 @@ __device__ __forceinline__ float ex2(float x) {
 
 // c = log2(e) / T, one correctly rounded binary32 division of the binary32
 // log2(e) (no FP64 on the hot path: FP64 is a small fraction of FP32 here).
-__device__ __forceinline__ float temp_scale(float T) { return __fdiv_rn(1.44269504088896340736f, T); }
+// Temperatures in (0, 2^-16) are read as 2^-16. The row statistics sum
+// 2^(l c - fl(m c)) with c = log2(e) / T; the largest term is 2^r, r the
+// rounding error of fl(m c), which stays far from overflow while |m c| < 2^31
+// (logits up to ~2.2e4 at T = 2^-16). At T = 2^-16, p is one-hot (uniform over
+// exact ties) to within e^-128 for logits more than 2^-9 apart.
+constexpr float kTempMin = 1.52587890625e-05f;  // 2^-16
+__device__ __forceinline__ float temp_floor(float T) { return (T > 0.0f && T < kTempMin) ? kTempMin : T; }
+__device__ __forceinline__ float temp_scale(float T) { return __fdiv_rn(1.44269504088896340736f, temp_floor(T)); }
 
 __device__ __forceinline__ float bf16_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 __device__ __forceinline__ float bf16x2_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -124,12 +131,6 @@ __device__ __forceinline__ double prob_from_stats(float l, float m, float s, flo
     return exp2(static_cast<double>(l) * static_cast<double>(c) - mc) / static_cast<double>(s);
 }
 
-// u < alpha with alpha = min(1, p/q); alpha = 1 if q == 0 < p, 0 if p == q == 0.
-__device__ __forceinline__ bool accept_draft(double p, double q, float u) {
-    double alpha = q > 0.0 ? fmin(1.0, p / q) : (p > 0.0 ? 1.0 : 0.0);
-    return static_cast<double>(u) < alpha;
-}
-
 // The accept test u < min(1, p(x)/q(x)) from the gathered logits and the two
 // rows' (m, s): p/q = 2^e * s_q / s_p with e = (lt - ld) c - (fl(mp c) - fl(mq c)),
 // e formed exactly in double, then rounded once and raised on the SFU (relative
@@ -157,7 +158,7 @@ __device__ __forceinline__ bool accept_from_logits(float lt, float ld, float mp,
 __device__ __forceinline__ double lse_from_stats(float m, float s, float c, float T) {
     const double mc_exact = static_cast<double>(m) * static_cast<double>(c);
     const double mc = static_cast<double>(scaled_max(m, c));
-    return static_cast<double>(m) / static_cast<double>(T) + log(static_cast<double>(s)) -
+    return static_cast<double>(m) / static_cast<double>(temp_floor(T)) + log(static_cast<double>(s)) -
            (mc_exact - mc) * 0.69314718055994530942;
 }
 

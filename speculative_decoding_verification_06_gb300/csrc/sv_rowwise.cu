@@ -213,13 +213,16 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                             stop = tok[i] != st.idx ? 1 : 0;
                         } else {
                             const int x = tok[i];
-                            const double p = prob_from_stats(
-                                load_logit<DT>(a.target, trow * V + x), st.m, st.s, c);
-                            const double q = a.onehot ? 1.0
-                                                      : prob_from_stats(load_logit<DT>(
-                                                                            a.draft, (static_cast<size_t>(b) * G + i) * V + x),
-                                                                        sd.m, sd.s, c);
-                            stop = accept_draft(p, q, a.u_accept[static_cast<size_t>(b) * G + i]) ? 0 : 1;
+                            const float lt = load_logit<DT>(a.target, trow * V + x);
+                            const float u = a.u_accept[static_cast<size_t>(b) * G + i];
+                            // alpha from the logits: p(x) and q(x) may both lie below
+                            // the floating-point range while their ratio does not
+                            const bool acc =
+                                a.onehot ? accept_from_logits(lt, 0.0f, st.m, st.s, 0.0f, 1.0f, c, u)
+                                         : accept_from_logits(
+                                               lt, load_logit<DT>(a.draft, (static_cast<size_t>(b) * G + i) * V + x),
+                                               st.m, st.s, sd.m, sd.s, c, u);
+                            stop = acc ? 0 : 1;
                         }
                     }
                     sh.stop = stop;
@@ -398,12 +401,16 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                     const size_t dr = static_cast<size_t>(b) * G + i;
                     const RowStat& sp = sh.st[i];
                     const RowStat& sq = sh.st[G + 1 + i];
-                    double p = prob_from_stats(load_logit<DT>(a.target, tr * V + x), sp.m, sp.s, c);
+                    const float lt = load_logit<DT>(a.target, tr * V + x);
+                    const float ld = a.onehot ? 0.0f : load_logit<DT>(a.draft, dr * V + x);
+                    if (a.dbg.p_x) a.dbg.p_x[dr] = prob_from_stats(lt, sp.m, sp.s, c);
                     // a one-hot proposal has q(x) = 1
-                    double q = a.onehot ? 1.0 : prob_from_stats(load_logit<DT>(a.draft, dr * V + x), sq.m, sq.s, c);
-                    if (a.dbg.p_x) a.dbg.p_x[dr] = p;
-                    if (a.dbg.q_x) a.dbg.q_x[dr] = q;
-                    if (!accept_draft(p, q, ua[i])) {
+                    if (a.dbg.q_x) a.dbg.q_x[dr] = a.onehot ? 1.0 : prob_from_stats(ld, sq.m, sq.s, c);
+                    // alpha from the logits: p(x) and q(x) may both lie below the
+                    // floating-point range while their ratio does not
+                    const bool acc = a.onehot ? accept_from_logits(lt, 0.0f, sp.m, sp.s, 0.0f, 1.0f, c, ua[i])
+                                              : accept_from_logits(lt, ld, sp.m, sp.s, sq.m, sq.s, c, ua[i]);
+                    if (!acc) {
                         n = i;
                         break;
                     }

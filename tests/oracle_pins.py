@@ -242,6 +242,33 @@ def pin_small_temperature_matches_greedy(lib, quick=False):
     assert np.array_equal(n1, n0) and np.array_equal(o1, o0)
 
 
+def pin_temperature_floor(lib, quick=False):
+    """The reading on temperatures below 2^-16: any 0 < T < 2^-16 gives
+    exactly the outputs of T = 2^-16 (checked at T = 1e-6, 1e-20 and the
+    binary32 subnormal 1e-40), and T = 2^-16 itself gives the greedy result
+    when every runner-up is at least 2^-9 below the max (p and q are one-hot to
+    within e^-128 there)."""
+    rng = np.random.Generator(np.random.Philox(67))
+    B, G, V = 64, 3, 50
+    lt = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+    ld = rng.normal(0, 2, (B, G, V)).astype(np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    ref = _run(lib, lt, ld, x, ua, us, np.full(B, 2.0 ** -16, np.float32))
+    for T in (1e-6, 1e-20, 1e-40):
+        o, n, _ = _run(lib, lt, ld, x, ua, us, np.full(B, T, np.float32))
+        assert np.array_equal(n, ref[1]) and np.array_equal(o, ref[0]), T
+    for arr in (lt, ld):
+        flat = arr.reshape(-1, V)
+        top = rng.integers(V, size=flat.shape[0])
+        flat[np.arange(flat.shape[0]), top] = flat.max(axis=1) + 2.0 ** -8
+    xg = np.argmax(ld, axis=2).astype(np.int32)
+    o1, n1, _ = _run(lib, lt, ld, xg, ua, us, np.full(B, 2.0 ** -16, np.float32))
+    o0, n0, _ = _run(lib, lt, ld, xg, ua, us, np.zeros(B, np.float32))
+    assert np.array_equal(n1, n0) and np.array_equal(o1, o0)
+
+
 # ------------------------------------------------------------ normalisers etc.
 
 def pin_logsumexp_and_row_facts(lib, quick=False):
@@ -640,6 +667,7 @@ ALL_PINS = [
     pin_position_acceptance,
     pin_greedy_is_argmax_decoding,
     pin_small_temperature_matches_greedy,
+    pin_temperature_floor,
     pin_logsumexp_and_row_facts,
     pin_residual_mass_identity,
     pin_equal_rows_reduce_to_categorical,

@@ -146,3 +146,12 @@ def test_longest_row_streaming():
     """Early exit at V = 1572864 (bf16): 128 chunks a row, 32 items a task."""
     w = synthetic.WORKLOADS[4].variant(B=3, gamma=2, V=128 * 24576 // 2)
     check(model_batch(w, seed=54), path=2)
+
+
+@pytest.mark.parametrize("T", [1e-4, 1e-20])
+def test_small_temperatures(T):
+    w = synthetic.WORKLOADS[4].variant(B=16, gamma=3, V=4096)
+    b = model_batch(w, seed=11, poison_after=False)
+    b.temperature = np.full_like(b.temperature, np.float32(T))
+    for opts in (ROWWISE, STREAM):
+        check(b, **opts)

@@ -362,3 +362,19 @@ def test_largest_vocabulary():
     batch = synthetic.generate(w, seed=53)
     rep = parity.check(batch)
     assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
+
+
+@pytest.mark.parametrize("T", [1e-4, 1e-8, 1e-20, 1e-40])
+@pytest.mark.parametrize("cfg", [3, 4], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+def test_small_temperatures(T, cfg, opts):
+    """T -> 0+: below 2^-16 both sides read T as 2^-16; p and q are then near
+    one-hot, so residual masses fall below what binary32 resolves and those
+    draws are judged as near ties (the draw from p of the fallback reading is
+    valid there too)."""
+    w = synthetic.WORKLOADS[cfg].variant(B=16, gamma=3, V=4096)
+    for seed in (7, 8):
+        batch = synthetic.generate(w, seed=seed)
+        batch.temperature[:] = np.float32(T)
+        rep = parity.check(batch, **opts)
+        assert rep.invalid == 0

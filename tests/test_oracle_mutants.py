@@ -17,12 +17,13 @@ from oracle_pins import ALL_PINS
 SRC = os.path.join(os.path.dirname(oracle.__file__), "specverify_oracle.c")
 
 SAMPLED_TARGET_ROW = ("load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);\n"
-                      "        softmax_T(s->lt, V, T, s->p);\n        load_row(s->draft")
+                      "        const double lse_p = softmax_T(s->lt, V, T, s->p);\n        load_row(s->draft")
 SAMPLED_BONUS_ROW = ("load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)G, V, s->lt);\n"
                      "        softmax_T")
 
 MUTANTS = [
-    ("alpha_q_over_p", "alpha = px / qx < 1.0 ? px / qx : 1.0;", "alpha = qx / px < 1.0 ? qx / px : 1.0;"),
+    ("alpha_q_over_p", "const double lr = (lt_x / T - lse_p) - (ld_x / T - lse_q);",
+     "const double lr = (ld_x / T - lse_q) - (lt_x / T - lse_p);"),
     ("accept_flipped", "if (u < alpha) {", "if (u > alpha) {"),
     ("residual_q_minus_p", "double diff = s->p[x] - s->q[x];", "double diff = s->q[x] - s->p[x];"),
     ("temperature_multiplied", "p[x] = exp((l[x] - m) / T);", "p[x] = exp((l[x] - m) * T);"),
@@ -39,9 +40,9 @@ MUTANTS = [
      "            out[i] = a;\n            return i + 1;"),
     ("target_row_stride_gamma", SAMPLED_TARGET_ROW,
      SAMPLED_TARGET_ROW.replace("(size_t)b * (size_t)(G + 1) + (size_t)i", "(size_t)b * (size_t)G + (size_t)i")),
-    ("draft_rows_reversed", "load_row(s->draft, s->dtype, r, V, s->ld);\n        softmax_T(s->ld, V, T, s->q);",
+    ("draft_rows_reversed", "load_row(s->draft, s->dtype, r, V, s->ld);\n        const double lse_q = softmax_T(s->ld, V, T, s->q);",
      "load_row(s->draft, s->dtype, (size_t)b * (size_t)G + (size_t)(G - 1 - i), V, s->ld);\n"
-     "        softmax_T(s->ld, V, T, s->q);"),
+     "        const double lse_q = softmax_T(s->ld, V, T, s->q);"),
     ("bf16_decoded_wrong", "[idx]) << 16;", "[idx]) << 15;"),
     ("accepted_token_not_copied", "            out[i] = x;\n        } else {", "            out[i] = tok[0];\n        } else {"),
     ("no_padding_after_n", "for (int j = 0; j <= gamma; ++j) out[j] = -1;",
@@ -50,7 +51,7 @@ MUTANTS = [
      "            n = i;\n            if (i + 1 < G) {\n"
      "                load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)(i + 1), V, s->lt);\n"
      "                softmax_T(s->lt, V, T, s->p);\n            }\n            break;"),
-    ("q_zero_rejects", "alpha = px > 0.0 ? 1.0 : 0.0;", "alpha = 0.0;"),
+    ("q_zero_rejects", "    if (ld_x == -INFINITY) return 1.0;", "    if (ld_x == -INFINITY) return 0.0;"),
     ("nan_not_detected", "if (isnan(l[x])) return 0;", "if (0) return 0;"),
     ("draw_from_first_token", "        if (C > t) {", "        if (C >= 0.0) {"),
     # deterministic (one-hot) proposals
@@ -60,7 +61,8 @@ MUTANTS = [
      "(size_t)b * (size_t)(G + 1) + (size_t)G, V, s->lt);\n        softmax_T"),
     ("onehot_count_ignored", "        int k = num_draft[b];", "        int k = gamma;"),
     # early exit
-    ("early_alpha_ignores_q", "            alpha = fmin(px / qx, 1.0);", "            alpha = fmin(px, 1.0);"),
+    ("early_alpha_ignores_q", "            alpha = accept_alpha(s->lt[x], lse_p, s->ld[x], lse_q, T);",
+     "            alpha = fmin(px, 1.0);"),
     ("early_greedy_keeps_draft_token", "                out[i] = a;\n                return i;",
      "                out[i] = x;\n                return i;"),
     ("early_extra_token_from_row_k_minus_1", "    for (int i = 0; i <= k; ++i) {\n        size_t tr",
