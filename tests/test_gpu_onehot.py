@@ -211,3 +211,12 @@ def test_largest_gamma(opts):
     w = synthetic.WORKLOADS[4].variant(B=10, gamma=64, V=1024)
     for seed in (5, 6):
         check(onehot_batch(w, seed), **opts)
+
+
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+@pytest.mark.parametrize("T", [1e-4, 1e-20])
+def test_small_temperatures(opts, T):
+    w = synthetic.WORKLOADS[4].variant(B=24, gamma=6, V=2048)
+    b = onehot_batch(w, 17)
+    b.temperature = np.full_like(b.temperature, np.float32(T))
+    check(b, **opts)

@@ -219,3 +219,12 @@ def test_largest_tree(opts):
     t = random_trees(16, 64, 1024, "bf16", seed=9)
     gpu = run_gpu(t, **opts)
     compare(t, gpu)
+
+
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+def test_small_temperatures(opts):
+    """Trees at T = 1e-6 and 1e-20 (read as 2^-16): one-hot rows, so the
+    renormalised mass left after rejected children can be tiny."""
+    t = random_trees(32, 8, 1024, "bf16", seed=13, temps=(1e-6, 1e-20))
+    gpu = run_gpu(t, **opts)
+    compare(t, gpu)
