@@ -378,3 +378,43 @@ def test_small_temperatures(T, cfg, opts):
         batch.temperature[:] = np.float32(T)
         rep = parity.check(batch, **opts)
         assert rep.invalid == 0
+
+
+@pytest.mark.parametrize("T", [1e3, 1e30, float(np.finfo(np.float32).max)])
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+def test_large_temperatures(T, opts):
+    """T -> inf: p and q flatten towards uniform (c = log2(e)/T is subnormal at
+    the largest binary32 T); residual masses shrink below resolution."""
+    w = synthetic.WORKLOADS[4].variant(B=12, gamma=3, V=2048)
+    batch = synthetic.generate(w, seed=61)
+    batch.temperature[:] = np.float32(T)
+    rep = parity.check(batch, **opts)
+    assert rep.invalid == 0
+
+
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=3)],
+                         ids=["rowwise", "stream", "stream-g3"])
+def test_masked_logits(opts):
+    """-inf logits (a masked vocabulary): 30 % of each row masked at random;
+    in some requests the draft masks its own proposal (q(x) = 0 < p(x): alpha
+    = 1, reading R3), in others the target masks it (p(x) = 0: alpha = 0)."""
+    rng = np.random.Generator(np.random.Philox(71))
+    w = synthetic.WORKLOADS[3].variant(B=12, gamma=4, V=1024, hot_tokens=5)
+    batch = synthetic.generate(w, seed=71)
+    B, G = batch.tokens.shape
+    for arr in (batch.target, batch.draft):
+        mask = rng.random(arr.shape) < 0.3
+        arr[mask] = -np.inf
+    for b in range(B):
+        for i in range(G):
+            x = batch.tokens[b, i]
+            batch.target[b, i, x] = max(batch.target[b, i, x], np.float32(0.0))  # proposals not masked by default
+            batch.draft[b, i, x] = max(batch.draft[b, i, x], np.float32(0.0))
+        if b % 3 == 1:
+            batch.draft[b, 0, batch.tokens[b, 0]] = -np.inf   # q(x) = 0 < p(x)
+        elif b % 3 == 2:
+            batch.target[b, 0, batch.tokens[b, 0]] = -np.inf  # p(x) = 0
+    batch.temperature[:] = np.float32(0.9)
+    batch.temperature[::4] = 0.0
+    rep = parity.check(batch, **opts)
+    assert rep.invalid == 0
