@@ -32,7 +32,10 @@
  * (0, 2^-16) is read as 2^-16 (p is then one-hot to within e^-128 for logits
  * more than 2^-9 apart, and the binary32 row statistics stay in range for
  * logits up to ~2.2e4); alpha is evaluated from the logits, so it stays exact
- * when p(x) and q(x) both lie below the floating-point range.
+ * when p(x) and q(x) both lie below the floating-point range. At T > 0 a
+ * request with a row whose scaled max |fl(m * fl(log2(e) / T))| reaches 2^31
+ * in binary32 is invalid (logits beyond ~1.5e9 at T = 1): the binary32 row
+ * statistics cannot represent it.
  *
  * Conventions for every entry point:
  *  - Memory: the caller owns every buffer. Array arguments of spec_verify and

@@ -33,17 +33,29 @@ static void load_row(const void* base, int dtype, size_t row, int V, double* l) 
 
 /* A row can be used when it holds no NaN, no +inf, and at least one value
  * above -inf (a row of only -inf has no distribution). */
-static int row_usable(const double* l, int V) {
+static int row_usable(const double* l, int V, double T) {
     int has_finite = 0;
+    double m = -INFINITY;
     for (int x = 0; x < V; ++x) {
         if (isnan(l[x])) return 0;
         if (isinf(l[x])) {
             if (l[x] > 0) return 0;
         } else {
             has_finite = 1;
+            if (l[x] > m) m = l[x];
         }
     }
-    return has_finite;
+    if (!has_finite) return 0;
+    /* Reading (range): at T > 0 a row whose scaled max m log2(e) / T reaches
+     * 2^31 in binary32 is outside the range of the binary32 statistics, and
+     * its request is invalid. Decided in binary32, as the kernels decide it:
+     * c = fl(log2(e) / T), then fl(m c). */
+    if (T > 0.0) {
+        const float c = 1.44269504088896340736f / (float)T;
+        const float mc = (float)m * c;
+        if (!(fabsf(mc) < 2147483648.0f)) return 0;
+    }
+    return 1;
 }
 
 static double row_max(const double* l, int V) {
@@ -191,12 +203,12 @@ static int request_valid(const scratch_t* s, int b, double T, const int32_t* tok
         if (tok[i] < 0 || tok[i] >= V) return 0;
     for (int i = 0; i <= G; ++i) {
         load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
-        if (!row_usable(s->lt, V)) return 0;
+        if (!row_usable(s->lt, V, T)) return 0;
     }
     if (T > 0.0) {
         for (int i = 0; i < G; ++i) {
             load_row(s->draft, s->dtype, (size_t)b * (size_t)G + (size_t)i, V, s->ld);
-            if (!row_usable(s->ld, V)) return 0;
+            if (!row_usable(s->ld, V, T)) return 0;
         }
     }
     return 1;
@@ -356,7 +368,7 @@ static int request_valid_onehot(const scratch_t* s, int b, double T, const int32
         if (tok[i] < 0 || tok[i] >= V) return 0;
     for (int i = 0; i <= k; ++i) {
         load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
-        if (!row_usable(s->lt, V)) return 0;
+        if (!row_usable(s->lt, V, T)) return 0;
     }
     return 1;
 }
@@ -505,9 +517,9 @@ int oracle_spec_verify_onehot(const void* target, int dtype, int B, int gamma, i
  * 0, model proposals), and row n again for the draw. T, the proposal count and
  * every proposed token are checked first, as before. */
 
-static int row_ok_at(const scratch_t* s, const void* base, size_t row, double* l) {
+static int row_ok_at(const scratch_t* s, const void* base, size_t row, double* l, double T) {
     load_row(base, s->dtype, row, s->V, l);
-    return row_usable(l, s->V);
+    return row_usable(l, s->V, T);
 }
 
 /* Returns n, or -1 for an invalid request. */
@@ -517,7 +529,7 @@ static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok,
     const int onehot = s->draft == NULL;
     for (int i = 0; i <= k; ++i) {
         size_t tr = (size_t)b * (size_t)(G + 1) + (size_t)i;
-        if (!row_ok_at(s, s->target, tr, s->lt)) return -1;
+        if (!row_ok_at(s, s->target, tr, s->lt, T)) return -1;
         set_d(d->max_target, tr, row_max(s->lt, V));
         set_i(d->argmax_target, tr, row_argmax(s->lt, V));
         double lse_p = 0.0;
@@ -541,7 +553,7 @@ static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok,
         double alpha;
         const double px = s->p[x];
         if (!onehot) {
-            if (!row_ok_at(s, s->draft, r, s->ld)) return -1;
+            if (!row_ok_at(s, s->draft, r, s->ld, T)) return -1;
             set_d(d->max_draft, r, row_max(s->ld, V));
             const double lse_q = softmax_T(s->ld, V, T, s->q);
             set_d(d->lse_draft, r, lse_q);
@@ -779,7 +791,7 @@ int oracle_spec_verify_tree(const void* target, int dtype, int B, int gamma, int
             if (par[j - 1] < 0 || par[j - 1] >= j || tok[j - 1] < 0 || tok[j - 1] >= V) ok = 0;
         for (int j = 0; ok && j <= m; ++j) {
             load_row(s.target, s.dtype, (size_t)b * (size_t)(gamma + 1) + (size_t)j, V, s.lt);
-            if (!row_usable(s.lt, V)) ok = 0;
+            if (!row_usable(s.lt, V, T)) ok = 0;
         }
         if (!ok) {
             out_num_accepted[b] = -1;

@@ -84,6 +84,14 @@ __device__ __forceinline__ MaxSum maxsum_empty() { return {neg_inf(), 0.0f}; }
 
 __device__ __forceinline__ float scaled_max(float m, float c) { return __fmul_rn(m, c); }
 
+// A sampled row is in range while its scaled max fl(m c) stays below 2^31 in
+// magnitude: the largest term of its statistics is 2^r with r the rounding
+// error of fl(m c), at most half an ulp of it. A row out of range makes its
+// request invalid (the same test, in binary32, as the reading on both sides).
+__device__ __forceinline__ bool scaled_in_range(float m, float c) {
+    return fabsf(scaled_max(m, c)) < 2147483648.0f;
+}
+
 // 2^(l c - mc), the term of logit l in a row whose scaled max is mc.
 __device__ __forceinline__ float row_term(float l, float c, float mc) { return ex2(__fmaf_rn(l, c, -mc)); }
 

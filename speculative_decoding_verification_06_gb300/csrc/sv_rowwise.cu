@@ -87,7 +87,7 @@ __device__ RowStat row_maxsum(const void* base, size_t row, int V, float c, Shar
             acc = maxsum_merge(acc, sh.ms[w], c);
             b |= sh.bad[w];
         }
-        r = {acc.m, acc.s, -1, (b || acc.m == neg_inf()) ? 1 : 0};
+        r = {acc.m, acc.s, -1, (b || acc.m == neg_inf() || !scaled_in_range(acc.m, c)) ? 1 : 0};
     }
     __syncthreads();
     return r;  // meaningful on thread 0 only

@@ -1108,6 +1108,7 @@ struct Kern {
                 x = merge_row(kind, row_of(r), am, c);
             st[r] = x;
             bad |= x.bad;
+            if (!am && !scaled_in_range(x.m, c)) bad = 1;  // out of the binary32 statistics' range
         }
         bad = __any_sync(0xffffffffu, bad);
         __syncwarp();
@@ -2152,7 +2153,8 @@ struct Kern {
         }
         bad = __any_sync(0xffffffffu, bad);
         if (lane != 0) return;
-        const bool row_bad = rt.bad || rt.m == neg_inf() || (has_draft && (rd.bad || rd.m == neg_inf()));
+        const bool row_bad = rt.bad || rt.m == neg_inf() || (has_draft && (rd.bad || rd.m == neg_inf())) ||
+                             (samp && (!scaled_in_range(rt.m, c) || (has_draft && !scaled_in_range(rd.m, c))));
         int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
         const sv_debug_out& dbg = a.dbg;
         if (bad || row_bad) {

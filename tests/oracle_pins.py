@@ -269,6 +269,22 @@ def pin_temperature_floor(lib, quick=False):
     assert np.array_equal(n1, n0) and np.array_equal(o1, o0)
 
 
+def pin_range_limit(lib, quick=False):
+    """The range reading: at T > 0 a row whose scaled max |m| log2(e) / T
+    reaches 2^31 (in binary32) makes its request invalid; below it the request
+    is verified; a T = 0 request has no such limit."""
+    B, G, V = 4, 1, 8
+    lt = np.zeros((B, G + 1, V), np.float32)
+    ld = np.zeros((B, G, V), np.float32)
+    lt[1, 0, 2] = 1.3e9   # 1.9e9 scaled: in range
+    lt[2, 1, 2] = 1.6e9   # 2.3e9 scaled: out of range
+    lt[3, 0, 2] = 1.6e9   # greedy below
+    x = np.zeros((B, G), np.int32)
+    T = np.array([1.0, 1.0, 1.0, 0.0], np.float32)
+    _, n, _ = _run(lib, lt, ld, x, np.full((B, G), 0.5, np.float32), np.full(B, 0.5, np.float32), T)
+    assert n[0] >= 0 and n[1] >= 0 and n[2] == -1 and n[3] >= 0, n
+
+
 # ------------------------------------------------------------ normalisers etc.
 
 def pin_logsumexp_and_row_facts(lib, quick=False):
@@ -668,6 +684,7 @@ ALL_PINS = [
     pin_greedy_is_argmax_decoding,
     pin_small_temperature_matches_greedy,
     pin_temperature_floor,
+    pin_range_limit,
     pin_logsumexp_and_row_facts,
     pin_residual_mass_identity,
     pin_equal_rows_reduce_to_categorical,

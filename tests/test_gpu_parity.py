@@ -418,3 +418,25 @@ def test_masked_logits(opts):
     batch.temperature[::4] = 0.0
     rep = parity.check(batch, **opts)
     assert rep.invalid == 0
+
+
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+def test_logits_at_the_range_limit(opts):
+    """A sampled row whose scaled max |m| log2(e) / T reaches 2^31 is outside
+    the binary32 statistics' range and its request is invalid on both sides;
+    just below the limit it is verified as usual; greedy rows have no limit."""
+    w = synthetic.WORKLOADS[3].variant(B=8, gamma=2, V=512, hot_tokens=5)
+    batch = synthetic.generate(w, seed=81)
+    batch.temperature[:] = np.float32(1.0)
+    batch.temperature[6:] = 0.0
+    batch.target[0, 1, 7] = np.float32(1.3e9)   # 1.9e9 scaled: in range
+    batch.draft[1, 0, 9] = np.float32(-1.3e9)   # a very negative row max is fine too
+    batch.draft[1, 0, :] = np.minimum(batch.draft[1, 0, :], np.float32(-1.3e9))
+    batch.target[2, 0, 3] = np.float32(1.6e9)   # 2.3e9 scaled: out of range
+    batch.draft[3, 1, 4] = np.float32(2e9)      # out of range in a draft row
+    batch.target[6, 0, 5] = np.float32(3e30)    # greedy: only the argmax matters
+    gpu = parity.run_gpu(batch, **opts)
+    ora, det = parity.run_oracle(batch)
+    assert list(ora[1][[2, 3]]) == [-1, -1] and (ora[1][[0, 1, 4, 5, 6, 7]] >= 0).all()
+    rep = parity.compare(batch, gpu, ora, det)
+    assert rep.invalid == 2 and gpu["status"] & sv.SV_STATUS_BAD_REQUEST
