@@ -440,3 +440,30 @@ def test_logits_at_the_range_limit(opts):
     assert list(ora[1][[2, 3]]) == [-1, -1] and (ora[1][[0, 1, 4, 5, 6, 7]] >= 0).all()
     rep = parity.compare(batch, gpu, ora, det)
     assert rep.invalid == 2 and gpu["status"] & sv.SV_STATUS_BAD_REQUEST
+
+
+def test_misaligned_logits_take_the_one_block_path():
+    """Logit tensors that start 2 bytes past a 16-byte boundary (a view into a
+    larger buffer): the streaming path refuses them before launch, and the
+    library's own choice verifies them on the one-block-per-request path."""
+    import torch
+    w = synthetic.WORKLOADS[4].variant(B=6, gamma=3, V=4096)
+    batch = synthetic.generate(w, seed=91)
+    args = parity.to_device(batch)
+    views = []
+    for t in args[:2]:
+        flat = torch.empty(t.numel() + 1, dtype=t.dtype, device="cuda")
+        v = flat[1:].view(t.shape)
+        v.copy_(t)
+        assert v.data_ptr() % 16 != 0
+        views.append(v)
+    with pytest.raises(sv.SpecVerifyError) as err:
+        sv.spec_verify(*views, *args[2:], path=sv.SV_PATH_STREAMING)
+    assert err.value.status == sv.SV_ERR_INVALID_ARG
+    res = sv.spec_verify(*views, *args[2:], debug=True)
+    torch.cuda.synchronize()
+    gpu = {"out_tokens": res.out_tokens.cpu().numpy(), "out_num_accepted": res.out_num_accepted.cpu().numpy()}
+    gpu.update({k: v.cpu().numpy() for k, v in res.debug.items()})
+    ora, det = parity.run_oracle(batch)
+    rep = parity.compare(batch, gpu, ora, det)
+    assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
