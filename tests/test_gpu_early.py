@@ -155,3 +155,26 @@ def test_small_temperatures(T):
     b.temperature = np.full_like(b.temperature, np.float32(T))
     for opts in (ROWWISE, STREAM):
         check(b, **opts)
+
+
+def test_masked_and_out_of_range_rows():
+    """Early exit with masked (-inf) vocabularies, a proposal the draft rules
+    out (q(x) = 0: accepted), one the target rules out (p(x) = 0: rejected),
+    and an out-of-range row (the range reading): read rows decide validity."""
+    rng = np.random.Generator(np.random.Philox(93))
+    w = synthetic.WORKLOADS[3].variant(B=10, gamma=3, V=1024, hot_tokens=5)
+    b = model_batch(w, seed=93, poison_after=False)
+    for arr in (b.target, b.draft):
+        arr[rng.random(arr.shape) < 0.3] = -np.inf
+    for r in range(b.tokens.shape[0]):
+        for i in range(b.tokens.shape[1]):
+            x = b.tokens[r, i]
+            b.target[r, i, x] = max(b.target[r, i, x], np.float32(0.0))
+            b.draft[r, i, x] = max(b.draft[r, i, x], np.float32(0.0))
+    b.draft[1, 0, b.tokens[1, 0]] = -np.inf
+    b.target[2, 0, b.tokens[2, 0]] = -np.inf
+    b.target[3, 0, 5] = np.float32(2e9)  # read at position 0: invalid
+    b.temperature = np.full_like(b.temperature, np.float32(0.9))
+    for opts in (ROWWISE, STREAM):
+        rep, n = check(b, **opts)
+        assert n[3] == -1

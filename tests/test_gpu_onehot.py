@@ -220,3 +220,16 @@ def test_small_temperatures(opts, T):
     b = onehot_batch(w, 17)
     b.temperature = np.full_like(b.temperature, np.float32(T))
     check(b, **opts)
+
+
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+def test_out_of_range_row(opts):
+    """The range reading with one-hot proposals: a target row whose scaled max
+    reaches 2^31 makes its request invalid; the others are verified."""
+    w = synthetic.WORKLOADS[3].variant(B=6, gamma=4, V=1024, hot_tokens=5)
+    b = onehot_batch(w, 19, nan_past_k=False)
+    b.temperature = np.full_like(b.temperature, np.float32(1.0))
+    b.num_draft = np.full_like(b.num_draft, 4)
+    b.target[1, 2, 7] = np.float32(2e9)
+    rep = check(b, **opts)
+    assert rep.invalid == 1

@@ -228,3 +228,20 @@ def test_small_temperatures(opts):
     t = random_trees(32, 8, 1024, "bf16", seed=13, temps=(1e-6, 1e-20))
     gpu = run_gpu(t, **opts)
     compare(t, gpu)
+
+
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+def test_masked_vocabularies(opts):
+    """Trees over rows with 30 % of the vocabulary masked (-inf); candidates
+    stay unmasked unless planted: a masked candidate has p = 0 and is rejected."""
+    t = random_trees(24, 8, 1024, "f32", seed=17)
+    rng = np.random.Generator(np.random.Philox(17))
+    lt = t["target"]
+    lt[rng.random(lt.shape) < 0.3] = -np.inf
+    for b in range(lt.shape[0]):
+        for j in range(1, 9):
+            lt[b, t["parents"][b, j - 1], t["tokens"][b, j - 1]] = max(
+                lt[b, t["parents"][b, j - 1], t["tokens"][b, j - 1]], np.float32(0.0))
+    lt[3, t["parents"][3, 0], t["tokens"][3, 0]] = -np.inf  # a candidate the target rules out
+    gpu = run_gpu(t, **opts)
+    compare(t, gpu)
