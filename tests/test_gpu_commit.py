@@ -89,3 +89,22 @@ def test_empty_batch_enqueues_nothing():
     sv.spec_commit(z, torch.zeros(0, dtype=torch.int32, device="cuda"), torch.zeros((0, 8), dtype=torch.int32, device="cuda"),
                    torch.zeros(0, dtype=torch.int32, device="cuda"))
     assert sv.last_launch_count() == 0
+
+
+def test_buffers_that_fill_exactly():
+    """Histories that end exactly at max_len after the commit, one slot short of
+    it, already full, and max_len = 1; gamma = 64 (the largest)."""
+    rng = np.random.default_rng(11)
+    B, G, M = 64, 64, 200
+    out = rng.integers(0, 32000, (B, G + 1)).astype(np.int32)
+    n = rng.integers(0, G + 1, B).astype(np.int32)
+    room = n + 1
+    lens = (M - room).astype(np.int32)
+    lens[1::4] = M - room[1::4] + 1  # one slot short: the last token is cut
+    lens[2::4] = M                   # full already
+    lens[3::8] = 0
+    buf = rng.integers(0, 32000, (B, M)).astype(np.int32)
+    _check(out, n, buf, lens, M)
+    one = rng.integers(0, 32000, (6, 1)).astype(np.int32)
+    _check(out[:6, :2], np.array([0, 0, 1, 1, 0, -1], np.int32), one,
+           np.array([0, 1, 0, 1, -1, 0], np.int32), 1)

@@ -94,3 +94,48 @@ def test_bench_config():
     tokens over a 128256-token vocabulary, copy probability 0.5, gamma 8."""
     h = synthetic.histories(256, 4096, (256, 4096), vocab=128256, copy_prob=0.5, seed=1)
     _check(h.token_buf, h.seq_lens, 8)
+
+
+def test_one_slot_buffers():
+    """max_len = 1: histories of 0 and 1 token have no earlier occurrence."""
+    buf = np.array([[5], [5], [9]], dtype=np.int32)
+    lens = np.array([0, 1, 1], dtype=np.int32)
+    for n_min, n_max in ((1, 1), (1, 16)):
+        _check(buf, lens, 1, n_min, n_max)
+        _check(buf, lens, 64, n_min, n_max)
+
+
+def test_histories_as_long_as_the_query():
+    """Lengths n_max - 1 .. n_max + 2 around the longest query, n_max = 16 and
+    n_min = n_max: a match needs every one of the 16 tokens."""
+    rng = np.random.default_rng(16)
+    B, M = 64, 40
+    buf = rng.integers(0, 2, (B, M)).astype(np.int32)
+    lens = np.tile(np.arange(14, 20, dtype=np.int32), B)[:B]
+    _check(buf, lens, 8, 16, 16)
+    _check(buf, lens, 8, 1, 16)
+    buf[:] = 3  # one repeated token: every earlier position matches
+    _check(buf, lens, 8, 16, 16)
+    _check(buf, lens, 8, 2, 5)
+
+
+def test_largest_gamma_and_long_copies():
+    """gamma = 64 over histories that repeat a 100-token block, so proposals run
+    to the end of the history or to gamma."""
+    rng = np.random.default_rng(64)
+    B, M = 96, 1000
+    block = rng.integers(0, 32000, 100).astype(np.int32)
+    buf = np.tile(block, (B, M // 100))
+    lens = rng.integers(0, M + 1, B).astype(np.int32)
+    lens[:4] = [100, 101, 150, M]
+    _check(buf, lens, 64, 1, 16)
+    _check(buf, lens, 64, 2, 5)
+
+
+def test_empty_batch_enqueues_nothing():
+    import torch
+    tb = torch.zeros((0, 8), dtype=torch.int32, device="cuda")
+    sl = torch.zeros(0, dtype=torch.int32, device="cuda")
+    out, num = sv.spec_ngram_propose(tb, sl, 4, 2, 5)
+    assert sv.last_launch_count() == 0
+    assert tuple(out.shape) == (0, 4) and tuple(num.shape) == (0,)
