@@ -56,3 +56,16 @@ def test_matches_rfind_formulation():
         gamma = int(rng.integers(1, 9))
         got, _ = ngram.propose_one(hist, gamma, 2, 5)
         assert got == _by_rfind(hist, gamma, 2, 5), (hist, gamma)
+
+
+def test_matches_rfind_formulation_every_n_range():
+    rng = np.random.default_rng(12)
+    for trial in range(300):
+        n_min = int(rng.integers(1, 17))
+        n_max = int(rng.integers(n_min, 17))
+        L = int(rng.integers(0, 60))
+        vocab = int(rng.choice([1, 2, 3]))
+        hist = [int(x) for x in rng.integers(0, vocab, L)]
+        gamma = int(rng.integers(1, 65))
+        got, _ = ngram.propose_one(hist, gamma, n_min, n_max)
+        assert got == _by_rfind(hist, gamma, n_min, n_max), (hist, gamma, n_min, n_max)
