@@ -11,12 +11,21 @@
 // largest m, at least n_min) and, among those, the latest occurrence (the
 // largest e): both at once as the maximum of the 64-bit key (m << 32) | e over
 // the block. Tokens h[e .. e + k - 1] follow, k = min(gamma, L - e).
+//
+// The history is read once: the block copies up to 8192 tokens into shared
+// memory with eight independent loads per thread (one memory latency instead
+// of a chain of dependent loads per candidate), then compares there. Longer
+// histories take several passes of 8176 candidates, each tile starting
+// SV_NGRAM_MAX_N tokens before its first candidate so a match can reach back.
 #include "sv_internal.h"
 
 namespace sv {
 namespace {
 
-constexpr int kNgramThreads = 256;
+constexpr int kNgramThreads = 1024;
+constexpr int kNgramLoads = 8;                                  // tokens each thread copies per pass
+constexpr int kNgramTile = kNgramThreads * kNgramLoads;         // tokens staged per pass
+constexpr int kNgramChunk = kNgramTile - SV_NGRAM_MAX_N;        // candidates per pass
 
 __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(const int32_t* __restrict__ token_buf, int max_len,
                                                               const int32_t* __restrict__ seq_lens, int gamma,
@@ -24,6 +33,7 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(const int32_t* __r
                                                               int32_t* __restrict__ num_draft,
                                                               int32_t* __restrict__ d_status) {
     __shared__ int32_t query[SV_NGRAM_MAX_N];  // query[t] = h[L - 1 - t]
+    __shared__ int32_t tile[kNgramTile];        // tile[i - lo] = h[i]
     __shared__ unsigned long long warp_best[kNgramThreads / 32];
     const int b = blockIdx.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int L = seq_lens[b];
@@ -38,15 +48,34 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(const int32_t* __r
     }
     const int32_t* h = token_buf + static_cast<size_t>(b) * max_len;
     if (t < n_max && t < L) query[t] = h[L - 1 - t];
-    __syncthreads();
     unsigned long long best = 0ull;  // (m << 32) | e; 0 = no match of at least n_min
-    for (int e = n_min + t; e <= L - 1; e += kNgramThreads) {
-        int m = 0;
-        const int lim = min(n_max, e);
-        while (m < lim && h[e - 1 - m] == query[m]) ++m;
-        if (m >= n_min) {
-            const unsigned long long key = (static_cast<unsigned long long>(m) << 32) | static_cast<unsigned>(e);
-            best = key > best ? key : best;
+    // Candidates e in [e0, e1) read h[e - 1 - m] for m < min(n_max, e): tokens
+    // [lo, hi) with lo >= e0 - SV_NGRAM_MAX_N and hi = e1 - 1, at most
+    // kNgramTile of them. The loop bounds are the same for every thread.
+    for (int e0 = n_min; e0 <= L - 1; e0 += kNgramChunk) {
+        const int e1 = min(e0 + kNgramChunk, L);
+        const int lo = max(0, e0 - SV_NGRAM_MAX_N), hi = e1 - 1;
+        __syncthreads();  // the previous pass is done with the tile; query is written
+        int32_t v[kNgramLoads];
+#pragma unroll
+        for (int r = 0; r < kNgramLoads; ++r) {
+            const int i = lo + r * kNgramThreads + t;
+            v[r] = i < hi ? h[i] : 0;
+        }
+#pragma unroll
+        for (int r = 0; r < kNgramLoads; ++r) {
+            const int i = lo + r * kNgramThreads + t;
+            if (i < hi) tile[i - lo] = v[r];
+        }
+        __syncthreads();
+        for (int e = e0 + t; e < e1; e += kNgramThreads) {
+            int m = 0;
+            const int lim = min(n_max, e);
+            while (m < lim && tile[e - 1 - m - lo] == query[m]) ++m;
+            if (m >= n_min) {
+                const unsigned long long key = (static_cast<unsigned long long>(m) << 32) | static_cast<unsigned>(e);
+                best = key > best ? key : best;
+            }
         }
     }
 #pragma unroll

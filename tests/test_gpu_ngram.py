@@ -139,3 +139,19 @@ def test_empty_batch_enqueues_nothing():
     out, num = sv.spec_ngram_propose(tb, sl, 4, 2, 5)
     assert sv.last_launch_count() == 0
     assert tuple(out.shape) == (0, 4) and tuple(num.shape) == (0,)
+
+
+def test_histories_longer_than_one_tile():
+    """Lengths around the edges of the kernel's passes (8176 candidates each,
+    tiles of 8192 tokens), with repeats that cross a pass edge."""
+    rng = np.random.default_rng(8192)
+    M = 20000
+    lens = np.array([8176, 8177, 8178, 8192, 8193, 16352, 16353, 16354, 16369, 20000] * 2, dtype=np.int32)
+    B = len(lens)
+    buf = rng.integers(0, 3, (B, M)).astype(np.int32)
+    buf[B // 2:] = rng.integers(0, 50000, (B - B // 2, M))
+    for b in range(B // 2, B):  # the history's last 20 tokens also end 8 tokens past the first edge
+        L = lens[b]
+        buf[b, 8170:8190] = buf[b, L - 20:L]
+    _check(buf, lens, 8, 2, 5)
+    _check(buf, lens, 64, 1, 16)
