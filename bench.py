@@ -291,6 +291,38 @@ def time_calls(call, K, W, stream):
     return t0.elapsed_time(t1), np.array([a.elapsed_time(b) for a, b in zip(starts, ends)])
 
 
+def graph_us_per_call(op, sv, B, G, out_t, out_n, buf0, lens0, props, nprop, GN=50, R=20):
+    """Device time per call of a latency-bound op (eager calls there measure the
+    host's enqueue rate): GN calls captured in one CUDA graph, 3 warm-up
+    replays, then R replays between CUDA events. The commit appends into a
+    buffer of its own with room for every replayed call."""
+    import torch
+    if op == "commit":
+        gbuf = torch.zeros((B, (G + 1) * GN * (R + 4)), dtype=torch.int32, device="cuda")
+        glens = torch.zeros((B,), dtype=torch.int32, device="cuda")
+
+        def call():
+            sv.spec_commit(out_t, out_n, gbuf, glens)
+    else:
+        def call():
+            sv.spec_ngram_propose(buf0, lens0, G, 2, 5, props, nprop)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):  # the binding enqueues on the current (capturing) stream
+        for _ in range(GN):
+            call()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(R):
+        graph.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) * 1e3 / (R * GN)
+
+
 def run_aux(args, w, local):
     """--op onehot | ngram | commit | loop | tree on one GPU: one JSON line each, with
     the same timing rules as the headline (warm-up, CUDA events on the
@@ -385,6 +417,8 @@ def run_aux(args, w, local):
         extra["mean_proposed"] = float(nprop.float().mean().item())
     else:
         abytes = B * (G + 1) * 4 + B * 4 * 3 + int((np.maximum(n_acc, -1) + 1).sum()) * 4
+    if args.op in ("ngram", "commit"):
+        extra["graph_us_per_call"] = graph_us_per_call(args.op, sv, B, G, out_t, out_n, buf0, lens0, props, nprop)
     avg = float(per_call.mean()) * 1e-3
     achieved = abytes / avg / 1e9
     line = {
