@@ -28,14 +28,13 @@
  * smallest k with C_k > u_sample * W, C_k the inclusive prefix sum of the
  * weights in index order and W their total (if rounding leaves none, the last
  * k with a positive weight); residual weights that sum to zero fall back to
- * p at that position; argmax ties go to the lowest index; a temperature in
- * (0, 2^-16) is read as 2^-16 (p is then one-hot to within e^-128 for logits
- * more than 2^-9 apart, and the binary32 row statistics stay in range for
- * logits up to ~2.2e4); alpha is evaluated from the logits, so it stays exact
- * when p(x) and q(x) both lie below the floating-point range. At T > 0 a
- * request with a row whose scaled max |fl(m * fl(log2(e) / T))| reaches 2^31
- * in binary32 is invalid (logits beyond ~1.5e9 at T = 1): the binary32 row
- * statistics cannot represent it.
+ * p at that position; argmax ties go to the lowest index. Every finite T > 0
+ * and every finite logit is verified: alpha is evaluated from the logits, so
+ * it stays exact when p(x) and q(x) both lie below the floating-point range,
+ * and rows whose logits are large against T (beyond about 5.8e6 T) or whose T
+ * is so small that log2(e)/T overflows binary32 are summed from the
+ * differences to the row max (2^((l - max) log2(e) / T)) instead of the
+ * faster fused form, on both execution paths.
  *
  * Conventions for every entry point:
  *  - Memory: the caller owns every buffer. Array arguments of spec_verify and

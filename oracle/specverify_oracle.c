@@ -32,30 +32,20 @@ static void load_row(const void* base, int dtype, size_t row, int V, double* l) 
 }
 
 /* A row can be used when it holds no NaN, no +inf, and at least one value
- * above -inf (a row of only -inf has no distribution). */
-static int row_usable(const double* l, int V, double T) {
+ * above -inf (a row of only -inf has no distribution). Any finite logit is
+ * allowed, at any T > 0: the softmax below is formed in double from the
+ * differences l - max, which stay in range whatever the magnitude of l. */
+static int row_usable(const double* l, int V) {
     int has_finite = 0;
-    double m = -INFINITY;
     for (int x = 0; x < V; ++x) {
         if (isnan(l[x])) return 0;
         if (isinf(l[x])) {
             if (l[x] > 0) return 0;
         } else {
             has_finite = 1;
-            if (l[x] > m) m = l[x];
         }
     }
-    if (!has_finite) return 0;
-    /* Reading (range): at T > 0 a row whose scaled max m log2(e) / T reaches
-     * 2^31 in binary32 is outside the range of the binary32 statistics, and
-     * its request is invalid. Decided in binary32, as the kernels decide it:
-     * c = fl(log2(e) / T), then fl(m c). */
-    if (T > 0.0) {
-        const float c = 1.44269504088896340736f / (float)T;
-        const float mc = (float)m * c;
-        if (!(fabsf(mc) < 2147483648.0f)) return 0;
-    }
-    return 1;
+    return has_finite;
 }
 
 static double row_max(const double* l, int V) {
@@ -75,19 +65,11 @@ static int row_argmax(const double* l, int V) {
     return a;
 }
 
-/* Reading (temperature floor): 0 < T < 2^-16 is read as T = 2^-16. The pages
- * define p = softmax(l/T) for T > 0 and the greedy rule at T = 0; they do not
- * say how close to 0 a positive T may come. At 2^-16 the softmax of logits
- * more than 2^-9 apart is already one-hot to within e^-128. NaN, negative and
- * infinite T are left as they are (such requests are invalid), and T = 0
- * stays the greedy rule. */
-#define ORACLE_TEMP_MIN 0x1p-16
-static double temp_floor(double T) { return (T > 0.0 && T < ORACLE_TEMP_MIN) ? ORACLE_TEMP_MIN : T; }
-
-/* Temperature softmax p(x) = exp(l(x)/T) / sum_y exp(l(y)/T), evaluated as
- * exp((l(x) - m)/T) / Z with m the row max so that no term overflows; Z is
- * summed in index order. Returns log sum_y exp(l(y)/T) = m/T + log Z. */
-static double softmax_T(const double* l, int V, double T, double* p) {
+/* Temperature softmax p(x) = exp(l(x)/T) / sum_y exp(l(y)/T), for any
+ * T > 0, evaluated as exp((l(x) - m)/T) / Z with m the row max, so that no
+ * term overflows; Z is summed in index order. Reports m and log Z (either
+ * pointer may be NULL) and returns log sum_y exp(l(y)/T) = m/T + log Z. */
+static double softmax_T2(const double* l, int V, double T, double* p, double* m_out, double* logZ_out) {
     double m = row_max(l, V);
     double Z = 0.0;
     for (int x = 0; x < V; ++x) {
@@ -95,21 +77,38 @@ static double softmax_T(const double* l, int V, double T, double* p) {
         Z += p[x];
     }
     for (int x = 0; x < V; ++x) p[x] /= Z;
+    if (m_out) *m_out = m;
+    if (logZ_out) *logZ_out = log(Z);
     return m / T + log(Z);
 }
 
+static double softmax_T(const double* l, int V, double T, double* p) {
+    return softmax_T2(l, V, T, p, NULL, NULL);
+}
+
 /* alpha = min(1, p(x) / q(x)) (eq. alpha(x) of the wiki page "Speculative
- * Decoding") for the softmax rows whose log-normalisers are lse_p and lse_q,
- * evaluated as exp(log p(x) - log q(x)) with log p(x) = l(x)/T - lse_p: the
- * same value as the ratio of the probabilities, still defined when both lie
- * below the fp64 range (at small T they underflow together while their ratio
- * need not be small). A softmax probability is 0 only at a -inf logit: then
- * alpha = 1 if q(x) = 0 < p(x), 0 if p(x) = 0 (reading R3). */
-static double accept_alpha(double lt_x, double lse_p, double ld_x, double lse_q, double T) {
+ * Decoding") for softmax rows with maxima m_p, m_q and log-normalisers
+ * logZ_p, logZ_q: log p(x) - log q(x) = ((l_t(x) - m_p) - (l_d(x) - m_q)) / T
+ * - (logZ_p - logZ_q). The differences to the row maxima are formed first, so
+ * the value stays accurate at any T > 0 and any logit magnitude, and it is
+ * still defined when both probabilities lie below the fp64 range (at small T
+ * they underflow together while their ratio need not be small). A softmax
+ * probability is 0 only at a -inf logit: then alpha = 1 if q(x) = 0 < p(x),
+ * 0 if p(x) = 0 (reading R3). */
+static double accept_alpha(double lt_x, double m_p, double logZ_p, double ld_x, double m_q, double logZ_q,
+                           double T) {
     if (lt_x == -INFINITY) return 0.0;
     if (ld_x == -INFINITY) return 1.0;
-    const double lr = (lt_x / T - lse_p) - (ld_x / T - lse_q);
+    const double lr = ((lt_x - m_p) - (ld_x - m_q)) / T - (logZ_p - logZ_q);
     return lr >= 0.0 ? 1.0 : exp(lr);
+}
+
+/* The acceptance test u < alpha for u in [0, 1). alpha is positive whenever
+ * p(x) > 0 (a finite target logit), also where its double value underflowed
+ * to 0; the only uniform below such an alpha is u = 0. */
+static int accepts(double u, double alpha, int p_positive) {
+    if (!p_positive) return 0;
+    return u < alpha || u == 0.0;
 }
 
 /* Inverse-CDF draw over non-negative weights w (need not sum to one):
@@ -203,12 +202,12 @@ static int request_valid(const scratch_t* s, int b, double T, const int32_t* tok
         if (tok[i] < 0 || tok[i] >= V) return 0;
     for (int i = 0; i <= G; ++i) {
         load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
-        if (!row_usable(s->lt, V, T)) return 0;
+        if (!row_usable(s->lt, V)) return 0;
     }
     if (T > 0.0) {
         for (int i = 0; i < G; ++i) {
             load_row(s->draft, s->dtype, (size_t)b * (size_t)G + (size_t)i, V, s->ld);
-            if (!row_usable(s->ld, V, T)) return 0;
+            if (!row_usable(s->ld, V)) return 0;
         }
     }
     return 1;
@@ -253,17 +252,18 @@ static int verify_sampled(const scratch_t* s, int b, double T, const int32_t* to
         size_t r = (size_t)b * (size_t)G + (size_t)i;
         int x = tok[i];
         load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
-        const double lse_p = softmax_T(s->lt, V, T, s->p);
+        double m_p, logZ_p, m_q, logZ_q;
+        softmax_T2(s->lt, V, T, s->p, &m_p, &logZ_p);
         load_row(s->draft, s->dtype, r, V, s->ld);
-        const double lse_q = softmax_T(s->ld, V, T, s->q);
+        softmax_T2(s->ld, V, T, s->q, &m_q, &logZ_q);
         double px = s->p[x], qx = s->q[x];
-        double alpha = accept_alpha(s->lt[x], lse_p, s->ld[x], lse_q, T);
+        double alpha = accept_alpha(s->lt[x], m_p, logZ_p, s->ld[x], m_q, logZ_q, T);
         double u = (double)ua[i];
         set_d(d->p_x, r, px);
         set_d(d->q_x, r, qx);
         set_d(d->alpha, r, alpha);
         set_d(d->accept_margin, r, alpha > 0.0 ? fabs(u - alpha) / alpha : INFINITY);
-        if (u < alpha) {
+        if (accepts(u, alpha, s->lt[x] > -INFINITY)) {
             out[i] = x;
         } else {
             n = i;
@@ -328,7 +328,7 @@ int oracle_spec_verify(const void* target, const void* draft, int dtype, int B, 
     for (int b = 0; b < B; ++b) {
         const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
         int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
-        double T = temp_floor((double)temperature[b]);
+        double T = (double)temperature[b];
         for (int j = 0; j <= gamma; ++j) out[j] = -1;
         clear_detail(d, b, gamma);
         if (!request_valid(&s, b, T, tok)) {
@@ -368,7 +368,7 @@ static int request_valid_onehot(const scratch_t* s, int b, double T, const int32
         if (tok[i] < 0 || tok[i] >= V) return 0;
     for (int i = 0; i <= k; ++i) {
         load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);
-        if (!row_usable(s->lt, V, T)) return 0;
+        if (!row_usable(s->lt, V)) return 0;
     }
     return 1;
 }
@@ -420,7 +420,7 @@ static int verify_sampled_onehot(const scratch_t* s, int b, double T, const int3
         set_d(d->q_x, r, qx);
         set_d(d->alpha, r, alpha);
         set_d(d->accept_margin, r, alpha > 0.0 ? fabs(u - alpha) / alpha : INFINITY);
-        if (alpha > u) {
+        if (accepts(u, alpha, s->lt[x] > -INFINITY)) {
             out[i] = x; /* accepted */
         } else {
             n = i; /* the first rejection */
@@ -482,7 +482,7 @@ int oracle_spec_verify_onehot(const void* target, int dtype, int B, int gamma, i
     for (int b = 0; b < B; ++b) {
         const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
         int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
-        double T = temp_floor((double)temperature[b]);
+        double T = (double)temperature[b];
         int k = num_draft[b];
         for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
         clear_detail(d, b, gamma);
@@ -517,9 +517,9 @@ int oracle_spec_verify_onehot(const void* target, int dtype, int B, int gamma, i
  * 0, model proposals), and row n again for the draw. T, the proposal count and
  * every proposed token are checked first, as before. */
 
-static int row_ok_at(const scratch_t* s, const void* base, size_t row, double* l, double T) {
+static int row_ok_at(const scratch_t* s, const void* base, size_t row, double* l) {
     load_row(base, s->dtype, row, s->V, l);
-    return row_usable(l, s->V, T);
+    return row_usable(l, s->V);
 }
 
 /* Returns n, or -1 for an invalid request. */
@@ -529,14 +529,11 @@ static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok,
     const int onehot = s->draft == NULL;
     for (int i = 0; i <= k; ++i) {
         size_t tr = (size_t)b * (size_t)(G + 1) + (size_t)i;
-        if (!row_ok_at(s, s->target, tr, s->lt, T)) return -1;
+        if (!row_ok_at(s, s->target, tr, s->lt)) return -1;
         set_d(d->max_target, tr, row_max(s->lt, V));
         set_i(d->argmax_target, tr, row_argmax(s->lt, V));
-        double lse_p = 0.0;
-        if (T > 0.0) {
-            lse_p = softmax_T(s->lt, V, T, s->p);
-            set_d(d->lse_target, tr, lse_p);
-        }
+        double m_p = 0.0, logZ_p = 0.0;
+        if (T > 0.0) set_d(d->lse_target, tr, softmax_T2(s->lt, V, T, s->p, &m_p, &logZ_p));
         if (i == k) break; /* the extra-token row */
         const int x = tok[i];
         size_t r = (size_t)b * (size_t)G + (size_t)i;
@@ -553,12 +550,12 @@ static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok,
         double alpha;
         const double px = s->p[x];
         if (!onehot) {
-            if (!row_ok_at(s, s->draft, r, s->ld, T)) return -1;
+            if (!row_ok_at(s, s->draft, r, s->ld)) return -1;
             set_d(d->max_draft, r, row_max(s->ld, V));
-            const double lse_q = softmax_T(s->ld, V, T, s->q);
-            set_d(d->lse_draft, r, lse_q);
+            double m_q, logZ_q;
+            set_d(d->lse_draft, r, softmax_T2(s->ld, V, T, s->q, &m_q, &logZ_q));
             qx = s->q[x];
-            alpha = accept_alpha(s->lt[x], lse_p, s->ld[x], lse_q, T);
+            alpha = accept_alpha(s->lt[x], m_p, logZ_p, s->ld[x], m_q, logZ_q, T);
         } else {
             alpha = fmin(px, 1.0);  /* q one-hot at the proposal */
         }
@@ -567,7 +564,7 @@ static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok,
         set_d(d->q_x, r, qx);
         set_d(d->alpha, r, alpha);
         set_d(d->accept_margin, r, alpha > 0.0 ? fabs(u - alpha) / alpha : INFINITY);
-        if (!(u < alpha)) {
+        if (!accepts(u, alpha, s->lt[x] > -INFINITY)) {
             /* the residual of position i: p and q of that position are still in s->p, s->q */
             double W = 0.0;
             for (int y = 0; y < V; ++y) {
@@ -633,7 +630,7 @@ int oracle_spec_verify_early(const void* target, const void* draft, int dtype, i
     for (int b = 0; b < B; ++b) {
         const int32_t* tok = tokens + (size_t)b * (size_t)gamma;
         int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
-        const double T = temp_floor((double)temperature[b]);
+        const double T = (double)temperature[b];
         const int k = draft ? gamma : num_draft[b];
         for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
         clear_detail(d, b, gamma);
@@ -716,7 +713,7 @@ static int verify_tree_walk(const scratch_t* s, int b, double T, const int32_t* 
             set_d(d->alpha, (size_t)b * (size_t)G + (size_t)(c - 1), alpha);
             set_d(d->accept_margin, (size_t)b * (size_t)G + (size_t)(c - 1),
                   alpha > 0.0 ? fabs(uc - alpha) / alpha : INFINITY);
-            if (uc < alpha) {
+            if (accepts(uc, alpha, !seen && s->lt[x] > -INFINITY && rest > 0.0)) {
                 next = c;
             } else if (!seen) {
                 excl[ne++] = x;
@@ -781,7 +778,7 @@ int oracle_spec_verify_tree(const void* target, int dtype, int B, int gamma, int
         const int32_t* par = parents + (size_t)b * (size_t)gamma;
         int32_t* out = out_tokens + (size_t)b * (size_t)(gamma + 1);
         int32_t* nodes = out_nodes + (size_t)b * (size_t)gamma;
-        const double T = temp_floor((double)temperature[b]);
+        const double T = (double)temperature[b];
         const int m = num_nodes[b];
         for (int j = 0; j < gamma + 1; ++j) out[j] = -1;
         for (int j = 0; j < gamma; ++j) nodes[j] = -1;
@@ -791,7 +788,7 @@ int oracle_spec_verify_tree(const void* target, int dtype, int B, int gamma, int
             if (par[j - 1] < 0 || par[j - 1] >= j || tok[j - 1] < 0 || tok[j - 1] >= V) ok = 0;
         for (int j = 0; ok && j <= m; ++j) {
             load_row(s.target, s.dtype, (size_t)b * (size_t)(gamma + 1) + (size_t)j, V, s.lt);
-            if (!row_usable(s.lt, V, T)) ok = 0;
+            if (!row_usable(s.lt, V)) ok = 0;
         }
         if (!ok) {
             out_num_accepted[b] = -1;

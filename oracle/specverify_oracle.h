@@ -27,9 +27,10 @@
  *    n + 1 tokens per step; the target logits at the mismatch position or at
  *    the end of the sequence give the extra token).
  *
- * Readings where the pages are silent (all stated again in the design doc):
+ * Readings where the pages are silent:
  *  - temperature: p = softmax(l_target / T), q = softmax(l_draft / T), the
- *    same T for both rows; T == 0 is the greedy rule;
+ *    same T for both rows, for every finite T > 0 and every finite logit;
+ *    T == 0 is the greedy rule;
  *  - accept iff u_accept < alpha, u in [0, 1); alpha = min(1, p/q); q == 0
  *    gives alpha = 1 when p > 0 and alpha = 0 when p == 0;
  *  - one uniform u_sample per request draws the replacement or the bonus

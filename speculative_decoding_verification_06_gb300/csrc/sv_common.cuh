@@ -3,22 +3,35 @@
 // argmax state, the acceptance test and the inverse-CDF weights.
 //
 // Arithmetic conventions (both paths):
-//  * c = log2(e) / T, rounded once to binary32. A row's normaliser is kept as
-//    (m, s): m the row max and s = sum_x 2^(l(x) * c - mc), mc = fl(m * c)
-//    (the binary32 product). Each term is one fused multiply-add and one
-//    2^x; the rounding of mc is a common factor 2^(m*c - mc) of every term of
-//    the row, and every consumer of (m, s) recomputes mc the same way, so it
-//    cancels exactly in p(x) = 2^(l(x) c - mc) / s.
+//  * c = log2(e) / T, rounded once to binary32 (taken as +inf below T = 2^-64;
+//    ck = log2(e) / (T 2^64) then stands in for it, applied to differences
+//    scaled by 2^64, exactly). A row's
+//    normaliser is kept as (m, s) in one of two forms:
+//     - anchored: s = sum_x 2^(l(x) * c - mc), mc = fl(m * c) the binary32
+//       product. Each term is one fused multiply-add and one 2^x; the
+//       rounding r = m c - mc of the anchor is a common factor 2^r of every
+//       term of the row, and every consumer of (m, s) recomputes mc the same
+//       way, so it cancels exactly in p(x) = 2^(l(x) c - mc) / s. Used while
+//       c is finite and |mc| < 2^23, so that |r| <= 1/2 and no term exceeds
+//       2^(1/2);
+//     - plain: s = sum_x 2^(fl(l(x) - m) c), each exponent formed from the
+//       difference to the row max (fl(l - m) is exact for every logit close
+//       enough to the max to matter), whatever the magnitude of the logits
+//       and for any T > 0. Used for rows with |fl(m c)| >= 2^23 (logits
+//       beyond about 5.8e6 T) and for T small enough that c overflows.
+//    The two forms differ by the factor 2^r; states are merged in the
+//    anchored form when both are anchored, else both are turned plain
+//    (s * 2^-r) first.
 //  * 2^x uses the special-function unit (PTX ex2.approx.ftz.f32).
 //  * The acceptance test of "Speculative Decoding : accélérer l'inférence des
 //    LLM", §Pourquoi la qualité est préservée, u < min(1, p(x)/q(x)), is
-//    evaluated in double from the row statistics.
+//    evaluated from the gathered logits and the rows' statistics.
 //  * Inverse-CDF draws: each thread sums the binary32 weights of a run of
 //    consecutive tokens; the run sums are converted to unsigned 64-bit fixed
 //    point (2^-60 units for residual weights, which sum to at most 1; 2^-39
-//    for unnormalised target weights, each at most 1 and at most 2^24 of
-//    them) so that every prefix sum is exact and independent of the order in
-//    which a reduction or scan adds them.
+//    for unnormalised target weights, each at most 2^(1/2) and at most 2^24
+//    of them) so that every prefix sum is exact and independent of the order
+//    in which a reduction or scan adds them.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -41,16 +54,31 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// c = log2(e) / T, one correctly rounded binary32 division of the binary32
-// log2(e) (no FP64 on the hot path: FP64 is a small fraction of FP32 here).
-// Temperatures in (0, 2^-16) are read as 2^-16. The row statistics sum
-// 2^(l c - fl(m c)) with c = log2(e) / T; the largest term is 2^r, r the
-// rounding error of fl(m c), which stays far from overflow while |m c| < 2^31
-// (logits up to ~2.2e4 at T = 2^-16). At T = 2^-16, p is one-hot (uniform over
-// exact ties) to within e^-128 for logits more than 2^-9 apart.
-constexpr float kTempMin = 1.52587890625e-05f;  // 2^-16
-__device__ __forceinline__ float temp_floor(float T) { return (T > 0.0f && T < kTempMin) ? kTempMin : T; }
-__device__ __forceinline__ float temp_scale(float T) { return __fdiv_rn(1.44269504088896340736f, temp_floor(T)); }
+// The scale of a sampled row: c = log2(e) / T, one correctly rounded binary32
+// division of the binary32 log2(e) (no FP64 on the hot path: FP64 is a small
+// fraction of FP32 here). Below T = 2^-64 (where c overflows for T under about
+// 4.2e-39, and no row of ordinary logits could be anchored anyway) c is +inf,
+// so every such row takes the plain form, and ck = log2(e) / (T 2^64) scales
+// it instead (T 2^64 is exact and at least 2^-85, so ck is finite); else ck = 0.
+constexpr float kLog2eF = 1.44269504088896340736f;
+constexpr float kTwo64 = 18446744073709551616.0f;  // 2^64
+struct Scale {
+    float c;
+    float ck;
+};
+__device__ __forceinline__ Scale temp_scale(float T) {
+    const bool tiny = T < 5.42101086242752217004e-20f;  // 2^-64
+    const float q = __fdiv_rn(kLog2eF, tiny ? __fmul_rn(T, kTwo64) : T);
+    return Scale{tiny ? __int_as_float(0x7f800000u) : q, tiny ? q : 0.0f};
+}
+
+// The exponent d log2(e) / T of a difference d = l - m <= 0 to the row max,
+// for the plain form: d * c, or (d 2^64) * ck where c overflowed (d 2^64 is
+// exact, or -inf where the true exponent is below -2^64 anyway).
+__device__ __forceinline__ float plain_arg(float d, const Scale& sc) {
+    if (sc.c < __int_as_float(0x7f800000u)) return __fmul_rn(d, sc.c);
+    return __fmul_rn(__fmul_rn(d, kTwo64), sc.ck);
+}
 
 __device__ __forceinline__ float bf16_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 __device__ __forceinline__ float bf16x2_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -74,43 +102,95 @@ __device__ __forceinline__ float load_logit<SV_BF16>(const void* base, size_t id
 
 // ---------------------------------------------------------------- row state
 
-// Online normaliser state: s = sum 2^(l c - fl(m c)) over the logits seen.
+// Online normaliser state: s = sum 2^(l c - fl(m c)) over the logits seen
+// (anchored form, plain = 0) or s = sum 2^((l - m) c) (plain form, plain = 1).
 struct MaxSum {
     float m;
     float s;
+    int plain;
 };
 
-__device__ __forceinline__ MaxSum maxsum_empty() { return {neg_inf(), 0.0f}; }
+__device__ __forceinline__ MaxSum maxsum_empty() { return {neg_inf(), 0.0f, 0}; }
 
 __device__ __forceinline__ float scaled_max(float m, float c) { return __fmul_rn(m, c); }
 
-// A sampled row is in range while its scaled max fl(m c) stays below 2^31 in
-// magnitude: the largest term of its statistics is 2^r with r the rounding
-// error of fl(m c), at most half an ulp of it. A row out of range makes its
-// request invalid (the same test, in binary32, as the reading on both sides).
-__device__ __forceinline__ bool scaled_in_range(float m, float c) {
-    return fabsf(scaled_max(m, c)) < 2147483648.0f;
-}
+// Whether a row whose max is m may be kept in the anchored form: c finite
+// and |fl(m c)| < 2^23 (NaN, from 0 * inf, fails too).
+__device__ __forceinline__ bool anchor_ok(float m, float c) { return fabsf(scaled_max(m, c)) < 8388608.0f; }
 
-// 2^(l c - mc), the term of logit l in a row whose scaled max is mc.
+// r = m c - fl(m c), exact (the error of a product is a binary32 number and a
+// fused multiply-add forms it without rounding).
+__device__ __forceinline__ float anchor_err(float m, float c) { return __fmaf_rn(m, c, -scaled_max(m, c)); }
+
+// 2^(l c - mc), the term of logit l in an anchored row whose scaled max is mc.
 __device__ __forceinline__ float row_term(float l, float c, float mc) { return ex2(__fmaf_rn(l, c, -mc)); }
 
+// 2^((l - m) c), the term of logit l in a plain row whose max is m.
+__device__ __forceinline__ float plain_term(float l, float m, const Scale& sc) {
+    return ex2(plain_arg(__fsub_rn(l, m), sc));
+}
+
+// The sum of an anchored state in the plain form: s 2^-r.
+__device__ __forceinline__ float plain_sum(float m, float s, float c) {
+    return m == neg_inf() ? s : __fmul_rn(s, ex2(-anchor_err(m, c)));
+}
+
+__device__ __forceinline__ void maxsum_to_plain(MaxSum& st, const Scale& sc) {
+    if (!st.plain) {
+        st.s = plain_sum(st.m, st.s, sc.c);
+        st.plain = 1;
+    }
+}
+
 // Adds one logit (the caller screens NaN and +inf).
-__device__ __forceinline__ void maxsum_add(MaxSum& st, float x, float c) {
+__device__ __forceinline__ void maxsum_add(MaxSum& st, float x, const Scale& sc) {
+    const float c = sc.c;
     if (x > st.m) {
-        const float mc = scaled_max(x, c);
-        st.s = (st.m == neg_inf()) ? 0.0f : __fmul_rn(st.s, ex2(__fsub_rn(scaled_max(st.m, c), mc)));
-        st.m = x;
-        st.s = __fadd_rn(st.s, row_term(x, c, mc));
+        if (!st.plain && anchor_ok(x, c)) {
+            const float mc = scaled_max(x, c);
+            st.s = (st.m == neg_inf()) ? 0.0f : __fmul_rn(st.s, ex2(__fsub_rn(scaled_max(st.m, c), mc)));
+            st.m = x;
+            st.s = __fadd_rn(st.s, row_term(x, c, mc));
+        } else {
+            maxsum_to_plain(st, sc);
+            st.s = (st.m == neg_inf()) ? 0.0f : __fmul_rn(st.s, plain_term(st.m, x, sc));
+            st.m = x;
+            st.s = __fadd_rn(st.s, 1.0f);
+        }
     } else if (x != neg_inf()) {
-        st.s = __fadd_rn(st.s, row_term(x, c, scaled_max(st.m, c)));
+        st.s = __fadd_rn(st.s, st.plain ? plain_term(x, st.m, sc) : row_term(x, c, scaled_max(st.m, c)));
     }
 }
 
 // Merges b into a.
-__device__ __forceinline__ MaxSum maxsum_merge(MaxSum a, MaxSum b, float c) {
+__device__ __forceinline__ MaxSum maxsum_merge(MaxSum a, MaxSum b, const Scale& sc) {
     if (b.m > a.m) {
         MaxSum t = a;
+        a = b;
+        b = t;
+    }
+    if (b.m == neg_inf()) return a;
+    if (!a.plain && !b.plain) {
+        a.s = __fadd_rn(a.s, __fmul_rn(b.s, ex2(__fsub_rn(scaled_max(b.m, sc.c), scaled_max(a.m, sc.c)))));
+        return a;
+    }
+    maxsum_to_plain(a, sc);
+    maxsum_to_plain(b, sc);
+    a.s = __fadd_rn(a.s, __fmul_rn(b.s, plain_term(b.m, a.m, sc)));
+    return a;
+}
+
+// The anchored state alone, as the streaming kernels' consumers keep it: they
+// flag a row whose anchor leaves the range (kBadPlain) instead of switching
+// forms, and the warp that decides the request recomputes that row plain.
+struct MaxSumA {
+    float m;
+    float s;
+};
+
+__device__ __forceinline__ MaxSumA maxsum_merge_a(MaxSumA a, MaxSumA b, float c) {
+    if (b.m > a.m) {
+        MaxSumA t = a;
         a = b;
         b = t;
     }
@@ -133,46 +213,74 @@ __device__ __forceinline__ ArgMax argmax_merge(ArgMax a, ArgMax b) {
 
 // ------------------------------------------------------------ decisions
 
-// p(x) = 2^(l c - fl(m c)) / s, in double.
-__device__ __forceinline__ double prob_from_stats(float l, float m, float s, float c) {
-    const double mc = static_cast<double>(scaled_max(m, c));
-    return exp2(static_cast<double>(l) * static_cast<double>(c) - mc) / static_cast<double>(s);
+// p(x) from the row's statistics, in double: 2^(l c - fl(m c)) / s
+// (anchored) or 2^((l - m) c) / s (plain).
+__device__ __forceinline__ double prob_from_stats(float l, const MaxSum& st, const Scale& sc) {
+    if (!st.plain) {
+        const double mc = static_cast<double>(scaled_max(st.m, sc.c));
+        return exp2(static_cast<double>(l) * static_cast<double>(sc.c) - mc) / static_cast<double>(st.s);
+    }
+    const double d = static_cast<double>(l) - static_cast<double>(st.m);
+    const double e = sc.c < pos_inf() ? d * static_cast<double>(sc.c)
+                                      : d * static_cast<double>(kTwo64) * static_cast<double>(sc.ck);
+    return exp2(e) / static_cast<double>(st.s);
 }
 
 // The accept test u < min(1, p(x)/q(x)) from the gathered logits and the two
-// rows' (m, s): p/q = 2^e * s_q / s_p with e = (lt - ld) c - (fl(mp c) - fl(mq c)),
-// e formed exactly in double, then rounded once and raised on the SFU (relative
-// error about 3e-7). q(x) = 0 (ld = -inf) gives alpha = 1 if p(x) > 0, else 0;
-// u = 0 accepts whenever p(x) > 0, even where 2^e underflows.
-__device__ __forceinline__ bool accept_from_logits(float lt, float ld, float mp, float sp, float mq, float sq,
-                                                   float c, float u) {
+// rows' statistics. q(x) = 0 (ld = -inf) gives alpha = 1 if p(x) > 0, else 0;
+// u = 0 accepts whenever p(x) > 0, even where p/q underflows.
+// Two anchored rows: p/q = 2^e * s_q / s_p with e = (lt - ld) c - (fl(mp c) -
+// fl(mq c)) formed with error-free transformations in binary32, rounded once
+// and raised on the SFU (relative error about 3e-7; no FP64 on the common
+// path). Otherwise (a plain row: large logits or tiny T) in double:
+// e = ((lt - mp) - (ld - mq)) c + r_p - r_q, r the anchor rounding of an
+// anchored row (0 for a plain one); the differences to the maxima keep e
+// accurate whatever the magnitude of the logits.
+__device__ __forceinline__ bool accept_from_logits(float lt, float ld, const MaxSum& P, const MaxSum& Q,
+                                                   const Scale& sc, float u) {
     if (lt == neg_inf()) return false;  // p(x) = 0 < alpha requires p(x) > 0
     if (ld == neg_inf() || u == 0.0f) return true;
-    // e with error-free transformations in binary32: d = lt - ld and
-    // m = fl(mp c) - fl(mq c) as two-sums, d * c as a two-product
-    const float d = __fsub_rn(lt, ld);
-    const float dz = __fsub_rn(d, lt), d_lo = __fadd_rn(__fsub_rn(lt, __fsub_rn(d, dz)), __fsub_rn(-ld, dz));
-    const float mcp = scaled_max(mp, c), mcq = scaled_max(mq, c);
-    const float m = __fsub_rn(mcp, mcq);
-    const float mz = __fsub_rn(m, mcp), m_lo = __fadd_rn(__fsub_rn(mcp, __fsub_rn(m, mz)), __fsub_rn(-mcq, mz));
-    const float p_hi = __fmul_rn(d, c), p_lo = __fmaf_rn(d, c, -p_hi);
-    const float e = __fadd_rn(__fsub_rn(p_hi, m), __fsub_rn(__fmaf_rn(d_lo, c, p_lo), m_lo));
-    const float alpha = __fmul_rn(ex2(e), __fdiv_rn(sq, sp));
-    return u < alpha;
+    const float c = sc.c;
+    if (!P.plain && !Q.plain) {
+        const float d = __fsub_rn(lt, ld);
+        const float dz = __fsub_rn(d, lt), d_lo = __fadd_rn(__fsub_rn(lt, __fsub_rn(d, dz)), __fsub_rn(-ld, dz));
+        const float mcp = scaled_max(P.m, c), mcq = scaled_max(Q.m, c);
+        const float m = __fsub_rn(mcp, mcq);
+        const float mz = __fsub_rn(m, mcp), m_lo = __fadd_rn(__fsub_rn(mcp, __fsub_rn(m, mz)), __fsub_rn(-mcq, mz));
+        const float p_hi = __fmul_rn(d, c), p_lo = __fmaf_rn(d, c, -p_hi);
+        const float e = __fadd_rn(__fsub_rn(p_hi, m), __fsub_rn(__fmaf_rn(d_lo, c, p_lo), m_lo));
+        const float alpha = __fmul_rn(ex2(e), __fdiv_rn(Q.s, P.s));
+        return u < alpha;
+    }
+    const double D = (static_cast<double>(lt) - static_cast<double>(P.m)) -
+                     (static_cast<double>(ld) - static_cast<double>(Q.m));
+    double e;
+    if (c < pos_inf()) {
+        const double rp = P.plain ? 0.0 : static_cast<double>(anchor_err(P.m, c));
+        const double rq = Q.plain ? 0.0 : static_cast<double>(anchor_err(Q.m, c));
+        e = D * static_cast<double>(c) + (rp - rq);
+    } else {
+        e = D * static_cast<double>(kTwo64) * static_cast<double>(sc.ck);  // no anchored row without a finite c
+    }
+    const double alpha = exp2(e) * (static_cast<double>(Q.s) / static_cast<double>(P.s));
+    return static_cast<double>(u) < alpha;
 }
 
-// log sum_x exp(l(x)/T) from (m, s, c): s = 2^(m c - fl(m c)) sum 2^((l - m) c),
-// so the log is m/T + ln s - (m c - fl(m c)) ln 2, with m/T and m c in double.
-__device__ __forceinline__ double lse_from_stats(float m, float s, float c, float T) {
-    const double mc_exact = static_cast<double>(m) * static_cast<double>(c);
-    const double mc = static_cast<double>(scaled_max(m, c));
-    return static_cast<double>(m) / static_cast<double>(temp_floor(T)) + log(static_cast<double>(s)) -
-           (mc_exact - mc) * 0.69314718055994530942;
+// log sum_x exp(l(x)/T) from the statistics: m/T + ln s, less r ln 2 for an
+// anchored row (its s carries the factor 2^r, r = m c - fl(m c)), with m/T and
+// m c in double.
+__device__ __forceinline__ double lse_from_stats(const MaxSum& st, const Scale& sc, float T) {
+    const double base = static_cast<double>(st.m) / static_cast<double>(T) + log(static_cast<double>(st.s));
+    if (st.plain) return base;
+    const double mc_exact = static_cast<double>(st.m) * static_cast<double>(sc.c);
+    const double mc = static_cast<double>(scaled_max(st.m, sc.c));
+    return base - (mc_exact - mc) * 0.69314718055994530942;
 }
 
 // ------------------------------------------------------- inverse-CDF weights
 
 // Draw kinds, also reported in sv_debug_out.kind.
+constexpr int kDrawPlain = 0x100;  // DrawParams.kind flag: the draw's exponents are plain
 constexpr int kKindInvalid = -1;
 constexpr int kKindGreedy = 0;
 constexpr int kKindResidual = 1;
@@ -180,6 +288,9 @@ constexpr int kKindBonus = 2;
 // Internal draw kind, reported as kKindResidual: the residual of a one-hot
 // (deterministic) proposal, p_n without the proposed token x_n.
 constexpr int kKindResidualOnehot = 3;
+// Internal job kind of the streaming kernels: a draw already made by the
+// warp that published the job (a plain draw); no items, no search.
+constexpr int kKindDrawn = 5;
 
 constexpr float kFixResidual = 1152921504606846976.0f;  // 2^60
 constexpr float kFixTarget = 549755813888.0f;           // 2^39
@@ -189,23 +300,53 @@ constexpr double kFixTargetInv = 1.0 / 549755813888.0;
 // Weights of one draw. Residual: max(p - q, 0) from target row n and draft
 // row n ("Speculative Decoding" wiki, eq. p_corr). Target: 2^((l - m) c),
 // proportional to p at the target row (the extra token, or the fallback when
-// residual weights sum to zero).
+// residual weights sum to zero). Anchored draws (every row anchored) form the
+// exponents with one fused multiply-add against fl(m c); plain draws from the
+// difference to the row max (the maxima in mcp, mcq and the plain sums'
+// reciprocals in isp, isq).
 struct DrawParams {
-    int kind;       // kKindResidual, kKindBonus or kKindResidualOnehot
-    float c;
-    float mcp, isp; // target row: fl(max * c) and 1/s
+    int kind;       // kKindResidual, kKindBonus, ... (| kDrawPlain for a plain draw)
+    float c;        // c; a plain draw whose c overflowed holds -ck (see draw_scale)
+    float mcp, isp; // target row: fl(max * c) (plain: the max) and 1/s
     float mcq, isq; // draft row (residual only)
     float fix;      // fixed-point scale
     int excl;       // kKindResidualOnehot: the token whose weight is zero
+    __device__ bool plain() const { return (kind & kDrawPlain) != 0; }
+    __device__ int base_kind() const { return kind & ~kDrawPlain; }
 };
 
+// The scale of a draw: c, or (+inf, ck) where c overflowed (stored as -ck).
+__device__ __forceinline__ Scale draw_scale(const DrawParams& d) {
+    return d.c > 0.0f ? Scale{d.c, 0.0f} : Scale{pos_inf(), -d.c};
+}
+
+// Fills the row part of a draw's parameters from the statistics of its target
+// row P and, for a residual, its draft row Q, and sets the draw's kind.
+__device__ __forceinline__ void draw_rows(DrawParams& d, int kind, const MaxSum& P, const MaxSum* Q,
+                                          const Scale& sc) {
+    const bool plain = P.plain || (Q && Q->plain);
+    d.kind = kind | (plain ? kDrawPlain : 0);
+    d.c = sc.c < pos_inf() ? sc.c : -sc.ck;
+    if (!plain) {
+        d.mcp = scaled_max(P.m, sc.c);
+        d.isp = __frcp_rn(P.s);
+        d.mcq = Q ? scaled_max(Q->m, sc.c) : 0.0f;
+        d.isq = Q ? __frcp_rn(Q->s) : 0.0f;
+    } else {
+        d.mcp = P.m;
+        d.isp = __frcp_rn(P.plain ? P.s : plain_sum(P.m, P.s, sc.c));
+        d.mcq = Q ? Q->m : 0.0f;
+        d.isq = Q ? __frcp_rn(Q->plain ? Q->s : plain_sum(Q->m, Q->s, sc.c)) : 0.0f;
+    }
+}
+
 __device__ __forceinline__ float weight_target(float lt, const DrawParams& d) {
-    return row_term(lt, d.c, d.mcp);
+    return d.plain() ? plain_term(lt, d.mcp, draw_scale(d)) : row_term(lt, d.c, d.mcp);
 }
 
 __device__ __forceinline__ float weight_residual(float lt, float ld, const DrawParams& d) {
-    const float p = __fmul_rn(row_term(lt, d.c, d.mcp), d.isp);
-    const float q = __fmul_rn(row_term(ld, d.c, d.mcq), d.isq);
+    const float p = __fmul_rn(weight_target(lt, d), d.isp);
+    const float q = __fmul_rn(d.plain() ? plain_term(ld, d.mcq, draw_scale(d)) : row_term(ld, d.c, d.mcq), d.isq);
     return fmaxf(__fsub_rn(p, q), 0.0f);
 }
 

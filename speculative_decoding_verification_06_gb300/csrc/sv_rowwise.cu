@@ -23,10 +23,13 @@ constexpr int kWarps = kThreads / 32;
 
 struct RowStat {
     float m;      // max (T > 0) or max value (T == 0)
-    float s;      // sum 2^(l c - fl(m c)) (T > 0)
+    float s;      // sum of the terms of the row (T > 0), anchored or plain
     int32_t idx;  // lowest-index argmax (T == 0)
     int32_t bad;  // NaN, +inf, or only -inf
+    int32_t plain;  // s is in the plain form (T > 0)
 };
+
+__device__ __forceinline__ MaxSum ms_of(const RowStat& r) { return MaxSum{r.m, r.s, r.plain}; }
 
 struct Shared {
     RowStat st[2 * SV_MAX_GAMMA + 1];
@@ -50,7 +53,7 @@ struct Shared {
 constexpr int kInner = 64;
 
 template <int DT>
-__device__ RowStat row_maxsum(const void* base, size_t row, int V, float c, Shared& sh) {
+__device__ RowStat row_maxsum(const void* base, size_t row, int V, const Scale& c, Shared& sh) {
     MaxSum st = maxsum_empty();
     int bad = 0;
     const size_t off = row * static_cast<size_t>(V);
@@ -69,7 +72,8 @@ __device__ RowStat row_maxsum(const void* base, size_t row, int V, float c, Shar
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        MaxSum other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
+        MaxSum other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o),
+                     __shfl_xor_sync(0xffffffffu, st.plain, o)};
         st = maxsum_merge(st, other, c);
     }
     bad = __any_sync(0xffffffffu, bad);
@@ -87,7 +91,7 @@ __device__ RowStat row_maxsum(const void* base, size_t row, int V, float c, Shar
             acc = maxsum_merge(acc, sh.ms[w], c);
             b |= sh.bad[w];
         }
-        r = {acc.m, acc.s, -1, (b || acc.m == neg_inf() || !scaled_in_range(acc.m, c)) ? 1 : 0};
+        r = {acc.m, acc.s, -1, (b || acc.m == neg_inf()) ? 1 : 0, acc.plain};
     }
     __syncthreads();
     return r;  // meaningful on thread 0 only
@@ -124,7 +128,7 @@ __device__ RowStat row_argmax(const void* base, size_t row, int V, Shared& sh) {
             b |= sh.bad[w];
         }
         if (acc.i == 0x7fffffff) acc.i = 0;
-        r = {acc.v, 0.0f, acc.i, (b || acc.v == neg_inf()) ? 1 : 0};
+        r = {acc.v, 0.0f, acc.i, (b || acc.v == neg_inf()) ? 1 : 0, 0};
     }
     __syncthreads();
     return r;
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
         const float T = a.temperature[b];
         const bool t_ok = (T >= 0.0f) && (T < pos_inf());
         const bool greedy = t_ok && T == 0.0f;
-        const float c = (t_ok && !greedy) ? temp_scale(T) : 0.0f;
+        const Scale c = (t_ok && !greedy) ? temp_scale(T) : Scale{0.0f, 0.0f};
         // proposals: gamma, or num_draft[b] for one-hot proposals (no draft
         // rows; target rows past num_draft[b] take no part)
         const int kb = a.onehot && a.num_draft ? a.num_draft[b] : G;
@@ -218,10 +222,10 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                             // alpha from the logits: p(x) and q(x) may both lie below
                             // the floating-point range while their ratio does not
                             const bool acc =
-                                a.onehot ? accept_from_logits(lt, 0.0f, st.m, st.s, 0.0f, 1.0f, c, u)
+                                a.onehot ? accept_from_logits(lt, 0.0f, ms_of(st), MaxSum{0.0f, 1.0f, 0}, c, u)
                                          : accept_from_logits(
                                                lt, load_logit<DT>(a.draft, (static_cast<size_t>(b) * G + i) * V + x),
-                                               st.m, st.s, sd.m, sd.s, c, u);
+                                               ms_of(st), ms_of(sd), c, u);
                             stop = acc ? 0 : 1;
                         }
                     }
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             const RowStat& st = sh.st[j];
             if (a.dbg.max_target) a.dbg.max_target[r] = read ? st.m : nanf("");
             if (a.dbg.lse_target)
-                a.dbg.lse_target[r] = (greedy || !read) ? nan("") : lse_from_stats(st.m, st.s, c, T);
+                a.dbg.lse_target[r] = (greedy || !read) ? nan("") : lse_from_stats(ms_of(st), c, T);
             if (a.dbg.argmax_target) a.dbg.argmax_target[r] = (greedy && read) ? st.idx : -1;
         }
         for (int j = threadIdx.x; j < G; j += kThreads) {
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             const bool draft = !greedy && !a.onehot && (!a.early || (j <= last && j < np));
             const RowStat& st = sh.st[G + 1 + j];
             if (a.dbg.max_draft) a.dbg.max_draft[r] = draft ? st.m : nanf("");
-            if (a.dbg.lse_draft) a.dbg.lse_draft[r] = draft ? lse_from_stats(st.m, st.s, c, T) : nan("");
+            if (a.dbg.lse_draft) a.dbg.lse_draft[r] = draft ? lse_from_stats(ms_of(st), c, T) : nan("");
             if (a.dbg.p_x) a.dbg.p_x[r] = nan("");
             if (a.dbg.q_x) a.dbg.q_x[r] = nan("");
         }
@@ -337,13 +341,15 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                     const int x = tok[cn - 1];
                     const bool seen = in_set(x, sh.excl, ne);
                     const double px =
-                        seen ? 0.0 : prob_from_stats(load_logit<DT>(a.target, tr * V + x), sh.st[u].m, sh.st[u].s, c);
+                        seen ? 0.0 : prob_from_stats(load_logit<DT>(a.target, tr * V + x), ms_of(sh.st[u]), c);
                     const double rest = 1.0 - R;
                     const double alpha = rest > 0.0 ? fmin(1.0, px / rest) : 0.0;
                     const size_t dr = static_cast<size_t>(b) * G + (cn - 1);
                     if (a.dbg.p_x) a.dbg.p_x[dr] = px;
                     if (a.dbg.q_x) a.dbg.q_x[dr] = 1.0;
-                    if (ua[cn - 1] < alpha) {
+                    // u = 0 accepts whenever p'(x) > 0, also where it underflows
+                    if (ua[cn - 1] < alpha || (ua[cn - 1] == 0.0f && !seen && rest > 0.0 &&
+                                               load_logit<DT>(a.target, tr * V + x) > neg_inf())) {
                         next = cn;
                     } else if (!seen) {
                         sh.excl[ne++] = x;
@@ -363,13 +369,8 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                 if (a.dbg.w_total) a.dbg.w_total[b] = nan("");
             } else {
                 DrawParams d;
-                d.c = c;
-                d.mcp = scaled_max(sh.st[u].m, c);
-                d.isp = __frcp_rn(sh.st[u].s);
+                draw_rows(d, ne > 0 ? kKindResidualTree : kKindBonus, ms_of(sh.st[u]), nullptr, c);
                 d.excl = -1;
-                d.kind = ne > 0 ? kKindResidualTree : kKindBonus;
-                d.mcq = 0.0f;
-                d.isq = 0.0f;
                 d.fix = kFixTarget;
                 sh.draw = d;
                 if (a.dbg.kind) a.dbg.kind[b] = ne > 0 ? kKindResidual : kKindBonus;
@@ -403,13 +404,13 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                     const RowStat& sq = sh.st[G + 1 + i];
                     const float lt = load_logit<DT>(a.target, tr * V + x);
                     const float ld = a.onehot ? 0.0f : load_logit<DT>(a.draft, dr * V + x);
-                    if (a.dbg.p_x) a.dbg.p_x[dr] = prob_from_stats(lt, sp.m, sp.s, c);
+                    if (a.dbg.p_x) a.dbg.p_x[dr] = prob_from_stats(lt, ms_of(sp), c);
                     // a one-hot proposal has q(x) = 1
-                    if (a.dbg.q_x) a.dbg.q_x[dr] = a.onehot ? 1.0 : prob_from_stats(ld, sq.m, sq.s, c);
+                    if (a.dbg.q_x) a.dbg.q_x[dr] = a.onehot ? 1.0 : prob_from_stats(ld, ms_of(sq), c);
                     // alpha from the logits: p(x) and q(x) may both lie below the
                     // floating-point range while their ratio does not
-                    const bool acc = a.onehot ? accept_from_logits(lt, 0.0f, sp.m, sp.s, 0.0f, 1.0f, c, ua[i])
-                                              : accept_from_logits(lt, ld, sp.m, sp.s, sq.m, sq.s, c, ua[i]);
+                    const bool acc = a.onehot ? accept_from_logits(lt, 0.0f, ms_of(sp), MaxSum{0.0f, 1.0f, 0}, c, ua[i])
+                                              : accept_from_logits(lt, ld, ms_of(sp), ms_of(sq), c, ua[i]);
                     if (!acc) {
                         n = i;
                         break;
@@ -417,26 +418,20 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
                     out[i] = x;
                 }
                 DrawParams d;
-                d.c = c;
-                d.mcp = scaled_max(sh.st[n].m, c);
-                d.isp = __frcp_rn(sh.st[n].s);
                 d.excl = -1;
                 if (n < np && !a.onehot) {
-                    d.kind = kKindResidual;
-                    d.mcq = scaled_max(sh.st[G + 1 + n].m, c);
-                    d.isq = __frcp_rn(sh.st[G + 1 + n].s);
+                    const MaxSum sq = ms_of(sh.st[G + 1 + n]);
+                    draw_rows(d, kKindResidual, ms_of(sh.st[n]), &sq, c);
                     d.fix = kFixResidual;
                 } else {
                     // the extra token, or the residual of a one-hot proposal
                     // (p_n without x_n, unnormalised weights)
-                    d.kind = n < np ? kKindResidualOnehot : kKindBonus;
+                    draw_rows(d, n < np ? kKindResidualOnehot : kKindBonus, ms_of(sh.st[n]), nullptr, c);
                     d.excl = n < np ? tok[n] : -1;
-                    d.mcq = 0.0f;
-                    d.isq = 0.0f;
                     d.fix = kFixTarget;
                 }
                 sh.draw = d;
-                if (a.dbg.kind) a.dbg.kind[b] = d.kind == kKindResidualOnehot ? kKindResidual : d.kind;
+                if (a.dbg.kind) a.dbg.kind[b] = d.base_kind() == kKindResidualOnehot ? kKindResidual : d.base_kind();
             }
             for (int j = n + 1; j <= G; ++j) out[j] = -1;
             a.out_num_accepted[b] = n;
@@ -454,7 +449,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             const size_t drow = (static_cast<size_t>(b) * G + (row < G ? row : 0)) * V;
             const int E = (V + kThreads - 1) / kThreads;
             const int lo = min(V, static_cast<int>(threadIdx.x) * E), hi = min(V, lo + E);
-            int kind = d.kind;
+            int kind = d.base_kind();
             unsigned long long qv = range_weights<DT>(a.target, a.draft, trow, drow, lo, hi, d, kind, sh.excl, nexcl);
             unsigned long long total;
             unsigned long long excl = block_excl_scan_u64<kThreads>(qv, sh.scan, &total);
@@ -494,8 +489,7 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             if (threadIdx.x == 0 && a.dbg.w_total)  // target weights reported normalised by s
                 a.dbg.w_total[b] = kind == kKindResidual
                                        ? static_cast<double>(total) * kFixResidualInv
-                                       : static_cast<double>(total) * kFixTargetInv /
-                                             static_cast<double>(sh.st[row].s);
+                                       : static_cast<double>(total) * kFixTargetInv * static_cast<double>(d.isp);
         }
         __syncthreads();
     }

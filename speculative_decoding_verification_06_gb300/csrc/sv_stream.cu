@@ -77,11 +77,16 @@ constexpr int kBarHandoff = 2;    // consumers arrive, producer waits (kHandoffT
 
 struct Rec {
     float m;      // max value (both modes)
-    float s;      // sum 2^(l c - fl(m c)) (max/sum mode)
-    int32_t idx;  // argmax (argmax mode)
-    int32_t bad;  // NaN or +inf seen
+    float s;      // sum 2^(l c - fl(m c)) (max/sum mode; plain where idx says so)
+    int32_t idx;  // argmax (argmax mode); max/sum mode: kRecPlain for a plain sum, else -1
+    int32_t bad;  // kBadData: NaN or +inf seen; kBadPlain: the anchor left its range
 };
 constexpr uint32_t kNoPiece = 0xffffffffu;  // Rec.bad of a piece that does not exist
+constexpr int32_t kRecPlain = 1;
+constexpr int kBadData = 1;   // a NaN or +inf logit, or a row of only -inf: the request is invalid
+constexpr int kBadPlain = 2;  // |fl(m c)| >= 2^23 or c overflowed: the row is recomputed plain
+
+__device__ __forceinline__ MaxSum ms_of(const Rec& r) { return MaxSum{r.m, r.s, r.idx == kRecPlain ? 1 : 0}; }
 
 struct Job {
     int32_t b, n, kind, pad;  // request, the draw's row, kind, u_sample bits
@@ -806,7 +811,7 @@ struct Kern {
     __device__ void start_row(RowState& rs, const RowLoc& loc) const {
         const float T = a.temperature[loc.req];
         rs.argmax = loc.kind == 0 && !sampled(T);
-        rs.c = rs.argmax ? 0.0f : temp_scale(T);
+        rs.c = rs.argmax ? 0.0f : temp_scale(T).c;
         rs.m = neg_inf();
         rs.mc = neg_inf();
         rs.s = 0.0f;
@@ -821,7 +826,7 @@ struct Kern {
     // When `share` is non-zero this piece ends the request's rows in the slice:
     // the merging warp then posts the request with the share's element count.
     __device__ void flush_row(const RowState& rs, const RowLoc& loc, unsigned seq, unsigned share) const {
-        const int bad = __any_sync(0xffffffffu, rs.bad);
+        const int bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(rs.bad)));
         Rec rec;
         if (rs.argmax) {
             ArgMax st{rs.m, rs.idx};
@@ -832,11 +837,11 @@ struct Kern {
             }
             rec = {st.v, 0.0f, st.i, bad};
         } else {
-            MaxSum st{rs.m, rs.s};
+            MaxSumA st{rs.m, rs.s};
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
-                MaxSum ot{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
-                st = maxsum_merge(st, ot, rs.c);
+                MaxSumA ot{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
+                st = maxsum_merge_a(st, ot, rs.c);
             }
             rec = {st.m, st.s, -1, bad};
         }
@@ -856,7 +861,7 @@ struct Kern {
                         out.m = m.v;
                         out.idx = m.i;
                     } else {
-                        const MaxSum m = maxsum_merge(MaxSum{out.m, out.s}, MaxSum{x.m, x.s}, rs.c);
+                        const MaxSumA m = maxsum_merge_a(MaxSumA{out.m, out.s}, MaxSumA{x.m, x.s}, rs.c);
                         out.m = m.m;
                         out.s = m.s;
                     }
@@ -916,7 +921,7 @@ struct Kern {
                                                      f32_max_nan(__uint_as_float(v[k].z), __uint_as_float(v[k].w))));
         }
         if (bad_logit(tmax)) {
-            rs.bad = 1;
+            rs.bad |= kBadData;
             return;
         }
         if (tmax == neg_inf()) return;
@@ -945,6 +950,9 @@ struct Kern {
         const float c = rs.c;
         if (tmax > rs.m) {
             const float mc = scaled_max(tmax, c);
+            // beyond the anchored form's range (or c overflowed): flagged, and
+            // recomputed in the plain form by the warp that decides the request
+            if (!(fabsf(mc) < 8388608.0f)) rs.bad |= kBadPlain;
             rs.s = (rs.m == neg_inf()) ? 0.0f : __fmul_rn(rs.s, ex2(__fsub_rn(rs.mc, mc)));
             rs.m = tmax;
             rs.mc = mc;
@@ -1011,7 +1019,7 @@ struct Kern {
         }
     }
     __device__ Rec row_combine(int kind, long long row, const RowRaw& rr, bool argmax, float c) const {
-        MaxSum ms = maxsum_empty();
+        MaxSumA ms{neg_inf(), 0.0f};
         ArgMax am = argmax_empty();
         int bad = 0;
         auto take = [&](const uint4& x) {
@@ -1021,7 +1029,7 @@ struct Kern {
             if (argmax)
                 am = argmax_merge(am, ArgMax{m, static_cast<int32_t>(x.z)});
             else
-                ms = maxsum_merge(ms, MaxSum{m, s}, c);
+                ms = maxsum_merge_a(ms, MaxSumA{m, s}, c);
         };
         take(rr.x[0]);
         take(rr.x[1]);
@@ -1034,9 +1042,9 @@ struct Kern {
         }
         Rec out;
         if (argmax)
-            out = {am.v, 0.0f, am.i == 0x7fffffff ? 0 : am.i, (bad || am.v == neg_inf()) ? 1 : 0};
+            out = {am.v, 0.0f, am.i == 0x7fffffff ? 0 : am.i, (bad || am.v == neg_inf()) ? kBadData : 0};
         else
-            out = {ms.m, ms.s, -1, (bad || ms.m == neg_inf()) ? 1 : 0};
+            out = {ms.m, ms.s, -1, (bad & kBadPlain) | (((bad & kBadData) || ms.m == neg_inf()) ? kBadData : 0)};
         return out;
     }
     __device__ Rec merge_row(int kind, long long row, bool argmax, float c) const {
@@ -1083,7 +1091,8 @@ struct Kern {
         const bool t_ok = (T >= 0.0f) && (T < pos_inf());
         const bool greedy = t_ok && T == 0.0f;
         const bool samp = sampled(T);
-        const float c = samp ? temp_scale(T) : 0.0f;
+        const Scale sc = samp ? temp_scale(T) : Scale{0.0f, 0.0f};
+        const float c = sc.c;
         const bool range_ok = t_ok && kb >= 0 && kb <= GM;
         int bad = range_ok ? 0 : 1;
         const int np = range_ok ? kb : 0;
@@ -1096,6 +1105,7 @@ struct Kern {
             }
         }
         const int nrows = !range_ok ? 0 : (samp && !onehot ? 2 * GM + 1 : np + 1);
+        int plain = 0;  // a row flagged kBadPlain
         for (int r = lane; r < nrows; r += 32) {
             const int kind = kind_of(r);
             const bool am = r <= GM && !samp;
@@ -1107,11 +1117,12 @@ struct Kern {
             else
                 x = merge_row(kind, row_of(r), am, c);
             st[r] = x;
-            bad |= x.bad;
-            if (!am && !scaled_in_range(x.m, c)) bad = 1;  // out of the binary32 statistics' range
+            if (x.bad & kBadData) bad = 1;
+            if (x.bad & kBadPlain) plain = 1;
         }
         bad = __any_sync(0xffffffffu, bad);
         __syncwarp();
+        if (!bad && __any_sync(0xffffffffu, plain)) recompute_plain(b, st, nrows, sc);
         int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
         const sv_debug_out& dbg = a.dbg;
         if (bad) {
@@ -1146,7 +1157,7 @@ struct Kern {
             const bool read = j <= np;  // one-hot: rows past the proposals are not part of the request
             if (dbg.max_target) dbg.max_target[r] = read ? st[j].m : nanf("");
             if (dbg.lse_target)
-                dbg.lse_target[r] = (greedy || !read) ? nan("") : lse_from_stats(st[j].m, st[j].s, c, T);
+                dbg.lse_target[r] = (greedy || !read) ? nan("") : lse_from_stats(ms_of(st[j]), sc, T);
             if (dbg.argmax_target) dbg.argmax_target[r] = (greedy && read) ? st[j].idx : -1;
         }
         for (int j = lane; j < GM; j += 32) {
@@ -1154,10 +1165,10 @@ struct Kern {
             const bool draft = !greedy && !onehot;
             if (dbg.max_draft) dbg.max_draft[r] = draft ? st[GM + 1 + j].m : nanf("");
             if (dbg.lse_draft)
-                dbg.lse_draft[r] = draft ? lse_from_stats(st[GM + 1 + j].m, st[GM + 1 + j].s, c, T) : nan("");
+                dbg.lse_draft[r] = draft ? lse_from_stats(ms_of(st[GM + 1 + j]), sc, T) : nan("");
         }
         if (a.tree) {
-            tree_walk(b, k, st, greedy, c, np);
+            tree_walk(b, k, st, greedy, sc, np);
             return;
         }
         // first failing position over all lanes (gamma may exceed 32)
@@ -1175,17 +1186,16 @@ struct Kern {
                     const bool pre_loaded = base == 0;
                     const float lt = pre_loaded ? lt_l : load_logit<DT>(a.target, tr * V + x);
                     const float u = pre_loaded ? u_l : a.u_accept[dr];
-                    if (dbg.p_x) dbg.p_x[dr] = prob_from_stats(lt, st[i].m, st[i].s, c);
+                    if (dbg.p_x) dbg.p_x[dr] = prob_from_stats(lt, ms_of(st[i]), sc);
                     if (onehot) {
                         // q(x) = 1: the draft side of the test is a row whose only
                         // logit is 0 (max 0, sum 1)
                         if (dbg.q_x) dbg.q_x[dr] = 1.0;
-                        fail = !accept_from_logits(lt, 0.0f, st[i].m, st[i].s, 0.0f, 1.0f, c, u);
+                        fail = !accept_from_logits(lt, 0.0f, ms_of(st[i]), MaxSum{0.0f, 1.0f, 0}, sc, u);
                     } else {
                         const float ld = pre_loaded ? ld_l : load_logit<DT>(a.draft, dr * V + x);
-                        if (dbg.q_x) dbg.q_x[dr] = prob_from_stats(ld, st[GM + 1 + i].m, st[GM + 1 + i].s, c);
-                        fail = !accept_from_logits(lt, ld, st[i].m, st[i].s, st[GM + 1 + i].m, st[GM + 1 + i].s,
-                                                   c, u);
+                        if (dbg.q_x) dbg.q_x[dr] = prob_from_stats(ld, ms_of(st[GM + 1 + i]), sc);
+                        fail = !accept_from_logits(lt, ld, ms_of(st[i]), ms_of(st[GM + 1 + i]), sc, u);
                     }
                 }
             }
@@ -1213,36 +1223,167 @@ struct Kern {
             if (greedy) {
                 if (dbg.kind) dbg.kind[b] = kKindGreedy;
                 if (dbg.w_total) dbg.w_total[b] = nan("");
-            } else {
-                Job j;
-                j.b = b;
-                j.n = n;
-                j.slot = n;
-                j.pad = __float_as_int(a.u_sample[b]);  // the draw's uniform
-                DrawParams& d = j.d;
-                d.c = c;
-                d.mcp = scaled_max(st[n].m, c);
-                d.isp = __frcp_rn(st[n].s);
-                d.excl = -1;
-                if (n < np && !onehot) {
-                    d.kind = kKindResidual;
-                    d.mcq = scaled_max(st[GM + 1 + n].m, c);
-                    d.isq = __frcp_rn(st[GM + 1 + n].s);
-                    d.fix = kFixResidual;
-                } else {
-                    // the extra token (n = np), or the residual of a one-hot
-                    // proposal: p_n without x_n, unnormalised weights
-                    d.kind = n < np ? kKindResidualOnehot : kKindBonus;
-                    d.excl = n < np ? tok[n] : -1;
-                    d.mcq = 0.0f;
-                    d.isq = 0.0f;
-                    d.fix = kFixTarget;
-                }
-                j.kind = d.kind;
-                jobs()[k] = j;
-                publish(k);
-                if (dbg.kind) dbg.kind[b] = d.kind == kKindResidualOnehot ? kKindResidual : d.kind;
             }
+        }
+        if (greedy) return;
+        Job j;
+        j.b = b;
+        j.n = n;
+        j.slot = n;
+        j.pad = __float_as_int(a.u_sample[b]);  // the draw's uniform
+        DrawParams& d = j.d;
+        d.excl = -1;
+        if (n < np && !onehot) {
+            const MaxSum sq = ms_of(st[GM + 1 + n]);
+            draw_rows(d, kKindResidual, ms_of(st[n]), &sq, sc);
+            d.fix = kFixResidual;
+        } else {
+            // the extra token (n = np), or the residual of a one-hot
+            // proposal: p_n without x_n, unnormalised weights
+            draw_rows(d, n < np ? kKindResidualOnehot : kKindBonus, ms_of(st[n]), nullptr, sc);
+            d.excl = n < np ? tok[n] : -1;
+            d.fix = kFixTarget;
+        }
+        j.kind = d.base_kind();
+        if (lane == 0 && dbg.kind) dbg.kind[b] = j.kind == kKindResidualOnehot ? kKindResidual : j.kind;
+        finish_job(k, j, nullptr);
+    }
+
+    // Lane 0 publishes draw job k of request j.b. An anchored draw goes to the
+    // draw stream (items, then the owner's search); a plain draw (large logits
+    // or a tiny T) is drawn here by the whole warp and published as done, so
+    // that the producers and the owner pass over it. `set`: a tree draw's
+    // excluded tokens.
+    __device__ void finish_job(int k, Job j, const int* set) const {
+        const int lane = threadIdx.x & 31;
+        if (j.d.plain()) {
+            plain_draw_warp(j, set);
+            j.kind = kKindDrawn;
+        }
+        if (lane == 0) {
+            jobs()[k] = j;
+            publish(k);
+        }
+    }
+
+    // ---- the plain form on one warp. The consumers fold every row in the
+    // anchored form and flag (kBadPlain) a row whose anchor leaves its range
+    // (logits beyond about 5.8e6 T, or c = log2(e)/T overflowed); the warp
+    // that decides the request recomputes such rows here, off the streams,
+    // and draws over them itself (sv_common.cuh states both forms).
+
+    // Plain statistics of row `row` of `base`: max m and s = sum 2^((l - m) c),
+    // each lane over the logits lane, lane + 32, ... in order, then the lanes
+    // merged in a fixed order.
+    __device__ MaxSum plain_row_warp(const void* base, long long row, const Scale& sc) const {
+        const int lane = threadIdx.x & 31, V = a.V;
+        const long long e0 = row * V;
+        MaxSum st{neg_inf(), 0.0f, 1};
+        for (int x = lane; x < V; x += 128) {
+            float l[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) l[q] = x + 32 * q < V ? load_logit<DT>(base, e0 + x + 32 * q) : neg_inf();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) maxsum_add(st, l[q], sc);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            MaxSum ot{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o), 1};
+            st = maxsum_merge(st, ot, sc);
+        }
+        return st;
+    }
+
+    // Rows 0..nrows-1 of request b (target rows 0..gamma, then draft rows) whose
+    // records are flagged kBadPlain get plain statistics (whole warp).
+    __device__ void recompute_plain(int b, Rec* st, int nrows, const Scale& sc) const {
+        const int lane = threadIdx.x & 31, GM = a.gamma;
+        for (int base = 0; base < nrows; base += 32) {
+            unsigned flagged = __ballot_sync(0xffffffffu, base + lane < nrows && (st[base + lane].bad & kBadPlain));
+            while (flagged) {
+                const int r = base + __ffs(flagged) - 1;
+                flagged &= flagged - 1;
+                const MaxSum ms = r <= GM ? plain_row_warp(a.target, static_cast<long long>(b) * (GM + 1) + r, sc)
+                                          : plain_row_warp(a.draft, static_cast<long long>(b) * GM + (r - GM - 1), sc);
+                __syncwarp();
+                if (lane == 0) st[r] = Rec{ms.m, ms.s, kRecPlain, 0};
+                __syncwarp();
+            }
+        }
+    }
+
+    // The draw of a plain job on one warp: weights from sv_common.cuh in their
+    // plain form, summed in runs of 32 tokens (lane l of each step of 1024
+    // tokens takes run l), each run in binary32 in index order and converted
+    // to fixed point, so prefix sums are exact; the token is the smallest k
+    // with C_k > u W. Residual weights that are all zero fall back to p.
+    __device__ void plain_draw_warp(const Job& jb, const int* set) const {
+        const int lane = threadIdx.x & 31, V = a.V, GM = a.gamma;
+        constexpr int RUN = 32;
+        DrawParams d = jb.d;
+        int kind = jb.kind;
+        const long long trow = (static_cast<long long>(jb.b) * (GM + 1) + jb.n) * V;
+        const long long drow = (static_cast<long long>(jb.b) * GM + (jb.n < GM ? jb.n : 0)) * V;
+        auto weight = [&](int e) -> float {
+            const float lt = load_logit<DT>(a.target, trow + e);
+            if (kind == kKindResidual) return weight_residual(lt, load_logit<DT>(a.draft, drow + e), d);
+            if (kind == kKindResidualOnehot && e == d.excl) return 0.0f;
+            if (kind == kKindResidualTree && in_set(e, set, d.excl)) return 0.0f;
+            return weight_target(lt, d);
+        };
+        auto run_fixed = [&](int r0) -> unsigned long long {
+            float sum = 0.0f;
+            for (int e = r0; e < min(V, r0 + RUN); ++e) sum = __fadd_rn(sum, weight(e));
+            return r0 < V ? to_fixed(sum, d.fix) : 0ull;
+        };
+        auto total_of = [&]() {
+            unsigned long long tot = 0;
+            for (int s0 = 0; s0 < V; s0 += 32 * RUN) tot += warp_sum_u64(run_fixed(s0 + lane * RUN));
+            return tot;
+        };
+        unsigned long long total = total_of();
+        if (total == 0ull) {  // residual weights rounded to zero everywhere: draw from p_n
+            kind = kKindBonus;
+            d.fix = kFixTarget;
+            total = total_of();
+        }
+        const unsigned long long t = scale_uniform(__int_as_float(jb.pad), total);
+        unsigned long long before = 0;
+        int token = -1;
+        for (int s0 = 0; s0 < V && token < 0; s0 += 32 * RUN) {
+            const int r0 = s0 + lane * RUN;
+            const unsigned long long q = run_fixed(r0);
+            unsigned long long incl = q;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const unsigned long long start = before + incl - q;
+            const unsigned hit = __ballot_sync(0xffffffffu, q > 0 && start <= t && t < start + q);
+            if (hit) {
+                int mine = -1;
+                if (lane == __ffs(hit) - 1) {
+                    float part = 0.0f;
+                    int last_pos = -1;
+                    for (int e = r0; e < min(V, r0 + RUN) && mine < 0; ++e) {
+                        const float w = weight(e);
+                        part = __fadd_rn(part, w);
+                        if (w > 0.0f) last_pos = e;
+                        if (start + to_fixed(part, d.fix) > t) mine = e;
+                    }
+                    if (mine < 0) mine = last_pos;  // cannot happen: the run's total passes t
+                }
+                token = __shfl_sync(0xffffffffu, mine, __ffs(hit) - 1);
+            }
+            before += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            a.out_tokens[static_cast<size_t>(jb.b) * (GM + 1) + jb.slot] = token >= 0 ? token : V - 1;
+            if (a.dbg.w_total)
+                a.dbg.w_total[jb.b] = kind == kKindResidual ? static_cast<double>(total) * kFixResidualInv
+                                                            : static_cast<double>(total) * kFixTargetInv *
+                                                                  static_cast<double>(d.isp);
         }
     }
 
@@ -1255,7 +1396,7 @@ struct Kern {
     // the job's set. At T = 0 the first child whose token is the argmax of
     // p_u is followed. The test is made in binary64 on lane 0, as the
     // one-block-per-request kernel makes it.
-    __device__ void tree_walk(int b, int k, const Rec* st, bool greedy, float c, int np) const {
+    __device__ void tree_walk(int b, int k, const Rec* st, bool greedy, const Scale& c, int np) const {
         const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V;
         const sv_debug_out& dbg = a.dbg;
         int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
@@ -1267,13 +1408,12 @@ struct Kern {
         }
         for (int j = lane; j <= GM; j += 32) out[j] = -1;
         __syncwarp();
-        if (lane != 0) return;
         const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
         const int32_t* par = a.parents + static_cast<size_t>(b) * GM;
         const float* ua = a.u_accept + static_cast<size_t>(b) * GM;
         int* set = greedy ? nullptr : jobset() + static_cast<size_t>(k) * GM;
         int u = 0, n = 0, ne = 0;
-        for (;;) {
+        while (lane == 0) {  // the walk, on lane 0
             int next = -1;
             if (greedy) {
                 const int am = st[u].idx;
@@ -1291,14 +1431,15 @@ struct Kern {
                     if (par[cn - 1] != u) continue;
                     const int x = tok[cn - 1];
                     const bool seen = in_set(x, set, ne);
-                    const double px = seen ? 0.0 : prob_from_stats(load_logit<DT>(a.target, tr * V + x), st[u].m,
-                                                                   st[u].s, c);
+                    const float lx = load_logit<DT>(a.target, tr * V + x);
+                    const double px = seen ? 0.0 : prob_from_stats(lx, ms_of(st[u]), c);
                     const double rest = 1.0 - R;
                     const double alpha = rest > 0.0 ? fmin(1.0, px / rest) : 0.0;
                     const size_t dr = static_cast<size_t>(b) * GM + (cn - 1);
                     if (dbg.p_x) dbg.p_x[dr] = px;
                     if (dbg.q_x) dbg.q_x[dr] = 1.0;
-                    if (ua[cn - 1] < alpha) {
+                    // u = 0 accepts whenever p'(x) > 0, also where it underflows
+                    if (ua[cn - 1] < alpha || (ua[cn - 1] == 0.0f && !seen && rest > 0.0 && lx > neg_inf())) {
                         next = cn;
                     } else if (!seen) {
                         set[ne++] = x;
@@ -1312,30 +1453,31 @@ struct Kern {
             ++n;
             u = next;
         }
-        a.out_num_accepted[b] = n;
-        if (greedy) {
-            if (dbg.kind) dbg.kind[b] = kKindGreedy;
-            if (dbg.w_total) dbg.w_total[b] = nan("");
-            return;
+        if (lane == 0) {
+            a.out_num_accepted[b] = n;
+            if (greedy) {
+                if (dbg.kind) dbg.kind[b] = kKindGreedy;
+                if (dbg.w_total) dbg.w_total[b] = nan("");
+            } else if (dbg.kind) {
+                dbg.kind[b] = ne > 0 ? kKindResidual : kKindBonus;
+            }
         }
+        if (greedy) return;
+        u = __shfl_sync(0xffffffffu, u, 0);
+        n = __shfl_sync(0xffffffffu, n, 0);
+        ne = __shfl_sync(0xffffffffu, ne, 0);
         Job j;
         j.b = b;
         j.n = u;  // the draw's row: the last node
         j.slot = n;
         j.pad = __float_as_int(a.u_sample[b]);
         DrawParams& d = j.d;
-        d.c = c;
-        d.mcp = scaled_max(st[u].m, c);
-        d.isp = __frcp_rn(st[u].s);
-        d.kind = ne > 0 ? kKindResidualTree : kKindBonus;
+        draw_rows(d, ne > 0 ? kKindResidualTree : kKindBonus, ms_of(st[u]), nullptr, c);
         d.excl = ne > 0 ? ne : -1;
-        d.mcq = 0.0f;
-        d.isq = 0.0f;
         d.fix = kFixTarget;
-        j.kind = d.kind;
-        jobs()[k] = j;
-        publish(k);  // its fence also orders the set before the job
-        if (dbg.kind) dbg.kind[b] = ne > 0 ? kKindResidual : kKindBonus;
+        j.kind = d.base_kind();
+        __syncwarp();  // lane 0's set, before the other lanes read it
+        finish_job(k, j, set);  // publish's fence also orders the set before the job
     }
 
     // A run is kTPT consecutive tokens, 64 bytes, held packed as 4 vectors of
@@ -1785,7 +1927,7 @@ struct Kern {
 
     // The lanes of a warp reduced to one record (every lane holds it).
     __device__ static Rec warp_rec(const RowState& rs) {
-        const int bad = __any_sync(0xffffffffu, rs.bad);
+        const int bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(rs.bad)));
         if (rs.argmax) {
             ArgMax st{rs.m, rs.idx};
 #pragma unroll
@@ -1795,11 +1937,11 @@ struct Kern {
             }
             return Rec{st.v, 0.0f, st.i, bad};
         }
-        MaxSum st{rs.m, rs.s};
+        MaxSumA st{rs.m, rs.s};
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            MaxSum ot{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
-            st = maxsum_merge(st, ot, rs.c);
+            MaxSumA ot{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
+            st = maxsum_merge_a(st, ot, rs.c);
         }
         return Rec{st.m, st.s, -1, bad};
     }
@@ -1811,7 +1953,7 @@ struct Kern {
             x.m = m.v;
             x.idx = m.i;
         } else {
-            const MaxSum m = maxsum_merge(MaxSum{x.m, x.s}, MaxSum{y.m, y.s}, c);
+            const MaxSumA m = maxsum_merge_a(MaxSumA{x.m, x.s}, MaxSumA{y.m, y.s}, c);
             x.m = m.m;
             x.s = m.s;
         }
@@ -1913,7 +2055,7 @@ struct Kern {
                                 const float T = a.temperature[b];
                                 const bool samp = sampled(T);
                                 const int kb = ee_kb(b);
-                                desc.job.d.c = samp ? temp_scale(T) : 0.0f;
+                                desc.job.d.c = samp ? temp_scale(T).c : 0.0f;
                                 task_flags = (samp ? 0 : kStatsArgmax) |
                                              ((samp && !a.onehot && pos < kb && pos < GM) ? kStatsDraft : 0);
                             } else {  // published with its scale and flags
@@ -2109,15 +2251,13 @@ struct Kern {
         const int lane = threadIdx.x & 31, GM = a.gamma, NI = L.NI;
         const float T = e.T;
         const bool t_ok = (T >= 0.0f) && (T < pos_inf());
-        const bool greedy = t_ok && T == 0.0f;
         const bool samp = sampled(T);
-        const float c = samp ? temp_scale(T) : 0.0f;
+        const Scale sc = samp ? temp_scale(T) : Scale{0.0f, 0.0f};
+        const float c = sc.c;
         const int kb = e.kb;
         const bool range_ok = t_ok && kb >= 0 && kb <= GM;
         const bool proposal = range_ok && pos < kb;
         const bool has_draft = samp && !a.onehot && proposal;
-        const int x = e.x;
-        const float lt = e.lt, ld = e.ld, u = e.u;
         int bad = e.bad;
         // the item records of the position's rows, merged in item order per lane
         // and then across lanes; lane 0's result is used
@@ -2152,32 +2292,82 @@ struct Kern {
             }
         }
         bad = __any_sync(0xffffffffu, bad);
-        if (lane != 0) return;
-        const bool row_bad = rt.bad || rt.m == neg_inf() || (has_draft && (rd.bad || rd.m == neg_inf())) ||
-                             (samp && (!scaled_in_range(rt.m, c) || (has_draft && !scaled_in_range(rd.m, c))));
+        // rows flagged kBadPlain get plain statistics (whole warp; lane 0's
+        // merged records decide)
+        {
+            const int tb = __shfl_sync(0xffffffffu, rt.bad, 0), db = __shfl_sync(0xffffffffu, rd.bad, 0);
+            const bool ok = !bad && !(tb & kBadData) && !(has_draft && (db & kBadData));
+            if (ok && samp && (tb & kBadPlain)) {
+                const MaxSum ms = plain_row_warp(a.target, static_cast<long long>(b) * (GM + 1) + pos, sc);
+                rt = Rec{ms.m, ms.s, kRecPlain, 0};
+            }
+            if (ok && has_draft && (db & kBadPlain)) {
+                const MaxSum ms = plain_row_warp(a.draft, static_cast<long long>(b) * GM + pos, sc);
+                rd = Rec{ms.m, ms.s, kRecPlain, 0};
+            }
+        }
+        int plain_draw = 0;
+        if (lane == 0) plain_draw = ee_decide_lane0(p, b, pos, e, rt, rd, sc, bad);
+        if (__shfl_sync(0xffffffffu, plain_draw, 0)) ee_plain_draw(b);
+    }
+
+    // A plain draw of request b (its job written by lane 0), made by the whole
+    // warp; the request is then finished.
+    __device__ void ee_plain_draw(int b) const {
+        __syncwarp();
+        Job j;
+        const int* src = reinterpret_cast<const int*>(jobs() + b);
+        int* dst = reinterpret_cast<int*>(&j);
+        for (int q = 0; q < static_cast<int>(sizeof(Job) / 4); ++q) dst[q] = src[q];
+        plain_draw_warp(j, nullptr);
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) ee_finish_request();
+    }
+
+    // The decision at position pos of request b on lane 0, from the merged
+    // records rt (target row) and rd (draft row). Returns 1 when the decision
+    // is a plain draw, which the caller's warp then makes (job j); the
+    // request's other outputs are written here.
+    __device__ int ee_decide_lane0(int p, int b, int pos, const EePre& e, Rec rt, Rec rd, const Scale& sc,
+                                   int bad) const {
+        const int GM = a.gamma;
+        const float T = e.T;
+        const bool t_ok = (T >= 0.0f) && (T < pos_inf());
+        const bool greedy = t_ok && T == 0.0f;
+        const bool samp = sampled(T);
+        const float c = sc.c;
+        const int kb = e.kb;
+        const bool range_ok = t_ok && kb >= 0 && kb <= GM;
+        const bool proposal = range_ok && pos < kb;
+        const bool has_draft = samp && !a.onehot && proposal;
+        const int x = e.x;
+        const float lt = e.lt, ld = e.ld, u = e.u;
+        (void)p;
+        const bool row_bad = (rt.bad & kBadData) || rt.m == neg_inf() ||
+                             (has_draft && ((rd.bad & kBadData) || rd.m == neg_inf()));
         int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
         const sv_debug_out& dbg = a.dbg;
         if (bad || row_bad) {
             ee_close(b, -1, 0);
-            for (int j = 0; j <= GM; ++j) out[j] = -1;
+            for (int q = 0; q <= GM; ++q) out[q] = -1;
             if (a.d_status) atomicOr(a.d_status, SV_STATUS_BAD_REQUEST);
             if (dbg.kind) dbg.kind[b] = kKindInvalid;
             if (dbg.w_total) dbg.w_total[b] = nan("");
             ee_finish_request();
-            return;
+            return 0;
         }
         {  // this position's checking outputs
             const size_t r = static_cast<size_t>(b) * (GM + 1) + pos;
             if (dbg.max_target) dbg.max_target[r] = rt.m;
-            if (dbg.lse_target) dbg.lse_target[r] = greedy ? nan("") : lse_from_stats(rt.m, rt.s, c, T);
+            if (dbg.lse_target) dbg.lse_target[r] = greedy ? nan("") : lse_from_stats(ms_of(rt), sc, T);
             if (dbg.argmax_target) dbg.argmax_target[r] = greedy ? (rt.idx == 0x7fffffff ? 0 : rt.idx) : -1;
             if (pos < GM) {
                 const size_t q = static_cast<size_t>(b) * GM + pos;
                 if (dbg.max_draft) dbg.max_draft[q] = has_draft ? rd.m : nanf("");
-                if (dbg.lse_draft) dbg.lse_draft[q] = has_draft ? lse_from_stats(rd.m, rd.s, c, T) : nan("");
-                if (dbg.p_x) dbg.p_x[q] = (samp && proposal) ? prob_from_stats(lt, rt.m, rt.s, c) : nan("");
+                if (dbg.lse_draft) dbg.lse_draft[q] = has_draft ? lse_from_stats(ms_of(rd), sc, T) : nan("");
+                if (dbg.p_x) dbg.p_x[q] = (samp && proposal) ? prob_from_stats(lt, ms_of(rt), sc) : nan("");
                 if (dbg.q_x)
-                    dbg.q_x[q] = (samp && proposal) ? (a.onehot ? 1.0 : prob_from_stats(ld, rd.m, rd.s, c)) : nan("");
+                    dbg.q_x[q] = (samp && proposal) ? (a.onehot ? 1.0 : prob_from_stats(ld, ms_of(rd), sc)) : nan("");
             }
         }
         if (greedy) {
@@ -2185,23 +2375,23 @@ struct Kern {
             if (proposal && x == am) {
                 out[pos] = am;
                 ee_publish(kTaskStats, b, pos + 1, 0.0f, kStatsArgmax);
-                return;
+                return 0;
             }
             out[pos] = am;
             ee_close(b, pos, pos + 1);
             if (dbg.kind) dbg.kind[b] = kKindGreedy;
             if (dbg.w_total) dbg.w_total[b] = nan("");
             ee_finish_request();
-            return;
+            return 0;
         }
         if (proposal) {
-            const bool acc = a.onehot ? accept_from_logits(lt, 0.0f, rt.m, rt.s, 0.0f, 1.0f, c, u)
-                                      : accept_from_logits(lt, ld, rt.m, rt.s, rd.m, rd.s, c, u);
+            const bool acc = a.onehot ? accept_from_logits(lt, 0.0f, ms_of(rt), MaxSum{0.0f, 1.0f, 0}, sc, u)
+                                      : accept_from_logits(lt, ld, ms_of(rt), ms_of(rd), sc, u);
             if (acc) {
                 out[pos] = x;
                 ee_publish(kTaskStats, b, pos + 1, c,
                            (!a.onehot && pos + 1 < kb && pos + 1 < GM) ? kStatsDraft : 0);
-                return;
+                return 0;
             }
         }
         // the draw: the residual at a rejection, or the extra token from row kb
@@ -2211,28 +2401,24 @@ struct Kern {
         j.slot = pos;
         j.pad = __float_as_int(a.u_sample[b]);
         DrawParams& d = j.d;
-        d.c = c;
-        d.mcp = scaled_max(rt.m, c);
-        d.isp = __frcp_rn(rt.s);
         d.excl = -1;
         if (proposal && !a.onehot) {
-            d.kind = kKindResidual;
-            d.mcq = scaled_max(rd.m, c);
-            d.isq = __frcp_rn(rd.s);
+            const MaxSum sq = ms_of(rd);
+            draw_rows(d, kKindResidual, ms_of(rt), &sq, sc);
             d.fix = kFixResidual;
         } else {
-            d.kind = proposal ? kKindResidualOnehot : kKindBonus;
+            draw_rows(d, proposal ? kKindResidualOnehot : kKindBonus, ms_of(rt), nullptr, sc);
             d.excl = proposal ? x : -1;
-            d.mcq = 0.0f;
-            d.isq = 0.0f;
             d.fix = kFixTarget;
         }
-        j.kind = d.kind;
-        jobs()[b] = j;
-        out[pos] = -1;  // the search fills it in
+        j.kind = d.base_kind();
+        out[pos] = -1;  // the search (or the plain draw) fills it in
         ee_close(b, pos, pos + 1);
-        if (dbg.kind) dbg.kind[b] = d.kind == kKindResidualOnehot ? kKindResidual : d.kind;
+        if (dbg.kind) dbg.kind[b] = j.kind == kKindResidualOnehot ? kKindResidual : j.kind;
+        jobs()[b] = j;
+        if (d.plain()) return 1;  // drawn by the caller's warp
         ee_publish(kTaskDraw, b, pos);
+        return 0;
     }
 
     // Search warp: the next owned task (g, g + G, g + 2G, ...), decided or

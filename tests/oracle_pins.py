@@ -242,47 +242,103 @@ def pin_small_temperature_matches_greedy(lib, quick=False):
     assert np.array_equal(n1, n0) and np.array_equal(o1, o0)
 
 
-def pin_temperature_floor(lib, quick=False):
-    """The reading on temperatures below 2^-16: any 0 < T < 2^-16 gives
-    exactly the outputs of T = 2^-16 (checked at T = 1e-6, 1e-20 and the
-    binary32 subnormal 1e-40), and T = 2^-16 itself gives the greedy result
-    when every runner-up is at least 2^-9 below the max (p and q are one-hot to
-    within e^-128 there)."""
-    rng = np.random.Generator(np.random.Philox(67))
-    B, G, V = 64, 3, 50
+def _one_hot_rows(rng, B, G, V, gap_choices):
+    """Target and draft logits whose row max leads every other logit by one
+    of `gap_choices` (binary32 N(0, 2) rows with the max planted)."""
     lt = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
     ld = rng.normal(0, 2, (B, G, V)).astype(np.float32)
-    x = rng.integers(0, V, (B, G)).astype(np.int32)
-    ua = rng.random((B, G), dtype=np.float32)
-    us = rng.random(B, dtype=np.float32)
-    ref = _run(lib, lt, ld, x, ua, us, np.full(B, 2.0 ** -16, np.float32))
-    for T in (1e-6, 1e-20, 1e-40):
-        o, n, _ = _run(lib, lt, ld, x, ua, us, np.full(B, T, np.float32))
-        assert np.array_equal(n, ref[1]) and np.array_equal(o, ref[0]), T
     for arr in (lt, ld):
         flat = arr.reshape(-1, V)
         top = rng.integers(V, size=flat.shape[0])
-        flat[np.arange(flat.shape[0]), top] = flat.max(axis=1) + 2.0 ** -8
-    xg = np.argmax(ld, axis=2).astype(np.int32)
-    o1, n1, _ = _run(lib, lt, ld, xg, ua, us, np.full(B, 2.0 ** -16, np.float32))
-    o0, n0, _ = _run(lib, lt, ld, xg, ua, us, np.zeros(B, np.float32))
-    assert np.array_equal(n1, n0) and np.array_equal(o1, o0)
+        gap = np.asarray(gap_choices, np.float32)[rng.integers(len(gap_choices), size=flat.shape[0])]
+        flat[np.arange(flat.shape[0]), top] = flat.max(axis=1) + gap
+    return lt, ld
 
 
-def pin_range_limit(lib, quick=False):
-    """The range reading: at T > 0 a row whose scaled max |m| log2(e) / T
-    reaches 2^31 (in binary32) makes its request invalid; below it the request
-    is verified; a T = 0 request has no such limit."""
-    B, G, V = 4, 1, 8
-    lt = np.zeros((B, G + 1, V), np.float32)
-    ld = np.zeros((B, G, V), np.float32)
-    lt[1, 0, 2] = 1.3e9   # 1.9e9 scaled: in range
-    lt[2, 1, 2] = 1.6e9   # 2.3e9 scaled: out of range
-    lt[3, 0, 2] = 1.6e9   # greedy below
-    x = np.zeros((B, G), np.int32)
-    T = np.array([1.0, 1.0, 1.0, 0.0], np.float32)
-    _, n, _ = _run(lib, lt, ld, x, np.full((B, G), 0.5, np.float32), np.full(B, 0.5, np.float32), T)
-    assert n[0] >= 0 and n[1] >= 0 and n[2] == -1 and n[3] >= 0, n
+def pin_one_hot_limit_is_greedy(lib, quick=False):
+    """p = softmax(l/T) at any T > 0. When every logit of a row lies more than
+    1e5 T below the row max, exp((l - max)/T) is exactly 0 in double for every
+    other token, so p and q are one-hot; with draft tokens at the draft argmax
+    (q(x) = 1) and u > 0 the rule then gives exactly the greedy result: accept
+    iff x is the target argmax, the residual max(p - q, 0) is one-hot at that
+    argmax, the extra token is the argmax. Checked at T = 1e-30 and at the
+    binary32 subnormal T = 1e-40 with gaps down to 2^-20 at the max, and at
+    T = 0.25 with logits of magnitude 1.6e9 (binary32 spacing 128 there, so
+    every gap is at least 512 T)."""
+    rng = np.random.Generator(np.random.Philox(67))
+    B, G, V = 64, 3, 50
+    ua = np.maximum(rng.random((B, G), dtype=np.float32), np.float32(1e-3))
+    us = rng.random(B, dtype=np.float32)
+    lt, ld = _one_hot_rows(rng, B, G, V, [2.0 ** -20, 2.0 ** -12, 0.5])
+    x = np.argmax(ld, axis=2).astype(np.int32)
+    o0, n0, _ = _run(lib, lt, ld, x, ua, us, np.zeros(B, np.float32))
+    for T in (1e-30, 1e-40):
+        o, n, _ = _run(lib, lt, ld, x, ua, us, np.full(B, T, np.float32))
+        assert np.array_equal(n, n0) and np.array_equal(o, o0), T
+    # |l| ~ 1.6e9: binary32 logits there are multiples of 128
+    base = (128.0 * np.round(rng.normal(0, 3, (B, G + 1 + G, V)))).astype(np.float64)
+    flat = base.reshape(-1, V)
+    flat[np.arange(flat.shape[0]), rng.integers(V, size=flat.shape[0])] = flat.max(axis=1) + 512.0  # no ties
+    shift = np.where(rng.random((B, 1, 1)) < 0.5, 1.6e9, -1.6e9)
+    big = (base + shift).astype(np.float32)
+    assert np.all(big.astype(np.float64) == base + np.float32(shift).astype(np.float64))
+    lt2, ld2 = big[:, :G + 1].copy(), big[:, G + 1:].copy()
+    x2 = np.argmax(ld2, axis=2).astype(np.int32)
+    o0, n0, _ = _run(lib, lt2, ld2, x2, ua, us, np.zeros(B, np.float32))
+    o, n, _ = _run(lib, lt2, ld2, x2, ua, us, np.full(B, 0.25, np.float32))
+    assert np.all(n >= 0) and np.array_equal(n, n0) and np.array_equal(o, o0)
+
+
+def pin_shift_invariance(lib, quick=False):
+    """softmax(l/T) does not change when a constant is added to every logit
+    of a row. Rows on a grid of multiples of 128 (exact in binary32 up to
+    2^31) are verified as they are and shifted by 2^30 (target rows) and
+    -3 * 2^29 (draft rows): the tokens and counts are identical and p(x),
+    q(x), alpha and the draw total W agree to 1e-12 relative. T = 256 keeps
+    the distributions far from one-hot (l/T has steps of 1/2)."""
+    rng = np.random.Generator(np.random.Philox(69))
+    B, G, V = 64, 4, 60
+    base_t = (128.0 * np.round(rng.normal(0, 3, (B, G + 1, V)) * 2.0)).astype(np.float32)
+    base_d = (base_t[:, :G] + 128.0 * np.round(rng.normal(0, 1, (B, G, V)) * 2.0)).astype(np.float32)
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    ua = rng.random((B, G), dtype=np.float32)
+    us = rng.random(B, dtype=np.float32)
+    T = np.full(B, 256.0, np.float32)
+    sh_t = (base_t.astype(np.float64) + 2.0 ** 30).astype(np.float32)
+    sh_d = (base_d.astype(np.float64) - 3.0 * 2.0 ** 29).astype(np.float32)
+    assert np.all(sh_t.astype(np.float64) - 2.0 ** 30 == base_t)
+    assert np.all(sh_d.astype(np.float64) + 3.0 * 2.0 ** 29 == base_d)
+    o0, n0, d0 = _run(lib, base_t, base_d, x, ua, us, T, detail=True)
+    o1, n1, d1 = _run(lib, sh_t, sh_d, x, ua, us, T, detail=True)
+    assert np.all(n0 >= 0)
+    assert np.array_equal(n0, n1) and np.array_equal(o0, o1)
+    for key in ("p_x", "q_x", "alpha", "w_total"):
+        a, b = d0[key], d1[key]
+        fin = np.isfinite(a)
+        assert np.array_equal(fin, np.isfinite(b)), key
+        assert np.all(np.abs(a[fin] - b[fin]) <= 1e-12 * np.abs(a[fin])), key
+    # the log-normalisers move by exactly the shift over T
+    fin = np.isfinite(d0["lse_target"])
+    assert np.allclose(d1["lse_target"][fin] - d0["lse_target"][fin], 2.0 ** 30 / 256.0, rtol=0, atol=1e-6)
+
+
+def pin_zero_uniform_accepts(lib, quick=False):
+    """u_accept is in [0, 1) and alpha = min(1, p/q) is positive whenever the
+    target logit of the proposal is finite, so u = 0 accepts every such
+    proposal, also where p and q are far below the double range (T = 1e-30,
+    proposals far from the argmax); a -inf target logit (p = 0) still rejects."""
+    rng = np.random.Generator(np.random.Philox(73))
+    B, G, V = 16, 3, 40
+    lt = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+    ld = rng.normal(0, 2, (B, G, V)).astype(np.float32)
+    x = np.argmin(lt[:, :G], axis=2).astype(np.int32)  # the least likely target token
+    ua = np.zeros((B, G), np.float32)
+    us = rng.random(B, dtype=np.float32)
+    lt[B - 1, 1, x[B - 1, 1]] = -np.inf
+    for T in (1.0, 1e-30):
+        o, n, _ = _run(lib, lt, ld, x, ua, us, np.full(B, T, np.float32))
+        assert np.all(n[:B - 1] == G) and n[B - 1] == 1, (T, n)
+        assert np.array_equal(o[:B - 1, :G], x[:B - 1])
 
 
 # ------------------------------------------------------------ normalisers etc.
@@ -683,8 +739,9 @@ ALL_PINS = [
     pin_position_acceptance,
     pin_greedy_is_argmax_decoding,
     pin_small_temperature_matches_greedy,
-    pin_temperature_floor,
-    pin_range_limit,
+    pin_one_hot_limit_is_greedy,
+    pin_shift_invariance,
+    pin_zero_uniform_accepts,
     pin_logsumexp_and_row_facts,
     pin_residual_mass_identity,
     pin_equal_rows_reduce_to_categorical,

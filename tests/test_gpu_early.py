@@ -148,7 +148,7 @@ def test_longest_row_streaming():
     check(model_batch(w, seed=54), path=2)
 
 
-@pytest.mark.parametrize("T", [1e-4, 1e-20])
+@pytest.mark.parametrize("T", [1e-4, 1e-20, 1e-40])
 def test_small_temperatures(T):
     w = synthetic.WORKLOADS[4].variant(B=16, gamma=3, V=4096)
     b = model_batch(w, seed=11, poison_after=False)
@@ -157,10 +157,10 @@ def test_small_temperatures(T):
         check(b, **opts)
 
 
-def test_masked_and_out_of_range_rows():
+def test_masked_rows_and_large_logits():
     """Early exit with masked (-inf) vocabularies, a proposal the draft rules
     out (q(x) = 0: accepted), one the target rules out (p(x) = 0: rejected),
-    and an out-of-range row (the range reading): read rows decide validity."""
+    and a row whose max is 2e9 (summed from the differences to the max)."""
     rng = np.random.Generator(np.random.Philox(93))
     w = synthetic.WORKLOADS[3].variant(B=10, gamma=3, V=1024, hot_tokens=5)
     b = model_batch(w, seed=93, poison_after=False)
@@ -173,8 +173,8 @@ def test_masked_and_out_of_range_rows():
             b.draft[r, i, x] = max(b.draft[r, i, x], np.float32(0.0))
     b.draft[1, 0, b.tokens[1, 0]] = -np.inf
     b.target[2, 0, b.tokens[2, 0]] = -np.inf
-    b.target[3, 0, 5] = np.float32(2e9)  # read at position 0: invalid
+    b.target[3, 0, 5] = np.float32(2e9)  # read at position 0: p one-hot at token 5
     b.temperature = np.full_like(b.temperature, np.float32(0.9))
     for opts in (ROWWISE, STREAM):
         rep, n = check(b, **opts)
-        assert n[3] == -1
+        assert np.all(n >= 0)

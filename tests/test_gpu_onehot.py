@@ -223,13 +223,13 @@ def test_small_temperatures(opts, T):
 
 
 @pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
-def test_out_of_range_row(opts):
-    """The range reading with one-hot proposals: a target row whose scaled max
-    reaches 2^31 makes its request invalid; the others are verified."""
+def test_large_logit_row(opts):
+    """One-hot proposals with a target row whose max is 2e9 (summed from the
+    differences to the row max): every request is verified."""
     w = synthetic.WORKLOADS[3].variant(B=6, gamma=4, V=1024, hot_tokens=5)
     b = onehot_batch(w, 19, nan_past_k=False)
     b.temperature = np.full_like(b.temperature, np.float32(1.0))
     b.num_draft = np.full_like(b.num_draft, 4)
     b.target[1, 2, 7] = np.float32(2e9)
     rep = check(b, **opts)
-    assert rep.invalid == 1
+    assert rep.invalid == 0

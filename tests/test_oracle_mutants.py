@@ -17,14 +17,23 @@ from oracle_pins import ALL_PINS
 SRC = os.path.join(os.path.dirname(oracle.__file__), "specverify_oracle.c")
 
 SAMPLED_TARGET_ROW = ("load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)i, V, s->lt);\n"
-                      "        const double lse_p = softmax_T(s->lt, V, T, s->p);\n        load_row(s->draft")
+                      "        double m_p, logZ_p, m_q, logZ_q;\n"
+                      "        softmax_T2(s->lt, V, T, s->p, &m_p, &logZ_p);\n        load_row(s->draft")
 SAMPLED_BONUS_ROW = ("load_row(s->target, s->dtype, (size_t)b * (size_t)(G + 1) + (size_t)G, V, s->lt);\n"
                      "        softmax_T")
 
 MUTANTS = [
-    ("alpha_q_over_p", "const double lr = (lt_x / T - lse_p) - (ld_x / T - lse_q);",
-     "const double lr = (ld_x / T - lse_q) - (lt_x / T - lse_p);"),
-    ("accept_flipped", "if (u < alpha) {", "if (u > alpha) {"),
+    ("alpha_q_over_p", "const double lr = ((lt_x - m_p) - (ld_x - m_q)) / T - (logZ_p - logZ_q);",
+     "const double lr = ((ld_x - m_q) - (lt_x - m_p)) / T - (logZ_q - logZ_p);"),
+    ("alpha_from_unshifted_logits", "const double lr = ((lt_x - m_p) - (ld_x - m_q)) / T - (logZ_p - logZ_q);",
+     "const double lr = (lt_x / T - (m_p / T + logZ_p)) - (ld_x / T - (m_q / T + logZ_q));"),
+    ("accept_flipped", "return u < alpha || u == 0.0;", "return u > alpha || u == 0.0;"),
+    ("zero_uniform_rejects_underflowed_alpha", "return u < alpha || u == 0.0;", "return u < alpha;"),
+    ("temperature_floor", "        double T = (double)temperature[b];\n        for (int j = 0; j <= gamma; ++j)",
+     "        double T = (temperature[b] > 0.0f && temperature[b] < 0x1p-16f) ? 0x1p-16 : (double)temperature[b];\n"
+     "        for (int j = 0; j <= gamma; ++j)"),
+    ("logit_magnitude_limit", "            has_finite = 1;",
+     "            has_finite = 1;\n            if (fabs(l[x]) >= 1.5e9) return 0;"),
     ("residual_q_minus_p", "double diff = s->p[x] - s->q[x];", "double diff = s->q[x] - s->p[x];"),
     ("temperature_multiplied", "p[x] = exp((l[x] - m) / T);", "p[x] = exp((l[x] - m) * T);"),
     ("tie_to_highest_index", "if (l[x] > l[a]) a = x;", "if (l[x] >= l[a]) a = x;"),
@@ -40,9 +49,9 @@ MUTANTS = [
      "            out[i] = a;\n            return i + 1;"),
     ("target_row_stride_gamma", SAMPLED_TARGET_ROW,
      SAMPLED_TARGET_ROW.replace("(size_t)b * (size_t)(G + 1) + (size_t)i", "(size_t)b * (size_t)G + (size_t)i")),
-    ("draft_rows_reversed", "load_row(s->draft, s->dtype, r, V, s->ld);\n        const double lse_q = softmax_T(s->ld, V, T, s->q);",
+    ("draft_rows_reversed", "load_row(s->draft, s->dtype, r, V, s->ld);\n        softmax_T2(s->ld, V, T, s->q, &m_q, &logZ_q);",
      "load_row(s->draft, s->dtype, (size_t)b * (size_t)G + (size_t)(G - 1 - i), V, s->ld);\n"
-     "        const double lse_q = softmax_T(s->ld, V, T, s->q);"),
+     "        softmax_T2(s->ld, V, T, s->q, &m_q, &logZ_q);"),
     ("bf16_decoded_wrong", "[idx]) << 16;", "[idx]) << 15;"),
     ("accepted_token_not_copied", "            out[i] = x;\n        } else {", "            out[i] = tok[0];\n        } else {"),
     ("no_padding_after_n", "for (int j = 0; j <= gamma; ++j) out[j] = -1;",
@@ -61,7 +70,7 @@ MUTANTS = [
      "(size_t)b * (size_t)(G + 1) + (size_t)G, V, s->lt);\n        softmax_T"),
     ("onehot_count_ignored", "        int k = num_draft[b];", "        int k = gamma;"),
     # early exit
-    ("early_alpha_ignores_q", "            alpha = accept_alpha(s->lt[x], lse_p, s->ld[x], lse_q, T);",
+    ("early_alpha_ignores_q", "            alpha = accept_alpha(s->lt[x], m_p, logZ_p, s->ld[x], m_q, logZ_q, T);",
      "            alpha = fmin(px, 1.0);"),
     ("early_greedy_keeps_draft_token", "                out[i] = a;\n                return i;",
      "                out[i] = x;\n                return i;"),
