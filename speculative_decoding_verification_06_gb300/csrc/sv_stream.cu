@@ -1167,10 +1167,31 @@ struct Kern {
             if (dbg.lse_draft)
                 dbg.lse_draft[r] = draft ? lse_from_stats(ms_of(st[GM + 1 + j]), sc, T) : nan("");
         }
-        if (a.tree) {
-            tree_walk(b, k, st, greedy, sc, np);
-            return;
-        }
+        const ScanPre pre{x_l, u_l, lt_l, ld_l};
+        Job j;
+        const int* set = nullptr;  // a tree draw's excluded tokens
+        if (a.tree ? tree_walk(b, k, st, greedy, sc, np, j, set) : linear_scan(b, st, greedy, sc, np, pre, j))
+            finish_job(k, j, set);
+    }
+
+    // What the acceptance scan reads before it knows the temperature: lane's
+    // token, uniform and the logits at the token (rows lane < 32).
+    struct ScanPre {
+        int x_l;
+        float u_l, lt_l, ld_l;
+    };
+
+    // The left-to-right scan of request b (not a tree): writes the accepted
+    // tokens and count; for a draw fills job j and returns true.
+    __device__ bool linear_scan(int b, const Rec* st, bool greedy, const Scale& sc, int np, const ScanPre& pre,
+                                Job& j) const {
+        const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V;
+        const bool onehot = a.onehot;
+        const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
+        const sv_debug_out& dbg = a.dbg;
+        int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
+        const int x_l = pre.x_l;
+        const float u_l = pre.u_l, lt_l = pre.lt_l, ld_l = pre.ld_l;
         // first failing position over all lanes (gamma may exceed 32)
         int n = np;
         for (int base = 0; base < np; base += 32) {
@@ -1225,8 +1246,7 @@ struct Kern {
                 if (dbg.w_total) dbg.w_total[b] = nan("");
             }
         }
-        if (greedy) return;
-        Job j;
+        if (greedy) return false;
         j.b = b;
         j.n = n;
         j.slot = n;
@@ -1246,7 +1266,7 @@ struct Kern {
         }
         j.kind = d.base_kind();
         if (lane == 0 && dbg.kind) dbg.kind[b] = j.kind == kKindResidualOnehot ? kKindResidual : j.kind;
-        finish_job(k, j, nullptr);
+        return true;
     }
 
     // Lane 0 publishes draw job k of request j.b. An anchored draw goes to the
@@ -1396,7 +1416,8 @@ struct Kern {
     // the job's set. At T = 0 the first child whose token is the argmax of
     // p_u is followed. The test is made in binary64 on lane 0, as the
     // one-block-per-request kernel makes it.
-    __device__ void tree_walk(int b, int k, const Rec* st, bool greedy, const Scale& c, int np) const {
+    __device__ bool tree_walk(int b, int k, const Rec* st, bool greedy, const Scale& c, int np, Job& j,
+                              const int*& set_out) const {
         const int lane = threadIdx.x & 31, GM = a.gamma, V = a.V;
         const sv_debug_out& dbg = a.dbg;
         int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
@@ -1462,11 +1483,10 @@ struct Kern {
                 dbg.kind[b] = ne > 0 ? kKindResidual : kKindBonus;
             }
         }
-        if (greedy) return;
+        if (greedy) return false;
         u = __shfl_sync(0xffffffffu, u, 0);
         n = __shfl_sync(0xffffffffu, n, 0);
         ne = __shfl_sync(0xffffffffu, ne, 0);
-        Job j;
         j.b = b;
         j.n = u;  // the draw's row: the last node
         j.slot = n;
@@ -1477,7 +1497,8 @@ struct Kern {
         d.fix = kFixTarget;
         j.kind = d.base_kind();
         __syncwarp();  // lane 0's set, before the other lanes read it
-        finish_job(k, j, set);  // publish's fence also orders the set before the job
+        set_out = set;  // publish's fence also orders the set before the job
+        return true;
     }
 
     // A run is kTPT consecutive tokens, 64 bytes, held packed as 4 vectors of
@@ -2297,13 +2318,17 @@ struct Kern {
         {
             const int tb = __shfl_sync(0xffffffffu, rt.bad, 0), db = __shfl_sync(0xffffffffu, rd.bad, 0);
             const bool ok = !bad && !(tb & kBadData) && !(has_draft && (db & kBadData));
-            if (ok && samp && (tb & kBadPlain)) {
-                const MaxSum ms = plain_row_warp(a.target, static_cast<long long>(b) * (GM + 1) + pos, sc);
-                rt = Rec{ms.m, ms.s, kRecPlain, 0};
-            }
-            if (ok && has_draft && (db & kBadPlain)) {
-                const MaxSum ms = plain_row_warp(a.draft, static_cast<long long>(b) * GM + pos, sc);
-                rd = Rec{ms.m, ms.s, kRecPlain, 0};
+            for (int w = 0; w < 2; ++w) {  // the target row, then the draft row
+                if (!(ok && (w == 0 ? samp && (tb & kBadPlain) : has_draft && (db & kBadPlain)))) continue;
+                const MaxSum ms = plain_row_warp(w == 0 ? a.target : a.draft,
+                                                 w == 0 ? static_cast<long long>(b) * (GM + 1) + pos
+                                                        : static_cast<long long>(b) * GM + pos,
+                                                 sc);
+                const Rec r{ms.m, ms.s, kRecPlain, 0};
+                if (w == 0)
+                    rt = r;
+                else
+                    rd = r;
             }
         }
         int plain_draw = 0;
