@@ -16,6 +16,10 @@ spec_verify_host (host buffers; copies inside the timed region).
 roofline: algorithmic bytes per call / average call duration, against the
 measured HBM copy bandwidth. cpu_baseline / --impl reference: the CPU oracle
 (test infrastructure) timed on this host's cores on a bounded sample.
+near_ties (N = 1): the headline batch's outputs judged by the oracle under the
+parity rules, with the near-tie counts and their exact expectation.
+per_workload (N = 1): each of the five workloads timed alone in the same run
+(per-call figures, rows/s, achieved GB/s and roofline fraction, clocks).
 """
 from __future__ import annotations
 
@@ -59,6 +63,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the per-workload block (all five workloads, timed in the same run at N = 1)")
+    ap.add_argument("--no-near-ties", action="store_true",
+                    help="skip the near-tie counts (the oracle over the headline batch, threaded)")
     ap.add_argument("--early-exit", action="store_true",
                     help="early-exit verification: nothing after a request's first rejection is read")
     ap.add_argument("--op", choices=["verify", "onehot", "ngram", "commit", "loop", "tree"], default="verify",
@@ -440,6 +448,73 @@ def run_aux(args, w, local):
     print(json.dumps(line), flush=True)
 
 
+def measure_workload(sv, w, path, early, stream, seconds=0.5, steps=None, warmup=10):
+    """One workload timed alone: its batch resident on the device, calls
+    bracketed by CUDA events on `stream` after warm-up, a clock sampler
+    running. The number of calls fills about `seconds` (at least 200) unless
+    `steps` is given. Returns the per-call figures and the roofline."""
+    import torch
+    from workloads import synthetic
+    batch = synthetic.generate(w, k=0)
+    dev = [torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in batch.arrays()]
+    B, G, V = batch.B, w.gamma, w.V
+    dt = sv.SV_F32 if w.dtype == "f32" else sv.SV_BF16
+    out_t = torch.empty((B, G + 1), dtype=torch.int32, device="cuda")
+    out_n = torch.empty((B,), dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(16, sv.workspace_size(B, G, V, dt)), dtype=torch.uint8, device="cuda")
+
+    def call():
+        sv.spec_verify(*dev, out_tokens=out_t, out_num_accepted=out_n, workspace=ws, stream=stream, path=path,
+                       early_exit=early)
+
+    _, probe = time_calls(call, 20, warmup, stream)
+    K = steps or int(min(20000, max(200, seconds / max(float(np.median(probe)) * 1e-3, 1e-6))))
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    total_ms, per_call = time_calls(call, K, 3, stream)
+    clk = clocks.stop()
+    num_acc = out_n.cpu().numpy()
+    abytes = (algorithmic_bytes_early if early else algorithmic_bytes)(batch, num_acc)
+    peak, _ = peak_hbm()
+    avg = float(per_call.mean()) * 1e-3
+    achieved = abytes / avg / 1e9
+    del dev, ws
+    torch.cuda.empty_cache()
+    return {"workload": w.description, "calls": K, "avg_call_us": avg * 1e6,
+            "p10_p50_p90_call_us": [float(np.percentile(per_call, q)) * 1e3 for q in (10, 50, 90)],
+            "rows_per_s": K * B * (G + 1) / (total_ms * 1e-3), "algorithmic_bytes_per_call": int(abytes),
+            "achieved_gbs": achieved, "frac": achieved / peak, "clocks": clk,
+            "launches_per_call": sv.last_launch_count()}
+
+
+def near_tie_counts(batch, out_tokens, num_acc):
+    """The headline batch's outputs judged by the oracle under the parity
+    rules (test infrastructure, run here on the host cores): near-tie counts
+    and their expectation. Returns a dict, with "parity": "ok" or the first
+    mismatch."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import parity
+    t0 = time.perf_counter()
+    ora, det = parity.run_oracle(batch)
+    gpu = {"out_tokens": out_tokens, "out_num_accepted": num_acc}
+    res = {"requests": int(batch.B)}
+    try:
+        rep = parity.compare(batch, gpu, ora, det)
+        res["parity"] = "ok"
+    except AssertionError as e:
+        return {"requests": int(batch.B), "parity": f"mismatch: {str(e)[:200]}"}
+    res.update({"accept_decisions": rep.accept_decisions, "accept_near_ties": rep.accept_near_ties,
+                "accept_near_ties_expected": rep.accept_ties_expected, "accept_cap": rep.accept_tie_cap(),
+                "draws": rep.draws, "draw_near_ties": rep.sample_near_ties,
+                "draw_near_ties_at_margin": rep.draw_ties_at_margin,
+                "draw_near_ties_expected": rep.draw_ties_expected,
+                "draw_near_ties_sigma": rep.draw_ties_var ** 0.5,
+                "draw_ties_within_5_sigma": bool(rep.draw_ties_consistent()),
+                "oracle_s": time.perf_counter() - t0})
+    return res
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -554,6 +629,26 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(batch, args.cpu_seconds, G + 1)
 
+    ties = None
+    if rank == 0 and world == 1 and not args.no_near_ties:
+        ties = near_tie_counts(batch, out_tokens.cpu().numpy(), num_acc)
+
+    per_workload = None
+    if rank == 0 and world == 1 and not args.no_per_workload:
+        headline = {"workload": w.description, "calls": K, "avg_call_us": avg_call_s * 1e6,
+                    "p10_p50_p90_call_us": [float(np.percentile(per_call_ms, q)) * 1e3 for q in (10, 50, 90)],
+                    "rows_per_s": value / world, "algorithmic_bytes_per_call": int(abytes),
+                    "achieved_gbs": achieved, "frac": achieved / peak, "clocks": clk,
+                    "launches_per_call": launches_per_call}
+        per_workload = {}
+        del dev, ws
+        torch.cuda.empty_cache()
+        for name in ("tiny", "greedy", "sampling", "mixed", "large"):
+            if name == args.workload:
+                per_workload[name] = headline
+            else:
+                per_workload[name] = measure_workload(sv, synthetic.BY_NAME[name], path, args.early_exit, stream)
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -583,6 +678,8 @@ def main():
         "requests_per_s": world * K * B / (total_ms * 1e-3),
         "mean_accepted": float(num_acc[num_acc >= 0].mean()),
         "acceptance_rate_sampled": float(num_acc[samp_mask].mean() / G) if samp_mask.any() else None,
+        "near_ties": ties,
+        "per_workload": per_workload,
     }
     print(json.dumps(line), flush=True)
     if dist:

@@ -86,8 +86,12 @@ typedef int32_t sv_status;
 
 /* Bits of the optional device status word (int32), OR-ed in by the kernels. */
 #define SV_STATUS_BAD_REQUEST 0x1 /* at least one request was invalid (-1) */
-#define SV_STATUS_TIMEOUT 0x2     /* a bounded wait inside a kernel ran out; the
-                                     outputs of that call are not valid */
+#define SV_STATUS_TIMEOUT 0x2     /* a bounded wait inside a streaming kernel ran
+                                     out. Whether or not a status word was given, every
+                                     request that was not final by then keeps
+                                     out_num_accepted = -1 (the kernels write a count
+                                     only once its request is final); its out_tokens
+                                     may hold a partial result */
 #define SV_STATUS_TRUNCATED 0x4   /* spec_commit: not every emitted token of a request
                                      fitted in its token buffer */
 
@@ -242,11 +246,16 @@ sv_status spec_verify_host(const void* target_logits, const void* draft_logits, 
  * library; a shape that needs more returns SV_ERR_SCRATCH_LIMIT before
  * anything is enqueued. Nothing is allocated: no cudaMalloc, no cudaFree.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. All calls in the process share the one array,
- * which keeps the previous call's contents (the call clears the part that
- * must start at zero itself): two calls that overlap on the GPU, on any
- * streams, race on it and give undefined results. */
+ * (cudaGetSymbolAddress) with that device current, and keeps it with the
+ * driver's id of the current context; a call in another context (after a
+ * device reset, say) looks it up again. Make the first call on a device, and
+ * the first after a reset, before any stream capture. All calls in the
+ * process share the one array, which keeps the previous call's contents (the
+ * call clears the part that must start at zero itself): two calls that
+ * overlap on the GPU, on any streams, race on it and give undefined results.
+ * There is no status word: if a bounded wait inside the kernel runs out (see
+ * SV_STATUS_TIMEOUT), every request that was not final keeps
+ * out_num_accepted = -1. */
 sv_status spec_verify_noalloc(const void* target_logits, const void* draft_logits, sv_dtype dtype,
                               int B, int gamma, int V, const int32_t* draft_tokens,
                               const float* u_accept, const float* u_sample, const float* temperature,

@@ -56,7 +56,7 @@ def build(force: bool = False, src: str | None = None, out: str | None = None) -
 class _Detail(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "max_target", "lse_target", "argmax_target", "max_draft", "lse_draft",
-        "p_x", "q_x", "alpha", "accept_margin", "w_total", "sample_margin", "kind")]
+        "p_x", "q_x", "alpha", "accept_margin", "w_total", "sample_margin", "kind", "tie_measure")]
 
 
 def _bind(lib):
@@ -153,6 +153,7 @@ def _detail_arrays(B, G):
             "p_x": np.empty((B, G)), "q_x": np.empty((B, G)), "alpha": np.empty((B, G)),
             "accept_margin": np.empty((B, G)), "w_total": np.empty((B,)),
             "sample_margin": np.empty((B,)), "kind": np.empty((B,), dtype=np.int32),
+            "tie_measure": np.empty((B,)),
     }
 
 

@@ -111,6 +111,31 @@ static int accepts(double u, double alpha, int p_positive) {
     return u < alpha || u == 0.0;
 }
 
+/* For the checker: the measure of {t in [0, W) : |t - e| <= delta for an edge
+ * e of the inverse CDF}, divided by W, with delta = ORACLE_TIE_MARGIN * W and
+ * the edges 0, C_0, ..., C_{V-1} = W in index order (non-decreasing): the
+ * union of the intervals [e - delta, e + delta], merged left to right and
+ * clipped to [0, W]. */
+static double tie_measure(const double* w, int V, double W) {
+    if (!(W > 0.0)) return 1.0;
+    const double delta = ORACLE_TIE_MARGIN * W;
+    double lo = 0.0, hi = delta, total = 0.0, C = 0.0;
+    for (int k = 0; k < V; ++k) {
+        C += w[k];
+        const double a = C - delta, b = C + delta;
+        if (a <= hi) {
+            if (b > hi) hi = b;
+        } else {
+            total += hi - lo;
+            lo = a;
+            hi = b;
+        }
+    }
+    if (hi > W) hi = W;
+    if (lo < W) total += hi - lo;
+    return total / W;
+}
+
 /* Inverse-CDF draw over non-negative weights w (need not sum to one):
  * W = sum w, t = u * W, and the token is the smallest k whose inclusive
  * prefix sum C_k exceeds t, so a zero-weight token is never drawn. If
@@ -191,6 +216,7 @@ static void clear_detail(const oracle_detail* d, int b, int G) {
     }
     set_d(d->w_total, (size_t)b, NAN);
     set_d(d->sample_margin, (size_t)b, NAN);
+    set_d(d->tie_measure, (size_t)b, NAN);
     set_i(d->kind, (size_t)b, ORACLE_KIND_ERROR);
 }
 
@@ -291,6 +317,7 @@ static int verify_sampled(const scratch_t* s, int b, double T, const int32_t* to
     out[n] = draw_inverse_cdf(s->w, V, (double)us, &W, &margin);
     set_d(d->w_total, (size_t)b, W);
     set_d(d->sample_margin, (size_t)b, margin);
+    if (d->tie_measure) d->tie_measure[b] = tie_measure(s->w, V, W);
     return n;
 }
 
@@ -448,6 +475,7 @@ static int verify_sampled_onehot(const scratch_t* s, int b, double T, const int3
     out[n] = draw_inverse_cdf(s->w, V, (double)us, &W, &margin);
     set_d(d->w_total, (size_t)b, W);
     set_d(d->sample_margin, (size_t)b, margin);
+    if (d->tie_measure) d->tie_measure[b] = tie_measure(s->w, V, W);
     return n;
 }
 
@@ -580,6 +608,7 @@ static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok,
             set_i(d->kind, (size_t)b, ORACLE_KIND_RESIDUAL);
             set_d(d->w_total, (size_t)b, W);
             set_d(d->sample_margin, (size_t)b, margin);
+            if (d->tie_measure) d->tie_measure[b] = tie_measure(s->w, V, W);
             return i;
         }
         out[i] = x;
@@ -595,6 +624,7 @@ static int verify_early(const scratch_t* s, int b, double T, const int32_t* tok,
     set_i(d->kind, (size_t)b, ORACLE_KIND_BONUS);
     set_d(d->w_total, (size_t)b, W);
     set_d(d->sample_margin, (size_t)b, margin);
+    if (d->tie_measure) d->tie_measure[b] = tie_measure(s->w, V, W);
     return k;
 }
 
@@ -743,6 +773,7 @@ static int verify_tree_walk(const scratch_t* s, int b, double T, const int32_t* 
         set_i(d->kind, (size_t)b, ne > 0 ? ORACLE_KIND_RESIDUAL : ORACLE_KIND_BONUS);
         set_d(d->w_total, (size_t)b, W);
         set_d(d->sample_margin, (size_t)b, margin);
+        if (d->tie_measure) d->tie_measure[b] = tie_measure(s->w, V, W);
         return n;
     }
 }

@@ -79,7 +79,14 @@ typedef struct {
     double* w_total;       /* [B] W of the residual or bonus draw */
     double* sample_margin; /* [B] min(t - C_{k-1}, C_k - t) / W of that draw */
     int32_t* kind;         /* [B] ORACLE_KIND_* */
+    double* tie_measure;   /* [B] for the checker: the probability, over u_sample
+                              uniform on [0, 1), that t = u W lies within
+                              ORACLE_TIE_MARGIN * W of an edge of that draw's CDF
+                              (0, C_0, ..., C_{V-1} = W), in fp64 */
 } oracle_detail;
+
+/* The checker's margin for near-tie draws, relative to W. */
+#define ORACLE_TIE_MARGIN 1e-5
 
 /* The verification step for B independent requests, all on host memory.
  *   target      [B, gamma+1, V] logits (dtype), row i scores draft token i,

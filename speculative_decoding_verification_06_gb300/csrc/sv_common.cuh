@@ -188,6 +188,21 @@ struct MaxSumA {
     float s;
 };
 
+// Adds one logit to an anchored state (the caller screens NaN and +inf);
+// sets `flag` when the anchor leaves its range (the row is then recomputed
+// plain).
+__device__ __forceinline__ void maxsum_add_a(MaxSumA& st, float x, float c, int& flag) {
+    if (x > st.m) {
+        const float mc = scaled_max(x, c);
+        if (!(fabsf(mc) < 8388608.0f)) flag = 1;
+        st.s = (st.m == neg_inf()) ? 0.0f : __fmul_rn(st.s, ex2(__fsub_rn(scaled_max(st.m, c), mc)));
+        st.m = x;
+        st.s = __fadd_rn(st.s, row_term(x, c, mc));
+    } else if (x != neg_inf()) {
+        st.s = __fadd_rn(st.s, row_term(x, c, scaled_max(st.m, c)));
+    }
+}
+
 __device__ __forceinline__ MaxSumA maxsum_merge_a(MaxSumA a, MaxSumA b, float c) {
     if (b.m > a.m) {
         MaxSumA t = a;

@@ -8,6 +8,8 @@
 // process's footprint). The entry point allocates nothing: the scratch is the
 // file-scope array below, which every GPU that loads this library holds, at
 // its full size, until the process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "sv_internal.h"
@@ -22,20 +24,63 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx_id = 0;  // the driver's id of the context the address belongs to (0: none)
+    void* ptr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 
-// Device address of g_noalloc_scratch on the current device. In host code the
-// array's name is only a host-side handle; the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// The driver's current-context calls, reached through the runtime (the
+// library links no driver library of its own). Null where the driver lacks
+// them; every call then asks the runtime for the address afresh.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+std::once_flag g_entry_once;
+
+void load_entry_points() {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_ctx_id = reinterpret_cast<CtxGetIdFn>(f);
+    cudaGetLastError();
+}
+
+// The id of the calling thread's current context, 0 when it cannot be told.
+unsigned long long current_context_id() {
+    if (!g_ctx_current || !g_ctx_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_noalloc_scratch in the current context. In host code
+// the array's name is only a host-side handle; the address comes from
+// cudaGetSymbolAddress with the device current, once per context: it is
+// kept with the driver's id of that context, so that after a device reset
+// (a new context, where the module may load at another address) it is asked
+// for again instead of reused.
 cudaError_t scratch_address(int device, void** ptr) {
+    std::call_once(g_entry_once, load_entry_points);
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[device]) {
+    ScratchAddr& c = g_scratch[device];
+    const unsigned long long id = current_context_id();
+    if (id == 0 || c.ctx_id != id || !c.ptr) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_ptr[device] = p;
+        c.ptr = p;
+        c.ctx_id = current_context_id();  // the call above made the device's context current if it was not
     }
-    *ptr = g_scratch_ptr[device];
+    *ptr = c.ptr;
     return cudaSuccess;
 }
 

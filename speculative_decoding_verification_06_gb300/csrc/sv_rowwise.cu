@@ -11,6 +11,7 @@
 // préservée; wiki "Speculative Decoding", eq. alpha(x) and eq. p_corr;
 // "Accélérer Sonar grâce à la spéculation", §Décodage spéculatif.
 #include <cmath>
+#include <type_traits>
 
 #include "sv_common.cuh"
 #include "sv_internal.h"
@@ -45,6 +46,7 @@ struct Shared {
     int excl[SV_MAX_GAMMA];  // tree: tokens of the rejected children at the last node
     int nexcl;
     int draw_row;            // the row of the draw (tree: the last node)
+    int row_flag;            // the last row pass found the anchored form out of range
 };
 
 // Logits a thread folds into one partial before the partial joins its running
@@ -52,35 +54,49 @@ struct Shared {
 // row, 131072 logits at V = 2^24).
 constexpr int kInner = 64;
 
-template <int DT>
-__device__ RowStat row_maxsum(const void* base, size_t row, int V, const Scale& c, Shared& sh) {
-    MaxSum st = maxsum_empty();
-    int bad = 0;
+// One pass over a row: the anchored form (PLAIN false; a thread whose
+// anchor leaves its range sets the row's plain flag) or the plain form.
+template <int DT, bool PLAIN>
+__device__ RowStat row_pass(const void* base, size_t row, int V, const Scale& c, Shared& sh) {
+    using State = typename std::conditional<PLAIN, MaxSum, MaxSumA>::type;
+    auto empty = []() -> State {
+        if constexpr (PLAIN) return MaxSum{neg_inf(), 0.0f, 1};
+        else return MaxSumA{neg_inf(), 0.0f};
+    };
+    auto merge = [&](State a, State b) -> State {
+        if constexpr (PLAIN) return maxsum_merge(a, b, c);
+        else return maxsum_merge_a(a, b, c.c);
+    };
+    State st = empty();
+    int bad = 0, flag = 0;
     const size_t off = row * static_cast<size_t>(V);
     for (int x0 = threadIdx.x; x0 < V; x0 += kThreads * kInner) {
-        MaxSum part = maxsum_empty();
+        State part = empty();
         const int x1 = static_cast<int>(min(static_cast<long long>(V), static_cast<long long>(x0) + kThreads * kInner));
         for (int x = x0; x < x1; x += kThreads) {
             const float l = load_logit<DT>(base, off + x);
             if (bad_logit(l)) {
                 bad = 1;
             } else {
-                maxsum_add(part, l, c);
+                if constexpr (PLAIN) maxsum_add(part, l, c);
+                else maxsum_add_a(part, l, c.c, flag);
             }
         }
-        st = maxsum_merge(st, part, c);
+        st = merge(st, part);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        MaxSum other{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o),
-                     __shfl_xor_sync(0xffffffffu, st.plain, o)};
-        st = maxsum_merge(st, other, c);
+        State other = st;
+        other.m = __shfl_xor_sync(0xffffffffu, st.m, o);
+        other.s = __shfl_xor_sync(0xffffffffu, st.s, o);
+        st = merge(st, other);
     }
     bad = __any_sync(0xffffffffu, bad);
+    flag = __any_sync(0xffffffffu, flag);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) {
-        sh.ms[warp] = st;
-        sh.bad[warp] = bad;
+        sh.ms[warp] = MaxSum{st.m, st.s, PLAIN ? 1 : 0};
+        sh.bad[warp] = bad | (flag << 1);
     }
     __syncthreads();
     RowStat r;
@@ -91,10 +107,21 @@ __device__ RowStat row_maxsum(const void* base, size_t row, int V, const Scale& 
             acc = maxsum_merge(acc, sh.ms[w], c);
             b |= sh.bad[w];
         }
-        r = {acc.m, acc.s, -1, (b || acc.m == neg_inf()) ? 1 : 0, acc.plain};
+        r = {acc.m, acc.s, -1, ((b & 1) || acc.m == neg_inf()) ? 1 : 0, acc.plain};
+        sh.row_flag = (b & 2) && !(r.bad);
     }
     __syncthreads();
     return r;  // meaningful on thread 0 only
+}
+
+// A row's statistics in the anchored form, or (when its anchor left the
+// range, or c overflowed) recomputed in the plain form by a second pass.
+template <int DT>
+__device__ RowStat row_maxsum(const void* base, size_t row, int V, const Scale& c, Shared& sh) {
+    const RowStat r = row_pass<DT, false>(base, row, V, c, sh);
+    if (!sh.row_flag) return r;
+    __syncthreads();  // every thread has read the flag before the next pass clears it
+    return row_pass<DT, true>(base, row, V, c, sh);
 }
 
 template <int DT>

@@ -118,8 +118,8 @@ struct Layout {
     long long Et;  // target elements B*(gamma+1)*V
     int G, MT, MD, NCH, vec;
     int NI;  // early exit: items per task, groups of kEeGroup chunks
-    size_t hdr, req_done, job_done, ready, ee_tasks, ee_done, clear_bytes, rec_t, rec_d, ee_rec, jobs, jobset, wsums,
-        total;
+    size_t hdr, req_done, job_done, ready, ee_tasks, ee_done, clear_bytes, rec_t, rec_d, ee_rec, jobs, jobset,
+        wsums, total;
     int ee_cap;  // early exit: task slots, B (gamma + 2)
 };
 
@@ -569,11 +569,14 @@ struct Kern {
         ++c.it;
     }
 
+    // A bounded wait ran out: the block stops and the status bit is set.
     __device__ void set_abort(int32_t* d_status) const {
         ctl.abort = 1;
         atomicOr(&hdr()->status, SV_STATUS_TIMEOUT);
         if (d_status) atomicOr(d_status, SV_STATUS_TIMEOUT);
     }
+
+
 
     // Publishes draw job k (its record written by this thread): the producers
     // of every block take draw items from the jobs in publication order.
@@ -793,10 +796,21 @@ struct Kern {
                     if (rel3 >= 0 && rel3 < kMapMax) ctl.map3[rel3] = static_cast<short>(b);
                     ctl.kmap[b] = static_cast<short>(-(j + 1));
                 }
+                // A request's count stays -1 until the request is final (then its
+                // scan, or its draw, writes it), so that a call that gives up on a
+                // wait shows -1 for every request not yet final. The block whose
+                // slice holds the first element of the request's target rows
+                // clears it here, before it posts any share (the scan comes after
+                // every share).
+                const long long first = f ? static_cast<long long>(k) * R : E1 + static_cast<long long>(b - k) * R;
+                const long long lo = f ? part_begin(E1, G, g, L.vec) : E1 + part_begin(E3, G, g, L.vec);
+                const long long hi = f ? part_begin(E1, G, g + 1, L.vec) : E1 + part_begin(E3, G, g + 1, L.vec);
+                if (first >= lo && first < hi) a.out_num_accepted[b] = -1;
             }
             carry += total;
             bar_sync(kBarConsumers, kConsumers);
         }
+        __threadfence();  // the cleared counts, before this block's first post
     }
 
     // ---- phase-1 consumer: per-thread state of the current row piece
@@ -1140,6 +1154,7 @@ struct Kern {
                 if (dbg.p_x) dbg.p_x[r] = nan("");
                 if (dbg.q_x) dbg.q_x[r] = nan("");
             }
+            __syncwarp();
             if (lane == 0) {
                 a.out_num_accepted[b] = -1;
                 if (a.d_status) atomicOr(a.d_status, SV_STATUS_BAD_REQUEST);
@@ -1239,12 +1254,12 @@ struct Kern {
             else
                 out[j] = -1;
         }
-        if (lane == 0) {
+        // the count is written once the request is final: here at T = 0, else
+        // with the drawn token (until then it stays -1, see prologue)
+        if (lane == 0 && greedy) {
             a.out_num_accepted[b] = n;
-            if (greedy) {
-                if (dbg.kind) dbg.kind[b] = kKindGreedy;
-                if (dbg.w_total) dbg.w_total[b] = nan("");
-            }
+            if (dbg.kind) dbg.kind[b] = kKindGreedy;
+            if (dbg.w_total) dbg.w_total[b] = nan("");
         }
         if (greedy) return false;
         j.b = b;
@@ -1400,6 +1415,7 @@ struct Kern {
         }
         if (lane == 0) {
             a.out_tokens[static_cast<size_t>(jb.b) * (GM + 1) + jb.slot] = token >= 0 ? token : V - 1;
+            a.out_num_accepted[jb.b] = jb.slot;  // the request is final
             if (a.dbg.w_total)
                 a.dbg.w_total[jb.b] = kind == kKindResidual ? static_cast<double>(total) * kFixResidualInv
                                                             : static_cast<double>(total) * kFixTargetInv *
@@ -1475,8 +1491,8 @@ struct Kern {
             u = next;
         }
         if (lane == 0) {
-            a.out_num_accepted[b] = n;
             if (greedy) {
+                a.out_num_accepted[b] = n;
                 if (dbg.kind) dbg.kind[b] = kKindGreedy;
                 if (dbg.w_total) dbg.w_total[b] = nan("");
             } else if (dbg.kind) {
@@ -1873,6 +1889,8 @@ struct Kern {
             // cannot happen: the runs partition [0, total) exactly
             a.out_tokens[static_cast<size_t>(jb.b) * (a.gamma + 1) + jb.slot] = a.V - 1;
         }
+        __syncwarp();
+        if (lane == 0) a.out_num_accepted[jb.b] = jb.slot;  // the request is final
         if (lane == 0 && a.dbg.w_total) {
             const double W = static_cast<double>(total);
             a.dbg.w_total[jb.b] =
@@ -1921,7 +1939,8 @@ struct Kern {
     }
 
     // One lane: request b is done (its outputs are written).
-    __device__ void ee_finish_request() const {
+    __device__ void ee_finish_request(int b) const {
+        (void)b;
         __threadfence();
         atomicAdd(&hdr()->n_fin, 1u);
     }
@@ -2201,14 +2220,16 @@ struct Kern {
         }
     }
 
-    // Finisher, one lane: the request ends at n (-1: invalid); positions after
-    // n are -1, and the checking outputs of the rows not read are NaN / -1.
-    __device__ void ee_close(int b, int n, int from_row) const {
+    // One lane: the request ends at n (-1: invalid); positions after n are -1,
+    // and the checking outputs of the rows not read are NaN / -1. The count
+    // is written when the request is final (`final`); a pending draw writes it
+    // with its token.
+    __device__ void ee_close(int b, int n, int from_row, bool final = true) const {
         const int GM = a.gamma;
         int32_t* out = a.out_tokens + static_cast<size_t>(b) * (GM + 1);
         const sv_debug_out& dbg = a.dbg;
         for (int j = n < 0 ? 0 : n + 1; j <= GM; ++j) out[j] = -1;
-        a.out_num_accepted[b] = n;
+        if (final) a.out_num_accepted[b] = n;
         for (int j = from_row; j <= GM; ++j) {
             const size_t r = static_cast<size_t>(b) * (GM + 1) + j;
             if (dbg.max_target) dbg.max_target[r] = nanf("");
@@ -2346,7 +2367,7 @@ struct Kern {
         for (int q = 0; q < static_cast<int>(sizeof(Job) / 4); ++q) dst[q] = src[q];
         plain_draw_warp(j, nullptr);
         __syncwarp();
-        if ((threadIdx.x & 31) == 0) ee_finish_request();
+        if ((threadIdx.x & 31) == 0) ee_finish_request(b);
     }
 
     // The decision at position pos of request b on lane 0, from the merged
@@ -2378,7 +2399,7 @@ struct Kern {
             if (a.d_status) atomicOr(a.d_status, SV_STATUS_BAD_REQUEST);
             if (dbg.kind) dbg.kind[b] = kKindInvalid;
             if (dbg.w_total) dbg.w_total[b] = nan("");
-            ee_finish_request();
+            ee_finish_request(b);
             return 0;
         }
         {  // this position's checking outputs
@@ -2406,7 +2427,7 @@ struct Kern {
             ee_close(b, pos, pos + 1);
             if (dbg.kind) dbg.kind[b] = kKindGreedy;
             if (dbg.w_total) dbg.w_total[b] = nan("");
-            ee_finish_request();
+            ee_finish_request(b);
             return 0;
         }
         if (proposal) {
@@ -2438,7 +2459,7 @@ struct Kern {
         }
         j.kind = d.base_kind();
         out[pos] = -1;  // the search (or the plain draw) fills it in
-        ee_close(b, pos, pos + 1);
+        ee_close(b, pos, pos + 1, false);
         if (dbg.kind) dbg.kind[b] = j.kind == kKindResidualOnehot ? kKindResidual : j.kind;
         jobs()[b] = j;
         if (d.plain()) return 1;  // drawn by the caller's warp
@@ -2492,7 +2513,7 @@ struct Kern {
         } else {
             search_job(b);
             __syncwarp();
-            if ((threadIdx.x & 31) == 0) ee_finish_request();
+            if ((threadIdx.x & 31) == 0) ee_finish_request(b);
         }
         __syncwarp();
         return true;
@@ -2848,6 +2869,10 @@ __global__ void __launch_bounds__(kThreads, 1) early_kernel(Args a, Layout L, ch
     if (warp == kSearchWarp) {
         // the owned tasks g, g + G, ...: decided or searched as soon as their
         // last chunk is counted
+        // a request's count stays -1 until it is final (the owner of its
+        // position 0 clears it before deciding anything)
+        for (int b = blockIdx.x + lane * K.G; b < a.B; b += 32 * K.G) a.out_num_accepted[b] = -1;
+        __threadfence();
         int own_p = blockIdx.x, own_v = 0, pre_p = -1;  // lane 0: next owned task, its code once published
         typename KT::EePre pre{};
         volatile int* vab = &ctl.abort;

@@ -341,6 +341,39 @@ def pin_zero_uniform_accepts(lib, quick=False):
         assert np.array_equal(o[:B - 1, :G], x[:B - 1])
 
 
+def pin_tie_measure_by_brute_force(lib, quick=False):
+    """The checker's tie measure of a draw (oracle detail ``tie_measure``):
+    the probability that t = u W falls within 1e-5 W of an edge of the CDF
+    (0, C_0, ..., W), against a brute-force count over a fine regular grid of
+    u. Extra tokens drawn from p at T = 1 over weights that include runs of
+    tiny ones (their intervals overlap and must be merged, not added)."""
+    rng = np.random.Generator(np.random.Philox(79))
+    B, V = 6, 24
+    w = rng.random((B, V)) + 0.05
+    w[:, 5:9] = 1e-7       # four edges within 1e-5 W of each other
+    w[:, 15] = 3e-6
+    w[1, :] = 1.0 / V      # equal weights
+    target = np.log(np.stack([w, w], axis=1)).astype(np.float32)  # rows 0 and 1
+    draft = target[:, :1].copy()                                   # q = p at row 0: always accepted
+    x = np.zeros((B, 1), np.int32)
+    _, n, det = _run(lib, target, draft, x, np.full((B, 1), 0.5, np.float32), rng.random(B, dtype=np.float32),
+                     np.ones(B, np.float32), detail=True)
+    assert np.all(n == 1)
+    N = 1_000_000 if quick else 4_000_000
+    u = (np.arange(N) + 0.5) / N
+    for b in range(B):
+        p = np.exp(target[b, 1].astype(np.float64))
+        p /= p.sum()
+        edges = np.concatenate([[0.0], np.cumsum(p)])
+        delta = 1e-5 * edges[-1]
+        t = u * edges[-1]
+        k = np.searchsorted(edges, t)
+        near = np.minimum(np.abs(t - edges[np.clip(k - 1, 0, V)]), np.abs(edges[np.clip(k, 0, V)] - t)) <= delta
+        brute = near.mean()
+        got = float(det["tie_measure"][b])
+        assert abs(got - brute) <= 0.02 * brute + 4.0 / N, (b, got, brute)
+
+
 # ------------------------------------------------------------ normalisers etc.
 
 def pin_logsumexp_and_row_facts(lib, quick=False):
@@ -742,6 +775,7 @@ ALL_PINS = [
     pin_one_hot_limit_is_greedy,
     pin_shift_invariance,
     pin_zero_uniform_accepts,
+    pin_tie_measure_by_brute_force,
     pin_logsumexp_and_row_facts,
     pin_residual_mass_identity,
     pin_equal_rows_reduce_to_categorical,

@@ -36,14 +36,33 @@ class Report:
     max_lse_err: float = 0.0
     max_px_rel: float = 0.0
     max_w_rel: float = 0.0
+    # the near-tie population, from the oracle alone (see draw_tie_stats)
+    accept_decisions: int = 0       # sampled accept decisions the oracle evaluated
+    accept_ties_expected: float = 0.0  # sum over them of P(|u - alpha| <= 1e-5 alpha)
+    draws: int = 0                  # draws judged (no near-tie accept before them)
+    draw_ties_at_margin: int = 0    # of them, oracle margin <= 1e-5 W
+    draw_ties_expected: float = 0.0  # sum of the oracle's tie measures
+    draw_ties_var: float = 0.0      # sum of pi (1 - pi)
     notes: list = field(default_factory=list)
 
     def summary(self) -> str:
         return (f"{self.requests} requests ({self.greedy} greedy, {self.sampled} sampled, "
                 f"{self.invalid} invalid): {self.exact_rows} exact, near ties: "
-                f"{self.accept_near_ties} accept / {self.sample_near_ties} draw; max |dlse| "
+                f"{self.accept_near_ties} accept (of {self.accept_decisions} decisions, "
+                f"{self.accept_ties_expected:.3g} expected) / {self.sample_near_ties} draw "
+                f"({self.draw_ties_at_margin} at the 1e-5 margin, {self.draw_ties_expected:.1f} +- "
+                f"{self.draw_ties_var ** 0.5:.1f} expected); max |dlse| "
                 f"{self.max_lse_err:.2e}, max rel p/q {self.max_px_rel:.2e}, max rel W "
                 f"{self.max_w_rel:.2e}")
+
+    def draw_ties_consistent(self) -> bool:
+        """The draws at the 1e-5 margin number within 5 sigma (plus one, for
+        small counts) of the oracle's exact expectation."""
+        return abs(self.draw_ties_at_margin - self.draw_ties_expected) <= 5.0 * self.draw_ties_var ** 0.5 + 1.0
+
+    def accept_tie_cap(self) -> int:
+        """At most 0.01 % of the accept decisions may be near ties."""
+        return int(1e-4 * self.accept_decisions)
 
 
 def _row_values(arr, dtype):
@@ -130,6 +149,11 @@ def compare(batch, gpu, ora, det, margin=MARGIN, rel_tol=REL_TOL, onehot=False) 
         rep.sampled += 1
         n_o = int(on[b])
         am = det["accept_margin"][b]
+        for i in range(min(n_o + 1, G)):  # the decisions the oracle evaluated
+            alpha = float(det["alpha"][b, i])
+            if np.isfinite(alpha) and alpha > 0:
+                rep.accept_decisions += 1
+                rep.accept_ties_expected += min(1.0, alpha * (1 + margin)) - max(0.0, alpha * (1 - margin))
         tie = next((i for i in range(min(n_o + 1, G)) if am[i] <= margin), None)
         if tie is not None:
             rep.accept_near_ties += 1
@@ -148,6 +172,12 @@ def compare(batch, gpu, ora, det, margin=MARGIN, rel_tol=REL_TOL, onehot=False) 
         res_mass = _residual_mass(batch, b, n_o, onehot) if kind == 1 else None
         below = res_mass is not None and res_mass <= 2 * RESIDUAL_RESOLUTION
         tol = margin * W + (RESIDUAL_RESOLUTION if kind == 1 else 0.0)
+        if not below and "tie_measure" in det:
+            pi = float(det["tie_measure"][b])
+            rep.draws += 1
+            rep.draw_ties_expected += pi
+            rep.draw_ties_var += pi * (1.0 - pi)
+            rep.draw_ties_at_margin += int(det["sample_margin"][b] <= margin)
         if not below and det["sample_margin"][b] * W > tol:
             assert k == oo[b, n_o], \
                 f"{ctx}: draw mismatch gpu {k} oracle {oo[b, n_o]} margin {det['sample_margin'][b]}"

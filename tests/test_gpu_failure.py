@@ -59,3 +59,28 @@ def test_a_set_hold_flag_changes_nothing():
     gpu = {"out_tokens": res.out_tokens.cpu().numpy(), "out_num_accepted": res.out_num_accepted.cpu().numpy()}
     ora, det = parity.run_oracle(batch)
     parity.compare(batch, gpu, ora, det)
+
+
+def test_timeout_marks_unfinished_requests_without_a_status_word():
+    """No status word: the outputs alone must show the failure. Every block
+    waits before its draw phase on a flag nothing sets (1 ms limit), so no
+    draw runs: every sampled request must come back with count -1, and a
+    greedy request either -1 or exactly the oracle's result (its scan may have
+    completed before the timeout). The outputs start as 7, so a count the
+    kernels never wrote would show."""
+    import numpy as np
+    batch = synthetic.generate(synthetic.WORKLOADS[4].variant(B=64, V=40000), k=2)
+    args = parity.to_device(batch)
+    out_t = torch.full((batch.B, batch.workload.gamma + 1), 7, dtype=torch.int32, device="cuda")
+    out_n = torch.full((batch.B,), 7, dtype=torch.int32, device="cuda")
+    never = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sv.spec_verify(*args, out_tokens=out_t, out_num_accepted=out_n, path=sv.SV_PATH_STREAMING,
+                   peer_wait_us=1000, hold_flag=never)
+    torch.cuda.synchronize()
+    go, gn = out_t.cpu().numpy(), out_n.cpu().numpy()
+    (oo, on), _ = parity.run_oracle(batch)
+    sampled = batch.temperature > 0
+    assert sampled.any() and (~sampled).any()
+    assert np.all(gn[sampled] == -1)
+    for b in np.flatnonzero(~sampled):
+        assert gn[b] == -1 or (gn[b] == on[b] and np.array_equal(go[b], oo[b])), b

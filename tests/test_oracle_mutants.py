@@ -63,6 +63,10 @@ MUTANTS = [
     ("q_zero_rejects", "    if (ld_x == -INFINITY) return 1.0;", "    if (ld_x == -INFINITY) return 0.0;"),
     ("nan_not_detected", "if (isnan(l[x])) return 0;", "if (0) return 0;"),
     ("draw_from_first_token", "        if (C > t) {", "        if (C >= 0.0) {"),
+    # the checker's tie measure
+    ("tie_measure_adds_overlaps", "        if (a <= hi) {\n            if (b > hi) hi = b;\n        } else {",
+     "        if (0) {\n            if (b > hi) hi = b;\n        } else {"),
+    ("tie_measure_wide_margin", "    const double delta = ORACLE_TIE_MARGIN * W;", "    const double delta = 10.0 * ORACLE_TIE_MARGIN * W;"),
     # deterministic (one-hot) proposals
     ("onehot_residual_keeps_x", "double diff = s->p[x] - (x == tok[n] ? 1.0 : 0.0);", "double diff = s->p[x];"),
     ("onehot_alpha_always_one", "double alpha = fmin(1.0, px / qx);", "double alpha = 1.0;"),

@@ -57,6 +57,9 @@ def test_noalloc_matches_spec_verify_on_consecutive_calls():
             # integer outputs: the tolerance of the parity tests is exact equality
             assert np.array_equal(out_t.cpu().numpy(), ref_t)
             assert np.array_equal(out_n.cpu().numpy(), ref_n)
+        # and against the oracle directly, under the parity tests' rules
+        ora, det = parity.run_oracle(batch)
+        parity.compare(batch, {"out_tokens": out_t.cpu().numpy(), "out_num_accepted": out_n.cpu().numpy()}, ora, det)
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
