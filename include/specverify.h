@@ -105,6 +105,10 @@ typedef int32_t sv_status;
 #define SV_PATH_STREAMING 2 /* persistent grid streaming all rows with bulk copies into
                                shared memory; needs V * element size to be a multiple of
                                16 bytes and 16-byte aligned logit pointers */
+#define SV_PATH_CLUSTER 3   /* one thread-block cluster per request: each row cut into up to
+                               16 slices, one per CTA, merged over distributed shared memory;
+                               no workspace. Needs V * element size a multiple of 16 bytes,
+                               16-byte aligned logits, V <= 2^20, no tree, no early exit */
 
 /* Bytes of device workspace spec_verify needs for this shape on the current
  * device (the streaming path's per-row partial results, draw jobs, sampling

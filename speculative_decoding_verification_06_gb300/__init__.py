@@ -25,7 +25,7 @@ SV_PHASE_SLOTS = 10
 SV_STATUS_BAD_REQUEST, SV_STATUS_TIMEOUT = 0x1, 0x2
 SV_STATUS_TRUNCATED = 0x4
 SV_MAX_GAMMA, SV_MAX_V = 64, 1 << 24
-SV_PATH_AUTO, SV_PATH_ROWWISE, SV_PATH_STREAMING = 0, 1, 2
+SV_PATH_AUTO, SV_PATH_ROWWISE, SV_PATH_STREAMING, SV_PATH_CLUSTER = 0, 1, 2, 3
 KIND_INVALID, KIND_GREEDY, KIND_RESIDUAL, KIND_BONUS = -1, 0, 1, 2
 
 EXPORTED = (

@@ -93,25 +93,35 @@ sv_status spec_verify_workspace_size(int B, int gamma, int V, sv_dtype dtype, si
     return SV_OK;
 }
 
-// Picks the kernel and launches it: the streaming kernel when asked for (or,
-// on SV_PATH_AUTO, when it applies and the target logits reach 64 KB: below
-// that one block per request is quicker), else one block per request.
+// Picks the kernel and launches it. On SV_PATH_AUTO: one cluster per request
+// for small batches (at most kClusterMaxB requests) of rows of at least
+// kClusterMinRow bytes where it applies, the streaming kernel where it
+// applies and the target logits reach 64 KB, else one block per request.
+constexpr int kClusterMaxB = 16;
+constexpr size_t kClusterMinRow = 16u << 10;
 static sv_status dispatch(const Args& a, const DeviceInfo& dev, int path, int grid_ctas, void* workspace,
                    size_t workspace_bytes, sv_stream_t stream) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int grid = streaming_default_grid(dev);
     if (grid_ctas > 0) grid = std::min(grid, grid_ctas);
     const bool stream_ok = streaming_applicable(a) && streaming_grid_ok(a.B, grid);
-    bool use_stream = false;
+    bool use_stream = false, use_cluster = false;
     if (path == SV_PATH_STREAMING) {
         if (!stream_ok) return SV_ERR_INVALID_ARG;
         use_stream = true;
+    } else if (path == SV_PATH_CLUSTER) {
+        if (!cluster_applicable(a)) return SV_ERR_INVALID_ARG;
+        use_cluster = true;
     } else if (path == SV_PATH_AUTO) {
         const size_t target_bytes = static_cast<size_t>(a.B) * (a.gamma + 1) * a.V * elem_bytes(a.dtype);
-        use_stream = stream_ok && target_bytes >= (64u << 10);
+        use_cluster = a.B <= kClusterMaxB && static_cast<size_t>(a.V) * elem_bytes(a.dtype) >= kClusterMinRow &&
+                      cluster_applicable(a);
+        use_stream = !use_cluster && stream_ok && target_bytes >= (64u << 10);
     }
     cudaError_t err;
-    if (use_stream) {
+    if (use_cluster) {
+        err = launch_cluster(a, dev, s);
+    } else if (use_stream) {
         const size_t need = streaming_workspace_bytes(a.B, a.gamma, a.V, a.dtype, grid);
         if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15))
             return SV_ERR_WORKSPACE;
@@ -138,7 +148,7 @@ sv_status spec_verify_ex(const void* target_logits, const void* draft_logits, sv
         !out_num_accepted)
         return SV_ERR_INVALID_ARG;
     const int path = opts ? opts->path : SV_PATH_AUTO;
-    if (path != SV_PATH_AUTO && path != SV_PATH_ROWWISE && path != SV_PATH_STREAMING)
+    if (path != SV_PATH_AUTO && path != SV_PATH_ROWWISE && path != SV_PATH_STREAMING && path != SV_PATH_CLUSTER)
         return SV_ERR_INVALID_ARG;
     if (opts && (opts->grid_ctas < 0 || opts->peer_wait_us < 0)) return SV_ERR_INVALID_ARG;
     DeviceInfo dev;

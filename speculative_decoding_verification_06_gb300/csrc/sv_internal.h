@@ -58,4 +58,9 @@ int streaming_default_grid(const DeviceInfo& dev);
 cudaError_t launch_streaming(const Args& a, const DeviceInfo& dev, int grid, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream);
 
+// Cluster path: one thread-block cluster per request (small batches).
+bool cluster_applicable(const Args& a);
+int cluster_size(int V, int dtype);
+cudaError_t launch_cluster(const Args& a, const DeviceInfo& dev, cudaStream_t stream);
+
 }  // namespace sv

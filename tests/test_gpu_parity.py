@@ -28,6 +28,7 @@ def built():
 ROWWISE = dict(path=sv.SV_PATH_ROWWISE)
 AUTO = dict(path=sv.SV_PATH_AUTO)
 STREAM = dict(path=sv.SV_PATH_STREAMING)
+CLUSTER = dict(path=sv.SV_PATH_CLUSTER)
 
 
 def _small(config, **changes):
@@ -78,6 +79,36 @@ def test_streaming_small_cases(name, w, grid):
         batch = synthetic.generate(w, k=k)
         rep = parity.check(batch, path=sv.SV_PATH_STREAMING, grid_ctas=grid)
         assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
+
+
+CLUSTER_CASES = STREAM_CASES + [
+    ("tiny_V32_f32", _small(1)),
+    ("sampling_V1024_f32_B1", _small(3, B=1, gamma=4, V=1024, hot_tokens=5)),
+    ("mixed_gamma16_V8192", _small(4, B=5, gamma=16, V=8192)),
+    ("greedy_V32000_B8", _small(2)),
+    ("sampling_V128256_B3", _small(3, B=3, gamma=4)),
+]
+
+
+@pytest.mark.parametrize("name,w", CLUSTER_CASES, ids=[c[0] for c in CLUSTER_CASES])
+def test_cluster_cases(name, w):
+    """One thread-block cluster per request: rows cut into up to 16 slices
+    (V = 8 and V = 32 in one CTA; V = 128256 fp32 in 16), merged over
+    distributed shared memory."""
+    for k in range(2):
+        batch = synthetic.generate(w, k=k)
+        rep = parity.check(batch, **CLUSTER)
+        assert rep.exact_rows + rep.accept_near_ties + rep.sample_near_ties + rep.invalid == batch.B
+
+
+@pytest.mark.parametrize("config", [1, 2, 3])
+def test_full_configs_on_the_cluster_path(config):
+    batch = synthetic.generate(config)
+    rep = parity.check(batch, **CLUSTER)
+    print(f"config {config} (clusters):", rep.summary())
+    assert rep.invalid == 0
+    assert rep.accept_near_ties <= rep.accept_tie_cap(), rep.summary()
+    assert rep.draw_ties_consistent(), rep.summary()
 
 
 @pytest.mark.parametrize("config", [1, 2, 3, 4, 5])
@@ -136,7 +167,7 @@ def test_invalid_requests():
     lt[11, 1, :300] = -np.inf
     w = synthetic.WORKLOADS[3].variant(B=B, gamma=G, V=V)
     batch = synthetic.Batch(w, 0, lt, ld, x, ua, us, T)
-    for opts in (ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=5)):
+    for opts in (ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=5), CLUSTER):
         gpu = parity.run_gpu(batch, **opts)
         ora, det = parity.run_oracle(batch)
         rep = parity.compare(batch, gpu, ora, det)
@@ -165,7 +196,7 @@ def test_residual_rounding_to_zero_falls_back_to_p():
     batch = synthetic.Batch(w, 0, lt, ld, x[:, None], np.full((B, 1), 0.99999, np.float32), us,
                             np.ones(B, np.float32))
     C = np.cumsum(special.softmax(lt[0, 0].astype(np.float64)))
-    for opts in (ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=3)):
+    for opts in (ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=3), CLUSTER):
         gpu = parity.run_gpu(batch, **opts)
         assert gpu["status"] == 0
         assert np.all(gpu["out_num_accepted"] == 0)
@@ -370,7 +401,7 @@ def test_largest_vocabulary():
 
 @pytest.mark.parametrize("T", [1e-4, 1e-8, 1e-20, 1e-40])
 @pytest.mark.parametrize("cfg", [3, 4], ids=["fp32", "bf16"])
-@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM, CLUSTER], ids=["rowwise", "stream", "cluster"])
 def test_small_temperatures(T, cfg, opts):
     """T -> 0+: p = softmax(l/T) at every T > 0 on both sides. Below
     T ~ 1.2e-7 (bf16 logits) or where log2(e)/T overflows binary32 (T =
@@ -385,7 +416,7 @@ def test_small_temperatures(T, cfg, opts):
         assert rep.invalid == 0
 
 
-@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM, CLUSTER], ids=["rowwise", "stream", "cluster"])
 def test_tiny_logit_differences_at_subnormal_temperature(opts):
     """Logits a few binary32 subnormal steps apart (multiples of 2^-149) at
     T = 4 * 2^-149: log2(e)/T overflows binary32, yet l/T is of order one, so
@@ -406,7 +437,7 @@ def test_tiny_logit_differences_at_subnormal_temperature(opts):
 
 
 @pytest.mark.parametrize("T", [1e3, 1e30, float(np.finfo(np.float32).max)])
-@pytest.mark.parametrize("opts", [ROWWISE, STREAM], ids=["rowwise", "stream"])
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM, CLUSTER], ids=["rowwise", "stream", "cluster"])
 def test_large_temperatures(T, opts):
     """T -> inf: p and q flatten towards uniform (c = log2(e)/T is subnormal at
     the largest binary32 T); residual masses shrink below resolution."""
@@ -417,8 +448,8 @@ def test_large_temperatures(T, opts):
     assert rep.invalid == 0
 
 
-@pytest.mark.parametrize("opts", [ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=3)],
-                         ids=["rowwise", "stream", "stream-g3"])
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=3), CLUSTER],
+                         ids=["rowwise", "stream", "stream-g3", "cluster"])
 def test_masked_logits(opts):
     """-inf logits (a masked vocabulary): 30 % of each row masked at random;
     in some requests the draft masks its own proposal (q(x) = 0 < p(x): alpha
@@ -445,8 +476,8 @@ def test_masked_logits(opts):
     assert rep.invalid == 0
 
 
-@pytest.mark.parametrize("opts", [ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=3)],
-                         ids=["rowwise", "stream", "stream-g3"])
+@pytest.mark.parametrize("opts", [ROWWISE, STREAM, dict(path=sv.SV_PATH_STREAMING, grid_ctas=3), CLUSTER],
+                         ids=["rowwise", "stream", "stream-g3", "cluster"])
 def test_logits_of_large_magnitude(opts):
     """Logits far beyond the anchored form's range (|fl(m c)| >= 2^23: about
     5.8e6 at T = 1) are summed from the differences to the row max, so every
