@@ -9,12 +9,16 @@
 // warps, one producer warp, one finisher warp and one search warp; there is
 // no grid barrier.
 //
-//  1. Row statistics. Three streams of logits are each cut into G equal
-//     16-byte-aligned slices, one per thread block: the target rows of the
-//     T > 0 requests, their draft rows, and the target rows of the others
-//     (greedy, or invalid). A block streams its three slices in that order,
-//     so that every request that needs a draw completes while the rows of
-//     those that need none are still streaming. The
+//  1. Row statistics. Three streams of logits are cut into equal
+//     16-byte-aligned slices: the target rows of the T > 0 requests, their
+//     draft rows, and the target rows of the others (greedy, or invalid).
+//     The first two are cut into W waves of G slices each (slice w G + g
+//     goes to block g), the third into G slices. A block streams, wave by
+//     wave, its target slice and its draft slice, then its slice of the
+//     third stream. The requests of wave w are complete once wave w has
+//     streamed, so their scans and draw jobs are done while later waves
+//     still stream, and only the last wave's draws wait at the end; the
+//     requests that need no draw come last. The
 //     producer copies its slices through a ring of kStages shared-memory
 //     stages with cp.async.bulk (completion on mbarriers); the consumers fold
 //     each stage into per-thread (max, sum of 2^(l c - fl(m c))) or argmax
@@ -60,7 +64,16 @@ constexpr int kStages = 4;
 constexpr int kStageBytes = 49152;
 constexpr int kVecPerThread = kStageBytes / 16 / kConsumers;  // 8
 constexpr int kChunkBytes = 24576;  // draw-phase chunk of one row (a residual item fills a stage)
-constexpr int kMapMax = 256;   // compacted requests in one block's draft slice
+constexpr int kMapMax = 256;   // requests in one block's slices of one stream (all waves)
+// Waves of the T > 0 requests' streams. More waves let the early requests'
+// scans and draws run while later waves stream, but every wave adds row pieces
+// to each block, and each piece ends with a reduction across the block's
+// warps; the bf16 fold already keeps the SFU (one 2^x a logit) busy most of
+// the time at the copy rate, so on GB300 4 and 16 waves streamed 5% to 60%
+// slower than they saved at the end. One wave.
+constexpr int kMaxWaves = 1;
+constexpr long long kWaveSliceBytes = 256 << 10;  // a block's target slice of one wave, at least
+constexpr int kPrePieces = 3;  // row pieces the acceptance scan reads in its first round
 constexpr int kMaxGrid = 256;  // blocks (partition tables live in shared memory)
 constexpr int kGrab = 4;       // draw items a producer takes per atomic
 constexpr int kEeGroup = 4;    // early exit: chunks of one task taken as one item
@@ -116,18 +129,29 @@ constexpr int kItemLast = 8;     // StageDesc.flags: the last stage of an early-
 // Byte offsets into the caller's workspace and the partition constants.
 struct Layout {
     long long Et;  // target elements B*(gamma+1)*V
-    int G, MT, MD, NCH, vec;
+    int G, NRT, NRD, NCH, vec;  // NRT, NRD: row-piece records of the target and draft streams
     int NI;  // early exit: items per task, groups of kEeGroup chunks
     size_t hdr, req_done, job_done, ready, ee_tasks, ee_done, clear_bytes, rec_t, rec_d, ee_rec, jobs, jobset,
         wsums, total;
     int ee_cap;  // early exit: task slots, B (gamma + 2)
 };
 
-__host__ __device__ inline long long part_begin(long long E, int G, int g, int vec) {
-    if (g <= 0) return 0;
-    if (g >= G) return E;
-    long long x = (E * g) / G;
-    return x - x % vec;
+// A stream of E elements cut into NS slices of S elements (S a multiple of
+// the 16-byte vector; the last slices may be short or empty): slice i is
+// [min(E, i S), min(E, (i + 1) S)).
+struct Slicing {
+    long long E, S;
+    int NS;
+};
+__host__ __device__ inline Slicing make_slicing(long long E, int NS, int vec) {
+    long long S = (E + NS - 1) / NS;
+    S = (S + vec - 1) / vec * vec;
+    return Slicing{E, S > vec ? S : vec, NS};
+}
+__device__ __forceinline__ long long slice_begin(const Slicing& s, long long i) { return min(s.E, i * s.S); }
+// The slice holding element e (0 <= e < E).
+__device__ __forceinline__ int slice_of(const Slicing& s, long long e) {
+    return static_cast<int>(min(static_cast<long long>(s.NS - 1), e / s.S));
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -138,10 +162,10 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.vec = 16 / es;
     L.Et = static_cast<long long>(B) * (gamma + 1) * V;
     const long long Ed_max = static_cast<long long>(B) * gamma * V;
-    // a block's two target slices (sampled requests', then the others') hold
-    // at most this many rows between them
-    L.MT = static_cast<int>(((L.Et + 2 * G - 1) / G + 2 * L.vec) / V + 6);
-    L.MD = static_cast<int>(((Ed_max + G - 1) / G + L.vec - 1) / V + 2);
+    // the piece of row r in slice i has record r + i (see piece_rec): at most
+    // the rows plus the slices of each stream
+    L.NRT = static_cast<int>(L.Et / V) + (kMaxWaves + 1) * G;
+    L.NRD = static_cast<int>(Ed_max / V) + kMaxWaves * G;
     const int chunk_elems = kChunkBytes / es;
     L.NCH = (V + chunk_elems - 1) / chunk_elems;
     L.NI = (L.NCH + kEeGroup - 1) / kEeGroup;
@@ -161,8 +185,8 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.ee_tasks = take(static_cast<size_t>(L.ee_cap) * 8);  // published tasks: code (low word), scale c
     L.ee_done = take(static_cast<size_t>(L.ee_cap) * 4);   // chunks done, per task
     L.clear_bytes = off;  // cleared before every launch (up to ee_tasks without early exit)
-    L.rec_t = take(static_cast<size_t>(G) * L.MT * sizeof(Rec));
-    L.rec_d = take(static_cast<size_t>(G) * L.MD * sizeof(Rec));
+    L.rec_t = take(static_cast<size_t>(L.NRT) * sizeof(Rec));
+    L.rec_d = take(static_cast<size_t>(L.NRD) * sizeof(Rec));
     L.ee_rec = take(static_cast<size_t>(L.ee_cap) * L.NI * 2 * sizeof(Rec));  // per (task, item): target, draft
     L.jobs = take(static_cast<size_t>(B) * sizeof(Job));
     L.jobset = take(static_cast<size_t>(B) * gamma * 4);  // tree jobs: tokens excluded from the last draw
@@ -338,16 +362,20 @@ __device__ __forceinline__ void stamp(unsigned long long* slots, int i, bool who
 struct Ctl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    long long tbeg[kMaxGrid + 1];   // partition of the sampled requests' target rows (virtual elements 0..E1)
-    long long t3beg[kMaxGrid + 1];  // ... of the other requests' target rows (virtual elements E1..Et)
-    long long dbeg[kMaxGrid + 1];  // draft partition (after the prologue)
+    // the three streams (after the prologue): the sampled requests' target
+    // rows (virtual elements 0..E1), their draft rows, the others' target rows
+    // (virtual elements E1..Et, sliced from 0)
+    Slicing sl[3];
+    int nwave;                     // W: waves of the first two streams (slices W G each)
     StageDesc desc[kStages];       // draw phase: the item in each stage
     int n_samp;
-    int k_lo;  // first compacted request of this block's draft slice
-    int k1_lo;  // first compacted request of this block's sampled-target slice
     int j3_lo;  // first other request (by its index among them) of this block's other-target slice
     int abort;
-    int map[kMapMax];
+    // this block's slices of the first two streams, wave by wave: the first
+    // compacted request (lo) and the place of its entry in the map (off)
+    int wlo[2][kMaxWaves];
+    int woff[2][kMaxWaves + 1];
+    short wmap[2][kMapMax];  // request b of each compacted index those slices hold
     int wtmp[kConsumerWarps + 1];
     Rec wrec[kFlushSlots][kConsumerWarps];  // per-warp partials of a row piece
     Rec wrec2[kFlushSlots][kConsumerWarps]; // early exit: per-warp partials of the draft row
@@ -360,7 +388,6 @@ struct Ctl {
     int cons_done;                          // consumer warps done with both phases
     short kmap[kMaxB];                      // compacted index k of each T > 0 request, else -(j + 1),
                                             // j its index among the others
-    short map1[kMapMax];                    // sampled-target slice: request of compacted index k1_lo + i
     short map3[kMapMax];                    // other-target slice: request of other index j3_lo + i
     int dset[kStages][SV_MAX_GAMMA];        // tree draws: the excluded tokens of the item in each stage
     int fset[SV_MAX_GAMMA];                 // tree draws: the excluded tokens of the job being searched
@@ -383,18 +410,6 @@ struct Segment {
     bool last;     // the last piece of this request's rows in the slice
 };
 
-// Largest g with beg[g] <= e (beg non-decreasing, beg[0] = 0 <= e < beg[G]).
-__device__ __forceinline__ int owner(const long long* beg, int G, long long e) {
-    int lo = 0, hi = G - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (beg[mid] <= e)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
 
 template <int DT>
 struct Kern {
@@ -435,24 +450,25 @@ struct Kern {
     // Target rows are streamed in a virtual order: the T > 0 requests' rows
     // (request of compacted index k at virtual rows k (gamma+1) ...), then the
     // other requests' (index j among them, after all n_samp of the former).
-    // A block streams its slice of the first, its draft slice, and its slice
-    // of the second last, so that the requests that need a draw are complete
-    // (scanned, their jobs published) while the rows of those that need none
-    // still stream.
+    // Wave by wave, a block streams its slice of the first and its slice of
+    // the T > 0 requests' draft rows; then its slice of the others' rows, so
+    // that the requests that need a draw are complete (scanned, their jobs
+    // published) while the rows of those that need none still stream. The
+    // piece of row r in slice i of a stream has record r + i (slices of the
+    // others' rows count after the first stream's W G).
 
-    // Rows of block gg's slice of the T > 0 requests' target rows: its slice
-    // of the others' rows has its records after them.
-    __device__ int t1_rows(int gg) const {
-        const long long b0 = ctl.tbeg[gg], b1 = ctl.tbeg[gg + 1];
-        return b1 > b0 ? static_cast<int>((b1 - 1) / a.V - b0 / a.V + 1) : 0;
+    // Request b of compacted index k in this block's slices of stream st
+    // (0 target, 1 draft) of wave w; -1 if it is not there.
+    __device__ int wave_req(int st, int w, long long k) const {
+        const long long rel = k - ctl.wlo[st][w];
+        return (rel >= 0 && rel < ctl.woff[st][w + 1] - ctl.woff[st][w]) ? ctl.wmap[st][ctl.woff[st][w] + rel] : -1;
     }
 
-    // Virtual target elements [vs, ve) of one slice; slot0 is the record slot
-    // of its first row.
+    // Virtual target elements [vs, ve) of slice `is` (wave w of the first
+    // stream; w < 0: the others' rows).
     template <typename F>
-    __device__ void for_each_target_segment(long long vs, long long ve, int slot0, F&& f) const {
+    __device__ void for_each_target_segment(long long vs, long long ve, int is, int w, F& f) const {
         const int V = a.V, GM = a.gamma, ns = ctl.n_samp;
-        const long long first = vs / V;
         for (long long e = vs; e < ve;) {
             const long long vr = e / V;
             const long long end = min(ve, (vr + 1) * V);
@@ -460,14 +476,13 @@ struct Kern {
             const int i = static_cast<int>(vr - pos * (GM + 1));
             int b = -1;
             if (pos < ns) {
-                const long long rel = pos - ctl.k1_lo;
-                if (rel >= 0 && rel < kMapMax) b = ctl.map1[rel];
+                if (w >= 0) b = wave_req(0, w, pos);
             } else {
                 const long long rel = pos - ns - ctl.j3_lo;
                 if (rel >= 0 && rel < kMapMax) b = ctl.map3[rel];
             }
-            const int slot = slot0 + static_cast<int>(vr - first);
-            if (b < 0 || b >= a.B || slot >= L.MT) {  // cannot happen when the host checks hold
+            const long long slot = vr + is;
+            if (b < 0 || b >= a.B || slot >= L.NRT) {  // cannot happen when the host checks hold
                 ctl.abort = 1;
                 return;
             }
@@ -476,25 +491,24 @@ struct Kern {
             sg.src = static_cast<const char*>(a.target) + (row * V + (e - vr * V)) * ES;
             sg.elems = end - e;
             sg.e0 = e - vr * V;
-            sg.loc = {0, vr, b, slot};
+            sg.loc = {0, vr, b, static_cast<int>(slot)};
             sg.last = end == ve || (vr + 1) % (GM + 1) == 0;
             f(sg);
             e = end;
         }
     }
 
+    // Compacted draft elements [ds, de) of slice `is` (wave w).
     template <typename F>
-    __device__ void for_each_draft_segment(F&& f) const {
+    __device__ void for_each_draft_segment(long long ds, long long de, int is, int w, F& f) const {
         const int V = a.V, GM = a.gamma;
-        const long long ds = ctl.dbeg[g], de = ctl.dbeg[g + 1];
-        const long long first = ds / V;
         for (long long e = ds; e < de;) {
             const long long kr = e / V;
             const long long end = min(de, (kr + 1) * V);
             const int k = static_cast<int>(kr / GM), i = static_cast<int>(kr % GM);
-            const int rel = k - ctl.k_lo;
-            const int b = (rel >= 0 && rel < kMapMax) ? ctl.map[rel] : -1;
-            if (b < 0 || b >= a.B) {  // cannot happen when the host checks hold
+            const int b = wave_req(1, w, k);
+            const long long slot = kr + is;
+            if (b < 0 || b >= a.B || slot >= L.NRD) {  // cannot happen when the host checks hold
                 ctl.abort = 1;
                 return;
             }
@@ -503,11 +517,24 @@ struct Kern {
             sg.src = static_cast<const char*>(a.draft) + (base + (e - kr * V)) * ES;
             sg.elems = end - e;
             sg.e0 = e - kr * V;
-            sg.loc = {1, kr, b, static_cast<int>(kr - first)};
+            sg.loc = {1, kr, b, static_cast<int>(slot)};
             sg.last = end == de || (kr + 1) % GM == 0;
             f(sg);
             e = end;
         }
+    }
+
+    // Every row piece of this block, in streaming order.
+    template <typename F>
+    __device__ void for_each_segment(F&& f) const {
+        const int W = ctl.nwave;
+        for (int w = 0; w < W; ++w) {
+            const int is = w * G + g;
+            for_each_target_segment(slice_begin(ctl.sl[0], is), slice_begin(ctl.sl[0], is + 1), is, w, f);
+            for_each_draft_segment(slice_begin(ctl.sl[1], is), slice_begin(ctl.sl[1], is + 1), is, w, f);
+        }
+        const long long E1 = ctl.sl[0].E;
+        for_each_target_segment(E1 + slice_begin(ctl.sl[2], g), E1 + slice_begin(ctl.sl[2], g + 1), W * G + g, -1, f);
     }
 
     // ---- the ring: producer and consumer cursors
@@ -747,26 +774,44 @@ struct Kern {
         bar_sync(kBarConsumers, kConsumers);
         int n = 0;
         for (int w = 0; w < kConsumerWarps; ++w) n += ctl.wtmp[w];
-        // draft rows of the T > 0 requests (none for one-hot proposals)
-        const long long E2 = a.onehot ? 0ll : static_cast<long long>(n) * a.gamma * a.V;
-        for (int gg = t; gg <= G; gg += kConsumers) ctl.dbeg[gg] = part_begin(E2, G, gg, L.vec);
-        const int k_lo = n > 0 ? static_cast<int>(part_begin(E2, G, g, L.vec) /
-                                                  (static_cast<long long>(a.gamma) * a.V))
-                               : 0;
-        // target rows in request order within each group: T > 0 requests first
+        // the streams: the T > 0 requests' target rows (E1) and draft rows (E2,
+        // none for one-hot proposals) in W waves, the others' target rows (E3)
         const long long R = static_cast<long long>(a.gamma + 1) * a.V;
+        const long long D = static_cast<long long>(a.gamma) * a.V;
         const long long E1 = static_cast<long long>(n) * R, E3 = static_cast<long long>(a.B - n) * R;
-        for (int gg = t; gg <= G; gg += kConsumers) {
-            ctl.tbeg[gg] = part_begin(E1, G, gg, L.vec);
-            ctl.t3beg[gg] = E1 + part_begin(E3, G, gg, L.vec);
-        }
-        const int k1_lo = static_cast<int>(part_begin(E1, G, g, L.vec) / R);
-        const int j3_lo = static_cast<int>(part_begin(E3, G, g, L.vec) / R);
+        const long long E2 = a.onehot ? 0ll : static_cast<long long>(n) * D;
+        // waves: a block's target slice of one wave holds kWaveSliceBytes or
+        // more, and its slices of all waves fit the maps (each slice holds at
+        // most (S - 1) / R + 2 requests, so W waves at most n / G + 3 W)
+        int W = static_cast<int>(min(static_cast<long long>(kMaxWaves),
+                                     max(1ll, E1 * ES / (static_cast<long long>(G) * kWaveSliceBytes))));
+        while (W > 1 && (n + G - 1) / G + 3 * W + 1 > kMapMax) --W;
+        const Slicing s1 = make_slicing(E1, W * G, L.vec), s2 = make_slicing(E2, W * G, L.vec);
+        const Slicing s3 = make_slicing(E3, G, L.vec);
+        const int j3_lo = static_cast<int>(slice_begin(s3, g) / R);
         if (t == 0) {
             ctl.n_samp = n;
-            ctl.k_lo = k_lo;
-            ctl.k1_lo = k1_lo;
+            ctl.nwave = W;
+            ctl.sl[0] = s1;
+            ctl.sl[1] = s2;
+            ctl.sl[2] = s3;
             ctl.j3_lo = j3_lo;
+            // the compacted requests of this block's slices, wave by wave
+            for (int st = 0; st < 2; ++st) {
+                const Slicing& sl = st == 0 ? s1 : s2;
+                const long long per = st == 0 ? R : D;
+                int off = 0;
+                for (int w = 0; w < W; ++w) {
+                    const long long b0 = slice_begin(sl, static_cast<long long>(w) * G + g);
+                    const long long b1 = slice_begin(sl, static_cast<long long>(w) * G + g + 1);
+                    const int lo = b1 > b0 ? static_cast<int>(b0 / per) : 0;
+                    const int cnt = b1 > b0 ? static_cast<int>((b1 - 1) / per) - lo + 1 : 0;
+                    ctl.wlo[st][w] = lo;
+                    ctl.woff[st][w] = off;
+                    off = min(off + cnt, kMapMax);
+                }
+                ctl.woff[st][W] = off;
+            }
         }
         bar_sync(kBarConsumers, kConsumers);
         int carry = 0;
@@ -785,10 +830,12 @@ struct Kern {
             const int k = before + in_warp;  // T > 0 requests before b
             if (b < a.B) {
                 if (f) {
-                    const int rel = k - k_lo;
-                    if (rel >= 0 && rel < kMapMax) ctl.map[rel] = b;
-                    const int rel1 = k - k1_lo;
-                    if (rel1 >= 0 && rel1 < kMapMax) ctl.map1[rel1] = static_cast<short>(b);
+                    for (int st = 0; st < 2; ++st)
+                        for (int w = 0; w < W; ++w) {
+                            const int rel = k - ctl.wlo[st][w];
+                            if (rel >= 0 && rel < ctl.woff[st][w + 1] - ctl.woff[st][w])
+                                ctl.wmap[st][ctl.woff[st][w] + rel] = static_cast<short>(b);
+                        }
                     ctl.kmap[b] = static_cast<short>(k);
                 } else {
                     const int j = b - k;  // the others before b
@@ -802,10 +849,9 @@ struct Kern {
                 // slice holds the first element of the request's target rows
                 // clears it here, before it posts any share (the scan comes after
                 // every share).
-                const long long first = f ? static_cast<long long>(k) * R : E1 + static_cast<long long>(b - k) * R;
-                const long long lo = f ? part_begin(E1, G, g, L.vec) : E1 + part_begin(E3, G, g, L.vec);
-                const long long hi = f ? part_begin(E1, G, g + 1, L.vec) : E1 + part_begin(E3, G, g + 1, L.vec);
-                if (first >= lo && first < hi) a.out_num_accepted[b] = -1;
+                const int first_slice = f ? slice_of(s1, static_cast<long long>(k) * R)
+                                          : slice_of(s3, static_cast<long long>(b - k) * R);
+                if (first_slice % G == g) a.out_num_accepted[b] = -1;
             }
             carry += total;
             bar_sync(kBarConsumers, kConsumers);
@@ -835,11 +881,21 @@ struct Kern {
 
     // The warps of a block fold disjoint parts of each row piece. Each warp
     // reduces its lanes, parks the result in shared slot `seq % kFlushSlots`,
-    // and the last warp to arrive merges the 8 partials in warp order and
-    // writes the block's record for the piece (no block-wide barrier).
-    // When `share` is non-zero this piece ends the request's rows in the slice:
-    // the merging warp then posts the request with the share's element count.
+    // and the last warp to arrive merges the 12 partials (lane w holding warp
+    // w's) and writes the block's record for the piece (no block-wide
+    // barrier). A max/sum reduction takes the max first and then sums each
+    // part rescaled to it, so that the dependent chain holds one 2^x, not one
+    // a level. When `share` is non-zero this piece ends the request's rows in
+    // the slice: the merging warp then posts the request with the share's
+    // element count.
+    __device__ static float rescaled_sum(float m, float s, float M, float c) {
+        float t = m == neg_inf() ? 0.0f : __fmul_rn(s, ex2(__fsub_rn(scaled_max(m, c), scaled_max(M, c))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
+        return t;
+    }
     __device__ void flush_row(const RowState& rs, const RowLoc& loc, unsigned seq, unsigned share) const {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const int bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(rs.bad)));
         Rec rec;
         if (rs.argmax) {
@@ -851,41 +907,42 @@ struct Kern {
             }
             rec = {st.v, 0.0f, st.i, bad};
         } else {
-            MaxSumA st{rs.m, rs.s};
+            float m = rs.m;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                MaxSumA ot{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
-                st = maxsum_merge_a(st, ot, rs.c);
-            }
-            rec = {st.m, st.s, -1, bad};
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            rec = {m, rescaled_sum(rs.m, rs.s, m, rs.c), -1, bad};
         }
-        if ((threadIdx.x & 31) == 0) {
-            const int warp = threadIdx.x >> 5;
-            const int fs = static_cast<int>(seq % kFlushSlots);
+        const int fs = static_cast<int>(seq % kFlushSlots);
+        int last = 0;
+        if (lane == 0) {
             ctl.wrec[fs][warp] = rec;
             __threadfence_block();
-            if (atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1) {
-                __threadfence_block();
-                Rec out = ctl.wrec[fs][0];
-                for (int w = 1; w < kConsumerWarps; ++w) {
-                    const Rec x = ctl.wrec[fs][w];
-                    out.bad |= x.bad;
-                    if (rs.argmax) {
-                        const ArgMax m = argmax_merge(ArgMax{out.m, out.idx}, ArgMax{x.m, x.idx});
-                        out.m = m.v;
-                        out.idx = m.i;
-                    } else {
-                        const MaxSumA m = maxsum_merge_a(MaxSumA{out.m, out.s}, MaxSumA{x.m, x.s}, rs.c);
-                        out.m = m.m;
-                        out.s = m.s;
-                    }
-                }
-                ctl.wcnt[fs] = 0;
-                Rec* dst = loc.kind == 0 ? rec_t() + (static_cast<size_t>(g) * L.MT + loc.slot)
-                                         : rec_d() + (static_cast<size_t>(g) * L.MD + loc.slot);
-                *dst = out;
-                if (share && !post(loc.req, share)) set_abort(a.d_status);
+            last = atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1;
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) return;
+        __threadfence_block();
+        const Rec x = lane < kConsumerWarps ? ctl.wrec[fs][lane] : Rec{neg_inf(), 0.0f, 0x7fffffff, 0};
+        const int bad_all = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(x.bad)));
+        Rec out;
+        if (rs.argmax) {
+            ArgMax st{x.m, x.idx};
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                ArgMax ot{__shfl_xor_sync(0xffffffffu, st.v, o), __shfl_xor_sync(0xffffffffu, st.i, o)};
+                st = argmax_merge(st, ot);
             }
+            out = {st.v, 0.0f, st.i, bad_all};
+        } else {
+            float m = x.m;
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            out = {m, rescaled_sum(x.m, x.s, m, rs.c), -1, bad_all};
+        }
+        if (lane == 0) {
+            ctl.wcnt[fs] = 0;
+            Rec* dst = (loc.kind == 0 ? rec_t() : rec_d()) + loc.slot;
+            *dst = out;
+            if (share && !post(loc.req, share)) set_abort(a.d_status);
         }
     }
 
@@ -995,42 +1052,30 @@ struct Kern {
         rs.s = __fadd_rn(rs.s, __fadd_rn(a0, a1));
     }
 
-    // ---- acceptance scan: merge of a row's pieces, in block and warp order.
-    // The records of a row's first two pieces are read first (row_load) and
-    // merged once the request's temperature is known (row_combine); a row
-    // over more slices reads the rest then.
+    // ---- acceptance scan: merge of a row's pieces, in slice and warp order.
+    // The records of a row's first kPrePieces pieces are read first
+    // (row_load) and merged once the request's temperature is known
+    // (row_combine); a row over more slices reads the rest then.
     // Row kinds: 0 a target row of a T > 0 request, 2 a target row of another
     // request (`row` virtual in both), 1 a draft row (compacted).
     struct RowRaw {
-        uint4 x[2];
-        int g0, g1;
+        uint4 x[kPrePieces];
+        int i0, i1;  // the row's first and last slice
     };
-    __device__ const long long* row_part(int kind) const {
-        return kind == 1 ? ctl.dbeg : kind == 2 ? ctl.t3beg : ctl.tbeg;
-    }
-    // The record of `row`'s piece in block gg (whose slice starts at b0).
-    __device__ const uint4* piece_rec(int kind, int gg, long long b0, long long row) const {
-        if (kind == 1)
-            return reinterpret_cast<const uint4*>(rec_d() + static_cast<size_t>(gg) * L.MD +
-                                                  static_cast<int>(row - b0 / a.V));
-        const int slot0 = kind == 2 ? t1_rows(gg) : 0;
-        return reinterpret_cast<const uint4*>(rec_t() + static_cast<size_t>(gg) * L.MT + slot0 +
-                                              static_cast<int>(row - b0 / a.V));
+    __device__ const Slicing& row_slicing(int kind) const { return ctl.sl[kind == 1 ? 1 : kind == 2 ? 2 : 0]; }
+    // The record of `row`'s piece in slice i.
+    __device__ const uint4* piece_rec(int kind, int i, long long row) const {
+        const Rec* base = kind == 1 ? rec_d() : rec_t() + (kind == 2 ? ctl.nwave * G : 0);
+        return reinterpret_cast<const uint4*>(base + row + i);
     }
     __device__ void row_load(int kind, long long row, RowRaw& rr) const {
-        const long long* beg = row_part(kind);
-        const long long e0 = row * a.V, e1 = e0 + a.V - 1;
-        rr.g0 = owner(beg, G, e0);
-        rr.g1 = owner(beg, G, e1);
+        const Slicing& sl = row_slicing(kind);
+        const long long e0 = row * a.V - (kind == 2 ? ctl.sl[0].E : 0ll);
+        rr.i0 = slice_of(sl, e0);
+        rr.i1 = slice_of(sl, e0 + a.V - 1);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int gg = rr.g0 + q;
-            rr.x[q] = make_uint4(0u, 0u, 0u, kNoPiece);
-            if (gg <= rr.g1) {
-                const long long b0 = beg[gg], b1 = beg[gg + 1];
-                if (b1 > b0) rr.x[q] = __ldcg(piece_rec(kind, gg, b0, row));
-            }
-        }
+        for (int q = 0; q < kPrePieces; ++q)
+            rr.x[q] = rr.i0 + q <= rr.i1 ? __ldcg(piece_rec(kind, rr.i0 + q, row)) : make_uint4(0u, 0u, 0u, kNoPiece);
     }
     __device__ Rec row_combine(int kind, long long row, const RowRaw& rr, bool argmax, float c) const {
         MaxSumA ms{neg_inf(), 0.0f};
@@ -1045,15 +1090,9 @@ struct Kern {
             else
                 ms = maxsum_merge_a(ms, MaxSumA{m, s}, c);
         };
-        take(rr.x[0]);
-        take(rr.x[1]);
-        if (rr.g1 > rr.g0 + 1) {
-            const long long* beg = row_part(kind);
-            for (int gg = rr.g0 + 2; gg <= rr.g1; ++gg) {
-                const long long b0 = beg[gg], b1 = beg[gg + 1];
-                if (b1 > b0) take(__ldcg(piece_rec(kind, gg, b0, row)));
-            }
-        }
+#pragma unroll
+        for (int q = 0; q < kPrePieces; ++q) take(rr.x[q]);
+        for (int i = rr.i0 + kPrePieces; i <= rr.i1; ++i) take(__ldcg(piece_rec(kind, i, row)));
         Rec out;
         if (argmax)
             out = {am.v, 0.0f, am.i == 0x7fffffff ? 0 : am.i, (bad || am.v == neg_inf()) ? kBadData : 0};
@@ -1079,10 +1118,11 @@ struct Kern {
         const bool onehot = a.onehot;
         // The reads come in two rounds. First everything that depends on no
         // other read: the temperature, the proposal count, this lane's token
-        // and uniform, and the first two piece records of rows `lane` and
-        // `lane + 32` (rows numbered target 0..gamma, then draft
-        // gamma+1..2 gamma). Then the logits at this lane's token, which need
-        // only the token (read even when the request turns out greedy).
+        // and uniform, and the first piece records of row `lane` (rows
+        // numbered target 0..gamma, then draft gamma+1..2 gamma; rows from 32
+        // on are read in the second round). Then the logits at this lane's
+        // token, which need only the token (read even when the request turns
+        // out greedy).
         const float T = a.temperature[b];
         // proposals of this request: gamma, or num_draft[b] for one-hot proposals
         // (whose rows past it take no part)
@@ -1094,9 +1134,8 @@ struct Kern {
             return r <= GM ? static_cast<long long>(vpos) * (GM + 1) + r : static_cast<long long>(k) * GM + (r - GM - 1);
         };
         auto kind_of = [&](int r) { return r <= GM ? tkind : 1; };
-        RowRaw raw0, raw1;
+        RowRaw raw0;
         if (lane < nrows_max) row_load(kind_of(lane), row_of(lane), raw0);
-        if (lane + 32 < nrows_max) row_load(kind_of(lane + 32), row_of(lane + 32), raw1);
         float lt_l = 0.0f, ld_l = 0.0f;
         if (!a.tree && x_l >= 0 && x_l < V) {
             lt_l = load_logit<DT>(a.target, (static_cast<size_t>(b) * (GM + 1) + lane) * V + x_l);
@@ -1126,8 +1165,6 @@ struct Kern {
             Rec x;
             if (r == lane)
                 x = row_combine(kind, row_of(r), raw0, am, c);
-            else if (r == lane + 32)
-                x = row_combine(kind, row_of(r), raw1, am, c);
             else
                 x = merge_row(kind, row_of(r), am, c);
             st[r] = x;
@@ -2546,7 +2583,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         ctl.cons_done = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int i = t; i < kMapMax; i += kThreads) ctl.map[i] = -1;
+    for (int i = t; i < kMapMax; i += kThreads) {
+        ctl.wmap[0][i] = -1;
+        ctl.wmap[1][i] = -1;
+        ctl.map3[i] = -1;
+    }
     for (int i = t; i < kFlushSlots; i += kThreads) ctl.wcnt[i] = 0;
     for (int i = t; i < kQueue; i += kThreads) ctl.fq_seq[i] = 0;
     __syncthreads();
@@ -2630,9 +2671,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             }
         };
         bar_sync(kBarHandoff, kHandoffThreads);  // the consumers' prologue (partitions, maps) is done
-        K.for_each_target_segment(ctl.tbeg[K.g], ctl.tbeg[K.g + 1], 0, issue);
-        K.for_each_draft_segment(issue);
-        K.for_each_target_segment(ctl.t3beg[K.g], ctl.t3beg[K.g + 1], K.t1_rows(K.g), issue);
+        K.for_each_segment(issue);
         const int ns = ctl.n_samp;
         if (ns > 0) {
             // draw items i = 0 .. ns * NCH - 1: chunk i % NCH of the job published
@@ -2772,9 +2811,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
         K.flush_row(rs, sg.loc, seq++, sg.last ? share : 0u);
         if (sg.last) share = 0;
     };
-    K.for_each_target_segment(ctl.tbeg[K.g], ctl.tbeg[K.g + 1], 0, fold);
-    K.for_each_draft_segment(fold);
-    K.for_each_target_segment(ctl.t3beg[K.g], ctl.t3beg[K.g + 1], K.t1_rows(K.g), fold);
+    K.for_each_segment(fold);
     stamp(ph, 2, lane == 0);
 
     if (ctl.n_samp > 0 && ok) {
@@ -2937,7 +2974,7 @@ bool streaming_applicable(const Args& a) {
 
 int streaming_default_grid(const DeviceInfo& dev) { return std::min(dev.num_sms, kMaxGrid); }
 
-bool streaming_grid_ok(int B, int grid) { return grid <= kMaxGrid && (B + grid - 1) / grid + 3 <= kMapMax; }
+bool streaming_grid_ok(int B, int grid) { return grid <= kMaxGrid && (B + grid - 1) / grid + 4 <= kMapMax; }
 
 size_t streaming_workspace_bytes(int B, int gamma, int V, int dtype, int grid) {
     return make_layout(B, gamma, V, dtype == SV_F32 ? 4 : 2, grid).total;
