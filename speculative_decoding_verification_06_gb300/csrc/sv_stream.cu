@@ -879,39 +879,43 @@ struct Kern {
         rs.bad = 0;
     }
 
-    // The warps of a block fold disjoint parts of each row piece. Each warp
-    // reduces its lanes, parks the result in shared slot `seq % kFlushSlots`,
-    // and the last warp to arrive merges the 12 partials (lane w holding warp
-    // w's) and writes the block's record for the piece (no block-wide
-    // barrier). A max/sum reduction takes the max first and then sums each
-    // part rescaled to it, so that the dependent chain holds one 2^x, not one
-    // a level. When `share` is non-zero this piece ends the request's rows in
-    // the slice: the merging warp then posts the request with the share's
-    // element count.
-    __device__ static float rescaled_sum(float m, float s, float M, float c) {
-        float t = m == neg_inf() ? 0.0f : __fmul_rn(s, ex2(__fsub_rn(scaled_max(m, c), scaled_max(M, c))));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
-        return t;
-    }
-    __device__ void flush_row(const RowState& rs, const RowLoc& loc, unsigned seq, unsigned share) const {
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        const int bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(rs.bad)));
-        Rec rec;
-        if (rs.argmax) {
-            ArgMax st{rs.m, rs.idx};
+    // The records of a warp's lanes merged (every lane gets the result): the
+    // lowest-index argmax, or for (max, sum) the max first and then each
+    // lane's sum rescaled to it and added up in a butterfly, so that the
+    // dependent chain holds one 2^x rather than one a level. Lanes with
+    // nothing to add hold (-inf, 0).
+    __device__ static Rec rec_reduce(Rec x, bool argmax, float c) {
+        const int bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(x.bad)));
+        if (argmax) {
+            ArgMax st{x.m, x.idx};
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 ArgMax ot{__shfl_xor_sync(0xffffffffu, st.v, o), __shfl_xor_sync(0xffffffffu, st.i, o)};
                 st = argmax_merge(st, ot);
             }
-            rec = {st.v, 0.0f, st.i, bad};
-        } else {
-            float m = rs.m;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            rec = {m, rescaled_sum(rs.m, rs.s, m, rs.c), -1, bad};
+            return Rec{st.v, 0.0f, st.i, bad};
         }
+        float m = x.m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float t = x.m == neg_inf() ? 0.0f : __fmul_rn(x.s, ex2(__fsub_rn(scaled_max(x.m, c), scaled_max(m, c))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
+        return Rec{m, t, -1, bad};
+    }
+    __device__ static Rec lane_rec(const RowState& rs) { return Rec{rs.m, rs.s, rs.idx, rs.bad}; }
+    __device__ static Rec no_rec() { return Rec{neg_inf(), 0.0f, 0x7fffffff, 0}; }
+
+    // The warps of a block fold disjoint parts of each row piece. Each warp
+    // reduces its lanes, parks the result in shared slot `seq % kFlushSlots`,
+    // and the last warp to arrive merges the 12 partials (lane w holding warp
+    // w's) and writes the block's record for the piece (no block-wide
+    // barrier). When `share` is non-zero this piece ends the request's rows in
+    // the slice: the merging warp then posts the request with the share's
+    // element count.
+    __device__ void flush_row(const RowState& rs, const RowLoc& loc, unsigned seq, unsigned share) const {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const Rec rec = rec_reduce(lane_rec(rs), rs.argmax, rs.c);
         const int fs = static_cast<int>(seq % kFlushSlots);
         int last = 0;
         if (lane == 0) {
@@ -921,23 +925,7 @@ struct Kern {
         }
         if (!__shfl_sync(0xffffffffu, last, 0)) return;
         __threadfence_block();
-        const Rec x = lane < kConsumerWarps ? ctl.wrec[fs][lane] : Rec{neg_inf(), 0.0f, 0x7fffffff, 0};
-        const int bad_all = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(x.bad)));
-        Rec out;
-        if (rs.argmax) {
-            ArgMax st{x.m, x.idx};
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
-                ArgMax ot{__shfl_xor_sync(0xffffffffu, st.v, o), __shfl_xor_sync(0xffffffffu, st.i, o)};
-                st = argmax_merge(st, ot);
-            }
-            out = {st.v, 0.0f, st.i, bad_all};
-        } else {
-            float m = x.m;
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            out = {m, rescaled_sum(x.m, x.s, m, rs.c), -1, bad_all};
-        }
+        const Rec out = rec_reduce(lane < kConsumerWarps ? ctl.wrec[fs][lane] : no_rec(), rs.argmax, rs.c);
         if (lane == 0) {
             ctl.wcnt[fs] = 0;
             Rec* dst = (loc.kind == 0 ? rec_t() : rec_d()) + loc.slot;
@@ -2003,25 +1991,7 @@ struct Kern {
     }
 
     // The lanes of a warp reduced to one record (every lane holds it).
-    __device__ static Rec warp_rec(const RowState& rs) {
-        const int bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(rs.bad)));
-        if (rs.argmax) {
-            ArgMax st{rs.m, rs.idx};
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                ArgMax ot{__shfl_xor_sync(0xffffffffu, st.v, o), __shfl_xor_sync(0xffffffffu, st.i, o)};
-                st = argmax_merge(st, ot);
-            }
-            return Rec{st.v, 0.0f, st.i, bad};
-        }
-        MaxSumA st{rs.m, rs.s};
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            MaxSumA ot{__shfl_xor_sync(0xffffffffu, st.m, o), __shfl_xor_sync(0xffffffffu, st.s, o)};
-            st = maxsum_merge_a(st, ot, rs.c);
-        }
-        return Rec{st.m, st.s, -1, bad};
-    }
+    __device__ static Rec warp_rec(const RowState& rs) { return rec_reduce(lane_rec(rs), rs.argmax, rs.c); }
 
     __device__ static Rec rec_merge(Rec x, const Rec& y, bool argmax, float c) {
         x.bad |= y.bad;
@@ -2038,32 +2008,33 @@ struct Kern {
     }
 
     // End of a statistics item (group grp of task p, nch chunks): each warp
-    // parks its records; the last warp merges the twelve in warp order, writes
-    // the item's records and posts its chunks to the finisher.
+    // parks its records; the last warp merges the twelve (lane w holding warp
+    // w's), writes the item's records and posts its chunks to the finisher.
     __device__ void ee_flush_item(const RowState& rt, const RowState& rd, bool has_draft, unsigned seq, int p,
                                   int grp, unsigned nch) const {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         const Rec t = warp_rec(rt);
         Rec d = t;
         if (has_draft) d = warp_rec(rd);
-        if ((threadIdx.x & 31) == 0) {
-            const int warp = threadIdx.x >> 5;
-            const int fs = static_cast<int>(seq % kFlushSlots);
+        const int fs = static_cast<int>(seq % kFlushSlots);
+        int last = 0;
+        if (lane == 0) {
             ctl.wrec[fs][warp] = t;
             ctl.wrec2[fs][warp] = d;
             __threadfence_block();
-            if (atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1) {
-                __threadfence_block();
-                Rec ot = ctl.wrec[fs][0], od = ctl.wrec2[fs][0];
-                for (int w = 1; w < kConsumerWarps; ++w) {
-                    ot = rec_merge(ot, ctl.wrec[fs][w], rt.argmax, rt.c);
-                    if (has_draft) od = rec_merge(od, ctl.wrec2[fs][w], false, rd.c);
-                }
-                ctl.wcnt[fs] = 0;
-                Rec* dst = ee_rec() + (static_cast<size_t>(p) * L.NI + grp) * 2;
-                dst[0] = ot;
-                dst[1] = od;
-                if (!post(p | kJobMsg, nch)) set_abort(a.d_status);
-            }
+            last = atomicAdd(&ctl.wcnt[fs], 1) == kConsumerWarps - 1;
+        }
+        if (!__shfl_sync(0xffffffffu, last, 0)) return;
+        __threadfence_block();
+        const Rec ot = rec_reduce(lane < kConsumerWarps ? ctl.wrec[fs][lane] : no_rec(), rt.argmax, rt.c);
+        Rec od = ot;
+        if (has_draft) od = rec_reduce(lane < kConsumerWarps ? ctl.wrec2[fs][lane] : no_rec(), false, rd.c);
+        if (lane == 0) {
+            ctl.wcnt[fs] = 0;
+            Rec* dst = ee_rec() + (static_cast<size_t>(p) * L.NI + grp) * 2;
+            dst[0] = ot;
+            dst[1] = od;
+            if (!post(p | kJobMsg, nch)) set_abort(a.d_status);
         }
     }
 
