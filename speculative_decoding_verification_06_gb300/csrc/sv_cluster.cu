@@ -4,10 +4,10 @@
 // kernel (a few requests, or short rows), every row of a request is cut into
 // C equal 16-byte-aligned slices, one per CTA of the request's cluster
 // (C <= 16). Each CTA folds its slice of every row the request needs into a
-// (max, sum) or argmax record in its own shared memory; the cluster leader
-// (rank 0) merges the C records of each row over distributed shared memory
-// (mapa + ld.shared::cluster), in rank order, and runs the acceptance scan on
-// one warp. A draw is made by the whole cluster: each CTA sums the weights of
+// (max, sum) or argmax record and pushes it into the leader's (rank 0's)
+// shared memory over distributed shared memory (mapa + st.shared::cluster);
+// after a cluster barrier the leader merges the C records of each row in rank
+// order and runs the acceptance scan on one warp. A draw is made by the whole cluster: each CTA sums the weights of
 // its slice of the draw row in runs of 32 tokens (fixed point, exact), the
 // leader finds the CTA whose share holds u * W, and that CTA finds the run,
 // then the token. Four cluster barriers separate the phases; nothing goes
