@@ -466,14 +466,17 @@ struct Kern {
 
     // Virtual target elements [vs, ve) of slice `is` (wave w of the first
     // stream; w < 0: the others' rows).
+    // The row, request and position advance by increments from the slice's
+    // first element (one division per slice, none per piece).
     template <typename F>
     __device__ void for_each_target_segment(long long vs, long long ve, int is, int w, F& f) const {
         const int V = a.V, GM = a.gamma, ns = ctl.n_samp;
-        for (long long e = vs; e < ve;) {
-            const long long vr = e / V;
+        if (vs >= ve) return;
+        long long vr = vs / V;
+        long long pos = vr / (GM + 1);
+        int i = static_cast<int>(vr - pos * (GM + 1));
+        for (long long e = vs; e < ve; ++vr) {
             const long long end = min(ve, (vr + 1) * V);
-            const long long pos = vr / (GM + 1);
-            const int i = static_cast<int>(vr - pos * (GM + 1));
             int b = -1;
             if (pos < ns) {
                 if (w >= 0) b = wave_req(0, w, pos);
@@ -492,9 +495,13 @@ struct Kern {
             sg.elems = end - e;
             sg.e0 = e - vr * V;
             sg.loc = {0, vr, b, static_cast<int>(slot)};
-            sg.last = end == ve || (vr + 1) % (GM + 1) == 0;
+            sg.last = end == ve || i == GM;
             f(sg);
             e = end;
+            if (++i > GM) {
+                i = 0;
+                ++pos;
+            }
         }
     }
 
@@ -502,10 +509,11 @@ struct Kern {
     template <typename F>
     __device__ void for_each_draft_segment(long long ds, long long de, int is, int w, F& f) const {
         const int V = a.V, GM = a.gamma;
-        for (long long e = ds; e < de;) {
-            const long long kr = e / V;
+        if (ds >= de) return;
+        long long kr = ds / V;
+        int k = static_cast<int>(kr / GM), i = static_cast<int>(kr - static_cast<long long>(k) * GM);
+        for (long long e = ds; e < de; ++kr) {
             const long long end = min(de, (kr + 1) * V);
-            const int k = static_cast<int>(kr / GM), i = static_cast<int>(kr % GM);
             const int b = wave_req(1, w, k);
             const long long slot = kr + is;
             if (b < 0 || b >= a.B || slot >= L.NRD) {  // cannot happen when the host checks hold
@@ -518,9 +526,13 @@ struct Kern {
             sg.elems = end - e;
             sg.e0 = e - kr * V;
             sg.loc = {1, kr, b, static_cast<int>(slot)};
-            sg.last = end == de || (kr + 1) % GM == 0;
+            sg.last = end == de || i == GM - 1;
             f(sg);
             e = end;
+            if (++i == GM) {
+                i = 0;
+                ++k;
+            }
         }
     }
 
