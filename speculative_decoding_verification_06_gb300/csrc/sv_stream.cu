@@ -880,10 +880,22 @@ struct Kern {
         float c;
     };
 
-    __device__ void start_row(RowState& rs, const RowLoc& loc) const {
-        const float T = a.temperature[loc.req];
-        rs.argmax = loc.kind == 0 && !sampled(T);
-        rs.c = rs.argmax ? 0.0f : temp_scale(T).c;
+    // The request's temperature turned into (sampled, c), kept for the pieces
+    // of the same request that follow (a request's rows are consecutive).
+    struct ReqScale {
+        int req = -1;
+        bool samp = false;
+        float c = 0.0f;
+    };
+    __device__ void start_row(RowState& rs, const RowLoc& loc, ReqScale& rq) const {
+        if (loc.req != rq.req) {
+            const float T = a.temperature[loc.req];
+            rq.req = loc.req;
+            rq.samp = sampled(T);
+            rq.c = rq.samp ? temp_scale(T).c : 0.0f;
+        }
+        rs.argmax = loc.kind == 0 && !rq.samp;
+        rs.c = rs.argmax ? 0.0f : rq.c;
         rs.m = neg_inf();
         rs.mc = neg_inf();
         rs.s = 0.0f;
@@ -2773,10 +2785,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
     bool ok = true;
     unsigned seq = 0;    // row pieces folded so far (the same on every consumer warp)
     unsigned share = 0;  // elements of the current request folded in this slice
+    typename KT::ReqScale rq;
     auto fold = [&](const Segment& sg) {
         if (!ok) return;
         typename KT::RowState rs;
-        K.start_row(rs, sg.loc);
+        K.start_row(rs, sg.loc, rq);
         for (long long off = 0; off < sg.elems; off += KT::kStageElems) {
             const long long n = min(static_cast<long long>(KT::kStageElems), sg.elems - off);
             const char* sm = K.consume_begin(cons);
