@@ -67,10 +67,10 @@ constexpr int kChunkBytes = 24576;  // draw-phase chunk of one row (a residual i
 constexpr int kMapMax = 256;   // requests in one block's slices of one stream (all waves)
 // Waves of the T > 0 requests' streams. More waves let the early requests'
 // scans and draws run while later waves stream, but every wave adds row pieces
-// to each block, and each piece ends with a reduction across the block's
-// warps; the bf16 fold already keeps the SFU (one 2^x a logit) busy most of
-// the time at the copy rate, so on GB300 4 and 16 waves streamed 5% to 60%
-// slower than they saved at the end. One wave.
+// to each block (each ends in a reduction across the block's warps and a
+// partial stage), and a wave's scans fall on the blocks whose pieces finish
+// last; on GB300 4 and 16 waves were slower than one on the sampling, mixed
+// and large batches. One wave (the general slicing passed the GPU tests at 16).
 constexpr int kMaxWaves = 1;
 constexpr long long kWaveSliceBytes = 256 << 10;  // a block's target slice of one wave, at least
 constexpr int kPrePieces = 3;  // row pieces the acceptance scan reads in its first round
