@@ -76,7 +76,8 @@ constexpr long long kWaveSliceBytes = 256 << 10;  // a block's target slice of o
 constexpr int kPrePieces = 3;  // row pieces the acceptance scan reads in its first round
 constexpr int kMaxGrid = 256;  // blocks (partition tables live in shared memory)
 constexpr int kGrab = 4;       // draw items a producer takes per atomic
-constexpr int kEeGroup = 4;    // early exit: chunks of one task taken as one item
+constexpr int kEeItemsPerProducer2 = 11;  // early exit: position-0 items a producer takes, about, times 2
+constexpr int kEeGroupMax = 8;            // early exit: chunks of one task in one item, at most
 constexpr int kJobMsg = 0x40000000;  // finisher message flag: a draw item of job (item & ~flag)
 constexpr int kEndKind = -2;   // stage descriptor kind: no more draw items
 constexpr int kMaxB = 4096;
@@ -115,6 +116,7 @@ struct StageDesc {
     Job job;
     int32_t k, j;
     int32_t type, flags;
+    int32_t item, nch;  // early exit: the chunk's item within its task, chunks of the item up to it
 };
 
 // Early-exit tasks: the row statistics of one position of one request (the
@@ -130,7 +132,8 @@ constexpr int kItemLast = 8;     // StageDesc.flags: the last stage of an early-
 struct Layout {
     long long Et;  // target elements B*(gamma+1)*V
     int G, NRT, NRD, NCH, vec;  // NRT, NRD: row-piece records of the target and draft streams
-    int NI;  // early exit: items per task, groups of kEeGroup chunks
+    int NI;   // early exit: items per task, groups of GRP chunks
+    int GRP;  // early exit: chunks of one task taken as one item
     size_t hdr, req_done, job_done, ready, ee_tasks, ee_done, clear_bytes, rec_t, rec_d, ee_rec, jobs, jobset,
         wsums, total;
     int ee_cap;  // early exit: task slots, B (gamma + 2)
@@ -168,7 +171,18 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.NRD = static_cast<int>(Ed_max / V) + kMaxWaves * G;
     const int chunk_elems = kChunkBytes / es;
     L.NCH = (V + chunk_elems - 1) / chunk_elems;
-    L.NI = (L.NCH + kEeGroup - 1) / kEeGroup;
+    // Early exit: items of GRP chunks. Large items amortise the per-item costs
+    // (the grab, the task lookup, the flush) when the batch keeps every
+    // producer busy; small ones spread a task over more blocks, which
+    // shortens the chain of a request that keeps accepting. GRP is chosen so
+    // that the position-0 tasks (B of them) make about 5.5 items a producer
+    // (same-box sweeps: 2 chunks best for B = 64 fp32 rows of 128256, 3 for
+    // 256 bf16 rows of 128256, 6 to 8 for 512 bf16 rows of 152064).
+    {
+        const long long x = 2LL * B * L.NCH, d = static_cast<long long>(kEeItemsPerProducer2) * G;
+        L.GRP = static_cast<int>(std::min<long long>(kEeGroupMax, std::max<long long>(1, (x + d / 2) / d)));
+    }
+    L.NI = (L.NCH + L.GRP - 1) / L.GRP;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t at = off;
@@ -1956,7 +1970,7 @@ struct Kern {
     // row for model proposals at T > 0), or one draw. Tasks 0..B-1 are position 0
     // of every request; the owner of a statistics task (block p mod G) decides
     // that position and publishes the request's next task: its next position,
-    // or its draw. Producers take items, fixed groups of kEeGroup consecutive
+    // or its draw. Producers take items, fixed groups of GRP consecutive
     // chunks of one task (L.NI per task), in publication order; an item's
     // statistics are folded into one record, so that the per-chunk costs (the
     // grab, the task lookup, the cross-warp flush) are paid once per group,
@@ -2159,9 +2173,11 @@ struct Kern {
             const long long trow = static_cast<long long>(b) * (GM + 1) + pos;  // pos: the draw's row n for draws
             const long long drow = static_cast<long long>(b) * GM + pos;
             const bool two = type == kTaskStats ? (flags & kStatsDraft) != 0 : kind == kKindResidual;
-            const int j0 = grp * kEeGroup, j1 = min(NCH, j0 + kEeGroup);
+            const int j0 = grp * L.GRP, j1 = min(NCH, j0 + L.GRP);
+            desc.item = grp;
             for (int j = j0; ok && j < j1; ++j) {
                 desc.j = j;
+                desc.nch = j - j0 + 1;
                 desc.flags = flags | (j == j0 ? kItemFirst : 0) | (j == j1 - 1 ? kItemLast : 0);
                 const long long e0 = static_cast<long long>(j) * CH;
                 const int cnt = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
@@ -2209,7 +2225,7 @@ struct Kern {
             }
             const long long e0 = static_cast<long long>(ds.j) * CH;
             const int n = static_cast<int>(min(static_cast<long long>(CH), a.V - e0));
-            const unsigned nch = static_cast<unsigned>(ds.j % kEeGroup) + 1;  // chunks of the item so far
+            const unsigned nch = static_cast<unsigned>(ds.nch);  // chunks of the item so far
             if (ds.type == kTaskStats) {
                 const bool argmax = (ds.flags & kStatsArgmax) != 0, has_draft = (ds.flags & kStatsDraft) != 0;
                 if (ds.flags & kItemFirst) {
@@ -2222,7 +2238,7 @@ struct Kern {
                 consume_end(cons);
                 fold_vectors<NVC>(rt, vt, e0);
                 if (has_draft) fold_vectors<NVC>(rd, vd, e0);
-                if (ds.flags & kItemLast) ee_flush_item(rt, rd, has_draft, nitem++, ds.k, ds.j / kEeGroup, nch);
+                if (ds.flags & kItemLast) ee_flush_item(rt, rd, has_draft, nitem++, ds.k, ds.item, nch);
             } else {
                 const int valid = max(0, min(TPT, n - t * TPT));
                 Run lt, ld;
