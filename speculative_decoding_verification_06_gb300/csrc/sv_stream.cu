@@ -2100,7 +2100,8 @@ struct Kern {
         while (ok && !*vabort) {
             const long long i = __shfl_sync(0xffffffffu, next, 0);
             if (lane == 0) next = atomicAdd(&h->next_item, 1u);  // the next item, in flight meanwhile
-            const int p = static_cast<int>(i / NI), grp = static_cast<int>(i - static_cast<long long>(p) * NI);
+            const int p = static_cast<int>(static_cast<unsigned>(i) / static_cast<unsigned>(NI));
+            const int grp = static_cast<int>(i) - p * NI;
             if (p != cur_p) {
                 int state = 1;  // 1 task known, 0 no more tasks, -1 the wait ran out
                 if (lane == 0) {
@@ -2704,6 +2705,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
             unsigned next = 0;
             if (lane == 0) next = atomicAdd(&h->next_item, static_cast<unsigned>(kGrab));
             long long i = 0, i_end = 0;
+            int ip = 0, ij = 0;  // item i's job position and chunk (advanced by increments within a grab)
             int cur_p = -1;
             StageDesc desc;  // lane 0's copy of the current job
             desc.k = -1;
@@ -2714,9 +2716,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                     i_end = i + kGrab;
                     if (i >= n_items) break;
                     if (lane == 0) next = atomicAdd(&h->next_item, static_cast<unsigned>(kGrab));
+                    ip = static_cast<int>(static_cast<unsigned>(i) / static_cast<unsigned>(L.NCH));
+                    ij = static_cast<int>(i) - ip * L.NCH;
                 }
                 if (i >= n_items) break;
-                const int p = static_cast<int>(i / L.NCH), j = static_cast<int>(i - static_cast<long long>(p) * L.NCH);
+                const int p = ip, j = ij;
+                if (++ij == L.NCH) {
+                    ij = 0;
+                    ++ip;
+                }
                 if (p != cur_p) {
                     // the p-th published job (bounded wait: it is published by the
                     // finisher of the block that completes its request)
