@@ -167,7 +167,7 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     const long long Ed_max = static_cast<long long>(B) * gamma * V;
     // the piece of row r in slice i has record r + i (see piece_rec): at most
     // the rows plus the slices of each stream
-    L.NRT = static_cast<int>(L.Et / V) + (kMaxWaves + 1) * G;
+    L.NRT = static_cast<int>(L.Et / V) + (kMaxWaves + 2) * G;
     L.NRD = static_cast<int>(Ed_max / V) + kMaxWaves * G;
     const int chunk_elems = kChunkBytes / es;
     L.NCH = (V + chunk_elems - 1) / chunk_elems;
@@ -550,7 +550,11 @@ struct Kern {
         }
     }
 
-    // Every row piece of this block, in streaming order.
+    // Every row piece of this block, in streaming order: its slices of the
+    // T > 0 requests' rows, wave by wave, then its two slices of the others'
+    // rows (cut into 2G slices, block g taking 2g and 2g + 1: measured a
+    // little faster than one slice a block, its fp32 build spilling 24 bytes a
+    // thread instead of 48).
     template <typename F>
     __device__ void for_each_segment(F&& f) const {
         const int W = ctl.nwave;
@@ -560,7 +564,9 @@ struct Kern {
             for_each_draft_segment(slice_begin(ctl.sl[1], is), slice_begin(ctl.sl[1], is + 1), is, w, f);
         }
         const long long E1 = ctl.sl[0].E;
-        for_each_target_segment(E1 + slice_begin(ctl.sl[2], g), E1 + slice_begin(ctl.sl[2], g + 1), W * G + g, -1, f);
+        for (int i3 = 2 * g; i3 < 2 * g + 2; ++i3)
+            for_each_target_segment(E1 + slice_begin(ctl.sl[2], i3), E1 + slice_begin(ctl.sl[2], i3 + 1), W * G + i3,
+                                    -1, f);
     }
 
     // ---- the ring: producer and consumer cursors
@@ -813,8 +819,8 @@ struct Kern {
                                      max(1ll, E1 * ES / (static_cast<long long>(G) * kWaveSliceBytes))));
         while (W > 1 && (n + G - 1) / G + 3 * W + 1 > kMapMax) --W;
         const Slicing s1 = make_slicing(E1, W * G, L.vec), s2 = make_slicing(E2, W * G, L.vec);
-        const Slicing s3 = make_slicing(E3, G, L.vec);
-        const int j3_lo = static_cast<int>(slice_begin(s3, g) / R);
+        const Slicing s3 = make_slicing(E3, 2 * G, L.vec);
+        const int j3_lo = static_cast<int>(slice_begin(s3, 2 * g) / R);
         if (t == 0) {
             ctl.n_samp = n;
             ctl.nwave = W;
@@ -875,9 +881,9 @@ struct Kern {
                 // slice holds the first element of the request's target rows
                 // clears it here, before it posts any share (the scan comes after
                 // every share).
-                const int first_slice = f ? slice_of(s1, static_cast<long long>(k) * R)
-                                          : slice_of(s3, static_cast<long long>(b - k) * R);
-                if (first_slice % G == g) a.out_num_accepted[b] = -1;
+                const int first_block = f ? slice_of(s1, static_cast<long long>(k) * R) % G
+                                          : slice_of(s3, static_cast<long long>(b - k) * R) / 2;
+                if (first_block == g) a.out_num_accepted[b] = -1;
             }
             carry += total;
             bar_sync(kBarConsumers, kConsumers);
