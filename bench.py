@@ -337,21 +337,7 @@ def graph_us_per_call(op, sv, B, G, out_t, out_n, buf0, lens0, props, nprop, GN=
     else:
         def call():
             sv.spec_ngram_propose(buf0, lens0, G, 2, 5, props, nprop)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):  # the binding enqueues on the current (capturing) stream
-        for _ in range(GN):
-            call()
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(R):
-        graph.replay()
-    t1.record()
-    torch.cuda.synchronize()
-    return t0.elapsed_time(t1) * 1e3 / (R * GN)
+    return replay_us_per_call(call, GN, R)  # the binding enqueues on the current (capturing) stream
 
 
 def run_aux(args, w, local):
