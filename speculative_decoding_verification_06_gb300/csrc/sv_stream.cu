@@ -166,7 +166,8 @@ Layout make_layout(int B, int gamma, int V, int es, int G) {
     L.Et = static_cast<long long>(B) * (gamma + 1) * V;
     const long long Ed_max = static_cast<long long>(B) * gamma * V;
     // the piece of row r in slice i has record r + i (see piece_rec): at most
-    // the rows plus the slices of each stream
+    // the rows plus the slices of each stream (W G of the T > 0 requests'
+    // target rows, then 2G of the others')
     L.NRT = static_cast<int>(L.Et / V) + (kMaxWaves + 2) * G;
     L.NRD = static_cast<int>(Ed_max / V) + kMaxWaves * G;
     const int chunk_elems = kChunkBytes / es;
