@@ -286,8 +286,16 @@ __device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
     asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-__device__ __forceinline__ void st_relaxed(int* p, int v) {
-    asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// Publishes a word after the writer's earlier stores (release at GPU scope).
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Adds v to a global counter and returns the old value; release orders the
+// caller's earlier writes before the add, acquire its later reads after it.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 __device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* p) {
     unsigned long long v;
@@ -636,14 +644,11 @@ struct Kern {
         if (d_status) atomicOr(d_status, SV_STATUS_TIMEOUT);
     }
 
-
-
     // Publishes draw job k (its record written by this thread): the producers
     // of every block take draw items from the jobs in publication order.
     __device__ void publish(int k) const {
-        __threadfence();
         const unsigned p = atomicAdd(&hdr()->n_pub, 1u);
-        st_relaxed(ready() + p, k + 1);
+        st_release(ready() + p, k + 1);  // the job's record lands before its entry
     }
 
     // Search warp: the token searches of the jobs published at positions
@@ -1150,13 +1155,14 @@ struct Kern {
         const int32_t* tok = a.tokens + static_cast<size_t>(b) * GM;
         const bool onehot = a.onehot;
         // The reads come in two rounds. First everything that depends on no
-        // other read: the temperature, the proposal count, this lane's token
-        // and uniform, and the first piece records of row `lane` (rows
-        // numbered target 0..gamma, then draft gamma+1..2 gamma; rows from 32
-        // on are read in the second round). Then the logits at this lane's
-        // token, which need only the token (read even when the request turns
-        // out greedy).
+        // other read: the temperature, the draw's uniform, the proposal
+        // count, this lane's token and uniform, and the first piece records
+        // of row `lane` (rows numbered target 0..gamma, then draft
+        // gamma+1..2 gamma; rows from 32 on are read in the second round).
+        // Then the logits at this lane's token, which need only the token
+        // (read even when the request turns out greedy).
         const float T = a.temperature[b];
+        const int us_bits = __float_as_int(a.u_sample[b]);  // the draw's uniform
         // proposals of this request: gamma, or num_draft[b] for one-hot proposals
         // (whose rows past it take no part)
         const int kb = onehot && a.num_draft ? a.num_draft[b] : GM;
@@ -1252,7 +1258,7 @@ struct Kern {
             if (dbg.lse_draft)
                 dbg.lse_draft[r] = draft ? lse_from_stats(ms_of(st[GM + 1 + j]), sc, T) : nan("");
         }
-        const ScanPre pre{x_l, u_l, lt_l, ld_l};
+        const ScanPre pre{x_l, u_l, lt_l, ld_l, us_bits};
         Job j;
         const int* set = nullptr;  // a tree draw's excluded tokens
         if (a.tree ? tree_walk(b, k, st, greedy, sc, np, j, set) : linear_scan(b, st, greedy, sc, np, pre, j))
@@ -1260,10 +1266,12 @@ struct Kern {
     }
 
     // What the acceptance scan reads before it knows the temperature: lane's
-    // token, uniform and the logits at the token (rows lane < 32).
+    // token, uniform and the logits at the token (rows lane < 32), and the
+    // request's draw uniform.
     struct ScanPre {
         int x_l;
         float u_l, lt_l, ld_l;
+        int us_bits;  // u_sample[b]
     };
 
     // The left-to-right scan of request b (not a tree): writes the accepted
@@ -1318,7 +1326,7 @@ struct Kern {
             }
         for (int j = lane; j <= GM; j += 32) {
             if (j < n)
-                out[j] = tok[j];
+                out[j] = j < 32 ? x_l : tok[j];  // lane j read token j in the first round
             else if (j == n)
                 out[j] = greedy ? st[n].idx : -1;  // the draw fills it in phase 2
             else
@@ -1335,7 +1343,7 @@ struct Kern {
         j.b = b;
         j.n = n;
         j.slot = n;
-        j.pad = __float_as_int(a.u_sample[b]);  // the draw's uniform
+        j.pad = pre.us_bits;  // the draw's uniform
         DrawParams& d = j.d;
         d.excl = -1;
         if (n < np && !onehot) {
@@ -1583,7 +1591,7 @@ struct Kern {
         d.fix = kFixTarget;
         j.kind = d.base_kind();
         __syncwarp();  // lane 0's set, before the other lanes read it
-        set_out = set;  // publish's fence also orders the set before the job
+        set_out = set;  // publish's release store also orders the set before the job
         return true;
     }
 
@@ -2627,11 +2635,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(Args a, Layout L, c
                     red_release_add(job_done + (item & ~kJobMsg), share);
                     return false;
                 }
-                const unsigned need = (!a.onehot && KT::sampled(a.temperature[item]) ? 2 * GM + 1 : GM + 1) * V;
-                __threadfence();  // this block's row records are visible before they are counted
-                const bool done = atomicAdd(req_done + item, share) + share == need;
-                __threadfence();  // and the other blocks' records before they are read
-                return done;
+                // the rows the request streams (kmap: T > 0 or not, from the
+                // prologue, so no global read per message)
+                const unsigned need = (!a.onehot && ctl.kmap[item] >= 0 ? 2 * GM + 1 : GM + 1) * V;
+                // release: this block's row records are visible before they are
+                // counted; acquire: the other blocks' records before they are read
+                return atom_add_acq_rel(req_done + item, share) + share == need;
             },
             [&](int item) {
                 if (!(item & kJobMsg)) {
