@@ -44,12 +44,13 @@ UNIT = "rows/s"
 PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
-# The files the streaming kernel is compiled from: the captured DRAM traffic
-# applies while they are unchanged.
-KERNEL_SOURCES = ["speculative_decoding_verification_06_gb300/csrc/sv_stream.cu",
-                  "speculative_decoding_verification_06_gb300/csrc/sv_common.cuh",
-                  "speculative_decoding_verification_06_gb300/csrc/sv_internal.h",
-                  "include/specverify.h"]
+# The files each captured kernel is compiled from (its own source plus the
+# shared headers): a captured DRAM traffic applies while they are unchanged.
+_CSRC = "speculative_decoding_verification_06_gb300/csrc/"
+KERNEL_COMMON = [_CSRC + "sv_common.cuh", _CSRC + "sv_internal.h", "include/specverify.h"]
+KERNEL_FILES = {"stream_kernel": _CSRC + "sv_stream.cu", "early_kernel": _CSRC + "sv_stream.cu",
+                "rowwise_kernel": _CSRC + "sv_rowwise.cu", "cluster_kernel": _CSRC + "sv_cluster.cu"}
+KERNEL_SOURCES = sorted(set(KERNEL_FILES.values())) + KERNEL_COMMON
 
 
 def parse():
@@ -109,9 +110,11 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str = "stream_kernel") -> str:
+    """Hash of the sources `kernel` (a name as in the launch list, template
+    arguments dropped) is compiled from."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in [KERNEL_FILES[kernel.split("<")[0]]] + KERNEL_COMMON:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(os.path.basename(rel).encode() + f.read())
     return h.hexdigest()[:16]
@@ -160,7 +163,7 @@ def captured_traffic(workload: str, early: bool, path: str | None = None):
         with open(path or PROFILE_TRAFFIC) as f:
             prof = json.load(f)
         entry = prof.get(workload + ("-early" if early else ""))
-        if entry and entry.get("kernel_hash") == kernel_hash():
+        if entry and entry.get("kernel_hash") == kernel_hash(entry.get("kernel", "stream_kernel")):
             return entry.get("dram_bytes_per_launch")
     except Exception:
         pass

@@ -83,3 +83,18 @@ def test_kernel_hash_covers_existing_sources():
     for rel in bench.KERNEL_SOURCES:
         assert os.path.isfile(os.path.join(ROOT, rel)), rel
     assert len(bench.kernel_hash()) == 16
+    # each kernel is keyed on its own source: the streaming and early-exit
+    # kernels share one, the one-block and cluster kernels have their own
+    assert bench.kernel_hash("early_kernel<bf16>") == bench.kernel_hash("stream_kernel<f32>")
+    assert len({bench.kernel_hash(k) for k in ("stream_kernel", "rowwise_kernel", "cluster_kernel")}) == 3
+
+
+def test_captured_traffic_uses_the_entry_kernels_sources(tmp_path):
+    prof = {"greedy": {"kernel": "cluster_kernel<bf16, 16>", "kernel_hash": bench.kernel_hash("cluster_kernel"),
+                       "dram_bytes_per_launch": 44.0},
+            "tiny": {"kernel": "rowwise_kernel<f32>", "kernel_hash": bench.kernel_hash("stream_kernel"),
+                     "dram_bytes_per_launch": 55.0}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(prof))
+    assert bench.captured_traffic("greedy", False, str(path)) == 44.0
+    assert bench.captured_traffic("tiny", False, str(path)) is None  # keyed on another kernel's sources
