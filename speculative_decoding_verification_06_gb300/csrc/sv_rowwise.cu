@@ -47,6 +47,11 @@ struct Shared {
     int nexcl;
     int draw_row;            // the row of the draw (tree: the last node)
     int row_flag;            // the last row pass found the anchored form out of range
+    // the scan's inputs, read by one thread a position before the scan
+    int px[SV_MAX_GAMMA];    // proposed token
+    float pu[SV_MAX_GAMMA];  // its uniform
+    float plt[SV_MAX_GAMMA]; // target logit at the token
+    float pld[SV_MAX_GAMMA]; // draft logit at the token
 };
 
 // Logits a thread folds into one partial before the partial joins its running
@@ -161,6 +166,73 @@ __device__ RowStat row_argmax(const void* base, size_t row, int V, Shared& sh) {
     return r;
 }
 
+// Rows of at most kWarpRow logits are reduced by one warp each (at most 64
+// logits a lane, so one partial, as in the block pass), with no block
+// barrier: the block's warps take the request's rows kWarps at a time and
+// their loads overlap. Same forms and flags as row_pass / row_argmax; the
+// result is on every lane.
+constexpr int kWarpRow = 32 * kInner;
+
+template <int DT, bool PLAIN>
+__device__ RowStat warp_row_pass(const void* base, size_t row, int V, const Scale& c, int& flag_out) {
+    using State = typename std::conditional<PLAIN, MaxSum, MaxSumA>::type;
+    State st;
+    if constexpr (PLAIN) st = MaxSum{neg_inf(), 0.0f, 1};
+    else st = MaxSumA{neg_inf(), 0.0f};
+    int bad = 0, flag = 0;
+    const size_t off = row * static_cast<size_t>(V);
+    for (int x = threadIdx.x & 31; x < V; x += 32) {
+        const float l = load_logit<DT>(base, off + x);
+        if (bad_logit(l)) {
+            bad = 1;
+        } else {
+            if constexpr (PLAIN) maxsum_add(st, l, c);
+            else maxsum_add_a(st, l, c.c, flag);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        State other = st;
+        other.m = __shfl_xor_sync(0xffffffffu, st.m, o);
+        other.s = __shfl_xor_sync(0xffffffffu, st.s, o);
+        if constexpr (PLAIN) st = maxsum_merge(st, other, c);
+        else st = maxsum_merge_a(st, other, c.c);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    flag = __any_sync(0xffffffffu, flag);
+    const RowStat r{st.m, st.s, -1, (bad || st.m == neg_inf()) ? 1 : 0, PLAIN ? 1 : 0};
+    flag_out = flag && !r.bad;
+    return r;
+}
+
+template <int DT>
+__device__ RowStat warp_row_maxsum(const void* base, size_t row, int V, const Scale& c) {
+    int flag = 0;
+    const RowStat r = warp_row_pass<DT, false>(base, row, V, c, flag);
+    if (!flag) return r;
+    return warp_row_pass<DT, true>(base, row, V, c, flag);
+}
+
+template <int DT>
+__device__ RowStat warp_row_argmax(const void* base, size_t row, int V) {
+    ArgMax st = argmax_empty();
+    int bad = 0;
+    const size_t off = row * static_cast<size_t>(V);
+    for (int x = threadIdx.x & 31; x < V; x += 32) {
+        const float l = load_logit<DT>(base, off + x);
+        if (bad_logit(l)) bad = 1;
+        if (l > st.v) st = {l, x};  // increasing x: the first maximum stays
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ArgMax other{__shfl_xor_sync(0xffffffffu, st.v, o), __shfl_xor_sync(0xffffffffu, st.i, o)};
+        st = argmax_merge(st, other);
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (st.i == 0x7fffffff) st.i = 0;
+    return RowStat{st.v, 0.0f, st.i, (bad || st.v == neg_inf()) ? 1 : 0, 0};
+}
+
 // Sum of the draw weights over [lo, hi) in index order (binary32).
 // Weight of token e of a draw (residual, extra token, one-hot or tree residual).
 template <int DT>
@@ -265,17 +337,32 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             bad = sh.stop == 2;
         } else if (!bad) {
             const int nrows = (greedy || a.onehot) ? np + 1 : 2 * G + 1;
-            for (int r = 0; r < nrows; ++r) {
-                RowStat st;
-                if (r <= G) {
-                    size_t row = static_cast<size_t>(b) * (G + 1) + r;
-                    st = greedy ? row_argmax<DT>(a.target, row, V, sh)
-                                : row_maxsum<DT>(a.target, row, V, c, sh);
-                } else {
-                    size_t row = static_cast<size_t>(b) * G + (r - G - 1);
-                    st = row_maxsum<DT>(a.draft, row, V, c, sh);
+            if (V <= kWarpRow) {
+                // a warp a row (the warp's loop is uniform: r depends on the warp only)
+                for (int r = threadIdx.x >> 5; r < nrows; r += kWarps) {
+                    RowStat st;
+                    if (r <= G) {
+                        size_t row = static_cast<size_t>(b) * (G + 1) + r;
+                        st = greedy ? warp_row_argmax<DT>(a.target, row, V) : warp_row_maxsum<DT>(a.target, row, V, c);
+                    } else {
+                        st = warp_row_maxsum<DT>(a.draft, static_cast<size_t>(b) * G + (r - G - 1), V, c);
+                    }
+                    if ((threadIdx.x & 31) == 0) sh.st[r] = st;
                 }
-                if (threadIdx.x == 0) sh.st[r] = st;
+                __syncthreads();
+            } else {
+                for (int r = 0; r < nrows; ++r) {
+                    RowStat st;
+                    if (r <= G) {
+                        size_t row = static_cast<size_t>(b) * (G + 1) + r;
+                        st = greedy ? row_argmax<DT>(a.target, row, V, sh)
+                                    : row_maxsum<DT>(a.target, row, V, c, sh);
+                    } else {
+                        size_t row = static_cast<size_t>(b) * G + (r - G - 1);
+                        st = row_maxsum<DT>(a.draft, row, V, c, sh);
+                    }
+                    if (threadIdx.x == 0) sh.st[r] = st;
+                }
             }
             if (threadIdx.x == 0) {
                 int any = 0;
@@ -331,6 +418,21 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             if (a.dbg.lse_draft) a.dbg.lse_draft[r] = draft ? lse_from_stats(ms_of(st), c, T) : nan("");
             if (a.dbg.p_x) a.dbg.p_x[r] = nan("");
             if (a.dbg.q_x) a.dbg.q_x[r] = nan("");
+        }
+        // The linear scan's inputs, a thread a position, so that the scan on
+        // one thread does not wait on a read per position (positions up to
+        // the last row read: early exit reads nothing past it).
+        if (!a.tree) {
+            const int npre = min(np, last + 1);
+            for (int i = threadIdx.x; i < npre; i += kThreads) {
+                const int x = a.tokens[static_cast<size_t>(b) * G + i];
+                sh.px[i] = x;
+                if (!greedy) {
+                    sh.pu[i] = a.u_accept[static_cast<size_t>(b) * G + i];
+                    sh.plt[i] = load_logit<DT>(a.target, (static_cast<size_t>(b) * (G + 1) + i) * V + x);
+                    sh.pld[i] = a.onehot ? 0.0f : load_logit<DT>(a.draft, (static_cast<size_t>(b) * G + i) * V + x);
+                }
+            }
         }
         __syncthreads();
 
@@ -412,32 +514,29 @@ __global__ void __launch_bounds__(kThreads) rowwise_kernel(Args a) {
             int n = np;
             if (greedy) {
                 for (int i = 0; i < np; ++i) {
-                    if (tok[i] != sh.st[i].idx) {
+                    if (sh.px[i] != sh.st[i].idx) {
                         n = i;
                         break;
                     }
-                    out[i] = tok[i];
+                    out[i] = sh.px[i];
                 }
                 out[n] = sh.st[n].idx;
                 if (a.dbg.kind) a.dbg.kind[b] = kKindGreedy;
                 if (a.dbg.w_total) a.dbg.w_total[b] = nan("");
             } else {
-                const float* ua = a.u_accept + static_cast<size_t>(b) * G;
                 for (int i = 0; i < np; ++i) {
-                    const int x = tok[i];
-                    const size_t tr = static_cast<size_t>(b) * (G + 1) + i;
+                    const int x = sh.px[i];
                     const size_t dr = static_cast<size_t>(b) * G + i;
                     const RowStat& sp = sh.st[i];
                     const RowStat& sq = sh.st[G + 1 + i];
-                    const float lt = load_logit<DT>(a.target, tr * V + x);
-                    const float ld = a.onehot ? 0.0f : load_logit<DT>(a.draft, dr * V + x);
+                    const float lt = sh.plt[i], ld = sh.pld[i];
                     if (a.dbg.p_x) a.dbg.p_x[dr] = prob_from_stats(lt, ms_of(sp), c);
                     // a one-hot proposal has q(x) = 1
                     if (a.dbg.q_x) a.dbg.q_x[dr] = a.onehot ? 1.0 : prob_from_stats(ld, ms_of(sq), c);
                     // alpha from the logits: p(x) and q(x) may both lie below the
                     // floating-point range while their ratio does not
-                    const bool acc = a.onehot ? accept_from_logits(lt, 0.0f, ms_of(sp), MaxSum{0.0f, 1.0f, 0}, c, ua[i])
-                                              : accept_from_logits(lt, ld, ms_of(sp), ms_of(sq), c, ua[i]);
+                    const bool acc = a.onehot ? accept_from_logits(lt, 0.0f, ms_of(sp), MaxSum{0.0f, 1.0f, 0}, c, sh.pu[i])
+                                              : accept_from_logits(lt, ld, ms_of(sp), ms_of(sq), c, sh.pu[i]);
                     if (!acc) {
                         n = i;
                         break;
