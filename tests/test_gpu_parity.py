@@ -416,6 +416,20 @@ def test_small_temperatures(T, cfg, opts):
         assert rep.invalid == 0
 
 
+@pytest.mark.parametrize("T", [1e-4, 1e-20, 1e-40])
+@pytest.mark.parametrize("cfg", [3, 4], ids=["fp32", "bf16"])
+def test_small_temperatures_short_rows(T, cfg):
+    """The one-block-per-request kernel reduces rows of at most 2048 logits
+    a warp a row (longer rows, as above, with the whole block): the same
+    temperatures on that form, anchored and plain."""
+    w = synthetic.WORKLOADS[cfg].variant(B=16, gamma=3, V=1024)
+    for seed in (9, 10):
+        batch = synthetic.generate(w, seed=seed)
+        batch.temperature[:] = np.float32(T)
+        rep = parity.check(batch, **ROWWISE)
+        assert rep.invalid == 0
+
+
 @pytest.mark.parametrize("opts", [ROWWISE, STREAM, CLUSTER], ids=["rowwise", "stream", "cluster"])
 def test_tiny_logit_differences_at_subnormal_temperature(opts):
     """Logits a few binary32 subnormal steps apart (multiples of 2^-149) at
