@@ -20,7 +20,9 @@
 //     still stream, and only the last wave's draws wait at the end; the
 //     requests that need no draw come last. The
 //     producer copies its slices through a ring of kStages shared-memory
-//     stages with cp.async.bulk (completion on mbarriers); the consumers fold
+//     stages with cp.async.bulk (completion on mbarriers; an evict-first L2
+//     policy, so the streamed lines leave L2 before the small data the scans
+//     and searches read); the consumers fold
 //     each stage into per-thread (max, sum of 2^(l c - fl(m c))) or argmax
 //     states, and the last warp to finish a row piece writes the block's
 //     record for it. When a block's share of a request's rows is written, a
