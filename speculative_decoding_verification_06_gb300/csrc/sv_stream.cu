@@ -294,7 +294,8 @@ __device__ __forceinline__ void red_release_add(unsigned* addr, unsigned v) {
 
 // Polled words in global memory are read and written with device-scope
 // relaxed accesses (a volatile access has system scope, more than these
-// words need); the orderings they need come from explicit fences.
+// words need); the orderings they need come from explicit fences or from
+// release and acquire-release operations (st_release, atom_add_acq_rel).
 __device__ __forceinline__ int ld_relaxed(const int* p) {
     int v;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -768,7 +769,7 @@ struct Kern {
     // microsecond). It returns once every consumer warp is done, the ring is
     // empty and every owned search has run.
     // count(item, val), one lane per message, adds the share to the item's
-    // global counter (with the fences its reader needs) and returns whether
+    // global counter (with the ordering its reader needs) and returns whether
     // that completed the item; work(item), on the whole warp, then finishes
     // each completed item.
     // poll(), on the whole warp, runs owned work that became ready and says
